@@ -1,0 +1,425 @@
+"""Benchmark of the CSR sparse-adapter hot path on GB300.
+
+One step = one pass of the whole path over the RoSA-adapter workload (4096 x 4096 fp16
+weight, 1 % density clustered in 10 % of rows and columns, 2048 tokens):
+  sort_rows (row_idx from row_offsets) -> spmm (C = A X, the row bins computed inside)
+  -> sddmm (structure-aware backend, grad = dY^T X sampled on the mask) -> csr_add (W + A).
+metric: GFLOP/s counting 2 * nnz * N for SpMM and 2 * nnz * kd for SDDMM (csr_add adds no
+flops; its time is in the step). Each step is a CUDA-graph replay of the library calls;
+L2 is flushed (a 256 MB write) before every timed step, outside the step's events.
+
+--impl reference times the fp64 CPU oracle on the host cores on the same workload, metric
+and unit (a deliberately slow baseline, not a target).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+WORKLOAD = "rosa"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ work accounting
+
+
+def accounting(w):
+    """Algorithmic flops and compulsory HBM bytes of each operator on workload w."""
+    ro = w.row_offsets.numpy()
+    col = w.col_idx.numpy()
+    m, n, nnz = w.m, w.n, w.nnz
+    b = w.values.element_size()
+    ib = 2 if max(m, n) <= 32768 else 4
+    lens = np.diff(ro)
+    active_rows = int((lens > 0).sum())
+    active_cols = int(np.unique(col).size)
+    csr_bytes = nnz * (b + ib) + 4 * (m + 1) + ib * m
+    acc = {}
+    if w.B is not None:
+        N = w.B.shape[1]
+        acc["spmm"] = {"flops": 2 * nnz * N,
+                       "bytes": csr_bytes + active_cols * N * b + m * N * b}
+    if w.A is not None:
+        kd = w.A.shape[1]
+        acc["sddmm"] = {"flops": 2 * nnz * kd,
+                        "bytes": csr_bytes - nnz * b + active_rows * kd * b + active_cols * kd * b + nnz * b}
+    if w.W is not None:
+        acc["csr_add"] = {"flops": nnz, "bytes": csr_bytes - ib * m + 2 * m * n * b}
+    acc["sort_rows"] = {"flops": 0, "bytes": 4 * (m + 1) + ib * m}
+    return acc
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{self.gpu}.csv")
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]), "power": float(parts[3]),
+                             "reasons": parts[4:9]})
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["active_mask", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        seen = set()
+        for r in rows:
+            for nm, v in zip(names[1:], r["reasons"][1:]):
+                if v.lower() in ("active", "1", "yes"):
+                    seen.add(nm)
+        return {"sm_mhz": statistics.median(r["sm"] for r in rows), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(seen), "samples": len(rows),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+# ------------------------------------------------------------------ profile summary (traffic)
+
+
+def kernel_source_hash(path):
+    return hashlib.sha256(open(os.path.join(ROOT, path), "rb").read()).hexdigest()[:16]
+
+
+def recorded_traffic(op: str):
+    """Per-launch DRAM bytes of the op's kernel from the committed ncu summary, if the
+    kernel source still matches the hash recorded with the counters."""
+    p = os.path.join(ROOT, "profiles", "traffic.md")
+    if not os.path.exists(p):
+        return None
+    for line in open(p):
+        m = re.match(r"\|\s*" + re.escape(op) + r"\s*\|\s*([\w./]+)\s*\|\s*([0-9a-f]+)\s*\|\s*([0-9]+)\s*\|", line)
+        if m:
+            src, h, traffic = m.group(1), m.group(2), int(m.group(3))
+            try:
+                if kernel_source_hash(src) == h:
+                    return traffic
+            except OSError:
+                return None
+    return None
+
+
+# ------------------------------------------------------------------ GPU arm
+
+
+def run_gpu(args):
+    import torch.distributed as dist
+
+    import unstructured_sparse_linear_gb300 as sp
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = wl.generate(WORKLOAD)
+    acc = accounting(w)
+    N, kd = w.B.shape[1], w.A.shape[1]
+    step_flops = acc["spmm"]["flops"] + acc["sddmm"]["flops"]
+    idx = torch.int16
+
+    # device-resident inputs
+    ro = w.row_offsets.to(dev)
+    col = w.col_idx.to(idx).to(dev)
+    val = w.values.to(dev)
+    B, A, BT, W = (t.to(dev) for t in (w.B, w.A, w.BT, w.W))
+    nnz, m = w.nnz, w.m
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    outs = {}
+
+    def op_sort():
+        outs["row_idx"] = sp.sort_rows(ro, nnz=nnz, index_dtype=idx)
+
+    def op_spmm():
+        outs["C"] = sp.spmm(val, ro, outs["row_idx"], col, B, m)
+
+    def op_sddmm():
+        outs["G"] = sp.sddmm(ro, outs["row_idx"], col, A, BT, backend=args.sddmm_backend)
+
+    def op_add():
+        outs["D"] = sp.csr_add(val, ro, outs["row_idx"], col, W)
+
+    ops = [("sort_rows", op_sort), ("spmm", op_spmm), ("sddmm", op_sddmm), ("csr_add", op_add)]
+
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 1)):
+            for _, f in ops:
+                f()
+        torch.cuda.synchronize(dev)
+        launches0 = sp._lib.load().spops_kernel_launches()
+        graphs = []
+        pool = torch.cuda.graph_pool_handle()
+        for name, f in ops:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, pool=pool):
+                f()
+            graphs.append((name, g))
+        launches_per_step = sp._lib.load().spops_kernel_launches() - launches0
+        for _ in range(args.warmup):
+            for _, g in graphs:
+                g.replay()
+        torch.cuda.synchronize(dev)
+
+        nops = len(graphs)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nops + 1)] for _ in range(args.steps)]
+        sampler = ClockSampler(local)
+        if ws > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        sampler.start()
+        time.sleep(0.2)
+        t0 = time.perf_counter()
+        for s in range(args.steps):
+            flush.zero_()
+            ev[s][0].record(stream)
+            for j, (_, g) in enumerate(graphs):
+                g.replay()
+                ev[s][j + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+        if ws > 1:
+            dist.barrier()
+        clocks = sampler.stop()
+
+    step_ms = [ev[s][0].elapsed_time(ev[s][nops]) for s in range(args.steps)]
+    op_ms = {name: [ev[s][j].elapsed_time(ev[s][j + 1]) for s in range(args.steps)]
+             for j, (name, _) in enumerate(graphs)}
+    total_ms = sum(step_ms)
+    if ws > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = ws * step_flops * args.steps / (total_ms * 1e-3) / 1e9
+
+    # ---- end to end through the public API with host buffers
+    e2e = run_e2e(sp, w, dev, idx, args, step_flops, ws)
+
+    pk = peaks()
+    per_op = {}
+    for name, times in op_ms.items():
+        t_avg = sum(times) / len(times)
+        a = acc[name]
+        per_op[name] = {"ms": round(t_avg, 5), "ms_min": round(min(times), 5),
+                        "GFLOP/s": round(a["flops"] / (t_avg * 1e-3) / 1e9, 2) if a["flops"] else None,
+                        "GB/s": round(a["bytes"] / (t_avg * 1e-3) / 1e9, 1),
+                        "hbm_frac": round(a["bytes"] / (t_avg * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}
+    dominant = max((k for k in per_op if k != "sort_rows"), key=lambda k: per_op[k]["ms"])
+    dom_t = per_op[dominant]["ms"] * 1e-3
+    achieved = acc[dominant]["bytes"] / dom_t / 1e9
+    roofline = {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
+                "traffic": recorded_traffic(dominant), "algorithmic_bytes": acc[dominant]["bytes"],
+                "peak_source": pk["source"]}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, acc, steps=args.cpu_steps)
+
+    line = {
+        "metric": "SpMM+SDDMM GFLOP/s (2*nnz*N + 2*nnz*kd per step; step = sort_rows+spmm+sddmm+csr_add)",
+        "value": round(value, 2), "unit": "GFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16", "data": "synthetic (seeded; RoSA-adapter mask recipe)",
+        "config": {"workload": "rosa_adapter_4096x4096_fp16_1pct_clustered_2048tok", "m": m, "n": w.n, "nnz": nnz,
+                   "N": N, "kd": kd, "index": "int16", "sddmm_backend": args.sddmm_backend,
+                   "l2": "flushed before every step (256 MB write, outside step events)",
+                   "parallelism": f"replicas x{ws} (independent adapters per GPU)"},
+        "per_op": per_op, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": int(launches_per_step) * args.steps, "clocks": clocks,
+        "wall_s_timed_region": round(wall, 4),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(sp, w, dev, idx, args, step_flops, ws):
+    """Same metric through the public calls, with inputs copied from pinned host memory
+    and the results copied back inside every timed step."""
+    host = {"ro": w.row_offsets, "col": w.col_idx.to(idx), "val": w.values, "B": w.B, "A": w.A, "BT": w.BT,
+            "W": w.W}
+    host = {k: v.contiguous().pin_memory() for k, v in host.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    res_h = {"C": torch.empty((w.m, w.B.shape[1]), dtype=w.B.dtype).pin_memory(),
+             "G": torch.empty(w.nnz, dtype=w.B.dtype).pin_memory(),
+             "D": torch.empty((w.m, w.n), dtype=w.B.dtype).pin_memory()}
+    d2h = sum(v.numel() * v.element_size() for v in res_h.values())
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        d = {k: v.to(dev, non_blocking=True) for k, v in host.items()}
+        ri = sp.sort_rows(d["ro"], nnz=w.nnz, index_dtype=idx)
+        C = sp.spmm(d["val"], d["ro"], ri, d["col"], d["B"], w.m)
+        G = sp.sddmm(d["ro"], ri, d["col"], d["A"], d["BT"], backend=args.sddmm_backend)
+        D = sp.csr_add(d["val"], d["ro"], ri, d["col"], d["W"])
+        res_h["C"].copy_(C, non_blocking=True)
+        res_h["G"].copy_(G, non_blocking=True)
+        res_h["D"].copy_(D, non_blocking=True)
+
+    for _ in range(max(2, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    steps = max(3, min(args.steps, 200))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": round(ws * step_flops / (ms * 1e-3) / 1e9, 2), "unit": "GFLOP/s", "ms_per_step": round(ms, 4),
+            "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+
+def _oracle_step(o, w, ro, col, vals64, B64, A64, BT64, W64):
+    o.sort_rows(ro)
+    o.spmm(ro, col, vals64, B64)
+    o.sddmm(ro, col, A64, BT64)
+    o.csr_add(ro, col, vals64, W64)
+
+
+def cpu_baseline(w, acc, steps: int):
+    """The fp64 oracle as it stands, on the host cores, full workload per step."""
+    import oracle as o
+    ro, col = w.row_offsets.numpy(), w.col_idx.numpy()
+    vals64 = w.values.double().numpy()
+    B64, A64, BT64, W64 = (t.double().numpy() for t in (w.B, w.A, w.BT, w.W))
+    o.build()
+    _oracle_step(o, w, ro, col, vals64, B64, A64, BT64, W64)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        _oracle_step(o, w, ro, col, vals64, B64, A64, BT64, W64)
+    dt = (time.perf_counter() - t0) / steps
+    flops = acc["spmm"]["flops"] + acc["sddmm"]["flops"]
+    return {"value": round(flops / dt / 1e9, 3), "unit": "GFLOP/s", "cores": o.num_threads(), "kind": "oracle",
+            "sample": f"full workload, {steps} step(s) of sort_rows+spmm+sddmm+csr_add in fp64",
+            "ms_per_step": round(dt * 1e3, 2)}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    w = wl.generate(WORKLOAD)
+    acc = accounting(w)
+    steps = max(1, min(args.steps, args.ref_max_steps))
+    import oracle as o
+    ro, col = w.row_offsets.numpy(), w.col_idx.numpy()
+    vals64 = w.values.double().numpy()
+    B64, A64, BT64, W64 = (t.double().numpy() for t in (w.B, w.A, w.BT, w.W))
+    o.build()
+    for _ in range(min(args.warmup, 1)):
+        _oracle_step(o, w, ro, col, vals64, B64, A64, BT64, W64)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        _oracle_step(o, w, ro, col, vals64, B64, A64, BT64, W64)
+    dt = (time.perf_counter() - t0) / steps
+    flops = acc["spmm"]["flops"] + acc["sddmm"]["flops"]
+    value = round(flops / dt / 1e9, 3)
+    line = {"impl": "reference",
+            "metric": "SpMM+SDDMM GFLOP/s (2*nnz*N + 2*nnz*kd per step; step = sort_rows+spmm+sddmm+csr_add)",
+            "value": value, "unit": "GFLOP/s", "n_gpus": ws, "steps": steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded; RoSA-adapter mask recipe)",
+            "config": {"workload": "rosa_adapter_4096x4096_fp16_1pct_clustered_2048tok", "m": w.m, "n": w.n,
+                       "nnz": w.nnz, "N": w.B.shape[1], "kd": w.A.shape[1]},
+            "cpu_baseline": {"value": value, "unit": "GFLOP/s", "cores": o.num_threads(), "kind": "oracle",
+                             "sample": f"full workload per step, {steps} step(s)"},
+            "e2e": {"value": value, "unit": "GFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--sddmm-backend", default="structure_aware", choices=["structure_aware", "general"])
+    ap.add_argument("--cpu-steps", type=int, default=3)
+    ap.add_argument("--ref-max-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl != "reference":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,171 @@
+/*
+ * spops_gb300.h -- C ABI of the GB300 (sm_103a) CSR sparse-adapter operators.
+ *
+ * The operators are the ones the spops README ("Sparse Operations (spops)") lists:
+ *   csr_add  [dense = sparse + dense]      section "Sparse Addition"
+ *   spmm     [dense = sparse x dense]      section "Sparse Matrix Multiplication (SpMM)"
+ *   sddmm    [sparse = dense x dense]      section "Sampled Dense-Dense Matrix
+ *                                          Multiplication (SDDMM)", with a general and a
+ *                                          structure-aware backend (structure-aware is the
+ *                                          default)
+ * plus the row permutation row_idx and the row bins that schedule them.
+ *
+ * CSR layout (section "Usage"): an m x n matrix with nnz entries is
+ *   values      [nnz]    entry values, dtype `dtype`;
+ *   row_offsets [m + 1]  int32; row i holds entries row_offsets[i] .. row_offsets[i+1]-1;
+ *   col_idx     [nnz]    column of each entry, int16 (SPOPS_IDX16) or int32 (SPOPS_IDX32);
+ *   row_idx     [m]      permutation of 0..m-1 sorting rows by nnz, same width as col_idx.
+ * Section "Important Notes" fixes int32 row_offsets and int16 index lists; int16 limits m
+ * and n to 32768, so SPOPS_IDX32 is offered for larger matrices.
+ * The library expects canonical CSR: row_offsets[0] = 0, non-decreasing, row_offsets[m] =
+ * nnz, and columns strictly increasing inside each row. spops_check_csr verifies this on
+ * the device. Results are correct for ANY permutation in row_idx; a sorted one (as
+ * spops_sort_rows writes) only balances the work.
+ *
+ * Conventions for every call:
+ *   - Every array is a DEVICE pointer into memory the caller owns and keeps alive until the
+ *     work on `stream` finishes. All arrays are dense and contiguous (row-major for
+ *     matrices). Element pointers must be aligned to their element size.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream). Calls are
+ *     asynchronous on that stream and never synchronize, except spops_get_device_error.
+ *   - The library allocates no device memory. Calls that need scratch take a caller
+ *     `workspace` of at least the size the matching *_workspace_size function returns,
+ *     16-byte aligned; it may be reused once the call's work on `stream` has finished.
+ *   - Return value: an spops_status. Argument errors are detected on the host before any
+ *     work is queued and leave every output untouched. SPOPS_ERR_CUDA reports a failed
+ *     launch. spops_last_error() gives a one-line description of the last failure on the
+ *     calling thread.
+ *   - Floating-point results accumulate in fp32 and are rounded once (round to nearest
+ *     even) to the operand dtype. Values and dense operands share one dtype.
+ */
+#ifndef SPOPS_GB300_H
+#define SPOPS_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SPOPS_API __attribute__((visibility("default")))
+#else
+#define SPOPS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum spops_status {
+    SPOPS_OK = 0,
+    SPOPS_ERR_INVALID_ARG = 1,  /* bad enum, negative size, null or misaligned pointer */
+    SPOPS_ERR_UNSUPPORTED = 2,  /* valid request this library does not serve (e.g. int16 overflow) */
+    SPOPS_ERR_WORKSPACE = 3,    /* workspace missing, misaligned or smaller than required */
+    SPOPS_ERR_CUDA = 4,         /* a CUDA runtime call or kernel launch failed */
+    SPOPS_ERR_DEVICE_CHECK = 5  /* a device-side check recorded a violation */
+} spops_status;
+
+typedef enum spops_dtype { SPOPS_F32 = 0, SPOPS_F16 = 1, SPOPS_BF16 = 2 } spops_dtype;
+typedef enum spops_itype { SPOPS_IDX16 = 0, SPOPS_IDX32 = 1 } spops_itype;
+typedef enum spops_sddmm_backend {
+    SPOPS_SDDMM_STRUCTURE_AWARE = 0, /* default: dense panels on tensor cores, the rest general */
+    SPOPS_SDDMM_GENERAL = 1          /* any sparsity pattern, CUDA cores */
+} spops_sddmm_backend;
+
+/* Device error codes reported by spops_get_device_error. */
+#define SPOPS_DEV_OK 0
+#define SPOPS_DEV_MBAR_TIMEOUT 1 /* an asynchronous-copy or tensor-core wait exceeded its time limit */
+#define SPOPS_DEV_ROW_OFFSETS 2  /* row_offsets not non-decreasing, or wrong first/last value */
+#define SPOPS_DEV_COL_RANGE 3    /* a column index outside [0, n) */
+#define SPOPS_DEV_COL_ORDER 4    /* columns not strictly increasing inside a row */
+#define SPOPS_DEV_ROW_IDX 5      /* row_idx is not a permutation of 0..m-1 */
+#define SPOPS_DEV_TMEM 6         /* tensor-memory allocation failed */
+
+/* Row-bin thresholds the operators use: rows with at least this many entries are "long". */
+#define SPOPS_SPMM_LONG_ROW 256
+#define SPOPS_SDDMM_LONG_ROW 64
+
+/* Human-readable name of a status code (static string). */
+SPOPS_API const char* spops_status_string(int status);
+
+/* One-line description of the most recent failed call on this thread ("" if none). */
+SPOPS_API const char* spops_last_error(void);
+
+/* Library version string, e.g. "spops_gb300 0.1 sm_103a". */
+SPOPS_API const char* spops_version(void);
+
+/* Number of kernels this library has launched in this process (all devices, all
+ * threads). A call captured into a CUDA graph counts once, at capture. */
+SPOPS_API uint64_t spops_kernel_launches(void);
+
+/* ---------------------------------------------------------------- row scheduler */
+
+/* Scratch bytes spops_sort_rows needs for m rows. */
+SPOPS_API size_t spops_sort_rows_workspace_size(int32_t m);
+
+/* row_idx_out[0..m) = the rows ordered by nnz_i = row_offsets[i+1] - row_offsets[i],
+ * largest first, ties by ascending row id (spops README, section "Usage": row_idx sorts
+ * the rows by their number of non-zeros; the README leaves the direction open).
+ * row_offsets: [m+1] int32 device; nnz = row_offsets[m] (bounds the sort key);
+ * row_idx_out: [m] device, int16 or int32 per `itype` (int16 needs m <= 32768).
+ * Deterministic: bit-identical output on every call. */
+SPOPS_API int spops_sort_rows(const int32_t* row_offsets, int32_t m, int32_t nnz, void* row_idx_out, int itype,
+                    void* workspace, size_t ws_bytes, void* stream);
+
+/* bins_out[0..4) (device int32) = {0, #rows with nnz >= t_long, #rows with nnz >= 1, m}:
+ * prefix offsets that split a sorted row_idx into long, short and empty rows. The counts
+ * do not depend on row_idx, so the call takes only row_offsets. t_long >= 1. */
+SPOPS_API int spops_row_bins(const int32_t* row_offsets, int32_t m, int32_t t_long, int32_t* bins_out, void* stream);
+
+/* ---------------------------------------------------------------- operators */
+
+/* Scratch bytes spops_spmm needs (row bins and, for dense panels, the panel plan). */
+SPOPS_API size_t spops_spmm_workspace_size(int32_t m, int32_t k, int32_t n, int32_t nnz, int dtype, int itype);
+
+/* SpMM (spops README, "Sparse Matrix Multiplication (SpMM)"): C = A * B.
+ * A: m x k CSR (A_val [nnz] dtype, row_offsets [m+1], row_idx [m], col_idx [nnz]);
+ * B: k x n row-major dtype; C: m x n row-major dtype, every element written (rows without
+ * entries become zeros). C must not overlap B or A's arrays. */
+SPOPS_API int spops_spmm(const void* A_val, const int32_t* row_offsets, const void* row_idx, const void* col_idx, int itype,
+               int dtype, int32_t m, int32_t k, int32_t nnz, const void* B, int32_t n, void* C, void* workspace,
+               size_t ws_bytes, void* stream);
+
+/* Scratch bytes spops_sddmm needs for the chosen backend. */
+SPOPS_API size_t spops_sddmm_workspace_size(int32_t m, int32_t n, int32_t kd, int32_t nnz, int dtype, int itype, int backend);
+
+/* SDDMM (spops README, "Sampled Dense-Dense Matrix Multiplication (SDDMM)"):
+ * out_val[k] = sum_t A[i, t] * BT[col_idx[k], t] for every entry k of row i of the m x n
+ * mask (out_row_offsets [m+1], out_row_idx [m], out_col_idx [nnz]).
+ * A: m x kd row-major; BT: n x kd row-major (the right operand transposed);
+ * out_val: [nnz] dtype, in CSR order. backend: spops_sddmm_backend. No scaling by mask
+ * values (the call takes none). */
+SPOPS_API int spops_sddmm(const int32_t* out_row_offsets, const void* out_row_idx, const void* out_col_idx, int itype,
+                int dtype, int32_t m, int32_t n, int32_t kd, int32_t nnz, const void* A, const void* BT,
+                void* out_val, int backend, void* workspace, size_t ws_bytes, void* stream);
+
+/* csr_add (spops README, "Sparse Addition"): C = B + A with A an m x n CSR matrix and B, C
+ * dense m x n row-major. C == B (in place) is allowed; partial overlap is not. Each entry
+ * is the correctly rounded sum of the two dtype values (bit-exact). row_idx is accepted
+ * for signature parity with the README and may be NULL. */
+SPOPS_API int spops_csr_add(const void* A_val, const int32_t* row_offsets, const void* row_idx, const void* col_idx,
+                  int itype, int dtype, int32_t m, int32_t n, int32_t nnz, const void* B, void* C, void* stream);
+
+/* ---------------------------------------------------------------- checks */
+
+/* Scratch bytes spops_check_csr needs (a bitmap of m bits for the permutation check). */
+SPOPS_API size_t spops_check_csr_workspace_size(int32_t m);
+
+/* Queue device-side checks of the CSR structure (row_offsets ends and order, column range
+ * and order) and, when row_idx is non-NULL, that row_idx is a permutation of 0..m-1.
+ * Violations are recorded in the device error word; read them with
+ * spops_get_device_error. */
+SPOPS_API int spops_check_csr(const int32_t* row_offsets, const void* col_idx, const void* row_idx, int itype, int32_t m,
+                    int32_t n, int32_t nnz, void* workspace, size_t ws_bytes, void* stream);
+
+/* Synchronize `stream`, then return in *code_out the first device error recorded on the
+ * current device since the last call (SPOPS_DEV_*), and clear it. */
+SPOPS_API int spops_get_device_error(void* stream, int32_t* code_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPOPS_GB300_H */

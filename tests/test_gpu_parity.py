@@ -1,0 +1,274 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same seeded
+inputs. Small cases compare every element; the full-size workloads compare sampled rows
+(and every element for csr_add, sort_rows and row_bins)."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from helpers import TOL, as_f64, assert_bits_equal, assert_close, index_dtype, sample_rows, to_gpu
+
+pytestmark = pytest.mark.gpu
+
+sp = pytest.importorskip("unstructured_sparse_linear_gb300")
+
+# Scaled-down versions of the five workloads: several tiles and ragged tails everywhere.
+SMALL = {
+    "tiny": wl.spec("tiny"),
+    "rosa_s": wl.spec("rosa", m=1000, n=1000, N=200, kd=200),
+    "llama_s": wl.spec("llama_mlp", m=1100, n=512, N=520, kd=264),
+    "zipf_s": wl.spec("zipf", m=4000, n=4000, N=36, mask_kw=(("max_len", 600), ("band", 700))),
+    "butterfly_s": wl.spec("butterfly", m=1024, n=256, N=256, kd=136, mask_kw=(("block", 32),)),
+    "rosa_i32": wl.spec("rosa", m=700, n=900, N=64, kd=72, mask_kw=(("row_frac", 0.3), ("col_frac", 0.3))),
+}
+
+
+@pytest.fixture(scope="module")
+def small_cases():
+    return {k: wl.generate(s) for k, s in SMALL.items()}
+
+
+def run_all_ops(w, g, backend="structure_aware"):
+    out = {}
+    if w.B is not None:
+        out["spmm"] = sp.spmm(g["val"], g["ro"], g["row_idx"], g["col"], g["B"], w.m)
+    if w.A is not None:
+        out["sddmm"] = sp.sddmm(g["ro"], g["row_idx"], g["col"], g["A"], g["BT"], backend=backend)
+    if w.W is not None:
+        out["csr_add"] = sp.csr_add(g["val"], g["ro"], g["row_idx"], g["col"], g["W"])
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+@pytest.mark.parametrize("backend", ["structure_aware", "general"])
+def test_small_all_elements(small_cases, name, backend):
+    w = small_cases[name]
+    idx = torch.int32 if name == "rosa_i32" else None
+    g = to_gpu(w, idx_dtype=idx)
+    out = run_all_ops(w, g, backend)
+    ro, col = w.row_offsets.numpy(), w.col_idx.numpy()
+    if "spmm" in out:
+        assert_close(out["spmm"], oracle.spmm(ro, col, w.values, w.B), w.dtype, f"{name} spmm")
+    if "sddmm" in out:
+        assert_close(out["sddmm"], oracle.sddmm(ro, col, w.A, w.BT), w.dtype, f"{name} sddmm {backend}")
+    if "csr_add" in out:
+        assert_bits_equal(out["csr_add"], oracle.csr_add(ro, col, w.values, w.W), w.dtype, f"{name} csr_add")
+
+
+@pytest.mark.parametrize("name", ["tiny", "rosa_s", "llama_s", "butterfly_s"])
+def test_integer_valued_inputs_are_exact(name):
+    """Small-integer inputs make every product and partial sum exact in fp32, so the GPU
+    must equal the oracle bit for bit whatever its summation order."""
+    s = SMALL[name]
+    if s.kd:
+        s = dataclasses.replace(s, kd=min(s.kd, 64))
+    w = wl.generate(s, integer_valued=True)
+    g = to_gpu(w)
+    ro, col = w.row_offsets.numpy(), w.col_idx.numpy()
+    for backend in ("structure_aware", "general"):
+        out = run_all_ops(w, g, backend)
+        if "spmm" in out:
+            assert_bits_equal(out["spmm"], oracle.spmm(ro, col, w.values, w.B), w.dtype, f"{name} spmm")
+        if "sddmm" in out:
+            assert_bits_equal(out["sddmm"], oracle.sddmm(ro, col, w.A, w.BT), w.dtype, f"{name} sddmm {backend}")
+
+
+def test_row_idx_any_permutation_gives_same_result(small_cases):
+    """No row of this case reaches a long-row bin, so every row is summed in the same order
+    whatever its position, and the results must be bitwise identical."""
+    w = small_cases["llama_s"]
+    assert np.diff(w.row_offsets.numpy()).max() < min(sp.SDDMM_LONG_ROW, sp.SPMM_LONG_ROW)
+    g = to_gpu(w)
+    ref = run_all_ops(w, g)
+    perm = wl.random_permutation(5, w.m)
+    g2 = to_gpu(w, row_idx=perm)
+    out = run_all_ops(w, g2)
+    for k in ref:
+        assert torch.equal(ref[k].view(torch.int16), out[k].view(torch.int16)), k
+
+
+def test_repeated_calls_are_bitwise_deterministic(small_cases):
+    w = small_cases["rosa_s"]
+    g = to_gpu(w)
+    a = run_all_ops(w, g)
+    b = run_all_ops(w, g)
+    for k in a:
+        assert torch.equal(a[k].view(torch.int16), b[k].view(torch.int16)), k
+
+
+# ------------------------------------------------------------------ row scheduler
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_sort_rows_and_bins_bit_exact(small_cases, name):
+    w = small_cases[name]
+    ro = w.row_offsets.numpy()
+    dev_ro = w.row_offsets.cuda()
+    for itd in ([torch.int16, torch.int32] if w.m <= 32768 else [torch.int32]):
+        got = sp.sort_rows(dev_ro, index_dtype=itd).cpu().numpy().astype(np.int64)
+        assert np.array_equal(got, oracle.sort_rows(ro))
+    for t in (1, 64, 256):
+        assert np.array_equal(sp.row_bins(dev_ro, t).cpu().numpy(), oracle.row_bins(ro, t))
+
+
+def test_sort_rows_many_ties_and_wide_keys():
+    rng = np.random.default_rng(3)
+    m = 70000
+    lens = rng.integers(0, 3, size=m)
+    lens[rng.choice(m, 20, replace=False)] = rng.integers(1000, 300000, size=20)  # keys over 3 radix digits
+    ro = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    got = sp.sort_rows(torch.from_numpy(ro).cuda(), index_dtype=torch.int32).cpu().numpy()
+    assert np.array_equal(got, oracle.sort_rows(ro))
+
+
+# ------------------------------------------------------------------ edge cases
+
+
+def _csr(m, n, rows, cols, dtype, seed=0):
+    ro, col = wl.csr_from_coords(np.asarray(rows), np.asarray(cols), m)
+    vals = wl.normal(seed, 1, (col.size,), 1.0, dtype)
+    return ro, col, vals
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_empty_matrix(dtype):
+    m, n, N = 37, 29, 24
+    ro = np.zeros(m + 1, dtype=np.int32)
+    col = np.zeros(0, dtype=np.int32)
+    tdt = wl.DTYPES[dtype]
+    B = torch.randn(n, N).to(tdt).cuda()
+    W = torch.randn(m, n).to(tdt).cuda()
+    dro, dcol = torch.from_numpy(ro).cuda(), torch.from_numpy(col).to(torch.int16).cuda()
+    ridx = torch.arange(m, dtype=torch.int16).cuda()
+    vals = torch.zeros(0, dtype=tdt).cuda()
+    C = sp.spmm(vals, dro, ridx, dcol, B, m)
+    assert torch.count_nonzero(C) == 0
+    assert torch.equal(sp.csr_add(vals, dro, ridx, dcol, W), W)
+    A = torch.randn(m, 16).to(tdt).cuda()
+    BT = torch.randn(n, 16).to(tdt).cuda()
+    assert sp.sddmm(dro, ridx, dcol, A, BT).numel() == 0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("N", [1, 7, 8, 33, 264])
+def test_ragged_and_unaligned_widths(dtype, N):
+    rng = np.random.default_rng(N)
+    m, n = 301, 257
+    mask = rng.random((m, n)) < 0.05
+    mask[5] = False
+    mask[7, :] = True  # one dense row (257 entries: a long row for SpMM)
+    ro, col, vals = _csr(m, n, *np.nonzero(mask), dtype)
+    tdt = wl.DTYPES[dtype]
+    B = wl.normal(9, 2, (n, N), 1.0, dtype)
+    A = wl.normal(9, 3, (m, N), 1.0, dtype)
+    BT = wl.normal(9, 4, (n, N), 1.0, dtype)
+    W = wl.normal(9, 5, (m, n), 1.0, dtype)
+    dro = torch.from_numpy(ro).cuda()
+    dcol = torch.from_numpy(col).to(torch.int16).cuda()
+    ridx = torch.from_numpy(oracle.sort_rows(ro)).to(torch.int16).cuda()
+    dv = vals.cuda()
+    C = sp.spmm(dv, dro, ridx, dcol, B.cuda(), m)
+    assert_close(C, oracle.spmm(ro, col, vals, B), dtype, "spmm")
+    for be in ("structure_aware", "general"):
+        o = sp.sddmm(dro, ridx, dcol, A.cuda(), BT.cuda(), backend=be)
+        assert_close(o, oracle.sddmm(ro, col, A, BT), dtype, f"sddmm {be}")
+    assert_bits_equal(sp.csr_add(dv, dro, ridx, dcol, W.cuda()), oracle.csr_add(ro, col, vals, W), dtype, "csr_add")
+
+
+def test_unaligned_pointers_take_the_plain_path():
+    """Operands that start 2 bytes into an allocation (not 16-byte aligned)."""
+    m, n, N = 64, 80, 40
+    rng = np.random.default_rng(1)
+    ro, col, vals = _csr(m, n, *np.nonzero(rng.random((m, n)) < 0.1), "f16")
+    B = wl.normal(1, 2, (n, N), 1.0, "f16")
+    W = wl.normal(1, 3, (m, n), 1.0, "f16")
+    Bbuf = torch.empty(n * N + 1, dtype=torch.float16, device="cuda")
+    Bbuf[1:] = B.cuda().view(-1)
+    Bu = Bbuf[1:].view(n, N)
+    Wbuf = torch.empty(m * n + 1, dtype=torch.float16, device="cuda")
+    Wbuf[1:] = W.cuda().view(-1)
+    Wu = Wbuf[1:].view(m, n)
+    Cbuf = torch.empty(m * N + 1, dtype=torch.float16, device="cuda")
+    dro, dcol = torch.from_numpy(ro).cuda(), torch.from_numpy(col).to(torch.int16).cuda()
+    ridx = torch.from_numpy(oracle.sort_rows(ro)).to(torch.int16).cuda()
+    C = sp.spmm(vals.cuda(), dro, ridx, dcol, Bu, m, out=Cbuf[1:].view(m, N))
+    assert_close(C, oracle.spmm(ro, col, vals, B), "f16", "spmm unaligned")
+    assert_bits_equal(sp.csr_add(vals.cuda(), dro, ridx, dcol, Wu), oracle.csr_add(ro, col, vals, W), "f16",
+                      "csr_add unaligned")
+
+
+def test_csr_add_in_place():
+    w = wl.generate(SMALL["llama_s"])
+    g = to_gpu(w)
+    want = oracle.csr_add(w.row_offsets.numpy(), w.col_idx.numpy(), w.values, w.W)
+    Wd = g["W"].clone()
+    out = sp.csr_add(g["val"], g["ro"], g["row_idx"], g["col"], Wd, out=Wd)
+    assert out.data_ptr() == Wd.data_ptr()
+    assert_bits_equal(Wd, want, "bf16", "csr_add in place")
+
+
+def test_single_long_row_and_int16_edge_columns():
+    m, n, N = 3, 32768, 16
+    cols = np.concatenate([np.arange(0, 32768, 8), [32767]])
+    cols = np.unique(cols)
+    rows = np.zeros_like(cols)
+    rows = np.concatenate([rows, [2]])
+    cols = np.concatenate([cols, [32767]])
+    ro, col, vals = _csr(m, n, rows, cols, "f32")
+    B = wl.normal(2, 2, (n, N), 1.0, "f32")
+    A = wl.normal(2, 3, (m, N), 1.0, "f32")
+    BT = wl.normal(2, 4, (n, N), 1.0, "f32")
+    dro = torch.from_numpy(ro).cuda()
+    dcol = torch.from_numpy(col.astype(np.int16)).cuda()
+    ridx = torch.from_numpy(oracle.sort_rows(ro)).to(torch.int16).cuda()
+    C = sp.spmm(vals.cuda(), dro, ridx, dcol, B.cuda(), m)
+    assert_close(C, oracle.spmm(ro, col, vals, B), "f32", "spmm long row")
+    for be in ("structure_aware", "general"):
+        assert_close(sp.sddmm(dro, ridx, dcol, A.cuda(), BT.cuda(), backend=be), oracle.sddmm(ro, col, A, BT),
+                     "f32", f"sddmm long row {be}")
+
+
+def test_check_csr_accepts_valid_and_flags_invalid():
+    w = wl.generate(SMALL["rosa_s"])
+    g = to_gpu(w)
+    sp.check_csr(g["ro"], g["col"], g["row_idx"], w.n)
+    bad_col = g["col"].clone()
+    bad_col[10] = w.n + 3  # out of range: the check reads it, never indexes with it
+    with pytest.raises(sp.SpopsError):
+        sp.check_csr(g["ro"], bad_col, g["row_idx"], w.n)
+    dup = g["row_idx"].clone()
+    dup[1] = dup[0]
+    with pytest.raises(sp.SpopsError):
+        sp.check_csr(g["ro"], g["col"], dup, w.n)
+    sp.check_csr(g["ro"], g["col"], g["row_idx"], w.n)  # the error word was cleared
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", wl.CONFIG_ORDER)
+def test_full_size_sampled(name):
+    w = wl.generate(name)
+    g = to_gpu(w)
+    ro, col = w.row_offsets.numpy(), w.col_idx.numpy()
+    dev_ro = g["ro"]
+    assert np.array_equal(sp.sort_rows(dev_ro, index_dtype=g["row_idx"].dtype).cpu().numpy().astype(np.int64),
+                          oracle.sort_rows(ro))
+    rows = sample_rows(ro, 48)
+    out = run_all_ops(w, g)
+    if "spmm" in out:
+        want = oracle.spmm(ro, col, w.values, w.B, rows=rows)
+        assert_close(out["spmm"][torch.from_numpy(rows).cuda()], want, w.dtype, f"{name} spmm rows")
+    if "sddmm" in out:
+        want = oracle.sddmm(ro, col, w.A, w.BT, rows=rows)
+        sel = np.concatenate([np.arange(ro[i], ro[i + 1]) for i in rows])
+        assert_close(out["sddmm"][torch.from_numpy(sel).cuda()], want, w.dtype, f"{name} sddmm rows")
+        gen = sp.sddmm(g["ro"], g["row_idx"], g["col"], g["A"], g["BT"], backend="general")
+        assert_close(gen[torch.from_numpy(sel).cuda()], want, w.dtype, f"{name} sddmm general rows")
+    if "csr_add" in out:
+        assert_bits_equal(out["csr_add"], oracle.csr_add(ro, col, w.values, w.W), w.dtype, f"{name} csr_add")

@@ -1,0 +1,217 @@
+"""spops_gb300: CSR sparse-adapter operators (SpMM, SDDMM, csr_add) for GB300 (sm_103a).
+
+Thin PyTorch binding over the C ABI in ``include/spops_gb300.h``. PyTorch provides device
+memory and the current stream; every step of every operator runs in this package's CUDA
+kernels. The functions keep the spops README signatures ("Sparse Operations (spops)",
+section "Usage"):
+
+    csr_add(A_val, A_row_offsets, A_row_indices, A_col_indices, B)
+    spmm(A_val, A_row_offsets, A_row_indices, A_col_indices, B, m)
+    sddmm(out_row_offsets, out_row_indices, out_col_indices, A, BT, backend="structure_aware")
+
+plus the row scheduler helpers ``sort_rows`` (builds row_idx) and ``row_bins``, and
+``check_csr`` (device-side structure check). Index lists are int16 (the README's type) or
+int32 (for matrices with more than 32768 rows or columns); row_offsets is int32. All
+inputs must be contiguous CUDA tensors on the same device.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+
+__all__ = ["spmm", "sddmm", "csr_add", "sort_rows", "row_bins", "check_csr", "SpopsError", "library_path",
+           "SPMM_LONG_ROW", "SDDMM_LONG_ROW"]
+
+SPMM_LONG_ROW = 256
+SDDMM_LONG_ROW = 64
+
+_DTYPE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+_ITYPE = {torch.int16: 0, torch.int32: 1}
+_BACKEND = {"structure_aware": 0, "general": 1, "sputnik": 1}
+_ERR_CLASS = {1: ValueError, 2: ValueError, 3: ValueError}
+
+
+class SpopsError(RuntimeError):
+    pass
+
+
+def library_path() -> str:
+    return _lib.lib_path()
+
+
+def _L():
+    return _lib.load()
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        lib = _L()
+        name = lib.spops_status_string(status).decode()
+        msg = lib.spops_last_error().decode()
+        raise _ERR_CLASS.get(status, SpopsError)(f"{what}: {name}: {msg}")
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _p(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None and t.numel() > 0 else ctypes.c_void_p(0)
+
+
+def _req(t, name, dtype=None, dtypes=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise ValueError(f"{name} dtype {t.dtype} not in {list(dtypes)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    return t
+
+
+def _itype(col_idx, row_idx=None):
+    it = _ITYPE.get(col_idx.dtype)
+    if it is None:
+        raise ValueError(f"index lists must be int16 or int32, got {col_idx.dtype}")
+    if row_idx is not None and row_idx.dtype != col_idx.dtype:
+        raise ValueError("row_idx and col_idx must have the same dtype")
+    return it
+
+
+def _ws(nbytes: int, device):
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+def sort_rows(row_offsets: torch.Tensor, nnz: int | None = None, index_dtype=torch.int16) -> torch.Tensor:
+    """row_idx: the rows ordered by nnz descending, ties by ascending row id."""
+    _req(row_offsets, "row_offsets", torch.int32)
+    m = row_offsets.numel() - 1
+    if nnz is None:
+        nnz = int(row_offsets[-1].item())
+    out = torch.empty(m, dtype=index_dtype, device=row_offsets.device)
+    lib = _L()
+    with torch.cuda.device(row_offsets.device):
+        ws = _ws(lib.spops_sort_rows_workspace_size(m), row_offsets.device)
+        _check(lib.spops_sort_rows(_p(row_offsets), m, int(nnz), _p(out), _ITYPE[index_dtype], _p(ws), ws.numel(),
+                                   _stream()), "sort_rows")
+    return out
+
+
+def row_bins(row_offsets: torch.Tensor, t_long: int) -> torch.Tensor:
+    """Device int32[4] = {0, #rows with nnz >= t_long, #rows with nnz >= 1, m}."""
+    _req(row_offsets, "row_offsets", torch.int32)
+    m = row_offsets.numel() - 1
+    out = torch.empty(4, dtype=torch.int32, device=row_offsets.device)
+    with torch.cuda.device(row_offsets.device):
+        _check(_L().spops_row_bins(_p(row_offsets), m, int(t_long), _p(out), _stream()), "row_bins")
+    return out
+
+
+def spmm(A_val, A_row_offsets, A_row_indices, A_col_indices, B, m: int, out: torch.Tensor | None = None):
+    """C = A @ B for a CSR matrix A (m rows) and a dense row-major B."""
+    _req(B, "B", dtypes=_DTYPE)
+    dev = B.device
+    _req(A_val, "A_val", B.dtype, device=dev)
+    _req(A_row_offsets, "A_row_offsets", torch.int32, device=dev)
+    _req(A_col_indices, "A_col_indices", device=dev)
+    _req(A_row_indices, "A_row_indices", device=dev)
+    if B.dim() != 2:
+        raise ValueError("B must be 2-D")
+    m = int(m)
+    if A_row_offsets.numel() != m + 1:
+        raise ValueError(f"A_row_offsets must have m + 1 = {m + 1} entries")
+    k, n = B.shape
+    it = _itype(A_col_indices, A_row_indices)
+    nnz = A_col_indices.numel()
+    if A_val.numel() != nnz or A_row_indices.numel() != m:
+        raise ValueError("A_val / A_row_indices lengths do not match col_idx / m")
+    C = out if out is not None else torch.empty((m, n), dtype=B.dtype, device=dev)
+    _req(C, "out", B.dtype, device=dev)
+    lib = _L()
+    dt = _DTYPE[B.dtype]
+    with torch.cuda.device(dev):
+        ws = _ws(lib.spops_spmm_workspace_size(m, k, n, nnz, dt, it), dev)
+        _check(lib.spops_spmm(_p(A_val), _p(A_row_offsets), _p(A_row_indices), _p(A_col_indices), it, dt, m, k, nnz,
+                              _p(B), n, _p(C), _p(ws), ws.numel(), _stream()), "spmm")
+    return C
+
+
+def sddmm(out_row_offsets, out_row_indices, out_col_indices, A, BT, backend: str = "structure_aware",
+          out: torch.Tensor | None = None):
+    """out[k] = A[i, :] . BT[col[k], :] for every entry k (row i) of the CSR mask."""
+    _req(A, "A", dtypes=_DTYPE)
+    dev = A.device
+    _req(BT, "BT", A.dtype, device=dev)
+    _req(out_row_offsets, "out_row_offsets", torch.int32, device=dev)
+    _req(out_col_indices, "out_col_indices", device=dev)
+    _req(out_row_indices, "out_row_indices", device=dev)
+    if A.dim() != 2 or BT.dim() != 2 or A.shape[1] != BT.shape[1]:
+        raise ValueError("A (m x kd) and BT (n x kd) must be 2-D with the same kd")
+    if backend not in _BACKEND:
+        raise ValueError(f"backend must be one of {list(_BACKEND)}")
+    m, kd = A.shape
+    n = BT.shape[0]
+    if out_row_offsets.numel() != m + 1 or out_row_indices.numel() != m:
+        raise ValueError("mask row arrays do not match A's rows")
+    it = _itype(out_col_indices, out_row_indices)
+    nnz = out_col_indices.numel()
+    res = out if out is not None else torch.empty(nnz, dtype=A.dtype, device=dev)
+    _req(res, "out", A.dtype, device=dev)
+    lib = _L()
+    dt, be = _DTYPE[A.dtype], _BACKEND[backend]
+    with torch.cuda.device(dev):
+        ws = _ws(lib.spops_sddmm_workspace_size(m, n, kd, nnz, dt, it, be), dev)
+        _check(lib.spops_sddmm(_p(out_row_offsets), _p(out_row_indices), _p(out_col_indices), it, dt, m, n, kd, nnz,
+                               _p(A), _p(BT), _p(res), be, _p(ws), ws.numel(), _stream()), "sddmm")
+    return res
+
+
+def csr_add(A_val, A_row_offsets, A_row_indices, A_col_indices, B, out: torch.Tensor | None = None):
+    """C = B + A for a CSR matrix A and a dense B of the same shape (out=B: in place)."""
+    _req(B, "B", dtypes=_DTYPE)
+    dev = B.device
+    _req(A_val, "A_val", B.dtype, device=dev)
+    _req(A_row_offsets, "A_row_offsets", torch.int32, device=dev)
+    _req(A_col_indices, "A_col_indices", device=dev)
+    if A_row_indices is not None:
+        _req(A_row_indices, "A_row_indices", device=dev)
+    if B.dim() != 2:
+        raise ValueError("B must be 2-D")
+    m, n = B.shape
+    if A_row_offsets.numel() != m + 1:
+        raise ValueError("A_row_offsets must have B.shape[0] + 1 entries")
+    it = _itype(A_col_indices, A_row_indices)
+    nnz = A_col_indices.numel()
+    C = out if out is not None else torch.empty_like(B)
+    _req(C, "out", B.dtype, device=dev)
+    with torch.cuda.device(dev):
+        _check(_L().spops_csr_add(_p(A_val), _p(A_row_offsets), _p(A_row_indices), _p(A_col_indices), it,
+                                  _DTYPE[B.dtype], m, n, nnz, _p(B), _p(C), _stream()), "csr_add")
+    return C
+
+
+def check_csr(row_offsets, col_idx, row_idx, n: int) -> None:
+    """Run the device-side CSR structure check; raise SpopsError on a violation."""
+    _req(row_offsets, "row_offsets", torch.int32)
+    dev = row_offsets.device
+    _req(col_idx, "col_idx", device=dev)
+    m = row_offsets.numel() - 1
+    it = _itype(col_idx, row_idx)
+    lib = _L()
+    with torch.cuda.device(dev):
+        ws = _ws(lib.spops_check_csr_workspace_size(m), dev)
+        _check(lib.spops_check_csr(_p(row_offsets), _p(col_idx), _p(row_idx), it, m, int(n), col_idx.numel(), _p(ws),
+                                   ws.numel(), _stream()), "check_csr")
+        code = ctypes.c_int32(0)
+        _check(lib.spops_get_device_error(_stream(), ctypes.byref(code)), "get_device_error")
+    if code.value != 0:
+        raise SpopsError(f"CSR check failed: device error code {code.value}")

@@ -1,0 +1,273 @@
+// C-ABI entry points: host-side argument validation, workspace carving and dispatch to
+// the kernels. Declarations and the contract of every call are in include/spops_gb300.h.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/spops_gb300.h"
+#include "common.cuh"
+#include "internal.h"
+#include "panel.h"
+
+namespace spops {
+
+// The device error word: one per device (a __device__ variable exists once per device
+// context). Kernels receive its address; spops_get_device_error reads and clears it.
+static __device__ int g_device_error;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+DeviceProps g_props[kMaxDevices];
+int* g_err_addr[kMaxDevices];
+thread_local char g_last_error[320];
+std::atomic<uint64_t> g_launches{0};
+
+int current_device() {
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess) return -1;
+    return d;
+}
+
+}  // namespace
+
+const DeviceProps& device_props() {
+    static DeviceProps none;
+    const int d = current_device();
+    if (d < 0 || d >= kMaxDevices) return none;
+    DeviceProps& p = g_props[d];
+    if (p.device != d) {
+        cudaDeviceGetAttribute(&p.sm_count, cudaDevAttrMultiProcessorCount, d);
+        cudaDeviceGetAttribute(&p.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d);
+        cudaDeviceGetAttribute(&p.cc_major, cudaDevAttrComputeCapabilityMajor, d);
+        cudaDeviceGetAttribute(&p.cc_minor, cudaDevAttrComputeCapabilityMinor, d);
+        if (p.sm_count <= 0) p.sm_count = 1;
+        p.device = d;
+    }
+    return p;
+}
+
+int* device_error_word() {
+    const int d = current_device();
+    if (d < 0 || d >= kMaxDevices) return nullptr;
+    if (!g_err_addr[d]) {
+        void* addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_device_error) != cudaSuccess) return nullptr;
+        g_err_addr[d] = static_cast<int*>(addr);
+    }
+    return g_err_addr[d];
+}
+
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+}  // namespace spops
+
+using namespace spops;
+
+namespace {
+
+int fail(int status, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+int ok() {
+    g_last_error[0] = 0;
+    return SPOPS_OK;
+}
+
+int cuda_status(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return ok();
+    return fail(SPOPS_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Checks shared by the CSR-consuming calls. Returns SPOPS_OK or an error status.
+int check_common(int itype, int dtype, int32_t m, int32_t ncols, int32_t nnz, const void* vals,
+                 const int32_t* ro, const void* row_idx, const void* col, bool need_vals, bool need_row_idx) {
+    if (dtype < SPOPS_F32 || dtype > SPOPS_BF16) return fail(SPOPS_ERR_INVALID_ARG, "dtype %d is not a spops_dtype", dtype);
+    if (itype != SPOPS_IDX16 && itype != SPOPS_IDX32)
+        return fail(SPOPS_ERR_INVALID_ARG, "itype %d is not a spops_itype", itype);
+    if (m < 0 || ncols < 0 || nnz < 0) return fail(SPOPS_ERR_INVALID_ARG, "negative size (m=%d n=%d nnz=%d)", m, ncols, nnz);
+    if (itype == SPOPS_IDX16 && (m > 32768 || ncols > 32768))
+        return fail(SPOPS_ERR_UNSUPPORTED, "int16 indices hold at most 32768 rows/columns (m=%d n=%d); use SPOPS_IDX32",
+                    m, ncols);
+    if (!ro) return fail(SPOPS_ERR_INVALID_ARG, "row_offsets is NULL");
+    if (!aligned(ro, 4)) return fail(SPOPS_ERR_INVALID_ARG, "row_offsets is not 4-byte aligned");
+    const size_t is = itype_size(itype), ds = dtype_size(dtype);
+    if (nnz > 0) {
+        if (!col) return fail(SPOPS_ERR_INVALID_ARG, "col_idx is NULL with nnz=%d", nnz);
+        if (!aligned(col, is)) return fail(SPOPS_ERR_INVALID_ARG, "col_idx is not aligned to its index size");
+        if (need_vals && !vals) return fail(SPOPS_ERR_INVALID_ARG, "values is NULL with nnz=%d", nnz);
+        if (need_vals && !aligned(vals, ds)) return fail(SPOPS_ERR_INVALID_ARG, "values is not aligned to its dtype");
+    }
+    if (need_row_idx && m > 0) {
+        if (!row_idx) return fail(SPOPS_ERR_INVALID_ARG, "row_idx is NULL with m=%d", m);
+        if (!aligned(row_idx, is)) return fail(SPOPS_ERR_INVALID_ARG, "row_idx is not aligned to its index size");
+    }
+    return SPOPS_OK;
+}
+
+bool overlaps(const void* a, size_t abytes, const void* b, size_t bbytes) {
+    if (!a || !b || !abytes || !bbytes) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + bbytes && y < x + abytes;
+}
+
+constexpr size_t kBinsBytes = 256;
+
+}  // namespace
+
+extern "C" {
+
+const char* spops_status_string(int status) {
+    switch (status) {
+        case SPOPS_OK: return "SPOPS_OK";
+        case SPOPS_ERR_INVALID_ARG: return "SPOPS_ERR_INVALID_ARG";
+        case SPOPS_ERR_UNSUPPORTED: return "SPOPS_ERR_UNSUPPORTED";
+        case SPOPS_ERR_WORKSPACE: return "SPOPS_ERR_WORKSPACE";
+        case SPOPS_ERR_CUDA: return "SPOPS_ERR_CUDA";
+        case SPOPS_ERR_DEVICE_CHECK: return "SPOPS_ERR_DEVICE_CHECK";
+        default: return "SPOPS_UNKNOWN_STATUS";
+    }
+}
+
+const char* spops_last_error(void) { return g_last_error; }
+
+const char* spops_version(void) { return "spops_gb300 0.1 sm_103a"; }
+
+uint64_t spops_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+size_t spops_sort_rows_workspace_size(int32_t m) { return m > 0 ? sort_rows_workspace_bytes(m) : 16; }
+
+int spops_sort_rows(const int32_t* row_offsets, int32_t m, int32_t nnz, void* row_idx_out, int itype,
+                    void* workspace, size_t ws_bytes, void* stream) {
+    if (itype != SPOPS_IDX16 && itype != SPOPS_IDX32) return fail(SPOPS_ERR_INVALID_ARG, "itype %d is not a spops_itype", itype);
+    if (m < 0 || nnz < 0) return fail(SPOPS_ERR_INVALID_ARG, "negative size (m=%d nnz=%d)", m, nnz);
+    if (itype == SPOPS_IDX16 && m > 32768) return fail(SPOPS_ERR_UNSUPPORTED, "int16 row_idx holds at most 32768 rows (m=%d)", m);
+    if (m == 0) return ok();
+    if (!row_offsets || !row_idx_out) return fail(SPOPS_ERR_INVALID_ARG, "row_offsets or row_idx_out is NULL");
+    if (!aligned(row_offsets, 4) || !aligned(row_idx_out, itype_size(itype)))
+        return fail(SPOPS_ERR_INVALID_ARG, "misaligned row_offsets or row_idx_out");
+    if (!workspace || !aligned(workspace, 16) || ws_bytes < spops_sort_rows_workspace_size(m))
+        return fail(SPOPS_ERR_WORKSPACE, "sort_rows needs a 16-byte aligned workspace of %zu bytes (got %zu)",
+                    spops_sort_rows_workspace_size(m), ws_bytes);
+    return cuda_status(launch_sort_rows(row_offsets, m, nnz, row_idx_out, itype, workspace, (cudaStream_t)stream),
+                       "sort_rows launch");
+}
+
+int spops_row_bins(const int32_t* row_offsets, int32_t m, int32_t t_long, int32_t* bins_out, void* stream) {
+    if (m < 0 || t_long < 1) return fail(SPOPS_ERR_INVALID_ARG, "need m >= 0 and t_long >= 1 (m=%d t_long=%d)", m, t_long);
+    if (!row_offsets || !bins_out) return fail(SPOPS_ERR_INVALID_ARG, "row_offsets or bins_out is NULL");
+    if (!aligned(row_offsets, 4) || !aligned(bins_out, 4)) return fail(SPOPS_ERR_INVALID_ARG, "misaligned pointer");
+    return cuda_status(launch_row_bins(row_offsets, m, t_long, bins_out, (cudaStream_t)stream), "row_bins launch");
+}
+
+size_t spops_spmm_workspace_size(int32_t m, int32_t k, int32_t n, int32_t nnz, int dtype, int itype) {
+    return kBinsBytes + panel_spmm_workspace_bytes(m, k, n, nnz, dtype, itype);
+}
+
+int spops_spmm(const void* A_val, const int32_t* row_offsets, const void* row_idx, const void* col_idx, int itype,
+               int dtype, int32_t m, int32_t k, int32_t nnz, const void* B, int32_t n, void* C, void* workspace,
+               size_t ws_bytes, void* stream) {
+    int st = check_common(itype, dtype, m, k, nnz, A_val, row_offsets, row_idx, col_idx, true, true);
+    if (st != SPOPS_OK) return st;
+    if (n < 0) return fail(SPOPS_ERR_INVALID_ARG, "negative n=%d", n);
+    if ((int64_t)m * n == 0) return ok();
+    const size_t ds = dtype_size(dtype);
+    if (!C || !aligned(C, ds)) return fail(SPOPS_ERR_INVALID_ARG, "C is NULL or misaligned");
+    if ((int64_t)k * n > 0 && (!B || !aligned(B, ds))) return fail(SPOPS_ERR_INVALID_ARG, "B is NULL or misaligned");
+    if (overlaps(C, (size_t)m * n * ds, B, (size_t)k * n * ds)) return fail(SPOPS_ERR_INVALID_ARG, "C overlaps B");
+    const size_t need = spops_spmm_workspace_size(m, k, n, nnz, dtype, itype);
+    if (!workspace || !aligned(workspace, 16) || ws_bytes < need)
+        return fail(SPOPS_ERR_WORKSPACE, "spmm needs a 16-byte aligned workspace of %zu bytes (got %zu)", need, ws_bytes);
+    cudaStream_t s = (cudaStream_t)stream;
+    int32_t* bins = static_cast<int32_t*>(workspace);
+    cudaError_t e = launch_row_bins(row_offsets, m, kSpmmLongRow, bins, s);
+    if (e != cudaSuccess) return cuda_status(e, "row_bins launch");
+    e = launch_spmm(dtype, itype, A_val, row_offsets, row_idx, col_idx, m, k, nnz, B, n, C, bins,
+                    static_cast<char*>(workspace) + kBinsBytes, s);
+    return cuda_status(e, "spmm launch");
+}
+
+size_t spops_sddmm_workspace_size(int32_t m, int32_t n, int32_t kd, int32_t nnz, int dtype, int itype, int backend) {
+    size_t extra = backend == SPOPS_SDDMM_STRUCTURE_AWARE ? panel_sddmm_workspace_bytes(m, n, kd, nnz, dtype, itype) : 0;
+    return kBinsBytes + extra;
+}
+
+int spops_sddmm(const int32_t* out_row_offsets, const void* out_row_idx, const void* out_col_idx, int itype,
+                int dtype, int32_t m, int32_t n, int32_t kd, int32_t nnz, const void* A, const void* BT,
+                void* out_val, int backend, void* workspace, size_t ws_bytes, void* stream) {
+    int st = check_common(itype, dtype, m, n, nnz, out_val, out_row_offsets, out_row_idx, out_col_idx, true, true);
+    if (st != SPOPS_OK) return st;
+    if (backend != SPOPS_SDDMM_STRUCTURE_AWARE && backend != SPOPS_SDDMM_GENERAL)
+        return fail(SPOPS_ERR_INVALID_ARG, "backend %d is not a spops_sddmm_backend", backend);
+    if (kd < 0) return fail(SPOPS_ERR_INVALID_ARG, "negative kd=%d", kd);
+    if (nnz == 0) return ok();
+    const size_t ds = dtype_size(dtype);
+    if (kd > 0 && (!A || !BT || !aligned(A, ds) || !aligned(BT, ds)))
+        return fail(SPOPS_ERR_INVALID_ARG, "A or BT is NULL or misaligned");
+    const size_t need = spops_sddmm_workspace_size(m, n, kd, nnz, dtype, itype, backend);
+    if (!workspace || !aligned(workspace, 16) || ws_bytes < need)
+        return fail(SPOPS_ERR_WORKSPACE, "sddmm needs a 16-byte aligned workspace of %zu bytes (got %zu)", need, ws_bytes);
+    cudaStream_t s = (cudaStream_t)stream;
+    int32_t* bins = static_cast<int32_t*>(workspace);
+    cudaError_t e = launch_row_bins(out_row_offsets, m, kSddmmLongRow, bins, s);
+    if (e != cudaSuccess) return cuda_status(e, "row_bins launch");
+    e = launch_sddmm(dtype, itype, out_row_offsets, out_row_idx, out_col_idx, m, n, kd, nnz, A, BT, out_val,
+                     backend == SPOPS_SDDMM_STRUCTURE_AWARE, bins, static_cast<char*>(workspace) + kBinsBytes, s);
+    return cuda_status(e, "sddmm launch");
+}
+
+int spops_csr_add(const void* A_val, const int32_t* row_offsets, const void* row_idx, const void* col_idx,
+                  int itype, int dtype, int32_t m, int32_t n, int32_t nnz, const void* B, void* C, void* stream) {
+    int st = check_common(itype, dtype, m, n, nnz, A_val, row_offsets, row_idx, col_idx, true, false);
+    if (st != SPOPS_OK) return st;
+    if (row_idx && !aligned(row_idx, itype_size(itype))) return fail(SPOPS_ERR_INVALID_ARG, "row_idx is misaligned");
+    if ((int64_t)m * n == 0) return ok();
+    const size_t ds = dtype_size(dtype);
+    if (!B || !C || !aligned(B, ds) || !aligned(C, ds)) return fail(SPOPS_ERR_INVALID_ARG, "B or C is NULL or misaligned");
+    const size_t bytes = (size_t)m * n * ds;
+    if (B != C && overlaps(B, bytes, C, bytes)) return fail(SPOPS_ERR_INVALID_ARG, "C partially overlaps B");
+    return cuda_status(launch_csr_add(dtype, itype, A_val, row_offsets, col_idx, m, n, nnz, B, C, (cudaStream_t)stream),
+                       "csr_add launch");
+}
+
+size_t spops_check_csr_workspace_size(int32_t m) { return align_up(((size_t)(m > 0 ? m : 0) + 31) / 32 * 4, 256) + 16; }
+
+int spops_check_csr(const int32_t* row_offsets, const void* col_idx, const void* row_idx, int itype, int32_t m,
+                    int32_t n, int32_t nnz, void* workspace, size_t ws_bytes, void* stream) {
+    int st = check_common(itype, SPOPS_F32, m, n, nnz, nullptr, row_offsets, row_idx, col_idx, false, false);
+    if (st != SPOPS_OK) return st;
+    if (row_idx && (!workspace || !aligned(workspace, 16) || ws_bytes < spops_check_csr_workspace_size(m)))
+        return fail(SPOPS_ERR_WORKSPACE, "check_csr needs a workspace of %zu bytes to check row_idx",
+                    spops_check_csr_workspace_size(m));
+    int* err = device_error_word();
+    if (!err) return fail(SPOPS_ERR_CUDA, "no device error word on the current device");
+    return cuda_status(launch_check_csr(row_offsets, col_idx, row_idx, itype, m, n, nnz,
+                                        static_cast<uint32_t*>(workspace), err, (cudaStream_t)stream),
+                       "check_csr launch");
+}
+
+int spops_get_device_error(void* stream, int32_t* code_out) {
+    if (!code_out) return fail(SPOPS_ERR_INVALID_ARG, "code_out is NULL");
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_status(e, "stream synchronize");
+    int* err = device_error_word();
+    if (!err) return fail(SPOPS_ERR_CUDA, "no device error word on the current device");
+    int v = 0;
+    e = cudaMemcpy(&v, err, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_status(e, "read device error word");
+    const int zero = 0;
+    e = cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_status(e, "clear device error word");
+    *code_out = v;
+    return ok();
+}
+
+}  // extern "C"

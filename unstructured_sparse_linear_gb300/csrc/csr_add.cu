@@ -1,0 +1,153 @@
+// csr_add: C = B + A, A an m x n CSR matrix, B and C dense m x n row-major (C may be B).
+//
+// spops README ("Sparse Operations (spops)"), section "Sparse Addition [dense = sparse +
+// dense]": a sparse CSR matrix is added to a dense matrix.
+//
+// The operation is a dense stream (2 * m * n * sizeof(T) bytes) with a sparse scatter on
+// top, so the kernel is built around the copy engine: each CTA owns a ring of 16 KB shared
+// memory stages. One thread moves a tile of B into a stage with a 1-D bulk async copy
+// (TMA, completion on an mbarrier), the CTA adds the tile's CSR entries in place, and the
+// same thread streams the stage back to C with a bulk store. Tiles are flat 16 KB slices
+// of the row-major matrix, so the only alignment requirement is a 16-byte aligned B and
+// C; otherwise a plain-load variant of the same kernel runs.
+//
+// Each entry is added in fp32 and rounded once to T. For fp32 that is the IEEE sum. For
+// fp16/bf16 the fp32 sum of two such values is rounded twice (to fp32, then to T), which
+// gives the correctly rounded result because fp32 has at least 2p+2 significand bits
+// (Figueroa's double-rounding theorem), so the output matches the exact sum rounded once.
+#include "common.cuh"
+#include "internal.h"
+
+namespace spops {
+namespace {
+
+constexpr int kAddThreads = 256;
+constexpr int kAddTileBytes = 16384;
+constexpr int kAddStages = 3;
+constexpr int kAddSmem = kAddTileBytes * kAddStages;
+
+template <typename T, typename I, bool kBulk>
+__global__ void __launch_bounds__(kAddThreads) csr_add_kernel(const T* __restrict__ vals,
+                                                               const int32_t* __restrict__ ro,
+                                                               const I* __restrict__ col, int32_t n, const T* B,
+                                                               T* C, int64_t total, int* err) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ __align__(8) uint64_t full_bar[kAddStages];
+    constexpr int64_t E = kAddTileBytes / sizeof(T);
+    const int tid = threadIdx.x;
+    const int64_t ntiles = (total + E - 1) / E;
+    const int64_t my_tiles = (int64_t)blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+    auto stage = [&](int s) { return reinterpret_cast<T*>(smem + s * kAddTileBytes); };
+    auto tile_elems = [&](int64_t t) { return (int)min64(E, total - t * E); };
+    auto bulk_elems = [&](int cnt) { return (int)((cnt * (int)sizeof(T)) / 16 * 16 / (int)sizeof(T)); };
+    auto issue_load = [&](int64_t j, int s) {
+        const int64_t t = blockIdx.x + j * gridDim.x;
+        const int be = bulk_elems(tile_elems(t));
+        const uint32_t bar = smem_u32(&full_bar[s]);
+        mbar_arrive_expect_tx(bar, (uint32_t)(be * sizeof(T)));
+        if (be) bulk_g2s(smem_u32(stage(s)), B + t * E, (uint32_t)(be * sizeof(T)), bar);
+    };
+
+    if (kBulk) {
+        if (tid == 0) {
+            for (int s = 0; s < kAddStages; ++s) mbar_init(smem_u32(&full_bar[s]), 1);
+            fence_mbar_init();
+        }
+        __syncthreads();
+        if (tid == 0)
+            for (int64_t j = 0; j < min64(kAddStages, my_tiles); ++j) issue_load(j, (int)j);
+    }
+
+    for (int64_t j = 0; j < my_tiles; ++j) {
+        const int s = (int)(j % kAddStages);
+        const int64_t t = blockIdx.x + j * gridDim.x;
+        const int64_t f0 = t * E;
+        const int cnt = tile_elems(t);
+        const int64_t f1 = f0 + cnt;
+        T* buf = stage(s);
+        bool ok = true;
+        if (kBulk) {
+            ok = mbar_wait(smem_u32(&full_bar[s]), (uint32_t)((j / kAddStages) & 1), err);
+            const int be = bulk_elems(cnt);
+            if (tid < cnt - be) buf[be + tid] = B[f0 + be + tid];
+        } else {
+            for (int e = tid; e < cnt; e += kAddThreads) buf[e] = B[f0 + e];
+        }
+        if (!__syncthreads_and(ok)) {
+            if (tid == 0) bulk_wait<0>();
+            return;
+        }
+        // Entries whose flat position falls in [f0, f1): rows r0..r1, CSR range [kb, ke).
+        const int32_t r0 = (int32_t)(f0 / n), r1 = (int32_t)((f1 - 1) / n);
+        const int32_t kb = ro[r0], ke = ro[r1 + 1];
+        for (int32_t k = kb + tid; k < ke; k += kAddThreads) {
+            int32_t lo = r0, hi = r1;  // row of entry k: largest r with ro[r] <= k
+            while (lo < hi) {
+                const int32_t mid = (lo + hi + 1) >> 1;
+                if (ro[mid] <= k) lo = mid;
+                else hi = mid - 1;
+            }
+            const int64_t f = (int64_t)lo * n + idx_of(col[k]);
+            if (f >= f0 && f < f1) {
+                T& x = buf[f - f0];
+                x = Elt<T>::from_f(Elt<T>::to_f(x) + Elt<T>::to_f(vals[k]));
+            }
+        }
+        if (kBulk) fence_proxy_async_smem();
+        __syncthreads();
+        if (kBulk) {
+            if (tid == 0) {
+                const int be = bulk_elems(cnt);
+                if (be) {
+                    bulk_s2g(C + f0, smem_u32(buf), (uint32_t)(be * sizeof(T)));
+                    bulk_commit();
+                }
+                for (int e = be; e < cnt; ++e) C[f0 + e] = buf[e];
+                if (j + kAddStages < my_tiles) {
+                    bulk_wait_read<0>();  // stage s is free once the store has read it
+                    issue_load(j + kAddStages, s);
+                }
+            }
+        } else {
+            for (int e = tid; e < cnt; e += kAddThreads) C[f0 + e] = buf[e];
+            __syncthreads();
+        }
+    }
+    if (kBulk && tid == 0) bulk_wait<0>();
+}
+
+template <typename T, typename I>
+cudaError_t run(const void* vals, const int32_t* ro, const void* col, int32_t m, int32_t n, const void* B, void* C,
+                cudaStream_t s) {
+    const int64_t total = (int64_t)m * n;
+    if (total == 0) return cudaSuccess;
+    const int64_t E = kAddTileBytes / sizeof(T);
+    const int64_t ntiles = (total + E - 1) / E;
+    const DeviceProps& p = device_props();
+    const int grid = (int)min64(ntiles, (int64_t)p.sm_count * 4);
+    const bool bulk = ((uintptr_t)B % 16 == 0) && ((uintptr_t)C % 16 == 0);
+    auto kern = bulk ? csr_add_kernel<T, I, true> : csr_add_kernel<T, I, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAddSmem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kAddThreads, kAddSmem, s>>>(static_cast<const T*>(vals), ro, static_cast<const I*>(col), n,
+                                             static_cast<const T*>(B), static_cast<T*>(C), total,
+                                             device_error_word());
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_csr_add(int dt, int it, const void* vals, const int32_t* ro, const void* col, int32_t m,
+                           int32_t n, int32_t nnz, const void* B, void* C, cudaStream_t s) {
+    (void)nnz;
+    if (dt == kF32) return it == kIdx16 ? run<float, uint16_t>(vals, ro, col, m, n, B, C, s)
+                                        : run<float, int32_t>(vals, ro, col, m, n, B, C, s);
+    if (dt == kF16) return it == kIdx16 ? run<__half, uint16_t>(vals, ro, col, m, n, B, C, s)
+                                        : run<__half, int32_t>(vals, ro, col, m, n, B, C, s);
+    return it == kIdx16 ? run<__nv_bfloat16, uint16_t>(vals, ro, col, m, n, B, C, s)
+                        : run<__nv_bfloat16, int32_t>(vals, ro, col, m, n, B, C, s);
+}
+
+}  // namespace spops

@@ -1,0 +1,58 @@
+// Internal launcher interface between the C-ABI layer (abi.cu) and the kernel files.
+// Nothing here is exported from the shared library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace spops {
+
+enum DType { kF32 = 0, kF16 = 1, kBF16 = 2 };
+enum IType { kIdx16 = 0, kIdx32 = 1 };
+
+struct DeviceProps {
+    int device = -1;
+    int sm_count = 0;
+    int max_smem_optin = 0;
+    int cc_major = 0, cc_minor = 0;
+};
+
+// Properties of the current device (queried once per device).
+const DeviceProps& device_props();
+// Device address of this library's error word on the current device.
+int* device_error_word();
+// Add n to the process-wide count of kernels this library has launched.
+void count_launches(int n);
+
+inline size_t dtype_size(int dt) { return dt == kF32 ? 4 : 2; }
+inline size_t itype_size(int it) { return it == kIdx16 ? 2 : 4; }
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Row-bin thresholds used by the operators (rows with nnz >= threshold are "long").
+constexpr int32_t kSpmmLongRow = 256;
+constexpr int32_t kSddmmLongRow = 64;
+
+// csr_add.cu
+cudaError_t launch_csr_add(int dt, int it, const void* vals, const int32_t* ro, const void* col, int32_t m,
+                           int32_t n, int32_t nnz, const void* B, void* C, cudaStream_t s);
+
+// sort_rows.cu
+size_t sort_rows_workspace_bytes(int32_t m);
+cudaError_t launch_sort_rows(const int32_t* ro, int32_t m, int32_t nnz, void* row_idx_out, int it, void* ws,
+                             cudaStream_t s);
+cudaError_t launch_row_bins(const int32_t* ro, int32_t m, int32_t t_long, int32_t* bins, cudaStream_t s);
+cudaError_t launch_check_csr(const int32_t* ro, const void* col, const void* row_idx, int it, int32_t m, int32_t n,
+                             int32_t nnz, uint32_t* perm_bits, int* err, cudaStream_t s);
+
+// spmm.cu
+cudaError_t launch_spmm_general(int dt, int it, const void* vals, const int32_t* ro, const void* row_idx,
+                                const void* col, int32_t m, int32_t k, const void* B, int32_t n, void* C,
+                                const int32_t* bins, cudaStream_t s);
+
+// sddmm.cu
+cudaError_t launch_sddmm_general(int dt, int it, const int32_t* ro, const void* row_idx, const void* col, int32_t m,
+                                 int32_t n, int32_t kd, const void* A, const void* BT, void* out,
+                                 const int32_t* bins, cudaStream_t s);
+
+}  // namespace spops

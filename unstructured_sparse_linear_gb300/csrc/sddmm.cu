@@ -1,0 +1,137 @@
+// SDDMM, general path: out[k] = sum_t A[i, t] * BT[col[k], t] for every entry k (row i)
+// of an m x n CSR mask; A is m x kd and BT is n x kd, both row-major; fp32 accumulation,
+// one rounding to the operand dtype.
+//
+// spops README ("Sparse Operations (spops)"), section "Sampled Dense-Dense Matrix
+// Multiplication (SDDMM) [sparse = dense x dense]": the first kernel listed there works
+// for any sparsity pattern; BT is the transposed right operand.
+//
+// Row scheduler: rows in row_idx order, split by the row bins into
+//   * long rows (nnz >= kSddmmLongRow): one CTA per row, its 8 warps take interleaved
+//     batches of entries, so all of them stream the same A row through L1;
+//   * short rows: a group of G lanes per row (G covers kd in 16-byte vectors, at most 32).
+// A batch holds NB entries: the group walks kd once, loading each A vector once and the NB
+// BT vectors beside it, keeps NB per-lane partial dot products and finishes them with an
+// xor-shuffle butterfly inside the group. Empty rows are skipped.
+#include "common.cuh"
+#include "internal.h"
+
+namespace spops {
+namespace {
+
+constexpr int kSddmmThreads = 256;
+constexpr int kSddmmWarps = kSddmmThreads / 32;
+constexpr int kNB = 4;
+
+template <typename T, int V>
+__device__ __forceinline__ void load_vec(const T* __restrict__ p, float (&f)[V]) {
+    if constexpr (V == 1) {
+        f[0] = Elt<T>::to_f(*p);
+    } else {
+        Elt<T>::unpack(ld_nc_v4(p), f);
+    }
+}
+
+template <typename T, typename I, int V>
+__device__ __forceinline__ void sddmm_batch(int row, int32_t kb, int cnt, const I* __restrict__ col,
+                                            const T* __restrict__ A, const T* __restrict__ BT,
+                                            T* __restrict__ out, int32_t kd, int G, int gl, unsigned gmask) {
+    int c[kNB];
+#pragma unroll
+    for (int j = 0; j < kNB; ++j) c[j] = j < cnt ? idx_of(col[kb + j]) : 0;
+    float acc[kNB];
+#pragma unroll
+    for (int j = 0; j < kNB; ++j) acc[j] = 0.f;
+    const T* Arow = A + (int64_t)row * kd;
+    for (int32_t t = gl * V; t < kd; t += G * V) {
+        float a[V];
+        load_vec<T, V>(Arow + t, a);
+        float b[kNB][V];
+#pragma unroll
+        for (int j = 0; j < kNB; ++j) {
+            if (j < cnt) load_vec<T, V>(BT + (int64_t)c[j] * kd + t, b[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < kNB; ++j) {
+            if (j < cnt) {
+#pragma unroll
+                for (int e = 0; e < V; ++e) acc[j] = fmaf(a[e], b[j][e], acc[j]);
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < kNB; ++j)
+        for (int off = G >> 1; off; off >>= 1) acc[j] += __shfl_xor_sync(gmask, acc[j], off);
+    if (gl == 0) {
+#pragma unroll
+        for (int j = 0; j < kNB; ++j)
+            if (j < cnt) out[kb + j] = Elt<T>::from_f(acc[j]);
+    }
+}
+
+template <typename T, typename I, int V>
+__global__ void __launch_bounds__(kSddmmThreads)
+sddmm_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx, const I* __restrict__ col,
+                  const T* __restrict__ A, const T* __restrict__ BT, T* __restrict__ out, int32_t kd, int G,
+                  const int32_t* __restrict__ bins) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int32_t n_long = bins[1], n_nonempty = bins[2];
+
+    // ---- long rows: a CTA per row
+    for (int32_t p = blockIdx.x; p < n_long; p += gridDim.x) {
+        const int row = idx_of(row_idx[p]);
+        const int32_t k0 = ro[row], k1 = ro[row + 1];
+        for (int32_t kb = k0 + warp * kNB; kb < k1; kb += kSddmmWarps * kNB)
+            sddmm_batch<T, I, V>(row, kb, min(kNB, k1 - kb), col, A, BT, out, kd, 32, lane, 0xffffffffu);
+    }
+
+    // ---- short rows: a group of G lanes per row
+    const int gpw = 32 / G;
+    const int gw = lane / G, gl = lane % G;
+    const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (gw * G));
+    const int64_t gid = ((int64_t)blockIdx.x * kSddmmWarps + warp) * gpw + gw;
+    const int64_t ngroups = (int64_t)gridDim.x * kSddmmWarps * gpw;
+    for (int64_t p = n_long + gid; p < n_nonempty; p += ngroups) {
+        const int row = idx_of(row_idx[p]);
+        const int32_t k0 = ro[row], k1 = ro[row + 1];
+        for (int32_t kb = k0; kb < k1; kb += kNB)
+            sddmm_batch<T, I, V>(row, kb, min(kNB, k1 - kb), col, A, BT, out, kd, G, gl, gmask);
+    }
+}
+
+template <typename T, typename I>
+cudaError_t run(const int32_t* ro, const void* row_idx, const void* col, int32_t kd, const void* A, const void* BT,
+                void* out, const int32_t* bins, cudaStream_t s) {
+    constexpr int VV = Elt<T>::kVec;
+    const bool vec = ((int64_t)kd * sizeof(T)) % 16 == 0 && (uintptr_t)A % 16 == 0 && (uintptr_t)BT % 16 == 0;
+    auto kern = vec ? sddmm_rows_kernel<T, I, VV> : sddmm_rows_kernel<T, I, 1>;
+    const int V = vec ? VV : 1;
+    int G = 1;
+    while (G < 32 && (int64_t)G * V < kd) G <<= 1;
+    int occ = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kSddmmThreads, 0);
+    if (e != cudaSuccess) return e;
+    const int grid = device_props().sm_count * (occ > 0 ? occ : 1);
+    kern<<<grid, kSddmmThreads, 0, s>>>(ro, static_cast<const I*>(row_idx), static_cast<const I*>(col),
+                                        static_cast<const T*>(A), static_cast<const T*>(BT), static_cast<T*>(out),
+                                        kd, G, bins);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_sddmm_general(int dt, int it, const int32_t* ro, const void* row_idx, const void* col, int32_t m,
+                                 int32_t n, int32_t kd, const void* A, const void* BT, void* out,
+                                 const int32_t* bins, cudaStream_t s) {
+    (void)m;
+    (void)n;
+    if (dt == kF32) return it == kIdx16 ? run<float, uint16_t>(ro, row_idx, col, kd, A, BT, out, bins, s)
+                                        : run<float, int32_t>(ro, row_idx, col, kd, A, BT, out, bins, s);
+    if (dt == kF16) return it == kIdx16 ? run<__half, uint16_t>(ro, row_idx, col, kd, A, BT, out, bins, s)
+                                        : run<__half, int32_t>(ro, row_idx, col, kd, A, BT, out, bins, s);
+    return it == kIdx16 ? run<__nv_bfloat16, uint16_t>(ro, row_idx, col, kd, A, BT, out, bins, s)
+                        : run<__nv_bfloat16, int32_t>(ro, row_idx, col, kd, A, BT, out, bins, s);
+}
+
+}  // namespace spops

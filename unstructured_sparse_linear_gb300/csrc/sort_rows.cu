@@ -1,0 +1,277 @@
+// Row scheduler support: the nnz-sorted row permutation (row_idx), the row bins that
+// split it into long / short / empty rows, and an on-device CSR structure check.
+//
+// spops README ("Sparse Operations (spops)"), section "Usage": row_idx is a permutation
+// of 0..m-1 that sorts the rows by their number of non-zeros. The README does not give
+// the direction; this library sorts by nnz descending and keeps ascending row ids among
+// rows with equal counts, so long rows come first and empty rows last.
+//
+// sort_rows is a stable least-significant-digit radix sort on the key (nnz - nnz_i),
+// 8 bits per pass: a per-block digit histogram, one exclusive scan over all blocks'
+// histograms, and a stable scatter that ranks equal digits inside a block with warp
+// match masks. The first pass derives the key from row_offsets directly.
+#include "common.cuh"
+#include "internal.h"
+
+namespace spops {
+namespace {
+
+constexpr int kSortThreads = 256;
+constexpr int kSortRounds = 8;
+constexpr int kSortTile = kSortThreads * kSortRounds;
+constexpr int kRadix = 256;
+constexpr int kScanThreads = 1024;
+
+__device__ __forceinline__ uint32_t sort_key(const int32_t* ro, const uint32_t* keys_in, int32_t i,
+                                             uint32_t key_base) {
+    return keys_in ? keys_in[i] : key_base - (uint32_t)(ro[i + 1] - ro[i]);
+}
+
+__global__ void __launch_bounds__(kSortThreads)
+radix_hist_kernel(const int32_t* __restrict__ ro, const uint32_t* __restrict__ keys_in, int32_t m,
+                  uint32_t key_base, int shift, uint32_t* __restrict__ hist) {
+    __shared__ uint32_t cnt[kRadix];
+    cnt[threadIdx.x] = 0;
+    __syncthreads();
+    const int32_t base = blockIdx.x * kSortTile;
+    for (int r = 0; r < kSortRounds; ++r) {
+        const int32_t i = base + r * kSortThreads + threadIdx.x;
+        if (i < m) atomicAdd(&cnt[(sort_key(ro, keys_in, i, key_base) >> shift) & (kRadix - 1)], 1u);
+    }
+    __syncthreads();
+    hist[threadIdx.x * gridDim.x + blockIdx.x] = cnt[threadIdx.x];
+}
+
+// Exclusive scan, in place, of `total` counters with one block.
+__global__ void __launch_bounds__(kScanThreads) radix_scan_kernel(uint32_t* __restrict__ hist, int32_t total) {
+    __shared__ uint32_t part[kScanThreads];
+    const int32_t per = (total + kScanThreads - 1) / kScanThreads;
+    const int32_t b = threadIdx.x * per, e = min(total, b + per);
+    uint32_t s = 0;
+    for (int32_t i = b; i < e; ++i) s += hist[i];
+    part[threadIdx.x] = s;
+    __syncthreads();
+    for (int off = 1; off < kScanThreads; off <<= 1) {  // Hillis-Steele inclusive scan
+        uint32_t v = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
+        __syncthreads();
+        part[threadIdx.x] += v;
+        __syncthreads();
+    }
+    uint32_t run = threadIdx.x ? part[threadIdx.x - 1] : 0;
+    for (int32_t i = b; i < e; ++i) {
+        const uint32_t c = hist[i];
+        hist[i] = run;
+        run += c;
+    }
+}
+
+template <typename OutI>
+__global__ void __launch_bounds__(kSortThreads)
+radix_scatter_kernel(const int32_t* __restrict__ ro, const uint32_t* __restrict__ keys_in,
+                     const int32_t* __restrict__ vals_in, int32_t m, uint32_t key_base, int shift,
+                     const uint32_t* __restrict__ offsets, uint32_t* __restrict__ keys_out,
+                     OutI* __restrict__ vals_out) {
+    __shared__ uint32_t warp_cnt[kSortThreads / 32][kRadix];
+    __shared__ uint32_t running[kRadix];
+    __shared__ uint32_t dbase[kRadix];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    running[tid] = 0;
+    dbase[tid] = offsets[tid * gridDim.x + blockIdx.x];
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    const int32_t base = blockIdx.x * kSortTile;
+    for (int r = 0; r < kSortRounds; ++r) {
+#pragma unroll
+        for (int w = 0; w < kSortThreads / 32; ++w) warp_cnt[w][tid] = 0;
+        __syncthreads();
+        const int32_t i = base + r * kSortThreads + tid;
+        const bool valid = i < m;
+        uint32_t key = 0;
+        int32_t val = 0;
+        int d = kRadix + lane;  // unique per invalid lane: never matches a real digit
+        if (valid) {
+            key = sort_key(ro, keys_in, i, key_base);
+            val = vals_in ? vals_in[i] : i;
+            d = (int)((key >> shift) & (kRadix - 1));
+        }
+        const uint32_t peers = __match_any_sync(0xffffffffu, d);
+        const uint32_t rank = __popc(peers & lt_mask);
+        if (valid && lane == __ffs(peers) - 1) warp_cnt[warp][d] = __popc(peers);
+        __syncthreads();
+        {  // digit tid: exclusive prefix over warps, continuing from earlier rounds
+            uint32_t acc = running[tid];
+#pragma unroll
+            for (int w = 0; w < kSortThreads / 32; ++w) {
+                const uint32_t c = warp_cnt[w][tid];
+                warp_cnt[w][tid] = acc;
+                acc += c;
+            }
+            running[tid] = acc;
+        }
+        __syncthreads();
+        if (valid) {
+            const uint32_t pos = dbase[d] + warp_cnt[warp][d] + rank;
+            if (keys_out) keys_out[pos] = key;
+            vals_out[pos] = static_cast<OutI>(val);
+        }
+        __syncthreads();
+    }
+}
+
+template <typename OutI>
+__global__ void iota_kernel(OutI* out, int32_t m) {
+    for (int32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < m; i += gridDim.x * blockDim.x)
+        out[i] = static_cast<OutI>(i);
+}
+
+__global__ void __launch_bounds__(1024) row_bins_kernel(const int32_t* __restrict__ ro, int32_t m, int32_t t_long,
+                                                        int32_t* __restrict__ bins) {
+    __shared__ int32_t red[2][32];
+    int32_t nl = 0, ne = 0;
+    for (int32_t i = threadIdx.x; i < m; i += blockDim.x) {
+        const int32_t c = ro[i + 1] - ro[i];
+        nl += c >= t_long;
+        ne += c >= 1;
+    }
+    for (int off = 16; off; off >>= 1) {
+        nl += __shfl_xor_sync(0xffffffffu, nl, off);
+        ne += __shfl_xor_sync(0xffffffffu, ne, off);
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) {
+        red[0][warp] = nl;
+        red[1][warp] = ne;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        nl = lane < (int)(blockDim.x >> 5) ? red[0][lane] : 0;
+        ne = lane < (int)(blockDim.x >> 5) ? red[1][lane] : 0;
+        for (int off = 16; off; off >>= 1) {
+            nl += __shfl_xor_sync(0xffffffffu, nl, off);
+            ne += __shfl_xor_sync(0xffffffffu, ne, off);
+        }
+        if (lane == 0) {
+            bins[0] = 0;
+            bins[1] = nl;
+            bins[2] = ne;
+            bins[3] = m;
+        }
+    }
+}
+
+// --------------------------------------------------------------- structure check
+
+template <typename I>
+__global__ void check_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ col, int32_t m, int32_t n,
+                                  int32_t nnz, int* err) {
+    const int32_t stride = gridDim.x * blockDim.x;
+    const int32_t tid = blockIdx.x * blockDim.x + threadIdx.x;
+    if (tid == 0 && (ro[0] != 0 || ro[m] != nnz)) record_error(err, kDevErrRowOffsets);
+    for (int32_t i = tid; i < m; i += stride) {
+        const int32_t b = ro[i], e = ro[i + 1];
+        if (b > e || b < 0 || e > nnz) {
+            record_error(err, kDevErrRowOffsets);
+            continue;
+        }
+        int prev = -1;
+        for (int32_t k = b; k < e; ++k) {
+            const int c = idx_of(col[k]);
+            if (c < 0 || c >= n) record_error(err, kDevErrColRange);
+            else if (c <= prev) record_error(err, kDevErrColOrder);
+            prev = c;
+        }
+    }
+}
+
+__global__ void zero_words_kernel(uint32_t* p, int32_t words) {
+    for (int32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < words; i += gridDim.x * blockDim.x) p[i] = 0;
+}
+
+template <typename I>
+__global__ void check_perm_kernel(const I* __restrict__ row_idx, int32_t m, uint32_t* bits, int* err) {
+    for (int32_t p = blockIdx.x * blockDim.x + threadIdx.x; p < m; p += gridDim.x * blockDim.x) {
+        const int r = idx_of(row_idx[p]);
+        if (r < 0 || r >= m) {
+            record_error(err, kDevErrRowIdxPerm);
+            continue;
+        }
+        const uint32_t bit = 1u << (r & 31);
+        if (atomicOr(&bits[r >> 5], bit) & bit) record_error(err, kDevErrRowIdxPerm);
+    }
+}
+
+int grid_for(int64_t items, int threads, int per_sm) {
+    const int64_t g = (items + threads - 1) / threads;
+    return (int)max64(1, min64(g, (int64_t)device_props().sm_count * per_sm));
+}
+
+}  // namespace
+
+size_t sort_rows_workspace_bytes(int32_t m) {
+    const size_t nb = (size_t)((m + kSortTile - 1) / kSortTile);
+    const size_t arr = align_up((size_t)m * 4, 256);
+    return 4 * arr + align_up(nb * kRadix * 4, 256);
+}
+
+cudaError_t launch_sort_rows(const int32_t* ro, int32_t m, int32_t nnz, void* row_idx_out, int it, void* ws,
+                             cudaStream_t s) {
+    if (m == 0) return cudaSuccess;
+    int bits = 0;
+    while (bits < 32 && ((uint64_t)nnz >> bits) != 0) ++bits;  // keys lie in [0, nnz]
+    const int passes = (bits + 7) / 8;
+    if (passes == 0) {
+        if (it == kIdx16) iota_kernel<uint16_t><<<grid_for(m, 256, 4), 256, 0, s>>>((uint16_t*)row_idx_out, m);
+        else iota_kernel<int32_t><<<grid_for(m, 256, 4), 256, 0, s>>>((int32_t*)row_idx_out, m);
+        count_launches(1);
+        return cudaGetLastError();
+    }
+    const int nb = (m + kSortTile - 1) / kSortTile;
+    const size_t arr = align_up((size_t)m * 4, 256);
+    char* w = static_cast<char*>(ws);
+    uint32_t* keys[2] = {reinterpret_cast<uint32_t*>(w), reinterpret_cast<uint32_t*>(w + arr)};
+    int32_t* vals[2] = {reinterpret_cast<int32_t*>(w + 2 * arr), reinterpret_cast<int32_t*>(w + 3 * arr)};
+    uint32_t* hist = reinterpret_cast<uint32_t*>(w + 4 * arr);
+    const uint32_t key_base = (uint32_t)nnz;
+    for (int p = 0; p < passes; ++p) {
+        const uint32_t* kin = p == 0 ? nullptr : keys[(p - 1) & 1];
+        const int32_t* vin = p == 0 ? nullptr : vals[(p - 1) & 1];
+        const bool last = p == passes - 1;
+        radix_hist_kernel<<<nb, kSortThreads, 0, s>>>(ro, kin, m, key_base, 8 * p, hist);
+        radix_scan_kernel<<<1, kScanThreads, 0, s>>>(hist, nb * kRadix);
+        if (!last) {
+            radix_scatter_kernel<int32_t><<<nb, kSortThreads, 0, s>>>(ro, kin, vin, m, key_base, 8 * p, hist,
+                                                                       keys[p & 1], vals[p & 1]);
+        } else if (it == kIdx16) {
+            radix_scatter_kernel<uint16_t><<<nb, kSortThreads, 0, s>>>(ro, kin, vin, m, key_base, 8 * p, hist,
+                                                                        nullptr, (uint16_t*)row_idx_out);
+        } else {
+            radix_scatter_kernel<int32_t><<<nb, kSortThreads, 0, s>>>(ro, kin, vin, m, key_base, 8 * p, hist,
+                                                                       nullptr, (int32_t*)row_idx_out);
+        }
+    }
+    count_launches(3 * passes);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_row_bins(const int32_t* ro, int32_t m, int32_t t_long, int32_t* bins, cudaStream_t s) {
+    row_bins_kernel<<<1, 1024, 0, s>>>(ro, m, t_long, bins);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_check_csr(const int32_t* ro, const void* col, const void* row_idx, int it, int32_t m, int32_t n,
+                             int32_t nnz, uint32_t* perm_bits, int* err, cudaStream_t s) {
+    const int g = grid_for(m > 0 ? m : 1, 256, 8);
+    if (it == kIdx16) check_rows_kernel<uint16_t><<<g, 256, 0, s>>>(ro, (const uint16_t*)col, m, n, nnz, err);
+    else check_rows_kernel<int32_t><<<g, 256, 0, s>>>(ro, (const int32_t*)col, m, n, nnz, err);
+    if (row_idx && perm_bits && m > 0) {
+        const int32_t words = (m + 31) / 32;
+        zero_words_kernel<<<grid_for(words, 256, 4), 256, 0, s>>>(perm_bits, words);
+        if (it == kIdx16) check_perm_kernel<uint16_t><<<g, 256, 0, s>>>((const uint16_t*)row_idx, m, perm_bits, err);
+        else check_perm_kernel<int32_t><<<g, 256, 0, s>>>((const int32_t*)row_idx, m, perm_bits, err);
+        count_launches(2);
+    }
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace spops

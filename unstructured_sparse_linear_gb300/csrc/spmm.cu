@@ -1,0 +1,206 @@
+// SpMM, general path: C = A * B with A an m x k CSR matrix, B dense k x n row-major and C
+// dense m x n row-major, accumulated in fp32 and rounded once to the operand dtype.
+//
+// spops README ("Sparse Operations (spops)"), section "Sparse Matrix Multiplication
+// (SpMM) [dense = sparse x dense]".
+//
+// Row scheduler: rows are visited in row_idx order (nnz descending) and split by the row
+// bins into
+//   * long rows (nnz >= kSpmmLongRow): one CTA per (row, 32*V-column chunk); the 8 warps
+//     take interleaved slices of the row's entries and their partial sums are combined in
+//     shared memory in warp order, so the result does not depend on timing;
+//   * short and empty rows: a group of G lanes per (row, G*V-column chunk), G the smallest
+//     power of two that covers n (at most 32); empty rows write zeros.
+// Each lane owns V = 16 / sizeof(T) consecutive output columns and gathers them from B with
+// one 16-byte load per entry. The group loads G (col, value) pairs at once, coalesced, and
+// broadcasts them with warp shuffles; four B rows are gathered before their FMAs so that
+// four loads are in flight per lane. Correctness does not depend on row_idx being sorted:
+// any row is valid in any bin, sortedness only balances the work.
+#include "common.cuh"
+#include "internal.h"
+
+namespace spops {
+namespace {
+
+constexpr int kSpmmThreads = 256;
+constexpr int kSpmmWarps = kSpmmThreads / 32;
+
+template <typename T, int V>
+__device__ __forceinline__ void load_b(const T* __restrict__ Brow, int col0, int N, float (&b)[V]) {
+    if constexpr (V == 1) {
+        b[0] = col0 < N ? Elt<T>::to_f(Brow[col0]) : 0.f;
+    } else {
+        if (col0 < N) {
+            Elt<T>::unpack(ld_nc_v4(Brow + col0), b);
+        } else {
+#pragma unroll
+            for (int e = 0; e < V; ++e) b[e] = 0.f;
+        }
+    }
+}
+
+// acc += sum over the cnt entries held by lanes src0 .. src0+cnt-1 (col cj, value vj).
+template <typename T, int V>
+__device__ __forceinline__ void accumulate(float (&acc)[V], int cj, float vj, int cnt, const T* __restrict__ B,
+                                           int N, int col0, unsigned mask, int src0) {
+    int j = 0;
+    for (; j + 4 <= cnt; j += 4) {
+        int c[4];
+        float v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            c[u] = __shfl_sync(mask, cj, src0 + j + u);
+            v[u] = __shfl_sync(mask, vj, src0 + j + u);
+        }
+        float b[4][V];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) load_b<T, V>(B + (int64_t)c[u] * N, col0, N, b[u]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int e = 0; e < V; ++e) acc[e] = fmaf(v[u], b[u][e], acc[e]);
+    }
+    for (; j < cnt; ++j) {
+        const int c = __shfl_sync(mask, cj, src0 + j);
+        const float v = __shfl_sync(mask, vj, src0 + j);
+        float b[V];
+        load_b<T, V>(B + (int64_t)c * N, col0, N, b);
+#pragma unroll
+        for (int e = 0; e < V; ++e) acc[e] = fmaf(v, b[e], acc[e]);
+    }
+}
+
+template <typename T, int V>
+__device__ __forceinline__ void store_c(T* __restrict__ Crow, int col0, int N, const float (&acc)[V]) {
+    if (col0 >= N) return;
+    if constexpr (V == 1) {
+        Crow[col0] = Elt<T>::from_f(acc[0]);
+    } else {
+        *reinterpret_cast<uint4*>(Crow + col0) = Elt<T>::pack(acc);
+    }
+}
+
+template <typename T, typename I, int V>
+__global__ void __launch_bounds__(kSpmmThreads)
+spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, const I* __restrict__ row_idx,
+                 const I* __restrict__ col, const T* __restrict__ B, T* __restrict__ C, int32_t m, int32_t N, int G,
+                 const int32_t* __restrict__ bins) {
+    __shared__ float red[kSpmmWarps][32 * V];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int32_t n_long = bins[1];
+
+    // ---- long rows: one CTA per (row, chunk of 32*V columns)
+    {
+        const int chunk = 32 * V;
+        const int nch = (N + chunk - 1) / chunk;
+        const int64_t items = (int64_t)n_long * nch;
+        for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
+            const int32_t p = (int32_t)(item / nch);
+            const int c = (int)(item % nch);
+            const int row = idx_of(row_idx[p]);
+            const int32_t k0 = ro[row], k1 = ro[row + 1];
+            const int col0 = c * chunk + lane * V;
+            float acc[V];
+#pragma unroll
+            for (int e = 0; e < V; ++e) acc[e] = 0.f;
+            for (int32_t kb = k0 + warp * 32; kb < k1; kb += kSpmmThreads) {
+                const int32_t kk = kb + lane;
+                int cj = 0;
+                float vj = 0.f;
+                if (kk < k1) {
+                    cj = idx_of(col[kk]);
+                    vj = Elt<T>::to_f(vals[kk]);
+                }
+                accumulate<T, V>(acc, cj, vj, min(32, k1 - kb), B, N, col0, 0xffffffffu, 0);
+            }
+#pragma unroll
+            for (int e = 0; e < V; ++e) red[warp][lane * V + e] = acc[e];
+            __syncthreads();
+            if (warp == 0) {
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                    float s = red[0][lane * V + e];
+#pragma unroll
+                    for (int w = 1; w < kSpmmWarps; ++w) s += red[w][lane * V + e];
+                    acc[e] = s;
+                }
+                store_c<T, V>(C + (int64_t)row * N, col0, N, acc);
+            }
+            __syncthreads();
+        }
+    }
+
+    // ---- short and empty rows: a group of G lanes per (row, chunk of G*V columns)
+    {
+        const int chunk = G * V;
+        const int nch = (N + chunk - 1) / chunk;
+        const int gpw = 32 / G;
+        const int gw = lane / G, gl = lane % G;
+        const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (gw * G));
+        const int64_t gid = ((int64_t)blockIdx.x * kSpmmWarps + warp) * gpw + gw;
+        const int64_t ngroups = (int64_t)gridDim.x * kSpmmWarps * gpw;
+        const int64_t items = (int64_t)(m - n_long) * nch;
+        for (int64_t item = gid; item < items; item += ngroups) {
+            const int32_t p = n_long + (int32_t)(item / nch);
+            const int c = (int)(item % nch);
+            const int row = idx_of(row_idx[p]);
+            const int32_t k0 = ro[row], k1 = ro[row + 1];
+            const int col0 = c * chunk + gl * V;
+            float acc[V];
+#pragma unroll
+            for (int e = 0; e < V; ++e) acc[e] = 0.f;
+            for (int32_t kb = k0; kb < k1; kb += G) {
+                const int32_t kk = kb + gl;
+                int cj = 0;
+                float vj = 0.f;
+                if (kk < k1) {
+                    cj = idx_of(col[kk]);
+                    vj = Elt<T>::to_f(vals[kk]);
+                }
+                accumulate<T, V>(acc, cj, vj, min(G, k1 - kb), B, N, col0, gmask, gw * G);
+            }
+            store_c<T, V>(C + (int64_t)row * N, col0, N, acc);
+        }
+    }
+}
+
+int pow2_cover(int64_t units) {
+    int g = 1;
+    while (g < 32 && g < units) g <<= 1;
+    return g;
+}
+
+template <typename T, typename I>
+cudaError_t run(const void* vals, const int32_t* ro, const void* row_idx, const void* col, int32_t m,
+                const void* B, int32_t N, void* C, const int32_t* bins, cudaStream_t s) {
+    constexpr int VV = Elt<T>::kVec;
+    const bool vec = ((int64_t)N * sizeof(T)) % 16 == 0 && (uintptr_t)B % 16 == 0 && (uintptr_t)C % 16 == 0;
+    auto kern = vec ? spmm_rows_kernel<T, I, VV> : spmm_rows_kernel<T, I, 1>;
+    const int V = vec ? VV : 1;
+    const int G = pow2_cover(((int64_t)N + V - 1) / V);
+    int occ = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kSpmmThreads, 0);
+    if (e != cudaSuccess) return e;
+    const int grid = device_props().sm_count * (occ > 0 ? occ : 1);
+    kern<<<grid, kSpmmThreads, 0, s>>>(static_cast<const T*>(vals), ro, static_cast<const I*>(row_idx),
+                                       static_cast<const I*>(col), static_cast<const T*>(B), static_cast<T*>(C), m,
+                                       N, G, bins);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_spmm_general(int dt, int it, const void* vals, const int32_t* ro, const void* row_idx,
+                                const void* col, int32_t m, int32_t k, const void* B, int32_t n, void* C,
+                                const int32_t* bins, cudaStream_t s) {
+    (void)k;
+    if (dt == kF32) return it == kIdx16 ? run<float, uint16_t>(vals, ro, row_idx, col, m, B, n, C, bins, s)
+                                        : run<float, int32_t>(vals, ro, row_idx, col, m, B, n, C, bins, s);
+    if (dt == kF16) return it == kIdx16 ? run<__half, uint16_t>(vals, ro, row_idx, col, m, B, n, C, bins, s)
+                                        : run<__half, int32_t>(vals, ro, row_idx, col, m, B, n, C, bins, s);
+    return it == kIdx16 ? run<__nv_bfloat16, uint16_t>(vals, ro, row_idx, col, m, B, n, C, bins, s)
+                        : run<__nv_bfloat16, int32_t>(vals, ro, row_idx, col, m, B, n, C, bins, s);
+}
+
+}  // namespace spops
