@@ -198,7 +198,7 @@ def run_gpu(args):
         outs["row_idx"] = sp.sort_rows(ro, nnz=nnz, index_dtype=idx)
 
     def op_spmm():
-        outs["C"] = sp.spmm(val, ro, outs["row_idx"], col, B, m)
+        outs["C"] = sp.spmm(val, ro, outs["row_idx"], col, B, m, path=args.spmm_path)
 
     def op_sddmm():
         outs["G"] = sp.sddmm(ro, outs["row_idx"], col, A, BT, backend=args.sddmm_backend)
@@ -291,6 +291,7 @@ def run_gpu(args):
         "dtype": "f16", "data": "synthetic (seeded; RoSA-adapter mask recipe)",
         "config": {"workload": "rosa_adapter_4096x4096_fp16_1pct_clustered_2048tok", "m": m, "n": w.n, "nnz": nnz,
                    "N": N, "kd": kd, "index": "int16", "sddmm_backend": args.sddmm_backend,
+                   "spmm_path": args.spmm_path,
                    "l2": "flushed before every step (256 MB write, outside step events)",
                    "parallelism": f"replicas x{ws} (independent adapters per GPU)"},
         "per_op": per_op, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
@@ -319,7 +320,7 @@ def run_e2e(sp, w, dev, idx, args, step_flops, ws):
     def step():
         d = {k: v.to(dev, non_blocking=True) for k, v in host.items()}
         ri = sp.sort_rows(d["ro"], nnz=w.nnz, index_dtype=idx)
-        C = sp.spmm(d["val"], d["ro"], ri, d["col"], d["B"], w.m)
+        C = sp.spmm(d["val"], d["ro"], ri, d["col"], d["B"], w.m, path=args.spmm_path)
         G = sp.sddmm(d["ro"], ri, d["col"], d["A"], d["BT"], backend=args.sddmm_backend)
         D = sp.csr_add(d["val"], d["ro"], ri, d["col"], d["W"])
         res_h["C"].copy_(C, non_blocking=True)
@@ -409,6 +410,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--sddmm-backend", default="structure_aware", choices=["structure_aware", "general"])
+    ap.add_argument("--spmm-path", default="auto", choices=["auto", "general"])
     ap.add_argument("--cpu-steps", type=int, default=3)
     ap.add_argument("--ref-max-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -65,6 +65,10 @@ typedef enum spops_status {
 
 typedef enum spops_dtype { SPOPS_F32 = 0, SPOPS_F16 = 1, SPOPS_BF16 = 2 } spops_dtype;
 typedef enum spops_itype { SPOPS_IDX16 = 0, SPOPS_IDX32 = 1 } spops_itype;
+typedef enum spops_spmm_path {
+    SPOPS_SPMM_AUTO = 0,   /* dense panels (fp16/bf16) on tensor cores, the other rows general */
+    SPOPS_SPMM_GENERAL = 1 /* every row on the general row kernels */
+} spops_spmm_path;
 typedef enum spops_sddmm_backend {
     SPOPS_SDDMM_STRUCTURE_AWARE = 0, /* default: dense panels on tensor cores, the rest general */
     SPOPS_SDDMM_GENERAL = 1          /* any sparsity pattern, CUDA cores */
@@ -123,10 +127,13 @@ SPOPS_API size_t spops_spmm_workspace_size(int32_t m, int32_t k, int32_t n, int3
 /* SpMM (spops README, "Sparse Matrix Multiplication (SpMM)"): C = A * B.
  * A: m x k CSR (A_val [nnz] dtype, row_offsets [m+1], row_idx [m], col_idx [nnz]);
  * B: k x n row-major dtype; C: m x n row-major dtype, every element written (rows without
- * entries become zeros). C must not overlap B or A's arrays. */
-SPOPS_API int spops_spmm(const void* A_val, const int32_t* row_offsets, const void* row_idx, const void* col_idx, int itype,
-               int dtype, int32_t m, int32_t k, int32_t nnz, const void* B, int32_t n, void* C, void* workspace,
-               size_t ws_bytes, void* stream);
+ * entries become zeros). C must not overlap B or A's arrays. path: spops_spmm_path; AUTO
+ * runs panels of 128 row_idx positions whose entries fill at least a quarter of a dense
+ * 128 x |columns| tile on the tensor cores (fp16/bf16, n a multiple of 8, 16-byte aligned
+ * B and C), the rest on the general row kernels. */
+SPOPS_API int spops_spmm(const void* A_val, const int32_t* row_offsets, const void* row_idx, const void* col_idx,
+                         int itype, int dtype, int32_t m, int32_t k, int32_t nnz, const void* B, int32_t n, void* C,
+                         int path, void* workspace, size_t ws_bytes, void* stream);
 
 /* Scratch bytes spops_sddmm needs for the chosen backend. */
 SPOPS_API size_t spops_sddmm_workspace_size(int32_t m, int32_t n, int32_t kd, int32_t nnz, int dtype, int itype, int backend);
@@ -147,6 +154,24 @@ SPOPS_API int spops_sddmm(const int32_t* out_row_offsets, const void* out_row_id
  * for signature parity with the README and may be NULL. */
 SPOPS_API int spops_csr_add(const void* A_val, const int32_t* row_offsets, const void* row_idx, const void* col_idx,
                   int itype, int dtype, int32_t m, int32_t n, int32_t nnz, const void* B, void* C, void* stream);
+
+/* ---------------------------------------------------------------- structure-aware plan */
+
+/* Scratch bytes spops_panel_plan needs. */
+SPOPS_API size_t spops_panel_plan_workspace_size(int32_t m, int32_t nnz);
+
+/* Build the plan the structure-aware paths use (the same one spops_sddmm and spops_spmm
+ * build internally) and report it: stats_out (device int32[4]) = {dense panels, entries in
+ * dense panels, 128-column SDDMM tiles over them, panels}. A panel is 128 consecutive
+ * row_idx positions; it is dense when its columns number at most 1024 and its entries
+ * fill at least a quarter of the 128 x |columns| tile. Mask of an m x n matrix with
+ * n <= 65536 (SPOPS_ERR_UNSUPPORTED otherwise). The spops README ("Sparse Operations
+ * (spops)", section "Sampled Dense-Dense Matrix Multiplication (SDDMM)") motivates the
+ * structure-aware kernel by non-zeros that cluster in few rows and columns; the plan is
+ * this library's reading of that. */
+SPOPS_API int spops_panel_plan(const int32_t* row_offsets, const void* row_idx, const void* col_idx, int itype,
+                               int32_t m, int32_t n, int32_t nnz, int32_t* stats_out, void* workspace, size_t ws_bytes,
+                               void* stream);
 
 /* ---------------------------------------------------------------- checks */
 

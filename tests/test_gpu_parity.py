@@ -23,7 +23,12 @@ SMALL = {
     "zipf_s": wl.spec("zipf", m=4000, n=4000, N=36, mask_kw=(("max_len", 600), ("band", 700))),
     "butterfly_s": wl.spec("butterfly", m=1024, n=256, N=256, kd=136, mask_kw=(("block", 32),)),
     "rosa_i32": wl.spec("rosa", m=700, n=900, N=64, kd=72, mask_kw=(("row_frac", 0.3), ("col_frac", 0.3))),
+    # fully dense 150 x 150 cluster: two dense panels (128 + 22 rows), ragged N and kd
+    "rosa_dense": wl.spec("rosa", m=1500, n=1500, density=0.02, N=264, kd=136),
+    # bf16, int32 indices, long K (split-K over 16 chunks of 64)
+    "rosa_dense_i32": wl.spec("rosa", m=1500, n=1300, density=0.02, dtype="bf16", N=64, kd=1000),
 }
+INT32_CASES = ("rosa_i32", "rosa_dense_i32")
 
 
 @pytest.fixture(scope="module")
@@ -32,9 +37,12 @@ def small_cases():
 
 
 def run_all_ops(w, g, backend="structure_aware"):
+    """backend "structure_aware" also lets SpMM take its dense-panel path; "general" runs
+    both on the general row kernels."""
     out = {}
     if w.B is not None:
-        out["spmm"] = sp.spmm(g["val"], g["ro"], g["row_idx"], g["col"], g["B"], w.m)
+        path = "auto" if backend == "structure_aware" else "general"
+        out["spmm"] = sp.spmm(g["val"], g["ro"], g["row_idx"], g["col"], g["B"], w.m, path=path)
     if w.A is not None:
         out["sddmm"] = sp.sddmm(g["ro"], g["row_idx"], g["col"], g["A"], g["BT"], backend=backend)
     if w.W is not None:
@@ -47,7 +55,7 @@ def run_all_ops(w, g, backend="structure_aware"):
 @pytest.mark.parametrize("backend", ["structure_aware", "general"])
 def test_small_all_elements(small_cases, name, backend):
     w = small_cases[name]
-    idx = torch.int32 if name == "rosa_i32" else None
+    idx = torch.int32 if name in INT32_CASES else None
     g = to_gpu(w, idx_dtype=idx)
     out = run_all_ops(w, g, backend)
     ro, col = w.row_offsets.numpy(), w.col_idx.numpy()
@@ -59,7 +67,7 @@ def test_small_all_elements(small_cases, name, backend):
         assert_bits_equal(out["csr_add"], oracle.csr_add(ro, col, w.values, w.W), w.dtype, f"{name} csr_add")
 
 
-@pytest.mark.parametrize("name", ["tiny", "rosa_s", "llama_s", "butterfly_s"])
+@pytest.mark.parametrize("name", ["tiny", "rosa_s", "llama_s", "butterfly_s", "rosa_dense"])
 def test_integer_valued_inputs_are_exact(name):
     """Small-integer inputs make every product and partial sum exact in fp32, so the GPU
     must equal the oracle bit for bit whatever its summation order."""
@@ -272,3 +280,36 @@ def test_full_size_sampled(name):
         assert_close(gen[torch.from_numpy(sel).cuda()], want, w.dtype, f"{name} sddmm general rows")
     if "csr_add" in out:
         assert_bits_equal(out["csr_add"], oracle.csr_add(ro, col, w.values, w.W), w.dtype, f"{name} csr_add")
+
+
+# ------------------------------------------------------------------ structure-aware plan
+
+
+def expected_plan(ro, col, row_idx, n):
+    """The panel rule restated on the host: 128 consecutive row_idx positions per panel;
+    dense when |columns| <= 1024 and entries * 4 >= 128 * |columns|."""
+    m = len(ro) - 1
+    dense = entries = tiles = 0
+    P = (m + 127) // 128
+    for p in range(P):
+        rows = row_idx[p * 128:(p + 1) * 128]
+        cols = [col[ro[i]:ro[i + 1]] for i in rows]
+        nnz_p = sum(len(c) for c in cols)
+        U = len(np.unique(np.concatenate(cols))) if nnz_p else 0
+        if nnz_p > 0 and U <= 1024 and nnz_p * 4 >= 128 * U:
+            dense += 1
+            entries += nnz_p
+            tiles += (U + 127) // 128
+    return {"dense_panels": dense, "dense_entries": entries, "sddmm_tiles": tiles, "panels": P}
+
+
+@pytest.mark.parametrize("name", ["rosa_s", "llama_s", "butterfly_s", "rosa_dense", "rosa_dense_i32"])
+def test_panel_plan_matches_rule(small_cases, name):
+    w = small_cases[name]
+    g = to_gpu(w, idx_dtype=torch.int32 if name in INT32_CASES else None)
+    got = sp.panel_plan(g["ro"], g["row_idx"], g["col"], w.n)
+    ro, col = w.row_offsets.numpy(), w.col_idx.numpy()
+    want = expected_plan(ro, col, oracle.sort_rows(ro), w.n)
+    assert got == want
+    if name in ("rosa_s", "butterfly_s", "rosa_dense", "rosa_dense_i32"):
+        assert got["dense_panels"] >= 1  # these cases exercise the tensor-core path

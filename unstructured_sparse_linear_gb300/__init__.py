@@ -22,7 +22,7 @@ import torch
 
 from . import _lib
 
-__all__ = ["spmm", "sddmm", "csr_add", "sort_rows", "row_bins", "check_csr", "SpopsError", "library_path",
+__all__ = ["spmm", "sddmm", "csr_add", "sort_rows", "row_bins", "check_csr", "panel_plan", "SpopsError", "library_path",
            "SPMM_LONG_ROW", "SDDMM_LONG_ROW"]
 
 SPMM_LONG_ROW = 256
@@ -31,6 +31,7 @@ SDDMM_LONG_ROW = 64
 _DTYPE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 _ITYPE = {torch.int16: 0, torch.int32: 1}
 _BACKEND = {"structure_aware": 0, "general": 1, "sputnik": 1}
+_SPMM_PATH = {"auto": 0, "general": 1}
 _ERR_CLASS = {1: ValueError, 2: ValueError, 3: ValueError}
 
 
@@ -116,8 +117,13 @@ def row_bins(row_offsets: torch.Tensor, t_long: int) -> torch.Tensor:
     return out
 
 
-def spmm(A_val, A_row_offsets, A_row_indices, A_col_indices, B, m: int, out: torch.Tensor | None = None):
-    """C = A @ B for a CSR matrix A (m rows) and a dense row-major B."""
+def spmm(A_val, A_row_offsets, A_row_indices, A_col_indices, B, m: int, out: torch.Tensor | None = None,
+         path: str = "auto"):
+    """C = A @ B for a CSR matrix A (m rows) and a dense row-major B.
+    path="auto" runs dense row panels on the tensor cores, "general" every row on the
+    general row kernels."""
+    if path not in _SPMM_PATH:
+        raise ValueError(f"path must be one of {list(_SPMM_PATH)}")
     _req(B, "B", dtypes=_DTYPE)
     dev = B.device
     _req(A_val, "A_val", B.dtype, device=dev)
@@ -141,7 +147,7 @@ def spmm(A_val, A_row_offsets, A_row_indices, A_col_indices, B, m: int, out: tor
     with torch.cuda.device(dev):
         ws = _ws(lib.spops_spmm_workspace_size(m, k, n, nnz, dt, it), dev)
         _check(lib.spops_spmm(_p(A_val), _p(A_row_offsets), _p(A_row_indices), _p(A_col_indices), it, dt, m, k, nnz,
-                              _p(B), n, _p(C), _p(ws), ws.numel(), _stream()), "spmm")
+                              _p(B), n, _p(C), _SPMM_PATH[path], _p(ws), ws.numel(), _stream()), "spmm")
     return C
 
 
@@ -197,6 +203,24 @@ def csr_add(A_val, A_row_offsets, A_row_indices, A_col_indices, B, out: torch.Te
         _check(_L().spops_csr_add(_p(A_val), _p(A_row_offsets), _p(A_row_indices), _p(A_col_indices), it,
                                   _DTYPE[B.dtype], m, n, nnz, _p(B), _p(C), _stream()), "csr_add")
     return C
+
+
+def panel_plan(row_offsets, row_idx, col_idx, n: int) -> dict:
+    """Build the structure-aware plan for a mask and return its summary (synchronizes):
+    dense panels, entries in dense panels, SDDMM tiles and panels."""
+    _req(row_offsets, "row_offsets", torch.int32)
+    dev = row_offsets.device
+    m = row_offsets.numel() - 1
+    it = _itype(col_idx, row_idx)
+    nnz = col_idx.numel()
+    stats = torch.zeros(4, dtype=torch.int32, device=dev)
+    lib = _L()
+    with torch.cuda.device(dev):
+        ws = _ws(lib.spops_panel_plan_workspace_size(m, nnz), dev)
+        _check(lib.spops_panel_plan(_p(row_offsets), _p(row_idx), _p(col_idx), it, m, int(n), nnz, _p(stats), _p(ws),
+                                    ws.numel(), _stream()), "panel_plan")
+    s = stats.cpu().tolist()
+    return {"dense_panels": s[0], "dense_entries": s[1], "sddmm_tiles": s[2], "panels": s[3]}
 
 
 def check_csr(row_offsets, col_idx, row_idx, n: int) -> None:

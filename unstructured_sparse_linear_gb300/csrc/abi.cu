@@ -173,10 +173,12 @@ size_t spops_spmm_workspace_size(int32_t m, int32_t k, int32_t n, int32_t nnz, i
 }
 
 int spops_spmm(const void* A_val, const int32_t* row_offsets, const void* row_idx, const void* col_idx, int itype,
-               int dtype, int32_t m, int32_t k, int32_t nnz, const void* B, int32_t n, void* C, void* workspace,
-               size_t ws_bytes, void* stream) {
+               int dtype, int32_t m, int32_t k, int32_t nnz, const void* B, int32_t n, void* C, int path,
+               void* workspace, size_t ws_bytes, void* stream) {
     int st = check_common(itype, dtype, m, k, nnz, A_val, row_offsets, row_idx, col_idx, true, true);
     if (st != SPOPS_OK) return st;
+    if (path != SPOPS_SPMM_AUTO && path != SPOPS_SPMM_GENERAL)
+        return fail(SPOPS_ERR_INVALID_ARG, "path %d is not a spops_spmm_path", path);
     if (n < 0) return fail(SPOPS_ERR_INVALID_ARG, "negative n=%d", n);
     if ((int64_t)m * n == 0) return ok();
     const size_t ds = dtype_size(dtype);
@@ -191,7 +193,7 @@ int spops_spmm(const void* A_val, const int32_t* row_offsets, const void* row_id
     cudaError_t e = launch_row_bins(row_offsets, m, kSpmmLongRow, bins, s);
     if (e != cudaSuccess) return cuda_status(e, "row_bins launch");
     e = launch_spmm(dtype, itype, A_val, row_offsets, row_idx, col_idx, m, k, nnz, B, n, C, bins,
-                    static_cast<char*>(workspace) + kBinsBytes, s);
+                    static_cast<char*>(workspace) + kBinsBytes, path == SPOPS_SPMM_AUTO, s);
     return cuda_status(e, "spmm launch");
 }
 
@@ -236,6 +238,25 @@ int spops_csr_add(const void* A_val, const int32_t* row_offsets, const void* row
     if (B != C && overlaps(B, bytes, C, bytes)) return fail(SPOPS_ERR_INVALID_ARG, "C partially overlaps B");
     return cuda_status(launch_csr_add(dtype, itype, A_val, row_offsets, col_idx, m, n, nnz, B, C, (cudaStream_t)stream),
                        "csr_add launch");
+}
+
+size_t spops_panel_plan_workspace_size(int32_t m, int32_t nnz) {
+    return (m > 0 && nnz >= 0) ? panel_plan_workspace_bytes(m, nnz) : 16;
+}
+
+int spops_panel_plan(const int32_t* row_offsets, const void* row_idx, const void* col_idx, int itype, int32_t m,
+                     int32_t n, int32_t nnz, int32_t* stats_out, void* workspace, size_t ws_bytes, void* stream) {
+    int st = check_common(itype, SPOPS_F16, m, n, nnz, nullptr, row_offsets, row_idx, col_idx, false, true);
+    if (st != SPOPS_OK) return st;
+    if (!stats_out || !aligned(stats_out, 4)) return fail(SPOPS_ERR_INVALID_ARG, "stats_out is NULL or misaligned");
+    if (n > 65536) return fail(SPOPS_ERR_UNSUPPORTED, "panel plans need n <= 65536 (n=%d)", n);
+    if (m == 0) return fail(SPOPS_ERR_INVALID_ARG, "panel plans need m >= 1");
+    const size_t need = spops_panel_plan_workspace_size(m, nnz);
+    if (!workspace || !aligned(workspace, 16) || ws_bytes < need)
+        return fail(SPOPS_ERR_WORKSPACE, "panel_plan needs a workspace of %zu bytes (got %zu)", need, ws_bytes);
+    return cuda_status(launch_panel_plan(itype, row_offsets, row_idx, col_idx, m, n, nnz, stats_out, workspace,
+                                         (cudaStream_t)stream),
+                       "panel_plan launch");
 }
 
 size_t spops_check_csr_workspace_size(int32_t m) { return align_up(((size_t)(m > 0 ? m : 0) + 31) / 32 * 4, 256) + 16; }

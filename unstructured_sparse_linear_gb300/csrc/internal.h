@@ -27,7 +27,7 @@ void count_launches(int n);
 
 inline size_t dtype_size(int dt) { return dt == kF32 ? 4 : 2; }
 inline size_t itype_size(int it) { return it == kIdx16 ? 2 : 4; }
-inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Row-bin thresholds used by the operators (rows with nnz >= threshold are "long").
 constexpr int32_t kSpmmLongRow = 256;
@@ -48,11 +48,15 @@ cudaError_t launch_check_csr(const int32_t* ro, const void* col, const void* row
 // spmm.cu
 cudaError_t launch_spmm_general(int dt, int it, const void* vals, const int32_t* ro, const void* row_idx,
                                 const void* col, int32_t m, int32_t k, const void* B, int32_t n, void* C,
-                                const int32_t* bins, cudaStream_t s);
+                                const int32_t* bins, const uint8_t* skip_panels, cudaStream_t s);
 
 // sddmm.cu
 cudaError_t launch_sddmm_general(int dt, int it, const int32_t* ro, const void* row_idx, const void* col, int32_t m,
                                  int32_t n, int32_t kd, const void* A, const void* BT, void* out,
-                                 const int32_t* bins, cudaStream_t s);
+                                 const int32_t* bins, const uint8_t* skip_panels, cudaStream_t s);
+
+// Rows are grouped in panels of kPanelRows consecutive row_idx positions; the general
+// kernels skip positions whose panel flag in skip_panels is set (handled on tensor cores).
+constexpr int kPanelRows = 128;
 
 }  // namespace spops

@@ -9,7 +9,8 @@
 // Row scheduler: rows in row_idx order, split by the row bins into
 //   * long rows (nnz >= kSddmmLongRow): one CTA per row, its 8 warps take interleaved
 //     batches of entries, so all of them stream the same A row through L1;
-//   * short rows: a group of G lanes per row (G covers kd in 16-byte vectors, at most 32).
+//   * short rows: a group of G lanes per row (G covers kd in 16-byte vectors, at most 32);
+//     empty rows cost one row_offsets read.
 // A batch holds NB entries: the group walks kd once, loading each A vector once and the NB
 // BT vectors beside it, keeps NB per-lane partial dot products and finishes them with an
 // xor-shuffle butterfly inside the group. Empty rows are skipped.
@@ -73,12 +74,15 @@ template <typename T, typename I, int V>
 __global__ void __launch_bounds__(kSddmmThreads)
 sddmm_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx, const I* __restrict__ col,
                   const T* __restrict__ A, const T* __restrict__ BT, T* __restrict__ out, int32_t kd, int G,
-                  const int32_t* __restrict__ bins) {
+                  const int32_t* __restrict__ bins, const uint8_t* __restrict__ skip) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int32_t n_long = bins[1], n_nonempty = bins[2];
+    // Short rows run over every position up to m, not only up to bins[2]: with an unsorted
+    // row_idx, rows with entries may sit past the count of non-empty rows.
+    const int32_t n_long = bins[1], n_rows = bins[3];
 
     // ---- long rows: a CTA per row
     for (int32_t p = blockIdx.x; p < n_long; p += gridDim.x) {
+        if (skip && skip[p / kPanelRows]) continue;
         const int row = idx_of(row_idx[p]);
         const int32_t k0 = ro[row], k1 = ro[row + 1];
         for (int32_t kb = k0 + warp * kNB; kb < k1; kb += kSddmmWarps * kNB)
@@ -91,7 +95,8 @@ sddmm_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx,
     const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (gw * G));
     const int64_t gid = ((int64_t)blockIdx.x * kSddmmWarps + warp) * gpw + gw;
     const int64_t ngroups = (int64_t)gridDim.x * kSddmmWarps * gpw;
-    for (int64_t p = n_long + gid; p < n_nonempty; p += ngroups) {
+    for (int64_t p = n_long + gid; p < n_rows; p += ngroups) {
+        if (skip && skip[p / kPanelRows]) continue;
         const int row = idx_of(row_idx[p]);
         const int32_t k0 = ro[row], k1 = ro[row + 1];
         for (int32_t kb = k0; kb < k1; kb += kNB)
@@ -101,7 +106,7 @@ sddmm_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx,
 
 template <typename T, typename I>
 cudaError_t run(const int32_t* ro, const void* row_idx, const void* col, int32_t kd, const void* A, const void* BT,
-                void* out, const int32_t* bins, cudaStream_t s) {
+                void* out, const int32_t* bins, const uint8_t* skip, cudaStream_t s) {
     constexpr int VV = Elt<T>::kVec;
     const bool vec = ((int64_t)kd * sizeof(T)) % 16 == 0 && (uintptr_t)A % 16 == 0 && (uintptr_t)BT % 16 == 0;
     auto kern = vec ? sddmm_rows_kernel<T, I, VV> : sddmm_rows_kernel<T, I, 1>;
@@ -114,7 +119,7 @@ cudaError_t run(const int32_t* ro, const void* row_idx, const void* col, int32_t
     const int grid = device_props().sm_count * (occ > 0 ? occ : 1);
     kern<<<grid, kSddmmThreads, 0, s>>>(ro, static_cast<const I*>(row_idx), static_cast<const I*>(col),
                                         static_cast<const T*>(A), static_cast<const T*>(BT), static_cast<T*>(out),
-                                        kd, G, bins);
+                                        kd, G, bins, skip);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -123,15 +128,15 @@ cudaError_t run(const int32_t* ro, const void* row_idx, const void* col, int32_t
 
 cudaError_t launch_sddmm_general(int dt, int it, const int32_t* ro, const void* row_idx, const void* col, int32_t m,
                                  int32_t n, int32_t kd, const void* A, const void* BT, void* out,
-                                 const int32_t* bins, cudaStream_t s) {
+                                 const int32_t* bins, const uint8_t* skip, cudaStream_t s) {
     (void)m;
     (void)n;
-    if (dt == kF32) return it == kIdx16 ? run<float, uint16_t>(ro, row_idx, col, kd, A, BT, out, bins, s)
-                                        : run<float, int32_t>(ro, row_idx, col, kd, A, BT, out, bins, s);
-    if (dt == kF16) return it == kIdx16 ? run<__half, uint16_t>(ro, row_idx, col, kd, A, BT, out, bins, s)
-                                        : run<__half, int32_t>(ro, row_idx, col, kd, A, BT, out, bins, s);
-    return it == kIdx16 ? run<__nv_bfloat16, uint16_t>(ro, row_idx, col, kd, A, BT, out, bins, s)
-                        : run<__nv_bfloat16, int32_t>(ro, row_idx, col, kd, A, BT, out, bins, s);
+    if (dt == kF32) return it == kIdx16 ? run<float, uint16_t>(ro, row_idx, col, kd, A, BT, out, bins, skip, s)
+                                        : run<float, int32_t>(ro, row_idx, col, kd, A, BT, out, bins, skip, s);
+    if (dt == kF16) return it == kIdx16 ? run<__half, uint16_t>(ro, row_idx, col, kd, A, BT, out, bins, skip, s)
+                                        : run<__half, int32_t>(ro, row_idx, col, kd, A, BT, out, bins, skip, s);
+    return it == kIdx16 ? run<__nv_bfloat16, uint16_t>(ro, row_idx, col, kd, A, BT, out, bins, skip, s)
+                        : run<__nv_bfloat16, int32_t>(ro, row_idx, col, kd, A, BT, out, bins, skip, s);
 }
 
 }  // namespace spops

@@ -84,7 +84,7 @@ template <typename T, typename I, int V>
 __global__ void __launch_bounds__(kSpmmThreads)
 spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, const I* __restrict__ row_idx,
                  const I* __restrict__ col, const T* __restrict__ B, T* __restrict__ C, int32_t m, int32_t N, int G,
-                 const int32_t* __restrict__ bins) {
+                 const int32_t* __restrict__ bins, const uint8_t* __restrict__ skip) {
     __shared__ float red[kSpmmWarps][32 * V];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int32_t n_long = bins[1];
@@ -96,6 +96,7 @@ spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, con
         const int64_t items = (int64_t)n_long * nch;
         for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
             const int32_t p = (int32_t)(item / nch);
+            if (skip && skip[p / kPanelRows]) continue;  // uniform across the CTA
             const int c = (int)(item % nch);
             const int row = idx_of(row_idx[p]);
             const int32_t k0 = ro[row], k1 = ro[row + 1];
@@ -142,6 +143,7 @@ spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, con
         const int64_t items = (int64_t)(m - n_long) * nch;
         for (int64_t item = gid; item < items; item += ngroups) {
             const int32_t p = n_long + (int32_t)(item / nch);
+            if (skip && skip[p / kPanelRows]) continue;  // uniform across the group
             const int c = (int)(item % nch);
             const int row = idx_of(row_idx[p]);
             const int32_t k0 = ro[row], k1 = ro[row + 1];
@@ -172,7 +174,7 @@ int pow2_cover(int64_t units) {
 
 template <typename T, typename I>
 cudaError_t run(const void* vals, const int32_t* ro, const void* row_idx, const void* col, int32_t m,
-                const void* B, int32_t N, void* C, const int32_t* bins, cudaStream_t s) {
+                const void* B, int32_t N, void* C, const int32_t* bins, const uint8_t* skip, cudaStream_t s) {
     constexpr int VV = Elt<T>::kVec;
     const bool vec = ((int64_t)N * sizeof(T)) % 16 == 0 && (uintptr_t)B % 16 == 0 && (uintptr_t)C % 16 == 0;
     auto kern = vec ? spmm_rows_kernel<T, I, VV> : spmm_rows_kernel<T, I, 1>;
@@ -184,7 +186,7 @@ cudaError_t run(const void* vals, const int32_t* ro, const void* row_idx, const 
     const int grid = device_props().sm_count * (occ > 0 ? occ : 1);
     kern<<<grid, kSpmmThreads, 0, s>>>(static_cast<const T*>(vals), ro, static_cast<const I*>(row_idx),
                                        static_cast<const I*>(col), static_cast<const T*>(B), static_cast<T*>(C), m,
-                                       N, G, bins);
+                                       N, G, bins, skip);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -193,14 +195,14 @@ cudaError_t run(const void* vals, const int32_t* ro, const void* row_idx, const 
 
 cudaError_t launch_spmm_general(int dt, int it, const void* vals, const int32_t* ro, const void* row_idx,
                                 const void* col, int32_t m, int32_t k, const void* B, int32_t n, void* C,
-                                const int32_t* bins, cudaStream_t s) {
+                                const int32_t* bins, const uint8_t* skip, cudaStream_t s) {
     (void)k;
-    if (dt == kF32) return it == kIdx16 ? run<float, uint16_t>(vals, ro, row_idx, col, m, B, n, C, bins, s)
-                                        : run<float, int32_t>(vals, ro, row_idx, col, m, B, n, C, bins, s);
-    if (dt == kF16) return it == kIdx16 ? run<__half, uint16_t>(vals, ro, row_idx, col, m, B, n, C, bins, s)
-                                        : run<__half, int32_t>(vals, ro, row_idx, col, m, B, n, C, bins, s);
-    return it == kIdx16 ? run<__nv_bfloat16, uint16_t>(vals, ro, row_idx, col, m, B, n, C, bins, s)
-                        : run<__nv_bfloat16, int32_t>(vals, ro, row_idx, col, m, B, n, C, bins, s);
+    if (dt == kF32) return it == kIdx16 ? run<float, uint16_t>(vals, ro, row_idx, col, m, B, n, C, bins, skip, s)
+                                        : run<float, int32_t>(vals, ro, row_idx, col, m, B, n, C, bins, skip, s);
+    if (dt == kF16) return it == kIdx16 ? run<__half, uint16_t>(vals, ro, row_idx, col, m, B, n, C, bins, skip, s)
+                                        : run<__half, int32_t>(vals, ro, row_idx, col, m, B, n, C, bins, skip, s);
+    return it == kIdx16 ? run<__nv_bfloat16, uint16_t>(vals, ro, row_idx, col, m, B, n, C, bins, skip, s)
+                        : run<__nv_bfloat16, int32_t>(vals, ro, row_idx, col, m, B, n, C, bins, skip, s);
 }
 
 }  // namespace spops
