@@ -114,6 +114,22 @@ SPOPS_API size_t spops_sort_rows_workspace_size(int32_t m);
 SPOPS_API int spops_sort_rows(const int32_t* row_offsets, int32_t m, int32_t nnz, void* row_idx_out, int itype,
                     void* workspace, size_t ws_bytes, void* stream);
 
+/* spops_sort_rows without a workspace, for callers that cannot allocate device memory
+ * where they need row_idx (a plugin whose host application owns every device allocation,
+ * or a loop that must not call cudaMalloc because it can synchronize the device). The
+ * pages have no counterpart of this call; it exists for such callers only.
+ * Same arguments and result as spops_sort_rows minus the workspace: the scratch is a
+ * static device array inside this library that holds at most
+ * spops_sort_rows_static_max_rows() rows (131072; about 2.1 MB reserved on every GPU that
+ * loads the library, until the process exits). Larger m returns SPOPS_ERR_UNSUPPORTED.
+ * The call allocates nothing. Its first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first call before any
+ * stream capture. All calls on a device share the array, so calls whose GPU work overlaps
+ * (e.g. on unordered streams) race and must be serialized by the caller. */
+SPOPS_API int spops_sort_rows_static(const int32_t* row_offsets, int32_t m, int32_t nnz, void* row_idx_out,
+                                     int itype, void* stream);
+SPOPS_API int32_t spops_sort_rows_static_max_rows(void);
+
 /* bins_out[0..4) (device int32) = {0, #rows with nnz >= t_long, #rows with nnz >= 1, m}:
  * prefix offsets that split a sorted row_idx into long, short and empty rows. The counts
  * do not depend on row_idx, so the call takes only row_offsets. t_long >= 1. */

@@ -23,6 +23,8 @@ SIGNATURES = {
     "spops_kernel_launches": (ctypes.c_uint64, []),
     "spops_sort_rows_workspace_size": (_SZ, [_I32]),
     "spops_sort_rows": (_INT, [_P, _I32, _I32, _P, _INT, _P, _SZ, _P]),
+    "spops_sort_rows_static": (_INT, [_P, _I32, _I32, _P, _INT, _P]),
+    "spops_sort_rows_static_max_rows": (_I32, []),
     "spops_row_bins": (_INT, [_P, _I32, _I32, _P, _P]),
     "spops_spmm_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _INT, _INT]),
     "spops_spmm": (_INT, [_P, _P, _P, _P, _INT, _INT, _I32, _I32, _I32, _P, _I32, _P, _INT, _P, _SZ, _P]),

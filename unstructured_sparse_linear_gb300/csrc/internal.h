@@ -24,6 +24,8 @@ const DeviceProps& device_props();
 int* device_error_word();
 // Add n to the process-wide count of kernels this library has launched.
 void count_launches(int n);
+// Record the calling thread's spops_last_error() text (printf format) and return status.
+int set_last_error(int status, const char* fmt, ...);
 
 inline size_t dtype_size(int dt) { return dt == kF32 ? 4 : 2; }
 inline size_t itype_size(int it) { return it == kIdx16 ? 2 : 4; }
