@@ -80,6 +80,7 @@ def accounting(w):
     if w.W is not None:
         acc["csr_add"] = {"flops": nnz, "bytes": csr_bytes - ib * m + 2 * m * n * b}
     acc["sort_rows"] = {"flops": 0, "bytes": 4 * (m + 1) + ib * m}
+    acc["plan"] = {"flops": 0, "bytes": 4 * (m + 1) + ib * m + nnz * ib + nnz * 2}
     return acc
 
 
@@ -197,16 +198,19 @@ def run_gpu(args):
     def op_sort():
         outs["row_idx"] = sp.sort_rows(ro, nnz=nnz, index_dtype=idx)
 
+    def op_plan():
+        outs["plan"] = sp.plan_build(ro, outs["row_idx"], col, w.n)
+
     def op_spmm():
-        outs["C"] = sp.spmm(val, ro, outs["row_idx"], col, B, m, path=args.spmm_path)
+        outs["C"] = sp.spmm(val, ro, outs["row_idx"], col, B, m, path=args.spmm_path, plan=outs["plan"])
 
     def op_sddmm():
-        outs["G"] = sp.sddmm(ro, outs["row_idx"], col, A, BT, backend=args.sddmm_backend)
+        outs["G"] = sp.sddmm(ro, outs["row_idx"], col, A, BT, backend=args.sddmm_backend, plan=outs["plan"])
 
     def op_add():
         outs["D"] = sp.csr_add(val, ro, outs["row_idx"], col, W)
 
-    ops = [("sort_rows", op_sort), ("spmm", op_spmm), ("sddmm", op_sddmm), ("csr_add", op_add)]
+    ops = [("sort_rows", op_sort), ("plan", op_plan), ("spmm", op_spmm), ("sddmm", op_sddmm), ("csr_add", op_add)]
 
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
@@ -272,7 +276,7 @@ def run_gpu(args):
                         "GFLOP/s": round(a["flops"] / (t_avg * 1e-3) / 1e9, 2) if a["flops"] else None,
                         "GB/s": round(a["bytes"] / (t_avg * 1e-3) / 1e9, 1),
                         "hbm_frac": round(a["bytes"] / (t_avg * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}
-    dominant = max((k for k in per_op if k != "sort_rows"), key=lambda k: per_op[k]["ms"])
+    dominant = max((k for k in per_op if k not in ("sort_rows", "plan")), key=lambda k: per_op[k]["ms"])
     dom_t = per_op[dominant]["ms"] * 1e-3
     achieved = acc[dominant]["bytes"] / dom_t / 1e9
     roofline = {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
@@ -320,8 +324,9 @@ def run_e2e(sp, w, dev, idx, args, step_flops, ws):
     def step():
         d = {k: v.to(dev, non_blocking=True) for k, v in host.items()}
         ri = sp.sort_rows(d["ro"], nnz=w.nnz, index_dtype=idx)
-        C = sp.spmm(d["val"], d["ro"], ri, d["col"], d["B"], w.m, path=args.spmm_path)
-        G = sp.sddmm(d["ro"], ri, d["col"], d["A"], d["BT"], backend=args.sddmm_backend)
+        plan = sp.plan_build(d["ro"], ri, d["col"], w.n)
+        C = sp.spmm(d["val"], d["ro"], ri, d["col"], d["B"], w.m, path=args.spmm_path, plan=plan)
+        G = sp.sddmm(d["ro"], ri, d["col"], d["A"], d["BT"], backend=args.sddmm_backend, plan=plan)
         D = sp.csr_add(d["val"], d["ro"], ri, d["col"], d["W"])
         res_h["C"].copy_(C, non_blocking=True)
         res_h["G"].copy_(G, non_blocking=True)

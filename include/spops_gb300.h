@@ -135,59 +135,73 @@ SPOPS_API int32_t spops_sort_rows_static_max_rows(void);
  * do not depend on row_idx, so the call takes only row_offsets. t_long >= 1. */
 SPOPS_API int spops_row_bins(const int32_t* row_offsets, int32_t m, int32_t t_long, int32_t* bins_out, void* stream);
 
+/* ---------------------------------------------------------------- mask plan */
+
+/* Bytes of a mask plan for an m x n mask with nnz entries (callers allocate it 1024-byte
+ * aligned). */
+SPOPS_API size_t spops_plan_size(int32_t m, int32_t n, int32_t nnz);
+
+/* Build the mask plan: everything the operators derive from the CSR structure alone, so a
+ * plan built once serves every spmm / sddmm call on the same mask (same row_offsets,
+ * row_idx, col_idx, m, n, nnz), like row_idx itself. It holds
+ *   - the row bins of each operator (spops README, "Usage": row_idx sorts the rows by
+ *     nnz; long rows get a CTA each, short rows a group of lanes), and, when n <= 65536,
+ *   - the panel decomposition behind the structure-aware paths (README, "Sampled
+ *     Dense-Dense Matrix Multiplication": the structure-aware kernel exploits non-zeros
+ *     that cluster in a few rows and columns): panels of 128 consecutive row_idx
+ *     positions; a panel is dense when the union U of its columns has at most 1024
+ *     columns, it has at least 16 non-empty rows, and its entries fill at least a quarter
+ *     of (non-empty rows) x |U|. Dense panels run on the tensor cores.
+ * plan: device buffer of spops_plan_size bytes, 1024-byte aligned, owned by the caller and
+ * left unchanged by the operators. Deterministic: the same mask gives the same plan. */
+SPOPS_API int spops_plan_build(const int32_t* row_offsets, const void* row_idx, const void* col_idx, int itype,
+                               int32_t m, int32_t n, int32_t nnz, void* plan, size_t plan_size, void* stream);
+
+/* stats_out (device int32[16]) = {dense panels, SDDMM tiles, panels with a SpMM image,
+ * entries in dense panels, SpMM image elements, panels, 0, 0, SpMM row bins [4], SDDMM
+ * row bins [4]} of a built plan. */
+SPOPS_API int spops_plan_stats(const void* plan, int32_t m, int32_t n, int32_t nnz, int32_t* stats_out, void* stream);
+
 /* ---------------------------------------------------------------- operators */
 
-/* Scratch bytes spops_spmm needs (row bins and, for dense panels, the panel plan). */
+/* Scratch bytes spops_spmm needs (enough to build its own plan and the dense-panel images). */
 SPOPS_API size_t spops_spmm_workspace_size(int32_t m, int32_t k, int32_t n, int32_t nnz, int dtype, int itype);
 
 /* SpMM (spops README, "Sparse Matrix Multiplication (SpMM)"): C = A * B.
  * A: m x k CSR (A_val [nnz] dtype, row_offsets [m+1], row_idx [m], col_idx [nnz]);
  * B: k x n row-major dtype; C: m x n row-major dtype, every element written (rows without
  * entries become zeros). C must not overlap B or A's arrays. path: spops_spmm_path; AUTO
- * runs panels of 128 row_idx positions whose entries fill at least a quarter of a dense
- * 128 x |columns| tile on the tensor cores (fp16/bf16, n a multiple of 8, 16-byte aligned
- * B and C), the rest on the general row kernels. */
+ * runs the plan's dense panels on the tensor cores (fp16/bf16, n a multiple of 8, 16-byte
+ * aligned B and C), the other rows on the general row kernels. plan: a plan built by
+ * spops_plan_build for this mask (m x k), or NULL to build one inside the workspace. */
 SPOPS_API int spops_spmm(const void* A_val, const int32_t* row_offsets, const void* row_idx, const void* col_idx,
                          int itype, int dtype, int32_t m, int32_t k, int32_t nnz, const void* B, int32_t n, void* C,
-                         int path, void* workspace, size_t ws_bytes, void* stream);
+                         int path, const void* plan, void* workspace, size_t ws_bytes, void* stream);
 
-/* Scratch bytes spops_sddmm needs for the chosen backend. */
-SPOPS_API size_t spops_sddmm_workspace_size(int32_t m, int32_t n, int32_t kd, int32_t nnz, int dtype, int itype, int backend);
+/* Scratch bytes spops_sddmm needs for the chosen backend (including its own plan). */
+SPOPS_API size_t spops_sddmm_workspace_size(int32_t m, int32_t n, int32_t kd, int32_t nnz, int dtype, int itype,
+                                            int backend);
 
 /* SDDMM (spops README, "Sampled Dense-Dense Matrix Multiplication (SDDMM)"):
  * out_val[k] = sum_t A[i, t] * BT[col_idx[k], t] for every entry k of row i of the m x n
  * mask (out_row_offsets [m+1], out_row_idx [m], out_col_idx [nnz]).
  * A: m x kd row-major; BT: n x kd row-major (the right operand transposed);
- * out_val: [nnz] dtype, in CSR order. backend: spops_sddmm_backend. No scaling by mask
- * values (the call takes none). */
-SPOPS_API int spops_sddmm(const int32_t* out_row_offsets, const void* out_row_idx, const void* out_col_idx, int itype,
-                int dtype, int32_t m, int32_t n, int32_t kd, int32_t nnz, const void* A, const void* BT,
-                void* out_val, int backend, void* workspace, size_t ws_bytes, void* stream);
+ * out_val: [nnz] dtype, in CSR order. backend: spops_sddmm_backend (STRUCTURE_AWARE runs
+ * the plan's dense panels on the tensor cores for fp16/bf16 with kd a multiple of 8 and
+ * 16-byte aligned A and BT). No scaling by mask values (the call takes none). plan: as for
+ * spops_spmm (an m x n plan), or NULL. */
+SPOPS_API int spops_sddmm(const int32_t* out_row_offsets, const void* out_row_idx, const void* out_col_idx,
+                          int itype, int dtype, int32_t m, int32_t n, int32_t kd, int32_t nnz, const void* A,
+                          const void* BT, void* out_val, int backend, const void* plan, void* workspace,
+                          size_t ws_bytes, void* stream);
 
 /* csr_add (spops README, "Sparse Addition"): C = B + A with A an m x n CSR matrix and B, C
  * dense m x n row-major. C == B (in place) is allowed; partial overlap is not. Each entry
  * is the correctly rounded sum of the two dtype values (bit-exact). row_idx is accepted
  * for signature parity with the README and may be NULL. */
 SPOPS_API int spops_csr_add(const void* A_val, const int32_t* row_offsets, const void* row_idx, const void* col_idx,
-                  int itype, int dtype, int32_t m, int32_t n, int32_t nnz, const void* B, void* C, void* stream);
-
-/* ---------------------------------------------------------------- structure-aware plan */
-
-/* Scratch bytes spops_panel_plan needs. */
-SPOPS_API size_t spops_panel_plan_workspace_size(int32_t m, int32_t nnz);
-
-/* Build the plan the structure-aware paths use (the same one spops_sddmm and spops_spmm
- * build internally) and report it: stats_out (device int32[4]) = {dense panels, entries in
- * dense panels, 128-column SDDMM tiles over them, panels}. A panel is 128 consecutive
- * row_idx positions; it is dense when its columns number at most 1024 and its entries
- * fill at least a quarter of the 128 x |columns| tile. Mask of an m x n matrix with
- * n <= 65536 (SPOPS_ERR_UNSUPPORTED otherwise). The spops README ("Sparse Operations
- * (spops)", section "Sampled Dense-Dense Matrix Multiplication (SDDMM)") motivates the
- * structure-aware kernel by non-zeros that cluster in few rows and columns; the plan is
- * this library's reading of that. */
-SPOPS_API int spops_panel_plan(const int32_t* row_offsets, const void* row_idx, const void* col_idx, int itype,
-                               int32_t m, int32_t n, int32_t nnz, int32_t* stats_out, void* workspace, size_t ws_bytes,
-                               void* stream);
+                            int itype, int dtype, int32_t m, int32_t n, int32_t nnz, const void* B, void* C,
+                            void* stream);
 
 /* ---------------------------------------------------------------- checks */
 

@@ -50,6 +50,7 @@ def test_workspace_sizes_are_positive_and_monotone(lib):
     assert lib.spops_sort_rows_workspace_size(100000) > lib.spops_sort_rows_workspace_size(1000)
     assert lib.spops_spmm_workspace_size(4096, 4096, 2048, 167772, 1, 0) >= 16
     assert lib.spops_sddmm_workspace_size(4096, 4096, 2048, 167772, 1, 0, 1) >= 16
+    assert lib.spops_plan_size(4096, 4096, 167772) >= 1024
     assert lib.spops_check_csr_workspace_size(64) >= 8
 
 
@@ -58,16 +59,17 @@ FAKE = P(0x10000)  # never dereferenced: every call below fails validation first
 
 
 def test_bad_arguments_rejected_on_host(lib):
-    # dtype / itype / backend out of range
-    assert lib.spops_spmm(FAKE, FAKE, FAKE, FAKE, 0, 7, 4, 4, 4, FAKE, 4, FAKE, 0, FAKE, 1 << 20, None) == 1
-    assert lib.spops_spmm(FAKE, FAKE, FAKE, FAKE, 5, 0, 4, 4, 4, FAKE, 4, FAKE, 0, FAKE, 1 << 20, None) == 1
-    assert lib.spops_spmm(FAKE, FAKE, FAKE, FAKE, 0, 0, 4, 4, 4, P(0x20000), 4, P(0x40000), 9, FAKE, 1 << 20,
+    W = 1 << 30  # a workspace size large enough for every call below
+    # dtype / itype / backend / path out of range
+    assert lib.spops_spmm(FAKE, FAKE, FAKE, FAKE, 0, 7, 4, 4, 4, FAKE, 4, FAKE, 0, None, FAKE, W, None) == 1
+    assert lib.spops_spmm(FAKE, FAKE, FAKE, FAKE, 5, 0, 4, 4, 4, FAKE, 4, FAKE, 0, None, FAKE, W, None) == 1
+    assert lib.spops_spmm(FAKE, FAKE, FAKE, FAKE, 0, 0, 4, 4, 4, P(0x20000), 4, P(0x40000), 9, None, FAKE, W,
                           None) == 1
-    assert lib.spops_sddmm(FAKE, FAKE, FAKE, 0, 0, 4, 4, 4, 4, FAKE, FAKE, FAKE, 9, FAKE, 1 << 20, None) == 1
+    assert lib.spops_sddmm(FAKE, FAKE, FAKE, 0, 0, 4, 4, 4, 4, FAKE, FAKE, FAKE, 9, None, FAKE, W, None) == 1
     # negative sizes
     assert lib.spops_csr_add(FAKE, FAKE, None, FAKE, 0, 0, -1, 4, 4, FAKE, FAKE, None) == 1
     # int16 cannot index 40000 rows
-    assert lib.spops_spmm(FAKE, FAKE, FAKE, FAKE, 0, 0, 40000, 4, 4, FAKE, 4, FAKE, 0, FAKE, 1 << 20, None) == 2
+    assert lib.spops_spmm(FAKE, FAKE, FAKE, FAKE, 0, 0, 40000, 4, 4, FAKE, 4, FAKE, 0, None, FAKE, W, None) == 2
     assert b"int16" in lib.spops_last_error()
     # NULL row_offsets / misaligned values
     assert lib.spops_csr_add(FAKE, None, None, FAKE, 0, 0, 4, 4, 4, FAKE, FAKE, None) == 1
@@ -75,17 +77,31 @@ def test_bad_arguments_rejected_on_host(lib):
     # partial overlap of B and C in csr_add
     assert lib.spops_csr_add(FAKE, FAKE, None, FAKE, 0, 0, 4, 4, 4, P(0x20000), P(0x20004), None) == 1
     # SpMM output overlapping B
-    assert lib.spops_spmm(FAKE, FAKE, FAKE, FAKE, 0, 0, 4, 4, 4, P(0x20000), 4, P(0x20010), 0, FAKE, 1 << 20,
+    assert lib.spops_spmm(FAKE, FAKE, FAKE, FAKE, 0, 0, 4, 4, 4, P(0x20000), 4, P(0x20010), 0, None, FAKE, W,
                           None) == 1
-    # workspace too small / missing
-    assert lib.spops_spmm(FAKE, FAKE, FAKE, FAKE, 0, 0, 4, 4, 4, P(0x20000), 4, P(0x40000), 0, None, 0, None) == 3
+    # a plan that is not 1024-byte aligned
+    assert lib.spops_spmm(FAKE, FAKE, FAKE, FAKE, 0, 0, 4, 4, 4, P(0x20000), 4, P(0x40000), 0, P(0x30010), FAKE, W,
+                          None) == 1
+    # workspace too small / missing; plan buffer too small
+    assert lib.spops_spmm(FAKE, FAKE, FAKE, FAKE, 0, 0, 4, 4, 4, P(0x20000), 4, P(0x40000), 0, None, None, 0,
+                          None) == 3
     assert lib.spops_sort_rows(FAKE, 10, 5, FAKE, 0, FAKE, 8, None) == 3
+    assert lib.spops_plan_build(FAKE, FAKE, FAKE, 0, 10, 10, 5, P(0x40000), 64, None) == 3
     assert lib.spops_row_bins(FAKE, 10, 0, FAKE, None) == 1
     assert lib.spops_get_device_error(None, None) == 1
 
 
+def test_plan_size_grows_with_the_mask(lib):
+    small = lib.spops_plan_size(4096, 4096, 167772)
+    assert small > 0
+    assert lib.spops_plan_size(8192, 4096, 167772) > small          # more panels
+    assert lib.spops_plan_size(4096, 200000, 167772) < small        # no panels beyond 65536 columns
+    assert lib.spops_spmm_workspace_size(4096, 4096, 2048, 167772, 1, 0) > small   # plan + images
+    assert lib.spops_sddmm_workspace_size(4096, 4096, 2048, 167772, 1, 0, 1) >= small
+
+
 def test_empty_problems_are_no_ops(lib):
     # m * n == 0 returns before any device work
-    assert lib.spops_spmm(None, FAKE, None, None, 0, 0, 0, 4, 0, FAKE, 4, None, 0, None, 0, None) == 0
+    assert lib.spops_spmm(None, FAKE, None, None, 0, 0, 0, 4, 0, FAKE, 4, None, 0, None, None, 0, None) == 0
     assert lib.spops_csr_add(None, FAKE, None, None, 0, 0, 5, 0, 0, None, None, None) == 0
     assert lib.spops_sort_rows(FAKE, 0, 0, None, 0, None, 0, None) == 0

@@ -22,7 +22,7 @@ import torch
 
 from . import _lib
 
-__all__ = ["spmm", "sddmm", "csr_add", "sort_rows", "row_bins", "check_csr", "panel_plan", "SpopsError", "library_path",
+__all__ = ["spmm", "sddmm", "csr_add", "sort_rows", "row_bins", "check_csr", "plan_build", "Plan", "SpopsError", "library_path",
            "SPMM_LONG_ROW", "SDDMM_LONG_ROW"]
 
 SPMM_LONG_ROW = 256
@@ -117,11 +117,61 @@ def row_bins(row_offsets: torch.Tensor, t_long: int) -> torch.Tensor:
     return out
 
 
+class Plan:
+    """A mask plan (row bins and dense panels) built once per CSR structure; pass it to
+    spmm / sddmm on the same mask to skip rebuilding it in every call."""
+
+    def __init__(self, buf: torch.Tensor, m: int, n: int, nnz: int):
+        self.buf, self.m, self.n, self.nnz = buf, m, n, nnz
+
+    def ptr(self):
+        return ctypes.c_void_p(self.buf.data_ptr())
+
+    def stats(self) -> dict:
+        """Summary of the plan (synchronizes)."""
+        out = torch.zeros(16, dtype=torch.int32, device=self.buf.device)
+        with torch.cuda.device(self.buf.device):
+            _check(_L().spops_plan_stats(self.ptr(), self.m, self.n, self.nnz, _p(out), _stream()), "plan_stats")
+        s = out.cpu().tolist()
+        return {"dense_panels": s[0], "sddmm_tiles": s[1], "spmm_panels": s[2], "dense_entries": s[3],
+                "image_elems": s[4], "panels": s[5], "bins_spmm": s[8:12], "bins_sddmm": s[12:16]}
+
+
+def plan_build(row_offsets, row_idx, col_idx, n: int) -> Plan:
+    """Build the mask plan of an m x n CSR structure (asynchronous on the current stream)."""
+    _req(row_offsets, "row_offsets", torch.int32)
+    dev = row_offsets.device
+    _req(col_idx, "col_idx", device=dev)
+    _req(row_idx, "row_idx", device=dev)
+    m = row_offsets.numel() - 1
+    it = _itype(col_idx, row_idx)
+    nnz = col_idx.numel()
+    lib = _L()
+    size = int(lib.spops_plan_size(m, int(n), nnz))
+    raw = torch.empty(size + 1024, dtype=torch.uint8, device=dev)
+    off = (-raw.data_ptr()) % 1024
+    buf = raw[off:off + size]
+    with torch.cuda.device(dev):
+        _check(lib.spops_plan_build(_p(row_offsets), _p(row_idx), _p(col_idx), it, m, int(n), nnz, _p(buf), size,
+                                    _stream()), "plan_build")
+    plan = Plan(buf, m, int(n), nnz)
+    plan._raw = raw
+    return plan
+
+
+def _plan_ptr(plan, m, n, nnz):
+    if plan is None:
+        return ctypes.c_void_p(0)
+    if (plan.m, plan.n, plan.nnz) != (m, n, nnz):
+        raise ValueError(f"plan was built for (m, n, nnz) = {(plan.m, plan.n, plan.nnz)}, not {(m, n, nnz)}")
+    return plan.ptr()
+
+
 def spmm(A_val, A_row_offsets, A_row_indices, A_col_indices, B, m: int, out: torch.Tensor | None = None,
-         path: str = "auto"):
+         path: str = "auto", plan: Plan | None = None):
     """C = A @ B for a CSR matrix A (m rows) and a dense row-major B.
     path="auto" runs dense row panels on the tensor cores, "general" every row on the
-    general row kernels."""
+    general row kernels. plan: a Plan of this mask (optional)."""
     if path not in _SPMM_PATH:
         raise ValueError(f"path must be one of {list(_SPMM_PATH)}")
     _req(B, "B", dtypes=_DTYPE)
@@ -147,13 +197,15 @@ def spmm(A_val, A_row_offsets, A_row_indices, A_col_indices, B, m: int, out: tor
     with torch.cuda.device(dev):
         ws = _ws(lib.spops_spmm_workspace_size(m, k, n, nnz, dt, it), dev)
         _check(lib.spops_spmm(_p(A_val), _p(A_row_offsets), _p(A_row_indices), _p(A_col_indices), it, dt, m, k, nnz,
-                              _p(B), n, _p(C), _SPMM_PATH[path], _p(ws), ws.numel(), _stream()), "spmm")
+                              _p(B), n, _p(C), _SPMM_PATH[path], _plan_ptr(plan, m, k, nnz), _p(ws), ws.numel(),
+                              _stream()), "spmm")
     return C
 
 
 def sddmm(out_row_offsets, out_row_indices, out_col_indices, A, BT, backend: str = "structure_aware",
-          out: torch.Tensor | None = None):
-    """out[k] = A[i, :] . BT[col[k], :] for every entry k (row i) of the CSR mask."""
+          out: torch.Tensor | None = None, plan: Plan | None = None):
+    """out[k] = A[i, :] . BT[col[k], :] for every entry k (row i) of the CSR mask.
+    plan: a Plan of this mask (optional)."""
     _req(A, "A", dtypes=_DTYPE)
     dev = A.device
     _req(BT, "BT", A.dtype, device=dev)
@@ -177,7 +229,8 @@ def sddmm(out_row_offsets, out_row_indices, out_col_indices, A, BT, backend: str
     with torch.cuda.device(dev):
         ws = _ws(lib.spops_sddmm_workspace_size(m, n, kd, nnz, dt, it, be), dev)
         _check(lib.spops_sddmm(_p(out_row_offsets), _p(out_row_indices), _p(out_col_indices), it, dt, m, n, kd, nnz,
-                               _p(A), _p(BT), _p(res), be, _p(ws), ws.numel(), _stream()), "sddmm")
+                               _p(A), _p(BT), _p(res), be, _plan_ptr(plan, m, n, nnz), _p(ws), ws.numel(),
+                               _stream()), "sddmm")
     return res
 
 
@@ -203,24 +256,6 @@ def csr_add(A_val, A_row_offsets, A_row_indices, A_col_indices, B, out: torch.Te
         _check(_L().spops_csr_add(_p(A_val), _p(A_row_offsets), _p(A_row_indices), _p(A_col_indices), it,
                                   _DTYPE[B.dtype], m, n, nnz, _p(B), _p(C), _stream()), "csr_add")
     return C
-
-
-def panel_plan(row_offsets, row_idx, col_idx, n: int) -> dict:
-    """Build the structure-aware plan for a mask and return its summary (synchronizes):
-    dense panels, entries in dense panels, SDDMM tiles and panels."""
-    _req(row_offsets, "row_offsets", torch.int32)
-    dev = row_offsets.device
-    m = row_offsets.numel() - 1
-    it = _itype(col_idx, row_idx)
-    nnz = col_idx.numel()
-    stats = torch.zeros(4, dtype=torch.int32, device=dev)
-    lib = _L()
-    with torch.cuda.device(dev):
-        ws = _ws(lib.spops_panel_plan_workspace_size(m, nnz), dev)
-        _check(lib.spops_panel_plan(_p(row_offsets), _p(row_idx), _p(col_idx), it, m, int(n), nnz, _p(stats), _p(ws),
-                                    ws.numel(), _stream()), "panel_plan")
-    s = stats.cpu().tolist()
-    return {"dense_panels": s[0], "dense_entries": s[1], "sddmm_tiles": s[2], "panels": s[3]}
 
 
 def check_csr(row_offsets, col_idx, row_idx, n: int) -> None:

@@ -27,12 +27,13 @@ SIGNATURES = {
     "spops_sort_rows_static_max_rows": (_I32, []),
     "spops_row_bins": (_INT, [_P, _I32, _I32, _P, _P]),
     "spops_spmm_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _INT, _INT]),
-    "spops_spmm": (_INT, [_P, _P, _P, _P, _INT, _INT, _I32, _I32, _I32, _P, _I32, _P, _INT, _P, _SZ, _P]),
+    "spops_plan_size": (_SZ, [_I32, _I32, _I32]),
+    "spops_plan_build": (_INT, [_P, _P, _P, _INT, _I32, _I32, _I32, _P, _SZ, _P]),
+    "spops_plan_stats": (_INT, [_P, _I32, _I32, _I32, _P, _P]),
+    "spops_spmm": (_INT, [_P, _P, _P, _P, _INT, _INT, _I32, _I32, _I32, _P, _I32, _P, _INT, _P, _P, _SZ, _P]),
     "spops_sddmm_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _INT, _INT, _INT]),
-    "spops_sddmm": (_INT, [_P, _P, _P, _INT, _INT, _I32, _I32, _I32, _I32, _P, _P, _P, _INT, _P, _SZ, _P]),
+    "spops_sddmm": (_INT, [_P, _P, _P, _INT, _INT, _I32, _I32, _I32, _I32, _P, _P, _P, _INT, _P, _P, _SZ, _P]),
     "spops_csr_add": (_INT, [_P, _P, _P, _P, _INT, _INT, _I32, _I32, _I32, _P, _P, _P]),
-    "spops_panel_plan_workspace_size": (_SZ, [_I32, _I32]),
-    "spops_panel_plan": (_INT, [_P, _P, _P, _INT, _I32, _I32, _I32, _P, _P, _SZ, _P]),
     "spops_check_csr_workspace_size": (_SZ, [_I32]),
     "spops_check_csr": (_INT, [_P, _P, _P, _INT, _I32, _I32, _I32, _P, _SZ, _P]),
     "spops_get_device_error": (_INT, [_P, ctypes.POINTER(ctypes.c_int32)]),

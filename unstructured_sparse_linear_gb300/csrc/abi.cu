@@ -9,6 +9,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "panel.h"
+#include "plan.h"
 
 namespace spops {
 
@@ -127,8 +128,6 @@ bool overlaps(const void* a, size_t abytes, const void* b, size_t bbytes) {
     return x < y + bbytes && y < x + abytes;
 }
 
-constexpr size_t kBinsBytes = 256;
-
 }  // namespace
 
 extern "C" {
@@ -176,13 +175,41 @@ int spops_row_bins(const int32_t* row_offsets, int32_t m, int32_t t_long, int32_
     return cuda_status(launch_row_bins(row_offsets, m, t_long, bins_out, (cudaStream_t)stream), "row_bins launch");
 }
 
+size_t spops_plan_size(int32_t m, int32_t n, int32_t nnz) {
+    if (m < 0 || n < 0 || nnz < 0) return 0;
+    return plan_bytes(m, n, nnz) + 1024;
+}
+
+int spops_plan_build(const int32_t* row_offsets, const void* row_idx, const void* col_idx, int itype, int32_t m,
+                     int32_t n, int32_t nnz, void* plan, size_t plan_size, void* stream) {
+    int st = check_common(itype, SPOPS_F16, m, n, nnz, nullptr, row_offsets, row_idx, col_idx, false, true);
+    if (st != SPOPS_OK) return st;
+    if (m == 0) return ok();
+    if (!plan || !aligned(plan, 1024) || plan_size < spops_plan_size(m, n, nnz))
+        return fail(SPOPS_ERR_WORKSPACE, "plan needs a 1024-byte aligned buffer of %zu bytes (got %zu)",
+                    spops_plan_size(m, n, nnz), plan_size);
+    const PlanView v = plan_view(plan, m, n, nnz);
+    return cuda_status(launch_plan_build(itype, row_offsets, row_idx, col_idx, v,
+                                         (int64_t)spmm_image_budget_elems(m, nnz), (cudaStream_t)stream),
+                       "plan_build launch");
+}
+
+int spops_plan_stats(const void* plan, int32_t m, int32_t n, int32_t nnz, int32_t* stats_out, void* stream) {
+    if (m <= 0 || n < 0 || nnz < 0) return fail(SPOPS_ERR_INVALID_ARG, "bad sizes (m=%d n=%d nnz=%d)", m, n, nnz);
+    if (!plan || !aligned(plan, 1024)) return fail(SPOPS_ERR_INVALID_ARG, "plan is NULL or not 1024-byte aligned");
+    if (!stats_out || !aligned(stats_out, 4)) return fail(SPOPS_ERR_INVALID_ARG, "stats_out is NULL or misaligned");
+    const PlanView v = plan_view(const_cast<void*>(plan), m, n, nnz);
+    return cuda_status(launch_plan_stats(v, stats_out, (cudaStream_t)stream), "plan_stats launch");
+}
+
 size_t spops_spmm_workspace_size(int32_t m, int32_t k, int32_t n, int32_t nnz, int dtype, int itype) {
-    return kBinsBytes + panel_spmm_workspace_bytes(m, k, n, nnz, dtype, itype);
+    (void)itype;
+    return spmm_workspace_bytes(m, k, n, nnz, dtype);
 }
 
 int spops_spmm(const void* A_val, const int32_t* row_offsets, const void* row_idx, const void* col_idx, int itype,
                int dtype, int32_t m, int32_t k, int32_t nnz, const void* B, int32_t n, void* C, int path,
-               void* workspace, size_t ws_bytes, void* stream) {
+               const void* plan, void* workspace, size_t ws_bytes, void* stream) {
     int st = check_common(itype, dtype, m, k, nnz, A_val, row_offsets, row_idx, col_idx, true, true);
     if (st != SPOPS_OK) return st;
     if (path != SPOPS_SPMM_AUTO && path != SPOPS_SPMM_GENERAL)
@@ -193,26 +220,23 @@ int spops_spmm(const void* A_val, const int32_t* row_offsets, const void* row_id
     if (!C || !aligned(C, ds)) return fail(SPOPS_ERR_INVALID_ARG, "C is NULL or misaligned");
     if ((int64_t)k * n > 0 && (!B || !aligned(B, ds))) return fail(SPOPS_ERR_INVALID_ARG, "B is NULL or misaligned");
     if (overlaps(C, (size_t)m * n * ds, B, (size_t)k * n * ds)) return fail(SPOPS_ERR_INVALID_ARG, "C overlaps B");
+    if (plan && !aligned(plan, 1024)) return fail(SPOPS_ERR_INVALID_ARG, "plan is not 1024-byte aligned");
     const size_t need = spops_spmm_workspace_size(m, k, n, nnz, dtype, itype);
     if (!workspace || !aligned(workspace, 16) || ws_bytes < need)
         return fail(SPOPS_ERR_WORKSPACE, "spmm needs a 16-byte aligned workspace of %zu bytes (got %zu)", need, ws_bytes);
-    cudaStream_t s = (cudaStream_t)stream;
-    int32_t* bins = static_cast<int32_t*>(workspace);
-    cudaError_t e = launch_row_bins(row_offsets, m, kSpmmLongRow, bins, s);
-    if (e != cudaSuccess) return cuda_status(e, "row_bins launch");
-    e = launch_spmm(dtype, itype, A_val, row_offsets, row_idx, col_idx, m, k, nnz, B, n, C, bins,
-                    static_cast<char*>(workspace) + kBinsBytes, path == SPOPS_SPMM_AUTO, s);
-    return cuda_status(e, "spmm launch");
+    return cuda_status(launch_spmm(dtype, itype, A_val, row_offsets, row_idx, col_idx, m, k, nnz, B, n, C, plan,
+                                   workspace, path == SPOPS_SPMM_AUTO, (cudaStream_t)stream),
+                       "spmm launch");
 }
 
 size_t spops_sddmm_workspace_size(int32_t m, int32_t n, int32_t kd, int32_t nnz, int dtype, int itype, int backend) {
-    size_t extra = backend == SPOPS_SDDMM_STRUCTURE_AWARE ? panel_sddmm_workspace_bytes(m, n, kd, nnz, dtype, itype) : 0;
-    return kBinsBytes + extra;
+    (void)itype;
+    return sddmm_workspace_bytes(m, n, kd, nnz, dtype, backend == SPOPS_SDDMM_STRUCTURE_AWARE);
 }
 
 int spops_sddmm(const int32_t* out_row_offsets, const void* out_row_idx, const void* out_col_idx, int itype,
                 int dtype, int32_t m, int32_t n, int32_t kd, int32_t nnz, const void* A, const void* BT,
-                void* out_val, int backend, void* workspace, size_t ws_bytes, void* stream) {
+                void* out_val, int backend, const void* plan, void* workspace, size_t ws_bytes, void* stream) {
     int st = check_common(itype, dtype, m, n, nnz, out_val, out_row_offsets, out_row_idx, out_col_idx, true, true);
     if (st != SPOPS_OK) return st;
     if (backend != SPOPS_SDDMM_STRUCTURE_AWARE && backend != SPOPS_SDDMM_GENERAL)
@@ -222,16 +246,14 @@ int spops_sddmm(const int32_t* out_row_offsets, const void* out_row_idx, const v
     const size_t ds = dtype_size(dtype);
     if (kd > 0 && (!A || !BT || !aligned(A, ds) || !aligned(BT, ds)))
         return fail(SPOPS_ERR_INVALID_ARG, "A or BT is NULL or misaligned");
+    if (plan && !aligned(plan, 1024)) return fail(SPOPS_ERR_INVALID_ARG, "plan is not 1024-byte aligned");
     const size_t need = spops_sddmm_workspace_size(m, n, kd, nnz, dtype, itype, backend);
     if (!workspace || !aligned(workspace, 16) || ws_bytes < need)
         return fail(SPOPS_ERR_WORKSPACE, "sddmm needs a 16-byte aligned workspace of %zu bytes (got %zu)", need, ws_bytes);
-    cudaStream_t s = (cudaStream_t)stream;
-    int32_t* bins = static_cast<int32_t*>(workspace);
-    cudaError_t e = launch_row_bins(out_row_offsets, m, kSddmmLongRow, bins, s);
-    if (e != cudaSuccess) return cuda_status(e, "row_bins launch");
-    e = launch_sddmm(dtype, itype, out_row_offsets, out_row_idx, out_col_idx, m, n, kd, nnz, A, BT, out_val,
-                     backend == SPOPS_SDDMM_STRUCTURE_AWARE, bins, static_cast<char*>(workspace) + kBinsBytes, s);
-    return cuda_status(e, "sddmm launch");
+    return cuda_status(launch_sddmm(dtype, itype, out_row_offsets, out_row_idx, out_col_idx, m, n, kd, nnz, A, BT,
+                                    out_val, backend == SPOPS_SDDMM_STRUCTURE_AWARE, plan, workspace,
+                                    (cudaStream_t)stream),
+                       "sddmm launch");
 }
 
 int spops_csr_add(const void* A_val, const int32_t* row_offsets, const void* row_idx, const void* col_idx,
@@ -246,25 +268,6 @@ int spops_csr_add(const void* A_val, const int32_t* row_offsets, const void* row
     if (B != C && overlaps(B, bytes, C, bytes)) return fail(SPOPS_ERR_INVALID_ARG, "C partially overlaps B");
     return cuda_status(launch_csr_add(dtype, itype, A_val, row_offsets, col_idx, m, n, nnz, B, C, (cudaStream_t)stream),
                        "csr_add launch");
-}
-
-size_t spops_panel_plan_workspace_size(int32_t m, int32_t nnz) {
-    return (m > 0 && nnz >= 0) ? panel_plan_workspace_bytes(m, nnz) : 16;
-}
-
-int spops_panel_plan(const int32_t* row_offsets, const void* row_idx, const void* col_idx, int itype, int32_t m,
-                     int32_t n, int32_t nnz, int32_t* stats_out, void* workspace, size_t ws_bytes, void* stream) {
-    int st = check_common(itype, SPOPS_F16, m, n, nnz, nullptr, row_offsets, row_idx, col_idx, false, true);
-    if (st != SPOPS_OK) return st;
-    if (!stats_out || !aligned(stats_out, 4)) return fail(SPOPS_ERR_INVALID_ARG, "stats_out is NULL or misaligned");
-    if (n > 65536) return fail(SPOPS_ERR_UNSUPPORTED, "panel plans need n <= 65536 (n=%d)", n);
-    if (m == 0) return fail(SPOPS_ERR_INVALID_ARG, "panel plans need m >= 1");
-    const size_t need = spops_panel_plan_workspace_size(m, nnz);
-    if (!workspace || !aligned(workspace, 16) || ws_bytes < need)
-        return fail(SPOPS_ERR_WORKSPACE, "panel_plan needs a workspace of %zu bytes (got %zu)", need, ws_bytes);
-    return cuda_status(launch_panel_plan(itype, row_offsets, row_idx, col_idx, m, n, nnz, stats_out, workspace,
-                                         (cudaStream_t)stream),
-                       "panel_plan launch");
 }
 
 size_t spops_check_csr_workspace_size(int32_t m) { return align_up(((size_t)(m > 0 ? m : 0) + 31) / 32 * 4, 256) + 16; }

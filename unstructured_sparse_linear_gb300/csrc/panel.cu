@@ -3,24 +3,18 @@
 // spops README ("Sparse Operations (spops)"), section "Sampled Dense-Dense Matrix
 // Multiplication (SDDMM)": besides the general kernel, SDDMM has a structure-aware kernel
 // for the masks seen in RoSA, whose non-zeros cluster in a small subset of rows and
-// columns. This file is that idea written for GB300:
-//
-// Plan (per call, from row_offsets / row_idx / col_idx only):
-//   * panels: consecutive groups of 128 positions of row_idx (128 = UMMA M). Because
-//     row_idx sorts rows by nnz, the clustered rows of a RoSA mask fill the first panels.
-//   * for each panel, the union U of its columns (bitmap + popcount scan), the compact
-//     position of every entry in U (upos), and a dense flag: |U| <= 1024 and the entries
-//     fill at least a quarter of the 128 x |U| tile the tensor cores would compute.
-//   * a work list of dense panels (and 128-column tiles of U for SDDMM).
-// Execution:
-//   * SDDMM: D = A[panel rows, :] * BT[U, :]^T per (panel, U tile, K split) on tcgen05
-//     (fp16/bf16 in, fp32 accumulate in TMEM); the epilogue samples D at the panel's entries.
-//     K is split across CTAs when there are fewer tiles than SMs; the fp32 partial sums are
-//     added in split order by a finalize kernel, so results are deterministic.
-//   * SpMM: the panel's values are scattered into a dense 128 x |U| image (already in the
-//     UMMA 128-byte-swizzled K-major layout), and C[panel rows, N tile] = image * B[U, N tile]
-//     on tcgen05, with B's rows gathered straight into an MN-major swizzled tile.
-//   * rows of non-dense panels run through the general row kernels, which skip dense ones.
+// columns. The mask plan (plan.cu) groups row_idx positions into panels of 128 rows and
+// marks a panel dense when its entries fill its 128 x |U| tile well (U = the union of the
+// panel's columns). Here:
+//   * SDDMM: D = A[panel rows, :] * BT[U, :]^T per (panel, 128-column tile of U, K split)
+//     on tcgen05 (fp16/bf16 operands, fp32 accumulators in tensor memory); the epilogue
+//     reads each row's entries of the tile (contiguous, located by the plan's tile starts)
+//     out of D. With fewer tiles than SMs, K is split in up to 4 parts whose fp32 partial
+//     sums a finalize kernel adds in split order, so results are deterministic.
+//   * SpMM: each dense panel's values are written into a 128 x |U| image already in the
+//     UMMA K-major 128-byte-swizzled layout; C[panel rows, 256-column tile] =
+//     image * B[U, tile] on tcgen05, with B's rows gathered into an MN-major swizzled tile.
+//   * the other rows run through the general row kernels, which skip dense panels.
 // Operands are gathered row by row with 16-byte cp.async copies into a 4-stage shared
 // memory ring; one thread issues the MMAs and commits them to per-stage mbarriers, whose
 // completion frees the stage for the next copy. Every mbarrier wait is bounded in time.
@@ -29,267 +23,59 @@
 #include "common.cuh"
 #include "internal.h"
 #include "panel.h"
+#include "plan.h"
 #include "tc.cuh"
 
 namespace spops {
 namespace {
 
-constexpr int kPM = 128;         // rows per panel (UMMA M)
-constexpr int kUCap = 1024;      // most distinct columns a dense panel may have
-constexpr int kKC = 64;          // K elements per pipeline chunk (128 bytes of 16-bit data)
+constexpr int kKC = 64;       // K elements per pipeline chunk (128 bytes of 16-bit data)
 constexpr int kStages = 4;
-constexpr int kSdNT = 128;       // SDDMM: columns of U per tile (UMMA N)
-constexpr int kSpNT = 256;       // SpMM: columns of C per tile (UMMA N)
-constexpr int kMaxWords = 2048;  // column bitmap words: n <= 65536
-constexpr int kMaxSplit = 16;
+constexpr int kSpNT = 256;    // SpMM: columns of C per tile (UMMA N)
+constexpr int kMaxSplit = 4;
 constexpr int kTileThreads = 128;
-constexpr size_t kPartialBudget = 64ull << 20;  // bytes of fp32 split-K partial sums
 
-constexpr uint32_t kSdStageBytes = 2 * kPM * kKC * 2;                  // A + BT tiles: 32 KB
-constexpr uint32_t kSpStageA = kPM * kKC * 2;                          // 16 KB
-constexpr uint32_t kSpStageB = kSpNT * kKC * 2;                        // 32 KB
-constexpr uint32_t kSpStageBytes = kSpStageA + kSpStageB;              // 48 KB
+constexpr uint32_t kSdStageA = kPM * kKC * 2;                 // 16 KB
+constexpr uint32_t kSdStageBytes = kSdStageA + kTileN * kKC * 2;  // A + BT tiles: 32 KB
+constexpr uint32_t kSpStageA = kPM * kKC * 2;                 // 16 KB
+constexpr uint32_t kSpStageB = kSpNT * kKC * 2;               // 32 KB
+constexpr uint32_t kSpStageBytes = kSpStageA + kSpStageB;     // 48 KB
 constexpr uint32_t kSdSmem = kStages * kSdStageBytes + 1024;
 constexpr uint32_t kSpSmem = kStages * kSpStageBytes + 1024;
 
-struct PanelWs {
-    int4* desc;        // [P] {dense, |U|, nnz of the panel, image offset in elements}
-    int32_t* prow;     // [P * 128] row id at each panel position, -1 past m
-    int32_t* ulist;    // [P * kUCap] sorted columns of U (dense panels)
-    uint16_t* upos;    // [nnz] position of each entry's column in its panel's U
-    uint8_t* dense;    // [P] dense flag
-    int32_t* counts;   // [4] {#dense panels, #SDDMM tiles, image elements, 0}
-    int32_t* dlist;    // [P] dense panel ids
-    int32_t* items;    // [P * kUCap / kSdNT] (panel << 8) | tile
-    float* partial;    // [max_split * nnz] SDDMM split-K partial sums
-    void* img;         // SpMM dense images
-};
+bool dtype_ok(int dt) { return dt == kF16 || dt == kBF16; }
 
-struct Layout {
-    size_t desc, prow, ulist, upos, dense, counts, dlist, items, partial, img, total;
-};
-
-Layout layout(int32_t m, int32_t nnz, bool sddmm, int max_split, bool spmm) {
-    const size_t P = (size_t)(m + kPM - 1) / kPM;
-    Layout L{};
-    size_t off = 0;
-    auto take = [&](size_t bytes) {
-        const size_t at = off;
-        off = align_up(off + bytes, 1024);
-        return at;
-    };
-    L.desc = take(P * 16);
-    L.prow = take(P * kPM * 4);
-    L.ulist = take(P * kUCap * 4);
-    L.upos = take((size_t)nnz * 2);
-    L.dense = take(P);
-    L.counts = take(16);
-    L.dlist = take(P * 4);
-    L.items = take(P * (kUCap / kSdNT) * 4);
-    L.partial = take(sddmm ? (size_t)max_split * nnz * 4 : 0);
-    L.img = take(spmm ? ((size_t)4 * nnz + P * kPM * kKC) * 2 : 0);
-    L.total = off + 1024;  // slack for aligning the base
-    return L;
-}
-
-PanelWs carve(void* ws, const Layout& L) {
-    char* b = reinterpret_cast<char*>(align_up(reinterpret_cast<uintptr_t>(ws), 1024));
-    PanelWs w;
-    w.desc = reinterpret_cast<int4*>(b + L.desc);
-    w.prow = reinterpret_cast<int32_t*>(b + L.prow);
-    w.ulist = reinterpret_cast<int32_t*>(b + L.ulist);
-    w.upos = reinterpret_cast<uint16_t*>(b + L.upos);
-    w.dense = reinterpret_cast<uint8_t*>(b + L.dense);
-    w.counts = reinterpret_cast<int32_t*>(b + L.counts);
-    w.dlist = reinterpret_cast<int32_t*>(b + L.dlist);
-    w.items = reinterpret_cast<int32_t*>(b + L.items);
-    w.partial = reinterpret_cast<float*>(b + L.partial);
-    w.img = b + L.img;
-    return w;
-}
-
-int sddmm_max_split(int32_t nnz, int32_t kd) {
+int sddmm_max_split(int32_t kd) {
     const int nkc = (kd + kKC - 1) / kKC;
-    size_t by_mem = nnz > 0 ? kPartialBudget / ((size_t)nnz * 4) : kMaxSplit;
-    int s = (int)min64((int64_t)kMaxSplit, (int64_t)by_mem);
-    s = (int)min64(s, nkc);
-    return s < 1 ? 1 : s;
+    return nkc < kMaxSplit ? (nkc < 1 ? 1 : nkc) : kMaxSplit;
 }
 
-bool panels_possible(int dt, int32_t m, int32_t ncols) {
-    return (dt == kF16 || dt == kBF16) && m > 0 && ncols > 0 && ncols <= kMaxWords * 32;
-}
-
-// ------------------------------------------------------------------ plan kernels
-
-__device__ __forceinline__ int warp_sum(int v) {
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
-template <typename I>
-__global__ void __launch_bounds__(256) plan_panels_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx,
-                                                          const I* __restrict__ col, int32_t m, int32_t ncols,
-                                                          PanelWs ws) {
-    __shared__ uint32_t bitmap[kMaxWords];
-    __shared__ uint32_t wbase[kMaxWords];
-    __shared__ int32_t rows[kPM];
-    __shared__ int32_t red[8];
-    __shared__ int32_t scan[256];
-    const int p = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int words = (ncols + 31) >> 5;
-    if (tid < kPM) {
-        const int64_t pos = (int64_t)p * kPM + tid;
-        const int r = pos < m ? idx_of(row_idx[pos]) : -1;
-        rows[tid] = r;
-        ws.prow[p * kPM + tid] = r;
-    }
-    for (int w = tid; w < words; w += 256) bitmap[w] = 0;
-    __syncthreads();
-    int cnt = 0;
-    for (int r = warp; r < kPM; r += 8) {
-        const int i = rows[r];
-        if (i < 0) continue;
-        const int32_t k1 = ro[i + 1];
-        for (int32_t k = ro[i] + lane; k < k1; k += 32) {
-            const int c = idx_of(col[k]);
-            atomicOr(&bitmap[c >> 5], 1u << (c & 31));
-            ++cnt;
-        }
-    }
-    cnt = warp_sum(cnt);
-    if (lane == 0) red[warp] = cnt;
-    __syncthreads();
-    int nnz_p = 0;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) nnz_p += red[w];
-    // exclusive scan of the words' popcounts
-    const int per = (words + 255) / 256;
-    const int b = tid * per, e = min(words, b + per);
-    int s = 0;
-    for (int w = b; w < e; ++w) s += __popc(bitmap[w]);
-    scan[tid] = s;
-    __syncthreads();
-    for (int off = 1; off < 256; off <<= 1) {
-        const int v = tid >= off ? scan[tid - off] : 0;
-        __syncthreads();
-        scan[tid] += v;
-        __syncthreads();
-    }
-    int run = tid ? scan[tid - 1] : 0;
-    for (int w = b; w < e; ++w) {
-        wbase[w] = run;
-        run += __popc(bitmap[w]);
-    }
-    const int U = scan[255];
-    __syncthreads();
-    const bool dense = nnz_p > 0 && U <= kUCap && (int64_t)nnz_p * 4 >= (int64_t)kPM * U;
-    if (tid == 0) {
-        ws.desc[p] = make_int4(dense ? 1 : 0, U, nnz_p, 0);
-        ws.dense[p] = dense ? 1 : 0;
-    }
-    if (!dense) return;
-    for (int w = tid; w < words; w += 256) {
-        uint32_t bits = bitmap[w];
-        int at = wbase[w];
-        while (bits) {
-            const int bit = __ffs(bits) - 1;
-            ws.ulist[p * kUCap + at++] = w * 32 + bit;
-            bits &= bits - 1;
-        }
-    }
-    for (int r = warp; r < kPM; r += 8) {
-        const int i = rows[r];
-        if (i < 0) continue;
-        const int32_t k1 = ro[i + 1];
-        for (int32_t k = ro[i] + lane; k < k1; k += 32) {
-            const int c = idx_of(col[k]);
-            ws.upos[k] = (uint16_t)(wbase[c >> 5] + __popc(bitmap[c >> 5] & ((1u << (c & 31)) - 1u)));
-        }
-    }
-}
-
-// Block-wide exclusive scan (1024 threads) of one int; returns the block total in *total.
-__device__ __forceinline__ int block_scan_1024(int v, int* sh, int* total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int x = v;
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) sh[warp] = x;
-    __syncthreads();
-    if (warp == 0) {
-        int w = sh[lane];
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, w, o);
-            if (lane >= o) w += y;
-        }
-        sh[lane] = w;
-    }
-    __syncthreads();
-    const int before = (warp ? sh[warp - 1] : 0) + x - v;
-    *total = sh[31];
-    __syncthreads();
-    return before;
-}
-
-__global__ void __launch_bounds__(1024) plan_worklist_kernel(int32_t P, PanelWs ws) {
-    __shared__ int sh[32];
-    int cd = 0, ct = 0, ci = 0;
-    for (int base = 0; base < P; base += 1024) {
-        const int p = base + threadIdx.x;
-        int4 d = p < P ? ws.desc[p] : make_int4(0, 0, 0, 0);
-        const int dn = d.x;
-        const int tiles = dn ? (d.y + kSdNT - 1) / kSdNT : 0;
-        const int img = dn ? kPM * ((d.y + kKC - 1) / kKC) * kKC : 0;
-        int td, tt, ti;
-        const int ed = block_scan_1024(dn, sh, &td);
-        const int et = block_scan_1024(tiles, sh, &tt);
-        const int ei = block_scan_1024(img, sh, &ti);
-        if (dn) {
-            ws.dlist[cd + ed] = p;
-            for (int j = 0; j < tiles; ++j) ws.items[ct + et + j] = (p << 8) | j;
-            ws.desc[p].w = ci + ei;
-        }
-        cd += td;
-        ct += tt;
-        ci += ti;
-    }
-    if (threadIdx.x == 0) {
-        ws.counts[0] = cd;
-        ws.counts[1] = ct;
-        ws.counts[2] = ci;
-        ws.counts[3] = 0;
-    }
-}
-
-// ------------------------------------------------------------------ SDDMM dense panels
-
-__device__ __forceinline__ int choose_split(int items, int grid, int max_split, int nkc) {
+// Number of K splits given the work items and the grid (identical on every CTA).
+__host__ __device__ __forceinline__ int choose_split(int items, int grid, int max_split, int nkc) {
     int s = items > 0 ? grid / items : 1;
     s = s < 1 ? 1 : s;
     s = s > max_split ? max_split : s;
     s = s > nkc ? nkc : s;
     const int per = (nkc + s - 1) / s;
-    return (nkc + per - 1) / per;  // splits actually used (each gets >= 1 chunk)
+    return (nkc + per - 1) / per;  // every split gets at least one chunk
 }
+
+// ------------------------------------------------------------------ SDDMM dense panels
 
 template <typename T>
 __global__ void __launch_bounds__(kTileThreads, 1)
-sddmm_panel_kernel(const int32_t* __restrict__ ro, const T* __restrict__ A, const T* __restrict__ BT,
-                   T* __restrict__ out, int32_t kd, int32_t nnz, PanelWs ws, int max_split, uint32_t idesc,
-                   int* err) {
+sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restrict__ out, float* __restrict__ partial,
+                   int32_t kd, PlanView v, int max_split, uint32_t idesc, int* err) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t mma_bar[kStages];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int32_t s_rows[kPM];
-    __shared__ int32_t s_u[kSdNT];
+    __shared__ int32_t s_u[kTileN];
     uint8_t* smem = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(smem_raw), 1024));
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5;
 
-    if (warp == 0) tc::tmem_alloc(smem_u32(&tmem_base_sh), kSdNT);
+    if (warp == 0) tc::tmem_alloc(smem_u32(&tmem_base_sh), kTileN);
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&mma_bar[s]), 1);
         fence_mbar_init();
@@ -299,7 +85,7 @@ sddmm_panel_kernel(const int32_t* __restrict__ ro, const T* __restrict__ A, cons
     tc::fence_after_sync();
     const uint32_t tmem = tmem_base_sh;
 
-    const int nitems = ws.counts[1];
+    const int nitems = v.counts()[kCntTiles];
     const int nkc = (kd + kKC - 1) / kKC;
     const int S = choose_split(nitems, gridDim.x, max_split, nkc);
     const int kc_per = (nkc + S - 1) / S;
@@ -308,17 +94,17 @@ sddmm_panel_kernel(const int32_t* __restrict__ ro, const T* __restrict__ A, cons
     bool failed = false;
 
     for (int64_t unit = blockIdx.x; unit < units && !failed; unit += gridDim.x) {
-        const int item = ws.items[unit / S];
+        const int item = v.items[unit / S];
         const int split = (int)(unit % S);
         const int p = item >> 8, t = item & 255;
         const int kc0 = split * kc_per;
         const int nk = min(nkc, kc0 + kc_per) - kc0;
-        const int nU = ws.desc[p].y;
-        const int u0 = t * kSdNT;
-        const int ncols = min(kSdNT, nU - u0);
-        __syncthreads();  // the previous unit's epilogue is done with s_rows / smem
-        s_rows[tid] = ws.prow[p * kPM + tid];
-        s_u[tid] = tid < ncols ? ws.ulist[p * kUCap + u0 + tid] : -1;
+        const int nU = v.desc[p].y;
+        const int u0 = t * kTileN;
+        const int ncols = min(kTileN, nU - u0);
+        __syncthreads();  // the previous unit's epilogue is done with s_rows and the stages
+        s_rows[tid] = v.prow[p * kPM + tid];
+        s_u[tid] = tid < ncols ? v.ulist[(size_t)p * kUCap + u0 + tid] : -1;
         __syncthreads();
 
         auto load = [&](int j, uint32_t gs) {
@@ -335,7 +121,7 @@ sddmm_panel_kernel(const int32_t* __restrict__ ro, const T* __restrict__ A, cons
                 tc::cp_async16(st + off, oka ? (const void*)(A + (int64_t)r * kd + kk) : (const void*)A, oka ? 16 : 0);
                 const int cc = s_u[row];
                 const bool okb = cc >= 0 && kk < kd;
-                tc::cp_async16(st + kPM * kKC * 2 + off, okb ? (const void*)(BT + (int64_t)cc * kd + kk) : (const void*)BT,
+                tc::cp_async16(st + kSdStageA + off, okb ? (const void*)(BT + (int64_t)cc * kd + kk) : (const void*)BT,
                                okb ? 16 : 0);
             }
             tc::cp_async_commit();
@@ -356,7 +142,7 @@ sddmm_panel_kernel(const int32_t* __restrict__ ro, const T* __restrict__ A, cons
 #pragma unroll
                 for (int kk = 0; kk < kKC / 16; ++kk) {
                     const uint64_t ad = tc::smem_desc_sw128(st + kk * 32, 16, 1024);
-                    const uint64_t bd = tc::smem_desc_sw128(st + kPM * kKC * 2 + kk * 32, 16, 1024);
+                    const uint64_t bd = tc::smem_desc_sw128(st + kSdStageA + kk * 32, 16, 1024);
                     tc::mma_f16(tmem, ad, bd, idesc, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc::mma_commit(smem_u32(&mma_bar[gs % kStages]));
@@ -384,59 +170,60 @@ sddmm_panel_kernel(const int32_t* __restrict__ ro, const T* __restrict__ A, cons
         }
         tc::fence_after_sync();
 
-        // epilogue: TMEM row tid -> padded shared scratch -> the row's entries in this tile
+        // epilogue: TMEM lane tid (panel row tid) -> padded shared scratch -> the row's
+        // entries of this tile, [ts[t], ts[t+1]) by the plan
         float* scratch = reinterpret_cast<float*>(smem);
         const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
 #pragma unroll 1
-        for (int c = 0; c < kSdNT / 32; ++c) {
-            float v[32];
-            tc::tmem_ld32(lane_addr + c * 32, v);
+        for (int c = 0; c < kTileN / 32; ++c) {
+            float x[32];
+            tc::tmem_ld32(lane_addr + c * 32, x);
 #pragma unroll
-            for (int x = 0; x < 32; ++x) scratch[tid * (kSdNT + 1) + c * 32 + x] = v[x];
+            for (int q = 0; q < 32; ++q) scratch[tid * (kTileN + 1) + c * 32 + q] = x[q];
         }
         tc::fence_before_sync();
-        const int i = s_rows[tid];
-        if (i >= 0) {
-            int32_t lo = ro[i], hi = ro[i + 1];
-            while (lo < hi) {  // first entry with upos >= u0
-                const int32_t mid = (lo + hi) >> 1;
-                if ((int)ws.upos[mid] < u0) lo = mid + 1;
-                else hi = mid;
-            }
-            const int32_t k1 = ro[i + 1];
-            for (int32_t k = lo; k < k1; ++k) {
-                const int u = (int)ws.upos[k] - u0;
-                if (u >= ncols) break;
-                const float v = scratch[tid * (kSdNT + 1) + u];
-                if (S == 1) out[k] = Elt<T>::from_f(v);
-                else ws.partial[(int64_t)split * nnz + k] = v;
+        if (s_rows[tid] >= 0) {
+            const int32_t* ts = v.ts + (size_t)(p * kPM + tid) * (kTiles + 1);
+            const int32_t kb = ts[t], ke = ts[t + 1];
+            const float* srow = scratch + tid * (kTileN + 1) - u0;
+#pragma unroll 4
+            for (int32_t k = kb; k < ke; ++k) {
+                const float x = srow[v.upos[k]];
+                if (S == 1) out[k] = Elt<T>::from_f(x);
+                else partial[(int64_t)split * v.nnz + k] = x;
             }
         }
     }
     tc::cp_async_wait<0>();
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tmem, kSdNT);
+    if (warp == 0) tc::tmem_dealloc(tmem, kTileN);
 }
 
-// out[k] = sum over splits, in split order, of the partial sums (dense panels only).
+// out[k] = sum of the split partial sums in split order (dense panels, S > 1 only).
 template <typename T>
 __global__ void __launch_bounds__(256) sddmm_finalize_kernel(const int32_t* __restrict__ ro, T* __restrict__ out,
-                                                             int32_t nnz, int32_t kd, PanelWs ws, int grid_tiles,
-                                                             int max_split) {
-    const int p = blockIdx.x;
-    if (!ws.dense[p]) return;
-    const int nkc = (kd + kKC - 1) / kKC;
-    const int S = choose_split(ws.counts[1], grid_tiles, max_split, nkc);
+                                                             const float* __restrict__ partial, int32_t kd, PlanView v,
+                                                             int grid_tiles, int max_split) {
+    const int p = blockIdx.x / kGroups;
+    if (!v.dense[p]) return;
+    const int S = choose_split(v.counts()[kCntTiles], grid_tiles, max_split, (kd + kKC - 1) / kKC);
     if (S == 1) return;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int r = warp; r < kPM; r += 8) {
-        const int i = ws.prow[p * kPM + r];
+    const int64_t nnz = v.nnz;
+    for (int rr = 0; rr < kGroupRows / 8; ++rr) {
+        const int pos = blockIdx.x * kGroupRows + warp * (kGroupRows / 8) + rr;
+        const int i = v.prow[pos];
         if (i < 0) continue;
-        const int32_t k1 = ro[i + 1];
-        for (int32_t k = ro[i] + lane; k < k1; k += 32) {
-            float s = ws.partial[k];
-            for (int sp = 1; sp < S; ++sp) s += ws.partial[(int64_t)sp * nnz + k];
+        const int32_t k0 = ro[i], k1 = ro[i + 1];
+        for (int32_t k = k0 + lane; k < k1; k += 32) {
+            float x[kMaxSplit];
+#pragma unroll
+            for (int sp = 0; sp < kMaxSplit; ++sp) x[sp] = sp < S ? partial[sp * nnz + k] : 0.f;
+            float s = x[0];
+#pragma unroll
+            for (int sp = 1; sp < kMaxSplit; ++sp)
+                if (sp < S) s += x[sp];
             out[k] = Elt<T>::from_f(s);
         }
     }
@@ -444,35 +231,47 @@ __global__ void __launch_bounds__(256) sddmm_finalize_kernel(const int32_t* __re
 
 // ------------------------------------------------------------------ SpMM dense panels
 
+// The 16 image rows of one row group: zeros, then the group's values at their U position,
+// written out as whole 128-byte-swizzled K-major rows (16-byte stores).
 template <typename T>
 __global__ void __launch_bounds__(256) densify_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro,
-                                                      PanelWs ws) {
-    const int p = blockIdx.x;
-    if (!ws.dense[p]) return;
-    const int4 d = ws.desc[p];
-    const int upad = (d.y + kKC - 1) / kKC * kKC;
-    T* img = static_cast<T*>(ws.img) + d.w;
-    uint4* img4 = reinterpret_cast<uint4*>(img);
-    const int n16 = kPM * upad * 2 / 16;
-    for (int x = threadIdx.x; x < n16; x += 256) img4[x] = make_uint4(0, 0, 0, 0);
+                                                     T* __restrict__ img_base, PlanView v) {
+    __shared__ __align__(16) T stage[kGroupRows][kUCap];
+    const int p = blockIdx.x / kGroups, grp = blockIdx.x % kGroups;
+    if (!v.sp_dense[p]) return;
+    const int nU = v.desc[p].y;
+    const int upad = (nU + kKC - 1) / kKC * kKC;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint4* st4 = reinterpret_cast<uint4*>(&stage[0][0]);
+    const int row_vec = kUCap * (int)sizeof(T) / 16;
+    for (int x = tid; x < kGroupRows * row_vec; x += 256) {
+        if ((x % row_vec) * 16 < upad * (int)sizeof(T)) st4[x] = make_uint4(0, 0, 0, 0);
+    }
     __syncthreads();
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int r = warp; r < kPM; r += 8) {
-        const int i = ws.prow[p * kPM + r];
+    for (int rr = 0; rr < kGroupRows / 8; ++rr) {
+        const int lr = warp * (kGroupRows / 8) + rr;
+        const int i = v.prow[p * kPM + grp * kGroupRows + lr];
         if (i < 0) continue;
         const int32_t k1 = ro[i + 1];
-        for (int32_t k = ro[i] + lane; k < k1; k += 32) {
-            const int u = ws.upos[k];
-            const int chunk = u / kKC, w = u % kKC;
-            const uint32_t byte = tc::sw128_off(r, (w * 2) >> 4) + ((w * 2) & 15);
-            img[(size_t)chunk * (kPM * kKC) + byte / 2] = vals[k];
-        }
+        for (int32_t k = ro[i] + lane; k < k1; k += 32) stage[lr][v.upos[k]] = vals[k];
+    }
+    __syncthreads();
+    T* img = img_base + v.img_slot[p];
+    const int chunks = upad / 8;  // 16-byte chunks per image row
+    for (int x = tid; x < kGroupRows * chunks; x += 256) {
+        const int lr = x / chunks, c = x % chunks;
+        const int r = grp * kGroupRows + lr;           // panel row = image row
+        const int kc = c / 8, w = c % 8;               // 64-column chunk, 16-byte piece in it
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<char*>(img + (size_t)kc * kPM * kKC) +
+                                              tc::sw128_off(r, w));
+        *dst = reinterpret_cast<const uint4*>(&stage[lr][0])[c];
     }
 }
 
 template <typename T>
 __global__ void __launch_bounds__(kTileThreads, 1)
-spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, int32_t N, PanelWs ws, uint32_t idesc, int* err) {
+spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restrict__ img_base, int32_t N, PlanView v,
+                  uint32_t idesc, int* err) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t mma_bar[kStages];
     __shared__ uint32_t tmem_base_sh;
@@ -491,21 +290,20 @@ spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, int32_t N, PanelWs
     tc::fence_after_sync();
     const uint32_t tmem = tmem_base_sh;
 
-    const int D = ws.counts[0];
+    const int D = v.counts()[kCntDenseSp];
     const int ntn = (N + kSpNT - 1) / kSpNT;
     const int64_t units = (int64_t)D * ntn;
     uint32_t g = 0;
     bool failed = false;
 
     for (int64_t unit = blockIdx.x; unit < units && !failed; unit += gridDim.x) {
-        const int p = ws.dlist[unit / ntn];
+        const int p = v.dlist_sp[unit / ntn];
         const int n0 = (int)(unit % ntn) * kSpNT;
-        const int4 d = ws.desc[p];
-        const int nU = d.y;
+        const int nU = v.desc[p].y;
         const int nk = (nU + kKC - 1) / kKC;
-        const T* img = static_cast<const T*>(ws.img) + d.w;
+        const T* img = img_base + v.img_slot[p];
         __syncthreads();
-        for (int x = tid; x < nk * kKC; x += kTileThreads) s_u[x] = x < nU ? ws.ulist[p * kUCap + x] : -1;
+        for (int x = tid; x < nk * kKC; x += kTileThreads) s_u[x] = x < nU ? v.ulist[(size_t)p * kUCap + x] : -1;
         __syncthreads();
 
         auto load = [&](int j, uint32_t gs) {
@@ -574,18 +372,17 @@ spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, int32_t N, PanelWs
         tc::fence_after_sync();
 
         // epilogue: TMEM row tid -> C[row, n0 .. n0 + 256)
-        const int i = ws.prow[p * kPM + tid];
+        const int i = v.prow[p * kPM + tid];
         const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
 #pragma unroll 1
         for (int c = 0; c < kSpNT / 32; ++c) {
-            float v[32];
-            tc::tmem_ld32(lane_addr + c * 32, v);
+            float x[32];
+            tc::tmem_ld32(lane_addr + c * 32, x);
             if (i >= 0) {
                 T* dst = C + (int64_t)i * N + n0 + c * 32;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    if (n0 + c * 32 + q * 8 < N)
-                        *reinterpret_cast<uint4*>(dst + q * 8) = Elt<T>::pack(v + q * 8);
+                    if (n0 + c * 32 + q * 8 < N) *reinterpret_cast<uint4*>(dst + q * 8) = Elt<T>::pack(x + q * 8);
                 }
             }
         }
@@ -599,139 +396,115 @@ spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, int32_t N, PanelWs
 
 // ------------------------------------------------------------------ host dispatch
 
-template <typename I>
-cudaError_t launch_plan(const int32_t* ro, const void* row_idx, const void* col, int32_t m, int32_t ncols,
-                        const PanelWs& w, cudaStream_t s) {
-    const int P = (m + kPM - 1) / kPM;
-    plan_panels_kernel<I><<<P, 256, 0, s>>>(ro, static_cast<const I*>(row_idx), static_cast<const I*>(col), m, ncols,
-                                            w);
-    plan_worklist_kernel<<<1, 1024, 0, s>>>(P, w);
-    count_launches(2);
-    return cudaGetLastError();
-}
-
 template <typename T>
-cudaError_t run_sddmm_panels(int it, const int32_t* ro, const void* row_idx, const void* col, int32_t m, int32_t n,
-                             int32_t kd, int32_t nnz, const void* A, const void* BT, void* out, const PanelWs& w,
-                             int max_split, cudaStream_t s) {
-    cudaError_t e = it == kIdx16 ? launch_plan<uint16_t>(ro, row_idx, col, m, n, w, s)
-                                 : launch_plan<int32_t>(ro, row_idx, col, m, n, w, s);
-    if (e != cudaSuccess) return e;
-    const int P = (m + kPM - 1) / kPM;
-    const int max_items = P * (kUCap / kSdNT);
+cudaError_t run_sddmm_panels(const int32_t* ro, const void* A, const void* BT, void* out, float* partial, int32_t kd,
+                             const PlanView& v, cudaStream_t s) {
+    const int max_split = sddmm_max_split(kd);
+    const int max_items = v.P * kTiles;
     const int grid = (int)min64((int64_t)device_props().sm_count, (int64_t)max_items * max_split);
     auto kern = sddmm_panel_kernel<T>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSdSmem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSdSmem);
     if (e != cudaSuccess) return e;
-    const uint32_t idesc = tc::instr_desc_f16(std::is_same<T, __nv_bfloat16>::value ? 1u : 0u, 0, 0, kPM, kSdNT);
-    kern<<<grid, kTileThreads, kSdSmem, s>>>(ro, static_cast<const T*>(A), static_cast<const T*>(BT),
-                                             static_cast<T*>(out), kd, nnz, w, max_split, idesc,
-                                             device_error_word());
-    sddmm_finalize_kernel<T><<<P, 256, 0, s>>>(ro, static_cast<T*>(out), nnz, kd, w, grid, max_split);
-    count_launches(2);
+    const uint32_t idesc = tc::instr_desc_f16(std::is_same<T, __nv_bfloat16>::value ? 1u : 0u, 0, 0, kPM, kTileN);
+    kern<<<grid, kTileThreads, kSdSmem, s>>>(static_cast<const T*>(A), static_cast<const T*>(BT), static_cast<T*>(out),
+                                             partial, kd, v, max_split, idesc, device_error_word());
+    count_launches(1);
+    if (max_split > 1) {
+        sddmm_finalize_kernel<T><<<v.P * kGroups, 256, 0, s>>>(ro, static_cast<T*>(out), partial, kd, v, grid,
+                                                               max_split);
+        count_launches(1);
+    }
     return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t run_spmm_panels(int it, const void* vals, const int32_t* ro, const void* row_idx, const void* col,
-                            int32_t m, int32_t k, const void* B, int32_t N, void* C, const PanelWs& w,
-                            cudaStream_t s) {
-    cudaError_t e = it == kIdx16 ? launch_plan<uint16_t>(ro, row_idx, col, m, k, w, s)
-                                 : launch_plan<int32_t>(ro, row_idx, col, m, k, w, s);
-    if (e != cudaSuccess) return e;
-    const int P = (m + kPM - 1) / kPM;
-    densify_kernel<T><<<P, 256, 0, s>>>(static_cast<const T*>(vals), ro, w);
+cudaError_t run_spmm_panels(const void* vals, const int32_t* ro, const void* B, int32_t N, void* C, void* img,
+                            const PlanView& v, cudaStream_t s) {
+    densify_kernel<T><<<v.P * kGroups, 256, 0, s>>>(static_cast<const T*>(vals), ro, static_cast<T*>(img), v);
     const int ntn = (N + kSpNT - 1) / kSpNT;
-    const int grid = (int)min64((int64_t)device_props().sm_count, (int64_t)P * ntn);
+    const int grid = (int)min64((int64_t)device_props().sm_count, (int64_t)v.P * ntn);
     auto kern = spmm_panel_kernel<T>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSpSmem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSpSmem);
     if (e != cudaSuccess) return e;
     const uint32_t idesc = tc::instr_desc_f16(std::is_same<T, __nv_bfloat16>::value ? 1u : 0u, 0, 1, kPM, kSpNT);
-    kern<<<grid, kTileThreads, kSpSmem, s>>>(static_cast<const T*>(B), static_cast<T*>(C), N, w, idesc,
-                                             device_error_word());
+    kern<<<grid, kTileThreads, kSpSmem, s>>>(static_cast<const T*>(B), static_cast<T*>(C), static_cast<const T*>(img),
+                                             N, v, idesc, device_error_word());
     count_launches(2);
     return cudaGetLastError();
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-__global__ void __launch_bounds__(1024) panel_stats_kernel(int32_t P, PanelWs ws, int32_t* out) {
-    __shared__ int sh[32];
-    int d = 0, e = 0;
-    for (int p = threadIdx.x; p < P; p += 1024) {
-        const int4 x = ws.desc[p];
-        d += x.x;
-        e += x.x ? x.z : 0;
+size_t image_bytes(int dt, int32_t m, int32_t k, int32_t nnz) {
+    if (!dtype_ok(dt) || !plan_panels_enabled(m, k)) return 0;
+    return align_up(spmm_image_budget_elems(m, nnz) * 2, 1024);
+}
+
+size_t partial_bytes(int dt, int32_t m, int32_t n, int32_t kd, int32_t nnz) {
+    if (!dtype_ok(dt) || !plan_panels_enabled(m, n) || kd <= 0) return 0;
+    const int s = sddmm_max_split(kd);
+    return s > 1 ? align_up((size_t)s * nnz * 4, 1024) : 0;
+}
+
+// The plan to use: the caller's, or one built now at the start of the workspace.
+// Returns the view and advances *ws past the plan if it was built there.
+cudaError_t resolve_plan(int it, const int32_t* ro, const void* row_idx, const void* col, int32_t m, int32_t n,
+                         int32_t nnz, const void* plan, char** ws, PlanView* v, cudaStream_t s) {
+    if (plan) {
+        *v = plan_view(const_cast<void*>(plan), m, n, nnz);
+        return cudaSuccess;
     }
-    int td, te;
-    block_scan_1024(d, sh, &td);
-    block_scan_1024(e, sh, &te);
-    if (threadIdx.x == 0) {
-        out[0] = td;
-        out[1] = te;
-        out[2] = ws.counts[1];
-        out[3] = P;
-    }
+    *v = plan_view(*ws, m, n, nnz);
+    *ws += align_up(plan_bytes(m, n, nnz), 1024);
+    return launch_plan_build(it, ro, row_idx, col, *v, (int64_t)spmm_image_budget_elems(m, nnz), s);
 }
 
 }  // namespace
 
-size_t panel_plan_workspace_bytes(int32_t m, int32_t nnz) { return layout(m, nnz, false, 1, false).total; }
-
-cudaError_t launch_panel_plan(int it, const int32_t* ro, const void* row_idx, const void* col, int32_t m, int32_t n,
-                              int32_t nnz, int32_t* stats, void* ws, cudaStream_t s) {
-    const Layout L = layout(m, nnz, false, 1, false);
-    const PanelWs w = carve(ws, L);
-    cudaError_t e = it == kIdx16 ? launch_plan<uint16_t>(ro, row_idx, col, m, n, w, s)
-                                 : launch_plan<int32_t>(ro, row_idx, col, m, n, w, s);
-    if (e != cudaSuccess) return e;
-    panel_stats_kernel<<<1, 1024, 0, s>>>((m + kPM - 1) / kPM, w, stats);
-    count_launches(1);
-    return cudaGetLastError();
-}
-
-size_t panel_spmm_workspace_bytes(int32_t m, int32_t k, int32_t n, int32_t nnz, int dt, int it) {
-    (void)it;
+size_t spmm_workspace_bytes(int32_t m, int32_t k, int32_t n, int32_t nnz, int dt) {
     (void)n;
-    if (!panels_possible(dt, m, k)) return 0;
-    return layout(m, nnz, false, 1, true).total;
+    return 1024 + align_up(plan_bytes(m, k, nnz), 1024) + image_bytes(dt, m, k, nnz);
 }
 
-size_t panel_sddmm_workspace_bytes(int32_t m, int32_t n, int32_t kd, int32_t nnz, int dt, int it) {
-    (void)it;
-    if (!panels_possible(dt, m, n) || kd <= 0) return 0;
-    return layout(m, nnz, true, sddmm_max_split(nnz, kd), false).total;
+size_t sddmm_workspace_bytes(int32_t m, int32_t n, int32_t kd, int32_t nnz, int dt, bool structure_aware) {
+    return 1024 + align_up(plan_bytes(m, n, nnz), 1024) + (structure_aware ? partial_bytes(dt, m, n, kd, nnz) : 0);
 }
 
 cudaError_t launch_spmm(int dt, int it, const void* vals, const int32_t* ro, const void* row_idx, const void* col,
-                        int32_t m, int32_t k, int32_t nnz, const void* B, int32_t n, void* C, const int32_t* bins,
+                        int32_t m, int32_t k, int32_t nnz, const void* B, int32_t n, void* C, const void* plan,
                         void* ws, bool allow_panels, cudaStream_t s) {
-    const bool panels = allow_panels && nnz > 0 && panels_possible(dt, m, k) && n % 8 == 0 && aligned16(B) &&
-                        aligned16(C);
-    if (!panels) return launch_spmm_general(dt, it, vals, ro, row_idx, col, m, k, B, n, C, bins, nullptr, s);
-    const Layout L = layout(m, nnz, false, 1, true);
-    const PanelWs w = carve(ws, L);
-    cudaError_t e = dt == kF16 ? run_spmm_panels<__half>(it, vals, ro, row_idx, col, m, k, B, n, C, w, s)
-                               : run_spmm_panels<__nv_bfloat16>(it, vals, ro, row_idx, col, m, k, B, n, C, w, s);
+    char* w = reinterpret_cast<char*>(align_up(reinterpret_cast<uintptr_t>(ws), 1024));
+    PlanView v;
+    cudaError_t e = resolve_plan(it, ro, row_idx, col, m, k, nnz, plan, &w, &v, s);
     if (e != cudaSuccess) return e;
-    return launch_spmm_general(dt, it, vals, ro, row_idx, col, m, k, B, n, C, bins, w.dense, s);
+    const bool panels = allow_panels && nnz > 0 && v.panels && dtype_ok(dt) && n % 8 == 0 && aligned16(B) &&
+                        aligned16(C);
+    if (panels) {
+        e = dt == kF16 ? run_spmm_panels<__half>(vals, ro, B, n, C, w, v, s)
+                       : run_spmm_panels<__nv_bfloat16>(vals, ro, B, n, C, w, v, s);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_spmm_general(dt, it, vals, ro, row_idx, col, m, k, B, n, C, v.bins_spmm(),
+                               panels ? v.sp_dense : nullptr, s);
 }
 
 cudaError_t launch_sddmm(int dt, int it, const int32_t* ro, const void* row_idx, const void* col, int32_t m,
                          int32_t n, int32_t kd, int32_t nnz, const void* A, const void* BT, void* out,
-                         bool structure_aware, const int32_t* bins, void* ws, cudaStream_t s) {
-    const bool panels = structure_aware && nnz > 0 && panels_possible(dt, m, n) && kd > 0 && kd % 8 == 0 &&
-                        aligned16(A) && aligned16(BT);
-    if (!panels) return launch_sddmm_general(dt, it, ro, row_idx, col, m, n, kd, A, BT, out, bins, nullptr, s);
-    const int max_split = sddmm_max_split(nnz, kd);
-    const Layout L = layout(m, nnz, true, max_split, false);
-    const PanelWs w = carve(ws, L);
-    cudaError_t e = dt == kF16
-                        ? run_sddmm_panels<__half>(it, ro, row_idx, col, m, n, kd, nnz, A, BT, out, w, max_split, s)
-                        : run_sddmm_panels<__nv_bfloat16>(it, ro, row_idx, col, m, n, kd, nnz, A, BT, out, w,
-                                                          max_split, s);
+                         bool structure_aware, const void* plan, void* ws, cudaStream_t s) {
+    char* w = reinterpret_cast<char*>(align_up(reinterpret_cast<uintptr_t>(ws), 1024));
+    PlanView v;
+    cudaError_t e = resolve_plan(it, ro, row_idx, col, m, n, nnz, plan, &w, &v, s);
     if (e != cudaSuccess) return e;
-    return launch_sddmm_general(dt, it, ro, row_idx, col, m, n, kd, A, BT, out, bins, w.dense, s);
+    const bool panels = structure_aware && nnz > 0 && v.panels && dtype_ok(dt) && kd > 0 && kd % 8 == 0 &&
+                        aligned16(A) && aligned16(BT);
+    if (panels) {
+        float* partial = reinterpret_cast<float*>(w);
+        e = dt == kF16 ? run_sddmm_panels<__half>(ro, A, BT, out, partial, kd, v, s)
+                       : run_sddmm_panels<__nv_bfloat16>(ro, A, BT, out, partial, kd, v, s);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_sddmm_general(dt, it, ro, row_idx, col, m, n, kd, A, BT, out, v.bins_sddmm(),
+                                panels ? v.dense : nullptr, s);
 }
 
 }  // namespace spops

@@ -1,5 +1,5 @@
 // Operator dispatch between the general row kernels and the dense-panel (tensor core)
-// path, and the workspace the panel path needs.
+// path, and the workspace each operator needs.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -8,21 +8,16 @@
 
 namespace spops {
 
-size_t panel_spmm_workspace_bytes(int32_t m, int32_t k, int32_t n, int32_t nnz, int dt, int it);
-size_t panel_sddmm_workspace_bytes(int32_t m, int32_t n, int32_t kd, int32_t nnz, int dt, int it);
+// Workspace of one call when it builds its own plan (a caller plan only lowers the need).
+size_t spmm_workspace_bytes(int32_t m, int32_t k, int32_t n, int32_t nnz, int dt);
+size_t sddmm_workspace_bytes(int32_t m, int32_t n, int32_t kd, int32_t nnz, int dt, bool structure_aware);
 
-// Build the panel plan alone and write {dense panels, entries in dense panels, SDDMM
-// tiles, panels} to stats (device int32[4]). Requires n <= 65536.
-size_t panel_plan_workspace_bytes(int32_t m, int32_t nnz);
-cudaError_t launch_panel_plan(int it, const int32_t* ro, const void* row_idx, const void* col, int32_t m, int32_t n,
-                              int32_t nnz, int32_t* stats, void* ws, cudaStream_t s);
-
-// bins: device int32[4] already written by the row-bins kernel on the same stream.
+// plan: a mask plan built by launch_plan_build for this mask, or nullptr to build one in ws.
 cudaError_t launch_spmm(int dt, int it, const void* vals, const int32_t* ro, const void* row_idx, const void* col,
-                        int32_t m, int32_t k, int32_t nnz, const void* B, int32_t n, void* C, const int32_t* bins,
+                        int32_t m, int32_t k, int32_t nnz, const void* B, int32_t n, void* C, const void* plan,
                         void* ws, bool allow_panels, cudaStream_t s);
 cudaError_t launch_sddmm(int dt, int it, const int32_t* ro, const void* row_idx, const void* col, int32_t m,
                          int32_t n, int32_t kd, int32_t nnz, const void* A, const void* BT, void* out,
-                         bool structure_aware, const int32_t* bins, void* ws, cudaStream_t s);
+                         bool structure_aware, const void* plan, void* ws, cudaStream_t s);
 
 }  // namespace spops

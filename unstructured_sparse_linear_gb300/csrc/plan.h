@@ -1,0 +1,91 @@
+// The mask plan: everything the operators derive from a CSR structure alone (row bins and
+// the dense-panel decomposition), built once per mask and shared by spmm and sddmm.
+//
+// Layout in caller memory (all offsets 1024-byte aligned, computed by plan_layout):
+//   hdr        int32[32]  bins_spmm[4], bins_sddmm[4], counts[8] (kCnt*), dims[4] {m, n, nnz, P}
+//   cta_part   int32[nc][4]   per row-group CTA: {#rows >= spmm long, #rows >= sddmm long,
+//                             #non-empty rows, #entries}; nc = 8 * P (16 positions each)
+// when panels are enabled (n <= 65536):
+//   bm_part    uint32[P][8][W]  column bitmap of each 16-row group of a panel
+//   bm, wbase  [P][W]          OR-ed bitmap; exclusive prefix of its popcounts
+//   desc       int4[P]         {dense, |U|, entries, non-empty rows}
+//   prow       int32[P*128]    row id at each panel position (-1 past m)
+//   ulist      int32[P][kUCap] sorted columns of a dense panel
+//   upos       uint16[nnz]     column position of each entry in its panel's U
+//   ts         int32[P*128][kTiles + 1]  first entry of each 128-column tile of U, per row
+//   dense      uint8[P]        panel runs on tensor cores (SDDMM)
+//   sp_dense   uint8[P]        ... and has a SpMM image slot
+//   items      int32[P*kTiles] SDDMM work items (panel << 8 | tile)
+//   dlist_sp   int32[P]        panels with an image slot
+//   img_slot   int32[P]        image offset (elements) or -1
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace spops {
+
+constexpr int kPM = kPanelRows;   // rows per panel (UMMA M)
+constexpr int kUCap = 1024;       // most distinct columns of a dense panel
+constexpr int kTileN = 128;       // SDDMM tile width over U (UMMA N)
+constexpr int kTiles = kUCap / kTileN;
+constexpr int kGroupRows = 16;    // rows per plan CTA (8 groups per panel)
+constexpr int kGroups = kPM / kGroupRows;
+constexpr int kMaxPanelCols = 65536;
+constexpr int kMinDenseRows = 16;
+
+enum PlanCount {
+    kCntDense = 0,      // dense panels (SDDMM)
+    kCntTiles = 1,      // SDDMM items
+    kCntDenseSp = 2,    // panels with a SpMM image
+    kCntDenseNnz = 3,   // entries in dense panels
+    kCntImgElems = 4,   // image elements assigned
+    kCntPanels = 5,
+};
+
+struct PlanView {
+    int32_t* hdr;
+    int32_t* cta_part;
+    uint32_t* bm_part;
+    uint32_t* bm;
+    int32_t* wbase;
+    int4* desc;
+    int32_t* prow;
+    int32_t* ulist;
+    uint16_t* upos;
+    int32_t* ts;
+    uint8_t* dense;
+    uint8_t* sp_dense;
+    int32_t* items;
+    int32_t* dlist_sp;
+    int32_t* img_slot;
+    int32_t m, n, nnz, P, W, ncta;
+    bool panels;
+    __host__ __device__ int32_t* bins_spmm() const { return hdr; }
+    __host__ __device__ int32_t* bins_sddmm() const { return hdr + 4; }
+    __host__ __device__ int32_t* counts() const { return hdr + 8; }
+};
+
+struct PlanLayout {
+    size_t hdr, cta_part, bm_part, bm, wbase, desc, prow, ulist, upos, ts, dense, sp_dense, items, dlist_sp, img_slot;
+    size_t total;
+};
+
+bool plan_panels_enabled(int32_t m, int32_t n);
+PlanLayout plan_layout(int32_t m, int32_t n, int32_t nnz);
+PlanView plan_view(void* base, int32_t m, int32_t n, int32_t nnz);
+inline size_t plan_bytes(int32_t m, int32_t n, int32_t nnz) { return plan_layout(m, n, nnz).total; }
+
+// Elements of SpMM image storage a workspace provides for this mask (images beyond this
+// budget are not assigned and those panels run on the general kernels).
+size_t spmm_image_budget_elems(int32_t m, int32_t nnz);
+
+// Queue the plan kernels on s. img_budget: SpMM image elements available (0: none).
+cudaError_t launch_plan_build(int it, const int32_t* ro, const void* row_idx, const void* col, const PlanView& v,
+                              int64_t img_budget, cudaStream_t s);
+cudaError_t launch_plan_stats(const PlanView& v, int32_t* out, cudaStream_t s);
+
+}  // namespace spops

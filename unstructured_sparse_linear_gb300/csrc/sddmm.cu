@@ -22,15 +22,30 @@ namespace {
 
 constexpr int kSddmmThreads = 256;
 constexpr int kSddmmWarps = kSddmmThreads / 32;
-constexpr int kNB = 4;
+constexpr int kNB = 8;  // entries per batch: 1 A load + up to 8 BT loads per lane per K step
+
+// Raw operand words: one 16-byte vector (V elements), or one element for the scalar path.
+template <typename T, int V>
+struct Raw {
+    uint4 v;
+};
+template <typename T>
+struct Raw<T, 1> {
+    T v;
+};
 
 template <typename T, int V>
-__device__ __forceinline__ void load_vec(const T* __restrict__ p, float (&f)[V]) {
-    if constexpr (V == 1) {
-        f[0] = Elt<T>::to_f(*p);
-    } else {
-        Elt<T>::unpack(ld_nc_v4(p), f);
-    }
+__device__ __forceinline__ Raw<T, V> load_raw(const T* __restrict__ p) {
+    Raw<T, V> r;
+    if constexpr (V == 1) r.v = *p;
+    else r.v = ld_nc_v4(p);
+    return r;
+}
+
+template <typename T, int V>
+__device__ __forceinline__ void widen(const Raw<T, V>& r, float (&f)[V]) {
+    if constexpr (V == 1) f[0] = Elt<T>::to_f(r.v);
+    else Elt<T>::unpack(r.v, f);
 }
 
 template <typename T, typename I, int V>
@@ -45,18 +60,21 @@ __device__ __forceinline__ void sddmm_batch(int row, int32_t kb, int cnt, const 
     for (int j = 0; j < kNB; ++j) acc[j] = 0.f;
     const T* Arow = A + (int64_t)row * kd;
     for (int32_t t = gl * V; t < kd; t += G * V) {
-        float a[V];
-        load_vec<T, V>(Arow + t, a);
-        float b[kNB][V];
+        // all loads of the step first (packed), then widen and multiply
+        const Raw<T, V> ar = load_raw<T, V>(Arow + t);
+        Raw<T, V> br[kNB];
 #pragma unroll
-        for (int j = 0; j < kNB; ++j) {
-            if (j < cnt) load_vec<T, V>(BT + (int64_t)c[j] * kd + t, b[j]);
-        }
+        for (int j = 0; j < kNB; ++j)
+            if (j < cnt) br[j] = load_raw<T, V>(BT + (int64_t)c[j] * kd + t);
+        float a[V];
+        widen<T, V>(ar, a);
 #pragma unroll
         for (int j = 0; j < kNB; ++j) {
             if (j < cnt) {
+                float b[V];
+                widen<T, V>(br[j], b);
 #pragma unroll
-                for (int e = 0; e < V; ++e) acc[j] = fmaf(a[e], b[j][e], acc[j]);
+                for (int e = 0; e < V; ++e) acc[j] = fmaf(a[e], b[e], acc[j]);
             }
         }
     }

@@ -43,20 +43,21 @@ __device__ __forceinline__ void load_b(const T* __restrict__ Brow, int col0, int
 template <typename T, int V>
 __device__ __forceinline__ void accumulate(float (&acc)[V], int cj, float vj, int cnt, const T* __restrict__ B,
                                            int N, int col0, unsigned mask, int src0) {
+    constexpr int U = V == 1 ? 8 : 32 / V;  // B rows gathered before their FMAs (8 for 16-bit, 4 for fp32)
     int j = 0;
-    for (; j + 4 <= cnt; j += 4) {
-        int c[4];
-        float v[4];
+    for (; j + U <= cnt; j += U) {
+        int c[U];
+        float v[U];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < U; ++u) {
             c[u] = __shfl_sync(mask, cj, src0 + j + u);
             v[u] = __shfl_sync(mask, vj, src0 + j + u);
         }
-        float b[4][V];
+        float b[U][V];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) load_b<T, V>(B + (int64_t)c[u] * N, col0, N, b[u]);
+        for (int u = 0; u < U; ++u) load_b<T, V>(B + (int64_t)c[u] * N, col0, N, b[u]);
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < U; ++u)
 #pragma unroll
             for (int e = 0; e < V; ++e) acc[e] = fmaf(v[u], b[u][e], acc[e]);
     }
