@@ -30,16 +30,16 @@ namespace spops {
 namespace {
 
 constexpr int kKC = 64;       // K elements per pipeline chunk (128 bytes of 16-bit data)
-constexpr int kStages = 4;
-constexpr int kSpNT = 256;    // SpMM: columns of C per tile (UMMA N)
+constexpr int kStages = 6;
+constexpr int kSpNT = 128;    // SpMM: columns of C per tile (UMMA N)
 constexpr int kMaxSplit = 4;
 constexpr int kTileThreads = 128;
 
 constexpr uint32_t kSdStageA = kPM * kKC * 2;                 // 16 KB
 constexpr uint32_t kSdStageBytes = kSdStageA + kTileN * kKC * 2;  // A + BT tiles: 32 KB
 constexpr uint32_t kSpStageA = kPM * kKC * 2;                 // 16 KB
-constexpr uint32_t kSpStageB = kSpNT * kKC * 2;               // 32 KB
-constexpr uint32_t kSpStageBytes = kSpStageA + kSpStageB;     // 48 KB
+constexpr uint32_t kSpStageB = kSpNT * kKC * 2;               // 16 KB
+constexpr uint32_t kSpStageBytes = kSpStageA + kSpStageB;     // 32 KB
 constexpr uint32_t kSdSmem = kStages * kSdStageBytes + 1024;
 constexpr uint32_t kSpSmem = kStages * kSpStageBytes + 1024;
 
@@ -170,8 +170,9 @@ sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
         }
         tc::fence_after_sync();
 
-        // epilogue: TMEM lane tid (panel row tid) -> padded shared scratch -> the row's
-        // entries of this tile, [ts[t], ts[t+1]) by the plan
+        // epilogue: TMEM lane tid (panel row tid) -> padded shared scratch; then each warp
+        // takes whole rows and its lanes walk the row's entries of this tile,
+        // [ts[t], ts[t+1]) by the plan, so entry loads and output stores are coalesced
         float* scratch = reinterpret_cast<float*>(smem);
         const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
 #pragma unroll 1
@@ -182,12 +183,14 @@ sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
             for (int q = 0; q < 32; ++q) scratch[tid * (kTileN + 1) + c * 32 + q] = x[q];
         }
         tc::fence_before_sync();
-        if (s_rows[tid] >= 0) {
-            const int32_t* ts = v.ts + (size_t)(p * kPM + tid) * (kTiles + 1);
+        __syncthreads();
+        const int lane = tid & 31;
+        for (int r = warp; r < kPM; r += kTileThreads / 32) {
+            if (s_rows[r] < 0) continue;
+            const int32_t* ts = v.ts + (size_t)(p * kPM + r) * (kTiles + 1);
             const int32_t kb = ts[t], ke = ts[t + 1];
-            const float* srow = scratch + tid * (kTileN + 1) - u0;
-#pragma unroll 4
-            for (int32_t k = kb; k < ke; ++k) {
+            const float* srow = scratch + r * (kTileN + 1) - u0;
+            for (int32_t k = kb + lane; k < ke; k += 32) {
                 const float x = srow[v.upos[k]];
                 if (S == 1) out[k] = Elt<T>::from_f(x);
                 else partial[(int64_t)split * v.nnz + k] = x;
@@ -201,31 +204,30 @@ sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
 }
 
 // out[k] = sum of the split partial sums in split order (dense panels, S > 1 only).
+// One CTA per panel row, so even a few dense panels spread over many SMs.
+constexpr int kFinalizeThreads = 128;
+
 template <typename T>
-__global__ void __launch_bounds__(256) sddmm_finalize_kernel(const int32_t* __restrict__ ro, T* __restrict__ out,
-                                                             const float* __restrict__ partial, int32_t kd, PlanView v,
-                                                             int grid_tiles, int max_split) {
-    const int p = blockIdx.x / kGroups;
-    if (!v.dense[p]) return;
+__global__ void __launch_bounds__(kFinalizeThreads)
+sddmm_finalize_kernel(const int32_t* __restrict__ ro, T* __restrict__ out, const float* __restrict__ partial,
+                      int32_t kd, PlanView v, int grid_tiles, int max_split) {
+    const int pos = blockIdx.x;
+    if (!v.dense[pos / kPM]) return;
+    const int i = v.prow[pos];
+    if (i < 0) return;
     const int S = choose_split(v.counts()[kCntTiles], grid_tiles, max_split, (kd + kKC - 1) / kKC);
     if (S == 1) return;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t nnz = v.nnz;
-    for (int rr = 0; rr < kGroupRows / 8; ++rr) {
-        const int pos = blockIdx.x * kGroupRows + warp * (kGroupRows / 8) + rr;
-        const int i = v.prow[pos];
-        if (i < 0) continue;
-        const int32_t k0 = ro[i], k1 = ro[i + 1];
-        for (int32_t k = k0 + lane; k < k1; k += 32) {
-            float x[kMaxSplit];
+    const int32_t k1 = ro[i + 1];
+    for (int32_t k = ro[i] + threadIdx.x; k < k1; k += kFinalizeThreads) {
+        float x[kMaxSplit];
 #pragma unroll
-            for (int sp = 0; sp < kMaxSplit; ++sp) x[sp] = sp < S ? partial[sp * nnz + k] : 0.f;
-            float s = x[0];
+        for (int sp = 0; sp < kMaxSplit; ++sp) x[sp] = sp < S ? partial[sp * nnz + k] : 0.f;
+        float s = x[0];
 #pragma unroll
-            for (int sp = 1; sp < kMaxSplit; ++sp)
-                if (sp < S) s += x[sp];
-            out[k] = Elt<T>::from_f(s);
-        }
+        for (int sp = 1; sp < kMaxSplit; ++sp)
+            if (sp < S) s += x[sp];
+        out[k] = Elt<T>::from_f(s);
     }
 }
 
@@ -314,10 +316,12 @@ spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restric
                 const int c = tid + kTileThreads * q;
                 tc::cp_async16(st + c * 16, src_a + c * 16, 16);
             }
+            // B[U rows j*64 .. +64, n0 .. n0 + kSpNT): kSpNT / 8 sixteen-byte pieces per row
+            constexpr int kPieces = kSpNT / 8;
 #pragma unroll
-            for (int q = 0; q < 16; ++q) {
+            for (int q = 0; q < kKC * kPieces / kTileThreads; ++q) {
                 const int c = tid + kTileThreads * q;
-                const int kk = c >> 5, nch = c & 31;
+                const int kk = c / kPieces, nch = c % kPieces;
                 const int u = s_u[j * kKC + kk];
                 const int ncol = n0 + nch * 8;
                 const bool ok = u >= 0 && ncol < N;
@@ -410,8 +414,8 @@ cudaError_t run_sddmm_panels(const int32_t* ro, const void* A, const void* BT, v
                                              partial, kd, v, max_split, idesc, device_error_word());
     count_launches(1);
     if (max_split > 1) {
-        sddmm_finalize_kernel<T><<<v.P * kGroups, 256, 0, s>>>(ro, static_cast<T*>(out), partial, kd, v, grid,
-                                                               max_split);
+        sddmm_finalize_kernel<T><<<v.P * kPM, kFinalizeThreads, 0, s>>>(ro, static_cast<T*>(out), partial, kd, v,
+                                                                        grid, max_split);
         count_launches(1);
     }
     return cudaGetLastError();

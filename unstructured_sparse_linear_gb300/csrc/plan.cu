@@ -11,8 +11,8 @@
 //     entries fill at least a quarter of (non-empty rows) x |U|. Dense panels run on the
 //     tensor cores as 128 x |U| tiles.
 // Four kernels, none with a serial per-thread loop over a panel:
-//   1. row groups (16 rows per CTA): row ids per position, per-group counts, and a column
-//      bitmap per 16-row group built with shared-memory atomics (no global atomics, no
+//   1. row groups (8 rows per CTA): row ids per position, per-group counts, and a column
+//      bitmap per 8-row group built with shared-memory atomics (no global atomics, no
 //      zeroing of caller memory needed);
 //   2. panels: OR the 8 group bitmaps, prefix-sum their popcounts, list U, decide density;
 //   3. one CTA: sum the group counts into row bins, list dense panels and SDDMM tiles, and

@@ -4,9 +4,9 @@
 // Layout in caller memory (all offsets 1024-byte aligned, computed by plan_layout):
 //   hdr        int32[32]  bins_spmm[4], bins_sddmm[4], counts[8] (kCnt*), dims[4] {m, n, nnz, P}
 //   cta_part   int32[nc][4]   per row-group CTA: {#rows >= spmm long, #rows >= sddmm long,
-//                             #non-empty rows, #entries}; nc = 8 * P (16 positions each)
+//                             #non-empty rows, #entries}; nc = 16 * P (8 positions each)
 // when panels are enabled (n <= 65536):
-//   bm_part    uint32[P][8][W]  column bitmap of each 16-row group of a panel
+//   bm_part    uint32[P][16][W] column bitmap of each 8-row group of a panel
 //   bm, wbase  [P][W]          OR-ed bitmap; exclusive prefix of its popcounts
 //   desc       int4[P]         {dense, |U|, entries, non-empty rows}
 //   prow       int32[P*128]    row id at each panel position (-1 past m)
@@ -32,7 +32,7 @@ constexpr int kPM = kPanelRows;   // rows per panel (UMMA M)
 constexpr int kUCap = 1024;       // most distinct columns of a dense panel
 constexpr int kTileN = 128;       // SDDMM tile width over U (UMMA N)
 constexpr int kTiles = kUCap / kTileN;
-constexpr int kGroupRows = 16;    // rows per plan CTA (8 groups per panel)
+constexpr int kGroupRows = 8;     // rows per plan CTA, one per warp (16 groups per panel)
 constexpr int kGroups = kPM / kGroupRows;
 constexpr int kMaxPanelCols = 65536;
 constexpr int kMinDenseRows = 16;

@@ -117,6 +117,102 @@ radix_scatter_kernel(const int32_t* __restrict__ ro, const uint32_t* __restrict_
     }
 }
 
+// One CTA sorts up to kSmallSortRows rows in shared memory: the key is (longest row -
+// nnz_i), so the number of 8-bit passes follows the actual key width (0 passes when all
+// rows have equal length). Same stable LSD radix scheme as the multi-CTA path.
+constexpr int kSmallSortRows = 16384;
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallWarps = kSmallThreads / 32;
+constexpr size_t kSmallSortSmem = 2 * kSmallSortRows * 2 + kSmallWarps * kRadix * 4;
+
+template <typename OutI>
+__global__ void __launch_bounds__(kSmallThreads) sort_small_kernel(const int32_t* __restrict__ ro, int32_t m,
+                                                                   OutI* __restrict__ out) {
+    extern __shared__ __align__(16) unsigned char sm[];
+    uint16_t* va = reinterpret_cast<uint16_t*>(sm);
+    uint16_t* vb = va + kSmallSortRows;
+    uint32_t(*wcnt)[kRadix] = reinterpret_cast<uint32_t(*)[kRadix]>(vb + kSmallSortRows);
+    __shared__ uint32_t hist[kRadix], base[kRadix], running[kRadix];
+    __shared__ int32_t red[kSmallWarps];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t lt_mask = (1u << lane) - 1u;
+
+    int32_t mx = 0;
+    for (int32_t i = tid; i < m; i += kSmallThreads) {
+        va[i] = (uint16_t)i;
+        mx = max(mx, ro[i + 1] - ro[i]);
+    }
+    for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    mx = 0;
+    for (int w = 0; w < kSmallWarps; ++w) mx = max(mx, red[w]);
+    const uint32_t key_base = (uint32_t)mx;
+    int bits = 0;
+    while (bits < 32 && (key_base >> bits) != 0) ++bits;
+    const int passes = (bits + 7) / 8;
+    auto digit = [&](uint32_t v, int shift) {
+        return (int)(((key_base - (uint32_t)(ro[v + 1] - ro[v])) >> shift) & (kRadix - 1));
+    };
+    for (int p = 0; p < passes; ++p) {
+        const int shift = 8 * p;
+        if (tid < kRadix) hist[tid] = 0;
+        __syncthreads();
+        for (int32_t i = tid; i < m; i += kSmallThreads) atomicAdd(&hist[digit(va[i], shift)], 1u);
+        __syncthreads();
+        if (warp == 0) {  // exclusive scan of 256 counters by one warp (8 per lane)
+            uint32_t c[8], s = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                c[q] = hist[lane * 8 + q];
+                s += c[q];
+            }
+            uint32_t x = s;
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            uint32_t run = x - s;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                base[lane * 8 + q] = run;
+                running[lane * 8 + q] = 0;
+                run += c[q];
+            }
+        }
+        __syncthreads();
+        for (int32_t r0 = 0; r0 < m; r0 += kSmallThreads) {
+#pragma unroll
+            for (int q = 0; q < kRadix / 32; ++q) wcnt[warp][lane + 32 * q] = 0;
+            __syncwarp();
+            const int32_t i = r0 + tid;
+            const bool valid = i < m;
+            const uint16_t v = valid ? va[i] : 0;
+            const int d = valid ? digit(v, shift) : kRadix + lane;
+            const uint32_t peers = __match_any_sync(0xffffffffu, d);
+            const uint32_t rank = __popc(peers & lt_mask);
+            if (valid && lane == __ffs(peers) - 1) wcnt[warp][d] = __popc(peers);
+            __syncthreads();
+            if (tid < kRadix) {
+                uint32_t acc = running[tid];
+                for (int w = 0; w < kSmallWarps; ++w) {
+                    const uint32_t c = wcnt[w][tid];
+                    wcnt[w][tid] = acc;
+                    acc += c;
+                }
+                running[tid] = acc;
+            }
+            __syncthreads();
+            if (valid) vb[base[d] + wcnt[warp][d] + rank] = v;
+            __syncthreads();
+        }
+        uint16_t* t = va;
+        va = vb;
+        vb = t;
+    }
+    for (int32_t i = tid; i < m; i += kSmallThreads) out[i] = static_cast<OutI>(va[i]);
+}
+
 template <typename OutI>
 __global__ void iota_kernel(OutI* out, int32_t m) {
     for (int32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < m; i += gridDim.x * blockDim.x)
@@ -215,6 +311,20 @@ size_t sort_rows_workspace_bytes(int32_t m) {
 cudaError_t launch_sort_rows(const int32_t* ro, int32_t m, int32_t nnz, void* row_idx_out, int it, void* ws,
                              cudaStream_t s) {
     if (m == 0) return cudaSuccess;
+    if (m <= kSmallSortRows) {
+        cudaError_t e = it == kIdx16
+                            ? cudaFuncSetAttribute(sort_small_kernel<uint16_t>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmallSortSmem)
+                            : cudaFuncSetAttribute(sort_small_kernel<int32_t>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmallSortSmem);
+        if (e != cudaSuccess) return e;
+        if (it == kIdx16)
+            sort_small_kernel<uint16_t><<<1, kSmallThreads, kSmallSortSmem, s>>>(ro, m, (uint16_t*)row_idx_out);
+        else
+            sort_small_kernel<int32_t><<<1, kSmallThreads, kSmallSortSmem, s>>>(ro, m, (int32_t*)row_idx_out);
+        count_launches(1);
+        return cudaGetLastError();
+    }
     int bits = 0;
     while (bits < 32 && ((uint64_t)nnz >> bits) != 0) ++bits;  // keys lie in [0, nnz]
     const int passes = (bits + 7) / 8;
