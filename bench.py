@@ -1,12 +1,14 @@
 """Benchmark of the CSR sparse-adapter hot path on GB300.
 
-One step = one pass of the whole path over the RoSA-adapter workload (4096 x 4096 fp16
-weight, 1 % density clustered in 10 % of rows and columns, 2048 tokens):
-  sort_rows (row_idx from row_offsets) -> spmm (C = A X, the row bins computed inside)
-  -> sddmm (structure-aware backend, grad = dY^T X sampled on the mask) -> csr_add (W + A).
-metric: GFLOP/s counting 2 * nnz * N for SpMM and 2 * nnz * kd for SDDMM (csr_add adds no
-flops; its time is in the step). Each step is a CUDA-graph replay of the library calls;
-L2 is flushed (a 256 MB write) before every timed step, outside the step's events.
+One step = one pass of the whole path over one workload (default: the RoSA adapter, a
+4096 x 4096 fp16 weight, 1 % density clustered in 10 % of rows and columns, 2048 tokens):
+  sort_rows (row_idx) -> plan_build (row bins + dense panels, shared by both products)
+  -> spmm (C = A X) -> sddmm (structure-aware backend, grad = dY^T X sampled on the mask)
+  -> csr_add (W + A)
+(operators the workload does not define are left out). metric: GFLOP/s counting
+2 * nnz * N for SpMM and 2 * nnz * kd for SDDMM; every operator's time is in the step.
+Each operator is a CUDA-graph replay of the library calls; L2 is flushed (a 256 MB write)
+before every timed step, outside the step's events.
 
 --impl reference times the fp64 CPU oracle on the host cores on the same workload, metric
 and unit (a deliberately slow baseline, not a target).
@@ -31,8 +33,15 @@ sys.path.insert(0, ROOT)
 
 import workloads as wl  # noqa: E402
 
-WORKLOAD = "rosa"
 L2_FLUSH_BYTES = 256 << 20
+METRIC = "SpMM+SDDMM GFLOP/s (2*nnz*N + 2*nnz*kd per step; step = sort_rows+plan+spmm+sddmm+csr_add)"
+DESCRIPTION = {
+    "tiny": "tiny_256x256_fp32_5pct_uniform_N64",
+    "rosa": "rosa_adapter_4096x4096_fp16_1pct_clustered_2048tok",
+    "llama_mlp": "llama_mlp_11008x4096_bf16_0.5pct_uniform_4096tok",
+    "zipf": "zipf_131072x131072_fp32_band8192_N128",
+    "butterfly": "pixelfly_butterfly_8192x2048_bf16_64x64blocks_8192tok",
+}
 
 
 def log(*a):
@@ -54,6 +63,10 @@ def peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
+def index_dtype(w):
+    return torch.int16 if max(w.m, w.n) <= 32768 else torch.int32
+
+
 # ------------------------------------------------------------------ work accounting
 
 
@@ -68,20 +81,22 @@ def accounting(w):
     active_rows = int((lens > 0).sum())
     active_cols = int(np.unique(col).size)
     csr_bytes = nnz * (b + ib) + 4 * (m + 1) + ib * m
-    acc = {}
+    acc = {"sort_rows": {"flops": 0, "bytes": 4 * (m + 1) + ib * m},
+           "plan": {"flops": 0, "bytes": 4 * (m + 1) + ib * m + nnz * ib}}
     if w.B is not None:
         N = w.B.shape[1]
-        acc["spmm"] = {"flops": 2 * nnz * N,
-                       "bytes": csr_bytes + active_cols * N * b + m * N * b}
+        acc["spmm"] = {"flops": 2 * nnz * N, "bytes": csr_bytes + active_cols * N * b + m * N * b}
     if w.A is not None:
         kd = w.A.shape[1]
         acc["sddmm"] = {"flops": 2 * nnz * kd,
                         "bytes": csr_bytes - nnz * b + active_rows * kd * b + active_cols * kd * b + nnz * b}
     if w.W is not None:
         acc["csr_add"] = {"flops": nnz, "bytes": csr_bytes - ib * m + 2 * m * n * b}
-    acc["sort_rows"] = {"flops": 0, "bytes": 4 * (m + 1) + ib * m}
-    acc["plan"] = {"flops": 0, "bytes": 4 * (m + 1) + ib * m + nnz * ib + nnz * 2}
     return acc
+
+
+def step_flops(acc):
+    return acc.get("spmm", {}).get("flops", 0) + acc.get("sddmm", {}).get("flops", 0)
 
 
 # ------------------------------------------------------------------ clocks
@@ -147,25 +162,53 @@ def kernel_source_hash(path):
     return hashlib.sha256(open(os.path.join(ROOT, path), "rb").read()).hexdigest()[:16]
 
 
-def recorded_traffic(op: str):
-    """Per-launch DRAM bytes of the op's kernel from the committed ncu summary, if the
-    kernel source still matches the hash recorded with the counters."""
+def recorded_traffic(op: str, workload: str):
+    """Per-launch DRAM bytes of the op's main kernel on this workload from the committed
+    ncu summary, if the kernel source still matches the hash recorded with the counters."""
     p = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(p):
         return None
+    pat = re.compile(r"\|\s*" + re.escape(workload) + r"\s*\|\s*" + re.escape(op) +
+                     r"\s*\|\s*([\w./]+)\s*\|\s*([0-9a-f]+)\s*\|\s*([0-9]+)\s*\|")
     for line in open(p):
-        m = re.match(r"\|\s*" + re.escape(op) + r"\s*\|\s*([\w./]+)\s*\|\s*([0-9a-f]+)\s*\|\s*([0-9]+)\s*\|", line)
-        if m:
-            src, h, traffic = m.group(1), m.group(2), int(m.group(3))
+        mt = pat.match(line)
+        if mt:
+            src, h, traffic = mt.group(1), mt.group(2), int(mt.group(3))
             try:
-                if kernel_source_hash(src) == h:
-                    return traffic
+                return traffic if kernel_source_hash(src) == h else None
             except OSError:
                 return None
     return None
 
 
 # ------------------------------------------------------------------ GPU arm
+
+
+def make_ops(sp, w, d, idx, args, outs):
+    """The step as a list of (name, callable) over device tensors d."""
+    ops = [("sort_rows", lambda: outs.__setitem__("row_idx", sp.sort_rows(d["ro"], nnz=w.nnz, index_dtype=idx))),
+           ("plan", lambda: outs.__setitem__("plan", sp.plan_build(d["ro"], outs["row_idx"], d["col"], w.n)))]
+    if "B" in d:
+        ops.append(("spmm", lambda: outs.__setitem__(
+            "C", sp.spmm(d["val"], d["ro"], outs["row_idx"], d["col"], d["B"], w.m, path=args.spmm_path,
+                         plan=outs["plan"]))))
+    if "A" in d:
+        ops.append(("sddmm", lambda: outs.__setitem__(
+            "G", sp.sddmm(d["ro"], outs["row_idx"], d["col"], d["A"], d["BT"], backend=args.sddmm_backend,
+                          plan=outs["plan"]))))
+    if "W" in d:
+        ops.append(("csr_add", lambda: outs.__setitem__(
+            "D", sp.csr_add(d["val"], d["ro"], outs["row_idx"], d["col"], d["W"]))))
+    return ops
+
+
+def host_inputs(w, idx):
+    h = {"ro": w.row_offsets, "col": w.col_idx.to(idx), "val": w.values}
+    for k in ("B", "A", "BT", "W"):
+        t = getattr(w, k)
+        if t is not None:
+            h[k] = t
+    return h
 
 
 def run_gpu(args):
@@ -179,38 +222,14 @@ def run_gpu(args):
     if ws > 1:
         dist.init_process_group("nccl", device_id=dev)
 
-    w = wl.generate(WORKLOAD)
+    w = wl.generate(args.workload)
     acc = accounting(w)
-    N, kd = w.B.shape[1], w.A.shape[1]
-    step_flops = acc["spmm"]["flops"] + acc["sddmm"]["flops"]
-    idx = torch.int16
-
-    # device-resident inputs
-    ro = w.row_offsets.to(dev)
-    col = w.col_idx.to(idx).to(dev)
-    val = w.values.to(dev)
-    B, A, BT, W = (t.to(dev) for t in (w.B, w.A, w.BT, w.W))
-    nnz, m = w.nnz, w.m
+    flops = step_flops(acc)
+    idx = index_dtype(w)
+    d = {k: v.to(dev) for k, v in host_inputs(w, idx).items()}
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-
     outs = {}
-
-    def op_sort():
-        outs["row_idx"] = sp.sort_rows(ro, nnz=nnz, index_dtype=idx)
-
-    def op_plan():
-        outs["plan"] = sp.plan_build(ro, outs["row_idx"], col, w.n)
-
-    def op_spmm():
-        outs["C"] = sp.spmm(val, ro, outs["row_idx"], col, B, m, path=args.spmm_path, plan=outs["plan"])
-
-    def op_sddmm():
-        outs["G"] = sp.sddmm(ro, outs["row_idx"], col, A, BT, backend=args.sddmm_backend, plan=outs["plan"])
-
-    def op_add():
-        outs["D"] = sp.csr_add(val, ro, outs["row_idx"], col, W)
-
-    ops = [("sort_rows", op_sort), ("plan", op_plan), ("spmm", op_spmm), ("sddmm", op_sddmm), ("csr_add", op_add)]
+    ops = make_ops(sp, w, d, idx, args, outs)
 
     stream = torch.cuda.Stream(device=dev)
     with torch.cuda.stream(stream):
@@ -262,10 +281,9 @@ def run_gpu(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         total_ms = float(t.item())
     ms_per_step = total_ms / args.steps
-    value = ws * step_flops * args.steps / (total_ms * 1e-3) / 1e9
+    value = ws * flops * args.steps / (total_ms * 1e-3) / 1e9
 
-    # ---- end to end through the public API with host buffers
-    e2e = run_e2e(sp, w, dev, idx, args, step_flops, ws)
+    e2e = run_e2e(sp, w, dev, idx, args, flops, ws)
 
     pk = peaks()
     per_op = {}
@@ -281,23 +299,25 @@ def run_gpu(args):
     achieved = acc[dominant]["bytes"] / dom_t / 1e9
     roofline = {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
-                "traffic": recorded_traffic(dominant), "algorithmic_bytes": acc[dominant]["bytes"],
-                "peak_source": pk["source"]}
+                "traffic": recorded_traffic(dominant, args.workload), "algorithmic_bytes": acc[dominant]["bytes"],
+                "peak_source": pk["source"],
+                "note": "achieved = algorithmic bytes of the op / its mean event time in the timed loop"}
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, acc, steps=args.cpu_steps)
+        cpu = cpu_baseline(w, acc, seconds=args.cpu_seconds)
 
     line = {
-        "metric": "SpMM+SDDMM GFLOP/s (2*nnz*N + 2*nnz*kd per step; step = sort_rows+spmm+sddmm+csr_add)",
-        "value": round(value, 2), "unit": "GFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f16", "data": "synthetic (seeded; RoSA-adapter mask recipe)",
-        "config": {"workload": "rosa_adapter_4096x4096_fp16_1pct_clustered_2048tok", "m": m, "n": w.n, "nnz": nnz,
-                   "N": N, "kd": kd, "index": "int16", "sddmm_backend": args.sddmm_backend,
+        "metric": METRIC, "value": round(value, 2), "unit": "GFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded; workload recipes in DESIGN.md)",
+        "config": {"workload": DESCRIPTION[args.workload], "m": w.m, "n": w.n, "nnz": w.nnz,
+                   "N": int(w.B.shape[1]) if w.B is not None else None,
+                   "kd": int(w.A.shape[1]) if w.A is not None else None,
+                   "index": str(idx).replace("torch.", ""), "sddmm_backend": args.sddmm_backend,
                    "spmm_path": args.spmm_path,
                    "l2": "flushed before every step (256 MB write, outside step events)",
-                   "parallelism": f"replicas x{ws} (independent adapters per GPU)"},
+                   "parallelism": f"replicas x{ws} (independent problems per GPU)"},
         "per_op": per_op, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": int(launches_per_step) * args.steps, "clocks": clocks,
         "wall_s_timed_region": round(wall, 4),
@@ -308,29 +328,28 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
-def run_e2e(sp, w, dev, idx, args, step_flops, ws):
+def run_e2e(sp, w, dev, idx, args, flops, ws):
     """Same metric through the public calls, with inputs copied from pinned host memory
     and the results copied back inside every timed step."""
-    host = {"ro": w.row_offsets, "col": w.col_idx.to(idx), "val": w.values, "B": w.B, "A": w.A, "BT": w.BT,
-            "W": w.W}
-    host = {k: v.contiguous().pin_memory() for k, v in host.items()}
+    host = {k: v.contiguous().pin_memory() for k, v in host_inputs(w, idx).items()}
     h2d = sum(v.numel() * v.element_size() for v in host.values())
-    res_h = {"C": torch.empty((w.m, w.B.shape[1]), dtype=w.B.dtype).pin_memory(),
-             "G": torch.empty(w.nnz, dtype=w.B.dtype).pin_memory(),
-             "D": torch.empty((w.m, w.n), dtype=w.B.dtype).pin_memory()}
-    d2h = sum(v.numel() * v.element_size() for v in res_h.values())
+    res = {}
+    if w.B is not None:
+        res["C"] = torch.empty((w.m, w.B.shape[1]), dtype=w.values.dtype).pin_memory()
+    if w.A is not None:
+        res["G"] = torch.empty(w.nnz, dtype=w.values.dtype).pin_memory()
+    if w.W is not None:
+        res["D"] = torch.empty((w.m, w.n), dtype=w.values.dtype).pin_memory()
+    d2h = sum(v.numel() * v.element_size() for v in res.values())
     stream = torch.cuda.current_stream(dev)
 
     def step():
         d = {k: v.to(dev, non_blocking=True) for k, v in host.items()}
-        ri = sp.sort_rows(d["ro"], nnz=w.nnz, index_dtype=idx)
-        plan = sp.plan_build(d["ro"], ri, d["col"], w.n)
-        C = sp.spmm(d["val"], d["ro"], ri, d["col"], d["B"], w.m, path=args.spmm_path, plan=plan)
-        G = sp.sddmm(d["ro"], ri, d["col"], d["A"], d["BT"], backend=args.sddmm_backend, plan=plan)
-        D = sp.csr_add(d["val"], d["ro"], ri, d["col"], d["W"])
-        res_h["C"].copy_(C, non_blocking=True)
-        res_h["G"].copy_(G, non_blocking=True)
-        res_h["D"].copy_(D, non_blocking=True)
+        outs = {}
+        for _, f in make_ops(sp, w, d, idx, args, outs):
+            f()
+        for k, t in res.items():
+            t.copy_(outs[k], non_blocking=True)
 
     for _ in range(max(2, args.warmup)):
         step()
@@ -343,35 +362,60 @@ def run_e2e(sp, w, dev, idx, args, step_flops, ws):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     ms = e0.elapsed_time(e1) / steps
-    return {"value": round(ws * step_flops / (ms * 1e-3) / 1e9, 2), "unit": "GFLOP/s", "ms_per_step": round(ms, 4),
+    return {"value": round(ws * flops / (ms * 1e-3) / 1e9, 2), "unit": "GFLOP/s", "ms_per_step": round(ms, 4),
             "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
 # ------------------------------------------------------------------ CPU oracle
 
 
-def _oracle_step(o, w, ro, col, vals64, B64, A64, BT64, W64):
-    o.sort_rows(ro)
-    o.spmm(ro, col, vals64, B64)
-    o.sddmm(ro, col, A64, BT64)
-    o.csr_add(ro, col, vals64, W64)
+class OracleStep:
+    """The step on the fp64 oracle, on all rows or on a row sample (bounded CPU time)."""
+
+    def __init__(self, w, acc, target_gflop: float):
+        import oracle as o
+        o.build()
+        self.o = o
+        self.w = w
+        self.ro, self.col = w.row_offsets.numpy(), w.col_idx.numpy()
+        self.vals = w.values.double().numpy()
+        self.dense = {k: getattr(w, k).double().numpy() for k in ("B", "A", "BT", "W") if getattr(w, k) is not None}
+        lens = np.diff(self.ro)
+        per_row = 2 * lens * ((w.B.shape[1] if w.B is not None else 0) + (w.A.shape[1] if w.A is not None else 0))
+        total = float(per_row.sum())
+        if total <= target_gflop * 1e9:
+            self.rows = None
+            self.flops = step_flops(acc)
+            self.sample = "full workload"
+        else:
+            frac = target_gflop * 1e9 / total
+            self.rows = np.sort(np.random.default_rng(0).choice(w.m, size=max(1, int(w.m * frac)), replace=False))
+            self.flops = float(per_row[self.rows].sum())
+            self.sample = f"{self.rows.size} random rows of {w.m} (all operators on those rows)"
+
+    def __call__(self):
+        o, d, r = self.o, self.dense, self.rows
+        o.sort_rows(self.ro)
+        if "B" in d:
+            o.spmm(self.ro, self.col, self.vals, d["B"], rows=r)
+        if "A" in d:
+            o.sddmm(self.ro, self.col, d["A"], d["BT"], rows=r)
+        if "W" in d:
+            o.csr_add(self.ro, self.col, self.vals, d["W"], rows=r)
 
 
-def cpu_baseline(w, acc, steps: int):
-    """The fp64 oracle as it stands, on the host cores, full workload per step."""
-    import oracle as o
-    ro, col = w.row_offsets.numpy(), w.col_idx.numpy()
-    vals64 = w.values.double().numpy()
-    B64, A64, BT64, W64 = (t.double().numpy() for t in (w.B, w.A, w.BT, w.W))
-    o.build()
-    _oracle_step(o, w, ro, col, vals64, B64, A64, BT64, W64)
-    t0 = time.perf_counter()
-    for _ in range(steps):
-        _oracle_step(o, w, ro, col, vals64, B64, A64, BT64, W64)
-    dt = (time.perf_counter() - t0) / steps
-    flops = acc["spmm"]["flops"] + acc["sddmm"]["flops"]
-    return {"value": round(flops / dt / 1e9, 3), "unit": "GFLOP/s", "cores": o.num_threads(), "kind": "oracle",
-            "sample": f"full workload, {steps} step(s) of sort_rows+spmm+sddmm+csr_add in fp64",
+def cpu_baseline(w, acc, seconds: float):
+    st = OracleStep(w, acc, target_gflop=2.0)
+    st()
+    n, t0 = 0, time.perf_counter()
+    while True:
+        st()
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = (time.perf_counter() - t0) / n
+    return {"value": round(st.flops / dt / 1e9, 3), "unit": "GFLOP/s", "cores": st.o.num_threads(), "kind": "oracle",
+            "sample": f"{st.sample}; {n} step(s) of sort_rows+spmm+sddmm+csr_add in fp64",
             "ms_per_step": round(dt * 1e3, 2)}
 
 
@@ -379,31 +423,23 @@ def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return
-    w = wl.generate(WORKLOAD)
+    w = wl.generate(args.workload)
     acc = accounting(w)
-    steps = max(1, min(args.steps, args.ref_max_steps))
-    import oracle as o
-    ro, col = w.row_offsets.numpy(), w.col_idx.numpy()
-    vals64 = w.values.double().numpy()
-    B64, A64, BT64, W64 = (t.double().numpy() for t in (w.B, w.A, w.BT, w.W))
-    o.build()
+    st = OracleStep(w, acc, target_gflop=2.0)
     for _ in range(min(args.warmup, 1)):
-        _oracle_step(o, w, ro, col, vals64, B64, A64, BT64, W64)
+        st()
+    steps = max(1, min(args.steps, args.ref_max_steps))
     t0 = time.perf_counter()
     for _ in range(steps):
-        _oracle_step(o, w, ro, col, vals64, B64, A64, BT64, W64)
+        st()
     dt = (time.perf_counter() - t0) / steps
-    flops = acc["spmm"]["flops"] + acc["sddmm"]["flops"]
-    value = round(flops / dt / 1e9, 3)
-    line = {"impl": "reference",
-            "metric": "SpMM+SDDMM GFLOP/s (2*nnz*N + 2*nnz*kd per step; step = sort_rows+spmm+sddmm+csr_add)",
-            "value": value, "unit": "GFLOP/s", "n_gpus": ws, "steps": steps, "warmup": args.warmup,
-            "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f64", "data": "synthetic (seeded; RoSA-adapter mask recipe)",
-            "config": {"workload": "rosa_adapter_4096x4096_fp16_1pct_clustered_2048tok", "m": w.m, "n": w.n,
-                       "nnz": w.nnz, "N": w.B.shape[1], "kd": w.A.shape[1]},
-            "cpu_baseline": {"value": value, "unit": "GFLOP/s", "cores": o.num_threads(), "kind": "oracle",
-                             "sample": f"full workload per step, {steps} step(s)"},
+    value = round(st.flops / dt / 1e9, 3)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": ws, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; workload recipes in DESIGN.md)",
+            "config": {"workload": DESCRIPTION[args.workload], "m": w.m, "n": w.n, "nnz": w.nnz},
+            "cpu_baseline": {"value": value, "unit": "GFLOP/s", "cores": st.o.num_threads(), "kind": "oracle",
+                             "sample": f"{st.sample}, {steps} step(s)"},
             "e2e": {"value": value, "unit": "GFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -414,9 +450,10 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="rosa", choices=list(wl.SPECS))
     ap.add_argument("--sddmm-backend", default="structure_aware", choices=["structure_aware", "general"])
     ap.add_argument("--spmm-path", default="auto", choices=["auto", "general"])
-    ap.add_argument("--cpu-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
     ap.add_argument("--ref-max-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

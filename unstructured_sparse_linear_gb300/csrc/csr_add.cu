@@ -25,6 +25,8 @@ constexpr int kAddThreads = 256;
 constexpr int kAddTileBytes = 16384;
 constexpr int kAddStages = 3;
 constexpr int kAddSmem = kAddTileBytes * kAddStages;
+constexpr int kRoCache = 512;  // row offsets of a tile kept in shared memory (tiles spanning fewer rows)
+constexpr int kPre = 4;        // entries per thread loaded before the tile arrives
 
 template <typename T, typename I, bool kBulk>
 __global__ void __launch_bounds__(kAddThreads) csr_add_kernel(const T* __restrict__ vals,
@@ -33,6 +35,7 @@ __global__ void __launch_bounds__(kAddThreads) csr_add_kernel(const T* __restric
                                                                T* C, int64_t total, int* err) {
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ __align__(8) uint64_t full_bar[kAddStages];
+    __shared__ int32_t ro_s[kRoCache];
     constexpr int64_t E = kAddTileBytes / sizeof(T);
     const int tid = threadIdx.x;
     const int64_t ntiles = (total + E - 1) / E;
@@ -66,6 +69,34 @@ __global__ void __launch_bounds__(kAddThreads) csr_add_kernel(const T* __restric
         const int cnt = tile_elems(t);
         const int64_t f1 = f0 + cnt;
         T* buf = stage(s);
+        // Entries whose flat position falls in [f0, f1): rows r0..r1, CSR range [kb, ke).
+        // Their row offsets go to shared memory and the first kPre entries per thread are
+        // loaded before waiting for the tile, so those loads overlap the tile's copy.
+        const int32_t r0 = (int32_t)(f0 / n), r1 = (int32_t)((f1 - 1) / n);
+        const int nro = r1 - r0 + 2;
+        const bool cached = nro <= kRoCache;
+        if (cached)
+            for (int x = tid; x < nro; x += kAddThreads) ro_s[x] = ro[r0 + x];
+        __syncthreads();
+        const int32_t kb = cached ? ro_s[0] : ro[r0];
+        const int32_t ke = cached ? ro_s[nro - 1] : ro[r1 + 1];
+        auto row_of = [&](int32_t k) {  // largest r in [r0, r1] with ro[r] <= k
+            int32_t lo = 0, hi = nro - 2;
+            while (lo < hi) {
+                const int32_t mid = (lo + hi + 1) >> 1;
+                if ((cached ? ro_s[mid] : ro[r0 + mid]) <= k) lo = mid;
+                else hi = mid - 1;
+            }
+            return r0 + lo;
+        };
+        int cq[kPre];
+        float vq[kPre];
+#pragma unroll
+        for (int q = 0; q < kPre; ++q) {
+            const int32_t k = kb + tid + q * kAddThreads;
+            cq[q] = k < ke ? idx_of(col[k]) : 0;
+            vq[q] = k < ke ? Elt<T>::to_f(vals[k]) : 0.f;
+        }
         bool ok = true;
         if (kBulk) {
             ok = mbar_wait(smem_u32(&full_bar[s]), (uint32_t)((j / kAddStages) & 1), err);
@@ -78,22 +109,20 @@ __global__ void __launch_bounds__(kAddThreads) csr_add_kernel(const T* __restric
             if (tid == 0) bulk_wait<0>();
             return;
         }
-        // Entries whose flat position falls in [f0, f1): rows r0..r1, CSR range [kb, ke).
-        const int32_t r0 = (int32_t)(f0 / n), r1 = (int32_t)((f1 - 1) / n);
-        const int32_t kb = ro[r0], ke = ro[r1 + 1];
-        for (int32_t k = kb + tid; k < ke; k += kAddThreads) {
-            int32_t lo = r0, hi = r1;  // row of entry k: largest r with ro[r] <= k
-            while (lo < hi) {
-                const int32_t mid = (lo + hi + 1) >> 1;
-                if (ro[mid] <= k) lo = mid;
-                else hi = mid - 1;
-            }
-            const int64_t f = (int64_t)lo * n + idx_of(col[k]);
+        auto add = [&](int32_t k, int c, float a) {
+            const int64_t f = (int64_t)row_of(k) * n + c;
             if (f >= f0 && f < f1) {
                 T& x = buf[f - f0];
-                x = Elt<T>::from_f(Elt<T>::to_f(x) + Elt<T>::to_f(vals[k]));
+                x = Elt<T>::from_f(Elt<T>::to_f(x) + a);
             }
+        };
+#pragma unroll
+        for (int q = 0; q < kPre; ++q) {
+            const int32_t k = kb + tid + q * kAddThreads;
+            if (k < ke) add(k, cq[q], vq[q]);
         }
+        for (int32_t k = kb + tid + kPre * kAddThreads; k < ke; k += kAddThreads)
+            add(k, idx_of(col[k]), Elt<T>::to_f(vals[k]));
         if (kBulk) fence_proxy_async_smem();
         __syncthreads();
         if (kBulk) {

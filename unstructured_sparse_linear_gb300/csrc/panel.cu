@@ -71,6 +71,8 @@ sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
     __shared__ uint32_t tmem_base_sh;
     __shared__ int32_t s_rows[kPM];
     __shared__ int32_t s_u[kTileN];
+    __shared__ int32_t s_off[kPM], s_kb[kPM], s_cnt[kPM];
+    __shared__ int32_t s_wsum[kTileThreads / 32];
     uint8_t* smem = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(smem_raw), 1024));
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -170,30 +172,62 @@ sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
         }
         tc::fence_after_sync();
 
-        // epilogue: TMEM lane tid (panel row tid) -> padded shared scratch; then each warp
-        // takes whole rows and its lanes walk the row's entries of this tile,
-        // [ts[t], ts[t+1]) by the plan, so entry loads and output stores are coalesced
-        float* scratch = reinterpret_cast<float*>(smem);
+        // epilogue. Thread tid owns TMEM lane tid = panel row tid. The plan's mask says which
+        // of the tile's 128 columns the row holds; its k-th set bit is the row's k-th entry
+        // of the tile (entries and U are both in column order), starting at ts[t]. Each
+        // thread packs its row's sampled values into a shared staging area (register index
+        // fixed per bit, no loads of entry positions), then warps copy whole rows out with
+        // coalesced stores.
+        const int lane = tid & 31;
+        int32_t kb = 0, cnt = 0;
+        uint32_t mk[kTileN / 32];
+        {
+            const size_t prow_at = (size_t)p * kPM + tid;
+#pragma unroll
+            for (int c = 0; c < kTileN / 32; ++c) mk[c] = 0;
+            if (s_rows[tid] >= 0) {
+                const int32_t* ts = v.ts + prow_at * (kTiles + 1);
+                kb = ts[t];
+                cnt = ts[t + 1] - kb;
+                const uint32_t* tm = v.tmask + prow_at * (kUCap / 32) + t * (kTileN / 32);
+#pragma unroll
+                for (int c = 0; c < kTileN / 32; ++c) mk[c] = tm[c];
+            }
+        }
+        int incl = cnt;  // exclusive scan of cnt over the 128 rows
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) s_wsum[warp] = incl;
+        __syncthreads();
+        int off = incl - cnt;
+        for (int w = 0; w < warp; ++w) off += s_wsum[w];
+        s_off[tid] = off;
+        s_kb[tid] = kb;
+        s_cnt[tid] = cnt;
+        float* stage = reinterpret_cast<float*>(smem);
         const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-#pragma unroll 1
+        int rank = off;
+#pragma unroll
         for (int c = 0; c < kTileN / 32; ++c) {
             float x[32];
             tc::tmem_ld32(lane_addr + c * 32, x);
+            const uint32_t word = mk[c];
 #pragma unroll
-            for (int q = 0; q < 32; ++q) scratch[tid * (kTileN + 1) + c * 32 + q] = x[q];
+            for (int q = 0; q < 32; ++q) {
+                if ((word >> q) & 1u) stage[rank++] = x[q];
+            }
         }
         tc::fence_before_sync();
         __syncthreads();
-        const int lane = tid & 31;
         for (int r = warp; r < kPM; r += kTileThreads / 32) {
-            if (s_rows[r] < 0) continue;
-            const int32_t* ts = v.ts + (size_t)(p * kPM + r) * (kTiles + 1);
-            const int32_t kb = ts[t], ke = ts[t + 1];
-            const float* srow = scratch + r * (kTileN + 1) - u0;
-            for (int32_t k = kb + lane; k < ke; k += 32) {
-                const float x = srow[v.upos[k]];
-                if (S == 1) out[k] = Elt<T>::from_f(x);
-                else partial[(int64_t)split * v.nnz + k] = x;
+            const int n_r = s_cnt[r];
+            const float* src = stage + s_off[r];
+            const int32_t kr = s_kb[r];
+            for (int j = lane; j < n_r; j += 32) {
+                if (S == 1) out[kr + j] = Elt<T>::from_f(src[j]);
+                else partial[(int64_t)split * v.nnz + kr + j] = src[j];
             }
         }
     }

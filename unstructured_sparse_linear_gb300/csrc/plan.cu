@@ -18,7 +18,7 @@
 //   3. one CTA: sum the group counts into row bins, list dense panels and SDDMM tiles, and
 //      assign SpMM image slots within the workspace's image budget (in panel order);
 //   4. row groups of dense panels: each entry's position in U and, per row, the first
-//      entry of every 128-column tile of U.
+//      entry of every 128-column tile of U and a bit mask of the U positions it holds.
 // Every count is an integer sum in a fixed order, so the plan is bit-identical on every
 // build.
 #include "common.cuh"
@@ -238,11 +238,14 @@ __global__ void __launch_bounds__(1024) plan_lists_kernel(PlanView v, int64_t im
     }
 }
 
-// ---- 4. entry positions in U and tile starts (dense panels only)
+// ---- 4. entry positions in U, tile starts and per-row column masks (dense panels only)
 template <typename I>
 __global__ void __launch_bounds__(kPlanThreads)
 plan_upos_kernel(const int32_t* __restrict__ ro, const I* __restrict__ col, PlanView v) {
     extern __shared__ uint32_t sm[];
+    constexpr int kMaskWords = kUCap / 32;
+    static_assert(kMaskWords == 32, "one mask word per lane");
+    __shared__ uint32_t rmask[8][kMaskWords];  // one row per warp
     const int p = blockIdx.x / kGroups;
     if (!v.dense[p]) return;
     uint32_t* bm = sm;
@@ -259,24 +262,32 @@ plan_upos_kernel(const int32_t* __restrict__ ro, const I* __restrict__ col, Plan
         const int64_t pos = p0 + warp * (kGroupRows / 8) + rr;
         const int row = v.prow[pos];
         int32_t* ts = v.ts + pos * (kTiles + 1);
+        uint32_t* tm = v.tmask + pos * kMaskWords;
+        rmask[warp][lane] = 0;  // kMaskWords == 32: one word per lane
+        __syncwarp();
         if (row < 0) {
             if (lane <= kTiles) ts[lane] = 0;
+            tm[lane] = 0;
             continue;
         }
         const int32_t k0 = ro[row], k1 = ro[row + 1];
         if (k0 == k1) {
             if (lane <= kTiles) ts[lane] = k0;
+            tm[lane] = 0;
             continue;
         }
         for (int32_t k = k0 + lane; k < k1; k += 32) {
             const int u = upos_of(idx_of(col[k]));
             v.upos[k] = (uint16_t)u;
+            atomicOr(&rmask[warp][u >> 5], 1u << (u & 31));
             const int t_cur = u / kTileN;
             const int t_prev = k > k0 ? upos_of(idx_of(col[k - 1])) / kTileN : -1;
             for (int t = t_prev + 1; t <= t_cur; ++t) ts[t] = k;  // tiles starting at entry k
             if (k == k1 - 1)
                 for (int t = t_cur + 1; t <= kTiles; ++t) ts[t] = k1;
         }
+        __syncwarp();
+        tm[lane] = rmask[warp][lane];
     }
 }
 
@@ -313,6 +324,7 @@ PlanLayout plan_layout(int32_t m, int32_t n, int32_t nnz) {
         L.ulist = take(P * kUCap * 4);
         L.upos = take((size_t)nnz * 2);
         L.ts = take(P * kPM * (kTiles + 1) * 4);
+        L.tmask = take(P * kPM * (kUCap / 32) * 4);
         L.dense = take(P);
         L.sp_dense = take(P);
         L.items = take(P * kTiles * 4);
@@ -345,6 +357,7 @@ PlanView plan_view(void* base, int32_t m, int32_t n, int32_t nnz) {
         v.ulist = at<int32_t>(b, L.ulist);
         v.upos = at<uint16_t>(b, L.upos);
         v.ts = at<int32_t>(b, L.ts);
+        v.tmask = at<uint32_t>(b, L.tmask);
         v.dense = at<uint8_t>(b, L.dense);
         v.sp_dense = at<uint8_t>(b, L.sp_dense);
         v.items = at<int32_t>(b, L.items);

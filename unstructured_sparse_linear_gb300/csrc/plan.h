@@ -13,6 +13,7 @@
 //   ulist      int32[P][kUCap] sorted columns of a dense panel
 //   upos       uint16[nnz]     column position of each entry in its panel's U
 //   ts         int32[P*128][kTiles + 1]  first entry of each 128-column tile of U, per row
+//   tmask      uint32[P*128][kUCap / 32] bit u set when the row has an entry at U position u
 //   dense      uint8[P]        panel runs on tensor cores (SDDMM)
 //   sp_dense   uint8[P]        ... and has a SpMM image slot
 //   items      int32[P*kTiles] SDDMM work items (panel << 8 | tile)
@@ -57,6 +58,7 @@ struct PlanView {
     int32_t* ulist;
     uint16_t* upos;
     int32_t* ts;
+    uint32_t* tmask;
     uint8_t* dense;
     uint8_t* sp_dense;
     int32_t* items;
@@ -70,7 +72,8 @@ struct PlanView {
 };
 
 struct PlanLayout {
-    size_t hdr, cta_part, bm_part, bm, wbase, desc, prow, ulist, upos, ts, dense, sp_dense, items, dlist_sp, img_slot;
+    size_t hdr, cta_part, bm_part, bm, wbase, desc, prow, ulist, upos, ts, tmask, dense, sp_dense, items, dlist_sp,
+        img_slot;
     size_t total;
 };
 
