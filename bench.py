@@ -67,6 +67,17 @@ def index_dtype(w):
     return torch.int16 if max(w.m, w.n) <= 32768 else torch.int32
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest value over all ranks of the default process group (the job's time is
+    the slowest rank's). Returns value unchanged without a process group."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ------------------------------------------------------------------ work accounting
 
 
@@ -275,11 +286,7 @@ def run_gpu(args):
     step_ms = [ev[s][0].elapsed_time(ev[s][nops]) for s in range(args.steps)]
     op_ms = {name: [ev[s][j].elapsed_time(ev[s][j + 1]) for s in range(args.steps)]
              for j, (name, _) in enumerate(graphs)}
-    total_ms = sum(step_ms)
-    if ws > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dev)
     ms_per_step = total_ms / args.steps
     value = ws * flops * args.steps / (total_ms * 1e-3) / 1e9
 

@@ -335,3 +335,25 @@ def test_prebuilt_plan_gives_identical_results(small_cases, name):
     assert torch.equal(c.view(torch.int16), d.view(torch.int16))
     with pytest.raises(ValueError):
         sp.spmm(g["val"], g["ro"], g["row_idx"], g["col"], g["B"][:-1].contiguous(), w.m, plan=plan)
+
+
+def test_padding_rows_never_leak_into_results(small_cases):
+    """Rows of B, A and BT that the mask never references are filled with NaN. The dense
+    panels pad their tiles (rows past a panel's |U|, positions past m); those pads must not
+    reach any output, so every result stays finite and matches the oracle."""
+    w = small_cases["rosa_dense"]
+    ro, col = w.row_offsets.numpy(), w.col_idx.numpy()
+    used_cols = np.unique(col)
+    unused_col = int(np.setdiff1d(np.arange(w.n), used_cols)[0])
+    empty_row = int(np.nonzero(np.diff(ro) == 0)[0][0])
+    B, A, BT = w.B.clone(), w.A.clone(), w.BT.clone()
+    B[unused_col] = float("nan")
+    BT[unused_col] = float("nan")
+    A[empty_row] = float("nan")
+    g = to_gpu(w)
+    C = sp.spmm(g["val"], g["ro"], g["row_idx"], g["col"], B.cuda(), w.m)
+    out = sp.sddmm(g["ro"], g["row_idx"], g["col"], A.cuda(), BT.cuda())
+    torch.cuda.synchronize()
+    assert sp.plan_build(g["ro"], g["row_idx"], g["col"], w.n).stats()["dense_panels"] >= 1
+    assert_close(C, oracle.spmm(ro, col, w.values, B), w.dtype, "spmm with poisoned unused rows")
+    assert_close(out, oracle.sddmm(ro, col, A, BT), w.dtype, "sddmm with poisoned unused rows")
