@@ -9,20 +9,15 @@
 //   * SDDMM: D = A[panel rows, :] * BT[U, :]^T per (panel, 128-column tile of U, K split)
 //     on tcgen05 (fp16/bf16 operands, fp32 accumulators in tensor memory); the epilogue
 //     reads each row's entries of the tile (contiguous, located by the plan's tile starts)
-//     out of D. With fewer tiles than SMs, K is split in up to 4 parts whose fp32 partial
+//     out of D. With fewer tiles than SMs, K is split in up to 16 parts whose fp32 partial
 //     sums a finalize kernel adds in split order, so results are deterministic.
 //   * SpMM: each dense panel's values are written into a 128 x |U| image already in the
-//     UMMA K-major 128-byte-swizzled layout; C[panel rows, 128-column tile] =
+//     UMMA K-major 128-byte-swizzled layout; C[panel rows, 256-column tile] =
 //     image * B[U, tile] on tcgen05, with B's rows gathered into an MN-major swizzled tile.
 //   * the other rows run through the general row kernels, which skip dense panels.
-// Operands move by TMA into a 6-stage shared-memory ring of 128-byte-swizzled tiles: the
-// gathered rows (A and BT rows, B's U rows) with tile::gather4 loads of four 128-byte rows
-// each, the SpMM image chunks with one 16 KB bulk copy. One thread issues the copies and the
-// MMAs; per-stage "full" mbarriers count the copied bytes and per-stage "empty" mbarriers
-// (tcgen05.commit) free a stage once its MMAs are done. Every mbarrier wait is bounded.
-#include <cuda.h>
-
-#include <mutex>
+// Operands are gathered row by row with 16-byte cp.async copies into a 4-stage shared
+// memory ring; one thread issues the MMAs and commits them to per-stage mbarriers, whose
+// completion frees the stage for the next copy. Every mbarrier wait is bounded in time.
 #include <type_traits>
 
 #include "common.cuh"
@@ -37,7 +32,8 @@ namespace {
 constexpr int kKC = 64;       // K elements per pipeline chunk (128 bytes of 16-bit data)
 constexpr int kStages = 6;
 constexpr int kSpNT = 128;    // SpMM: columns of C per tile (UMMA N)
-constexpr int kMaxSplit = 4;
+constexpr int kMaxSplit = 16;
+constexpr size_t kPartialBudget = 64ull << 20;  // bytes of fp32 split-K partial sums
 constexpr int kTileThreads = 128;
 
 constexpr uint32_t kSdStageA = kPM * kKC * 2;                 // 16 KB
@@ -50,9 +46,12 @@ constexpr uint32_t kSpSmem = kStages * kSpStageBytes + 1024;
 
 bool dtype_ok(int dt) { return dt == kF16 || dt == kBF16; }
 
-int sddmm_max_split(int32_t kd) {
-    const int nkc = (kd + kKC - 1) / kKC;
-    return nkc < kMaxSplit ? (nkc < 1 ? 1 : nkc) : kMaxSplit;
+// Most K splits a call may use: bounded by the chunks of K and by the partial-sum budget.
+int sddmm_max_split(int32_t kd, int32_t nnz) {
+    const int64_t nkc = (kd + kKC - 1) / kKC;
+    const int64_t by_mem = nnz > 0 ? (int64_t)(kPartialBudget / ((size_t)nnz * 4)) : kMaxSplit;
+    const int64_t s = min64(min64(kMaxSplit, nkc), by_mem);
+    return s < 1 ? 1 : (int)s;
 }
 
 // Number of K splits given the work items and the grid (identical on every CTA).
@@ -69,32 +68,23 @@ __host__ __device__ __forceinline__ int choose_split(int items, int grid, int ma
 
 template <typename T>
 __global__ void __launch_bounds__(kTileThreads, 1)
-sddmm_panel_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_bt,
-                   T* __restrict__ out, float* __restrict__ partial, int32_t kd, PlanView v, int max_split,
-                   uint32_t idesc, int* err) {
+sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restrict__ out, float* __restrict__ partial,
+                   int32_t kd, PlanView v, int max_split, uint32_t idesc, int* err) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t full_bar[kStages];
-    __shared__ __align__(8) uint64_t empty_bar[kStages];
+    __shared__ __align__(8) uint64_t mma_bar[kStages];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int32_t s_rows[kPM];
     __shared__ int32_t s_u[kTileN];
     __shared__ int32_t s_off[kPM], s_kb[kPM], s_cnt[kPM];
     __shared__ int32_t s_wsum[kTileThreads / 32];
-    __shared__ int s_failed;
     uint8_t* smem = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(smem_raw), 1024));
     const uint32_t sbase = smem_u32(smem);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, warp = tid >> 5;
 
     if (warp == 0) tc::tmem_alloc(smem_u32(&tmem_base_sh), kTileN);
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&full_bar[s]), 1);
-            mbar_init(smem_u32(&empty_bar[s]), 1);
-        }
+        for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&mma_bar[s]), 1);
         fence_mbar_init();
-        tc::tma_prefetch_map(&map_a);
-        tc::tma_prefetch_map(&map_bt);
-        s_failed = 0;
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -107,8 +97,9 @@ sddmm_panel_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
     const int kc_per = (nkc + S - 1) / S;
     const int64_t units = (int64_t)nitems * S;
     uint32_t g = 0;  // chunks consumed so far by this CTA: stage = g % kStages
+    bool failed = false;
 
-    for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
+    for (int64_t unit = blockIdx.x; unit < units && !failed; unit += gridDim.x) {
         const int item = v.items[unit / S];
         const int split = (int)(unit % S);
         const int p = item >> 8, t = item & 255;
@@ -117,41 +108,42 @@ sddmm_panel_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         const int nU = v.desc[p].y;
         const int u0 = t * kTileN;
         const int ncols = min(kTileN, nU - u0);
-        __syncthreads();  // the previous unit's epilogue is done with the row lists and the stages
+        __syncthreads();  // the previous unit's epilogue is done with s_rows and the stages
         s_rows[tid] = v.prow[p * kPM + tid];
         s_u[tid] = tid < ncols ? v.ulist[(size_t)p * kUCap + u0 + tid] : -1;
         __syncthreads();
 
-        if (tid == 0) {
-            // Producer and MMA issuer. Chunk j of this unit uses stage (g + j) % kStages; the
-            // TMA for chunk j + kStages - 1 is issued once the MMAs of chunk j - 1 (the last
-            // user of that stage) have completed, while the MMAs of chunk j are queued.
-            auto issue = [&](int j) {
-                const uint32_t gs = g + j;
-                const uint32_t st = sbase + (gs % kStages) * kSdStageBytes;
-                const uint32_t bar = smem_u32(&full_bar[gs % kStages]);
-                const int x = (kc0 + j) * kKC;
-                mbar_arrive_expect_tx(bar, kSdStageBytes);
-#pragma unroll 1
-                for (int q = 0; q < kPM / 4; ++q) {
-                    // padding positions gather row 0: their D rows / columns are never read
-                    const int a0 = max(s_rows[4 * q], 0), a1 = max(s_rows[4 * q + 1], 0);
-                    const int a2 = max(s_rows[4 * q + 2], 0), a3 = max(s_rows[4 * q + 3], 0);
-                    tc::tma_gather4(st + q * 512, &map_a, x, a0, a1, a2, a3, bar);
-                    const int b0 = max(s_u[4 * q], 0), b1 = max(s_u[4 * q + 1], 0);
-                    const int b2 = max(s_u[4 * q + 2], 0), b3 = max(s_u[4 * q + 3], 0);
-                    tc::tma_gather4(st + kSdStageA + q * 512, &map_bt, x, b0, b1, b2, b3, bar);
-                }
-            };
-            bool ok = true;
-            for (int j = 0; j < kStages - 1 && j < nk; ++j) issue(j);
-            for (int j = 0; j < nk && ok; ++j) {
-                const uint32_t gs = g + j;
-                const uint32_t st = sbase + (gs % kStages) * kSdStageBytes;
-                if (!mbar_wait(smem_u32(&full_bar[gs % kStages]), (gs / kStages) & 1u, err)) {
-                    ok = false;
-                    break;
-                }
+        auto load = [&](int j, uint32_t gs) {
+            const uint32_t st = sbase + (gs % kStages) * kSdStageBytes;
+            const int k0 = (kc0 + j) * kKC;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int c = tid + kTileThreads * q;
+                const int row = c >> 3, kch = c & 7;
+                const int kk = k0 + kch * 8;
+                const uint32_t off = tc::sw128_off(row, kch);
+                const int r = s_rows[row];
+                const bool oka = r >= 0 && kk < kd;
+                tc::cp_async16(st + off, oka ? (const void*)(A + (int64_t)r * kd + kk) : (const void*)A, oka ? 16 : 0);
+                const int cc = s_u[row];
+                const bool okb = cc >= 0 && kk < kd;
+                tc::cp_async16(st + kSdStageA + off, okb ? (const void*)(BT + (int64_t)cc * kd + kk) : (const void*)BT,
+                               okb ? 16 : 0);
+            }
+            tc::cp_async_commit();
+        };
+
+        for (int j = 0; j < kStages - 1; ++j) {
+            if (j < nk) load(j, g + j);
+            else tc::cp_async_commit();
+        }
+        for (int j = 0; j < nk; ++j) {
+            const uint32_t gs = g + j;
+            const uint32_t st = sbase + (gs % kStages) * kSdStageBytes;
+            tc::cp_async_wait<kStages - 2>();
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (tid == 0) {
                 tc::fence_after_sync();
 #pragma unroll
                 for (int kk = 0; kk < kKC / 16; ++kk) {
@@ -159,27 +151,29 @@ sddmm_panel_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
                     const uint64_t bd = tc::smem_desc_sw128(st + kSdStageA + kk * 32, 16, 1024);
                     tc::mma_f16(tmem, ad, bd, idesc, (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                tc::mma_commit(smem_u32(&empty_bar[gs % kStages]));
-                const int jn = j + kStages - 1;
-                if (jn < nk) {
-                    if (j >= 1) {
-                        const uint32_t gp = gs - 1;
-                        if (!mbar_wait(smem_u32(&empty_bar[gp % kStages]), (gp / kStages) & 1u, err)) {
-                            ok = false;
-                            break;
-                        }
-                    }
-                    issue(jn);
-                }
+                tc::mma_commit(smem_u32(&mma_bar[gs % kStages]));
             }
-            // MMAs complete in issue order, so the last chunk's commit covers the whole unit:
-            // after it the accumulator is final and every stage is free
-            if (ok) ok = mbar_wait(smem_u32(&empty_bar[(g + nk - 1) % kStages]), ((g + nk - 1) / kStages) & 1u, err);
-            if (!ok) s_failed = 1;
+            const int jn = j + kStages - 1;
+            if (jn < nk) {
+                if (j >= 1) {
+                    const uint32_t gp = gs - 1;
+                    if (!mbar_wait(smem_u32(&mma_bar[gp % kStages]), (gp / kStages) & 1u, err)) failed = true;
+                }
+                load(jn, gs + kStages - 1);
+            } else {
+                tc::cp_async_commit();
+            }
+        }
+        {
+            const uint32_t gl = g + nk - 1;
+            if (!mbar_wait(smem_u32(&mma_bar[gl % kStages]), (gl / kStages) & 1u, err)) failed = true;
         }
         g += nk;
-        __syncthreads();
-        if (s_failed) break;
+        tc::cp_async_wait<0>();
+        if (__syncthreads_or(failed)) {
+            failed = true;
+            break;
+        }
         tc::fence_after_sync();
 
         // epilogue. Thread tid owns TMEM lane tid = panel row tid. The plan's mask says which
@@ -188,6 +182,7 @@ sddmm_panel_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
         // thread packs its row's sampled values into a shared staging area (register index
         // fixed per bit, no loads of entry positions), then warps copy whole rows out with
         // coalesced stores.
+        const int lane = tid & 31;
         int32_t kb = 0, cnt = 0;
         uint32_t mk[kTileN / 32];
         {
@@ -240,6 +235,7 @@ sddmm_panel_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_const
             }
         }
     }
+    tc::cp_async_wait<0>();
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, kTileN);
@@ -314,27 +310,20 @@ __global__ void __launch_bounds__(256) densify_kernel(const T* __restrict__ vals
 
 template <typename T>
 __global__ void __launch_bounds__(kTileThreads, 1)
-spmm_panel_kernel(const __grid_constant__ CUtensorMap map_b, T* __restrict__ C, const T* __restrict__ img_base,
-                  int32_t N, int32_t kdim, PlanView v, uint32_t idesc, int* err) {
+spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restrict__ img_base, int32_t N, PlanView v,
+                  uint32_t idesc, int* err) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t full_bar[kStages];
-    __shared__ __align__(8) uint64_t empty_bar[kStages];
+    __shared__ __align__(8) uint64_t mma_bar[kStages];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int32_t s_u[kUCap];
-    __shared__ int s_failed;
     uint8_t* smem = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(smem_raw), 1024));
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5;
 
     if (warp == 0) tc::tmem_alloc(smem_u32(&tmem_base_sh), kSpNT);
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(smem_u32(&full_bar[s]), 1);
-            mbar_init(smem_u32(&empty_bar[s]), 1);
-        }
+        for (int s = 0; s < kStages; ++s) mbar_init(smem_u32(&mma_bar[s]), 1);
         fence_mbar_init();
-        tc::tma_prefetch_map(&map_b);
-        s_failed = 0;
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -345,46 +334,53 @@ spmm_panel_kernel(const __grid_constant__ CUtensorMap map_b, T* __restrict__ C, 
     const int ntn = (N + kSpNT - 1) / kSpNT;
     const int64_t units = (int64_t)D * ntn;
     uint32_t g = 0;
+    bool failed = false;
 
-    for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
+    for (int64_t unit = blockIdx.x; unit < units && !failed; unit += gridDim.x) {
         const int p = v.dlist_sp[unit / ntn];
         const int n0 = (int)(unit % ntn) * kSpNT;
         const int nU = v.desc[p].y;
         const int nk = (nU + kKC - 1) / kKC;
         const T* img = img_base + v.img_slot[p];
         __syncthreads();
-        // U rows of B; positions past |U| gather row kdim, outside B, which the copy engine
-        // fills with zeros (those rows meet zero columns of the image; zeros keep non-finite
-        // values elsewhere in B out of the product)
-        for (int x = tid; x < nk * kKC; x += kTileThreads) s_u[x] = x < nU ? v.ulist[(size_t)p * kUCap + x] : kdim;
+        for (int x = tid; x < nk * kKC; x += kTileThreads) s_u[x] = x < nU ? v.ulist[(size_t)p * kUCap + x] : -1;
         __syncthreads();
 
-        if (tid == 0) {
-            auto issue = [&](int j) {
-                const uint32_t gs = g + j;
-                const uint32_t st = sbase + (gs % kStages) * kSpStageBytes;
-                const uint32_t bar = smem_u32(&full_bar[gs % kStages]);
-                mbar_arrive_expect_tx(bar, kSpStageBytes);
-                bulk_g2s(st, img + (size_t)j * kPM * kKC, kSpStageA, bar);  // pre-swizzled image chunk
-#pragma unroll 1
-                for (int q = 0; q < kKC / 4; ++q) {  // 4 U rows per gather, one 64-column block at a time
-                    const int* u = s_u + j * kKC + 4 * q;
-                    const uint32_t row_off = (uint32_t)(q >> 1) * 1024u + (uint32_t)(q & 1) * 512u;
+        auto load = [&](int j, uint32_t gs) {
+            const uint32_t st = sbase + (gs % kStages) * kSpStageBytes;
+            const char* src_a = reinterpret_cast<const char*>(img + (size_t)j * kPM * kKC);
 #pragma unroll
-                    for (int blk = 0; blk < kSpNT / 64; ++blk)
-                        tc::tma_gather4(st + kSpStageA + blk * (kKC / 8 * 1024) + row_off, &map_b, n0 + blk * 64,
-                                        u[0], u[1], u[2], u[3], bar);
-                }
-            };
-            bool ok = true;
-            for (int j = 0; j < kStages - 1 && j < nk; ++j) issue(j);
-            for (int j = 0; j < nk && ok; ++j) {
-                const uint32_t gs = g + j;
-                const uint32_t st = sbase + (gs % kStages) * kSpStageBytes;
-                if (!mbar_wait(smem_u32(&full_bar[gs % kStages]), (gs / kStages) & 1u, err)) {
-                    ok = false;
-                    break;
-                }
+            for (int q = 0; q < 8; ++q) {
+                const int c = tid + kTileThreads * q;
+                tc::cp_async16(st + c * 16, src_a + c * 16, 16);
+            }
+            // B[U rows j*64 .. +64, n0 .. n0 + kSpNT): kSpNT / 8 sixteen-byte pieces per row
+            constexpr int kPieces = kSpNT / 8;
+#pragma unroll
+            for (int q = 0; q < kKC * kPieces / kTileThreads; ++q) {
+                const int c = tid + kTileThreads * q;
+                const int kk = c / kPieces, nch = c % kPieces;
+                const int u = s_u[j * kKC + kk];
+                const int ncol = n0 + nch * 8;
+                const bool ok = u >= 0 && ncol < N;
+                const uint32_t off = (uint32_t)(nch >> 3) * (kKC / 8 * 1024) + tc::sw128_off(kk, nch & 7);
+                tc::cp_async16(st + kSpStageA + off, ok ? (const void*)(B + (int64_t)u * N + ncol) : (const void*)B,
+                               ok ? 16 : 0);
+            }
+            tc::cp_async_commit();
+        };
+
+        for (int j = 0; j < kStages - 1; ++j) {
+            if (j < nk) load(j, g + j);
+            else tc::cp_async_commit();
+        }
+        for (int j = 0; j < nk; ++j) {
+            const uint32_t gs = g + j;
+            const uint32_t st = sbase + (gs % kStages) * kSpStageBytes;
+            tc::cp_async_wait<kStages - 2>();
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (tid == 0) {
                 tc::fence_after_sync();
 #pragma unroll
                 for (int kk = 0; kk < kKC / 16; ++kk) {
@@ -392,28 +388,32 @@ spmm_panel_kernel(const __grid_constant__ CUtensorMap map_b, T* __restrict__ C, 
                     const uint64_t bd = tc::smem_desc_sw128(st + kSpStageA + kk * 2048, kKC / 8 * 1024, 1024);
                     tc::mma_f16(tmem, ad, bd, idesc, (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                tc::mma_commit(smem_u32(&empty_bar[gs % kStages]));
-                const int jn = j + kStages - 1;
-                if (jn < nk) {
-                    if (j >= 1) {
-                        const uint32_t gp = gs - 1;
-                        if (!mbar_wait(smem_u32(&empty_bar[gp % kStages]), (gp / kStages) & 1u, err)) {
-                            ok = false;
-                            break;
-                        }
-                    }
-                    issue(jn);
-                }
+                tc::mma_commit(smem_u32(&mma_bar[gs % kStages]));
             }
-            if (ok) ok = mbar_wait(smem_u32(&empty_bar[(g + nk - 1) % kStages]), ((g + nk - 1) / kStages) & 1u, err);
-            if (!ok) s_failed = 1;
+            const int jn = j + kStages - 1;
+            if (jn < nk) {
+                if (j >= 1) {
+                    const uint32_t gp = gs - 1;
+                    if (!mbar_wait(smem_u32(&mma_bar[gp % kStages]), (gp / kStages) & 1u, err)) failed = true;
+                }
+                load(jn, gs + kStages - 1);
+            } else {
+                tc::cp_async_commit();
+            }
+        }
+        {
+            const uint32_t gl = g + nk - 1;
+            if (!mbar_wait(smem_u32(&mma_bar[gl % kStages]), (gl / kStages) & 1u, err)) failed = true;
         }
         g += nk;
-        __syncthreads();
-        if (s_failed) break;
+        tc::cp_async_wait<0>();
+        if (__syncthreads_or(failed)) {
+            failed = true;
+            break;
+        }
         tc::fence_after_sync();
 
-        // epilogue: TMEM row tid -> C[row, n0 .. n0 + kSpNT)
+        // epilogue: TMEM row tid -> C[row, n0 .. n0 + 256)
         const int i = v.prow[p * kPM + tid];
         const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
 #pragma unroll 1
@@ -430,6 +430,7 @@ spmm_panel_kernel(const __grid_constant__ CUtensorMap map_b, T* __restrict__ C, 
         }
         tc::fence_before_sync();
     }
+    tc::cp_async_wait<0>();
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, kSpNT);
@@ -437,52 +438,18 @@ spmm_panel_kernel(const __grid_constant__ CUtensorMap map_b, T* __restrict__ C, 
 
 // ------------------------------------------------------------------ host dispatch
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no link against libcuda).
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    });
-    return fn;
-}
-
-// A rows x cols row-major 16-bit matrix as a 2-D tensor map read in boxes of one row by
-// 64 columns (128 bytes) with the 128-byte swizzle, the box gather4 loads take.
-bool make_row_map(CUtensorMap* map, const void* base, int dt, int64_t rows, int64_t cols) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn || rows < 1 || cols < kKC || cols % 8 != 0 || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)kKC, 1};
-    const cuuint32_t es[2] = {1, 1};
-    return fn(map, dt == kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-              const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <typename T>
-cudaError_t run_sddmm_panels(const int32_t* ro, const CUtensorMap& map_a, const CUtensorMap& map_bt, void* out,
-                             float* partial, int32_t kd, const PlanView& v, cudaStream_t s) {
-    const int max_split = sddmm_max_split(kd);
+cudaError_t run_sddmm_panels(const int32_t* ro, const void* A, const void* BT, void* out, float* partial, int32_t kd,
+                             const PlanView& v, cudaStream_t s) {
+    const int max_split = sddmm_max_split(kd, v.nnz);
     const int max_items = v.P * kTiles;
     const int grid = (int)min64((int64_t)device_props().sm_count, (int64_t)max_items * max_split);
     auto kern = sddmm_panel_kernel<T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSdSmem);
     if (e != cudaSuccess) return e;
     const uint32_t idesc = tc::instr_desc_f16(std::is_same<T, __nv_bfloat16>::value ? 1u : 0u, 0, 0, kPM, kTileN);
-    kern<<<grid, kTileThreads, kSdSmem, s>>>(map_a, map_bt, static_cast<T*>(out), partial, kd, v, max_split, idesc,
-                                             device_error_word());
+    kern<<<grid, kTileThreads, kSdSmem, s>>>(static_cast<const T*>(A), static_cast<const T*>(BT), static_cast<T*>(out),
+                                             partial, kd, v, max_split, idesc, device_error_word());
     count_launches(1);
     if (max_split > 1) {
         sddmm_finalize_kernel<T><<<v.P * kPM, kFinalizeThreads, 0, s>>>(ro, static_cast<T*>(out), partial, kd, v,
@@ -493,8 +460,8 @@ cudaError_t run_sddmm_panels(const int32_t* ro, const CUtensorMap& map_a, const 
 }
 
 template <typename T>
-cudaError_t run_spmm_panels(const void* vals, const int32_t* ro, const CUtensorMap& map_b, int32_t kdim, int32_t N,
-                            void* C, void* img, const PlanView& v, cudaStream_t s) {
+cudaError_t run_spmm_panels(const void* vals, const int32_t* ro, const void* B, int32_t N, void* C, void* img,
+                            const PlanView& v, cudaStream_t s) {
     densify_kernel<T><<<v.P * kGroups, 256, 0, s>>>(static_cast<const T*>(vals), ro, static_cast<T*>(img), v);
     const int ntn = (N + kSpNT - 1) / kSpNT;
     const int grid = (int)min64((int64_t)device_props().sm_count, (int64_t)v.P * ntn);
@@ -502,8 +469,8 @@ cudaError_t run_spmm_panels(const void* vals, const int32_t* ro, const CUtensorM
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSpSmem);
     if (e != cudaSuccess) return e;
     const uint32_t idesc = tc::instr_desc_f16(std::is_same<T, __nv_bfloat16>::value ? 1u : 0u, 0, 1, kPM, kSpNT);
-    kern<<<grid, kTileThreads, kSpSmem, s>>>(map_b, static_cast<T*>(C), static_cast<const T*>(img), N, kdim, v, idesc,
-                                             device_error_word());
+    kern<<<grid, kTileThreads, kSpSmem, s>>>(static_cast<const T*>(B), static_cast<T*>(C), static_cast<const T*>(img),
+                                             N, v, idesc, device_error_word());
     count_launches(2);
     return cudaGetLastError();
 }
@@ -517,7 +484,7 @@ size_t image_bytes(int dt, int32_t m, int32_t k, int32_t nnz) {
 
 size_t partial_bytes(int dt, int32_t m, int32_t n, int32_t kd, int32_t nnz) {
     if (!dtype_ok(dt) || !plan_panels_enabled(m, n) || kd <= 0) return 0;
-    const int s = sddmm_max_split(kd);
+    const int s = sddmm_max_split(kd, nnz);
     return s > 1 ? align_up((size_t)s * nnz * 4, 1024) : 0;
 }
 
@@ -552,12 +519,11 @@ cudaError_t launch_spmm(int dt, int it, const void* vals, const int32_t* ro, con
     PlanView v;
     cudaError_t e = resolve_plan(it, ro, row_idx, col, m, k, nnz, plan, &w, &v, s);
     if (e != cudaSuccess) return e;
-    CUtensorMap map_b;
     const bool panels = allow_panels && nnz > 0 && v.panels && dtype_ok(dt) && n % 8 == 0 && aligned16(B) &&
-                        aligned16(C) && make_row_map(&map_b, B, dt, k, n);
+                        aligned16(C);
     if (panels) {
-        e = dt == kF16 ? run_spmm_panels<__half>(vals, ro, map_b, k, n, C, w, v, s)
-                       : run_spmm_panels<__nv_bfloat16>(vals, ro, map_b, k, n, C, w, v, s);
+        e = dt == kF16 ? run_spmm_panels<__half>(vals, ro, B, n, C, w, v, s)
+                       : run_spmm_panels<__nv_bfloat16>(vals, ro, B, n, C, w, v, s);
         if (e != cudaSuccess) return e;
     }
     return launch_spmm_general(dt, it, vals, ro, row_idx, col, m, k, B, n, C, v.bins_spmm(),
@@ -571,14 +537,12 @@ cudaError_t launch_sddmm(int dt, int it, const int32_t* ro, const void* row_idx,
     PlanView v;
     cudaError_t e = resolve_plan(it, ro, row_idx, col, m, n, nnz, plan, &w, &v, s);
     if (e != cudaSuccess) return e;
-    CUtensorMap map_a, map_bt;
     const bool panels = structure_aware && nnz > 0 && v.panels && dtype_ok(dt) && kd > 0 && kd % 8 == 0 &&
-                        aligned16(A) && aligned16(BT) && make_row_map(&map_a, A, dt, m, kd) &&
-                        make_row_map(&map_bt, BT, dt, n, kd);
+                        aligned16(A) && aligned16(BT);
     if (panels) {
         float* partial = reinterpret_cast<float*>(w);
-        e = dt == kF16 ? run_sddmm_panels<__half>(ro, map_a, map_bt, out, partial, kd, v, s)
-                       : run_sddmm_panels<__nv_bfloat16>(ro, map_a, map_bt, out, partial, kd, v, s);
+        e = dt == kF16 ? run_sddmm_panels<__half>(ro, A, BT, out, partial, kd, v, s)
+                       : run_sddmm_panels<__nv_bfloat16>(ro, A, BT, out, partial, kd, v, s);
         if (e != cudaSuccess) return e;
     }
     return launch_sddmm_general(dt, it, ro, row_idx, col, m, n, kd, A, BT, out, v.bins_sddmm(),

@@ -123,13 +123,14 @@ radix_scatter_kernel(const int32_t* __restrict__ ro, const uint32_t* __restrict_
 constexpr int kSmallSortRows = 16384;
 constexpr int kSmallThreads = 1024;
 constexpr int kSmallWarps = kSmallThreads / 32;
-constexpr size_t kSmallSortSmem = 2 * kSmallSortRows * 2 + kSmallWarps * kRadix * 4;
+constexpr size_t kSmallSortSmem = kSmallSortRows * 4 + 2 * kSmallSortRows * 2 + kSmallWarps * kRadix * 4;
 
 template <typename OutI>
 __global__ void __launch_bounds__(kSmallThreads) sort_small_kernel(const int32_t* __restrict__ ro, int32_t m,
                                                                    OutI* __restrict__ out) {
     extern __shared__ __align__(16) unsigned char sm[];
-    uint16_t* va = reinterpret_cast<uint16_t*>(sm);
+    uint32_t* len = reinterpret_cast<uint32_t*>(sm);  // nnz of every row, by row id
+    uint16_t* va = reinterpret_cast<uint16_t*>(len + kSmallSortRows);
     uint16_t* vb = va + kSmallSortRows;
     uint32_t(*wcnt)[kRadix] = reinterpret_cast<uint32_t(*)[kRadix]>(vb + kSmallSortRows);
     __shared__ uint32_t hist[kRadix], base[kRadix], running[kRadix];
@@ -140,7 +141,9 @@ __global__ void __launch_bounds__(kSmallThreads) sort_small_kernel(const int32_t
     int32_t mx = 0;
     for (int32_t i = tid; i < m; i += kSmallThreads) {
         va[i] = (uint16_t)i;
-        mx = max(mx, ro[i + 1] - ro[i]);
+        const int32_t c = ro[i + 1] - ro[i];
+        len[i] = (uint32_t)c;
+        mx = max(mx, c);
     }
     for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if (lane == 0) red[warp] = mx;
@@ -151,9 +154,7 @@ __global__ void __launch_bounds__(kSmallThreads) sort_small_kernel(const int32_t
     int bits = 0;
     while (bits < 32 && (key_base >> bits) != 0) ++bits;
     const int passes = (bits + 7) / 8;
-    auto digit = [&](uint32_t v, int shift) {
-        return (int)(((key_base - (uint32_t)(ro[v + 1] - ro[v])) >> shift) & (kRadix - 1));
-    };
+    auto digit = [&](uint32_t v, int shift) { return (int)(((key_base - len[v]) >> shift) & (kRadix - 1)); };
     for (int p = 0; p < passes; ++p) {
         const int shift = 8 * p;
         if (tid < kRadix) hist[tid] = 0;

@@ -82,7 +82,7 @@ __device__ __forceinline__ void store_c(T* __restrict__ Crow, int col0, int N, c
 }
 
 template <typename T, typename I, int V>
-__global__ void __launch_bounds__(kSpmmThreads)
+__global__ void __launch_bounds__(kSpmmThreads, 2)
 spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, const I* __restrict__ row_idx,
                  const I* __restrict__ col, const T* __restrict__ B, T* __restrict__ C, int32_t m, int32_t N, int G,
                  const int32_t* __restrict__ bins, const uint8_t* __restrict__ skip) {
@@ -142,27 +142,47 @@ spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, con
         const int64_t gid = ((int64_t)blockIdx.x * kSpmmWarps + warp) * gpw + gw;
         const int64_t ngroups = (int64_t)gridDim.x * kSpmmWarps * gpw;
         const int64_t items = (int64_t)(m - n_long) * nch;
-        for (int64_t item = gid; item < items; item += ngroups) {
-            const int32_t p = n_long + (int32_t)(item / nch);
-            if (skip && skip[p / kPanelRows]) continue;  // uniform across the group
-            const int c = (int)(item % nch);
-            const int row = idx_of(row_idx[p]);
-            const int32_t k0 = ro[row], k1 = ro[row + 1];
-            const int col0 = c * chunk + gl * V;
-            float acc[V];
+        // Items go in batches of kBatch: their row ids, then their row offsets, are loaded
+        // together before any is processed, so short and empty rows do not wait on one
+        // dependent load chain each.
+        constexpr int kBatch = 4;
+        for (int64_t base = gid; base < items; base += kBatch * ngroups) {
+            int rowq[kBatch], cq[kBatch];
+            int32_t k0q[kBatch], k1q[kBatch];
+            bool live[kBatch];
 #pragma unroll
-            for (int e = 0; e < V; ++e) acc[e] = 0.f;
-            for (int32_t kb = k0; kb < k1; kb += G) {
-                const int32_t kk = kb + gl;
-                int cj = 0;
-                float vj = 0.f;
-                if (kk < k1) {
-                    cj = idx_of(col[kk]);
-                    vj = Elt<T>::to_f(vals[kk]);
-                }
-                accumulate<T, V>(acc, cj, vj, min(G, k1 - kb), B, N, col0, gmask, gw * G);
+            for (int q = 0; q < kBatch; ++q) {
+                const int64_t item = base + q * ngroups;
+                const int32_t p = n_long + (int32_t)(item / nch);
+                live[q] = item < items && !(skip && skip[p / kPanelRows]);  // uniform across the group
+                cq[q] = (int)(item % nch);
+                rowq[q] = live[q] ? idx_of(row_idx[p]) : 0;
             }
-            store_c<T, V>(C + (int64_t)row * N, col0, N, acc);
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+                k0q[q] = live[q] ? ro[rowq[q]] : 0;
+                k1q[q] = live[q] ? ro[rowq[q] + 1] : 0;
+            }
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+                if (!live[q]) continue;
+                const int32_t k0 = k0q[q], k1 = k1q[q];
+                const int col0 = cq[q] * chunk + gl * V;
+                float acc[V];
+#pragma unroll
+                for (int e = 0; e < V; ++e) acc[e] = 0.f;
+                for (int32_t kb = k0; kb < k1; kb += G) {
+                    const int32_t kk = kb + gl;
+                    int cj = 0;
+                    float vj = 0.f;
+                    if (kk < k1) {
+                        cj = idx_of(col[kk]);
+                        vj = Elt<T>::to_f(vals[kk]);
+                    }
+                    accumulate<T, V>(acc, cj, vj, min(G, k1 - kb), B, N, col0, gmask, gw * G);
+                }
+                store_c<T, V>(C + (int64_t)rowq[q] * N, col0, N, acc);
+            }
         }
     }
 }

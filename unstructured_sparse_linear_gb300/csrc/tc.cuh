@@ -23,24 +23,6 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// ------------------------------------------------------------------ TMA
-
-// Four rows of a 2-D tensor map (box {64 elements, 1 row}, 128-byte swizzle) into 512
-// consecutive bytes of shared memory: rows r0..r3 starting at column x (x * element size a
-// multiple of 16 bytes). Completion is counted in bytes on the mbarrier.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int x, int r0, int r1, int r2, int r3,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(tmap), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_prefetch_map(const void* tmap) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
-}
-
 // ------------------------------------------------------------------ tensor memory
 
 // Allocate `ncols` TMEM columns (power of two, 32..512); one full warp executes it and the
