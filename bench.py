@@ -7,8 +7,10 @@ One step = one pass of the whole path over one workload (default: the RoSA adapt
   -> csr_add (W + A)
 (operators the workload does not define are left out). metric: GFLOP/s counting
 2 * nnz * N for SpMM and 2 * nnz * kd for SDDMM; every operator's time is in the step.
-Each operator is a CUDA-graph replay of the library calls; L2 is flushed (a 256 MB write)
-before every timed step, outside the step's events.
+Each step is one CUDA-graph replay of the library calls in which spmm, sddmm and csr_add
+(independent once row_idx and the plan exist) run on three streams; a second loop replays
+one graph per operator in order to give the per-operator times. L2 is flushed (a 256 MB
+write) before every timed step, outside the step's events.
 
 --impl reference times the fp64 CPU oracle on the host cores on the same workload, metric
 and unit (a deliberately slow baseline, not a target).
@@ -213,6 +215,31 @@ def make_ops(sp, w, d, idx, args, outs):
     return ops
 
 
+def run_step_forked(ops, stream, side):
+    """sort_rows and plan on `stream`, then spmm / sddmm / csr_add on `stream` and the side
+    streams, joined back into `stream`."""
+    first = [f for name, f in ops if name in ("sort_rows", "plan")]
+    rest = [f for name, f in ops if name not in ("sort_rows", "plan")]
+    for f in first:
+        f()
+    fork = torch.cuda.Event()
+    fork.record(stream)
+    joins = []
+    for f, s in zip(rest[1:], side):
+        s.wait_event(fork)
+        with torch.cuda.stream(s):
+            f()
+            e = torch.cuda.Event()
+            e.record(s)
+        joins.append(e)
+    for f in rest[:1]:
+        f()
+    for e in joins:
+        stream.wait_event(e)
+    for f in rest[1 + len(side):]:
+        f()
+
+
 def host_inputs(w, idx):
     h = {"ro": w.row_offsets, "col": w.col_idx.to(idx), "val": w.values}
     for k in ("B", "A", "BT", "W"):
@@ -243,27 +270,35 @@ def run_gpu(args):
     ops = make_ops(sp, w, d, idx, args, outs)
 
     stream = torch.cuda.Stream(device=dev)
+    side = [torch.cuda.Stream(device=dev) for _ in range(2)]
+    lib = sp._lib.load()
     with torch.cuda.stream(stream):
         for _ in range(max(args.warmup, 1)):
             for _, f in ops:
                 f()
         torch.cuda.synchronize(dev)
-        launches0 = sp._lib.load().spops_kernel_launches()
-        graphs = []
         pool = torch.cuda.graph_pool_handle()
+        # the step: sort_rows and plan, then the operators, which depend only on row_idx and
+        # the plan, on three streams (fork / join inside one graph)
+        step_graph = torch.cuda.CUDAGraph()
+        launches0 = lib.spops_kernel_launches()
+        with torch.cuda.graph(step_graph, stream=stream, pool=pool):
+            run_step_forked(ops, stream, side)
+        launches_per_step = lib.spops_kernel_launches() - launches0
+        # one graph per operator, replayed in order, for the per-operator breakdown
+        op_graphs = []
         for name, f in ops:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream, pool=pool):
                 f()
-            graphs.append((name, g))
-        launches_per_step = sp._lib.load().spops_kernel_launches() - launches0
+            op_graphs.append((name, g))
         for _ in range(args.warmup):
-            for _, g in graphs:
+            step_graph.replay()
+            for _, g in op_graphs:
                 g.replay()
         torch.cuda.synchronize(dev)
 
-        nops = len(graphs)
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nops + 1)] for _ in range(args.steps)]
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
         sampler = ClockSampler(local)
         if ws > 1:
             dist.barrier()
@@ -274,18 +309,29 @@ def run_gpu(args):
         for s in range(args.steps):
             flush.zero_()
             ev[s][0].record(stream)
-            for j, (_, g) in enumerate(graphs):
-                g.replay()
-                ev[s][j + 1].record(stream)
+            step_graph.replay()
+            ev[s][1].record(stream)
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - t0
         if ws > 1:
             dist.barrier()
         clocks = sampler.stop()
 
-    step_ms = [ev[s][0].elapsed_time(ev[s][nops]) for s in range(args.steps)]
-    op_ms = {name: [ev[s][j].elapsed_time(ev[s][j + 1]) for s in range(args.steps)]
-             for j, (name, _) in enumerate(graphs)}
+        # per-operator breakdown: the same graphs one operator at a time, events between them
+        nb = max(3, min(args.steps, args.breakdown_steps))
+        nops = len(op_graphs)
+        evb = [[torch.cuda.Event(enable_timing=True) for _ in range(nops + 1)] for _ in range(nb)]
+        for s in range(nb):
+            flush.zero_()
+            evb[s][0].record(stream)
+            for j, (_, g) in enumerate(op_graphs):
+                g.replay()
+                evb[s][j + 1].record(stream)
+        torch.cuda.synchronize(dev)
+
+    step_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
+    op_ms = {name: [evb[s][j].elapsed_time(evb[s][j + 1]) for s in range(nb)]
+             for j, (name, _) in enumerate(op_graphs)}
     total_ms = max_over_ranks(sum(step_ms), dev)
     ms_per_step = total_ms / args.steps
     value = ws * flops * args.steps / (total_ms * 1e-3) / 1e9
@@ -308,7 +354,7 @@ def run_gpu(args):
                 "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
                 "traffic": recorded_traffic(dominant, args.workload), "algorithmic_bytes": acc[dominant]["bytes"],
                 "peak_source": pk["source"],
-                "note": "achieved = algorithmic bytes of the op / its mean event time in the timed loop"}
+                "note": "achieved = algorithmic bytes of the op / its mean event time in the per-operator loop"}
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -327,6 +373,7 @@ def run_gpu(args):
                    "parallelism": f"replicas x{ws} (independent problems per GPU)"},
         "per_op": per_op, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": int(launches_per_step) * args.steps, "clocks": clocks,
+        "breakdown_steps": nb, "step_ms_sum_of_ops": round(sum(v["ms"] for v in per_op.values()), 5),
         "wall_s_timed_region": round(wall, 4),
     }
     if rank == 0:
@@ -461,6 +508,7 @@ def main():
     ap.add_argument("--sddmm-backend", default="structure_aware", choices=["structure_aware", "general"])
     ap.add_argument("--spmm-path", default="auto", choices=["auto", "general"])
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
+    ap.add_argument("--breakdown-steps", type=int, default=200)
     ap.add_argument("--ref-max-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -12,12 +12,13 @@
 //     out of D. With fewer tiles than SMs, K is split in up to 16 parts whose fp32 partial
 //     sums a finalize kernel adds in split order, so results are deterministic.
 //   * SpMM: each dense panel's values are written into a 128 x |U| image already in the
-//     UMMA K-major 128-byte-swizzled layout; C[panel rows, 256-column tile] =
+//     UMMA K-major 128-byte-swizzled layout; C[panel rows, 128-column tile] =
 //     image * B[U, tile] on tcgen05, with B's rows gathered into an MN-major swizzled tile.
 //   * the other rows run through the general row kernels, which skip dense panels.
-// Operands are gathered row by row with 16-byte cp.async copies into a 4-stage shared
-// memory ring; one thread issues the MMAs and commits them to per-stage mbarriers, whose
-// completion frees the stage for the next copy. Every mbarrier wait is bounded in time.
+// Operands are gathered row by row with 16-byte cp.async copies into a 3-stage shared
+// memory ring (two CTAs per SM, so two units' latency chains overlap); one thread issues
+// the MMAs and commits them to per-stage mbarriers, whose completion frees the stage for
+// the next copy. Every mbarrier wait is bounded in time.
 #include <type_traits>
 
 #include "common.cuh"
@@ -30,7 +31,7 @@ namespace spops {
 namespace {
 
 constexpr int kKC = 64;       // K elements per pipeline chunk (128 bytes of 16-bit data)
-constexpr int kStages = 6;
+constexpr int kStages = 3;      // 3 x 32 KB ring: two CTAs per SM
 constexpr int kSpNT = 128;    // SpMM: columns of C per tile (UMMA N)
 constexpr int kMaxSplit = 16;
 constexpr size_t kPartialBudget = 64ull << 20;  // bytes of fp32 split-K partial sums
@@ -67,7 +68,7 @@ __host__ __device__ __forceinline__ int choose_split(int items, int grid, int ma
 // ------------------------------------------------------------------ SDDMM dense panels
 
 template <typename T>
-__global__ void __launch_bounds__(kTileThreads, 1)
+__global__ void __launch_bounds__(kTileThreads, 2)
 sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restrict__ out, float* __restrict__ partial,
                    int32_t kd, PlanView v, int max_split, uint32_t idesc, int* err) {
     extern __shared__ uint8_t smem_raw[];
@@ -109,8 +110,24 @@ sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
         const int u0 = t * kTileN;
         const int ncols = min(kTileN, nU - u0);
         __syncthreads();  // the previous unit's epilogue is done with s_rows and the stages
-        s_rows[tid] = v.prow[p * kPM + tid];
+        const int my_row = v.prow[p * kPM + tid];
+        s_rows[tid] = my_row;
         s_u[tid] = tid < ncols ? v.ulist[(size_t)p * kUCap + u0 + tid] : -1;
+        // The epilogue's per-row metadata (see below), loaded now so that its latency hides
+        // behind the operand copies.
+        int32_t kb = 0, cnt = 0;
+        uint32_t mk[kTileN / 32];
+#pragma unroll
+        for (int c = 0; c < kTileN / 32; ++c) mk[c] = 0;
+        if (my_row >= 0) {
+            const size_t prow_at = (size_t)p * kPM + tid;
+            const int32_t* ts = v.ts + prow_at * (kTiles + 1);
+            kb = ts[t];
+            cnt = ts[t + 1] - kb;
+            const uint32_t* tm = v.tmask + prow_at * (kUCap / 32) + t * (kTileN / 32);
+#pragma unroll
+            for (int c = 0; c < kTileN / 32; ++c) mk[c] = tm[c];
+        }
         __syncthreads();
 
         auto load = [&](int j, uint32_t gs) {
@@ -183,21 +200,6 @@ sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
         // fixed per bit, no loads of entry positions), then warps copy whole rows out with
         // coalesced stores.
         const int lane = tid & 31;
-        int32_t kb = 0, cnt = 0;
-        uint32_t mk[kTileN / 32];
-        {
-            const size_t prow_at = (size_t)p * kPM + tid;
-#pragma unroll
-            for (int c = 0; c < kTileN / 32; ++c) mk[c] = 0;
-            if (s_rows[tid] >= 0) {
-                const int32_t* ts = v.ts + prow_at * (kTiles + 1);
-                kb = ts[t];
-                cnt = ts[t + 1] - kb;
-                const uint32_t* tm = v.tmask + prow_at * (kUCap / 32) + t * (kTileN / 32);
-#pragma unroll
-                for (int c = 0; c < kTileN / 32; ++c) mk[c] = tm[c];
-            }
-        }
         int incl = cnt;  // exclusive scan of cnt over the 128 rows
         for (int o = 1; o < 32; o <<= 1) {
             const int y = __shfl_up_sync(0xffffffffu, incl, o);
@@ -309,7 +311,7 @@ __global__ void __launch_bounds__(256) densify_kernel(const T* __restrict__ vals
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kTileThreads, 1)
+__global__ void __launch_bounds__(kTileThreads, 2)
 spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restrict__ img_base, int32_t N, PlanView v,
                   uint32_t idesc, int* err) {
     extern __shared__ uint8_t smem_raw[];
@@ -443,7 +445,7 @@ cudaError_t run_sddmm_panels(const int32_t* ro, const void* A, const void* BT, v
                              const PlanView& v, cudaStream_t s) {
     const int max_split = sddmm_max_split(kd, v.nnz);
     const int max_items = v.P * kTiles;
-    const int grid = (int)min64((int64_t)device_props().sm_count, (int64_t)max_items * max_split);
+    const int grid = (int)min64((int64_t)device_props().sm_count * 2, (int64_t)max_items * max_split);
     auto kern = sddmm_panel_kernel<T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSdSmem);
     if (e != cudaSuccess) return e;
@@ -464,7 +466,7 @@ cudaError_t run_spmm_panels(const void* vals, const int32_t* ro, const void* B, 
                             const PlanView& v, cudaStream_t s) {
     densify_kernel<T><<<v.P * kGroups, 256, 0, s>>>(static_cast<const T*>(vals), ro, static_cast<T*>(img), v);
     const int ntn = (N + kSpNT - 1) / kSpNT;
-    const int grid = (int)min64((int64_t)device_props().sm_count, (int64_t)v.P * ntn);
+    const int grid = (int)min64((int64_t)device_props().sm_count * 2, (int64_t)v.P * ntn);
     auto kern = spmm_panel_kernel<T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSpSmem);
     if (e != cudaSuccess) return e;
