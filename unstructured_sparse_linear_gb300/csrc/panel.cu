@@ -6,11 +6,12 @@
 // columns. The mask plan (plan.cu) groups row_idx positions into panels of 128 rows and
 // marks a panel dense when its entries fill its 128 x |U| tile well (U = the union of the
 // panel's columns). Here:
-//   * SDDMM: D = A[panel rows, :] * BT[U, :]^T per (panel, 128-column tile of U, K split)
-//     on tcgen05 (fp16/bf16 operands, fp32 accumulators in tensor memory); the epilogue
-//     reads each row's entries of the tile (contiguous, located by the plan's tile starts)
-//     out of D. With fewer tiles than SMs, K is split in up to 16 parts whose fp32 partial
-//     sums a finalize kernel adds in split order, so results are deterministic.
+//   * SDDMM: D = A[panel rows, :] * BT[U, :]^T per (panel, 128-column tile of U) on tcgen05
+//     (fp16/bf16 operands, fp32 accumulators in tensor memory). K is split over the CTAs of
+//     a thread-block cluster (up to 8); their fp32 partial tiles are added in rank order
+//     through distributed shared memory, so results are deterministic and no partial sums
+//     go to global memory. The epilogue reads each row's entries of the tile (contiguous,
+//     located by the plan's tile starts) out of D.
 //   * SpMM: each dense panel's values are written into a 128 x |U| image already in the
 //     UMMA K-major 128-byte-swizzled layout; C[panel rows, 128-column tile] =
 //     image * B[U, tile] on tcgen05, with B's rows gathered into an MN-major swizzled tile.
@@ -33,8 +34,10 @@ namespace {
 constexpr int kKC = 64;       // K elements per pipeline chunk (128 bytes of 16-bit data)
 constexpr int kStages = 3;      // 3 x 32 KB ring: two CTAs per SM
 constexpr int kSpNT = 128;    // SpMM: columns of C per tile (UMMA N)
-constexpr int kMaxSplit = 16;
-constexpr size_t kPartialBudget = 64ull << 20;  // bytes of fp32 split-K partial sums
+constexpr int kMaxCluster = 8;
+// Registers per thread of the SDDMM panel kernel: two CTAs must share an SM (above about 160
+// registers the occupancy calculator and the hardware place only one).
+constexpr int kPanelMaxRegs = 152;  // SDDMM: CTAs (K splits) per tile, the portable cluster limit
 constexpr int kTileThreads = 128;
 
 constexpr uint32_t kSdStageA = kPM * kKC * 2;                 // 16 KB
@@ -42,45 +45,70 @@ constexpr uint32_t kSdStageBytes = kSdStageA + kTileN * kKC * 2;  // A + BT tile
 constexpr uint32_t kSpStageA = kPM * kKC * 2;                 // 16 KB
 constexpr uint32_t kSpStageB = kSpNT * kKC * 2;               // 16 KB
 constexpr uint32_t kSpStageBytes = kSpStageA + kSpStageB;     // 32 KB
+constexpr uint32_t kSpCRowBytes = kSpNT * 2 + 16;              // staged C row (16-bit dtypes), padded
+static_assert(kPM * kSpCRowBytes <= kStages * kSpStageBytes, "C tile must fit in the operand ring");
 constexpr uint32_t kSdSmem = kStages * kSdStageBytes + 1024;
+// Receive slots (C * ceil(128 / C) rows of 132 floats, largest at C = 7) and row words.
+static_assert(133 * (kTileN + 4) * 4 + kPM * (kTileN / 4 + 1) * 4 <= kStages * kSdStageBytes,
+              "SDDMM receive slots and row words must fit in the operand ring");
 constexpr uint32_t kSpSmem = kStages * kSpStageBytes + 1024;
 
 bool dtype_ok(int dt) { return dt == kF16 || dt == kBF16; }
 
-// Most K splits a call may use: bounded by the chunks of K and by the partial-sum budget.
-int sddmm_max_split(int32_t kd, int32_t nnz) {
-    const int64_t nkc = (kd + kKC - 1) / kKC;
-    const int64_t by_mem = nnz > 0 ? (int64_t)(kPartialBudget / ((size_t)nnz * 4)) : kMaxSplit;
-    const int64_t s = min64(min64(kMaxSplit, nkc), by_mem);
-    return s < 1 ? 1 : (int)s;
-}
-
-// Number of K splits given the work items and the grid (identical on every CTA).
-__host__ __device__ __forceinline__ int choose_split(int items, int grid, int max_split, int nkc) {
-    int s = items > 0 ? grid / items : 1;
-    s = s < 1 ? 1 : s;
-    s = s > max_split ? max_split : s;
-    s = s > nkc ? nkc : s;
-    const int per = (nkc + s - 1) / s;
-    return (nkc + per - 1) / per;  // every split gets at least one chunk
-}
-
 // ------------------------------------------------------------------ SDDMM dense panels
 
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_size() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+// Every thread of every CTA of the cluster arrives; shared-memory writes before it are
+// visible to the cluster's reads after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address in CTA `rank`'s shared memory of the local shared address `addr`.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, int rank) {
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(addr), "r"(rank));
+    return ra;
+}
+__device__ __forceinline__ void st_cluster_f4(uint32_t addr, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void st_shared_f4(uint32_t addr, float4 v) {
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
+// A cluster of C CTAs computes one tile (panel p, 128 columns t of U): CTA rank r multiplies
+// K chunks [r * per, (r + 1) * per) into its tensor memory. Rows are split among the ranks
+// (rank o finishes rows [o * 128 / C, ...)); after a cluster barrier (every ring is idle),
+// each CTA stores its fp32 partial rows into a receive slot of the finishing rank through
+// distributed shared memory; after a second barrier, each rank adds its rows' slots in rank
+// order (so the result is deterministic) and writes the sampled entries. C = 1 is an
+// ordinary launch.
 template <typename T>
 __global__ void __launch_bounds__(kTileThreads, 2)
-sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restrict__ out, float* __restrict__ partial,
-                   int32_t kd, PlanView v, int max_split, uint32_t idesc, int* err) {
+sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restrict__ out, int32_t kd, PlanView v,
+                   uint32_t idesc, int* err) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t mma_bar[kStages];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int32_t s_rows[kPM];
     __shared__ int32_t s_u[kTileN];
-    __shared__ int32_t s_off[kPM], s_kb[kPM], s_cnt[kPM];
-    __shared__ int32_t s_wsum[kTileThreads / 32];
+    __shared__ int32_t s_kb[kPM], s_cnt[kPM];
+    __shared__ uint4 s_mask[kPM];
     uint8_t* smem = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(smem_raw), 1024));
     const uint32_t sbase = smem_u32(smem);
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (warp == 0) tc::tmem_alloc(smem_u32(&tmem_base_sh), kTileN);
     if (tid == 0) {
@@ -92,41 +120,51 @@ sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
     tc::fence_after_sync();
     const uint32_t tmem = tmem_base_sh;
 
+    // With at least one tile per two CTAs, K is not split: every CTA takes whole tiles on its
+    // own and the cluster barriers become CTA barriers (the choice is the same on every CTA).
     const int nitems = v.counts()[kCntTiles];
+    const bool split = (int)cluster_size() > 1 && 2 * nitems < (int)gridDim.x;
+    const int C = split ? (int)cluster_size() : 1;
+    const int crank = split ? (int)cluster_rank() : 0;
+    const int cid = blockIdx.x / C, ncl = gridDim.x / C;
     const int nkc = (kd + kKC - 1) / kKC;
-    const int S = choose_split(nitems, gridDim.x, max_split, nkc);
-    const int kc_per = (nkc + S - 1) / S;
-    const int64_t units = (int64_t)nitems * S;
+    const int per = (nkc + C - 1) / C;
+    const int S = (nkc + per - 1) / per;  // ranks that own at least one chunk
+    const int kc0 = crank * per;
+    const int nk = crank < S ? min(nkc, kc0 + per) - kc0 : 0;
+    const int rows_per = (kPM + C - 1) / C;
+    const int r0 = min(kPM, crank * rows_per), r1 = min(kPM, r0 + rows_per);
+
+    constexpr int kTS = kTileN + 4;      // receive slot row stride (floats)
+    constexpr int kMS = kTileN / 4 + 1;  // per-row word stride
+    float* recv = reinterpret_cast<float*>(smem);  // [C][rows_per][kTS] in the operand ring
+    uint32_t* meta = reinterpret_cast<uint32_t*>(recv + (size_t)C * rows_per * kTS);
     uint32_t g = 0;  // chunks consumed so far by this CTA: stage = g % kStages
     bool failed = false;
 
-    for (int64_t unit = blockIdx.x; unit < units && !failed; unit += gridDim.x) {
-        const int item = v.items[unit / S];
-        const int split = (int)(unit % S);
+    // The trip count is the same on every CTA of a cluster, and no CTA leaves the loop early
+    // (a failed wait only skips work), so the cluster barriers always match.
+    for (int it = cid; it < nitems; it += ncl) {
+        const int item = v.items[it];
         const int p = item >> 8, t = item & 255;
-        const int kc0 = split * kc_per;
-        const int nk = min(nkc, kc0 + kc_per) - kc0;
         const int nU = v.desc[p].y;
         const int u0 = t * kTileN;
         const int ncols = min(kTileN, nU - u0);
-        __syncthreads();  // the previous unit's epilogue is done with s_rows and the stages
-        const int my_row = v.prow[p * kPM + tid];
-        s_rows[tid] = my_row;
-        s_u[tid] = tid < ncols ? v.ulist[(size_t)p * kUCap + u0 + tid] : -1;
-        // The epilogue's per-row metadata (see below), loaded now so that its latency hides
-        // behind the operand copies.
-        int32_t kb = 0, cnt = 0;
-        uint32_t mk[kTileN / 32];
-#pragma unroll
-        for (int c = 0; c < kTileN / 32; ++c) mk[c] = 0;
-        if (my_row >= 0) {
+        // One round of independent loads (all indexed by panel position, not by row): the
+        // gather's row and column lists and the epilogue's per-row tile start, count and
+        // column mask. Values of padding positions are loaded but never used.
+        {
             const size_t prow_at = (size_t)p * kPM + tid;
+            const int my_row = v.prow[prow_at];
+            const int u = v.ulist[(size_t)p * kUCap + u0 + tid];
             const int32_t* ts = v.ts + prow_at * (kTiles + 1);
-            kb = ts[t];
-            cnt = ts[t + 1] - kb;
-            const uint32_t* tm = v.tmask + prow_at * (kUCap / 32) + t * (kTileN / 32);
-#pragma unroll
-            for (int c = 0; c < kTileN / 32; ++c) mk[c] = tm[c];
+            const int32_t kb = ts[t], kn = ts[t + 1];
+            const uint4 mk = *reinterpret_cast<const uint4*>(v.tmask + prow_at * (kUCap / 32) + t * (kTileN / 32));
+            s_rows[tid] = my_row;
+            s_u[tid] = tid < ncols ? u : -1;
+            s_kb[tid] = kb;
+            s_cnt[tid] = my_row >= 0 ? kn - kb : 0;
+            s_mask[tid] = mk;
         }
         __syncthreads();
 
@@ -150,125 +188,137 @@ sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
             tc::cp_async_commit();
         };
 
-        for (int j = 0; j < kStages - 1; ++j) {
-            if (j < nk) load(j, g + j);
-            else tc::cp_async_commit();
-        }
-        for (int j = 0; j < nk; ++j) {
-            const uint32_t gs = g + j;
-            const uint32_t st = sbase + (gs % kStages) * kSdStageBytes;
-            tc::cp_async_wait<kStages - 2>();
-            fence_proxy_async_smem();
-            __syncthreads();
-            if (tid == 0) {
-                tc::fence_after_sync();
+        if (nk > 0 && !failed) {
+            for (int j = 0; j < kStages - 1; ++j) {
+                if (j < nk) load(j, g + j);
+                else tc::cp_async_commit();
+            }
+            for (int j = 0; j < nk; ++j) {
+                const uint32_t gs = g + j;
+                const uint32_t st = sbase + (gs % kStages) * kSdStageBytes;
+                tc::cp_async_wait<kStages - 2>();
+                fence_proxy_async_smem();
+                __syncthreads();
+                if (tid == 0) {
+                    tc::fence_after_sync();
 #pragma unroll
-                for (int kk = 0; kk < kKC / 16; ++kk) {
-                    const uint64_t ad = tc::smem_desc_sw128(st + kk * 32, 16, 1024);
-                    const uint64_t bd = tc::smem_desc_sw128(st + kSdStageA + kk * 32, 16, 1024);
-                    tc::mma_f16(tmem, ad, bd, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < kKC / 16; ++kk) {
+                        const uint64_t ad = tc::smem_desc_sw128(st + kk * 32, 16, 1024);
+                        const uint64_t bd = tc::smem_desc_sw128(st + kSdStageA + kk * 32, 16, 1024);
+                        tc::mma_f16(tmem, ad, bd, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc::mma_commit(smem_u32(&mma_bar[gs % kStages]));
                 }
-                tc::mma_commit(smem_u32(&mma_bar[gs % kStages]));
-            }
-            const int jn = j + kStages - 1;
-            if (jn < nk) {
-                if (j >= 1) {
-                    const uint32_t gp = gs - 1;
-                    if (!mbar_wait(smem_u32(&mma_bar[gp % kStages]), (gp / kStages) & 1u, err)) failed = true;
+                const int jn = j + kStages - 1;
+                if (jn < nk) {
+                    if (j >= 1) {
+                        const uint32_t gp = gs - 1;
+                        if (!mbar_wait(smem_u32(&mma_bar[gp % kStages]), (gp / kStages) & 1u, err)) failed = true;
+                    }
+                    load(jn, gs + kStages - 1);
+                } else {
+                    tc::cp_async_commit();
                 }
-                load(jn, gs + kStages - 1);
-            } else {
-                tc::cp_async_commit();
             }
-        }
-        {
             const uint32_t gl = g + nk - 1;
             if (!mbar_wait(smem_u32(&mma_bar[gl % kStages]), (gl / kStages) & 1u, err)) failed = true;
+            g += nk;
         }
-        g += nk;
         tc::cp_async_wait<0>();
-        if (__syncthreads_or(failed)) {
-            failed = true;
-            break;
-        }
+        failed = __syncthreads_or(failed);
         tc::fence_after_sync();
 
-        // epilogue. Thread tid owns TMEM lane tid = panel row tid. The plan's mask says which
-        // of the tile's 128 columns the row holds; its k-th set bit is the row's k-th entry
-        // of the tile (entries and U are both in column order), starting at ts[t]. Each
-        // thread packs its row's sampled values into a shared staging area (register index
-        // fixed per bit, no loads of entry positions), then warps copy whole rows out with
-        // coalesced stores.
-        const int lane = tid & 31;
-        int incl = cnt;  // exclusive scan of cnt over the 128 rows
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        if (lane == 31) s_wsum[warp] = incl;
-        __syncthreads();
-        int off = incl - cnt;
-        for (int w = 0; w < warp; ++w) off += s_wsum[w];
-        s_off[tid] = off;
-        s_kb[tid] = kb;
-        s_cnt[tid] = cnt;
-        float* stage = reinterpret_cast<float*>(smem);
-        const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-        int rank = off;
+        // The ring is free on every CTA of the cluster once all have passed this barrier; the
+        // receive slots below live in it.
+        tc::fence_before_sync();
+        if (split) cluster_sync();
+        else __syncthreads();
+        tc::fence_after_sync();
+
+        // Partial tile: thread tid owns TMEM lane tid = panel row tid and sends the row's 128
+        // fp32 sums to the CTA that finishes the row (rank row / rows_per), into the slot of
+        // this CTA's rank (row stride 132 floats: the 16-byte stores of eight consecutive rows
+        // hit distinct banks).
+        // (tcgen05.ld is warp-collective: the whole warp loads, only rows with entries send.)
+        if (nk > 0 && !failed) {
+            const int owner = tid / rows_per;
+            const bool send = s_cnt[tid] > 0;
+            const uint32_t dst = smem_u32(recv + ((size_t)crank * rows_per + (tid - owner * rows_per)) * kTS);
+            const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+            const uint32_t rdst = C == 1 ? dst : cluster_map(dst, owner);
 #pragma unroll
-        for (int c = 0; c < kTileN / 32; ++c) {
-            float x[32];
-            tc::tmem_ld32(lane_addr + c * 32, x);
-            const uint32_t word = mk[c];
+            for (int c = 0; c < kTileN / 32; ++c) {
+                float x[32];
+                tc::tmem_ld32(lane_addr + c * 32, x);
+                if (send) {
 #pragma unroll
-            for (int q = 0; q < 32; ++q) {
-                if ((word >> q) & 1u) stage[rank++] = x[q];
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 y = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+                        if (C == 1) st_shared_f4(rdst + (c * 32 + q * 4) * 4, y);
+                        else st_cluster_f4(rdst + (c * 32 + q * 4) * 4, y);
+                    }
+                }
             }
+        }
+        // For each group of 4 columns of row tid: the group's bits of the row's column mask
+        // and the rank of its first entry among the row's entries of the tile (entries and U
+        // are both in column order).
+        if (tid >= r0 && tid < r1) {
+            const uint4 m = s_mask[tid];
+            const uint32_t w[4] = {m.x, m.y, m.z, m.w};
+            uint32_t run = 0;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t b = (w[c] >> (4 * j)) & 0xFu;
+                    meta[(tid - r0) * kMS + c * 8 + j] = run | (b << 8);
+                    run += __popc(b);
+                }
         }
         tc::fence_before_sync();
-        __syncthreads();
-        for (int r = warp; r < kPM; r += kTileThreads / 32) {
-            const int n_r = s_cnt[r];
-            const float* src = stage + s_off[r];
-            const int32_t kr = s_kb[r];
-            for (int j = lane; j < n_r; j += 32) {
-                if (S == 1) out[kr + j] = Elt<T>::from_f(src[j]);
-                else partial[(int64_t)split * v.nnz + kr + j] = src[j];
+        if (split) cluster_sync();  // every rank's rows have arrived
+        else __syncthreads();
+
+        // Rows [r0, r1): a warp per row; lane l adds columns 4l .. 4l+3 of the S slots in rank
+        // order and writes the sampled values to ts[t] + rank.
+        if (!failed) {
+#pragma unroll 2
+            for (int r = r0 + warp; r < r1; r += kTileThreads / 32) {
+                if (s_cnt[r] == 0) continue;  // uniform across the warp
+                const float4* slot = reinterpret_cast<const float4*>(recv + (size_t)(r - r0) * kTS) + lane;
+                const size_t slot_step = (size_t)rows_per * kTS / 4;
+                float4 x = slot[0];
+                for (int q0 = 1; q0 < S; q0 += 4) {
+                    float4 y[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        if (q0 + q < S) y[q] = slot[(q0 + q) * slot_step];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (q0 + q < S) {
+                            x.x += y[q].x;
+                            x.y += y[q].y;
+                            x.z += y[q].z;
+                            x.w += y[q].w;
+                        }
+                    }
+                }
+                const uint32_t mt = meta[(r - r0) * kMS + lane];
+                const uint32_t bits = mt >> 8;
+                T* o = out + (int64_t)s_kb[r] + (int)(mt & 0xFFu);
+                const int k1 = bits & 1u, k2 = k1 + ((bits >> 1) & 1u), k3 = k2 + ((bits >> 2) & 1u);
+                if (bits & 1u) o[0] = Elt<T>::from_f(x.x);
+                if (bits & 2u) o[k1] = Elt<T>::from_f(x.y);
+                if (bits & 4u) o[k2] = Elt<T>::from_f(x.z);
+                if (bits & 8u) o[k3] = Elt<T>::from_f(x.w);
             }
         }
+        __syncthreads();  // the shared arrays and the receive slots are rewritten by the next tile
     }
-    tc::cp_async_wait<0>();
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, kTileN);
-}
-
-// out[k] = sum of the split partial sums in split order (dense panels, S > 1 only).
-// One CTA per panel row, so even a few dense panels spread over many SMs.
-constexpr int kFinalizeThreads = 128;
-
-template <typename T>
-__global__ void __launch_bounds__(kFinalizeThreads)
-sddmm_finalize_kernel(const int32_t* __restrict__ ro, T* __restrict__ out, const float* __restrict__ partial,
-                      int32_t kd, PlanView v, int grid_tiles, int max_split) {
-    const int pos = blockIdx.x;
-    if (!v.dense[pos / kPM]) return;
-    const int i = v.prow[pos];
-    if (i < 0) return;
-    const int S = choose_split(v.counts()[kCntTiles], grid_tiles, max_split, (kd + kKC - 1) / kKC);
-    if (S == 1) return;
-    const int64_t nnz = v.nnz;
-    const int32_t k1 = ro[i + 1];
-    for (int32_t k = ro[i] + threadIdx.x; k < k1; k += kFinalizeThreads) {
-        float x[kMaxSplit];
-#pragma unroll
-        for (int sp = 0; sp < kMaxSplit; ++sp) x[sp] = sp < S ? partial[sp * nnz + k] : 0.f;
-        float s = x[0];
-#pragma unroll
-        for (int sp = 1; sp < kMaxSplit; ++sp)
-            if (sp < S) s += x[sp];
-        out[k] = Elt<T>::from_f(s);
-    }
 }
 
 // ------------------------------------------------------------------ SpMM dense panels
@@ -346,6 +396,7 @@ spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restric
         const T* img = img_base + v.img_slot[p];
         __syncthreads();
         for (int x = tid; x < nk * kKC; x += kTileThreads) s_u[x] = x < nU ? v.ulist[(size_t)p * kUCap + x] : -1;
+        bulk_wait_read<0>();  // the previous unit's staged C row has been read out of shared memory
         __syncthreads();
 
         auto load = [&](int j, uint32_t gs) {
@@ -415,23 +466,33 @@ spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restric
         }
         tc::fence_after_sync();
 
-        // epilogue: TMEM row tid -> C[row, n0 .. n0 + 256)
+        // epilogue: thread tid converts TMEM lane tid (panel row tid) to the output dtype into
+        // a shared row (stride 272 bytes: the 16-byte stores of eight consecutive rows hit
+        // distinct banks), then sends the row to C[row, n0 .. n0 + 128) with one bulk async
+        // copy; the copies drain while the next unit's operands are gathered.
         const int i = v.prow[p * kPM + tid];
         const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-#pragma unroll 1
+        const uint32_t crow = sbase + (uint32_t)tid * kSpCRowBytes;
+#pragma unroll
         for (int c = 0; c < kSpNT / 32; ++c) {
             float x[32];
             tc::tmem_ld32(lane_addr + c * 32, x);
-            if (i >= 0) {
-                T* dst = C + (int64_t)i * N + n0 + c * 32;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    if (n0 + c * 32 + q * 8 < N) *reinterpret_cast<uint4*>(dst + q * 8) = Elt<T>::pack(x + q * 8);
-                }
+            for (int q = 0; q < 4; ++q) {
+                const uint4 w = Elt<T>::pack(x + q * 8);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(crow + (c * 4 + q) * 16), "r"(w.x),
+                             "r"(w.y), "r"(w.z), "r"(w.w)
+                             : "memory");
             }
         }
         tc::fence_before_sync();
+        if (i >= 0) {
+            fence_proxy_async_smem();
+            bulk_s2g(C + (int64_t)i * N + n0, crow, (uint32_t)min(kSpNT, N - n0) * (uint32_t)sizeof(T));
+            bulk_commit();
+        }
     }
+    bulk_wait<0>();
     tc::cp_async_wait<0>();
     tc::fence_before_sync();
     __syncthreads();
@@ -441,23 +502,49 @@ spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restric
 // ------------------------------------------------------------------ host dispatch
 
 template <typename T>
-cudaError_t run_sddmm_panels(const int32_t* ro, const void* A, const void* BT, void* out, float* partial, int32_t kd,
-                             const PlanView& v, cudaStream_t s) {
-    const int max_split = sddmm_max_split(kd, v.nnz);
-    const int max_items = v.P * kTiles;
-    const int grid = (int)min64((int64_t)device_props().sm_count * 2, (int64_t)max_items * max_split);
+cudaError_t run_sddmm_panels(const void* A, const void* BT, void* out, int32_t kd, const PlanView& v, cudaStream_t s) {
     auto kern = sddmm_panel_kernel<T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSdSmem);
     if (e != cudaSuccess) return e;
+    // Largest shared-memory carveout, so that two CTAs fit on an SM (also when placing clusters).
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     const uint32_t idesc = tc::instr_desc_f16(std::is_same<T, __nv_bfloat16>::value ? 1u : 0u, 0, 0, kPM, kTileN);
-    kern<<<grid, kTileThreads, kSdSmem, s>>>(static_cast<const T*>(A), static_cast<const T*>(BT), static_cast<T*>(out),
-                                             partial, kd, v, max_split, idesc, device_error_word());
-    count_launches(1);
-    if (max_split > 1) {
-        sddmm_finalize_kernel<T><<<v.P * kPM, kFinalizeThreads, 0, s>>>(ro, static_cast<T*>(out), partial, kd, v,
-                                                                        grid, max_split);
-        count_launches(1);
+    const int64_t max_items = (int64_t)v.P * kTiles;
+    const int nkc = (kd + kKC - 1) / kKC;
+    int C = nkc < kMaxCluster ? nkc : kMaxCluster;
+
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(kTileThreads);
+    cfg.dynamicSmemBytes = kSdSmem;
+    cfg.stream = s;
+    int64_t nclusters = min64((int64_t)device_props().sm_count * 2, max_items);
+    if (C > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3((unsigned)(C * ((device_props().sm_count * 2) / C)));
+        int active = 0;
+        e = cudaOccupancyMaxActiveClusters(&active, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        if (active > 0) {
+            // Clusters beyond the co-resident count wait for a free slot; none waits on another.
+            nclusters = min64((int64_t)(device_props().sm_count * 2) / C, max_items);
+        } else {
+            C = 1;  // the cluster does not fit: one CTA per tile, no K split
+            cfg.attrs = nullptr;
+            cfg.numAttrs = 0;
+        }
     }
+    cfg.gridDim = dim3((unsigned)(nclusters * C));
+    e = cudaLaunchKernelEx(&cfg, kern, static_cast<const T*>(A), static_cast<const T*>(BT), static_cast<T*>(out), kd, v,
+                           idesc, device_error_word());
+    count_launches(1);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -469,6 +556,8 @@ cudaError_t run_spmm_panels(const void* vals, const int32_t* ro, const void* B, 
     const int grid = (int)min64((int64_t)device_props().sm_count * 2, (int64_t)v.P * ntn);
     auto kern = spmm_panel_kernel<T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSpSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     const uint32_t idesc = tc::instr_desc_f16(std::is_same<T, __nv_bfloat16>::value ? 1u : 0u, 0, 1, kPM, kSpNT);
     kern<<<grid, kTileThreads, kSpSmem, s>>>(static_cast<const T*>(B), static_cast<T*>(C), static_cast<const T*>(img),
@@ -482,12 +571,6 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 size_t image_bytes(int dt, int32_t m, int32_t k, int32_t nnz) {
     if (!dtype_ok(dt) || !plan_panels_enabled(m, k)) return 0;
     return align_up(spmm_image_budget_elems(m, nnz) * 2, 1024);
-}
-
-size_t partial_bytes(int dt, int32_t m, int32_t n, int32_t kd, int32_t nnz) {
-    if (!dtype_ok(dt) || !plan_panels_enabled(m, n) || kd <= 0) return 0;
-    const int s = sddmm_max_split(kd, nnz);
-    return s > 1 ? align_up((size_t)s * nnz * 4, 1024) : 0;
 }
 
 // The plan to use: the caller's, or one built now at the start of the workspace.
@@ -511,7 +594,10 @@ size_t spmm_workspace_bytes(int32_t m, int32_t k, int32_t n, int32_t nnz, int dt
 }
 
 size_t sddmm_workspace_bytes(int32_t m, int32_t n, int32_t kd, int32_t nnz, int dt, bool structure_aware) {
-    return 1024 + align_up(plan_bytes(m, n, nnz), 1024) + (structure_aware ? partial_bytes(dt, m, n, kd, nnz) : 0);
+    (void)kd;
+    (void)dt;
+    (void)structure_aware;
+    return 1024 + align_up(plan_bytes(m, n, nnz), 1024);
 }
 
 cudaError_t launch_spmm(int dt, int it, const void* vals, const int32_t* ro, const void* row_idx, const void* col,
@@ -542,9 +628,8 @@ cudaError_t launch_sddmm(int dt, int it, const int32_t* ro, const void* row_idx,
     const bool panels = structure_aware && nnz > 0 && v.panels && dtype_ok(dt) && kd > 0 && kd % 8 == 0 &&
                         aligned16(A) && aligned16(BT);
     if (panels) {
-        float* partial = reinterpret_cast<float*>(w);
-        e = dt == kF16 ? run_sddmm_panels<__half>(ro, A, BT, out, partial, kd, v, s)
-                       : run_sddmm_panels<__nv_bfloat16>(ro, A, BT, out, partial, kd, v, s);
+        e = dt == kF16 ? run_sddmm_panels<__half>(A, BT, out, kd, v, s)
+                       : run_sddmm_panels<__nv_bfloat16>(A, BT, out, kd, v, s);
         if (e != cudaSuccess) return e;
     }
     return launch_sddmm_general(dt, it, ro, row_idx, col, m, n, kd, A, BT, out, v.bins_sddmm(),
