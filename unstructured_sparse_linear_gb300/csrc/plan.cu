@@ -10,15 +10,17 @@
 //     columns; a panel is dense when |U| <= 1024, it has at least 16 non-empty rows and its
 //     entries fill at least a quarter of (non-empty rows) x |U|. Dense panels run on the
 //     tensor cores as 128 x |U| tiles.
-// Four kernels, none with a serial per-thread loop over a panel:
+// Two kernels (after zeroing P + 1 completion counters), none with a serial per-thread loop
+// over a panel:
 //   1. row groups (8 rows per CTA): row ids per position, per-group counts, and a column
-//      bitmap per 8-row group built with shared-memory atomics (no global atomics, no
-//      zeroing of caller memory needed);
-//   2. panels: OR the 8 group bitmaps, prefix-sum their popcounts, list U, decide density;
-//   3. one CTA: sum the group counts into row bins, list dense panels and SDDMM tiles, and
-//      assign SpMM image slots within the workspace's image budget (in panel order);
-//   4. row groups of dense panels: each entry's position in U and, per row, the first
-//      entry of every 128-column tile of U and a bit mask of the U positions it holds.
+//      bitmap per 8-row group built with shared-memory atomics; then
+//   2. the last group of a panel to finish: OR the group bitmaps, prefix-sum their
+//      popcounts, list U, decide density; then
+//   3. the last panel to finish: sum the group counts into row bins, list dense panels and
+//      SDDMM tiles, and assign SpMM image slots within the image budget (in panel order);
+//   4. second kernel, row groups of dense panels: each entry's position in U and, per row,
+//      the first entry of every 128-column tile of U and a bit mask of the U positions it
+//      holds.
 // Every count is an integer sum in a fixed order, so the plan is bit-identical on every
 // build.
 #include "common.cuh"
@@ -32,11 +34,6 @@ constexpr int kPlanThreads = 256;
 template <typename T>
 T* at(char* b, size_t off) {
     return reinterpret_cast<T*>(b + off);
-}
-
-__device__ __forceinline__ int warp_sum(int v) {
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
 }
 
 // Block-wide exclusive scan of one int per thread (blockDim.x a multiple of 32, <= 1024).
@@ -64,12 +61,15 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* sh, int* total) 
     return before;
 }
 
+__device__ void panel_work(const PlanView& v, int p, uint32_t* sm);
+__device__ void lists_work(const PlanView& v, int64_t img_budget);
+
 // ---- 1. row groups
 template <typename I>
 __global__ void __launch_bounds__(kPlanThreads)
 plan_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx, const I* __restrict__ col,
-                 PlanView v) {
-    extern __shared__ uint32_t bitmap[];  // W words when panels are enabled
+                 PlanView v, int64_t img_budget) {
+    extern __shared__ uint32_t bitmap[];  // 2 W words when panels are enabled (the panel step reuses them)
     __shared__ int red[4][8];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t p0 = (int64_t)blockIdx.x * kGroupRows;
@@ -111,19 +111,37 @@ plan_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx, 
         v.cta_part[blockIdx.x * 4 + tid] = s;
     }
     if (v.panels) {
-        uint32_t* dst = v.bm_part + (size_t)blockIdx.x * v.W;  // group g of panel p is CTA p*8+g
+        uint32_t* dst = v.bm_part + (size_t)blockIdx.x * v.W;  // group g of panel p is CTA p*kGroups+g
         for (int w = tid; w < v.W; w += kPlanThreads) dst[w] = bitmap[w];
     }
+    // The last row group of a panel to finish builds the panel; the last panel to finish
+    // builds the bins and work lists. Each CTA publishes its writes (fence) before it counts
+    // itself in; the one that completes a count fences again before reading the others'.
+    __shared__ int s_last;
+    const int p = blockIdx.x / kGroups;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(&v.done[p], 1) == kGroups - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (v.panels) panel_work(v, p, bitmap);
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(&v.done[v.P], 1) == v.P - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    lists_work(v, img_budget);
 }
 
-// ---- 2. panels
-__global__ void __launch_bounds__(kPlanThreads) plan_panels_kernel(PlanView v) {
-    extern __shared__ uint32_t sm[];  // bm[W], wbase[W]
-    uint32_t* bm = sm;
+// ---- 2. panel p (run by the last of its row-group CTAs to finish)
+__device__ void panel_work(const PlanView& v, int p, uint32_t* sm) {
+    uint32_t* bm = sm;  // bm[W], wbase[W]
     int* wb = reinterpret_cast<int*>(sm + v.W);
     __shared__ int sh[32];
     __shared__ int s_cnt[2];
-    const int p = blockIdx.x, tid = threadIdx.x;
+    const int tid = threadIdx.x;
     for (int w = tid; w < v.W; w += kPlanThreads) {
         uint32_t x = 0;
 #pragma unroll
@@ -170,12 +188,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_panels_kernel(PlanView v) {
     }
 }
 
-// ---- 3. bins and work lists
-__global__ void __launch_bounds__(1024) plan_lists_kernel(PlanView v, int64_t img_budget) {
+// ---- 3. bins and work lists (run by the last panel to finish)
+__device__ void lists_work(const PlanView& v, int64_t img_budget) {
     __shared__ int sh[32];
     // row bins: fixed-order sums over the group CTAs
     int a = 0, b = 0, c = 0;
-    for (int i = threadIdx.x; i < v.ncta; i += 1024) {
+    for (int i = threadIdx.x; i < v.ncta; i += blockDim.x) {
         a += v.cta_part[i * 4 + 0];
         b += v.cta_part[i * 4 + 1];
         c += v.cta_part[i * 4 + 2];
@@ -196,7 +214,7 @@ __global__ void __launch_bounds__(1024) plan_lists_kernel(PlanView v, int64_t im
     }
     int cd = 0, ct = 0, cs = 0, cn = 0;
     int64_t ci = 0;
-    for (int base = 0; base < v.P; base += 1024) {
+    for (int base = 0; base < v.P; base += blockDim.x) {
         const int p = base + threadIdx.x;
         const int4 d = p < v.P ? v.desc[p] : make_int4(0, 0, 0, 0);
         const int dn = d.x;
@@ -313,6 +331,7 @@ PlanLayout plan_layout(int32_t m, int32_t n, int32_t nnz) {
     const size_t nc = (size_t)((m + kPM - 1) / kPM) * kGroups;
     L.hdr = take(32 * 4);
     L.cta_part = take(nc * 16);
+    L.done = take((size_t)((m + kPM - 1) / kPM + 1) * 4);
     if (plan_panels_enabled(m, n)) {
         const size_t P = (size_t)(m + kPM - 1) / kPM;
         const size_t W = (size_t)(n + 31) / 32;
@@ -348,6 +367,7 @@ PlanView plan_view(void* base, int32_t m, int32_t n, int32_t nnz) {
     v.ncta = v.P * kGroups;
     v.hdr = at<int32_t>(b, L.hdr);
     v.cta_part = at<int32_t>(b, L.cta_part);
+    v.done = at<int32_t>(b, L.done);
     if (v.panels) {
         v.bm_part = at<uint32_t>(b, L.bm_part);
         v.bm = at<uint32_t>(b, L.bm);
@@ -378,11 +398,13 @@ size_t spmm_image_budget_elems(int32_t m, int32_t nnz) {
 cudaError_t launch_plan_build(int it, const int32_t* ro, const void* row_idx, const void* col, const PlanView& v,
                               int64_t img_budget, cudaStream_t s) {
     if (v.m <= 0) return cudaSuccess;
-    const size_t smem_rows = v.panels ? (size_t)v.W * 4 : 0;
+    const size_t smem_rows = v.panels ? (size_t)v.W * 8 : 0;
     const size_t smem_pan = (size_t)v.W * 8;
     if (smem_pan > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(plan_panels_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem_pan);
+        cudaError_t e = it == kIdx16 ? cudaFuncSetAttribute(plan_rows_kernel<uint16_t>,
+                                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_rows)
+                                     : cudaFuncSetAttribute(plan_rows_kernel<int32_t>,
+                                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_rows);
         if (e != cudaSuccess) return e;
         e = it == kIdx16 ? cudaFuncSetAttribute(plan_upos_kernel<uint16_t>,
                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_pan)
@@ -390,19 +412,15 @@ cudaError_t launch_plan_build(int it, const int32_t* ro, const void* row_idx, co
                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_pan);
         if (e != cudaSuccess) return e;
     }
+    cudaError_t e = cudaMemsetAsync(v.done, 0, (size_t)(v.P + 1) * sizeof(int32_t), s);
+    if (e != cudaSuccess) return e;
     if (it == kIdx16)
         plan_rows_kernel<uint16_t><<<v.ncta, kPlanThreads, smem_rows, s>>>(ro, (const uint16_t*)row_idx,
-                                                                           (const uint16_t*)col, v);
+                                                                           (const uint16_t*)col, v, img_budget);
     else
         plan_rows_kernel<int32_t><<<v.ncta, kPlanThreads, smem_rows, s>>>(ro, (const int32_t*)row_idx,
-                                                                          (const int32_t*)col, v);
+                                                                          (const int32_t*)col, v, img_budget);
     int launches = 1;
-    if (v.panels) {
-        plan_panels_kernel<<<v.P, kPlanThreads, smem_pan, s>>>(v);
-        ++launches;
-    }
-    plan_lists_kernel<<<1, 1024, 0, s>>>(v, img_budget);
-    ++launches;
     if (v.panels) {
         if (it == kIdx16) plan_upos_kernel<uint16_t><<<v.P * kGroups, kPlanThreads, smem_pan, s>>>(ro, (const uint16_t*)col, v);
         else plan_upos_kernel<int32_t><<<v.P * kGroups, kPlanThreads, smem_pan, s>>>(ro, (const int32_t*)col, v);

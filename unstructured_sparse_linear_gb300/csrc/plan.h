@@ -50,6 +50,7 @@ enum PlanCount {
 struct PlanView {
     int32_t* hdr;
     int32_t* cta_part;
+    int32_t* done;  // P + 1 completion counters of the plan kernel
     uint32_t* bm_part;
     uint32_t* bm;
     int32_t* wbase;
@@ -72,7 +73,7 @@ struct PlanView {
 };
 
 struct PlanLayout {
-    size_t hdr, cta_part, bm_part, bm, wbase, desc, prow, ulist, upos, ts, tmask, dense, sp_dense, items, dlist_sp,
+    size_t hdr, cta_part, done, bm_part, bm, wbase, desc, prow, ulist, upos, ts, tmask, dense, sp_dense, items, dlist_sp,
         img_slot;
     size_t total;
 };

@@ -117,13 +117,24 @@ radix_scatter_kernel(const int32_t* __restrict__ ro, const uint32_t* __restrict_
     }
 }
 
-// One CTA sorts up to kSmallSortRows rows in shared memory: the key is (longest row -
-// nnz_i), so the number of 8-bit passes follows the actual key width (0 passes when all
-// rows have equal length). Same stable LSD radix scheme as the multi-CTA path.
+// One CTA sorts up to kSmallSortRows rows in shared memory by a stable LSD radix sort of
+// the key (longest row - nnz_i), with digits of up to kSmallBits bits and as many passes as
+// the key range (longest - shortest row) needs: none when every row has the same length.
+// Warp w owns the contiguous positions [w*L, (w+1)*L), L = ceil(m / 32). Per pass:
+//   1. each warp counts its digits, 32 positions at a time (match_any gives each lane its
+//      rank among equal digits in the group, the group leader adds the group's count);
+//   2. one thread per digit turns the 32 warp counts into exclusive prefixes and a block
+//      scan over digits gives each digit's first position;
+//   3. each warp walks its positions again in the same order and scatters each row to
+//      digit start + earlier warps' count + running count in the warp + rank in the group.
+// Walking each warp's block in order and the warps in order keeps equal keys in input
+// order (stability), so ties stay by ascending row id.
 constexpr int kSmallSortRows = 16384;
 constexpr int kSmallThreads = 1024;
 constexpr int kSmallWarps = kSmallThreads / 32;
-constexpr size_t kSmallSortSmem = kSmallSortRows * 4 + 2 * kSmallSortRows * 2 + kSmallWarps * kRadix * 4;
+constexpr int kSmallBits = 9;
+constexpr int kSmallBins = 1 << kSmallBits;
+constexpr size_t kSmallSortSmem = kSmallSortRows * 4 + 2 * kSmallSortRows * 2 + kSmallWarps * kSmallBins * 4;
 
 template <typename OutI>
 __global__ void __launch_bounds__(kSmallThreads) sort_small_kernel(const int32_t* __restrict__ ro, int32_t m,
@@ -132,81 +143,101 @@ __global__ void __launch_bounds__(kSmallThreads) sort_small_kernel(const int32_t
     uint32_t* len = reinterpret_cast<uint32_t*>(sm);  // nnz of every row, by row id
     uint16_t* va = reinterpret_cast<uint16_t*>(len + kSmallSortRows);
     uint16_t* vb = va + kSmallSortRows;
-    uint32_t(*wcnt)[kRadix] = reinterpret_cast<uint32_t(*)[kRadix]>(vb + kSmallSortRows);
-    __shared__ uint32_t hist[kRadix], base[kRadix], running[kRadix];
-    __shared__ int32_t red[kSmallWarps];
+    uint32_t(*wcnt)[kSmallBins] = reinterpret_cast<uint32_t(*)[kSmallBins]>(vb + kSmallSortRows);
+    __shared__ int32_t red[2][kSmallWarps];
+    __shared__ int32_t sh[32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t lt_mask = (1u << lane) - 1u;
 
-    int32_t mx = 0;
+    int32_t mx = 0, mn = INT32_MAX;
     for (int32_t i = tid; i < m; i += kSmallThreads) {
         va[i] = (uint16_t)i;
         const int32_t c = ro[i + 1] - ro[i];
         len[i] = (uint32_t)c;
         mx = max(mx, c);
+        mn = min(mn, c);
     }
-    for (int o = 16; o; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) red[warp] = mx;
+    for (int o = 16; o; o >>= 1) {
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    }
+    if (lane == 0) {
+        red[0][warp] = mx;
+        red[1][warp] = mn;
+    }
     __syncthreads();
     mx = 0;
-    for (int w = 0; w < kSmallWarps; ++w) mx = max(mx, red[w]);
+    mn = INT32_MAX;
+    for (int w = 0; w < kSmallWarps; ++w) {
+        mx = max(mx, red[0][w]);
+        mn = min(mn, red[1][w]);
+    }
     const uint32_t key_base = (uint32_t)mx;
     int bits = 0;
-    while (bits < 32 && (key_base >> bits) != 0) ++bits;
-    const int passes = (bits + 7) / 8;
-    auto digit = [&](uint32_t v, int shift) { return (int)(((key_base - len[v]) >> shift) & (kRadix - 1)); };
-    for (int p = 0; p < passes; ++p) {
-        const int shift = 8 * p;
-        if (tid < kRadix) hist[tid] = 0;
+    while (bits < 32 && ((uint32_t)(mx - mn) >> bits) != 0) ++bits;
+    const int32_t L = (m + kSmallWarps - 1) / kSmallWarps;
+    const int32_t w0 = min(m, warp * L), w1 = min(m, w0 + L);
+    for (int shift = 0; shift < bits; shift += kSmallBits) {
+        const int db = min(kSmallBits, bits - shift);
+        const uint32_t dmask = (1u << db) - 1u;
+        const int nbins = 1 << db;
+        auto digit = [&](uint32_t v) { return (int)(((key_base - len[v]) >> shift) & dmask); };
+        for (int b = lane; b < nbins; b += 32) wcnt[warp][b] = 0;
+        __syncwarp();
+        // 1. counts per warp
+        for (int32_t c0 = w0; c0 < w1; c0 += 32) {
+            const int32_t i = c0 + lane;
+            const bool valid = i < w1;
+            const int d = valid ? digit(va[i]) : nbins + lane;  // invalid lanes never match a digit
+            const uint32_t peers = __match_any_sync(0xffffffffu, d);
+            if (valid && lane == __ffs(peers) - 1) wcnt[warp][d] += __popc(peers);
+            __syncwarp();
+        }
         __syncthreads();
-        for (int32_t i = tid; i < m; i += kSmallThreads) atomicAdd(&hist[digit(va[i], shift)], 1u);
-        __syncthreads();
-        if (warp == 0) {  // exclusive scan of 256 counters by one warp (8 per lane)
-            uint32_t c[8], s = 0;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                c[q] = hist[lane * 8 + q];
-                s += c[q];
+        // 2. per digit: exclusive prefix over warps, then over digits
+        int total = 0;
+        if (tid < nbins) {
+            for (int w = 0; w < kSmallWarps; ++w) {
+                const uint32_t c = wcnt[w][tid];
+                wcnt[w][tid] = (uint32_t)total;
+                total += (int)c;
             }
-            uint32_t x = s;
+        }
+        {  // block exclusive scan of `total` over threads (digits)
+            int x = total;
             for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
                 if (lane >= o) x += y;
             }
-            uint32_t run = x - s;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                base[lane * 8 + q] = run;
-                running[lane * 8 + q] = 0;
-                run += c[q];
+            if (lane == 31) sh[warp] = x;
+            __syncthreads();
+            if (warp == 0) {
+                int y = sh[lane];
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int z = __shfl_up_sync(0xffffffffu, y, o);
+                    if (lane >= o) y += z;
+                }
+                sh[lane] = y;
             }
+            __syncthreads();
+            const int start = (warp ? sh[warp - 1] : 0) + x - total;
+            if (tid < nbins)
+                for (int w = 0; w < kSmallWarps; ++w) wcnt[w][tid] += (uint32_t)start;
         }
         __syncthreads();
-        for (int32_t r0 = 0; r0 < m; r0 += kSmallThreads) {
-#pragma unroll
-            for (int q = 0; q < kRadix / 32; ++q) wcnt[warp][lane + 32 * q] = 0;
-            __syncwarp();
-            const int32_t i = r0 + tid;
-            const bool valid = i < m;
+        // 3. stable scatter
+        for (int32_t c0 = w0; c0 < w1; c0 += 32) {
+            const int32_t i = c0 + lane;
+            const bool valid = i < w1;
             const uint16_t v = valid ? va[i] : 0;
-            const int d = valid ? digit(v, shift) : kRadix + lane;
+            const int d = valid ? digit(v) : nbins + lane;
             const uint32_t peers = __match_any_sync(0xffffffffu, d);
-            const uint32_t rank = __popc(peers & lt_mask);
-            if (valid && lane == __ffs(peers) - 1) wcnt[warp][d] = __popc(peers);
-            __syncthreads();
-            if (tid < kRadix) {
-                uint32_t acc = running[tid];
-                for (int w = 0; w < kSmallWarps; ++w) {
-                    const uint32_t c = wcnt[w][tid];
-                    wcnt[w][tid] = acc;
-                    acc += c;
-                }
-                running[tid] = acc;
-            }
-            __syncthreads();
-            if (valid) vb[base[d] + wcnt[warp][d] + rank] = v;
-            __syncthreads();
+            if (valid) vb[wcnt[warp][d] + __popc(peers & lt_mask)] = v;
+            __syncwarp();
+            if (valid && lane == __ffs(peers) - 1) wcnt[warp][d] += __popc(peers);
+            __syncwarp();
         }
+        __syncthreads();
         uint16_t* t = va;
         va = vb;
         vb = t;
