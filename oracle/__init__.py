@@ -1,5 +1,5 @@
 """fp64 CPU oracle for the CSR sparse-adapter operators (spmm, sddmm, csr_add, sort_rows,
-row_bins) -- TEST INFRASTRUCTURE.
+row_bins, csr_transpose, masked_adam) -- TEST INFRASTRUCTURE.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may
 import this package. It shares no code with ``unstructured_sparse_linear_gb300`` and never
@@ -58,6 +58,9 @@ def _load():
             lib.oracle_spmm.argtypes = [i32, i32, i32, P, P, P, P, P, P, i32]
             lib.oracle_sddmm.argtypes = [i32, i32, i32, P, P, P, P, P, P, i32]
             lib.oracle_csr_add.argtypes = [i32, i32, P, P, P, P, P, P, i32]
+            lib.oracle_csr_transpose.argtypes = [i32, i32, P, P, P, P, P, P, P]
+            lib.oracle_masked_adam.argtypes = [ctypes.c_int64, P, P, P, P, P, i32, ctypes.c_double, ctypes.c_double,
+                                               ctypes.c_double, ctypes.c_double, i32]
             lib.oracle_round.argtypes = [ctypes.c_double, i32]
             lib.oracle_round.restype = ctypes.c_double
             lib.oracle_round_array.argtypes = [P, P, ctypes.c_int64, i32]
@@ -147,6 +150,42 @@ def csr_add(row_offsets, col_idx, values, B, rows=None) -> np.ndarray:
         out = np.empty_like(b)
         _load().oracle_csr_add(m, b.shape[1], _ptr(ro), _ptr(col), _ptr(val), _ptr(b), _ptr(out), _ptr(r), r.size)
     return out
+
+
+def csr_transpose(row_offsets, col_idx, values, n: int):
+    """A^T of the m x n CSR matrix as (row_offsets_t [n+1], row_ids [nnz], values_t [nnz],
+    perm [nnz]); perm[p] is the entry of A placed at position p (spops README operation
+    list, "csr_transpose")."""
+    ro, col, val = _i32(row_offsets), _i32(col_idx), _f64(values)
+    m = ro.size - 1
+    nnz = int(ro[-1]) if m >= 0 else 0
+    ro_t = np.empty(n + 1, dtype=np.int32)
+    row_t = np.empty(nnz, dtype=np.int32)
+    val_t = np.empty(nnz, dtype=np.float64)
+    perm = np.empty(nnz, dtype=np.int32)
+    _load().oracle_csr_transpose(m, int(n), _ptr(ro), _ptr(col), _ptr(val), _ptr(ro_t), _ptr(row_t), _ptr(val_t),
+                                 _ptr(perm))
+    return ro_t, row_t, val_t, perm
+
+
+def spmm_grad_b(row_offsets, col_idx, values, dC, n: int) -> np.ndarray:
+    """dB = A^T @ dC in fp64 for C = A @ B with A m x n in CSR: the SpMM of the transpose."""
+    ro_t, row_t, val_t, _ = csr_transpose(row_offsets, col_idx, values, n)
+    return spmm(ro_t, row_t, val_t, dC)
+
+
+def masked_adam(param, exp_avg, exp_avg_sq, grad, step: int, lr=1e-3, betas=(0.9, 0.999), eps=1e-8,
+                maximize=False, positions=None):
+    """One Adam step on the entries `positions` (all entries when None) of fp64 copies of
+    param / exp_avg / exp_avg_sq; returns the three updated arrays (SparseAdam page: moments
+    and parameters change only where the sparse gradient has a materialized value)."""
+    p, m1, m2 = _f64(param).copy(), _f64(exp_avg).copy(), _f64(exp_avg_sq).copy()
+    g = _f64(grad)
+    pos = None if positions is None else np.ascontiguousarray(np.asarray(positions, dtype=np.int64))
+    _load().oracle_masked_adam(g.size, None if pos is None else _ptr(pos), _ptr(g), _ptr(p), _ptr(m1), _ptr(m2),
+                               int(step), float(lr), float(betas[0]), float(betas[1]), float(eps),
+                               1 if maximize else 0)
+    return p, m1, m2
 
 
 def round_to(x, fmt: str) -> np.ndarray:

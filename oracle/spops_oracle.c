@@ -16,14 +16,23 @@
  *   - "Important Notes": row_offsets int32, other index lists int16.
  * torchsparsegradutils README, "Basic Sparse Matrix Multiplication": the gradient of a
  * sparse x dense product with respect to the sparse values is the sampled product, which
- * ties SDDMM to SpMM (tests check that adjoint identity on the oracle).
+ * ties SDDMM to SpMM (tests check that adjoint identity on the oracle); the gradient with
+ * respect to the dense operand is the transposed sparse matrix times the output gradient,
+ * hence csr_transpose (spops README, "csr_transpose" in the operation list).
+ * SparseAdam page (tensorplay.optim.sparse_adam.SparseAdam): Adam restricted to the
+ * entries the sparse gradient materializes -- masked_adam.
  *
  * Readings where the pages leave a step open:
  *   - row_idx sorts rows by nnz in DESCENDING order; equal counts keep ascending row id;
  *   - SDDMM does not scale by any mask value (the call takes no values);
  *   - results are rounded once, round-to-nearest-even, to the operand dtype;
  *   - row bins are counted (rows with nnz >= t_long, rows with nnz >= 1), so they are
- *     defined for any row permutation.
+ *     defined for any row permutation;
+ *   - the transpose is canonical CSR: row j of A^T lists column j of A by ascending row;
+ *   - masked Adam uses the Adam update with bias-corrected moments,
+ *     p -= lr * mhat / (sqrt(vhat) + eps), mhat = m / (1 - beta1^t), vhat = v / (1 - beta2^t),
+ *     on the materialized entries only (the page lists the defaults and the masking, not the
+ *     formula); maximize ascends.
  *
  * Parity pins: every function here is checked in the CPU test suite against brute force,
  * closed forms, library routines or the pages' worked structures. None is unpinned.
@@ -153,6 +162,49 @@ void oracle_csr_add(int32_t m, int32_t n, const int32_t* ro, const int32_t* col,
         double* c = C + (int64_t)r * n;
         for (int32_t j = 0; j < n; ++j) c[j] = b[j];
         for (int32_t k = ro[i]; k < ro[i + 1]; ++k) c[col[k]] = b[col[k]] + val[k];
+    }
+}
+
+/* ------------------------------------------------------------------ transpose */
+
+/* A^T of an m x n CSR matrix, as an n x m CSR matrix: ro_t[j] counts the entries with
+ * column < j; the entries of column j follow in ascending row order (the order in which a
+ * walk over A's rows meets them). perm[p] is the entry of A placed at position p. */
+void oracle_csr_transpose(int32_t m, int32_t n, const int32_t* ro, const int32_t* col, const double* val,
+                          int32_t* ro_t, int32_t* row_t, double* val_t, int32_t* perm) {
+    for (int32_t j = 0; j <= n; ++j) ro_t[j] = 0;
+    for (int32_t i = 0; i < m; ++i)
+        for (int32_t k = ro[i]; k < ro[i + 1]; ++k) ro_t[col[k] + 1] += 1;
+    for (int32_t j = 0; j < n; ++j) ro_t[j + 1] += ro_t[j];
+    int32_t* next = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
+    for (int32_t j = 0; j < n; ++j) next[j] = ro_t[j];
+    for (int32_t i = 0; i < m; ++i) {
+        for (int32_t k = ro[i]; k < ro[i + 1]; ++k) {
+            const int32_t p = next[col[k]]++;
+            row_t[p] = i;
+            val_t[p] = val[k];
+            perm[p] = k;
+        }
+    }
+    free(next);
+}
+
+/* ------------------------------------------------------------------ masked Adam */
+
+/* One Adam step (step number t >= 1) on the entries pos[g] of the parameter, g < count,
+ * with gradient grad[g]; every other entry of param, exp_avg and exp_avg_sq is left as it
+ * is. pos == NULL means pos[g] = g. */
+void oracle_masked_adam(int64_t count, const int64_t* pos, const double* grad, double* param, double* exp_avg,
+                        double* exp_avg_sq, int32_t t, double lr, double beta1, double beta2, double eps,
+                        int32_t maximize) {
+    const double bc1 = 1.0 - pow(beta1, (double)t), bc2 = 1.0 - pow(beta2, (double)t);
+    for (int64_t g = 0; g < count; ++g) {
+        const int64_t q = pos ? pos[g] : g;
+        const double d = maximize ? -grad[g] : grad[g];
+        exp_avg[q] = beta1 * exp_avg[q] + (1.0 - beta1) * d;
+        exp_avg_sq[q] = beta2 * exp_avg_sq[q] + (1.0 - beta2) * d * d;
+        const double mhat = exp_avg[q] / bc1, vhat = exp_avg_sq[q] / bc2;
+        param[q] -= lr * mhat / (sqrt(vhat) + eps);
     }
 }
 

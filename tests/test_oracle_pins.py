@@ -321,3 +321,123 @@ def test_workload_recipes_small_and_structured():
     lens = np.diff(r.row_offsets.numpy())
     assert (lens > 0).sum() <= round(0.1 * 1024) and len(np.unique(r.col_idx.numpy())) <= round(0.1 * 1024)
     assert r.nnz == min(round(0.01 * 1024 * 1024), 102 * 102)  # capped by the 10 % x 10 % block
+
+
+# ------------------------------------------------------------------ transpose and dB = A^T dC
+
+
+def test_golden_ust_transpose(golden_dir):
+    """The hand-derived transpose of the UST article's 4 x 8 COO example."""
+    g = json.load(open(os.path.join(golden_dir, "ust_coo_4x8.json")))
+    m, n = g["shape"]
+    ro, col = wl.csr_from_coords(np.array(g["row"]), np.array(g["col"]), m)
+    t = g["derived_by_hand"]["transpose"]
+    ro_t, row_t, val_t, perm = oracle.csr_transpose(ro, col, np.array(g["val"], dtype=np.float64), n)
+    assert ro_t.tolist() == t["row_offsets"]
+    assert row_t.tolist() == t["row_ids"]
+    assert val_t.tolist() == t["values"]
+    assert perm.tolist() == t["perm"]
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_transpose_dense_and_involution(seed):
+    rng = np.random.default_rng(400 + seed)
+    m, n = int(rng.integers(1, 40)), int(rng.integers(1, 40))
+    ro, col = rand_csr(rng, m, n, 0.2, empty_rows=(0,) if m > 2 else ())
+    val = rng.standard_normal(ro[-1])
+    ro_t, row_t, val_t, perm = oracle.csr_transpose(ro, col, val, n)
+    np.testing.assert_array_equal(densify(ro_t, row_t, val_t, n, m), densify(ro, col, val, m, n).T)
+    for j in range(n):  # canonical: ascending row ids inside every row of A^T
+        assert np.all(np.diff(row_t[ro_t[j]:ro_t[j + 1]]) > 0)
+    np.testing.assert_array_equal(val_t, val[perm])
+    ro2, col2, val2, _ = oracle.csr_transpose(ro_t, row_t, val_t, m)
+    np.testing.assert_array_equal(ro2, ro)
+    np.testing.assert_array_equal(col2, col)
+    np.testing.assert_array_equal(val2, val)
+
+
+def test_transpose_matches_scipy():
+    sparse = pytest.importorskip("scipy.sparse")
+    rng = np.random.default_rng(410)
+    m, n = 57, 91
+    ro, col = rand_csr(rng, m, n, 0.1)
+    val = rng.standard_normal(ro[-1])
+    At = sparse.csr_matrix((val, col, ro), shape=(m, n)).transpose().tocsr()
+    At.sort_indices()
+    ro_t, row_t, val_t, _ = oracle.csr_transpose(ro, col, val, n)
+    np.testing.assert_array_equal(ro_t, At.indptr)
+    np.testing.assert_array_equal(row_t, At.indices)
+    np.testing.assert_array_equal(val_t, At.data)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_spmm_grad_b_brute_force_and_adjoint(seed):
+    """dB = A^T dC: brute force on a dense copy, and <A X, Y> = <X, A^T Y>."""
+    rng = np.random.default_rng(420 + seed)
+    m, n, N = 23, 31, 7
+    ro, col = rand_csr(rng, m, n, 0.25)
+    val = rng.standard_normal(ro[-1])
+    dC = rng.standard_normal((m, N))
+    dB = oracle.spmm_grad_b(ro, col, val, dC, n)
+    np.testing.assert_allclose(dB, densify(ro, col, val, m, n).T @ dC, rtol=1e-13, atol=1e-13)
+    X = rng.standard_normal((n, N))
+    lhs = np.sum(oracle.spmm(ro, col, val, X) * dC)
+    rhs = np.sum(X * dB)
+    assert abs(lhs - rhs) <= 1e-11 * max(1.0, abs(lhs))
+    # integer-valued inputs: exact
+    vi = rng.integers(-3, 4, ro[-1]).astype(np.float64)
+    Ci = rng.integers(-3, 4, (m, N)).astype(np.float64)
+    np.testing.assert_array_equal(oracle.spmm_grad_b(ro, col, vi, Ci, n), densify(ro, col, vi, m, n).T @ Ci)
+
+
+# ------------------------------------------------------------------ masked Adam (SparseAdam page)
+
+
+def test_sparse_adam_page_mask(golden_dir):
+    """The page's example: only the entries under the gradient's mask move."""
+    g = json.load(open(os.path.join(golden_dir, "sparse_adam_mask.json")))
+    dense = np.array(g["gradient_dense"], dtype=np.float64)
+    pos = np.nonzero(dense)[0]
+    assert (dense != 0).astype(int).tolist() == g["mask"]
+    rng = np.random.default_rng(430)
+    p0 = rng.standard_normal(dense.size)
+    m0 = rng.standard_normal(dense.size) * 0.1
+    v0 = rng.random(dense.size) * 0.1
+    d = g["defaults"]
+    p, m1, v1 = oracle.masked_adam(p0, m0, v0, dense[pos], 3, lr=d["lr"], betas=d["betas"], eps=d["eps"],
+                                   maximize=d["maximize"], positions=pos)
+    off = np.array(g["mask"]) == 0
+    np.testing.assert_array_equal(p[off], p0[off])
+    np.testing.assert_array_equal(m1[off], m0[off])
+    np.testing.assert_array_equal(v1[off], v0[off])
+    assert np.all(p[~off] != p0[~off]) and np.all(m1[~off] != m0[~off]) and np.all(v1[~off] != v0[~off])
+
+
+def test_masked_adam_first_step_closed_form():
+    """From zero moments, step 1 moves each entry by lr * g / (|g| + eps)."""
+    g = np.array([5.0, -9.0, 1e-3, -2.5])
+    p, m1, v1 = oracle.masked_adam(np.zeros(4), np.zeros(4), np.zeros(4), g, 1)
+    np.testing.assert_allclose(p, -1e-3 * g / (np.abs(g) + 1e-8), rtol=1e-13)
+    np.testing.assert_allclose(m1, 0.1 * g, rtol=1e-15)
+    np.testing.assert_allclose(v1, 0.001 * g * g, rtol=1e-13)
+
+
+@pytest.mark.parametrize("maximize", [False, True])
+def test_masked_adam_matches_torch_adam(maximize):
+    """On the masked entries, several steps equal torch.optim.Adam (fp64, dense)."""
+    rng = np.random.default_rng(440 + int(maximize))
+    n = 37
+    pos = np.sort(rng.choice(n, 11, replace=False))
+    p0 = rng.standard_normal(n)
+    w = torch.tensor(p0[pos], dtype=torch.float64, requires_grad=True)
+    opt = torch.optim.Adam([w], lr=3e-3, betas=(0.8, 0.95), eps=1e-6, maximize=maximize)
+    p, m1, v1 = p0.copy(), np.zeros(n), np.zeros(n)
+    for t in range(1, 5):
+        g = rng.standard_normal(pos.size)
+        w.grad = torch.tensor(g, dtype=torch.float64)
+        opt.step()
+        p, m1, v1 = oracle.masked_adam(p, m1, v1, g, t, lr=3e-3, betas=(0.8, 0.95), eps=1e-6, maximize=maximize,
+                                       positions=pos)
+    np.testing.assert_allclose(p[pos], w.detach().numpy(), rtol=1e-13, atol=1e-15)
+    rest = np.setdiff1d(np.arange(n), pos)
+    np.testing.assert_array_equal(p[rest], p0[rest])
