@@ -203,6 +203,63 @@ SPOPS_API int spops_csr_add(const void* A_val, const int32_t* row_offsets, const
                             int itype, int dtype, int32_t m, int32_t n, int32_t nnz, const void* B, void* C,
                             void* stream);
 
+/* ---------------------------------------------------------------- transpose, dB = A^T dC */
+
+/* Scratch bytes spops_csr_transpose needs for nnz entries (radix-sort key and index
+ * buffers and per-block digit histograms). */
+SPOPS_API size_t spops_csr_transpose_workspace_size(int32_t nnz);
+
+/* A^T of the m x n CSR matrix (row_offsets, col_idx, values) as an n x m CSR matrix
+ * (row_offsets_t [n+1] int32, col_idx_t [nnz] = row ids of A, values_t [nnz]).
+ * spops README, operation list: "csr_transpose"; with it the gradient of C = A B with
+ * respect to B is dB = A^T dC, one spops_spmm call on the transpose (torchsparsegradutils
+ * README, "Basic Sparse Matrix Multiplication", gradients of sparse products).
+ * Output is canonical: row j of A^T lists column j of A by ascending row (a stable order
+ * by column), bit-exact and identical run to run. perm [nnz] int32 (may be NULL) receives,
+ * for every position p of A^T, the entry of A placed there, for spops_csr_permute_values.
+ * values and values_t may both be NULL (structure only). itype applies to col_idx and
+ * col_idx_t: int16 needs m, n <= 32768. All buffers are caller-owned device memory; the
+ * outputs must not overlap the inputs. workspace: 16-byte aligned, at least
+ * spops_csr_transpose_workspace_size(nnz) bytes. Returns SPOPS_ERR_INVALID_ARG /
+ * SPOPS_ERR_UNSUPPORTED / SPOPS_ERR_WORKSPACE before queueing anything, SPOPS_ERR_CUDA if
+ * a launch fails. */
+SPOPS_API int spops_csr_transpose(const int32_t* row_offsets, const void* col_idx, const void* values, int itype,
+                                  int dtype, int32_t m, int32_t n, int32_t nnz, int32_t* row_offsets_t,
+                                  void* col_idx_t, void* values_t, int32_t* perm, void* workspace, size_t ws_bytes,
+                                  void* stream);
+
+/* values_t[p] = values[perm[p]] for p < nnz: new values of A carried through a transpose
+ * computed earlier (the structure of a RoSA mask is fixed while its values train). */
+SPOPS_API int spops_csr_permute_values(const void* values, const int32_t* perm, int dtype, int32_t nnz,
+                                       void* values_t, void* stream);
+
+/* ---------------------------------------------------------------- masked Adam */
+
+/* One Adam step on the entries a sparse gradient materializes (SparseAdam page,
+ * tensorplay.optim.sparse_adam.SparseAdam: moments and parameters change only where the
+ * sparse gradient holds a value). With d = grad (negated when maximize != 0):
+ *   exp_avg = beta1 exp_avg + (1 - beta1) d;  exp_avg_sq = beta2 exp_avg_sq + (1 - beta2) d^2;
+ *   param -= lr * (exp_avg / (1 - beta1^step)) / (sqrt(exp_avg_sq / (1 - beta2^step)) + eps)
+ * in fp32. Here the gradient holds one value per parameter entry (count entries, the
+ * values of the parameter's own CSR mask, as for the RoSA adapter): entry g updates
+ * param[g], exp_avg[g], exp_avg_sq[g] in place. param / exp_avg / exp_avg_sq are fp32
+ * device arrays of count entries; grad is count values of grad_dtype. The four arrays must
+ * not overlap. Requires step >= 1, lr >= 0, eps >= 0, 0 <= beta1, beta2 < 1, else
+ * SPOPS_ERR_INVALID_ARG before anything is queued. */
+SPOPS_API int spops_masked_adam(float* param, float* exp_avg, float* exp_avg_sq, const void* grad, int grad_dtype,
+                                int64_t count, int32_t step, double lr, double beta1, double beta2, double eps,
+                                int maximize, void* stream);
+
+/* The same step for a dense m x n row-major fp32 parameter (and moments) with a CSR
+ * gradient (row_offsets, col_idx, nnz values of grad_dtype): entry k of row i updates
+ * position i * n + col_idx[k]; every other position is left untouched (the page's
+ * "parameters of a dense layout with gradients of a sparse layout"). The CSR must be
+ * canonical (no repeated column in a row). */
+SPOPS_API int spops_masked_adam_csr(float* param, float* exp_avg, float* exp_avg_sq, const void* grad, int grad_dtype,
+                                    const int32_t* row_offsets, const void* col_idx, int itype, int32_t m, int32_t n,
+                                    int32_t nnz, int32_t step, double lr, double beta1, double beta2, double eps,
+                                    int maximize, void* stream);
+
 /* ---------------------------------------------------------------- checks */
 
 /* Scratch bytes spops_check_csr needs (a bitmap of m bits for the permutation check). */

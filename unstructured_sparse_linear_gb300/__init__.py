@@ -274,3 +274,115 @@ def check_csr(row_offsets, col_idx, row_idx, n: int) -> None:
         _check(lib.spops_get_device_error(_stream(), ctypes.byref(code)), "get_device_error")
     if code.value != 0:
         raise SpopsError(f"CSR check failed: device error code {code.value}")
+
+
+# ---------------------------------------------------------------- transpose and dB = A^T dC
+
+
+class Transpose:
+    """A^T of a CSR matrix (n x m): row_offsets [n+1] int32, col_idx (row ids of A, the
+    index dtype of A's col_idx), values (or None), perm [nnz] int32 (the entry of A at each
+    position, for refreshing values with ``permute_values``)."""
+
+    def __init__(self, row_offsets, col_idx, values, perm):
+        self.row_offsets = row_offsets
+        self.col_idx = col_idx
+        self.values = values
+        self.perm = perm
+
+
+def csr_transpose(values, row_offsets, col_idx, n: int) -> Transpose:
+    """A^T of the m x n CSR matrix (values may be None for the structure only). Canonical:
+    row j of A^T lists column j of A by ascending row (spops README, "csr_transpose")."""
+    _req(row_offsets, "row_offsets", torch.int32)
+    dev = row_offsets.device
+    _req(col_idx, "col_idx", device=dev)
+    m = row_offsets.numel() - 1
+    nnz = col_idx.numel()
+    it = _itype(col_idx)
+    if values is not None:
+        _req(values, "values", dtypes=_DTYPE, device=dev)
+        if values.numel() != nnz:
+            raise ValueError("values and col_idx lengths differ")
+    dt = _DTYPE[values.dtype] if values is not None else 0
+    n = int(n)
+    ro_t = torch.empty(n + 1, dtype=torch.int32, device=dev)
+    col_t = torch.empty(nnz, dtype=col_idx.dtype, device=dev)
+    val_t = torch.empty(nnz, dtype=values.dtype, device=dev) if values is not None else None
+    perm = torch.empty(nnz, dtype=torch.int32, device=dev)
+    lib = _L()
+    with torch.cuda.device(dev):
+        ws = _ws(lib.spops_csr_transpose_workspace_size(nnz), dev)
+        _check(lib.spops_csr_transpose(_p(row_offsets), _p(col_idx), _p(values), it, dt, m, n, nnz, _p(ro_t), _p(col_t),
+                                       _p(val_t), _p(perm), _p(ws), ws.numel(), _stream()), "csr_transpose")
+    return Transpose(ro_t, col_t, val_t, perm)
+
+
+def permute_values(values, t: Transpose, out: torch.Tensor | None = None) -> torch.Tensor:
+    """New values of A in the order of an existing transpose: out[p] = values[t.perm[p]]."""
+    _req(values, "values", dtypes=_DTYPE)
+    dev = values.device
+    _req(t.perm, "perm", torch.int32, device=dev)
+    nnz = t.perm.numel()
+    if values.numel() != nnz:
+        raise ValueError("values and the transpose have different nnz")
+    res = out if out is not None else torch.empty(nnz, dtype=values.dtype, device=dev)
+    _req(res, "out", values.dtype, device=dev)
+    with torch.cuda.device(dev):
+        _check(_L().spops_csr_permute_values(_p(values), _p(t.perm), _DTYPE[values.dtype], nnz, _p(res), _stream()),
+               "csr_permute_values")
+    return res
+
+
+def spmm_grad_b(A_val, A_row_offsets, A_col_indices, dC, n: int, transpose: Transpose | None = None,
+                path: str = "auto"):
+    """dB = A^T @ dC, the gradient of C = A @ B (A m x n in CSR) with respect to B: the
+    transpose (built here unless given; its values are refreshed from A_val), its nnz-sorted
+    row permutation, and one spmm of the transpose."""
+    t = transpose if transpose is not None else csr_transpose(A_val, A_row_offsets, A_col_indices, n)
+    vals = t.values if (transpose is None and t.values is not None) else permute_values(A_val, t)
+    idx_dtype = t.col_idx.dtype
+    row_idx = sort_rows(t.row_offsets, nnz=t.col_idx.numel(), index_dtype=idx_dtype)
+    return spmm(vals, t.row_offsets, row_idx, t.col_idx, dC, int(n), path=path)
+
+
+# ---------------------------------------------------------------- masked Adam
+
+
+def masked_adam(param, exp_avg, exp_avg_sq, grad, step: int, lr: float = 1e-3, betas=(0.9, 0.999), eps: float = 1e-8,
+                maximize: bool = False, row_offsets=None, col_idx=None):
+    """One Adam step, in place, on the entries the sparse gradient materializes (SparseAdam
+    page: moments and parameters move only under the gradient's mask).
+    Without row_offsets: param / exp_avg / exp_avg_sq (fp32) and grad hold one value per
+    entry of one CSR mask (the RoSA adapter's values). With row_offsets / col_idx: param and
+    the moments are dense m x n fp32 and grad holds the CSR gradient's values."""
+    _req(param, "param", torch.float32)
+    dev = param.device
+    _req(exp_avg, "exp_avg", torch.float32, device=dev)
+    _req(exp_avg_sq, "exp_avg_sq", torch.float32, device=dev)
+    _req(grad, "grad", dtypes=_DTYPE, device=dev)
+    b1, b2 = float(betas[0]), float(betas[1])
+    lib = _L()
+    with torch.cuda.device(dev):
+        if row_offsets is None:
+            if not (param.numel() == exp_avg.numel() == exp_avg_sq.numel() == grad.numel()):
+                raise ValueError("param, exp_avg, exp_avg_sq and grad must have the same number of entries")
+            _check(lib.spops_masked_adam(_p(param), _p(exp_avg), _p(exp_avg_sq), _p(grad), _DTYPE[grad.dtype],
+                                         param.numel(), int(step), float(lr), b1, b2, float(eps), int(bool(maximize)),
+                                         _stream()), "masked_adam")
+        else:
+            _req(row_offsets, "row_offsets", torch.int32, device=dev)
+            _req(col_idx, "col_idx", device=dev)
+            if param.dim() != 2 or exp_avg.shape != param.shape or exp_avg_sq.shape != param.shape:
+                raise ValueError("param and moments must be the same 2-D shape")
+            m, n = param.shape
+            if row_offsets.numel() != m + 1 or grad.numel() != col_idx.numel():
+                raise ValueError("row_offsets / grad do not match param / col_idx")
+            _check(lib.spops_masked_adam_csr(_p(param), _p(exp_avg), _p(exp_avg_sq), _p(grad), _DTYPE[grad.dtype],
+                                             _p(row_offsets), _p(col_idx), _itype(col_idx), m, n, col_idx.numel(),
+                                             int(step), float(lr), b1, b2, float(eps), int(bool(maximize)), _stream()),
+                   "masked_adam_csr")
+    return param
+
+
+__all__ += ["Transpose", "csr_transpose", "permute_values", "spmm_grad_b", "masked_adam"]

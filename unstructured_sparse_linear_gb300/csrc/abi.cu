@@ -128,6 +128,26 @@ bool overlaps(const void* a, size_t abytes, const void* b, size_t bbytes) {
     return x < y + bbytes && y < x + abytes;
 }
 
+int check_adam(const float* param, const float* exp_avg, const float* exp_avg_sq, const void* grad, int grad_dtype,
+               int64_t entries, int64_t grad_count, int32_t step, double lr, double beta1, double beta2, double eps) {
+    if (grad_dtype < SPOPS_F32 || grad_dtype > SPOPS_BF16)
+        return fail(SPOPS_ERR_INVALID_ARG, "grad_dtype %d is not a spops_dtype", grad_dtype);
+    if (step < 1) return fail(SPOPS_ERR_INVALID_ARG, "step must be >= 1 (got %d)", step);
+    if (!(lr >= 0.0) || !(eps >= 0.0)) return fail(SPOPS_ERR_INVALID_ARG, "need lr >= 0 and eps >= 0");
+    if (!(beta1 >= 0.0 && beta1 < 1.0) || !(beta2 >= 0.0 && beta2 < 1.0))
+        return fail(SPOPS_ERR_INVALID_ARG, "betas must lie in [0, 1)");
+    if (entries == 0 || grad_count == 0) return SPOPS_OK;
+    if (!param || !exp_avg || !exp_avg_sq || !grad) return fail(SPOPS_ERR_INVALID_ARG, "a state or gradient pointer is NULL");
+    const size_t gs = dtype_size(grad_dtype);
+    if (!aligned(param, 4) || !aligned(exp_avg, 4) || !aligned(exp_avg_sq, 4) || !aligned(grad, gs))
+        return fail(SPOPS_ERR_INVALID_ARG, "misaligned state or gradient");
+    const size_t sb = (size_t)entries * 4, gb = (size_t)grad_count * gs;
+    if (overlaps(param, sb, exp_avg, sb) || overlaps(param, sb, exp_avg_sq, sb) || overlaps(exp_avg, sb, exp_avg_sq, sb) ||
+        overlaps(param, sb, grad, gb) || overlaps(exp_avg, sb, grad, gb) || overlaps(exp_avg_sq, sb, grad, gb))
+        return fail(SPOPS_ERR_INVALID_ARG, "param, exp_avg, exp_avg_sq and grad must not overlap");
+    return SPOPS_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -268,6 +288,79 @@ int spops_csr_add(const void* A_val, const int32_t* row_offsets, const void* row
     if (B != C && overlaps(B, bytes, C, bytes)) return fail(SPOPS_ERR_INVALID_ARG, "C partially overlaps B");
     return cuda_status(launch_csr_add(dtype, itype, A_val, row_offsets, col_idx, m, n, nnz, B, C, (cudaStream_t)stream),
                        "csr_add launch");
+}
+
+size_t spops_csr_transpose_workspace_size(int32_t nnz) { return csr_transpose_workspace_bytes(nnz); }
+
+int spops_csr_transpose(const int32_t* row_offsets, const void* col_idx, const void* values, int itype, int dtype,
+                        int32_t m, int32_t n, int32_t nnz, int32_t* row_offsets_t, void* col_idx_t, void* values_t,
+                        int32_t* perm, void* workspace, size_t ws_bytes, void* stream) {
+    int st = check_common(itype, dtype, m, n, nnz, values, row_offsets, nullptr, col_idx, false, false);
+    if (st != SPOPS_OK) return st;
+    if ((values == nullptr) != (values_t == nullptr))
+        return fail(SPOPS_ERR_INVALID_ARG, "values and values_t must both be given or both be NULL");
+    if (!row_offsets_t || !aligned(row_offsets_t, 4)) return fail(SPOPS_ERR_INVALID_ARG, "row_offsets_t is NULL or misaligned");
+    const size_t is = itype_size(itype), ds = dtype_size(dtype);
+    if (nnz > 0) {
+        if (!col_idx_t || !aligned(col_idx_t, is)) return fail(SPOPS_ERR_INVALID_ARG, "col_idx_t is NULL or misaligned");
+        if (values && (!aligned(values, ds) || !aligned(values_t, ds)))
+            return fail(SPOPS_ERR_INVALID_ARG, "values or values_t is misaligned");
+        if (perm && !aligned(perm, 4)) return fail(SPOPS_ERR_INVALID_ARG, "perm is misaligned");
+        const void* outs[3] = {col_idx_t, values_t, perm};
+        const size_t osz[3] = {(size_t)nnz * is, (size_t)nnz * ds, (size_t)nnz * 4};
+        const void* ins[3] = {col_idx, values, row_offsets};
+        const size_t isz[3] = {(size_t)nnz * is, (size_t)nnz * ds, (size_t)(m + 1) * 4};
+        for (int a = 0; a < 3; ++a)
+            for (int b = 0; b < 3; ++b)
+                if (outs[a] && ins[b] && overlaps(outs[a], osz[a], ins[b], isz[b]))
+                    return fail(SPOPS_ERR_INVALID_ARG, "an output of csr_transpose overlaps an input");
+        if (!workspace || !aligned(workspace, 16) || ws_bytes < spops_csr_transpose_workspace_size(nnz))
+            return fail(SPOPS_ERR_WORKSPACE, "csr_transpose needs a 16-byte aligned workspace of %zu bytes (got %zu)",
+                        spops_csr_transpose_workspace_size(nnz), ws_bytes);
+    }
+    return cuda_status(launch_csr_transpose(dtype, itype, row_offsets, col_idx, values, m, n, nnz, row_offsets_t,
+                                            col_idx_t, values_t, perm, workspace, (cudaStream_t)stream),
+                       "csr_transpose launch");
+}
+
+int spops_csr_permute_values(const void* values, const int32_t* perm, int dtype, int32_t nnz, void* values_t,
+                             void* stream) {
+    if (dtype < SPOPS_F32 || dtype > SPOPS_BF16) return fail(SPOPS_ERR_INVALID_ARG, "dtype %d is not a spops_dtype", dtype);
+    if (nnz < 0) return fail(SPOPS_ERR_INVALID_ARG, "negative nnz=%d", nnz);
+    if (nnz == 0) return ok();
+    const size_t ds = dtype_size(dtype);
+    if (!values || !perm || !values_t || !aligned(values, ds) || !aligned(values_t, ds) || !aligned(perm, 4))
+        return fail(SPOPS_ERR_INVALID_ARG, "values, perm or values_t is NULL or misaligned");
+    if (overlaps(values_t, (size_t)nnz * ds, values, (size_t)nnz * ds) ||
+        overlaps(values_t, (size_t)nnz * ds, perm, (size_t)nnz * 4))
+        return fail(SPOPS_ERR_INVALID_ARG, "values_t overlaps an input");
+    return cuda_status(launch_permute_values(dtype, values, perm, nnz, values_t, (cudaStream_t)stream),
+                       "csr_permute_values launch");
+}
+
+int spops_masked_adam(float* param, float* exp_avg, float* exp_avg_sq, const void* grad, int grad_dtype,
+                      int64_t count, int32_t step, double lr, double beta1, double beta2, double eps, int maximize,
+                      void* stream) {
+    if (count < 0) return fail(SPOPS_ERR_INVALID_ARG, "negative count");
+    int st = check_adam(param, exp_avg, exp_avg_sq, grad, grad_dtype, count, count, step, lr, beta1, beta2, eps);
+    if (st != SPOPS_OK) return st;
+    if (count == 0) return ok();
+    return cuda_status(launch_masked_adam(grad_dtype, param, exp_avg, exp_avg_sq, grad, count, step, lr, beta1, beta2,
+                                          eps, maximize, (cudaStream_t)stream),
+                       "masked_adam launch");
+}
+
+int spops_masked_adam_csr(float* param, float* exp_avg, float* exp_avg_sq, const void* grad, int grad_dtype,
+                          const int32_t* row_offsets, const void* col_idx, int itype, int32_t m, int32_t n, int32_t nnz,
+                          int32_t step, double lr, double beta1, double beta2, double eps, int maximize, void* stream) {
+    int st = check_common(itype, grad_dtype, m, n, nnz, grad, row_offsets, nullptr, col_idx, false, false);
+    if (st != SPOPS_OK) return st;
+    st = check_adam(param, exp_avg, exp_avg_sq, grad, grad_dtype, (int64_t)m * n, nnz, step, lr, beta1, beta2, eps);
+    if (st != SPOPS_OK) return st;
+    if (nnz == 0 || (int64_t)m * n == 0) return ok();
+    return cuda_status(launch_masked_adam_csr(grad_dtype, itype, param, exp_avg, exp_avg_sq, grad, row_offsets, col_idx,
+                                              m, n, step, lr, beta1, beta2, eps, maximize, (cudaStream_t)stream),
+                       "masked_adam_csr launch");
 }
 
 size_t spops_check_csr_workspace_size(int32_t m) { return align_up(((size_t)(m > 0 ? m : 0) + 31) / 32 * 4, 256) + 16; }

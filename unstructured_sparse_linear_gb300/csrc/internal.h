@@ -61,4 +61,20 @@ cudaError_t launch_sddmm_general(int dt, int it, const int32_t* ro, const void* 
 // kernels skip positions whose panel flag in skip_panels is set (handled on tensor cores).
 constexpr int kPanelRows = 128;
 
+// transpose.cu
+size_t csr_transpose_workspace_bytes(int32_t nnz);
+cudaError_t launch_csr_transpose(int dt, int it, const int32_t* ro, const void* col, const void* val, int32_t m,
+                                 int32_t n, int32_t nnz, int32_t* ro_t, void* row_t, void* val_t, int32_t* perm,
+                                 void* ws, cudaStream_t s);
+cudaError_t launch_permute_values(int dt, const void* val, const int32_t* perm, int32_t nnz, void* val_t,
+                                  cudaStream_t s);
+
+// adam.cu
+cudaError_t launch_masked_adam(int gdt, float* param, float* exp_avg, float* exp_avg_sq, const void* grad,
+                               int64_t count, int32_t step, double lr, double beta1, double beta2, double eps,
+                               int maximize, cudaStream_t s);
+cudaError_t launch_masked_adam_csr(int gdt, int it, float* param, float* exp_avg, float* exp_avg_sq, const void* grad,
+                                   const int32_t* ro, const void* col, int32_t m, int32_t n, int32_t step, double lr,
+                                   double beta1, double beta2, double eps, int maximize, cudaStream_t s);
+
 }  // namespace spops
