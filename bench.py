@@ -338,6 +338,8 @@ def run_gpu(args):
 
     e2e = run_e2e(sp, w, dev, idx, args, flops, ws)
 
+    next_ops = time_next_ops(sp, w, d, idx, stream, pool, flush, nb) if not args.no_next_ops else None
+
     pk = peaks()
     per_op = {}
     for name, times in op_ms.items():
@@ -371,7 +373,7 @@ def run_gpu(args):
                    "spmm_path": args.spmm_path,
                    "l2": "flushed before every step (256 MB write, outside step events)",
                    "parallelism": f"replicas x{ws} (independent problems per GPU)"},
-        "per_op": per_op, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "per_op": per_op, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "next_ops": next_ops,
         "gpu_launches": int(launches_per_step) * args.steps, "clocks": clocks,
         "breakdown_steps": nb, "step_ms_sum_of_ops": round(sum(v["ms"] for v in per_op.values()), 5),
         "wall_s_timed_region": round(wall, 4),
@@ -380,6 +382,72 @@ def run_gpu(args):
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
+
+
+def time_next_ops(sp, w, d, idx, stream, pool, flush, reps):
+    """The operators beyond the step, each as its own graph replayed `reps` times with an
+    L2 flush before every replay: csr_transpose of the mask (structure and values), the
+    value refresh through an existing transpose, dB = A^T dC with the transpose kept (the
+    mask is fixed while its values train: permute values, sort_rows of A^T, SpMM of A^T),
+    and one masked Adam step on the adapter's fp32 values."""
+    pk = peaks()
+    m, n, nnz = w.m, w.n, w.nnz
+    b = w.values.element_size()
+    ib = 2 if idx == torch.int16 else 4
+    ro, col, val = d["ro"], d["col"], d["val"]
+    ops, acc = [], {}
+    with torch.cuda.stream(stream):
+        t = sp.csr_transpose(val, ro, col, n)
+        ops.append(("csr_transpose", lambda: sp.csr_transpose(val, ro, col, n)))
+        acc["csr_transpose"] = (0, 4 * (m + 1) + nnz * (ib + b) + 4 * (n + 1) + nnz * (ib + b + 4))
+        vt = torch.empty_like(val)
+        ops.append(("permute_values", lambda: sp.permute_values(val, t, out=vt)))
+        acc["permute_values"] = (0, nnz * (4 + 2 * b))
+        if w.B is not None:
+            N = int(w.B.shape[1])
+            dC = torch.randn((m, N), device=val.device).to(val.dtype)
+            active_rows = int((np.diff(w.row_offsets.numpy()) > 0).sum())
+            ops.append(("spmm_grad_b", lambda: sp.spmm_grad_b(val, ro, col, dC, n, transpose=t)))
+            acc["spmm_grad_b"] = (2 * nnz * N, nnz * (4 + 2 * b) + 4 * (n + 1) + ib * n + nnz * (ib + b)
+                                  + active_rows * N * b + n * N * b)
+        P = torch.randn(nnz, device=val.device)
+        M1 = torch.zeros(nnz, device=val.device)
+        V1 = torch.zeros(nnz, device=val.device)
+        G = torch.randn(nnz, device=val.device).to(val.dtype)
+        ops.append(("masked_adam", lambda: sp.masked_adam(P, M1, V1, G, 10)))
+        acc["masked_adam"] = (0, nnz * (24 + b))
+        for _, f in ops:
+            f()
+        torch.cuda.synchronize()
+        graphs = []
+        for name, f in ops:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, pool=pool):
+                f()
+            graphs.append((name, g))
+        for _, g in graphs:
+            g.replay()
+        torch.cuda.synchronize()
+        ev = {name: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                     for _ in range(reps)] for name, _ in graphs}
+        for r in range(reps):
+            for name, g in graphs:
+                flush.zero_()
+                ev[name][r][0].record(stream)
+                g.replay()
+                ev[name][r][1].record(stream)
+        torch.cuda.synchronize()
+    out = {}
+    for name, _ in graphs:
+        ts = [a.elapsed_time(e) for a, e in ev[name]]
+        t_avg = sum(ts) / len(ts)
+        fl, by = acc[name]
+        out[name] = {"ms": round(t_avg, 5), "ms_min": round(min(ts), 5),
+                     "GFLOP/s": round(fl / (t_avg * 1e-3) / 1e9, 2) if fl else None,
+                     "GB/s": round(by / (t_avg * 1e-3) / 1e9, 1),
+                     "hbm_frac": round(by / (t_avg * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+                     "algorithmic_bytes": int(by)}
+    return out
 
 
 def run_e2e(sp, w, dev, idx, args, flops, ws):
@@ -510,6 +578,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
     ap.add_argument("--breakdown-steps", type=int, default=200)
     ap.add_argument("--ref-max-steps", type=int, default=20)
+    ap.add_argument("--no-next-ops", action="store_true", help="skip timing csr_transpose / dB / masked Adam")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl != "reference":
