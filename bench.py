@@ -43,6 +43,7 @@ DESCRIPTION = {
     "llama_mlp": "llama_mlp_11008x4096_bf16_0.5pct_uniform_4096tok",
     "zipf": "zipf_131072x131072_fp32_band8192_N128",
     "butterfly": "pixelfly_butterfly_8192x2048_bf16_64x64blocks_8192tok",
+    "spmv": "narrow_spmm_8192x8192_fp16_90pct_sparse_N8",
 }
 
 
@@ -410,6 +411,35 @@ def time_next_ops(sp, w, d, idx, stream, pool, flush, reps):
             ops.append(("spmm_grad_b", lambda: sp.spmm_grad_b(val, ro, col, dC, n, transpose=t)))
             acc["spmm_grad_b"] = (2 * nnz * N, nnz * (4 + 2 * b) + 4 * (n + 1) + ib * n + nnz * (ib + b)
                                   + active_rows * N * b + n * N * b)
+        if w.B is not None and w.A is not None and w.dtype in ("f16", "bf16") and w.B.shape[1] == w.A.shape[1]:
+            # the layer Y^T = W X^T (X^T = B: in x tokens) forward and backward with dY^T = A,
+            # on the mask's values (structure, plans and transpose built once), against the
+            # same layer with a dense weight on cuBLAS (three GEMMs)
+            T = int(w.B.shape[1])
+            Xt, dYt = d["B"], d["A"]
+            ri = sp.sort_rows(ro, nnz=nnz, index_dtype=idx)
+            pl = sp.plan_build(ro, ri, col, n)
+            ri_t = sp.sort_rows(t.row_offsets, nnz=nnz, index_dtype=idx)
+            pl_t = sp.plan_build(t.row_offsets, ri_t, t.col_idx, m)
+
+            def layer_sparse():
+                sp.spmm(val, ro, ri, col, Xt, m, plan=pl)
+                sp.sddmm(ro, ri, col, dYt, Xt, plan=pl)
+                sp.spmm(sp.permute_values(val, t), t.row_offsets, ri_t, t.col_idx, dYt, n, plan=pl_t)
+
+            Wd = torch.zeros((m, n), dtype=val.dtype, device=val.device)
+            rows_of = torch.repeat_interleave(torch.arange(m, device=val.device), torch.diff(ro.long()))
+            Wd[rows_of, col.long()] = val
+
+            def layer_dense():
+                torch.matmul(Wd, Xt)
+                torch.matmul(dYt, Xt.t())
+                torch.matmul(Wd.t(), dYt)
+
+            ops.append(("layer_fwd_bwd_sparse", layer_sparse))
+            acc["layer_fwd_bwd_sparse"] = (3 * 2 * nnz * T, 0)
+            ops.append(("layer_fwd_bwd_dense_cublas", layer_dense))
+            acc["layer_fwd_bwd_dense_cublas"] = (3 * 2 * m * n * T, 0)
         P = torch.randn(nnz, device=val.device)
         M1 = torch.zeros(nnz, device=val.device)
         V1 = torch.zeros(nnz, device=val.device)
@@ -443,10 +473,14 @@ def time_next_ops(sp, w, d, idx, stream, pool, flush, reps):
         t_avg = sum(ts) / len(ts)
         fl, by = acc[name]
         out[name] = {"ms": round(t_avg, 5), "ms_min": round(min(ts), 5),
-                     "GFLOP/s": round(fl / (t_avg * 1e-3) / 1e9, 2) if fl else None,
-                     "GB/s": round(by / (t_avg * 1e-3) / 1e9, 1),
-                     "hbm_frac": round(by / (t_avg * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
-                     "algorithmic_bytes": int(by)}
+                     "GFLOP/s": round(fl / (t_avg * 1e-3) / 1e9, 2) if fl else None}
+        if by:
+            out[name].update({"GB/s": round(by / (t_avg * 1e-3) / 1e9, 1),
+                              "hbm_frac": round(by / (t_avg * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+                              "algorithmic_bytes": int(by)})
+    if "layer_fwd_bwd_sparse" in out:
+        out["layer_speedup_vs_dense"] = round(out["layer_fwd_bwd_dense_cublas"]["ms"] /
+                                              out["layer_fwd_bwd_sparse"]["ms"], 3)
     return out
 
 

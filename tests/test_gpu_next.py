@@ -227,3 +227,85 @@ def test_masked_adam_rejects_bad_hyperparameters():
         sp.masked_adam(x, x.clone(), x.clone(), x.clone(), 1, betas=(1.0, 0.9))
     with pytest.raises(ValueError):
         sp.masked_adam(x, x, x.clone(), x.clone(), 1)  # param and exp_avg alias
+
+
+# ---------------------------------------------------------------- narrow-N SpMM (SpMV)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("N", [1, 3, 8, 16])
+def test_spmm_narrow_all_elements(dtype, N):
+    """N <= 16 takes the warp-per-row streaming kernel (vector or scalar B loads)."""
+    s = wl.spec("spmv", m=3000, n=2500, density=0.05, dtype=dtype, N=N)
+    w = wl.generate(s)
+    it = index_dtype(w.m, w.n)
+    ro, col = w.row_offsets.to(DEV), w.col_idx.to(it).to(DEV)
+    row_idx = torch.from_numpy(oracle.sort_rows(w.row_offsets.numpy())).to(it).to(DEV)
+    C = sp.spmm(w.values.to(DEV), ro, row_idx, col, w.B.to(DEV), w.m)
+    torch.cuda.synchronize()
+    want = oracle.spmm(w.row_offsets.numpy(), w.col_idx.numpy(), w.values, w.B)
+    assert_close(C, want, dtype, f"narrow spmm N={N}")
+
+
+def test_spmm_narrow_integer_exact_unaligned_b_and_empty_rows():
+    s = wl.spec("spmv", m=500, n=700, density=0.03, dtype="f16", N=8)
+    w = wl.generate(s, integer_valued=True)
+    ro, col = w.row_offsets.to(DEV), w.col_idx.to(torch.int16).to(DEV)
+    row_idx = torch.from_numpy(oracle.sort_rows(w.row_offsets.numpy())).to(torch.int16).to(DEV)
+    Bbig = torch.zeros(w.n * 8 + 1, dtype=torch.float16, device=DEV)
+    B = Bbig[1:].view(w.n, 8)  # 2-byte offset: the scalar path
+    B.copy_(w.B.to(DEV))
+    for b in (w.B.to(DEV), B):
+        C = sp.spmm(w.values.to(DEV), ro, row_idx, col, b, w.m)
+        torch.cuda.synchronize()
+        want = oracle.spmm(w.row_offsets.numpy(), w.col_idx.numpy(), w.values, w.B)
+        assert_bits_equal(C, want, "f16", "integer narrow spmm")
+    # a matrix whose rows are all empty but one
+    ro1 = torch.zeros(w.m + 1, dtype=torch.int32)
+    ro1[5:] = 1
+    C = sp.spmm(torch.ones(1, dtype=torch.float16, device=DEV), ro1.to(DEV), row_idx,
+                torch.tensor([3], dtype=torch.int16, device=DEV), w.B.to(DEV), w.m)
+    torch.cuda.synchronize()
+    expect = torch.zeros((w.m, 8), dtype=torch.float16)
+    expect[4] = w.B[3]
+    assert torch.equal(C.cpu(), expect)
+
+
+def test_spmm_narrow_full_size_sampled():
+    """The 8192 x 8192, 90 %-sparse, N = 8 workload: sampled rows against the oracle."""
+    w = wl.generate("spmv")
+    ro, col = w.row_offsets.to(DEV), w.col_idx.to(torch.int16).to(DEV)
+    row_idx = sp.sort_rows(ro, nnz=w.nnz, index_dtype=torch.int16)
+    C = sp.spmm(w.values.to(DEV), ro, row_idx, col, w.B.to(DEV), w.m)
+    torch.cuda.synchronize()
+    rows = np.random.default_rng(15).choice(w.m, 200, replace=False)
+    want = oracle.spmm(w.row_offsets.numpy(), w.col_idx.numpy(), w.values, w.B, rows=rows)
+    assert_close(C[torch.from_numpy(rows).to(DEV)], want, "f16", "spmv full size")
+
+
+# ---------------------------------------------------------------- sparse linear layer (pixelfly)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_sparse_linear_forward_backward(dtype):
+    """Feature-major butterfly layer: Y^T = W X^T, dW on the mask, dX^T = W^T dY^T, all
+    against the oracle; the forward also against a dense fp64 product."""
+    s = wl.spec("butterfly", m=512, n=256, N=136, kd=136, dtype=dtype, mask_kw=(("block", 32),))
+    w = wl.generate(s, operands=("B", "A"))
+    tdt = {"f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    layer = sp.SparseLinear(w.row_offsets.to(DEV), w.col_idx.to(torch.int16).to(DEV), w.values.to(DEV).clone(),
+                            in_features=w.n)
+    Xt = w.B.to(DEV).clone().requires_grad_(True)      # in x tokens
+    G = w.A.to(DEV)                                     # dY^T: out x tokens
+    Yt = layer(Xt)
+    Yt.backward(G)
+    torch.cuda.synchronize()
+    ro, col = w.row_offsets.numpy(), w.col_idx.numpy()
+    assert_close(Yt.detach(), oracle.spmm(ro, col, w.values, w.B), dtype, "layer forward")
+    assert_close(layer.values.grad, oracle.sddmm(ro, col, w.A, w.B), dtype, "layer dW")
+    assert_close(Xt.grad, oracle.spmm_grad_b(ro, col, w.values, w.A, w.n), dtype, "layer dX")
+    dense = torch.zeros((w.m, w.n), dtype=torch.float64)
+    rows = np.repeat(np.arange(w.m), np.diff(ro))
+    dense[rows, col] = w.values.double()
+    ref = (dense @ w.B.double()).numpy()
+    assert_close(Yt.detach(), ref, dtype, "layer forward vs dense fp64")

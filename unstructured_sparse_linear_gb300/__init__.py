@@ -386,3 +386,7 @@ def masked_adam(param, exp_avg, exp_avg_sq, grad, step: int, lr: float = 1e-3, b
 
 
 __all__ += ["Transpose", "csr_transpose", "permute_values", "spmm_grad_b", "masked_adam"]
+
+from .layer import SparseLinear, SparseLinearFunction  # noqa: E402  (uses the functions above)
+
+__all__ += ["SparseLinear", "SparseLinearFunction"]

@@ -35,6 +35,7 @@ constexpr int kKC = 64;       // K elements per pipeline chunk (128 bytes of 16-
 constexpr int kStages = 3;      // 3 x 32 KB ring: two CTAs per SM
 constexpr int kSpNT = 128;    // SpMM: columns of C per tile (UMMA N)
 constexpr int kMaxCluster = 8;
+constexpr int kNarrowMax = 16;  // SpMM with at most this many columns skips the panel path
 // Registers per thread of the SDDMM panel kernel: two CTAs must share an SM (above about 160
 // registers the occupancy calculator and the hardware place only one).
 constexpr int kPanelMaxRegs = 152;  // SDDMM: CTAs (K splits) per tile, the portable cluster limit
@@ -607,8 +608,9 @@ cudaError_t launch_spmm(int dt, int it, const void* vals, const int32_t* ro, con
     PlanView v;
     cudaError_t e = resolve_plan(it, ro, row_idx, col, m, k, nnz, plan, &w, &v, s);
     if (e != cudaSuccess) return e;
-    const bool panels = allow_panels && nnz > 0 && v.panels && dtype_ok(dt) && n % 8 == 0 && aligned16(B) &&
-                        aligned16(C);
+    // Narrow B (n <= 16) is bound by streaming A, not by products: no tensor-core tiles.
+    const bool panels = allow_panels && nnz > 0 && v.panels && dtype_ok(dt) && n % 8 == 0 && n > kNarrowMax &&
+                        aligned16(B) && aligned16(C);
     if (panels) {
         e = dt == kF16 ? run_spmm_panels<__half>(vals, ro, B, n, C, w, v, s)
                        : run_spmm_panels<__nv_bfloat16>(vals, ro, B, n, C, w, v, s);

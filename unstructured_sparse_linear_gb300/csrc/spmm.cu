@@ -24,6 +24,7 @@ namespace {
 
 constexpr int kSpmmThreads = 256;
 constexpr int kSpmmWarps = kSpmmThreads / 32;
+constexpr int kNarrowN = 16;  // B this narrow takes the warp-per-row streaming kernel
 
 template <typename T, int V>
 __device__ __forceinline__ void load_b(const T* __restrict__ Brow, int col0, int N, float (&b)[V]) {
@@ -187,6 +188,106 @@ spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, con
     }
 }
 
+// Narrow B (N <= 16, SpMV at N = 1): streaming A dominates, so a warp takes one row at a
+// time and its lanes read the row's (col, val) pairs coalesced, 32 at a time, each lane
+// gathering its entries' B rows (N elements, at most 64 bytes) and accumulating N fp32
+// sums; a butterfly of shuffles then adds the 32 lanes' sums in a fixed order and lanes
+// 0 .. N-1 write the row's outputs. NV 16-byte vectors per B row when N * sizeof(T) is a
+// multiple of 16 and B is aligned; NV = 0 loads N scalars. Rows go round-robin over the
+// warps in row_idx order (long rows first); empty rows write zeros.
+template <typename T, typename I, int NV>
+__global__ void __launch_bounds__(kSpmmThreads)
+spmm_narrow_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, const I* __restrict__ row_idx,
+                   const I* __restrict__ col, const T* __restrict__ B, T* __restrict__ C, int32_t m, int32_t N,
+                   const uint8_t* __restrict__ skip) {
+    constexpr int kMaxN = 16;
+    constexpr int VE = 16 / (int)sizeof(T);  // elements per 16-byte vector
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * kSpmmThreads + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * kSpmmThreads) >> 5;
+    for (int64_t p = warp; p < m; p += nwarps) {
+        if (skip && skip[p / kPanelRows]) continue;  // uniform across the warp
+        const int row = idx_of(row_idx[p]);
+        const int32_t k0 = ro[row], k1 = ro[row + 1];
+        float acc[kMaxN];
+#pragma unroll
+        for (int c = 0; c < kMaxN; ++c) acc[c] = 0.f;
+        // kU entries per lane per round: their (col, val) loads, then their B rows, are all
+        // in flight before the first FMA.
+        constexpr int kU = NV > 2 ? 2 : 4;
+        for (int32_t kb = k0; kb < k1; kb += 32 * kU) {
+            int jq[kU];
+            float aq[kU];
+            bool ok[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int32_t k = kb + u * 32 + lane;
+                ok[u] = k < k1;
+                jq[u] = ok[u] ? idx_of(col[k]) : 0;
+                aq[u] = ok[u] ? Elt<T>::to_f(vals[k]) : 0.f;
+            }
+            if constexpr (NV > 0) {
+                uint4 raw[kU][NV];
+#pragma unroll
+                for (int u = 0; u < kU; ++u)
+#pragma unroll
+                    for (int q = 0; q < NV; ++q)  // past the row end: zeros, so nothing is added
+                        raw[u][q] = ok[u] ? ld_nc_v4(B + (int64_t)jq[u] * N + q * VE) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int u = 0; u < kU; ++u)
+#pragma unroll
+                    for (int q = 0; q < NV; ++q) {
+                        float f[VE];
+                        Elt<T>::unpack(raw[u][q], f);
+#pragma unroll
+                        for (int e = 0; e < VE; ++e) acc[q * VE + e] = fmaf(aq[u], f[e], acc[q * VE + e]);
+                    }
+            } else {
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    if (!ok[u]) continue;
+                    const T* b = B + (int64_t)jq[u] * N;
+#pragma unroll
+                    for (int c = 0; c < kMaxN; ++c)
+                        if (c < N) acc[c] = fmaf(aq[u], Elt<T>::to_f(b[c]), acc[c]);
+                }
+            }
+        }
+        constexpr int kUsed = NV > 0 ? NV * VE : kMaxN;
+#pragma unroll
+        for (int c = 0; c < kUsed; ++c) {
+            if (NV == 0 && c >= N) break;
+            float x = acc[c];
+#pragma unroll
+            for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+            acc[c] = x;
+        }
+        T* crow = C + (int64_t)row * N;
+#pragma unroll
+        for (int c = 0; c < kUsed; ++c)
+            if (lane == c && c < N) crow[c] = Elt<T>::from_f(acc[c]);
+    }
+}
+
+template <typename T, typename I>
+cudaError_t run_narrow(const void* vals, const int32_t* ro, const void* row_idx, const void* col, int32_t m,
+                       const void* B, int32_t N, void* C, const uint8_t* skip, cudaStream_t s) {
+    constexpr int VE = 16 / (int)sizeof(T);
+    const int grid = (int)max64(1, min64((int64_t)device_props().sm_count * 8, ((int64_t)m + 7) / 8));
+    const bool vec = (N % VE) == 0 && (uintptr_t)B % 16 == 0;
+    const T* v = static_cast<const T*>(vals);
+    const I* ri = static_cast<const I*>(row_idx);
+    const I* ci = static_cast<const I*>(col);
+    const T* b = static_cast<const T*>(B);
+    T* c = static_cast<T*>(C);
+    if (vec && N / VE == 1) spmm_narrow_kernel<T, I, 1><<<grid, kSpmmThreads, 0, s>>>(v, ro, ri, ci, b, c, m, N, skip);
+    else if (vec && N / VE == 2) spmm_narrow_kernel<T, I, 2><<<grid, kSpmmThreads, 0, s>>>(v, ro, ri, ci, b, c, m, N, skip);
+    else if (vec && N / VE == 4) spmm_narrow_kernel<T, I, 4><<<grid, kSpmmThreads, 0, s>>>(v, ro, ri, ci, b, c, m, N, skip);
+    else spmm_narrow_kernel<T, I, 0><<<grid, kSpmmThreads, 0, s>>>(v, ro, ri, ci, b, c, m, N, skip);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
 int pow2_cover(int64_t units) {
     int g = 1;
     while (g < 32 && g < units) g <<= 1;
@@ -196,6 +297,7 @@ int pow2_cover(int64_t units) {
 template <typename T, typename I>
 cudaError_t run(const void* vals, const int32_t* ro, const void* row_idx, const void* col, int32_t m,
                 const void* B, int32_t N, void* C, const int32_t* bins, const uint8_t* skip, cudaStream_t s) {
+    if (N <= kNarrowN) return run_narrow<T, I>(vals, ro, row_idx, col, m, B, N, C, skip, s);
     constexpr int VV = Elt<T>::kVec;
     const bool vec = ((int64_t)N * sizeof(T)) % 16 == 0 && (uintptr_t)B % 16 == 0 && (uintptr_t)C % 16 == 0;
     auto kern = vec ? spmm_rows_kernel<T, I, VV> : spmm_rows_kernel<T, I, 1>;

@@ -8,55 +8,24 @@
 //
 // Output is canonical: row j of A^T lists column j of A by ascending row, i.e. the entries
 // are ordered stably by column. Steps:
-//   1. column counts with integer atomics (order-free, so the counts are exact), one block
-//      scan over n + 1 counters: ro_t;
-//   2. a stable least-significant-digit radix sort of the entry indices 0..nnz-1 by column,
-//      8 bits per pass (per-block digit histograms, one scan, a stable scatter that ranks
-//      equal digits inside a block with warp match masks);
-//   3. the last pass scatters the finished entries directly: the entry's row (binary search
-//      in row_offsets), its value and its index (perm).
+//   1. a stable least-significant-digit radix sort of the entry indices 0..nnz-1 by column,
+//      8 bits per pass (per-block digit histograms, a two-step parallel scan of them, a
+//      stable scatter that ranks equal digits inside a block with warp match masks);
+//   2. the last pass scatters the finished entries directly: the entry's row (from an
+//      entry -> row map written once, a warp per row), its value and its index (perm), and
+//      keeps the sorted columns;
+//   3. ro_t[j] = the first position whose column is >= j (binary search per j).
 // perm lets later calls move new values through the same structure (csr_permute_values).
 #include "common.cuh"
 #include "internal.h"
+#include "scan.cuh"
 
 namespace spops {
 namespace {
 
 constexpr int kTThreads = 256;
 constexpr int kTRounds = 8;
-constexpr int kTTile = kTThreads * kTRounds;
 constexpr int kTRadix = 256;
-constexpr int kTScanThreads = 1024;
-
-template <typename I>
-__global__ void __launch_bounds__(256) col_count_kernel(const I* __restrict__ col, int32_t nnz,
-                                                       int32_t* __restrict__ cnt) {
-    for (int32_t k = blockIdx.x * blockDim.x + threadIdx.x; k < nnz; k += gridDim.x * blockDim.x)
-        atomicAdd(&cnt[idx_of(col[k]) + 1], 1);
-}
-
-// Inclusive scan, in place, of `total` int32 counters with one block (cnt[0] = 0 stays 0,
-// so the result is the exclusive prefix of the column counts: row offsets of A^T).
-__global__ void __launch_bounds__(kTScanThreads) scan_counts_kernel(int32_t* __restrict__ cnt, int32_t total) {
-    __shared__ int32_t part[kTScanThreads];
-    const int32_t per = (total + kTScanThreads - 1) / kTScanThreads;
-    const int32_t b = threadIdx.x * per, e = min(total, b + per);
-    int32_t s = 0;
-    for (int32_t i = b; i < e; ++i) s += cnt[i];
-    part[threadIdx.x] = s;
-    __syncthreads();
-    for (int off = 1; off < kTScanThreads; off <<= 1) {
-        const int32_t v = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
-        __syncthreads();
-        part[threadIdx.x] += v;
-        __syncthreads();
-    }
-    int32_t run = threadIdx.x ? part[threadIdx.x - 1] : 0;
-    for (int32_t i = b; i < e; ++i) {
-        run += cnt[i];
-        cnt[i] = run;
-    }
-}
 
 // Key of position i in a pass: the column of entry i (first pass) or the carried key.
 template <typename I>
@@ -66,13 +35,13 @@ __device__ __forceinline__ uint32_t tkey(const I* col, const uint32_t* keys_in, 
 
 template <typename I>
 __global__ void __launch_bounds__(kTThreads)
-tr_hist_kernel(const I* __restrict__ col, const uint32_t* __restrict__ keys_in, int32_t nnz, int shift,
+tr_hist_kernel(const I* __restrict__ col, const uint32_t* __restrict__ keys_in, int32_t nnz, int shift, int rounds,
                uint32_t* __restrict__ hist) {
     __shared__ uint32_t cnt[kTRadix];
     cnt[threadIdx.x] = 0;
     __syncthreads();
-    const int32_t base = blockIdx.x * kTTile;
-    for (int r = 0; r < kTRounds; ++r) {
+    const int32_t base = blockIdx.x * rounds * kTThreads;
+    for (int r = 0; r < rounds; ++r) {
         const int32_t i = base + r * kTThreads + threadIdx.x;
         if (i < nnz) atomicAdd(&cnt[(tkey(col, keys_in, i) >> shift) & (kTRadix - 1)], 1u);
     }
@@ -80,38 +49,14 @@ tr_hist_kernel(const I* __restrict__ col, const uint32_t* __restrict__ keys_in, 
     hist[threadIdx.x * gridDim.x + blockIdx.x] = cnt[threadIdx.x];
 }
 
-// Exclusive scan, in place, of `total` uint32 counters with one block.
-__global__ void __launch_bounds__(kTScanThreads) tr_scan_kernel(uint32_t* __restrict__ hist, int32_t total) {
-    __shared__ uint32_t part[kTScanThreads];
-    const int32_t per = (total + kTScanThreads - 1) / kTScanThreads;
-    const int32_t b = threadIdx.x * per, e = min(total, b + per);
-    uint32_t s = 0;
-    for (int32_t i = b; i < e; ++i) s += hist[i];
-    part[threadIdx.x] = s;
-    __syncthreads();
-    for (int off = 1; off < kTScanThreads; off <<= 1) {
-        const uint32_t v = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
-        __syncthreads();
-        part[threadIdx.x] += v;
-        __syncthreads();
-    }
-    uint32_t run = threadIdx.x ? part[threadIdx.x - 1] : 0;
-    for (int32_t i = b; i < e; ++i) {
-        const uint32_t c = hist[i];
-        hist[i] = run;
-        run += c;
-    }
-}
-
-// Row of entry k: the last i with ro[i] <= k (rows with no entries are skipped over).
-__device__ __forceinline__ int32_t row_of(const int32_t* __restrict__ ro, int32_t m, int32_t k) {
-    int32_t lo = 0, hi = m;  // ro[lo] <= k < ro[hi]
-    while (hi - lo > 1) {
-        const int32_t mid = (lo + hi) >> 1;
-        if (__ldg(ro + mid) <= k) lo = mid;
-        else hi = mid;
-    }
-    return lo;
+// entry_row[k] = the row of entry k: a warp per row writes its id over the row's entries.
+__global__ void __launch_bounds__(256) tr_entry_rows_kernel(const int32_t* __restrict__ ro, int32_t m,
+                                                           int32_t* __restrict__ entry_row) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t i = warp; i < m; i += nwarps)
+        for (int32_t k = ro[i] + lane; k < ro[i + 1]; k += 32) entry_row[k] = (int32_t)i;
 }
 
 // Stable scatter of one pass. Intermediate passes carry (key, entry index); the last pass
@@ -119,19 +64,22 @@ __device__ __forceinline__ int32_t row_of(const int32_t* __restrict__ ro, int32_
 template <typename T, typename I>
 __global__ void __launch_bounds__(kTThreads)
 tr_scatter_kernel(const I* __restrict__ col, const uint32_t* __restrict__ keys_in, const int32_t* __restrict__ vals_in,
-                  int32_t nnz, int shift, const uint32_t* __restrict__ offsets, uint32_t* __restrict__ keys_out,
-                  int32_t* __restrict__ vals_out, const int32_t* __restrict__ ro, int32_t m,
-                  const T* __restrict__ val, I* __restrict__ row_t, T* __restrict__ val_t, int32_t* __restrict__ perm) {
+                  int32_t nnz, int shift, int rounds, const uint32_t* __restrict__ offsets,
+                  const uint32_t* __restrict__ sums, uint32_t* __restrict__ keys_out, int32_t* __restrict__ vals_out,
+                  bool last, const int32_t* __restrict__ entry_row, const T* __restrict__ val, I* __restrict__ row_t,
+                  T* __restrict__ val_t, int32_t* __restrict__ perm) {
     __shared__ uint32_t warp_cnt[kTThreads / 32][kTRadix];
     __shared__ uint32_t running[kTRadix];
     __shared__ uint32_t dbase[kTRadix];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     running[tid] = 0;
-    dbase[tid] = offsets[tid * gridDim.x + blockIdx.x];
+    {
+        const int64_t at = (int64_t)tid * gridDim.x + blockIdx.x;
+        dbase[tid] = offsets[at] + sums[at / kScanChunk];
+    }
     const uint32_t lt_mask = (1u << lane) - 1u;
-    const int32_t base = blockIdx.x * kTTile;
-    const bool last = keys_out == nullptr;
-    for (int r = 0; r < kTRounds; ++r) {
+    const int32_t base = blockIdx.x * rounds * kTThreads;
+    for (int r = 0; r < rounds; ++r) {
 #pragma unroll
         for (int w = 0; w < kTThreads / 32; ++w) warp_cnt[w][tid] = 0;
         __syncthreads();
@@ -162,11 +110,11 @@ tr_scatter_kernel(const I* __restrict__ col, const uint32_t* __restrict__ keys_i
         __syncthreads();
         if (valid) {
             const uint32_t pos = dbase[d] + warp_cnt[warp][d] + rank;
+            keys_out[pos] = key;
             if (!last) {
-                keys_out[pos] = key;
                 vals_out[pos] = k;
             } else {
-                row_t[pos] = static_cast<I>(row_of(ro, m, k));
+                row_t[pos] = static_cast<I>(entry_row[k]);
                 if (val_t) val_t[pos] = val[k];
                 if (perm) perm[pos] = k;
             }
@@ -175,11 +123,33 @@ tr_scatter_kernel(const I* __restrict__ col, const uint32_t* __restrict__ keys_i
     }
 }
 
+// ro_t[j] = number of entries with column < j: a lower bound of j in the sorted columns.
+__global__ void __launch_bounds__(256) tr_offsets_kernel(const uint32_t* __restrict__ keys, int32_t nnz, int32_t n,
+                                                        int32_t* __restrict__ ro_t) {
+    for (int32_t j = blockIdx.x * blockDim.x + threadIdx.x; j <= n; j += gridDim.x * blockDim.x) {
+        int32_t lo = 0, hi = nnz;  // first position with keys[p] >= j lies in [lo, hi]
+        while (lo < hi) {
+            const int32_t mid = (lo + hi) >> 1;
+            if (keys[mid] < (uint32_t)j) lo = mid + 1;
+            else hi = mid;
+        }
+        ro_t[j] = lo;
+    }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) permute_values_kernel(const T* __restrict__ val, const int32_t* __restrict__ perm,
                                                             int32_t nnz, T* __restrict__ val_t) {
     for (int32_t p = blockIdx.x * blockDim.x + threadIdx.x; p < nnz; p += gridDim.x * blockDim.x)
         val_t[p] = val[perm[p]];
+}
+
+// Entries per CTA = rounds * 256: enough CTAs to fill the GPU twice for small matrices,
+// up to 8 rounds (2048 entries) per CTA for large ones.
+int tr_rounds(int32_t nnz) {
+    const int64_t target = (int64_t)device_props().sm_count * 2 * kTThreads;
+    const int64_t r = nnz / (target > 0 ? target : 1);
+    return (int)max64(1, min64(kTRounds, r));
 }
 
 int bits_for(uint32_t x) {
@@ -195,33 +165,41 @@ cudaError_t run_transpose(const int32_t* ro, const void* col_v, const void* val_
     const T* val = static_cast<const T*>(val_v);
     I* row_t = static_cast<I*>(row_t_v);
     T* val_t = static_cast<T*>(val_t_v);
-    cudaError_t e = cudaMemsetAsync(ro_t, 0, (size_t)(n + 1) * sizeof(int32_t), s);
-    if (e != cudaSuccess) return e;
-    if (nnz == 0) return cudaSuccess;
-    const int sms = device_props().sm_count;
-    const int gcount = (int)min64((int64_t)sms * 8, ((int64_t)nnz + 255) / 256);
-    col_count_kernel<I><<<gcount, 256, 0, s>>>(col, nnz, ro_t);
-    scan_counts_kernel<<<1, kTScanThreads, 0, s>>>(ro_t, n + 1);
-    int launches = 2;
-
+    if (nnz == 0) {
+        cudaError_t e = cudaMemsetAsync(ro_t, 0, (size_t)(n + 1) * sizeof(int32_t), s);
+        return e;
+    }
     const int passes = max(1, (bits_for((uint32_t)(n - 1)) + 7) / 8);
-    const int nb = (nnz + kTTile - 1) / kTTile;
+    const int rounds = tr_rounds(nnz);
+    const int nb = (nnz + rounds * kTThreads - 1) / (rounds * kTThreads);
+    const int64_t counters = (int64_t)nb * kTRadix;
+    const int nchunks = (int)scan_chunks(counters);
     const size_t arr = align_up((size_t)nnz * 4, 256);
     char* w = static_cast<char*>(ws);
     uint32_t* keys[2] = {reinterpret_cast<uint32_t*>(w), reinterpret_cast<uint32_t*>(w + arr)};
     int32_t* vals[2] = {reinterpret_cast<int32_t*>(w + 2 * arr), reinterpret_cast<int32_t*>(w + 3 * arr)};
     uint32_t* hist = reinterpret_cast<uint32_t*>(w + 4 * arr);
+    uint32_t* sums = reinterpret_cast<uint32_t*>(w + 4 * arr + align_up((size_t)counters * 4, 256));
+    // entry -> row map, after the scan sums
+    int32_t* entry_row = reinterpret_cast<int32_t*>(reinterpret_cast<char*>(sums) +
+                                                    align_up((size_t)scan_chunks(counters) * 4, 256));
+    const int sms = device_props().sm_count;
+    tr_entry_rows_kernel<<<(int)min64((int64_t)sms * 8, ((int64_t)m + 7) / 8), 256, 0, s>>>(ro, m, entry_row);
+    int launches = 1;
     for (int p = 0; p < passes; ++p) {
         const uint32_t* kin = p == 0 ? nullptr : keys[(p - 1) & 1];
         const int32_t* vin = p == 0 ? nullptr : vals[(p - 1) & 1];
         const bool last = p == passes - 1;
-        tr_hist_kernel<I><<<nb, kTThreads, 0, s>>>(col, kin, nnz, 8 * p, hist);
-        tr_scan_kernel<<<1, kTScanThreads, 0, s>>>(hist, nb * kTRadix);
-        tr_scatter_kernel<T, I><<<nb, kTThreads, 0, s>>>(col, kin, vin, nnz, 8 * p, hist, last ? nullptr : keys[p & 1],
-                                                         last ? nullptr : vals[p & 1], ro, m, val, row_t, val_t, perm);
-        launches += 3;
+        tr_hist_kernel<I><<<nb, kTThreads, 0, s>>>(col, kin, nnz, 8 * p, rounds, hist);
+        chunk_scan_kernel<<<nchunks, kScanThreads1k, 0, s>>>(hist, counters, sums);
+        chunk_sums_kernel<<<1, kScanThreads1k, 0, s>>>(sums, nchunks);
+        tr_scatter_kernel<T, I><<<nb, kTThreads, 0, s>>>(col, kin, vin, nnz, 8 * p, rounds, hist, sums, keys[p & 1],
+                                                         vals[p & 1], last, entry_row, val, row_t, val_t, perm);
+        launches += 4;
     }
-    count_launches(launches);
+    const int grid = (int)min64((int64_t)sms * 4, ((int64_t)n + 256) / 256);
+    tr_offsets_kernel<<<grid, 256, 0, s>>>(keys[(passes - 1) & 1], nnz, n, ro_t);
+    count_launches(launches + 1);
     return cudaGetLastError();
 }
 
@@ -237,8 +215,9 @@ cudaError_t run_tr_dt(int it, const int32_t* ro, const void* col, const void* va
 size_t csr_transpose_workspace_bytes(int32_t nnz) {
     if (nnz <= 0) return 256;
     const size_t arr = align_up((size_t)nnz * 4, 256);
-    const size_t nb = ((size_t)nnz + kTTile - 1) / kTTile;
-    return 4 * arr + align_up(nb * kTRadix * 4, 256);
+    const size_t nb = ((size_t)nnz + kTThreads - 1) / kTThreads;  // the most CTAs (one round each)
+    const size_t counters = nb * kTRadix;
+    return 5 * arr + align_up(counters * 4, 256) + align_up((size_t)scan_chunks((int64_t)counters) * 4, 256);
 }
 
 cudaError_t launch_csr_transpose(int dt, int it, const int32_t* ro, const void* col, const void* val, int32_t m,

@@ -205,6 +205,8 @@ SPECS = {
     "zipf": Spec("zipf", 3, "f32", 131072, 131072, "zipf", 0.0, ("uniform", 1.0), N=128, kd=0, w_sigma=None),
     "butterfly": Spec("butterfly", 4, "bf16", 8192, 2048, "butterfly", 0.0, ("normal", 0.02), N=8192, kd=8192,
                       w_sigma=None),
+    # narrow-N SpMM (an SpMV regime): 8192 x 8192 at 90 % sparsity, 8 right-hand sides
+    "spmv": Spec("spmv", 5, "f16", 8192, 8192, "uniform", 0.1, ("normal", 0.02), N=8, kd=0, w_sigma=None),
 }
 CONFIG_ORDER = ["tiny", "rosa", "llama_mlp", "zipf", "butterfly"]
 
