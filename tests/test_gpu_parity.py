@@ -27,6 +27,9 @@ SMALL = {
     "rosa_dense": wl.spec("rosa", m=1500, n=1500, density=0.02, N=264, kd=136),
     # bf16, int32 indices, long K (split-K over 16 chunks of 64)
     "rosa_dense_i32": wl.spec("rosa", m=1500, n=1300, density=0.02, dtype="bf16", N=64, kd=1000),
+    # 200 x 1500 cluster half full: |U| = 1500 panels, SpMM on tensor cores, SDDMM general
+    "rosa_wide": wl.spec("rosa", m=2000, n=3000, density=0.025, N=136, kd=72,
+                         mask_kw=(("row_frac", 0.1), ("col_frac", 0.5))),
 }
 INT32_CASES = ("rosa_i32", "rosa_dense_i32")
 
@@ -287,9 +290,10 @@ def test_full_size_sampled(name):
 
 def expected_plan(ro, col, row_idx, n):
     """The panel rule restated on the host: 128 consecutive row_idx positions per panel;
-    dense when |U| <= 1024, at least 16 non-empty rows, and entries * 4 >= rows * |U|."""
+    filled when it has at least 16 non-empty rows and entries * 4 >= rows * |U|; SDDMM tiles
+    when also |U| <= 1024, a SpMM image when |U| <= 2048 (images all fit the budget here)."""
     m = len(ro) - 1
-    dense = entries = tiles = 0
+    dense = entries = tiles = spmm = 0
     P = (m + 127) // 128
     for p in range(P):
         rows = row_idx[p * 128:(p + 1) * 128]
@@ -297,17 +301,20 @@ def expected_plan(ro, col, row_idx, n):
         nnz_p = sum(len(c) for c in cols)
         ne = sum(1 for c in cols if len(c))
         U = len(np.unique(np.concatenate(cols))) if nnz_p else 0
-        if nnz_p > 0 and U <= 1024 and ne >= 16 and nnz_p * 4 >= ne * U:
+        filled = nnz_p > 0 and ne >= 16 and nnz_p * 4 >= ne * U
+        if filled and U <= 1024:
             dense += 1
             entries += nnz_p
             tiles += (U + 127) // 128
+        if filled and U <= 2048:
+            spmm += 1
     lens = np.diff(ro)
     bins = lambda t: [0, int((lens >= t).sum()), int((lens >= 1).sum()), m]  # noqa: E731
-    return {"dense_panels": dense, "dense_entries": entries, "sddmm_tiles": tiles, "panels": P,
+    return {"dense_panels": dense, "dense_entries": entries, "sddmm_tiles": tiles, "spmm_panels": spmm, "panels": P,
             "bins_spmm": bins(sp.SPMM_LONG_ROW), "bins_sddmm": bins(sp.SDDMM_LONG_ROW)}
 
 
-@pytest.mark.parametrize("name", ["rosa_s", "llama_s", "butterfly_s", "rosa_dense", "rosa_dense_i32"])
+@pytest.mark.parametrize("name", ["rosa_s", "llama_s", "butterfly_s", "rosa_dense", "rosa_dense_i32", "rosa_wide"])
 def test_plan_matches_rule(small_cases, name):
     w = small_cases[name]
     g = to_gpu(w, idx_dtype=torch.int32 if name in INT32_CASES else None)
@@ -316,8 +323,9 @@ def test_plan_matches_rule(small_cases, name):
     want = expected_plan(ro, col, oracle.sort_rows(ro), w.n)
     for k, v in want.items():
         assert got[k] == v, (k, got[k], v)
-    assert got["spmm_panels"] == got["dense_panels"]  # every image fits the default budget here
-    if name != "llama_s":
+    if name == "rosa_wide":  # the SpMM-only panels: |U| between 1024 and 2048
+        assert got["spmm_panels"] >= 1 and got["dense_panels"] == 0
+    elif name != "llama_s":
         assert got["dense_panels"] >= 1  # these cases exercise the tensor-core path
 
 

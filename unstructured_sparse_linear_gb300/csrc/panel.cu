@@ -157,7 +157,7 @@ sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
         {
             const size_t prow_at = (size_t)p * kPM + tid;
             const int my_row = v.prow[prow_at];
-            const int u = v.ulist[(size_t)p * kUCap + u0 + tid];
+            const int u = v.ulist[(size_t)p * kUList + u0 + tid];
             const int32_t* ts = v.ts + prow_at * (kTiles + 1);
             const int32_t kb = ts[t], kn = ts[t + 1];
             const uint4 mk = *reinterpret_cast<const uint4*>(v.tmask + prow_at * (kUCap / 32) + t * (kTileN / 32));
@@ -329,14 +329,14 @@ sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
 template <typename T>
 __global__ void __launch_bounds__(256) densify_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro,
                                                      T* __restrict__ img_base, PlanView v) {
-    __shared__ __align__(16) T stage[kGroupRows][kUCap];
+    __shared__ __align__(16) T stage[kGroupRows][kUList];
     const int p = blockIdx.x / kGroups, grp = blockIdx.x % kGroups;
     if (!v.sp_dense[p]) return;
     const int nU = v.desc[p].y;
     const int upad = (nU + kKC - 1) / kKC * kKC;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint4* st4 = reinterpret_cast<uint4*>(&stage[0][0]);
-    const int row_vec = kUCap * (int)sizeof(T) / 16;
+    const int row_vec = kUList * (int)sizeof(T) / 16;
     for (int x = tid; x < kGroupRows * row_vec; x += 256) {
         if ((x % row_vec) * 16 < upad * (int)sizeof(T)) st4[x] = make_uint4(0, 0, 0, 0);
     }
@@ -368,7 +368,7 @@ spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restric
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t mma_bar[kStages];
     __shared__ uint32_t tmem_base_sh;
-    __shared__ int32_t s_u[kUCap];
+    __shared__ int32_t s_u[kUList];
     uint8_t* smem = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(smem_raw), 1024));
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -396,7 +396,7 @@ spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restric
         const int nk = (nU + kKC - 1) / kKC;
         const T* img = img_base + v.img_slot[p];
         __syncthreads();
-        for (int x = tid; x < nk * kKC; x += kTileThreads) s_u[x] = x < nU ? v.ulist[(size_t)p * kUCap + x] : -1;
+        for (int x = tid; x < nk * kKC; x += kTileThreads) s_u[x] = x < nU ? v.ulist[(size_t)p * kUList + x] : -1;
         bulk_wait_read<0>();  // the previous unit's staged C row has been read out of shared memory
         __syncthreads();
 

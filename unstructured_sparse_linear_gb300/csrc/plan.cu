@@ -15,7 +15,8 @@
 //   1. row groups (8 rows per CTA): row ids per position, per-group counts, and a column
 //      bitmap per 8-row group built with shared-memory atomics; then
 //   2. the last group of a panel to finish: OR the group bitmaps, prefix-sum their
-//      popcounts, list U, decide density; then
+//      popcounts, list U, decide density (for SDDMM tiles |U| <= 1024, for a SpMM image
+//      |U| <= 2048); then
 //   3. the last panel to finish: sum the group counts into row bins, list dense panels and
 //      SDDMM tiles, and assign SpMM image slots within the image budget (in panel order);
 //   4. second kernel, row groups of dense panels: each entry's position in U and, per row,
@@ -169,12 +170,14 @@ __device__ void panel_work(const PlanView& v, int p, uint32_t* sm) {
     }
     __syncthreads();
     const int nnz_p = s_cnt[0], ne = s_cnt[1];
-    const bool dense = nnz_p > 0 && U <= kUCap && ne >= kMinDenseRows && (int64_t)nnz_p * 4 >= (int64_t)ne * U;
+    const bool filled = nnz_p > 0 && ne >= kMinDenseRows && (int64_t)nnz_p * 4 >= (int64_t)ne * U;
+    const bool dense = filled && U <= kUCap;     // SDDMM tiles
+    const bool dense_sp = filled && U <= kUList; // SpMM image
     if (tid == 0) {
-        v.desc[p] = make_int4(dense ? 1 : 0, U, nnz_p, ne);
+        v.desc[p] = make_int4((dense ? 1 : 0) | (dense_sp ? 2 : 0), U, nnz_p, ne);
         v.dense[p] = dense ? 1 : 0;
     }
-    if (!dense) return;
+    if (!dense_sp) return;
     for (int w = tid; w < v.W; w += kPlanThreads) {
         v.bm[(size_t)p * v.W + w] = bm[w];
         v.wbase[(size_t)p * v.W + w] = wb[w];
@@ -182,7 +185,7 @@ __device__ void panel_work(const PlanView& v, int p, uint32_t* sm) {
         int at = wb[w];
         while (bits) {
             const int bit = __ffs(bits) - 1;
-            v.ulist[(size_t)p * kUCap + at++] = w * 32 + bit;
+            v.ulist[(size_t)p * kUList + at++] = w * 32 + bit;
             bits &= bits - 1;
         }
     }
@@ -217,9 +220,10 @@ __device__ void lists_work(const PlanView& v, int64_t img_budget) {
     for (int base = 0; base < v.P; base += blockDim.x) {
         const int p = base + threadIdx.x;
         const int4 d = p < v.P ? v.desc[p] : make_int4(0, 0, 0, 0);
-        const int dn = d.x;
+        const int dn = d.x & 1;          // SDDMM tiles
+        const int dsp = (d.x >> 1) & 1;  // SpMM image candidate
         const int tiles = dn ? (d.y + kTileN - 1) / kTileN : 0;
-        const int img = dn ? kPM * ((d.y + 63) / 64) * 64 : 0;
+        const int img = dsp ? kPM * ((d.y + 63) / 64) * 64 : 0;
         int td, tt, ti, tn;
         const int ed = block_exclusive_scan(dn, sh, &td);
         const int et = block_exclusive_scan(tiles, sh, &tt);
@@ -228,7 +232,7 @@ __device__ void lists_work(const PlanView& v, int64_t img_budget) {
         (void)ed;
         (void)en;
         // image slots in panel order while they fit the budget
-        const bool fits = dn && ci + ei + img <= img_budget;
+        const bool fits = dsp && ci + ei + img <= img_budget;
         int tf;
         const int ef = block_exclusive_scan(fits ? 1 : 0, sh, &tf);
         if (p < v.P) {
@@ -265,7 +269,8 @@ plan_upos_kernel(const int32_t* __restrict__ ro, const I* __restrict__ col, Plan
     static_assert(kMaskWords == 32, "one mask word per lane");
     __shared__ uint32_t rmask[8][kMaskWords];  // one row per warp
     const int p = blockIdx.x / kGroups;
-    if (!v.dense[p]) return;
+    if (!(v.desc[p].x & 2)) return;  // U positions for SpMM-dense panels
+    const bool tiles = v.dense[p];    // tile starts and masks for SDDMM-dense ones (U <= kUCap)
     uint32_t* bm = sm;
     int* wb = reinterpret_cast<int*>(sm + v.W);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -284,19 +289,24 @@ plan_upos_kernel(const int32_t* __restrict__ ro, const I* __restrict__ col, Plan
         rmask[warp][lane] = 0;  // kMaskWords == 32: one word per lane
         __syncwarp();
         if (row < 0) {
-            if (lane <= kTiles) ts[lane] = 0;
-            tm[lane] = 0;
+            if (tiles) {
+                if (lane <= kTiles) ts[lane] = 0;
+                tm[lane] = 0;
+            }
             continue;
         }
         const int32_t k0 = ro[row], k1 = ro[row + 1];
         if (k0 == k1) {
-            if (lane <= kTiles) ts[lane] = k0;
-            tm[lane] = 0;
+            if (tiles) {
+                if (lane <= kTiles) ts[lane] = k0;
+                tm[lane] = 0;
+            }
             continue;
         }
         for (int32_t k = k0 + lane; k < k1; k += 32) {
             const int u = upos_of(idx_of(col[k]));
             v.upos[k] = (uint16_t)u;
+            if (!tiles) continue;
             atomicOr(&rmask[warp][u >> 5], 1u << (u & 31));
             const int t_cur = u / kTileN;
             const int t_prev = k > k0 ? upos_of(idx_of(col[k - 1])) / kTileN : -1;
@@ -305,7 +315,7 @@ plan_upos_kernel(const int32_t* __restrict__ ro, const I* __restrict__ col, Plan
                 for (int t = t_cur + 1; t <= kTiles; ++t) ts[t] = k1;
         }
         __syncwarp();
-        tm[lane] = rmask[warp][lane];
+        if (tiles) tm[lane] = rmask[warp][lane];
     }
 }
 
@@ -340,7 +350,7 @@ PlanLayout plan_layout(int32_t m, int32_t n, int32_t nnz) {
         L.wbase = take(P * W * 4);
         L.desc = take(P * 16);
         L.prow = take(P * kPM * 4);
-        L.ulist = take(P * kUCap * 4);
+        L.ulist = take(P * kUList * 4);
         L.upos = take((size_t)nnz * 2);
         L.ts = take(P * kPM * (kTiles + 1) * 4);
         L.tmask = take(P * kPM * (kUCap / 32) * 4);

@@ -8,14 +8,15 @@
 // when panels are enabled (n <= 65536):
 //   bm_part    uint32[P][16][W] column bitmap of each 8-row group of a panel
 //   bm, wbase  [P][W]          OR-ed bitmap; exclusive prefix of its popcounts
-//   desc       int4[P]         {dense, |U|, entries, non-empty rows}
+//   desc       int4[P]         {dense bits, |U|, entries, non-empty rows}; dense bit 0: SDDMM
+//                              tiles (|U| <= kUCap), bit 1: SpMM image (|U| <= kUList)
 //   prow       int32[P*128]    row id at each panel position (-1 past m)
-//   ulist      int32[P][kUCap] sorted columns of a dense panel
+//   ulist      int32[P][kUList] sorted columns of a dense panel
 //   upos       uint16[nnz]     column position of each entry in its panel's U
 //   ts         int32[P*128][kTiles + 1]  first entry of each 128-column tile of U, per row
 //   tmask      uint32[P*128][kUCap / 32] bit u set when the row has an entry at U position u
 //   dense      uint8[P]        panel runs on tensor cores (SDDMM)
-//   sp_dense   uint8[P]        ... and has a SpMM image slot
+//   sp_dense   uint8[P]        panel has a SpMM image slot (tensor cores for SpMM)
 //   items      int32[P*kTiles] SDDMM work items (panel << 8 | tile)
 //   dlist_sp   int32[P]        panels with an image slot
 //   img_slot   int32[P]        image offset (elements) or -1
@@ -30,7 +31,8 @@
 namespace spops {
 
 constexpr int kPM = kPanelRows;   // rows per panel (UMMA M)
-constexpr int kUCap = 1024;       // most distinct columns of a dense panel
+constexpr int kUCap = 1024;       // most distinct columns of an SDDMM-dense panel (8 tiles of 128)
+constexpr int kUList = 2048;      // most distinct columns of a SpMM-dense panel (the image's K)
 constexpr int kTileN = 128;       // SDDMM tile width over U (UMMA N)
 constexpr int kTiles = kUCap / kTileN;
 constexpr int kGroupRows = 8;     // rows per plan CTA, one per warp (16 groups per panel)
