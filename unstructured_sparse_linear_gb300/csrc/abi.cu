@@ -62,6 +62,44 @@ int* device_error_word() {
 
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
+namespace {
+struct Side {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    bool tried = false;
+};
+thread_local Side g_side[kMaxDevices];
+}  // namespace
+
+cudaStream_t side_fork(cudaStream_t s) {
+    const int d = current_device();
+    if (d < 0 || d >= kMaxDevices) return nullptr;
+    Side& sd = g_side[d];
+    if (!sd.tried) {
+        sd.tried = true;
+        if (cudaStreamCreateWithFlags(&sd.stream, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            sd.stream = nullptr;
+        }
+    }
+    if (!sd.stream) return nullptr;
+    if (cudaEventRecord(sd.fork, s) != cudaSuccess || cudaStreamWaitEvent(sd.stream, sd.fork, 0) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return sd.stream;
+}
+
+cudaError_t side_join(cudaStream_t s) {
+    const int d = current_device();
+    Side& sd = g_side[d];
+    cudaError_t e = cudaEventRecord(sd.join, sd.stream);
+    if (e != cudaSuccess) return e;
+    return cudaStreamWaitEvent(s, sd.join, 0);
+}
+
 int set_last_error(int status, const char* fmt, ...) {
     va_list ap;
     va_start(ap, fmt);

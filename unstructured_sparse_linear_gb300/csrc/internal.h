@@ -24,6 +24,14 @@ const DeviceProps& device_props();
 int* device_error_word();
 // Add n to the process-wide count of kernels this library has launched.
 void count_launches(int n);
+// A second stream for work that is independent of what follows on `s` (the general row
+// kernels beside the tensor-core panels). side_fork records an event on s and makes the
+// calling thread's side stream for the current device wait for it; side_join makes s wait
+// for everything queued on the side stream since. Both are captured into CUDA graphs as a
+// fork and a join. side_fork returns nullptr (run everything on s) if no side stream can
+// be made.
+cudaStream_t side_fork(cudaStream_t s);
+cudaError_t side_join(cudaStream_t s);
 // Record the calling thread's spops_last_error() text (printf format) and return status.
 int set_last_error(int status, const char* fmt, ...);
 
