@@ -172,18 +172,22 @@ class ClockSampler:
 # ------------------------------------------------------------------ profile summary (traffic)
 
 
-def kernel_source_hash(path):
-    return hashlib.sha256(open(os.path.join(ROOT, path), "rb").read()).hexdigest()[:16]
+def kernel_source_hash(paths):
+    """sha256[:16] over the listed source files ('+'-separated), in order."""
+    h = hashlib.sha256()
+    for p in paths.split("+"):
+        h.update(open(os.path.join(ROOT, p), "rb").read())
+    return h.hexdigest()[:16]
 
 
 def recorded_traffic(op: str, workload: str):
-    """Per-launch DRAM bytes of the op's main kernel on this workload from the committed
-    ncu summary, if the kernel source still matches the hash recorded with the counters."""
+    """DRAM bytes per call of the op (its kernels summed) on this workload from the committed
+    ncu summary, if the kernel sources still match the hash recorded with the counters."""
     p = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(p):
         return None
     pat = re.compile(r"\|\s*" + re.escape(workload) + r"\s*\|\s*" + re.escape(op) +
-                     r"\s*\|\s*([\w./]+)\s*\|\s*([0-9a-f]+)\s*\|\s*([0-9]+)\s*\|")
+                     r"\s*\|\s*([\w./+]+)\s*\|\s*([0-9a-f]+)\s*\|\s*([0-9]+)\s*\|")
     for line in open(p):
         mt = pat.match(line)
         if mt:

@@ -98,7 +98,13 @@ spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, con
         const int64_t items = (int64_t)n_long * nch;
         for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
             const int32_t p = (int32_t)(item / nch);
-            if (skip && skip[p / kPanelRows]) continue;  // uniform across the CTA
+            if (skip && skip[p / kPanelRows]) {  // uniform across the CTA
+                // jump to this CTA's first item in the next panel
+                const int64_t next = (int64_t)(p / kPanelRows + 1) * kPanelRows * nch;
+                const int64_t g = gridDim.x;
+                item = next + (((int64_t)blockIdx.x - next) % g + g) % g - g;
+                continue;
+            }
             const int c = (int)(item % nch);
             const int row = idx_of(row_idx[p]);
             const int32_t k0 = ro[row], k1 = ro[row + 1];
