@@ -38,6 +38,8 @@ __global__ void __launch_bounds__(kAddThreads) csr_add_kernel(const T* __restric
     __shared__ int32_t ro_s[kRoCache];
     constexpr int64_t E = kAddTileBytes / sizeof(T);
     const int tid = threadIdx.x;
+    pdl_trigger();
+    pdl_wait();
     const int64_t ntiles = (total + E - 1) / E;
     const int64_t my_tiles = (int64_t)blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
@@ -159,9 +161,9 @@ cudaError_t run(const void* vals, const int32_t* ro, const void* col, int32_t m,
     auto kern = bulk ? csr_add_kernel<T, I, true> : csr_add_kernel<T, I, false>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAddSmem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kAddThreads, kAddSmem, s>>>(static_cast<const T*>(vals), ro, static_cast<const I*>(col), n,
-                                             static_cast<const T*>(B), static_cast<T*>(C), total,
-                                             device_error_word());
+    e = launch_pdl(kern, grid, kAddThreads, kAddSmem, s, static_cast<const T*>(vals), ro, static_cast<const I*>(col), n,
+                   static_cast<const T*>(B), static_cast<T*>(C), total, device_error_word());
+    if (e != cudaSuccess) return e;
     count_launches(1);
     return cudaGetLastError();
 }

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace spops {
 
 enum DType { kF32 = 0, kF16 = 1, kBF16 = 2 };
@@ -34,6 +36,24 @@ cudaStream_t side_fork(cudaStream_t s);
 cudaError_t side_join(cudaStream_t s);
 // Record the calling thread's spops_last_error() text (printf format) and return status.
 int set_last_error(int status, const char* fmt, ...);
+
+// Launch with programmatic stream serialization: the kernel may start while the previous
+// kernel in the stream finishes (its CTAs call pdl_wait before reading earlier results), so
+// consecutive kernels overlap launch latency. Captured into CUDA graphs as programmatic edges.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 inline size_t dtype_size(int dt) { return dt == kF32 ? 4 : 2; }
 inline size_t itype_size(int it) { return it == kIdx16 ? 2 : 4; }

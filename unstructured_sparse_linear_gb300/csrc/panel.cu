@@ -110,6 +110,7 @@ sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
     uint8_t* smem = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(smem_raw), 1024));
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_trigger();
 
     if (warp == 0) tc::tmem_alloc(smem_u32(&tmem_base_sh), kTileN);
     if (tid == 0) {
@@ -120,6 +121,7 @@ sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = tmem_base_sh;
+    pdl_wait();  // the plan and the operands come from earlier kernels
 
     // With at least one tile per two CTAs, K is not split: every CTA takes whole tiles on its
     // own and the cluster barriers become CTA barriers (the choice is the same on every CTA).
@@ -330,6 +332,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) densify_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro,
                                                      T* __restrict__ img_base, PlanView v) {
     __shared__ __align__(16) T stage[kGroupRows][kUList];
+    pdl_trigger();
+    pdl_wait();
     const int p = blockIdx.x / kGroups, grp = blockIdx.x % kGroups;
     if (!v.sp_dense[p]) return;
     const int nU = v.desc[p].y;
@@ -372,6 +376,7 @@ spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restric
     uint8_t* smem = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(smem_raw), 1024));
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5;
+    pdl_trigger();
 
     if (warp == 0) tc::tmem_alloc(smem_u32(&tmem_base_sh), kSpNT);
     if (tid == 0) {
@@ -382,6 +387,7 @@ spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restric
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = tmem_base_sh;
+    pdl_wait();  // the plan and the operands come from earlier kernels
 
     const int D = v.counts()[kCntDenseSp];
     const int ntn = (N + kSpNT - 1) / kSpNT;
@@ -516,18 +522,21 @@ cudaError_t run_sddmm_panels(const void* A, const void* BT, void* out, int32_t k
     int C = nkc < kMaxCluster ? nkc : kMaxCluster;
 
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     cfg.blockDim = dim3(kTileThreads);
     cfg.dynamicSmemBytes = kSdSmem;
     cfg.stream = s;
     int64_t nclusters = min64((int64_t)device_props().sm_count * 2, max_items);
     if (C > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)C;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)C;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
         cfg.gridDim = dim3((unsigned)(C * ((device_props().sm_count * 2) / C)));
         int active = 0;
         e = cudaOccupancyMaxActiveClusters(&active, kern, &cfg);
@@ -537,8 +546,7 @@ cudaError_t run_sddmm_panels(const void* A, const void* BT, void* out, int32_t k
             nclusters = min64((int64_t)(device_props().sm_count * 2) / C, max_items);
         } else {
             C = 1;  // the cluster does not fit: one CTA per tile, no K split
-            cfg.attrs = nullptr;
-            cfg.numAttrs = 0;
+            cfg.numAttrs = 1;
         }
     }
     cfg.gridDim = dim3((unsigned)(nclusters * C));
@@ -552,18 +560,21 @@ cudaError_t run_sddmm_panels(const void* A, const void* BT, void* out, int32_t k
 template <typename T>
 cudaError_t run_spmm_panels(const void* vals, const int32_t* ro, const void* B, int32_t N, void* C, void* img,
                             const PlanView& v, cudaStream_t s) {
-    densify_kernel<T><<<v.P * kGroups, 256, 0, s>>>(static_cast<const T*>(vals), ro, static_cast<T*>(img), v);
+    cudaError_t e = launch_pdl(densify_kernel<T>, v.P * kGroups, 256, 0, s, static_cast<const T*>(vals), ro,
+                               static_cast<T*>(img), v);
+    if (e != cudaSuccess) return e;
     const int ntn = (N + kSpNT - 1) / kSpNT;
     const int grid = (int)min64((int64_t)device_props().sm_count * 2, (int64_t)v.P * ntn);
     auto kern = spmm_panel_kernel<T>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSpSmem);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSpSmem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     const uint32_t idesc = tc::instr_desc_f16(std::is_same<T, __nv_bfloat16>::value ? 1u : 0u, 0, 1, kPM, kSpNT);
-    kern<<<grid, kTileThreads, kSpSmem, s>>>(static_cast<const T*>(B), static_cast<T*>(C), static_cast<const T*>(img),
-                                             N, v, idesc, device_error_word());
+    e = launch_pdl(kern, grid, kTileThreads, kSpSmem, s, static_cast<const T*>(B), static_cast<T*>(C),
+                   static_cast<const T*>(img), N, v, idesc, device_error_word());
     count_launches(2);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -73,6 +73,8 @@ plan_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx, 
     extern __shared__ uint32_t bitmap[];  // 2 W words when panels are enabled (the panel step reuses them)
     __shared__ int red[4][8];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_trigger();
+    pdl_wait();
     const int64_t p0 = (int64_t)blockIdx.x * kGroupRows;
     if (v.panels)
         for (int w = tid; w < v.W; w += kPlanThreads) bitmap[w] = 0;
@@ -268,6 +270,8 @@ plan_upos_kernel(const int32_t* __restrict__ ro, const I* __restrict__ col, Plan
     constexpr int kMaskWords = kUCap / 32;
     static_assert(kMaskWords == 32, "one mask word per lane");
     __shared__ uint32_t rmask[8][kMaskWords];  // one row per warp
+    pdl_trigger();
+    pdl_wait();
     const int p = blockIdx.x / kGroups;
     if (!(v.desc[p].x & 2)) return;  // U positions for SpMM-dense panels
     const bool tiles = v.dense[p];    // tile starts and masks for SDDMM-dense ones (U <= kUCap)
@@ -424,16 +428,18 @@ cudaError_t launch_plan_build(int it, const int32_t* ro, const void* row_idx, co
     }
     cudaError_t e = cudaMemsetAsync(v.done, 0, (size_t)(v.P + 1) * sizeof(int32_t), s);
     if (e != cudaSuccess) return e;
-    if (it == kIdx16)
-        plan_rows_kernel<uint16_t><<<v.ncta, kPlanThreads, smem_rows, s>>>(ro, (const uint16_t*)row_idx,
-                                                                           (const uint16_t*)col, v, img_budget);
-    else
-        plan_rows_kernel<int32_t><<<v.ncta, kPlanThreads, smem_rows, s>>>(ro, (const int32_t*)row_idx,
-                                                                          (const int32_t*)col, v, img_budget);
+    e = it == kIdx16 ? launch_pdl(plan_rows_kernel<uint16_t>, v.ncta, kPlanThreads, smem_rows, s, ro,
+                                  (const uint16_t*)row_idx, (const uint16_t*)col, v, img_budget)
+                     : launch_pdl(plan_rows_kernel<int32_t>, v.ncta, kPlanThreads, smem_rows, s, ro,
+                                  (const int32_t*)row_idx, (const int32_t*)col, v, img_budget);
+    if (e != cudaSuccess) return e;
     int launches = 1;
     if (v.panels) {
-        if (it == kIdx16) plan_upos_kernel<uint16_t><<<v.P * kGroups, kPlanThreads, smem_pan, s>>>(ro, (const uint16_t*)col, v);
-        else plan_upos_kernel<int32_t><<<v.P * kGroups, kPlanThreads, smem_pan, s>>>(ro, (const int32_t*)col, v);
+        e = it == kIdx16 ? launch_pdl(plan_upos_kernel<uint16_t>, v.P * kGroups, kPlanThreads, smem_pan, s, ro,
+                                      (const uint16_t*)col, v)
+                         : launch_pdl(plan_upos_kernel<int32_t>, v.P * kGroups, kPlanThreads, smem_pan, s, ro,
+                                      (const int32_t*)col, v);
+        if (e != cudaSuccess) return e;
         ++launches;
     }
     count_launches(launches);

@@ -94,6 +94,8 @@ sddmm_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx,
                   const T* __restrict__ A, const T* __restrict__ BT, T* __restrict__ out, int32_t kd, int G,
                   const int32_t* __restrict__ bins, const uint8_t* __restrict__ skip) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    pdl_trigger();
+    pdl_wait();
     // Short rows run over every position up to m, not only up to bins[2]: with an unsorted
     // row_idx, rows with entries may sit past the count of non-empty rows.
     const int32_t n_long = bins[1], n_rows = bins[3];
@@ -135,9 +137,9 @@ cudaError_t run(const int32_t* ro, const void* row_idx, const void* col, int32_t
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kSddmmThreads, 0);
     if (e != cudaSuccess) return e;
     const int grid = device_props().sm_count * (occ > 0 ? occ : 1);
-    kern<<<grid, kSddmmThreads, 0, s>>>(ro, static_cast<const I*>(row_idx), static_cast<const I*>(col),
-                                        static_cast<const T*>(A), static_cast<const T*>(BT), static_cast<T*>(out),
-                                        kd, G, bins, skip);
+    e = launch_pdl(kern, grid, kSddmmThreads, 0, s, ro, static_cast<const I*>(row_idx), static_cast<const I*>(col),
+                   static_cast<const T*>(A), static_cast<const T*>(BT), static_cast<T*>(out), kd, G, bins, skip);
+    if (e != cudaSuccess) return e;
     count_launches(1);
     return cudaGetLastError();
 }

@@ -148,6 +148,8 @@ __global__ void __launch_bounds__(kSmallThreads) sort_small_kernel(const int32_t
     __shared__ int32_t sh[32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t lt_mask = (1u << lane) - 1u;
+    pdl_trigger();
+    pdl_wait();
 
     int32_t mx = 0, mn = INT32_MAX;
     for (int32_t i = tid; i < m; i += kSmallThreads) {
@@ -350,10 +352,11 @@ cudaError_t launch_sort_rows(const int32_t* ro, int32_t m, int32_t nnz, void* ro
                             : cudaFuncSetAttribute(sort_small_kernel<int32_t>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmallSortSmem);
         if (e != cudaSuccess) return e;
-        if (it == kIdx16)
-            sort_small_kernel<uint16_t><<<1, kSmallThreads, kSmallSortSmem, s>>>(ro, m, (uint16_t*)row_idx_out);
-        else
-            sort_small_kernel<int32_t><<<1, kSmallThreads, kSmallSortSmem, s>>>(ro, m, (int32_t*)row_idx_out);
+        e = it == kIdx16 ? launch_pdl(sort_small_kernel<uint16_t>, 1, kSmallThreads, kSmallSortSmem, s, ro, m,
+                                      (uint16_t*)row_idx_out)
+                         : launch_pdl(sort_small_kernel<int32_t>, 1, kSmallThreads, kSmallSortSmem, s, ro, m,
+                                      (int32_t*)row_idx_out);
+        if (e != cudaSuccess) return e;
         count_launches(1);
         return cudaGetLastError();
     }

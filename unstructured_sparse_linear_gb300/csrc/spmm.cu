@@ -89,6 +89,8 @@ spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, con
                  const int32_t* __restrict__ bins, const uint8_t* __restrict__ skip) {
     __shared__ float red[kSpmmWarps][32 * V];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    pdl_trigger();
+    pdl_wait();
     const int32_t n_long = bins[1];
 
     // ---- long rows: one CTA per (row, chunk of 32*V columns)
@@ -209,6 +211,8 @@ spmm_narrow_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, c
     constexpr int kMaxN = 16;
     constexpr int VE = 16 / (int)sizeof(T);  // elements per 16-byte vector
     const int lane = threadIdx.x & 31;
+    pdl_trigger();
+    pdl_wait();
     const int64_t warp = ((int64_t)blockIdx.x * kSpmmThreads + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * kSpmmThreads) >> 5;
     for (int64_t p = warp; p < m; p += nwarps) {
@@ -286,10 +290,12 @@ cudaError_t run_narrow(const void* vals, const int32_t* ro, const void* row_idx,
     const I* ci = static_cast<const I*>(col);
     const T* b = static_cast<const T*>(B);
     T* c = static_cast<T*>(C);
-    if (vec && N / VE == 1) spmm_narrow_kernel<T, I, 1><<<grid, kSpmmThreads, 0, s>>>(v, ro, ri, ci, b, c, m, N, skip);
-    else if (vec && N / VE == 2) spmm_narrow_kernel<T, I, 2><<<grid, kSpmmThreads, 0, s>>>(v, ro, ri, ci, b, c, m, N, skip);
-    else if (vec && N / VE == 4) spmm_narrow_kernel<T, I, 4><<<grid, kSpmmThreads, 0, s>>>(v, ro, ri, ci, b, c, m, N, skip);
-    else spmm_narrow_kernel<T, I, 0><<<grid, kSpmmThreads, 0, s>>>(v, ro, ri, ci, b, c, m, N, skip);
+    cudaError_t e;
+    if (vec && N / VE == 1) e = launch_pdl(spmm_narrow_kernel<T, I, 1>, grid, kSpmmThreads, 0, s, v, ro, ri, ci, b, c, m, N, skip);
+    else if (vec && N / VE == 2) e = launch_pdl(spmm_narrow_kernel<T, I, 2>, grid, kSpmmThreads, 0, s, v, ro, ri, ci, b, c, m, N, skip);
+    else if (vec && N / VE == 4) e = launch_pdl(spmm_narrow_kernel<T, I, 4>, grid, kSpmmThreads, 0, s, v, ro, ri, ci, b, c, m, N, skip);
+    else e = launch_pdl(spmm_narrow_kernel<T, I, 0>, grid, kSpmmThreads, 0, s, v, ro, ri, ci, b, c, m, N, skip);
+    if (e != cudaSuccess) return e;
     count_launches(1);
     return cudaGetLastError();
 }
@@ -313,9 +319,9 @@ cudaError_t run(const void* vals, const int32_t* ro, const void* row_idx, const 
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kSpmmThreads, 0);
     if (e != cudaSuccess) return e;
     const int grid = device_props().sm_count * (occ > 0 ? occ : 1);
-    kern<<<grid, kSpmmThreads, 0, s>>>(static_cast<const T*>(vals), ro, static_cast<const I*>(row_idx),
-                                       static_cast<const I*>(col), static_cast<const T*>(B), static_cast<T*>(C), m,
-                                       N, G, bins, skip);
+    e = launch_pdl(kern, grid, kSpmmThreads, 0, s, static_cast<const T*>(vals), ro, static_cast<const I*>(row_idx),
+                   static_cast<const I*>(col), static_cast<const T*>(B), static_cast<T*>(C), m, N, G, bins, skip);
+    if (e != cudaSuccess) return e;
     count_launches(1);
     return cudaGetLastError();
 }
