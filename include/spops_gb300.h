@@ -149,9 +149,10 @@ SPOPS_API size_t spops_plan_size(int32_t m, int32_t n, int32_t nnz);
  *   - the panel decomposition behind the structure-aware paths (README, "Sampled
  *     Dense-Dense Matrix Multiplication": the structure-aware kernel exploits non-zeros
  *     that cluster in a few rows and columns): panels of 128 consecutive row_idx
- *     positions; a panel is dense when the union U of its columns has at most 1024
- *     columns, it has at least 16 non-empty rows, and its entries fill at least a quarter
- *     of (non-empty rows) x |U|. Dense panels run on the tensor cores.
+ *     positions; a panel is filled when it has at least 16 non-empty rows and its entries
+ *     fill at least a quarter of (non-empty rows) x |U|, U the union of its columns. Filled
+ *     panels run SDDMM on the tensor cores when |U| <= 1024 and SpMM when |U| <= 2048
+ *     (and their SpMM image fits the workspace's budget).
  * plan: device buffer of spops_plan_size bytes, 1024-byte aligned, owned by the caller and
  * left unchanged by the operators. Deterministic: the same mask gives the same plan. */
 SPOPS_API int spops_plan_build(const int32_t* row_offsets, const void* row_idx, const void* col_idx, int itype,

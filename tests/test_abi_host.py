@@ -105,3 +105,35 @@ def test_empty_problems_are_no_ops(lib):
     assert lib.spops_spmm(None, FAKE, None, None, 0, 0, 0, 4, 0, FAKE, 4, None, 0, None, None, 0, None) == 0
     assert lib.spops_csr_add(None, FAKE, None, None, 0, 0, 5, 0, 0, None, None, None) == 0
     assert lib.spops_sort_rows(FAKE, 0, 0, None, 0, None, 0, None) == 0
+
+
+def test_widened_operators_reject_bad_arguments_on_host(lib):
+    W = 1 << 30
+    d = ctypes.c_double
+    # csr_transpose: values without values_t; int16 for 40000 columns; workspace too small
+    assert lib.spops_csr_transpose(FAKE, FAKE, FAKE, 0, 0, 4, 4, 4, FAKE, P(0x50000), None, None, FAKE, W, None) == 1
+    assert lib.spops_csr_transpose(FAKE, FAKE, None, 0, 0, 4, 40000, 4, FAKE, P(0x50000), None, None, FAKE, W,
+                                   None) == 2
+    assert lib.spops_csr_transpose(FAKE, FAKE, None, 0, 0, 4, 4, 4, FAKE, P(0x50000), None, None, FAKE, 8, None) == 3
+    # an output overlapping an input
+    assert lib.spops_csr_transpose(FAKE, P(0x50000), None, 0, 0, 4, 4, 4, FAKE, P(0x50002), None, None, FAKE, W,
+                                   None) == 1
+    assert lib.spops_csr_transpose_workspace_size(1000) >= 4 * 1000 * 4
+    # permute_values: bad dtype, negative nnz, output over the input
+    assert lib.spops_csr_permute_values(FAKE, FAKE, 9, 4, P(0x60000), None) == 1
+    assert lib.spops_csr_permute_values(FAKE, FAKE, 0, -1, P(0x60000), None) == 1
+    assert lib.spops_csr_permute_values(P(0x60000), FAKE, 0, 4, P(0x60004), None) == 1
+    # masked Adam: step 0, beta 1, negative lr, aliased state, grad dtype out of range
+    adam = lambda *a: lib.spops_masked_adam(*a)  # noqa: E731
+    args = (P(0x100000), P(0x200000), P(0x300000), P(0x400000), 0, 64)
+    assert adam(*args, 0, d(1e-3), d(0.9), d(0.999), d(1e-8), 0, None) == 1
+    assert adam(*args, 1, d(1e-3), d(1.0), d(0.999), d(1e-8), 0, None) == 1
+    assert adam(*args, 1, d(-1.0), d(0.9), d(0.999), d(1e-8), 0, None) == 1
+    assert adam(P(0x100000), P(0x100000), P(0x300000), P(0x400000), 0, 64, 1, d(1e-3), d(0.9), d(0.999), d(1e-8), 0,
+                None) == 1
+    assert adam(P(0x100000), P(0x200000), P(0x300000), P(0x400000), 7, 64, 1, d(1e-3), d(0.9), d(0.999), d(1e-8), 0,
+                None) == 1
+    assert adam(None, None, None, None, 0, 0, 1, d(1e-3), d(0.9), d(0.999), d(1e-8), 0, None) == 0  # nothing to do
+    # masked Adam on a dense parameter: int16 indices for 40000 columns
+    assert lib.spops_masked_adam_csr(P(0x100000), P(0x200000), P(0x300000), P(0x400000), 0, FAKE, FAKE, 0, 4, 40000,
+                                     4, 1, d(1e-3), d(0.9), d(0.999), d(1e-8), 0, None) == 2

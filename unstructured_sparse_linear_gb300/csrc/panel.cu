@@ -34,11 +34,8 @@ namespace {
 constexpr int kKC = 64;       // K elements per pipeline chunk (128 bytes of 16-bit data)
 constexpr int kStages = 3;      // 3 x 32 KB ring: two CTAs per SM
 constexpr int kSpNT = 128;    // SpMM: columns of C per tile (UMMA N)
-constexpr int kMaxCluster = 8;
+constexpr int kMaxCluster = 8;  // SDDMM: CTAs (K splits) per tile, the portable cluster limit
 constexpr int kNarrowMax = 16;  // SpMM with at most this many columns skips the panel path
-// Registers per thread of the SDDMM panel kernel: two CTAs must share an SM (above about 160
-// registers the occupancy calculator and the hardware place only one).
-constexpr int kPanelMaxRegs = 152;  // SDDMM: CTAs (K splits) per tile, the portable cluster limit
 constexpr int kTileThreads = 128;
 
 constexpr uint32_t kSdStageA = kPM * kKC * 2;                 // 16 KB
