@@ -362,8 +362,8 @@ __global__ void __launch_bounds__(256) densify_kernel(const T* __restrict__ vals
     }
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kTileThreads, 2)
+template <typename T, int NT>
+__global__ void __launch_bounds__(NT, 2)
 spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restrict__ img_base, int32_t N, PlanView v,
                   uint32_t idesc, int* err) {
     extern __shared__ uint8_t smem_raw[];
@@ -399,7 +399,7 @@ spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restric
         const int nk = (nU + kKC - 1) / kKC;
         const T* img = img_base + v.img_slot[p];
         __syncthreads();
-        for (int x = tid; x < nk * kKC; x += kTileThreads) s_u[x] = x < nU ? v.ulist[(size_t)p * kUList + x] : -1;
+        for (int x = tid; x < nk * kKC; x += NT) s_u[x] = x < nU ? v.ulist[(size_t)p * kUList + x] : -1;
         bulk_wait_read<0>();  // the previous unit's staged C row has been read out of shared memory
         __syncthreads();
 
@@ -407,15 +407,15 @@ spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restric
             const uint32_t st = sbase + (gs % kStages) * kSpStageBytes;
             const char* src_a = reinterpret_cast<const char*>(img + (size_t)j * kPM * kKC);
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int c = tid + kTileThreads * q;
+            for (int q = 0; q < kSpStageA / 16 / NT; ++q) {
+                const int c = tid + NT * q;
                 tc::cp_async16(st + c * 16, src_a + c * 16, 16);
             }
             // B[U rows j*64 .. +64, n0 .. n0 + kSpNT): kSpNT / 8 sixteen-byte pieces per row
             constexpr int kPieces = kSpNT / 8;
 #pragma unroll
-            for (int q = 0; q < kKC * kPieces / kTileThreads; ++q) {
-                const int c = tid + kTileThreads * q;
+            for (int q = 0; q < kKC * kPieces / NT; ++q) {
+                const int c = tid + NT * q;
                 const int kk = c / kPieces, nch = c % kPieces;
                 const int u = s_u[j * kKC + kk];
                 const int ncol = n0 + nch * 8;
@@ -470,28 +470,33 @@ spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restric
         }
         tc::fence_after_sync();
 
-        // epilogue: thread tid converts TMEM lane tid (panel row tid) to the output dtype into
-        // a shared row (stride 272 bytes: the 16-byte stores of eight consecutive rows hit
-        // distinct banks), then sends the row to C[row, n0 .. n0 + 128) with one bulk async
-        // copy; the copies drain while the next unit's operands are gathered.
-        const int i = v.prow[p * kPM + tid];
-        const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-        const uint32_t crow = sbase + (uint32_t)tid * kSpCRowBytes;
+        // epilogue: with NT / 128 threads per row, thread tid converts its share of TMEM
+        // lane tid % 128 (panel row tid % 128; a warp reads the lane quarter it may access)
+        // to the output dtype into a shared row (stride 272 bytes: the 16-byte stores of
+        // eight consecutive rows hit distinct banks); then the row's first thread sends it to
+        // C[row, n0 .. n0 + 128) with one bulk async copy, drained while the next unit's
+        // operands are gathered.
+        constexpr int kCols = kSpNT * kPM / NT;  // TMEM columns per thread
+        const int r = tid & (kPM - 1), half = tid / kPM;
+        const int i = v.prow[p * kPM + r];
+        const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + half * kCols;
+        const uint32_t crow = sbase + (uint32_t)r * kSpCRowBytes;
 #pragma unroll
-        for (int c = 0; c < kSpNT / 32; ++c) {
+        for (int c = 0; c < kCols / 32; ++c) {
             float x[32];
             tc::tmem_ld32(lane_addr + c * 32, x);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const uint4 w = Elt<T>::pack(x + q * 8);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(crow + (c * 4 + q) * 16), "r"(w.x),
-                             "r"(w.y), "r"(w.z), "r"(w.w)
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(crow + half * kCols * 2 + (c * 4 + q) * 16),
+                             "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w)
                              : "memory");
             }
         }
+        fence_proxy_async_smem();
         tc::fence_before_sync();
-        if (i >= 0) {
-            fence_proxy_async_smem();
+        __syncthreads();
+        if (half == 0 && i >= 0) {
             bulk_s2g(C + (int64_t)i * N + n0, crow, (uint32_t)min(kSpNT, N - n0) * (uint32_t)sizeof(T));
             bulk_commit();
         }
@@ -562,13 +567,17 @@ cudaError_t run_spmm_panels(const void* vals, const int32_t* ro, const void* B, 
     if (e != cudaSuccess) return e;
     const int ntn = (N + kSpNT - 1) / kSpNT;
     const int grid = (int)min64((int64_t)device_props().sm_count * 2, (int64_t)v.P * ntn);
-    auto kern = spmm_panel_kernel<T>;
+    // Many units per CTA: 8 warps per CTA keep more gathers in flight; few units (each
+    // CTA about one): 4 warps, which share the SMs better with concurrent operators.
+    const bool wide = (int64_t)v.P * ntn >= (int64_t)device_props().sm_count * 6;
+    auto kern = wide ? spmm_panel_kernel<T, 256> : spmm_panel_kernel<T, 128>;
+    const int threads = wide ? 256 : 128;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSpSmem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     const uint32_t idesc = tc::instr_desc_f16(std::is_same<T, __nv_bfloat16>::value ? 1u : 0u, 0, 1, kPM, kSpNT);
-    e = launch_pdl(kern, grid, kTileThreads, kSpSmem, s, static_cast<const T*>(B), static_cast<T*>(C),
+    e = launch_pdl(kern, grid, threads, kSpSmem, s, static_cast<const T*>(B), static_cast<T*>(C),
                    static_cast<const T*>(img), N, v, idesc, device_error_word());
     count_launches(2);
     if (e != cudaSuccess) return e;
