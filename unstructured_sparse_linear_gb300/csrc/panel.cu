@@ -93,8 +93,8 @@ __device__ __forceinline__ void st_shared_f4(uint32_t addr, float4 v) {
 // distributed shared memory; after a second barrier, each rank adds its rows' slots in rank
 // order (so the result is deterministic) and writes the sampled entries. C = 1 is an
 // ordinary launch.
-template <typename T>
-__global__ void __launch_bounds__(kTileThreads, 2)
+template <typename T, int NT>
+__global__ void __launch_bounds__(NT, 2)
 sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restrict__ out, int32_t kd, PlanView v,
                    uint32_t idesc, int* err) {
     extern __shared__ uint8_t smem_raw[];
@@ -153,7 +153,7 @@ sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
         // One round of independent loads (all indexed by panel position, not by row): the
         // gather's row and column lists and the epilogue's per-row tile start, count and
         // column mask. Values of padding positions are loaded but never used.
-        {
+        if (tid < kPM) {
             const size_t prow_at = (size_t)p * kPM + tid;
             const int my_row = v.prow[prow_at];
             const int u = v.ulist[(size_t)p * kUList + u0 + tid];
@@ -172,8 +172,8 @@ sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
             const uint32_t st = sbase + (gs % kStages) * kSdStageBytes;
             const int k0 = (kc0 + j) * kKC;
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int c = tid + kTileThreads * q;
+            for (int q = 0; q < kPM * 8 / NT; ++q) {
+                const int c = tid + NT * q;
                 const int row = c >> 3, kch = c & 7;
                 const int kk = k0 + kch * 8;
                 const uint32_t off = tc::sw128_off(row, kch);
@@ -235,19 +235,23 @@ sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
         else __syncthreads();
         tc::fence_after_sync();
 
-        // Partial tile: thread tid owns TMEM lane tid = panel row tid and sends the row's 128
-        // fp32 sums to the CTA that finishes the row (rank row / rows_per), into the slot of
-        // this CTA's rank (row stride 132 floats: the 16-byte stores of eight consecutive rows
-        // hit distinct banks).
+        // Partial tile: with NT / 128 threads per row, thread tid owns its share of TMEM lane
+        // tid % 128 (panel row tid % 128; a warp reads the lane quarter it may access) and
+        // sends those fp32 sums to the CTA that finishes the row (rank row / rows_per), into
+        // the slot of this CTA's rank (row stride 132 floats: the 16-byte stores of eight
+        // consecutive rows hit distinct banks).
         // (tcgen05.ld is warp-collective: the whole warp loads, only rows with entries send.)
         if (nk > 0 && !failed) {
-            const int owner = tid / rows_per;
-            const bool send = s_cnt[tid] > 0;
-            const uint32_t dst = smem_u32(recv + ((size_t)crank * rows_per + (tid - owner * rows_per)) * kTS);
-            const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+            constexpr int kCols = kTileN * kPM / NT;  // TMEM columns per thread
+            const int row = tid & (kPM - 1), half = tid / kPM;
+            const int owner = row / rows_per;
+            const bool send = s_cnt[row] > 0;
+            const uint32_t dst =
+                smem_u32(recv + ((size_t)crank * rows_per + (row - owner * rows_per)) * kTS + half * kCols);
+            const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16) + half * kCols;
             const uint32_t rdst = C == 1 ? dst : cluster_map(dst, owner);
 #pragma unroll
-            for (int c = 0; c < kTileN / 32; ++c) {
+            for (int c = 0; c < kCols / 32; ++c) {
                 float x[32];
                 tc::tmem_ld32(lane_addr + c * 32, x);
                 if (send) {
@@ -263,7 +267,7 @@ sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
         // For each group of 4 columns of row tid: the group's bits of the row's column mask
         // and the rank of its first entry among the row's entries of the tile (entries and U
         // are both in column order).
-        if (tid >= r0 && tid < r1) {
+        if (tid < kPM && tid >= r0 && tid < r1) {
             const uint4 m = s_mask[tid];
             const uint32_t w[4] = {m.x, m.y, m.z, m.w};
             uint32_t run = 0;
@@ -284,7 +288,7 @@ sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
         // order and writes the sampled values to ts[t] + rank.
         if (!failed) {
 #pragma unroll 2
-            for (int r = r0 + warp; r < r1; r += kTileThreads / 32) {
+            for (int r = r0 + warp; r < r1; r += NT / 32) {
                 if (s_cnt[r] == 0) continue;  // uniform across the warp
                 const float4* slot = reinterpret_cast<const float4*>(recv + (size_t)(r - r0) * kTS) + lane;
                 const size_t slot_step = (size_t)rows_per * kTS / 4;
@@ -512,7 +516,10 @@ spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restric
 
 template <typename T>
 cudaError_t run_sddmm_panels(const void* A, const void* BT, void* out, int32_t kd, const PlanView& v, cudaStream_t s) {
-    auto kern = sddmm_panel_kernel<T>;
+    // Many possible tiles (more than one per CTA): 8 warps per CTA keep more gathers in
+    // flight; otherwise 4 warps, which share the SMs better with concurrent operators.
+    const bool wide = (int64_t)v.P * kTiles >= (int64_t)device_props().sm_count * 2;
+    auto kern = wide ? sddmm_panel_kernel<T, 256> : sddmm_panel_kernel<T, 128>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSdSmem);
     if (e != cudaSuccess) return e;
     // Largest shared-memory carveout, so that two CTAs fit on an SM (also when placing clusters).
@@ -529,7 +536,7 @@ cudaError_t run_sddmm_panels(const void* A, const void* BT, void* out, int32_t k
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cfg.blockDim = dim3(kTileThreads);
+    cfg.blockDim = dim3(wide ? 256 : 128);
     cfg.dynamicSmemBytes = kSdSmem;
     cfg.stream = s;
     int64_t nclusters = min64((int64_t)device_props().sm_count * 2, max_items);
