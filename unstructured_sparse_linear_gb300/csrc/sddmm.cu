@@ -89,7 +89,7 @@ __device__ __forceinline__ void sddmm_batch(int row, int32_t kb, int cnt, const 
 }
 
 template <typename T, typename I, int V>
-__global__ void __launch_bounds__(kSddmmThreads)
+__global__ void __launch_bounds__(kSddmmThreads, 3)
 sddmm_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx, const I* __restrict__ col,
                   const T* __restrict__ A, const T* __restrict__ BT, T* __restrict__ out, int32_t kd, int G,
                   const int32_t* __restrict__ bins, const uint8_t* __restrict__ skip) {

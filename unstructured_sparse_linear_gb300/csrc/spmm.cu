@@ -83,7 +83,7 @@ __device__ __forceinline__ void store_c(T* __restrict__ Crow, int col0, int N, c
 }
 
 template <typename T, typename I, int V>
-__global__ void __launch_bounds__(kSpmmThreads, 2)
+__global__ void __launch_bounds__(kSpmmThreads, 3)
 spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, const I* __restrict__ row_idx,
                  const I* __restrict__ col, const T* __restrict__ B, T* __restrict__ C, int32_t m, int32_t N, int G,
                  const int32_t* __restrict__ bins, const uint8_t* __restrict__ skip) {
