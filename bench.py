@@ -444,6 +444,13 @@ def time_next_ops(sp, w, d, idx, stream, pool, flush, reps):
             acc["layer_fwd_bwd_sparse"] = (3 * 2 * nnz * T, 0)
             ops.append(("layer_fwd_bwd_dense_cublas", layer_dense))
             acc["layer_fwd_bwd_dense_cublas"] = (3 * 2 * m * n * T, 0)
+        if w.B is not None and w.B.shape[1] <= 16:
+            # the SpMV end of the narrow-N range: one right-hand side
+            ri1 = sp.sort_rows(ro, nnz=nnz, index_dtype=idx)
+            pl1 = sp.plan_build(ro, ri1, col, n)
+            b1 = d["B"][:, :1].contiguous()
+            ops.append(("spmv_n1", lambda: sp.spmm(val, ro, ri1, col, b1, m, plan=pl1)))
+            acc["spmv_n1"] = (2 * nnz, nnz * (ib + b) + 4 * (m + 1) + ib * m + n * b + m * b)
         P = torch.randn(nnz, device=val.device)
         M1 = torch.zeros(nnz, device=val.device)
         V1 = torch.zeros(nnz, device=val.device)

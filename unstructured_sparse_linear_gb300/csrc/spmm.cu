@@ -201,8 +201,9 @@ spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, con
 // gathering its entries' B rows (N elements, at most 64 bytes) and accumulating N fp32
 // sums; a butterfly of shuffles then adds the 32 lanes' sums in a fixed order and lanes
 // 0 .. N-1 write the row's outputs. NV 16-byte vectors per B row when N * sizeof(T) is a
-// multiple of 16 and B is aligned; NV = 0 loads N scalars. Rows go round-robin over the
-// warps in row_idx order (long rows first); empty rows write zeros.
+// multiple of 16 and B is aligned; NV = 0 loads N scalars; NV = -1 is N = 1 (eight entries
+// in flight per lane). Rows go round-robin over the warps in row_idx order (long rows
+// first); empty rows write zeros.
 template <typename T, typename I, int NV>
 __global__ void __launch_bounds__(kSpmmThreads)
 spmm_narrow_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, const I* __restrict__ row_idx,
@@ -224,7 +225,7 @@ spmm_narrow_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, c
         for (int c = 0; c < kMaxN; ++c) acc[c] = 0.f;
         // kU entries per lane per round: their (col, val) loads, then their B rows, are all
         // in flight before the first FMA.
-        constexpr int kU = NV > 2 ? 2 : 4;
+        constexpr int kU = NV > 2 ? 2 : (NV < 0 ? 8 : 4);
         for (int32_t kb = k0; kb < k1; kb += 32 * kU) {
             int jq[kU];
             float aq[kU];
@@ -236,7 +237,13 @@ spmm_narrow_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, c
                 jq[u] = ok[u] ? idx_of(col[k]) : 0;
                 aq[u] = ok[u] ? Elt<T>::to_f(vals[k]) : 0.f;
             }
-            if constexpr (NV > 0) {
+            if constexpr (NV < 0) {  // N == 1: gather kU values, then multiply
+                float bv[kU];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) bv[u] = ok[u] ? Elt<T>::to_f(B[jq[u]]) : 0.f;
+#pragma unroll
+                for (int u = 0; u < kU; ++u) acc[0] = fmaf(aq[u], bv[u], acc[0]);
+            } else if constexpr (NV > 0) {
                 uint4 raw[kU][NV];
 #pragma unroll
                 for (int u = 0; u < kU; ++u)
@@ -263,7 +270,7 @@ spmm_narrow_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, c
                 }
             }
         }
-        constexpr int kUsed = NV > 0 ? NV * VE : kMaxN;
+        constexpr int kUsed = NV > 0 ? NV * VE : (NV < 0 ? 1 : kMaxN);
 #pragma unroll
         for (int c = 0; c < kUsed; ++c) {
             if (NV == 0 && c >= N) break;
@@ -291,7 +298,8 @@ cudaError_t run_narrow(const void* vals, const int32_t* ro, const void* row_idx,
     const T* b = static_cast<const T*>(B);
     T* c = static_cast<T*>(C);
     cudaError_t e;
-    if (vec && N / VE == 1) e = launch_pdl(spmm_narrow_kernel<T, I, 1>, grid, kSpmmThreads, 0, s, v, ro, ri, ci, b, c, m, N, skip);
+    if (N == 1) e = launch_pdl(spmm_narrow_kernel<T, I, -1>, grid, kSpmmThreads, 0, s, v, ro, ri, ci, b, c, m, N, skip);
+    else if (vec && N / VE == 1) e = launch_pdl(spmm_narrow_kernel<T, I, 1>, grid, kSpmmThreads, 0, s, v, ro, ri, ci, b, c, m, N, skip);
     else if (vec && N / VE == 2) e = launch_pdl(spmm_narrow_kernel<T, I, 2>, grid, kSpmmThreads, 0, s, v, ro, ri, ci, b, c, m, N, skip);
     else if (vec && N / VE == 4) e = launch_pdl(spmm_narrow_kernel<T, I, 4>, grid, kSpmmThreads, 0, s, v, ro, ri, ci, b, c, m, N, skip);
     else e = launch_pdl(spmm_narrow_kernel<T, I, 0>, grid, kSpmmThreads, 0, s, v, ro, ri, ci, b, c, m, N, skip);
