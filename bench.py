@@ -221,28 +221,37 @@ def make_ops(sp, w, d, idx, args, outs):
 
 
 def run_step_forked(ops, stream, side):
-    """sort_rows and plan on `stream`, then spmm / sddmm / csr_add on `stream` and the side
-    streams, joined back into `stream`."""
-    first = [f for name, f in ops if name in ("sort_rows", "plan")]
-    rest = [f for name, f in ops if name not in ("sort_rows", "plan")]
-    for f in first:
-        f()
-    fork = torch.cuda.Event()
-    fork.record(stream)
+    """The step on `stream` and the side streams, by data dependence: sort_rows first; csr_add
+    (which needs only row_idx) forks right after it, beside the plan; after the plan, sddmm
+    forks and spmm runs on `stream`; everything joins back into `stream`."""
+    by = dict(ops)
+    spare = list(side)
     joins = []
-    for f, s in zip(rest[1:], side):
-        s.wait_event(fork)
+
+    def fork(f):
+        s = spare.pop(0)
+        e = torch.cuda.Event()
+        e.record(stream)
+        s.wait_event(e)
         with torch.cuda.stream(s):
             f()
-            e = torch.cuda.Event()
-            e.record(s)
-        joins.append(e)
-    for f in rest[:1]:
-        f()
-    for e in joins:
-        stream.wait_event(e)
-    for f in rest[1 + len(side):]:
-        f()
+            j = torch.cuda.Event()
+            j.record(s)
+        joins.append(j)
+
+    by["sort_rows"]()
+    if "csr_add" in by:
+        fork(by["csr_add"])
+    by["plan"]()
+    if "sddmm" in by and "spmm" in by:
+        fork(by["sddmm"])
+        by["spmm"]()
+    elif "sddmm" in by:
+        by["sddmm"]()
+    elif "spmm" in by:
+        by["spmm"]()
+    for j in joins:
+        stream.wait_event(j)
 
 
 def host_inputs(w, idx):
@@ -279,12 +288,10 @@ def run_gpu(args):
     lib = sp._lib.load()
     with torch.cuda.stream(stream):
         for _ in range(max(args.warmup, 1)):
-            for _, f in ops:
-                f()
-        torch.cuda.synchronize(dev)
+            run_step_forked(ops, stream, side)  # eager, on the streams the graph uses
+            torch.cuda.synchronize(dev)
         pool = torch.cuda.graph_pool_handle()
-        # the step: sort_rows and plan, then the operators, which depend only on row_idx and
-        # the plan, on three streams (fork / join inside one graph)
+        # the step on three streams by data dependence (fork / join inside one graph)
         step_graph = torch.cuda.CUDAGraph()
         launches0 = lib.spops_kernel_launches()
         with torch.cuda.graph(step_graph, stream=stream, pool=pool):

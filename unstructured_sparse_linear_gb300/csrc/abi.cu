@@ -63,41 +63,69 @@ int* device_error_word() {
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
 namespace {
+// One side stream per (device, caller stream), so operators queued on different streams do
+// not serialize on a shared side stream.
 struct Side {
+    int device = -1;
+    cudaStream_t caller = nullptr;
     cudaStream_t stream = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
-    bool tried = false;
 };
-thread_local Side g_side[kMaxDevices];
+constexpr int kMaxSides = 8;
+thread_local Side g_side[kMaxSides];
+
+Side* find_side(int d, cudaStream_t s) {
+    for (Side& sd : g_side)
+        if (sd.stream && sd.device == d && sd.caller == s) return &sd;
+    return nullptr;
+}
 }  // namespace
 
 cudaStream_t side_fork(cudaStream_t s) {
     const int d = current_device();
-    if (d < 0 || d >= kMaxDevices) return nullptr;
-    Side& sd = g_side[d];
-    if (!sd.tried) {
-        sd.tried = true;
-        if (cudaStreamCreateWithFlags(&sd.stream, cudaStreamNonBlocking) != cudaSuccess ||
-            cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming) != cudaSuccess) {
+    if (d < 0) return nullptr;
+    Side* sd = find_side(d, s);
+    if (!sd) {
+        // Streams are not created while s is being captured into a graph (no fork then).
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(s, &cap) != cudaSuccess || cap != cudaStreamCaptureStatusNone) {
             cudaGetLastError();
-            sd.stream = nullptr;
+            return nullptr;
         }
+        for (Side& x : g_side)
+            if (!x.stream) {
+                sd = &x;
+                break;
+            }
+        if (!sd) return nullptr;
+        if (cudaStreamCreateWithFlags(&sd->stream, cudaStreamNonBlocking) != cudaSuccess) {
+            cudaGetLastError();
+            sd->stream = nullptr;
+            return nullptr;
+        }
+        if (cudaEventCreateWithFlags(&sd->fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&sd->join, cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            cudaStreamDestroy(sd->stream);
+            sd->stream = nullptr;
+            return nullptr;
+        }
+        sd->device = d;
+        sd->caller = s;
     }
-    if (!sd.stream) return nullptr;
-    if (cudaEventRecord(sd.fork, s) != cudaSuccess || cudaStreamWaitEvent(sd.stream, sd.fork, 0) != cudaSuccess) {
+    if (cudaEventRecord(sd->fork, s) != cudaSuccess || cudaStreamWaitEvent(sd->stream, sd->fork, 0) != cudaSuccess) {
         cudaGetLastError();
         return nullptr;
     }
-    return sd.stream;
+    return sd->stream;
 }
 
 cudaError_t side_join(cudaStream_t s) {
-    const int d = current_device();
-    Side& sd = g_side[d];
-    cudaError_t e = cudaEventRecord(sd.join, sd.stream);
+    Side* sd = find_side(current_device(), s);
+    if (!sd) return cudaErrorInvalidResourceHandle;
+    cudaError_t e = cudaEventRecord(sd->join, sd->stream);
     if (e != cudaSuccess) return e;
-    return cudaStreamWaitEvent(s, sd.join, 0);
+    return cudaStreamWaitEvent(s, sd->join, 0);
 }
 
 int set_last_error(int status, const char* fmt, ...) {

@@ -55,37 +55,6 @@ bool dtype_ok(int dt) { return dt == kF16 || dt == kBF16; }
 
 // ------------------------------------------------------------------ SDDMM dense panels
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t cluster_size() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-// Every thread of every CTA of the cluster arrives; shared-memory writes before it are
-// visible to the cluster's reads after it.
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Address in CTA `rank`'s shared memory of the local shared address `addr`.
-__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, int rank) {
-    uint32_t ra;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(addr), "r"(rank));
-    return ra;
-}
-__device__ __forceinline__ void st_cluster_f4(uint32_t addr, float4 v) {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
-                 "f"(v.w)
-                 : "memory");
-}
-__device__ __forceinline__ void st_shared_f4(uint32_t addr, float4 v) {
-    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
-                 : "memory");
-}
-
 // A cluster of C CTAs computes one tile (panel p, 128 columns t of U): CTA rank r multiplies
 // K chunks [r * per, (r + 1) * per) into its tensor memory. Rows are split among the ranks
 // (rank o finishes rows [o * 128 / C, ...)); after a cluster barrier (every ring is idle),
@@ -346,12 +315,26 @@ __global__ void __launch_bounds__(256) densify_kernel(const T* __restrict__ vals
         if ((x % row_vec) * 16 < upad * (int)sizeof(T)) st4[x] = make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
-    for (int rr = 0; rr < kGroupRows / 8; ++rr) {
-        const int lr = warp * (kGroupRows / 8) + rr;
+    static_assert(kGroupRows == 8, "one row per warp");
+    {
+        const int lr = warp;
         const int i = v.prow[p * kPM + grp * kGroupRows + lr];
-        if (i < 0) continue;
-        const int32_t k1 = ro[i + 1];
-        for (int32_t k = ro[i] + lane; k < k1; k += 32) stage[lr][v.upos[k]] = vals[k];
+        const int32_t k0 = i >= 0 ? ro[i] : 0, k1 = i >= 0 ? ro[i + 1] : 0;
+        // 8 (position, value) pairs per lane loaded before any is stored
+        constexpr int kB = 8;
+        for (int32_t kb = k0; kb < k1; kb += 32 * kB) {
+            int u[kB];
+            T x[kB];
+#pragma unroll
+            for (int j = 0; j < kB; ++j) {
+                const int32_t k = kb + j * 32 + lane;
+                u[j] = k < k1 ? (int)v.upos[k] : -1;
+                x[j] = k < k1 ? vals[k] : T();
+            }
+#pragma unroll
+            for (int j = 0; j < kB; ++j)
+                if (u[j] >= 0) stage[lr][u[j]] = x[j];
+        }
     }
     __syncthreads();
     T* img = img_base + v.img_slot[p];

@@ -10,20 +10,19 @@
 //     columns; a panel is dense when |U| <= 1024, it has at least 16 non-empty rows and its
 //     entries fill at least a quarter of (non-empty rows) x |U|. Dense panels run on the
 //     tensor cores as 128 x |U| tiles.
-// Two kernels (after zeroing P + 1 completion counters), none with a serial per-thread loop
-// over a panel:
-//   1. row groups (8 rows per CTA): row ids per position, per-group counts, and a column
-//      bitmap per 8-row group built with shared-memory atomics; then
-//   2. the last group of a panel to finish: OR the group bitmaps, prefix-sum their
-//      popcounts, list U, decide density (for SDDMM tiles |U| <= 1024, for a SpMM image
-//      |U| <= 2048); then
-//   3. the last panel to finish: sum the group counts into row bins, list dense panels and
-//      SDDMM tiles, and assign SpMM image slots within the image budget (in panel order);
-//   4. second kernel, row groups of dense panels: each entry's position in U and, per row,
+// Two kernels, no counters to reset between builds:
+//   1. a thread-block cluster of 8 CTAs per panel, 16 positions per CTA: row ids per
+//      position, counts, and a column bitmap per CTA built with shared-memory atomics; after
+//      a cluster barrier, rank 0 ORs the 8 bitmaps through distributed shared memory,
+//      prefix-sums their popcounts, lists U and decides density (SDDMM tiles |U| <= 1024,
+//      SpMM image |U| <= 2048);
+//   2. row groups of dense panels (8 rows per CTA): each entry's position in U and, per row,
 //      the first entry of every 128-column tile of U and a bit mask of the U positions it
-//      holds.
-// Every count is an integer sum in a fixed order, so the plan is bit-identical on every
-// build.
+//      holds; one extra CTA sums the panel counts into row bins, lists dense panels and
+//      SDDMM tiles, and assigns SpMM image slots within the image budget (in panel order).
+// Index loads are batched (8 per lane) before their results are used, so a long row costs a
+// few dependent load latencies, not one per 32 entries. Every count is an integer sum in a
+// fixed order, so the plan is bit-identical on every build.
 #include "common.cuh"
 #include "plan.h"
 
@@ -62,43 +61,60 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* sh, int* total) 
     return before;
 }
 
-__device__ void panel_work(const PlanView& v, int p, uint32_t* sm);
-__device__ void lists_work(const PlanView& v, int64_t img_budget);
+constexpr int kRowsPerWarp = kCtaRows / (kPlanThreads / 32);  // positions per warp in the row step
+constexpr int kLoadBatch = 8;                                  // index loads per lane in flight
 
-// ---- 1. row groups
+__device__ void panel_work(const PlanView& v, int p, uint32_t* sm, int nnz_p, int ne);
+
+// ---- 1. row step: cluster of kPlanCluster CTAs per panel
 template <typename I>
 __global__ void __launch_bounds__(kPlanThreads)
 plan_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx, const I* __restrict__ col,
-                 PlanView v, int64_t img_budget) {
-    extern __shared__ uint32_t bitmap[];  // 2 W words when panels are enabled (the panel step reuses them)
-    __shared__ int red[4][8];
+                 PlanView v) {
+    extern __shared__ uint32_t bitmap[];  // W words (2 W in rank 0, whose panel step reuses them)
+    __shared__ int red[4][kPlanThreads / 32];
+    __shared__ int s_cnt[4], s_tot[4];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int p = blockIdx.x / kPlanCluster;
+    const int rank = (int)cluster_rank();
     pdl_trigger();
-    pdl_wait();
-    const int64_t p0 = (int64_t)blockIdx.x * kGroupRows;
     if (v.panels)
         for (int w = tid; w < v.W; w += kPlanThreads) bitmap[w] = 0;
-    __syncthreads();
-    int c_spmm = 0, c_sddmm = 0, c_ne = 0, c_ent = 0;
-    for (int rr = 0; rr < kGroupRows / 8; ++rr) {
-        const int64_t pos = p0 + warp * (kGroupRows / 8) + rr;
-        int row = -1;
-        if (pos < v.m) row = idx_of(row_idx[pos]);
-        if (lane == 0 && v.panels) v.prow[pos] = row;  // pos < P * 128 always
-        if (row < 0) continue;
-        const int32_t k0 = ro[row], k1 = ro[row + 1];
-        const int32_t c = k1 - k0;
-        if (lane == 0) {
-            c_spmm += c >= kSpmmLongRow;
-            c_sddmm += c >= kSddmmLongRow;
-            c_ne += c >= 1;
-            c_ent += c;
-        }
-        if (v.panels) {
-            for (int32_t k = k0 + lane; k < k1; k += 32) {
-                const int cc = idx_of(col[k]);
-                atomicOr(&bitmap[cc >> 5], 1u << (cc & 31));
+    pdl_wait();
+    // the warp's positions: their rows, then the rows' offsets, each batch loaded together
+    const int64_t pos0 = (int64_t)p * kPM + rank * kCtaRows + warp * kRowsPerWarp;
+    int row[kRowsPerWarp];
+    int32_t k0[kRowsPerWarp], len[kRowsPerWarp];
+#pragma unroll
+    for (int q = 0; q < kRowsPerWarp; ++q) row[q] = pos0 + q < v.m ? idx_of(row_idx[pos0 + q]) : -1;
+#pragma unroll
+    for (int q = 0; q < kRowsPerWarp; ++q) {
+        k0[q] = row[q] >= 0 ? ro[row[q]] : 0;
+        len[q] = row[q] >= 0 ? ro[row[q] + 1] - k0[q] : 0;
+    }
+    int c_spmm = 0, c_sddmm = 0, c_ne = 0, c_ent = 0, total = 0;
+#pragma unroll
+    for (int q = 0; q < kRowsPerWarp; ++q) {
+        if (v.panels && lane == q) v.prow[pos0 + q] = row[q];  // pos0 + q < P * 128 always
+        c_spmm += len[q] >= kSpmmLongRow;
+        c_sddmm += len[q] >= kSddmmLongRow;
+        c_ne += len[q] >= 1;
+        c_ent += len[q];
+        total += len[q];
+    }
+    if (v.panels) {
+        static_assert(kRowsPerWarp == 2, "entry t of the warp's rows is in row 0 below len[0], else row 1");
+        for (int t0 = 0; t0 < total; t0 += 32 * kLoadBatch) {
+            int cc[kLoadBatch];
+#pragma unroll
+            for (int j = 0; j < kLoadBatch; ++j) {
+                const int t = t0 + j * 32 + lane;
+                const int32_t k = t < len[0] ? k0[0] + t : k0[1] + (t - len[0]);
+                cc[j] = t < total ? idx_of(col[k]) : -1;
             }
+#pragma unroll
+            for (int j = 0; j < kLoadBatch; ++j)
+                if (cc[j] >= 0) atomicOr(&bitmap[cc[j] >> 5], 1u << (cc[j] & 31));
         }
     }
     if (lane == 0) {
@@ -109,57 +125,39 @@ plan_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx, 
     }
     __syncthreads();
     if (tid < 4) {
-        int s = 0;
-        for (int w = 0; w < 8; ++w) s += red[tid][w];
-        v.cta_part[blockIdx.x * 4 + tid] = s;
+        int x = 0;
+#pragma unroll
+        for (int w = 0; w < kPlanThreads / 32; ++w) x += red[tid][w];
+        s_cnt[tid] = x;
     }
-    if (v.panels) {
-        uint32_t* dst = v.bm_part + (size_t)blockIdx.x * v.W;  // group g of panel p is CTA p*kGroups+g
-        for (int w = tid; w < v.W; w += kPlanThreads) dst[w] = bitmap[w];
+    cluster_sync();  // every CTA's bitmap and counts are final and visible to rank 0
+    if (rank == 0) {
+        if (v.panels)
+            for (int w = tid; w < v.W; w += kPlanThreads) {
+                const uint32_t a = smem_u32(&bitmap[w]);
+                uint32_t x = bitmap[w];
+#pragma unroll
+                for (int r = 1; r < kPlanCluster; ++r) x |= ld_cluster_u32(cluster_map(a, r));
+                bitmap[w] = x;
+            }
+        if (tid < 4) {
+            int x = 0;
+            for (int r = 0; r < kPlanCluster; ++r) x += (int)ld_cluster_u32(cluster_map(smem_u32(&s_cnt[tid]), r));
+            v.pan_part[p * 4 + tid] = x;
+            s_tot[tid] = x;
+        }
     }
-    // The last row group of a panel to finish builds the panel; the last panel to finish
-    // builds the bins and work lists. Each CTA publishes its writes (fence) before it counts
-    // itself in; the one that completes a count fences again before reading the others'.
-    __shared__ int s_last;
-    const int p = blockIdx.x / kGroups;
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_last = atomicAdd(&v.done[p], 1) == kGroups - 1;
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    if (v.panels) panel_work(v, p, bitmap);
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_last = atomicAdd(&v.done[v.P], 1) == v.P - 1;
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    lists_work(v, img_budget);
+    cluster_sync();  // the other CTAs keep their shared memory until rank 0 has read it
+    if (rank != 0 || !v.panels) return;
+    panel_work(v, p, bitmap, s_tot[3], s_tot[2]);
 }
 
-// ---- 2. panel p (run by the last of its row-group CTAs to finish)
-__device__ void panel_work(const PlanView& v, int p, uint32_t* sm) {
+// ---- panel p (rank 0 of its cluster; sm holds the panel's OR-ed bitmap, W more words free)
+__device__ void panel_work(const PlanView& v, int p, uint32_t* sm, int nnz_p, int ne) {
     uint32_t* bm = sm;  // bm[W], wbase[W]
     int* wb = reinterpret_cast<int*>(sm + v.W);
     __shared__ int sh[32];
-    __shared__ int s_cnt[2];
     const int tid = threadIdx.x;
-    for (int w = tid; w < v.W; w += kPlanThreads) {
-        uint32_t x = 0;
-#pragma unroll
-        for (int g = 0; g < kGroups; ++g) x |= v.bm_part[((size_t)p * kGroups + g) * v.W + w];
-        bm[w] = x;
-    }
-    if (tid < 2) {
-        int s = 0;
-        for (int g = 0; g < kGroups; ++g) {
-            const int cta = p * kGroups + g;
-            if (cta < v.ncta) s += v.cta_part[cta * 4 + (tid == 0 ? 3 : 2)];
-        }
-        s_cnt[tid] = s;  // [0] entries, [1] non-empty rows
-    }
-    __syncthreads();
     const int per = (v.W + kPlanThreads - 1) / kPlanThreads;
     const int b = tid * per, e = min(v.W, b + per);
     int s = 0;
@@ -171,7 +169,6 @@ __device__ void panel_work(const PlanView& v, int p, uint32_t* sm) {
         run += __popc(bm[w]);
     }
     __syncthreads();
-    const int nnz_p = s_cnt[0], ne = s_cnt[1];
     const bool filled = nnz_p > 0 && ne >= kMinDenseRows && (int64_t)nnz_p * 4 >= (int64_t)ne * U;
     const bool dense = filled && U <= kUCap;     // SDDMM tiles
     const bool dense_sp = filled && U <= kUList; // SpMM image
@@ -193,15 +190,15 @@ __device__ void panel_work(const PlanView& v, int p, uint32_t* sm) {
     }
 }
 
-// ---- 3. bins and work lists (run by the last panel to finish)
+// ---- bins and work lists (one CTA, after the row step)
 __device__ void lists_work(const PlanView& v, int64_t img_budget) {
     __shared__ int sh[32];
-    // row bins: fixed-order sums over the group CTAs
+    // row bins: fixed-order sums over the panels
     int a = 0, b = 0, c = 0;
-    for (int i = threadIdx.x; i < v.ncta; i += blockDim.x) {
-        a += v.cta_part[i * 4 + 0];
-        b += v.cta_part[i * 4 + 1];
-        c += v.cta_part[i * 4 + 2];
+    for (int i = threadIdx.x; i < v.P; i += blockDim.x) {
+        a += v.pan_part[i * 4 + 0];
+        b += v.pan_part[i * 4 + 1];
+        c += v.pan_part[i * 4 + 2];
     }
     int ta, tb, tc;
     block_exclusive_scan(a, sh, &ta);
@@ -262,65 +259,78 @@ __device__ void lists_work(const PlanView& v, int64_t img_budget) {
     }
 }
 
-// ---- 4. entry positions in U, tile starts and per-row column masks (dense panels only)
+// ---- 2. entry positions in U, tile starts and per-row column masks (dense panels), and
+// the lists (the grid's last CTA)
 template <typename I>
 __global__ void __launch_bounds__(kPlanThreads)
-plan_upos_kernel(const int32_t* __restrict__ ro, const I* __restrict__ col, PlanView v) {
+plan_upos_kernel(const int32_t* __restrict__ ro, const I* __restrict__ col, PlanView v, int64_t img_budget) {
     extern __shared__ uint32_t sm[];
     constexpr int kMaskWords = kUCap / 32;
     static_assert(kMaskWords == 32, "one mask word per lane");
-    __shared__ uint32_t rmask[8][kMaskWords];  // one row per warp
+    static_assert(kGroupRows == kPlanThreads / 32, "one row per warp");
+    __shared__ uint32_t rmask[kGroupRows][kMaskWords];
     pdl_trigger();
     pdl_wait();
+    if (blockIdx.x == gridDim.x - 1) {
+        lists_work(v, img_budget);
+        return;
+    }
     const int p = blockIdx.x / kGroups;
     if (!(v.desc[p].x & 2)) return;  // U positions for SpMM-dense panels
     const bool tiles = v.dense[p];    // tile starts and masks for SDDMM-dense ones (U <= kUCap)
     uint32_t* bm = sm;
     int* wb = reinterpret_cast<int*>(sm + v.W);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t pos = (int64_t)blockIdx.x * kGroupRows + warp;
+    const int row = v.prow[pos];
+    const int32_t k0 = row >= 0 ? ro[row] : 0, k1 = row >= 0 ? ro[row + 1] : 0;
     for (int w = tid; w < v.W; w += kPlanThreads) {
         bm[w] = v.bm[(size_t)p * v.W + w];
         wb[w] = v.wbase[(size_t)p * v.W + w];
     }
+    rmask[warp][lane] = 0;
     __syncthreads();
     auto upos_of = [&](int c) { return wb[c >> 5] + __popc(bm[c >> 5] & ((1u << (c & 31)) - 1u)); };
-    const int64_t p0 = (int64_t)blockIdx.x * kGroupRows;
-    for (int rr = 0; rr < kGroupRows / 8; ++rr) {
-        const int64_t pos = p0 + warp * (kGroupRows / 8) + rr;
-        const int row = v.prow[pos];
-        int32_t* ts = v.ts + pos * (kTiles + 1);
-        uint32_t* tm = v.tmask + pos * kMaskWords;
-        rmask[warp][lane] = 0;  // kMaskWords == 32: one word per lane
-        __syncwarp();
-        if (row < 0) {
-            if (tiles) {
-                if (lane <= kTiles) ts[lane] = 0;
-                tm[lane] = 0;
-            }
-            continue;
+    int32_t* ts = v.ts + pos * (kTiles + 1);
+    uint32_t* tm = v.tmask + pos * kMaskWords;
+    if (k0 == k1) {  // empty row or a position past m
+        if (tiles) {
+            if (lane <= kTiles) ts[lane] = k0;
+            tm[lane] = 0;
         }
-        const int32_t k0 = ro[row], k1 = ro[row + 1];
-        if (k0 == k1) {
-            if (tiles) {
-                if (lane <= kTiles) ts[lane] = k0;
-                tm[lane] = 0;
-            }
-            continue;
+        return;
+    }
+    int carry = -1;  // U position of the entry before this batch (-1: none)
+    for (int32_t kb = k0; kb < k1; kb += 32 * kLoadBatch) {
+        int u[kLoadBatch];
+#pragma unroll
+        for (int j = 0; j < kLoadBatch; ++j) {
+            const int32_t k = kb + j * 32 + lane;
+            u[j] = k < k1 ? idx_of(col[k]) : 0;
         }
-        for (int32_t k = k0 + lane; k < k1; k += 32) {
-            const int u = upos_of(idx_of(col[k]));
-            v.upos[k] = (uint16_t)u;
+#pragma unroll
+        for (int j = 0; j < kLoadBatch; ++j) u[j] = upos_of(u[j]);
+#pragma unroll
+        for (int j = 0; j < kLoadBatch; ++j) {
+            const int32_t k = kb + j * 32 + lane;
+            // U position of entry k - 1: the lane below, lane 31 of the slice before, or the carry
+            const int up = __shfl_up_sync(0xffffffffu, u[j], 1);
+            const int last_prev = __shfl_sync(0xffffffffu, j > 0 ? u[j > 0 ? j - 1 : 0] : carry, 31);
+            const int u_prev = lane > 0 ? up : (j > 0 ? last_prev : carry);
+            if (k >= k1) continue;
+            v.upos[k] = (uint16_t)u[j];
             if (!tiles) continue;
-            atomicOr(&rmask[warp][u >> 5], 1u << (u & 31));
-            const int t_cur = u / kTileN;
-            const int t_prev = k > k0 ? upos_of(idx_of(col[k - 1])) / kTileN : -1;
+            atomicOr(&rmask[warp][u[j] >> 5], 1u << (u[j] & 31));
+            const int t_cur = u[j] / kTileN;
+            const int t_prev = k > k0 ? u_prev / kTileN : -1;
             for (int t = t_prev + 1; t <= t_cur; ++t) ts[t] = k;  // tiles starting at entry k
             if (k == k1 - 1)
                 for (int t = t_cur + 1; t <= kTiles; ++t) ts[t] = k1;
         }
-        __syncwarp();
-        if (tiles) tm[lane] = rmask[warp][lane];
+        carry = __shfl_sync(0xffffffffu, u[kLoadBatch - 1], 31);
     }
+    __syncwarp();
+    if (tiles) tm[lane] = rmask[warp][lane];
 }
 
 __global__ void plan_stats_kernel(PlanView v, int32_t* out) {
@@ -340,16 +350,11 @@ PlanLayout plan_layout(int32_t m, int32_t n, int32_t nnz) {
         off = align_up(off + bytes, 1024);
         return a;
     };
-    // one row-group CTA per 16 positions of every panel, including the positions past m in
-    // the last panel (they record row -1), so every panel position gets a row id
-    const size_t nc = (size_t)((m + kPM - 1) / kPM) * kGroups;
+    const size_t P = (size_t)(m + kPM - 1) / kPM;
     L.hdr = take(32 * 4);
-    L.cta_part = take(nc * 16);
-    L.done = take((size_t)((m + kPM - 1) / kPM + 1) * 4);
+    L.pan_part = take(P * 16);
     if (plan_panels_enabled(m, n)) {
-        const size_t P = (size_t)(m + kPM - 1) / kPM;
         const size_t W = (size_t)(n + 31) / 32;
-        L.bm_part = take(P * kGroups * W * 4);
         L.bm = take(P * W * 4);
         L.wbase = take(P * W * 4);
         L.desc = take(P * 16);
@@ -378,12 +383,9 @@ PlanView plan_view(void* base, int32_t m, int32_t n, int32_t nnz) {
     v.panels = plan_panels_enabled(m, n);
     v.P = (m + kPM - 1) / kPM;
     v.W = v.panels ? (n + 31) / 32 : 0;
-    v.ncta = v.P * kGroups;
     v.hdr = at<int32_t>(b, L.hdr);
-    v.cta_part = at<int32_t>(b, L.cta_part);
-    v.done = at<int32_t>(b, L.done);
+    v.pan_part = at<int32_t>(b, L.pan_part);
     if (v.panels) {
-        v.bm_part = at<uint32_t>(b, L.bm_part);
         v.bm = at<uint32_t>(b, L.bm);
         v.wbase = at<int32_t>(b, L.wbase);
         v.desc = at<int4>(b, L.desc);
@@ -412,37 +414,36 @@ size_t spmm_image_budget_elems(int32_t m, int32_t nnz) {
 cudaError_t launch_plan_build(int it, const int32_t* ro, const void* row_idx, const void* col, const PlanView& v,
                               int64_t img_budget, cudaStream_t s) {
     if (v.m <= 0) return cudaSuccess;
-    const size_t smem_rows = v.panels ? (size_t)v.W * 8 : 0;
-    const size_t smem_pan = (size_t)v.W * 8;
-    if (smem_pan > 48 * 1024) {
+    // both kernels: the panel bitmap and its word prefix (2 W words) when panels are enabled
+    const size_t smem = v.panels ? (size_t)v.W * 8 : 0;
+    if (smem > 48 * 1024) {
         cudaError_t e = it == kIdx16 ? cudaFuncSetAttribute(plan_rows_kernel<uint16_t>,
-                                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_rows)
+                                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
                                      : cudaFuncSetAttribute(plan_rows_kernel<int32_t>,
-                                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_rows);
+                                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         e = it == kIdx16 ? cudaFuncSetAttribute(plan_upos_kernel<uint16_t>,
-                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_pan)
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
                          : cudaFuncSetAttribute(plan_upos_kernel<int32_t>,
-                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_pan);
+                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
-    cudaError_t e = cudaMemsetAsync(v.done, 0, (size_t)(v.P + 1) * sizeof(int32_t), s);
+    const unsigned rows_grid = (unsigned)v.P * kPlanCluster;
+    cudaError_t e = it == kIdx16
+                        ? launch_pdl_cluster(plan_rows_kernel<uint16_t>, rows_grid, kPlanThreads, smem, kPlanCluster, s,
+                                             ro, (const uint16_t*)row_idx, (const uint16_t*)col, v)
+                        : launch_pdl_cluster(plan_rows_kernel<int32_t>, rows_grid, kPlanThreads, smem, kPlanCluster, s,
+                                             ro, (const int32_t*)row_idx, (const int32_t*)col, v);
     if (e != cudaSuccess) return e;
-    e = it == kIdx16 ? launch_pdl(plan_rows_kernel<uint16_t>, v.ncta, kPlanThreads, smem_rows, s, ro,
-                                  (const uint16_t*)row_idx, (const uint16_t*)col, v, img_budget)
-                     : launch_pdl(plan_rows_kernel<int32_t>, v.ncta, kPlanThreads, smem_rows, s, ro,
-                                  (const int32_t*)row_idx, (const int32_t*)col, v, img_budget);
+    // U positions for every row group of every panel (only dense panels do work), plus the
+    // lists CTA
+    const unsigned upos_grid = (v.panels ? (unsigned)v.P * kGroups : 0u) + 1u;
+    e = it == kIdx16 ? launch_pdl(plan_upos_kernel<uint16_t>, upos_grid, kPlanThreads, smem, s, ro,
+                                  (const uint16_t*)col, v, img_budget)
+                     : launch_pdl(plan_upos_kernel<int32_t>, upos_grid, kPlanThreads, smem, s, ro,
+                                  (const int32_t*)col, v, img_budget);
     if (e != cudaSuccess) return e;
-    int launches = 1;
-    if (v.panels) {
-        e = it == kIdx16 ? launch_pdl(plan_upos_kernel<uint16_t>, v.P * kGroups, kPlanThreads, smem_pan, s, ro,
-                                      (const uint16_t*)col, v)
-                         : launch_pdl(plan_upos_kernel<int32_t>, v.P * kGroups, kPlanThreads, smem_pan, s, ro,
-                                      (const int32_t*)col, v);
-        if (e != cudaSuccess) return e;
-        ++launches;
-    }
-    count_launches(launches);
+    count_launches(2);
     return cudaGetLastError();
 }
 

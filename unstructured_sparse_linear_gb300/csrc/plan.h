@@ -3,11 +3,10 @@
 //
 // Layout in caller memory (all offsets 1024-byte aligned, computed by plan_layout):
 //   hdr        int32[32]  bins_spmm[4], bins_sddmm[4], counts[8] (kCnt*), dims[4] {m, n, nnz, P}
-//   cta_part   int32[nc][4]   per row-group CTA: {#rows >= spmm long, #rows >= sddmm long,
-//                             #non-empty rows, #entries}; nc = 16 * P (8 positions each)
+//   pan_part   int32[P][4]    per panel: {#rows >= spmm long, #rows >= sddmm long,
+//                             #non-empty rows, #entries}
 // when panels are enabled (n <= 65536):
-//   bm_part    uint32[P][16][W] column bitmap of each 8-row group of a panel
-//   bm, wbase  [P][W]          OR-ed bitmap; exclusive prefix of its popcounts
+//   bm, wbase  [P][W]          column bitmap of a panel; exclusive prefix of its popcounts
 //   desc       int4[P]         {dense bits, |U|, entries, non-empty rows}; dense bit 0: SDDMM
 //                              tiles (|U| <= kUCap), bit 1: SpMM image (|U| <= kUList)
 //   prow       int32[P*128]    row id at each panel position (-1 past m)
@@ -35,8 +34,10 @@ constexpr int kUCap = 1024;       // most distinct columns of an SDDMM-dense pan
 constexpr int kUList = 2048;      // most distinct columns of a SpMM-dense panel (the image's K)
 constexpr int kTileN = 128;       // SDDMM tile width over U (UMMA N)
 constexpr int kTiles = kUCap / kTileN;
-constexpr int kGroupRows = 8;     // rows per plan CTA, one per warp (16 groups per panel)
+constexpr int kGroupRows = 8;     // rows per CTA of the U-position and image kernels, one per warp
 constexpr int kGroups = kPM / kGroupRows;
+constexpr int kPlanCluster = 8;   // CTAs per panel (one thread-block cluster) in the row step
+constexpr int kCtaRows = kPM / kPlanCluster;
 constexpr int kMaxPanelCols = 65536;
 constexpr int kMinDenseRows = 16;
 
@@ -51,9 +52,7 @@ enum PlanCount {
 
 struct PlanView {
     int32_t* hdr;
-    int32_t* cta_part;
-    int32_t* done;  // P + 1 completion counters of the plan kernel
-    uint32_t* bm_part;
+    int32_t* pan_part;
     uint32_t* bm;
     int32_t* wbase;
     int4* desc;
@@ -67,7 +66,7 @@ struct PlanView {
     int32_t* items;
     int32_t* dlist_sp;
     int32_t* img_slot;
-    int32_t m, n, nnz, P, W, ncta;
+    int32_t m, n, nnz, P, W;
     bool panels;
     __host__ __device__ int32_t* bins_spmm() const { return hdr; }
     __host__ __device__ int32_t* bins_sddmm() const { return hdr + 4; }
@@ -75,7 +74,7 @@ struct PlanView {
 };
 
 struct PlanLayout {
-    size_t hdr, cta_part, done, bm_part, bm, wbase, desc, prow, ulist, upos, ts, tmask, dense, sp_dense, items, dlist_sp,
+    size_t hdr, pan_part, bm, wbase, desc, prow, ulist, upos, ts, tmask, dense, sp_dense, items, dlist_sp,
         img_slot;
     size_t total;
 };
