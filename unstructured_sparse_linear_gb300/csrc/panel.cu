@@ -621,13 +621,14 @@ cudaError_t launch_spmm(int dt, int it, const void* vals, const int32_t* ro, con
     if (!panels)
         return launch_spmm_general(dt, it, vals, ro, row_idx, col, m, k, B, n, C, v.bins_spmm(), nullptr, s);
     // The general rows (outside the panels that get an image) and the panels write disjoint
-    // rows of C: the row kernel runs on the side stream while the panels run on s.
+    // rows of C: the row kernel runs on the side stream while the panels run on s. The panels
+    // are queued first, so that their CTAs are placed before the row kernel fills the SMs.
     cudaStream_t side = side_fork(s);
-    e = launch_spmm_general(dt, it, vals, ro, row_idx, col, m, k, B, n, C, v.bins_spmm(), v.sp_dense,
-                            side ? side : s);
-    if (e != cudaSuccess) return e;
     e = dt == kF16 ? run_spmm_panels<__half>(vals, ro, B, n, C, w, v, s)
                    : run_spmm_panels<__nv_bfloat16>(vals, ro, B, n, C, w, v, s);
+    if (e != cudaSuccess) return e;
+    e = launch_spmm_general(dt, it, vals, ro, row_idx, col, m, k, B, n, C, v.bins_spmm(), v.sp_dense,
+                            side ? side : s);
     if (e != cudaSuccess) return e;
     return side ? side_join(s) : cudaSuccess;
 }
@@ -643,13 +644,14 @@ cudaError_t launch_sddmm(int dt, int it, const int32_t* ro, const void* row_idx,
                         aligned16(A) && aligned16(BT);
     if (!panels)
         return launch_sddmm_general(dt, it, ro, row_idx, col, m, n, kd, A, BT, out, v.bins_sddmm(), nullptr, s);
-    // The general rows and the dense panels write disjoint entries: side stream for the rows.
+    // The general rows and the dense panels write disjoint entries: side stream for the rows,
+    // queued after the panels.
     cudaStream_t side = side_fork(s);
-    e = launch_sddmm_general(dt, it, ro, row_idx, col, m, n, kd, A, BT, out, v.bins_sddmm(), v.dense,
-                             side ? side : s);
-    if (e != cudaSuccess) return e;
     e = dt == kF16 ? run_sddmm_panels<__half>(A, BT, out, kd, v, s)
                    : run_sddmm_panels<__nv_bfloat16>(A, BT, out, kd, v, s);
+    if (e != cudaSuccess) return e;
+    e = launch_sddmm_general(dt, it, ro, row_idx, col, m, n, kd, A, BT, out, v.bins_sddmm(), v.dense,
+                             side ? side : s);
     if (e != cudaSuccess) return e;
     return side ? side_join(s) : cudaSuccess;
 }

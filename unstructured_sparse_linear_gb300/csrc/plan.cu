@@ -61,6 +61,42 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* sh, int* total) 
     return before;
 }
 
+// Set bits x[j] (x >= 0; -1: nothing) of the shared bitmap bm, called by all 32 lanes with
+// NB slices of entries. Lanes hold the entries of a row in U order, so lanes whose bits
+// fall in one word form runs; a segmented OR over the run (shuffles at distance 1, 2, 4, 8,
+// 16, taken while the lane at that distance has the same word) gathers the run's bits in its
+// first lane, which does the one atomic. A lane at distance d with the same word but outside
+// the run adds bits of that same word, which is harmless. The NB scans advance step by step
+// together, so their shuffle latencies overlap.
+template <int NB>
+__device__ __forceinline__ void or_bits_aggregated(uint32_t* bm, const int (&x)[NB], int lane) {
+    int w[NB];
+    uint32_t bits[NB];
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+        w[j] = x[j] >= 0 ? x[j] >> 5 : -1;
+        bits[j] = x[j] >= 0 ? 1u << (x[j] & 31) : 0u;
+    }
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        uint32_t ob[NB];
+        int ow[NB];
+#pragma unroll
+        for (int j = 0; j < NB; ++j) {
+            ob[j] = __shfl_down_sync(0xffffffffu, bits[j], d);
+            ow[j] = __shfl_down_sync(0xffffffffu, w[j], d);
+        }
+#pragma unroll
+        for (int j = 0; j < NB; ++j)
+            if (lane + d < 32 && ow[j] == w[j]) bits[j] |= ob[j];
+    }
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+        const int pw = __shfl_up_sync(0xffffffffu, w[j], 1);
+        if (w[j] >= 0 && (lane == 0 || pw != w[j])) atomicOr(&bm[w[j]], bits[j]);
+    }
+}
+
 constexpr int kRowsPerWarp = kCtaRows / (kPlanThreads / 32);  // positions per warp in the row step
 constexpr int kLoadBatch = 8;                                  // index loads per lane in flight
 
@@ -112,6 +148,7 @@ plan_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx, 
                 const int32_t k = t < len[0] ? k0[0] + t : k0[1] + (t - len[0]);
                 cc[j] = t < total ? idx_of(col[k]) : -1;
             }
+            // columns of a row are far apart in a sparse mask: plain atomics, few collide
 #pragma unroll
             for (int j = 0; j < kLoadBatch; ++j)
                 if (cc[j] >= 0) atomicOr(&bitmap[cc[j] >> 5], 1u << (cc[j] & 31));
@@ -320,12 +357,18 @@ plan_upos_kernel(const int32_t* __restrict__ ro, const I* __restrict__ col, Plan
             if (k >= k1) continue;
             v.upos[k] = (uint16_t)u[j];
             if (!tiles) continue;
-            atomicOr(&rmask[warp][u[j] >> 5], 1u << (u[j] & 31));
+
             const int t_cur = u[j] / kTileN;
             const int t_prev = k > k0 ? u_prev / kTileN : -1;
             for (int t = t_prev + 1; t <= t_cur; ++t) ts[t] = k;  // tiles starting at entry k
             if (k == k1 - 1)
                 for (int t = t_cur + 1; t <= kTiles; ++t) ts[t] = k1;
+        }
+        if (tiles) {
+            int um[kLoadBatch];
+#pragma unroll
+            for (int j = 0; j < kLoadBatch; ++j) um[j] = kb + j * 32 + lane < k1 ? u[j] : -1;
+            or_bits_aggregated<kLoadBatch>(rmask[warp], um, lane);  // U positions of a row are dense
         }
         carry = __shfl_sync(0xffffffffu, u[kLoadBatch - 1], 31);
     }

@@ -9,8 +9,9 @@
 //   * long rows (nnz >= kSpmmLongRow): one CTA per (row, 32*V-column chunk); the 8 warps
 //     take interleaved slices of the row's entries and their partial sums are combined in
 //     shared memory in warp order, so the result does not depend on timing;
-//   * short and empty rows: a group of G lanes per (row, G*V-column chunk), G the smallest
-//     power of two that covers n (at most 32); empty rows write zeros.
+//   * short rows: a group of G lanes per (row, G*V-column chunk), G the smallest power of
+//     two that covers n (at most 32);
+//   * empty rows (the positions past the non-empty count): a warp per row writes its zeros.
 // Each lane owns V = 16 / sizeof(T) consecutive output columns and gathers them from B with
 // one 16-byte load per entry. The group loads G (col, value) pairs at once, coalesced, and
 // broadcasts them with warp shuffles; four B rows are gathered before their FMAs so that
@@ -92,6 +93,7 @@ spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, con
     pdl_trigger();
     pdl_wait();
     const int32_t n_long = bins[1];
+    const int32_t n_ne = max(bins[2], n_long);  // positions before n_ne hold the non-empty rows
 
     // ---- long rows: one CTA per (row, chunk of 32*V columns)
     {
@@ -150,7 +152,7 @@ spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, con
         const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (gw * G));
         const int64_t gid = ((int64_t)blockIdx.x * kSpmmWarps + warp) * gpw + gw;
         const int64_t ngroups = (int64_t)gridDim.x * kSpmmWarps * gpw;
-        const int64_t items = (int64_t)(m - n_long) * nch;
+        const int64_t items = (int64_t)(n_ne - n_long) * nch;
         // Items go in batches of kBatch: their row ids, then their row offsets, are loaded
         // together before any is processed, so short and empty rows do not wait on one
         // dependent load chain each.
@@ -191,6 +193,55 @@ spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, con
                     accumulate<T, V>(acc, cj, vj, min(G, k1 - kb), B, N, col0, gmask, gw * G);
                 }
                 store_c<T, V>(C + (int64_t)rowq[q] * N, col0, N, acc);
+            }
+        }
+    }
+
+    // ---- positions from n_ne on (the empty rows when row_idx is sorted): a warp per row and
+    // all its column chunks, so an empty row costs one row id and one offset pair and then
+    // only stores of zeros. A row with entries here (unsorted row_idx) is summed the same way.
+    {
+        const int chunk = 32 * V;
+        const int nch = (N + chunk - 1) / chunk;
+        const int64_t gw = (int64_t)blockIdx.x * kSpmmWarps + warp;
+        const int64_t nw = (int64_t)gridDim.x * kSpmmWarps;
+        constexpr int kBatch = 4;
+        for (int64_t base = n_ne + gw; base < m; base += kBatch * nw) {
+            int rowq[kBatch];
+            int32_t k0q[kBatch], k1q[kBatch];
+            bool live[kBatch];
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+                const int64_t p = base + q * nw;
+                live[q] = p < m && !(skip && skip[p / kPanelRows]);  // uniform across the warp
+                rowq[q] = live[q] ? idx_of(row_idx[p]) : 0;
+            }
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+                k0q[q] = live[q] ? ro[rowq[q]] : 0;
+                k1q[q] = live[q] ? ro[rowq[q] + 1] : 0;
+            }
+#pragma unroll
+            for (int q = 0; q < kBatch; ++q) {
+                if (!live[q]) continue;
+                const int32_t k0 = k0q[q], k1 = k1q[q];
+                for (int c = 0; c < nch; ++c) {
+                    const int col0 = c * chunk + lane * V;
+                    float acc[V];
+#pragma unroll
+                    for (int e = 0; e < V; ++e) acc[e] = 0.f;
+                    for (int32_t kb = k0; kb < k1; kb += 32) {
+                        const int32_t kk = kb + lane;
+                        int cj = 0;
+                        float vj = 0.f;
+                        if (kk < k1) {
+                            cj = idx_of(col[kk]);
+                            vj = Elt<T>::to_f(vals[kk]);
+                        }
+                        accumulate<T, V>(acc, cj, vj, min(32, k1 - kb), B, N, col0, 0xffffffffu, 0);
+                    }
+                    store_c<T, V>(C + (int64_t)rowq[q] * N, col0, N, acc);
+                }
             }
         }
     }
