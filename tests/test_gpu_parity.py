@@ -102,6 +102,28 @@ def test_row_idx_any_permutation_gives_same_result(small_cases):
         assert torch.equal(ref[k].view(torch.int16), out[k].view(torch.int16)), k
 
 
+@pytest.mark.parametrize("name", ["rosa_s", "rosa_dense", "rosa_wide"])
+def test_row_idx_swaps_across_the_bins(small_cases, name):
+    """A row order that is sorted except for swaps across the bin boundaries: the longest row
+    goes to the last position (past the count of non-empty rows, where empty rows are
+    expected) and an empty row to the first, and a non-empty row of a dense panel trades
+    places with an empty row of a later panel. Every row must still be computed (or zeroed)
+    exactly once, on the panel or the general path."""
+    w = small_cases[name]
+    ro = w.row_offsets.numpy()
+    order = oracle.sort_rows(ro).copy()
+    lens = np.diff(ro)[order]
+    empty = np.flatnonzero(lens == 0)
+    assert empty.size >= 2 and lens[0] > 0
+    order[[0, -1]] = order[[-1, 0]]
+    j = int(empty[empty > 256][0]) if (empty > 256).any() else int(empty[-2])
+    order[[5, j]] = order[[j, 5]]
+    g = to_gpu(w, row_idx=torch.from_numpy(order))
+    out = run_all_ops(w, g)
+    assert_close(out["spmm"], oracle.spmm(ro, w.col_idx.numpy(), w.values, w.B), w.dtype, f"{name} spmm")
+    assert_close(out["sddmm"], oracle.sddmm(ro, w.col_idx.numpy(), w.A, w.BT), w.dtype, f"{name} sddmm")
+
+
 def test_repeated_calls_are_bitwise_deterministic(small_cases):
     w = small_cases["rosa_s"]
     g = to_gpu(w)
@@ -283,6 +305,33 @@ def test_full_size_sampled(name):
         assert_close(gen[torch.from_numpy(sel).cuda()], want, w.dtype, f"{name} sddmm general rows")
     if "csr_add" in out:
         assert_bits_equal(out["csr_add"], oracle.csr_add(ro, col, w.values, w.W), w.dtype, f"{name} csr_add")
+
+
+@pytest.mark.parametrize("case", ["butterfly", "clustered"])
+def test_spmm_many_units_pipeline_exact(case):
+    """More units (dense panels x column tiles) than four per SM, so SpMM takes the
+    warp-specialized tensor-core pipeline: a butterfly mask (64 dense panels whose U lists
+    are runs of 64 consecutive columns, loaded as tiles) and a clustered mask (random U
+    columns, gathered row by row); 17 or 9 column tiles, the last one 8 columns wide.
+    Small-integer inputs make every sum exact, so the result must equal the general row
+    kernel bit for bit on every element, and the oracle on sampled rows."""
+    if case == "butterfly":
+        s = wl.spec("butterfly", N=2056, kd=64)
+    else:
+        s = wl.spec("rosa", m=16384, n=4096, N=1032, kd=64)
+    w = wl.generate(s, integer_valued=True)
+    g = to_gpu(w)
+    plan = sp.plan_build(g["ro"], g["row_idx"], g["col"], w.n)
+    st = plan.stats()
+    assert st["spmm_panels"] == st["panels"] == 64 if case == "butterfly" else st["spmm_panels"] >= 10
+    C = sp.spmm(g["val"], g["ro"], g["row_idx"], g["col"], g["B"], w.m, plan=plan)
+    ref = sp.spmm(g["val"], g["ro"], g["row_idx"], g["col"], g["B"], w.m, path="general")
+    torch.cuda.synchronize()
+    assert torch.equal(C.view(torch.int16), ref.view(torch.int16))
+    ro, col = w.row_offsets.numpy(), w.col_idx.numpy()
+    rows = sample_rows(ro, 40)
+    want = oracle.spmm(ro, col, w.values, w.B, rows=rows)
+    assert_bits_equal(C[torch.from_numpy(rows).cuda()], want, w.dtype, f"{case} many-units spmm rows")
 
 
 # ------------------------------------------------------------------ mask plan

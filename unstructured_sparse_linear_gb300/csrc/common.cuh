@@ -196,6 +196,28 @@ __device__ __forceinline__ void bulk_wait() {
     asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// ------------------------------------------------------------------ panel skip flags
+
+// Per-panel skip flags (panels of 128 row_idx positions handled on the tensor cores) as the
+// general row kernels read them: copied into shared memory once per CTA when there are at
+// most kSkipCache panels, so the many tests of a persistent loop are not global loads.
+constexpr int kSkipCache = 4096;
+
+struct SkipFlags {
+    const uint8_t* f;  // the shared copy or the global flags (generic address); nullptr: none
+    __device__ __forceinline__ bool operator()(int64_t pos) const { return f && f[pos >> 7] != 0; }
+};
+
+// Call after pdl_wait (the flags come from the plan), by every thread of the CTA.
+__device__ __forceinline__ SkipFlags load_skip_flags(const uint8_t* skip, int64_t m, uint8_t* cache) {
+    const int64_t P = (m + 127) >> 7;
+    const bool cached = skip != nullptr && P <= kSkipCache;
+    if (cached)
+        for (int64_t i = threadIdx.x; i < P; i += blockDim.x) cache[i] = skip[i];
+    __syncthreads();
+    return SkipFlags{cached ? cache : skip};
+}
+
 // ------------------------------------------------------------------ thread-block clusters
 
 __device__ __forceinline__ uint32_t cluster_rank() {

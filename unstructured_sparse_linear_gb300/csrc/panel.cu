@@ -20,6 +20,9 @@
 // memory ring (two CTAs per SM, so two units' latency chains overlap); one thread issues
 // the MMAs and commits them to per-stage mbarriers, whose completion frees the stage for
 // the next copy. Every mbarrier wait is bounded in time.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <type_traits>
 
 #include "common.cuh"
@@ -495,6 +498,237 @@ spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restric
     if (warp == 0) tc::tmem_dealloc(tmem, kSpNT);
 }
 
+// Warp-specialized SpMM panels for masks with many units (units = dense panels x column
+// tiles well above the CTA count): one CTA per SM runs a persistent pipeline in which the
+// operand loads, the MMAs and the epilogue of consecutive units overlap. Each CTA takes a
+// contiguous range of units, so consecutive units mostly share their panel (its U list,
+// image and rows are looked up once per panel, not once per unit).
+//   warps 0-3   epilogue: thread r owns TMEM lane r (panel row r); it reads the finished
+//               accumulator, frees it, converts the row to the output dtype into its own
+//               shared row and sends it to C with one bulk async copy;
+//   warps 4-7   producers: per 64-wide K chunk, one bulk async copy of the image chunk
+//               (16 KB, contiguous, already swizzled) and the chunk's 64 B rows: when they
+//               are 64 consecutive rows of B (block-structured masks), two TMA tile loads
+//               (64 x 64 boxes, 128-byte swizzle) straight into the MN-major operand layout;
+//               otherwise a gather (cp.async, 16 bytes each) whose completion is signalled
+//               on the stage's mbarrier (cp.async.mbarrier.arrive.noinc). Each producer warp
+//               keeps its own shared copy of the panel's U list (no barrier between the
+//               producer warps);
+//   warp 8      TMEM owner and MMA issuer (one thread): 4 MMAs per chunk, a commit that
+//               frees the stage, and a commit per unit that hands the accumulator to the
+//               epilogue.
+// Two accumulators of 128 columns alternate between units, so the MMAs of a unit run while
+// the epilogue drains the previous one. Every wait is bounded in time; a role that gives up
+// stops, and the others then give up on their next wait.
+constexpr int kWsStages = 4;
+constexpr int kWsEpiWarps = 4;
+constexpr int kWsProdWarps = 4;
+constexpr int kWsProd = kWsProdWarps * 32;
+constexpr int kWsThreads = (kWsEpiWarps + kWsProdWarps + 1) * 32;
+constexpr uint32_t kWsCStage = kPM * kSpCRowBytes;  // staged C rows
+constexpr uint32_t kWsUList = kUList * 4;           // one producer warp's copy of a U list
+constexpr uint32_t kWsSmem = kWsStages * kSpStageBytes + kWsCStage + kWsProdWarps * kWsUList + 1024;
+static_assert(kWsSmem <= 227 * 1024, "warp-specialized SpMM shared memory");
+
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// 2-D TMA tile load of the box at (x = column, y = row) into shared memory, completing on bar.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kWsThreads, 1)
+spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restrict__ img_base, int32_t N,
+                     PlanView v, uint32_t idesc, int* err, const __grid_constant__ CUtensorMap tmap_b, int use_tma) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[kWsStages], empty_bar[kWsStages], tfull_bar[2], tempty_bar[2], drain_bar;
+    __shared__ uint32_t tmem_base_sh;
+    uint8_t* smem = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(smem_raw), 1024));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t cstage = sbase + kWsStages * kSpStageBytes;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_trigger();
+
+    if (warp == kWsEpiWarps + kWsProdWarps) tc::tmem_alloc(smem_u32(&tmem_base_sh), 2 * kSpNT);
+    if (tid == 0) {
+        for (int i = 0; i < kWsStages; ++i) {
+            mbar_init(smem_u32(&full_bar[i]), kWsProd + 1);  // producer threads' cp.async + the bulk copy's arrive
+            mbar_init(smem_u32(&empty_bar[i]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(&tfull_bar[i]), 1);
+            mbar_init(smem_u32(&tempty_bar[i]), kWsEpiWarps);
+        }
+        mbar_init(smem_u32(&drain_bar), 1);
+        fence_mbar_init();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = tmem_base_sh;
+    pdl_wait();  // the plan, the images and B come from earlier kernels
+
+    const int D = v.counts()[kCntDenseSp];
+    const int ntn = (N + kSpNT - 1) / kSpNT;
+    const int64_t units = (int64_t)D * ntn;
+    const int64_t per = (units + gridDim.x - 1) / gridDim.x;
+    const int64_t u_begin = min64(units, (int64_t)blockIdx.x * per), u_end = min64(units, u_begin + per);
+
+    if (warp < kWsEpiWarps) {
+        // ---------------- epilogue
+        const int r = tid;  // panel row = TMEM lane
+        const uint32_t crow = cstage + (uint32_t)r * kSpCRowBytes;
+        uint32_t t = 0;
+        int64_t cur = -1;
+        int i = -1;
+        for (int64_t unit = u_begin; unit < u_end; ++unit, ++t) {
+            if (unit / ntn != cur) {
+                cur = unit / ntn;
+                i = v.prow[v.dlist_sp[cur] * kPM + r];
+            }
+            const int n0 = (int)(unit % ntn) * kSpNT;
+            const uint32_t a = t & 1u;
+            // warp-uniform outcome: the TMEM loads below are warp-collective
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull_bar[a]), (t >> 1) & 1u, err))) break;
+            tc::fence_after_sync();
+            uint4 packed[kSpNT / 8];
+#pragma unroll
+            for (int c = 0; c < kSpNT / 32; ++c) {
+                float x[32];
+                tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + a * kSpNT + c * 32, x);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) packed[c * 4 + q] = Elt<T>::pack(x + q * 8);
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[a]));
+            bulk_wait_read<0>();  // this thread's previous row has left its shared row
+#pragma unroll
+            for (int q = 0; q < kSpNT / 8; ++q)
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(crow + q * 16), "r"(packed[q].x),
+                             "r"(packed[q].y), "r"(packed[q].z), "r"(packed[q].w)
+                             : "memory");
+            fence_proxy_async_smem();
+            if (i >= 0) {
+                bulk_s2g(C + (int64_t)i * N + n0, crow, (uint32_t)min(kSpNT, N - n0) * (uint32_t)sizeof(T));
+                bulk_commit();
+            }
+        }
+        bulk_wait<0>();
+    } else if (warp < kWsEpiWarps + kWsProdWarps) {
+        // ---------------- producers
+        const int pw = warp - kWsEpiWarps;
+        const int pt = tid - kWsEpiWarps * 32;  // 0 .. kWsProd - 1
+        int32_t* s_u = reinterpret_cast<int32_t*>(smem + kWsStages * kSpStageBytes + kWsCStage + pw * kWsUList);
+        constexpr int kPieces = kSpNT / 8;      // 16-byte pieces per B row of the tile
+        constexpr int kRowsPer = kKC * kPieces / kWsProd;
+        static_assert(kWsProd % kPieces == 0, "a producer thread keeps one piece column");
+        const int nch = pt % kPieces;           // this thread's piece of every row it copies
+        uint32_t g = 0;
+        bool ok = true;
+        int64_t cur = -1;
+        int nU = 0, nk = 0;
+        const T* img = img_base;
+        for (int64_t unit = u_begin; unit < u_end && ok; ++unit) {
+            if (unit / ntn != cur) {  // a new panel: its U list into this warp's shared copy
+                cur = unit / ntn;
+                const int p = v.dlist_sp[cur];
+                nU = v.desc[p].y;
+                nk = (nU + kKC - 1) / kKC;
+                img = img_base + v.img_slot[p];
+                const int32_t* ul = v.ulist + (size_t)p * kUList;
+                __syncwarp();  // the previous panel's copy has been read by the whole warp
+                for (int x = lane; x < nk * kKC; x += 32) s_u[x] = x < nU ? ul[x] : -1;
+                __syncwarp();
+            }
+            const int ncol = (int)(unit % ntn) * kSpNT + nch * 8;
+            for (int j = 0; j < nk; ++j, ++g) {
+                const uint32_t st = g % kWsStages;
+                // warp-uniform outcome: the warp synchronizes on its U list copy
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty_bar[st]), ((g / kWsStages) + 1) & 1u, err))) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sa = sbase + st * kSpStageBytes;
+                const uint32_t fb = smem_u32(&full_bar[st]);
+                // U is sorted and distinct, so 64 positions spanning 63 columns are consecutive
+                const int u0 = s_u[j * kKC];
+                if (use_tma && j * kKC + kKC - 1 < nU && s_u[j * kKC + kKC - 1] - u0 == kKC - 1) {
+                    if (pt == 0) {
+                        mbar_arrive_expect_tx(fb, kSpStageBytes);
+                        bulk_g2s(sa, img + (size_t)j * kPM * kKC, kSpStageA, fb);
+                        const int x0 = ncol - nch * 8;  // the tile's first column
+                        tma_load_2d(sa + kSpStageA, &tmap_b, x0, u0, fb);
+                        tma_load_2d(sa + kSpStageA + (kKC / 8) * 1024, &tmap_b, x0 + 64, u0, fb);
+                    }
+                    mbar_arrive(fb);  // every producer thread arrives once per chunk on either path
+                    continue;
+                }
+                if (pt == 0) {
+                    mbar_arrive_expect_tx(fb, kSpStageA);
+                    bulk_g2s(sa, img + (size_t)j * kPM * kKC, kSpStageA, fb);
+                }
+#pragma unroll
+                for (int q = 0; q < kRowsPer; ++q) {
+                    const int kk = pt / kPieces + (kWsProd / kPieces) * q;
+                    const int u = s_u[j * kKC + kk];
+                    const bool in = u >= 0 && ncol < N;
+                    const uint32_t off = (uint32_t)(nch >> 3) * (kKC / 8 * 1024) + tc::sw128_off(kk, nch & 7);
+                    tc::cp_async16(sa + kSpStageA + off, in ? (const void*)(B + (int64_t)u * N + ncol) : (const void*)B,
+                                   in ? 16 : 0);
+                }
+                cp_async_mbar_arrive(fb);
+            }
+        }
+        tc::cp_async_wait<0>();
+    } else if (lane == 0) {
+        // ---------------- MMA issuer
+        uint32_t g = 0, t = 0;
+        bool ok = true;
+        int64_t cur = -1;
+        int nk = 0;
+        for (int64_t unit = u_begin; unit < u_end && ok; ++unit, ++t) {
+            if (unit / ntn != cur) {
+                cur = unit / ntn;
+                nk = (v.desc[v.dlist_sp[cur]].y + kKC - 1) / kKC;
+            }
+            const uint32_t a = t & 1u;
+            if (!mbar_wait(smem_u32(&tempty_bar[a]), ((t >> 1) + 1) & 1u, err)) break;
+            tc::fence_after_sync();
+            for (int j = 0; j < nk; ++j, ++g) {
+                const uint32_t st = g % kWsStages;
+                if (!mbar_wait(smem_u32(&full_bar[st]), (g / kWsStages) & 1u, err)) {
+                    ok = false;
+                    break;
+                }
+                fence_proxy_async_smem();  // cp.async data (generic proxy) before the tensor core reads it
+                tc::fence_after_sync();
+                const uint32_t sa = sbase + st * kSpStageBytes;
+#pragma unroll
+                for (int kk = 0; kk < kKC / 16; ++kk) {
+                    const uint64_t ad = tc::smem_desc_sw128(sa + kk * 32, 16, 1024);
+                    const uint64_t bd = tc::smem_desc_sw128(sa + kSpStageA + kk * 2048, kKC / 8 * 1024, 1024);
+                    tc::mma_f16(tmem + a * kSpNT, ad, bd, idesc, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc::mma_commit(smem_u32(&empty_bar[st]));
+            }
+            if (ok) tc::mma_commit(smem_u32(&tfull_bar[a]));
+        }
+        // every MMA of this thread has completed before the accumulators are released
+        tc::mma_commit(smem_u32(&drain_bar));
+        mbar_wait(smem_u32(&drain_bar), 0, err);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == kWsEpiWarps + kWsProdWarps) tc::tmem_dealloc(tmem, 2 * kSpNT);
+}
+
 // ------------------------------------------------------------------ host dispatch
 
 template <typename T>
@@ -549,17 +783,57 @@ cudaError_t run_sddmm_panels(const void* A, const void* BT, void* out, int32_t k
     return cudaGetLastError();
 }
 
+// Tensor map of a row-major K x N matrix of 16-bit elements for 64 x 64 boxes with the
+// 128-byte swizzle (false if the driver entry point is unavailable or rejects it).
+bool encode_rows_map(CUtensorMap* map, const void* base, int32_t K, int32_t N, bool bf16) {
+    static const PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            f = nullptr;
+        }
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    if (!encode || K <= 0 || N <= 0 || (reinterpret_cast<uintptr_t>(base) & 15) || ((int64_t)N * 2) % 16) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)K};
+    const cuuint64_t strides[1] = {(cuuint64_t)N * 2};
+    const cuuint32_t box[2] = {64, 64};
+    const cuuint32_t elem[2] = {1, 1};
+    return encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <typename T>
-cudaError_t run_spmm_panels(const void* vals, const int32_t* ro, const void* B, int32_t N, void* C, void* img,
-                            const PlanView& v, cudaStream_t s) {
+cudaError_t run_spmm_panels(const void* vals, const int32_t* ro, const void* B, int32_t K, int32_t N, void* C,
+                            void* img, const PlanView& v, cudaStream_t s) {
     cudaError_t e = launch_pdl(densify_kernel<T>, v.P * kGroups, 256, 0, s, static_cast<const T*>(vals), ro,
                                static_cast<T*>(img), v);
     if (e != cudaSuccess) return e;
     const int ntn = (N + kSpNT - 1) / kSpNT;
+    const uint32_t idesc_ws = tc::instr_desc_f16(std::is_same<T, __nv_bfloat16>::value ? 1u : 0u, 0, 1, kPM, kSpNT);
+    // Many units per CTA: the warp-specialized pipeline, one CTA per SM.
+    if ((int64_t)v.P * ntn >= (int64_t)device_props().sm_count * 6) {
+        auto kws = spmm_panel_ws_kernel<T>;
+        e = cudaFuncSetAttribute(kws, cudaFuncAttributeMaxDynamicSharedMemorySize, kWsSmem);
+        if (e != cudaSuccess) return e;
+        CUtensorMap tmap;
+        const int use_tma = encode_rows_map(&tmap, B, K, N, std::is_same<T, __nv_bfloat16>::value) ? 1 : 0;
+        e = launch_pdl(kws, device_props().sm_count, kWsThreads, kWsSmem, s, static_cast<const T*>(B),
+                       static_cast<T*>(C), static_cast<const T*>(img), N, v, idesc_ws, device_error_word(), tmap,
+                       use_tma);
+        count_launches(2);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
     const int grid = (int)min64((int64_t)device_props().sm_count * 2, (int64_t)v.P * ntn);
-    // Many units per CTA: 8 warps per CTA keep more gathers in flight; few units (each
-    // CTA about one): 4 warps, which share the SMs better with concurrent operators.
-    const bool wide = (int64_t)v.P * ntn >= (int64_t)device_props().sm_count * 6;
+    // Few units (each CTA about one): 4 warps, which share the SMs better with concurrent
+    // operators.
+    const bool wide = false;
     auto kern = wide ? spmm_panel_kernel<T, 256> : spmm_panel_kernel<T, 128>;
     const int threads = wide ? 256 : 128;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSpSmem);
@@ -624,8 +898,8 @@ cudaError_t launch_spmm(int dt, int it, const void* vals, const int32_t* ro, con
     // rows of C: the row kernel runs on the side stream while the panels run on s. The panels
     // are queued first, so that their CTAs are placed before the row kernel fills the SMs.
     cudaStream_t side = side_fork(s);
-    e = dt == kF16 ? run_spmm_panels<__half>(vals, ro, B, n, C, w, v, s)
-                   : run_spmm_panels<__nv_bfloat16>(vals, ro, B, n, C, w, v, s);
+    e = dt == kF16 ? run_spmm_panels<__half>(vals, ro, B, k, n, C, w, v, s)
+                   : run_spmm_panels<__nv_bfloat16>(vals, ro, B, k, n, C, w, v, s);
     if (e != cudaSuccess) return e;
     e = launch_spmm_general(dt, it, vals, ro, row_idx, col, m, k, B, n, C, v.bins_spmm(), v.sp_dense,
                             side ? side : s);

@@ -93,16 +93,19 @@ __global__ void __launch_bounds__(kSddmmThreads, 3)
 sddmm_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx, const I* __restrict__ col,
                   const T* __restrict__ A, const T* __restrict__ BT, T* __restrict__ out, int32_t kd, int G,
                   const int32_t* __restrict__ bins, const uint8_t* __restrict__ skip) {
+    __shared__ uint8_t skip_cache[kSkipCache];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     pdl_trigger();
     pdl_wait();
     // Short rows run over every position up to m, not only up to bins[2]: with an unsorted
     // row_idx, rows with entries may sit past the count of non-empty rows.
     const int32_t n_long = bins[1], n_rows = bins[3];
+    static_assert(kPanelRows == 128, "skip flags are per 128 positions");
+    const SkipFlags skipped = load_skip_flags(skip, n_rows, skip_cache);
 
     // ---- long rows: a CTA per row
     for (int32_t p = blockIdx.x; p < n_long; p += gridDim.x) {
-        if (skip && skip[p / kPanelRows]) continue;
+        if (skipped(p)) continue;
         const int row = idx_of(row_idx[p]);
         const int32_t k0 = ro[row], k1 = ro[row + 1];
         for (int32_t kb = k0 + warp * kNB; kb < k1; kb += kSddmmWarps * kNB)
@@ -116,7 +119,7 @@ sddmm_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx,
     const int64_t gid = ((int64_t)blockIdx.x * kSddmmWarps + warp) * gpw + gw;
     const int64_t ngroups = (int64_t)gridDim.x * kSddmmWarps * gpw;
     for (int64_t p = n_long + gid; p < n_rows; p += ngroups) {
-        if (skip && skip[p / kPanelRows]) continue;
+        if (skipped(p)) continue;
         const int row = idx_of(row_idx[p]);
         const int32_t k0 = ro[row], k1 = ro[row + 1];
         for (int32_t kb = k0; kb < k1; kb += kNB)

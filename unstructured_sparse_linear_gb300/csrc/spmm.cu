@@ -89,61 +89,65 @@ spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, con
                  const I* __restrict__ col, const T* __restrict__ B, T* __restrict__ C, int32_t m, int32_t N, int G,
                  const int32_t* __restrict__ bins, const uint8_t* __restrict__ skip) {
     __shared__ float red[kSpmmWarps][32 * V];
+    __shared__ uint8_t skip_cache[kSkipCache];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     pdl_trigger();
     pdl_wait();
+    static_assert(kPanelRows == 128, "skip flags are per 128 positions");
+    const SkipFlags skipped = load_skip_flags(skip, m, skip_cache);
     const int32_t n_long = bins[1];
     const int32_t n_ne = max(bins[2], n_long);  // positions before n_ne hold the non-empty rows
 
-    // ---- long rows: one CTA per (row, chunk of 32*V columns)
+    // ---- long rows: one CTA per (row, chunk of 32*V columns). Items are numbered row-major
+    // over positions [0, n_long) and dealt round-robin to the CTAs; the loop walks the panels
+    // (skipping those on the tensor cores with one test each) and, inside a panel, this
+    // CTA's items, so skipped panels cost no per-item arithmetic.
     {
         const int chunk = 32 * V;
         const int nch = (N + chunk - 1) / chunk;
-        const int64_t items = (int64_t)n_long * nch;
-        for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
-            const int32_t p = (int32_t)(item / nch);
-            if (skip && skip[p / kPanelRows]) {  // uniform across the CTA
-                // jump to this CTA's first item in the next panel
-                const int64_t next = (int64_t)(p / kPanelRows + 1) * kPanelRows * nch;
-                const int64_t g = gridDim.x;
-                item = next + (((int64_t)blockIdx.x - next) % g + g) % g - g;
-                continue;
-            }
-            const int c = (int)(item % nch);
-            const int row = idx_of(row_idx[p]);
-            const int32_t k0 = ro[row], k1 = ro[row + 1];
-            const int col0 = c * chunk + lane * V;
-            float acc[V];
+        const int64_t g = gridDim.x;
+        for (int64_t pan0 = 0; pan0 < n_long; pan0 += kPanelRows) {
+            if (skipped(pan0)) continue;  // uniform across the CTA
+            const int64_t i0 = pan0 * nch, i1 = min64(n_long, pan0 + kPanelRows) * nch;
+            for (int64_t item = i0 + (((int64_t)blockIdx.x - i0) % g + g) % g; item < i1; item += g) {
+                const int64_t rel = item - i0;  // < 128 * nch
+                const int32_t p = (int32_t)(pan0 + (uint32_t)rel / (uint32_t)nch);
+                const int c = (int)((uint32_t)rel % (uint32_t)nch);
+                const int row = idx_of(row_idx[p]);
+                const int32_t k0 = ro[row], k1 = ro[row + 1];
+                const int col0 = c * chunk + lane * V;
+                float acc[V];
 #pragma unroll
-            for (int e = 0; e < V; ++e) acc[e] = 0.f;
-            for (int32_t kb = k0 + warp * 32; kb < k1; kb += kSpmmThreads) {
-                const int32_t kk = kb + lane;
-                int cj = 0;
-                float vj = 0.f;
-                if (kk < k1) {
-                    cj = idx_of(col[kk]);
-                    vj = Elt<T>::to_f(vals[kk]);
+                for (int e = 0; e < V; ++e) acc[e] = 0.f;
+                for (int32_t kb = k0 + warp * 32; kb < k1; kb += kSpmmThreads) {
+                    const int32_t kk = kb + lane;
+                    int cj = 0;
+                    float vj = 0.f;
+                    if (kk < k1) {
+                        cj = idx_of(col[kk]);
+                        vj = Elt<T>::to_f(vals[kk]);
+                    }
+                    accumulate<T, V>(acc, cj, vj, min(32, k1 - kb), B, N, col0, 0xffffffffu, 0);
                 }
-                accumulate<T, V>(acc, cj, vj, min(32, k1 - kb), B, N, col0, 0xffffffffu, 0);
-            }
 #pragma unroll
-            for (int e = 0; e < V; ++e) red[warp][lane * V + e] = acc[e];
-            __syncthreads();
-            if (warp == 0) {
+                for (int e = 0; e < V; ++e) red[warp][lane * V + e] = acc[e];
+                __syncthreads();
+                if (warp == 0) {
 #pragma unroll
-                for (int e = 0; e < V; ++e) {
-                    float s = red[0][lane * V + e];
+                    for (int e = 0; e < V; ++e) {
+                        float sum = red[0][lane * V + e];
 #pragma unroll
-                    for (int w = 1; w < kSpmmWarps; ++w) s += red[w][lane * V + e];
-                    acc[e] = s;
+                        for (int w = 1; w < kSpmmWarps; ++w) sum += red[w][lane * V + e];
+                        acc[e] = sum;
+                    }
+                    store_c<T, V>(C + (int64_t)row * N, col0, N, acc);
                 }
-                store_c<T, V>(C + (int64_t)row * N, col0, N, acc);
+                __syncthreads();
             }
-            __syncthreads();
         }
     }
 
-    // ---- short and empty rows: a group of G lanes per (row, chunk of G*V columns)
+    // ---- short rows: a group of G lanes per (row, chunk of G*V columns)
     {
         const int chunk = G * V;
         const int nch = (N + chunk - 1) / chunk;
@@ -153,6 +157,7 @@ spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, con
         const int64_t gid = ((int64_t)blockIdx.x * kSpmmWarps + warp) * gpw + gw;
         const int64_t ngroups = (int64_t)gridDim.x * kSpmmWarps * gpw;
         const int64_t items = (int64_t)(n_ne - n_long) * nch;
+        const bool items32 = items < (int64_t)0x7fffffff;
         // Items go in batches of kBatch: their row ids, then their row offsets, are loaded
         // together before any is processed, so short and empty rows do not wait on one
         // dependent load chain each.
@@ -164,9 +169,16 @@ spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, con
 #pragma unroll
             for (int q = 0; q < kBatch; ++q) {
                 const int64_t item = base + q * ngroups;
-                const int32_t p = n_long + (int32_t)(item / nch);
-                live[q] = item < items && !(skip && skip[p / kPanelRows]);  // uniform across the group
-                cq[q] = (int)(item % nch);
+                int32_t p;
+                if (items32) {  // 32-bit division where the item numbers fit
+                    const uint32_t it = (uint32_t)min64(item, items);
+                    p = n_long + (int32_t)(it / (uint32_t)nch);
+                    cq[q] = (int)(it % (uint32_t)nch);
+                } else {
+                    p = n_long + (int32_t)(item / nch);
+                    cq[q] = (int)(item % nch);
+                }
+                live[q] = item < items && !skipped(p);  // uniform across the group
                 rowq[q] = live[q] ? idx_of(row_idx[p]) : 0;
             }
 #pragma unroll
