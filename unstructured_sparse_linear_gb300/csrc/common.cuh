@@ -205,6 +205,7 @@ constexpr int kSkipCache = 4096;
 
 struct SkipFlags {
     const uint8_t* f;  // the shared copy or the global flags (generic address); nullptr: none
+    bool all;          // every panel is skipped (known when the flags are cached)
     __device__ __forceinline__ bool operator()(int64_t pos) const { return f && f[pos >> 7] != 0; }
 };
 
@@ -212,10 +213,14 @@ struct SkipFlags {
 __device__ __forceinline__ SkipFlags load_skip_flags(const uint8_t* skip, int64_t m, uint8_t* cache) {
     const int64_t P = (m + 127) >> 7;
     const bool cached = skip != nullptr && P <= kSkipCache;
+    int open = 0;  // this thread saw a panel that is not skipped
     if (cached)
-        for (int64_t i = threadIdx.x; i < P; i += blockDim.x) cache[i] = skip[i];
-    __syncthreads();
-    return SkipFlags{cached ? cache : skip};
+        for (int64_t i = threadIdx.x; i < P; i += blockDim.x) {
+            cache[i] = skip[i];
+            open |= skip[i] == 0;
+        }
+    const bool any_open = __syncthreads_or(open) != 0;
+    return SkipFlags{cached ? cache : skip, cached && !any_open};
 }
 
 // ------------------------------------------------------------------ thread-block clusters

@@ -504,30 +504,38 @@ spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restric
 // contiguous range of units, so consecutive units mostly share their panel (its U list,
 // image and rows are looked up once per panel, not once per unit).
 //   warps 0-3   epilogue: thread r owns TMEM lane r (panel row r); it reads the finished
-//               accumulator, frees it, converts the row to the output dtype into its own
-//               shared row and sends it to C with one bulk async copy;
+//               accumulator (256 columns, in two halves), frees it, converts each half to
+//               the output dtype into its own shared row and sends it to C with one bulk
+//               async copy;
 //   warps 4-7   producers: per 64-wide K chunk, one bulk async copy of the image chunk
-//               (16 KB, contiguous, already swizzled) and the chunk's 64 B rows: when they
-//               are 64 consecutive rows of B (block-structured masks), two TMA tile loads
-//               (64 x 64 boxes, 128-byte swizzle) straight into the MN-major operand layout;
+//               (16 KB, contiguous, already swizzled) and the chunk's 64 rows of B (256
+//               columns): when they are 64 consecutive rows (block-structured masks), four
+//               TMA tile loads (64 x 64 boxes, 128-byte swizzle) straight into the MN-major
+//               operand layout;
 //               otherwise a gather (cp.async, 16 bytes each) whose completion is signalled
 //               on the stage's mbarrier (cp.async.mbarrier.arrive.noinc). Each producer warp
 //               keeps its own shared copy of the panel's U list (no barrier between the
 //               producer warps);
-//   warp 8      TMEM owner and MMA issuer (one thread): 4 MMAs per chunk, a commit that
+//   warp 8      TMEM owner and MMA issuer (one thread): 4 MMAs (M = 128, N = 256, K = 16)
+//               per chunk, a commit that
 //               frees the stage, and a commit per unit that hands the accumulator to the
 //               epilogue.
-// Two accumulators of 128 columns alternate between units, so the MMAs of a unit run while
-// the epilogue drains the previous one. Every wait is bounded in time; a role that gives up
+// Units are 256 columns wide, so every A chunk read by the tensor core serves 256 output
+// columns (shared-memory bandwidth, not the tensor pipe, bounds 128-column tiles). Two
+// accumulators of 256 columns (all of TMEM) alternate between units, so the MMAs of a unit
+// run while the epilogue drains the previous one. Every wait is bounded in time; a role that gives up
 // stops, and the others then give up on their next wait.
-constexpr int kWsStages = 4;
+constexpr int kWsNT = 256;                                     // columns of C per unit (UMMA N)
+constexpr uint32_t kWsStageB = kKC * kWsNT * 2;                // 32 KB
+constexpr uint32_t kWsStageBytes = kSpStageA + kWsStageB;      // 48 KB
+constexpr int kWsStages = 3;
 constexpr int kWsEpiWarps = 4;
 constexpr int kWsProdWarps = 4;
 constexpr int kWsProd = kWsProdWarps * 32;
 constexpr int kWsThreads = (kWsEpiWarps + kWsProdWarps + 1) * 32;
-constexpr uint32_t kWsCStage = kPM * kSpCRowBytes;  // staged C rows
+constexpr uint32_t kWsCStage = kPM * kSpCRowBytes;  // staged C half rows (128 columns)
 constexpr uint32_t kWsUList = kUList * 4;           // one producer warp's copy of a U list
-constexpr uint32_t kWsSmem = kWsStages * kSpStageBytes + kWsCStage + kWsProdWarps * kWsUList + 1024;
+constexpr uint32_t kWsSmem = kWsStages * kWsStageBytes + kWsCStage + kWsProdWarps * kWsUList + 1024;
 static_assert(kWsSmem <= 227 * 1024, "warp-specialized SpMM shared memory");
 
 __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
@@ -551,11 +559,11 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
     __shared__ uint32_t tmem_base_sh;
     uint8_t* smem = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(smem_raw), 1024));
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t cstage = sbase + kWsStages * kSpStageBytes;
+    const uint32_t cstage = sbase + kWsStages * kWsStageBytes;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pdl_trigger();
 
-    if (warp == kWsEpiWarps + kWsProdWarps) tc::tmem_alloc(smem_u32(&tmem_base_sh), 2 * kSpNT);
+    if (warp == kWsEpiWarps + kWsProdWarps) tc::tmem_alloc(smem_u32(&tmem_base_sh), 2 * kWsNT);
     if (tid == 0) {
         for (int i = 0; i < kWsStages; ++i) {
             mbar_init(smem_u32(&full_bar[i]), kWsProd + 1);  // producer threads' cp.async + the bulk copy's arrive
@@ -575,7 +583,7 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
     pdl_wait();  // the plan, the images and B come from earlier kernels
 
     const int D = v.counts()[kCntDenseSp];
-    const int ntn = (N + kSpNT - 1) / kSpNT;
+    const int ntn = (N + kWsNT - 1) / kWsNT;
     const int64_t units = (int64_t)D * ntn;
     const int64_t per = (units + gridDim.x - 1) / gridDim.x;
     const int64_t u_begin = min64(units, (int64_t)blockIdx.x * per), u_end = min64(units, u_begin + per);
@@ -592,32 +600,39 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
                 cur = unit / ntn;
                 i = v.prow[v.dlist_sp[cur] * kPM + r];
             }
-            const int n0 = (int)(unit % ntn) * kSpNT;
+            const int n0 = (int)(unit % ntn) * kWsNT;
             const uint32_t a = t & 1u;
             // warp-uniform outcome: the TMEM loads below are warp-collective
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull_bar[a]), (t >> 1) & 1u, err))) break;
             tc::fence_after_sync();
-            uint4 packed[kSpNT / 8];
+            const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16) + a * kWsNT;
 #pragma unroll
-            for (int c = 0; c < kSpNT / 32; ++c) {
-                float x[32];
-                tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + a * kSpNT + c * 32, x);
+            for (int h = 0; h < kWsNT / kSpNT; ++h) {
+                uint4 packed[kSpNT / 8];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) packed[c * 4 + q] = Elt<T>::pack(x + q * 8);
-            }
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[a]));
-            bulk_wait_read<0>();  // this thread's previous row has left its shared row
+                for (int c = 0; c < kSpNT / 32; ++c) {
+                    float x[32];
+                    tc::tmem_ld32(lane_addr + h * kSpNT + c * 32, x);
 #pragma unroll
-            for (int q = 0; q < kSpNT / 8; ++q)
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(crow + q * 16), "r"(packed[q].x),
-                             "r"(packed[q].y), "r"(packed[q].z), "r"(packed[q].w)
-                             : "memory");
-            fence_proxy_async_smem();
-            if (i >= 0) {
-                bulk_s2g(C + (int64_t)i * N + n0, crow, (uint32_t)min(kSpNT, N - n0) * (uint32_t)sizeof(T));
-                bulk_commit();
+                    for (int q = 0; q < 4; ++q) packed[c * 4 + q] = Elt<T>::pack(x + q * 8);
+                }
+                if (h == kWsNT / kSpNT - 1) {  // the whole accumulator row has been read
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[a]));
+                }
+                bulk_wait_read<0>();  // this thread's previous half row has left its shared row
+#pragma unroll
+                for (int q = 0; q < kSpNT / 8; ++q)
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(crow + q * 16), "r"(packed[q].x),
+                                 "r"(packed[q].y), "r"(packed[q].z), "r"(packed[q].w)
+                                 : "memory");
+                fence_proxy_async_smem();
+                const int nh = min(kSpNT, N - n0 - h * kSpNT);  // columns of this half inside C
+                if (i >= 0 && nh > 0) {
+                    bulk_s2g(C + (int64_t)i * N + n0 + h * kSpNT, crow, (uint32_t)nh * (uint32_t)sizeof(T));
+                    bulk_commit();
+                }
             }
         }
         bulk_wait<0>();
@@ -625,8 +640,8 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
         // ---------------- producers
         const int pw = warp - kWsEpiWarps;
         const int pt = tid - kWsEpiWarps * 32;  // 0 .. kWsProd - 1
-        int32_t* s_u = reinterpret_cast<int32_t*>(smem + kWsStages * kSpStageBytes + kWsCStage + pw * kWsUList);
-        constexpr int kPieces = kSpNT / 8;      // 16-byte pieces per B row of the tile
+        int32_t* s_u = reinterpret_cast<int32_t*>(smem + kWsStages * kWsStageBytes + kWsCStage + pw * kWsUList);
+        constexpr int kPieces = kWsNT / 8;      // 16-byte pieces per B row of the tile
         constexpr int kRowsPer = kKC * kPieces / kWsProd;
         static_assert(kWsProd % kPieces == 0, "a producer thread keeps one piece column");
         const int nch = pt % kPieces;           // this thread's piece of every row it copies
@@ -647,7 +662,7 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
                 for (int x = lane; x < nk * kKC; x += 32) s_u[x] = x < nU ? ul[x] : -1;
                 __syncwarp();
             }
-            const int ncol = (int)(unit % ntn) * kSpNT + nch * 8;
+            const int ncol = (int)(unit % ntn) * kWsNT + nch * 8;
             for (int j = 0; j < nk; ++j, ++g) {
                 const uint32_t st = g % kWsStages;
                 // warp-uniform outcome: the warp synchronizes on its U list copy
@@ -655,17 +670,18 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
                     ok = false;
                     break;
                 }
-                const uint32_t sa = sbase + st * kSpStageBytes;
+                const uint32_t sa = sbase + st * kWsStageBytes;
                 const uint32_t fb = smem_u32(&full_bar[st]);
                 // U is sorted and distinct, so 64 positions spanning 63 columns are consecutive
                 const int u0 = s_u[j * kKC];
                 if (use_tma && j * kKC + kKC - 1 < nU && s_u[j * kKC + kKC - 1] - u0 == kKC - 1) {
                     if (pt == 0) {
-                        mbar_arrive_expect_tx(fb, kSpStageBytes);
+                        mbar_arrive_expect_tx(fb, kWsStageBytes);
                         bulk_g2s(sa, img + (size_t)j * kPM * kKC, kSpStageA, fb);
                         const int x0 = ncol - nch * 8;  // the tile's first column
-                        tma_load_2d(sa + kSpStageA, &tmap_b, x0, u0, fb);
-                        tma_load_2d(sa + kSpStageA + (kKC / 8) * 1024, &tmap_b, x0 + 64, u0, fb);
+#pragma unroll
+                        for (int bx = 0; bx < kWsNT / 64; ++bx)
+                            tma_load_2d(sa + kSpStageA + bx * (kKC / 8) * 1024, &tmap_b, x0 + 64 * bx, u0, fb);
                     }
                     mbar_arrive(fb);  // every producer thread arrives once per chunk on either path
                     continue;
@@ -689,7 +705,15 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
         tc::cp_async_wait<0>();
     } else if (lane == 0) {
         // ---------------- MMA issuer
-        uint32_t g = 0, t = 0;
+        // Descriptors of each stage's first K step; K step kk adds 32 B (A) or 2 KB (B) to
+        // the 16-byte-unit start address in the low bits (no carry: shared addresses < 256 KB).
+        uint64_t ad0[kWsStages], bd0[kWsStages];
+#pragma unroll
+        for (int i = 0; i < kWsStages; ++i) {
+            ad0[i] = tc::smem_desc_sw128(sbase + i * kWsStageBytes, 16, 1024);
+            bd0[i] = tc::smem_desc_sw128(sbase + i * kWsStageBytes + kSpStageA, kKC / 8 * 1024, 1024);
+        }
+        uint32_t g = 0, t = 0, st = 0, ph = 0;  // chunk count, unit count, stage, stage parity
         bool ok = true;
         int64_t cur = -1;
         int nk = 0;
@@ -701,22 +725,30 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
             const uint32_t a = t & 1u;
             if (!mbar_wait(smem_u32(&tempty_bar[a]), ((t >> 1) + 1) & 1u, err)) break;
             tc::fence_after_sync();
+            const uint32_t acc = tmem + a * kWsNT;
             for (int j = 0; j < nk; ++j, ++g) {
-                const uint32_t st = g % kWsStages;
-                if (!mbar_wait(smem_u32(&full_bar[st]), (g / kWsStages) & 1u, err)) {
+                if (!mbar_wait(smem_u32(&full_bar[st]), ph, err)) {
                     ok = false;
                     break;
                 }
                 fence_proxy_async_smem();  // cp.async data (generic proxy) before the tensor core reads it
                 tc::fence_after_sync();
-                const uint32_t sa = sbase + st * kSpStageBytes;
+                uint64_t ad = ad0[0], bd = bd0[0];
 #pragma unroll
-                for (int kk = 0; kk < kKC / 16; ++kk) {
-                    const uint64_t ad = tc::smem_desc_sw128(sa + kk * 32, 16, 1024);
-                    const uint64_t bd = tc::smem_desc_sw128(sa + kSpStageA + kk * 2048, kKC / 8 * 1024, 1024);
-                    tc::mma_f16(tmem + a * kSpNT, ad, bd, idesc, (j > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int i = 1; i < kWsStages; ++i)
+                    if (st == (uint32_t)i) {
+                        ad = ad0[i];
+                        bd = bd0[i];
+                    }
+                tc::mma_f16(acc, ad, bd, idesc, j > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 1; kk < kKC / 16; ++kk)
+                    tc::mma_f16(acc, ad + (uint64_t)(kk * 32 / 16), bd + (uint64_t)(kk * 2048 / 16), idesc, 1u);
                 tc::mma_commit(smem_u32(&empty_bar[st]));
+                if (++st == kWsStages) {
+                    st = 0;
+                    ph ^= 1u;
+                }
             }
             if (ok) tc::mma_commit(smem_u32(&tfull_bar[a]));
         }
@@ -726,7 +758,7 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == kWsEpiWarps + kWsProdWarps) tc::tmem_dealloc(tmem, 2 * kSpNT);
+    if (warp == kWsEpiWarps + kWsProdWarps) tc::tmem_dealloc(tmem, 2 * kWsNT);
 }
 
 // ------------------------------------------------------------------ host dispatch
@@ -815,7 +847,7 @@ cudaError_t run_spmm_panels(const void* vals, const int32_t* ro, const void* B, 
                                static_cast<T*>(img), v);
     if (e != cudaSuccess) return e;
     const int ntn = (N + kSpNT - 1) / kSpNT;
-    const uint32_t idesc_ws = tc::instr_desc_f16(std::is_same<T, __nv_bfloat16>::value ? 1u : 0u, 0, 1, kPM, kSpNT);
+    const uint32_t idesc_ws = tc::instr_desc_f16(std::is_same<T, __nv_bfloat16>::value ? 1u : 0u, 0, 1, kPM, kWsNT);
     // Many units per CTA: the warp-specialized pipeline, one CTA per SM.
     if ((int64_t)v.P * ntn >= (int64_t)device_props().sm_count * 6) {
         auto kws = spmm_panel_ws_kernel<T>;

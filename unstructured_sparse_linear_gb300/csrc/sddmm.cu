@@ -102,6 +102,7 @@ sddmm_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx,
     const int32_t n_long = bins[1], n_rows = bins[3];
     static_assert(kPanelRows == 128, "skip flags are per 128 positions");
     const SkipFlags skipped = load_skip_flags(skip, n_rows, skip_cache);
+    if (skipped.all) return;  // every row is on the tensor cores
 
     // ---- long rows: a CTA per row
     for (int32_t p = blockIdx.x; p < n_long; p += gridDim.x) {

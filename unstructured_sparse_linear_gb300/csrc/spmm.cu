@@ -95,6 +95,7 @@ spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, con
     pdl_wait();
     static_assert(kPanelRows == 128, "skip flags are per 128 positions");
     const SkipFlags skipped = load_skip_flags(skip, m, skip_cache);
+    if (skipped.all) return;  // every row is on the tensor cores
     const int32_t n_long = bins[1];
     const int32_t n_ne = max(bins[2], n_long);  // positions before n_ne hold the non-empty rows
 
