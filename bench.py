@@ -566,9 +566,40 @@ def run_e2e(sp, w, dev, idx, args, flops, ws):
     e1.record(s_in)
     torch.cuda.synchronize(dev)
     ms = e0.elapsed_time(e1) / steps
+    link = host_link_bound(dev, h2d, d2h, ms)
     return {"value": round(ws * flops / (ms * 1e-3) / 1e9, 2), "unit": "GFLOP/s", "ms_per_step": round(ms, 4),
-            "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "link": link,
             "note": "pinned host buffers; copies on separate streams, two steps in flight"}
+
+
+def host_link_bound(dev, h2d, d2h, ms):
+    """The host link's own limit for the step's copies: pinned copy bandwidth measured here in
+    each direction alone and in both at once (as the pipelined step runs them), and the step
+    time those copies need at that rate: the end-to-end leg cannot beat it."""
+    nb = 64 << 20
+    hs, hd = torch.empty(nb, dtype=torch.uint8).pin_memory(), torch.empty(nb, dtype=torch.uint8).pin_memory()
+    ds, dd = torch.empty(nb, dtype=torch.uint8, device=dev), torch.empty(nb, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def rate(h2d_on, d2h_on, reps=8):
+        for r in range(reps + 2):
+            if r == 2:
+                torch.cuda.synchronize(dev)
+                t0 = time.perf_counter()
+            if h2d_on:
+                with torch.cuda.stream(s1):
+                    ds.copy_(hs, non_blocking=True)
+            if d2h_on:
+                with torch.cuda.stream(s2):
+                    hd.copy_(dd, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        return nb * reps / (time.perf_counter() - t0) / 1e9
+
+    up, down, both = rate(True, False), rate(False, True), rate(True, True)
+    common = min(h2d, d2h)  # bytes that move while the other direction is busy too
+    bound_ms = (common / (both * 1e9) + (h2d - common) / (up * 1e9) + (d2h - common) / (down * 1e9)) * 1e3
+    return {"h2d_gbs": round(up, 1), "d2h_gbs": round(down, 1), "both_ways_gbs_each": round(both, 1),
+            "bound_ms_per_step": round(bound_ms, 4), "frac_of_bound": round(bound_ms / ms, 3) if ms > 0 else None}
 
 
 # ------------------------------------------------------------------ CPU oracle

@@ -334,6 +334,32 @@ def test_spmm_many_units_pipeline_exact(case):
     assert_bits_equal(C[torch.from_numpy(rows).cuda()], want, w.dtype, f"{case} many-units spmm rows")
 
 
+@pytest.mark.parametrize("case", ["butterfly", "clustered"])
+def test_sddmm_many_tiles_pipeline_exact(case):
+    """At least two SDDMM tiles per SM are possible, so the structure-aware SDDMM runs its
+    tiles without a K split, eight warps per CTA: a butterfly mask (192 tiles) and a
+    clustered mask with random rows and columns (52 tiles); kd = 136 leaves a partial last
+    K chunk. Small-integer inputs make every dot product exact, so every entry must equal
+    the general kernel bit for bit, and the oracle on sampled rows."""
+    if case == "butterfly":
+        s = wl.spec("butterfly", N=64, kd=136)
+    else:
+        s = wl.spec("rosa", m=16384, n=4096, N=64, kd=136)
+    w = wl.generate(s, integer_valued=True)
+    g = to_gpu(w)
+    plan = sp.plan_build(g["ro"], g["row_idx"], g["col"], w.n)
+    assert plan.stats()["sddmm_tiles"] >= 40
+    got = sp.sddmm(g["ro"], g["row_idx"], g["col"], g["A"], g["BT"], plan=plan)
+    ref = sp.sddmm(g["ro"], g["row_idx"], g["col"], g["A"], g["BT"], backend="general")
+    torch.cuda.synchronize()
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+    ro, col = w.row_offsets.numpy(), w.col_idx.numpy()
+    rows = sample_rows(ro, 40)
+    want = oracle.sddmm(ro, col, w.A, w.BT, rows=rows)
+    sel = np.concatenate([np.arange(ro[i], ro[i + 1]) for i in rows])
+    assert_bits_equal(got[torch.from_numpy(sel).cuda()], want, w.dtype, f"{case} many-tiles sddmm rows")
+
+
 # ------------------------------------------------------------------ mask plan
 
 
