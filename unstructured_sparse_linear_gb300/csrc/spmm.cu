@@ -9,9 +9,8 @@
 //   * long rows (nnz >= kSpmmLongRow): one CTA per (row, 32*V-column chunk); the 8 warps
 //     take interleaved slices of the row's entries and their partial sums are combined in
 //     shared memory in warp order, so the result does not depend on timing;
-//   * short rows: a group of G lanes per (row, G*V-column chunk), G the smallest power of
-//     two that covers n (at most 32);
-//   * empty rows (the positions past the non-empty count): a warp per row writes its zeros.
+//   * short and empty rows: a group of G lanes per (row, G*V-column chunk), G the smallest
+//     power of two that covers n (at most 32); empty rows write zeros.
 // Each lane owns V = 16 / sizeof(T) consecutive output columns and gathers them from B with
 // one 16-byte load per entry. The group loads G (col, value) pairs at once, coalesced, and
 // broadcasts them with warp shuffles; four B rows are gathered before their FMAs so that
@@ -97,20 +96,25 @@ spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, con
     const SkipFlags skipped = load_skip_flags(skip, m, skip_cache);
     if (skipped.all) return;  // every row is on the tensor cores
     const int32_t n_long = bins[1];
-    const int32_t n_ne = max(bins[2], n_long);  // positions before n_ne hold the non-empty rows
 
     // ---- long rows: one CTA per (row, chunk of 32*V columns). Items are numbered row-major
     // over positions [0, n_long) and dealt round-robin to the CTAs; the loop walks the panels
-    // (skipping those on the tensor cores with one test each) and, inside a panel, this
-    // CTA's items, so skipped panels cost no per-item arithmetic.
+    // carrying this CTA's next item: a panel without one costs a compare, a skipped panel
+    // (on the tensor cores) one division to jump past it, an item a 32-bit division.
     {
         const int chunk = 32 * V;
         const int nch = (N + chunk - 1) / chunk;
         const int64_t g = gridDim.x;
-        for (int64_t pan0 = 0; pan0 < n_long; pan0 += kPanelRows) {
-            if (skipped(pan0)) continue;  // uniform across the CTA
+        const int64_t items = (int64_t)n_long * nch;
+        int64_t item = blockIdx.x;
+        for (int64_t pan0 = 0; pan0 < n_long && item < items; pan0 += kPanelRows) {
             const int64_t i0 = pan0 * nch, i1 = min64(n_long, pan0 + kPanelRows) * nch;
-            for (int64_t item = i0 + (((int64_t)blockIdx.x - i0) % g + g) % g; item < i1; item += g) {
+            if (item >= i1) continue;  // uniform across the CTA
+            if (skipped(pan0)) {
+                item += (i1 - item + g - 1) / g * g;
+                continue;
+            }
+            for (; item < i1; item += g) {
                 const int64_t rel = item - i0;  // < 128 * nch
                 const int32_t p = (int32_t)(pan0 + (uint32_t)rel / (uint32_t)nch);
                 const int c = (int)((uint32_t)rel % (uint32_t)nch);
@@ -148,7 +152,7 @@ spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, con
         }
     }
 
-    // ---- short rows: a group of G lanes per (row, chunk of G*V columns)
+    // ---- short and empty rows: a group of G lanes per (row, chunk of G*V columns)
     {
         const int chunk = G * V;
         const int nch = (N + chunk - 1) / chunk;
@@ -157,7 +161,7 @@ spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, con
         const unsigned gmask = G == 32 ? 0xffffffffu : (((1u << G) - 1u) << (gw * G));
         const int64_t gid = ((int64_t)blockIdx.x * kSpmmWarps + warp) * gpw + gw;
         const int64_t ngroups = (int64_t)gridDim.x * kSpmmWarps * gpw;
-        const int64_t items = (int64_t)(n_ne - n_long) * nch;
+        const int64_t items = (int64_t)(m - n_long) * nch;
         const bool items32 = items < (int64_t)0x7fffffff;
         // Items go in batches of kBatch: their row ids, then their row offsets, are loaded
         // together before any is processed, so short and empty rows do not wait on one
@@ -210,54 +214,6 @@ spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, con
         }
     }
 
-    // ---- positions from n_ne on (the empty rows when row_idx is sorted): a warp per row and
-    // all its column chunks, so an empty row costs one row id and one offset pair and then
-    // only stores of zeros. A row with entries here (unsorted row_idx) is summed the same way.
-    {
-        const int chunk = 32 * V;
-        const int nch = (N + chunk - 1) / chunk;
-        const int64_t gw = (int64_t)blockIdx.x * kSpmmWarps + warp;
-        const int64_t nw = (int64_t)gridDim.x * kSpmmWarps;
-        constexpr int kBatch = 4;
-        for (int64_t base = n_ne + gw; base < m; base += kBatch * nw) {
-            int rowq[kBatch];
-            int32_t k0q[kBatch], k1q[kBatch];
-            bool live[kBatch];
-#pragma unroll
-            for (int q = 0; q < kBatch; ++q) {
-                const int64_t p = base + q * nw;
-                live[q] = p < m && !(skip && skip[p / kPanelRows]);  // uniform across the warp
-                rowq[q] = live[q] ? idx_of(row_idx[p]) : 0;
-            }
-#pragma unroll
-            for (int q = 0; q < kBatch; ++q) {
-                k0q[q] = live[q] ? ro[rowq[q]] : 0;
-                k1q[q] = live[q] ? ro[rowq[q] + 1] : 0;
-            }
-#pragma unroll
-            for (int q = 0; q < kBatch; ++q) {
-                if (!live[q]) continue;
-                const int32_t k0 = k0q[q], k1 = k1q[q];
-                for (int c = 0; c < nch; ++c) {
-                    const int col0 = c * chunk + lane * V;
-                    float acc[V];
-#pragma unroll
-                    for (int e = 0; e < V; ++e) acc[e] = 0.f;
-                    for (int32_t kb = k0; kb < k1; kb += 32) {
-                        const int32_t kk = kb + lane;
-                        int cj = 0;
-                        float vj = 0.f;
-                        if (kk < k1) {
-                            cj = idx_of(col[kk]);
-                            vj = Elt<T>::to_f(vals[kk]);
-                        }
-                        accumulate<T, V>(acc, cj, vj, min(32, k1 - kb), B, N, col0, 0xffffffffu, 0);
-                    }
-                    store_c<T, V>(C + (int64_t)rowq[q] * N, col0, N, acc);
-                }
-            }
-        }
-    }
 }
 
 // Narrow B (N <= 16, SpMV at N = 1): streaming A dominates, so a warp takes one row at a
