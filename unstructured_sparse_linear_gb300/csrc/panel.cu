@@ -16,10 +16,12 @@
 //     UMMA K-major 128-byte-swizzled layout; C[panel rows, 128-column tile] =
 //     image * B[U, tile] on tcgen05, with B's rows gathered into an MN-major swizzled tile.
 //   * the other rows run through the general row kernels, which skip dense panels.
-// Operands are gathered row by row with 16-byte cp.async copies into a 3-stage shared
-// memory ring (two CTAs per SM, so two units' latency chains overlap); one thread issues
-// the MMAs and commits them to per-stage mbarriers, whose completion frees the stage for
-// the next copy. Every mbarrier wait is bounded in time.
+// With few units, operands are gathered row by row with 16-byte cp.async copies into a
+// 3-stage shared memory ring (two CTAs per SM, so two units' latency chains overlap); one
+// thread issues the MMAs and commits them to per-stage mbarriers, whose completion frees the
+// stage for the next copy. With many SpMM units, a warp-specialized kernel (one CTA per SM:
+// producer warps with bulk and TMA tile copies, an MMA thread, epilogue warps on two TMEM
+// accumulators) overlaps consecutive units. Every mbarrier wait is bounded in time.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -865,9 +867,8 @@ cudaError_t run_spmm_panels(const void* vals, const int32_t* ro, const void* B, 
     const int grid = (int)min64((int64_t)device_props().sm_count * 2, (int64_t)v.P * ntn);
     // Few units (each CTA about one): 4 warps, which share the SMs better with concurrent
     // operators.
-    const bool wide = false;
-    auto kern = wide ? spmm_panel_kernel<T, 256> : spmm_panel_kernel<T, 128>;
-    const int threads = wide ? 256 : 128;
+    auto kern = spmm_panel_kernel<T, kTileThreads>;
+    const int threads = kTileThreads;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSpSmem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
