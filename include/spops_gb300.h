@@ -172,8 +172,9 @@ SPOPS_API size_t spops_spmm_workspace_size(int32_t m, int32_t k, int32_t n, int3
  * A: m x k CSR (A_val [nnz] dtype, row_offsets [m+1], row_idx [m], col_idx [nnz]);
  * B: k x n row-major dtype; C: m x n row-major dtype, every element written (rows without
  * entries become zeros). C must not overlap B or A's arrays. path: spops_spmm_path; AUTO
- * runs the plan's dense panels on the tensor cores (fp16/bf16, n a multiple of 8, 16-byte
- * aligned B and C), the other rows on the general row kernels. plan: a plan built by
+ * runs the plan's dense panels on the tensor cores (fp16/bf16, n > 16 and a multiple of 8,
+ * 16-byte aligned B and C), the other rows on the general row kernels; n <= 16 takes a
+ * streaming warp-per-row kernel. plan: a plan built by
  * spops_plan_build for this mask (m x k), or NULL to build one inside the workspace. */
 SPOPS_API int spops_spmm(const void* A_val, const int32_t* row_offsets, const void* row_idx, const void* col_idx,
                          int itype, int dtype, int32_t m, int32_t k, int32_t nnz, const void* B, int32_t n, void* C,
