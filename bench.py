@@ -25,6 +25,7 @@ import re
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -121,15 +122,16 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, log_dir: str | None = None):
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.log_dir = log_dir or tempfile.gettempdir()
 
     def start(self):
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{self.gpu}.csv")
+            os.makedirs(self.log_dir, exist_ok=True)
+            self.path = os.path.join(self.log_dir, f"clocks_rank{self.gpu}.csv")
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.fh,
@@ -311,7 +313,7 @@ def run_gpu(args):
         torch.cuda.synchronize(dev)
 
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-        sampler = ClockSampler(local)
+        sampler = ClockSampler(local, args.clock_log_dir)
         if ws > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
@@ -694,6 +696,8 @@ def main():
     ap.add_argument("--ref-max-steps", type=int, default=20)
     ap.add_argument("--no-next-ops", action="store_true", help="skip timing csr_transpose / dB / masked Adam")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clock-log-dir", default=None,
+                    help="where the raw nvidia-smi clock samples go (default: the temp directory)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl != "reference":
         args.warmup = 3
