@@ -103,9 +103,11 @@ cudaStream_t side_fork(cudaStream_t s) {
             sd->stream = nullptr;
             return nullptr;
         }
+        sd->fork = sd->join = nullptr;
         if (cudaEventCreateWithFlags(&sd->fork, cudaEventDisableTiming) != cudaSuccess ||
             cudaEventCreateWithFlags(&sd->join, cudaEventDisableTiming) != cudaSuccess) {
             cudaGetLastError();
+            if (sd->fork) cudaEventDestroy(sd->fork);
             cudaStreamDestroy(sd->stream);
             sd->stream = nullptr;
             return nullptr;
