@@ -1,19 +1,23 @@
 """Benchmark of the CSR sparse-adapter hot path on GB300.
 
-One step = one pass of the whole path over one workload (default: the RoSA adapter, a
-4096 x 4096 fp16 weight, 1 % density clustered in 10 % of rows and columns, 2048 tokens):
+One step = one pass of the whole path over one workload:
   sort_rows (row_idx) -> plan_build (row bins + dense panels, shared by both products)
   -> spmm (C = A X) -> sddmm (structure-aware backend, grad = dY^T X sampled on the mask)
   -> csr_add (W + A)
 (operators the workload does not define are left out). metric: GFLOP/s counting
 2 * nnz * N for SpMM and 2 * nnz * kd for SDDMM; every operator's time is in the step.
+
+By default every configuration is measured in one run (tiny 256^2, the RoSA adapter, the
+LLaMA MLP weight, the Zipf matrix, the pixelfly butterfly layer, plus the narrow-N SpMM
+workload) and the headline fields (value, ms_per_step, roofline, cpu_baseline, e2e) are the
+butterfly layer's, the largest configuration; `per_config` holds each workload's record.
 Each step is one CUDA-graph replay of the library calls in which spmm, sddmm and csr_add
 (independent once row_idx and the plan exist) run on three streams; a second loop replays
 one graph per operator in order to give the per-operator times. L2 is flushed (a 256 MB
 write) before every timed step, outside the step's events.
 
---impl reference times the fp64 CPU oracle on the host cores on the same workload, metric
-and unit (a deliberately slow baseline, not a target).
+--impl reference times the fp64 CPU oracle on the host cores on the headline workload, with
+the same metric, unit and config (a deliberately slow baseline, not a target).
 """
 from __future__ import annotations
 
@@ -46,6 +50,12 @@ DESCRIPTION = {
     "butterfly": "pixelfly_butterfly_8192x2048_bf16_64x64blocks_8192tok",
     "spmv": "narrow_spmm_8192x8192_fp16_90pct_sparse_N8",
 }
+for _n, _s in wl.SPECS.items():
+    if _n.startswith("fly_"):
+        DESCRIPTION[_n] = f"pixelfly_mlp_layer_{_s.m}x{_s.n}_bf16_block{dict(_s.mask_kw)['block']}_{_s.N}tok"
+HEADLINE = "butterfly"            # the largest configuration carries the headline fields
+EXTRA_WORKLOADS = ["spmv"]       # measured after the five configurations (narrow-N SpMM)
+SINGLE_THREAD_BASELINE = ("tiny", "rosa", "llama_mlp")  # oracle also timed on one core
 
 
 def log(*a):
@@ -184,20 +194,29 @@ def kernel_source_hash(paths):
 
 def recorded_traffic(op: str, workload: str):
     """DRAM bytes per call of the op (its kernels summed) on this workload from the committed
-    ncu summary, if the kernel sources still match the hash recorded with the counters."""
+    ncu summary, if the kernel sources still match the hash recorded with the counters:
+    {"bytes": read + write, "read": ..., "write": ...} (read / write None in rows that give
+    only the sum), or None."""
     p = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(p):
         return None
     pat = re.compile(r"\|\s*" + re.escape(workload) + r"\s*\|\s*" + re.escape(op) +
-                     r"\s*\|\s*([\w./+]+)\s*\|\s*([0-9a-f]+)\s*\|\s*([0-9]+)\s*\|")
+                     r"\s*\|\s*([\w./+]+)\s*\|\s*([0-9a-f]+)\s*\|\s*([0-9]+)\s*\|"
+                     r"(?:\s*([0-9]+)\s*\|\s*([0-9]+)\s*\|)?")
     for line in open(p):
         mt = pat.match(line)
         if mt:
-            src, h, traffic = mt.group(1), mt.group(2), int(mt.group(3))
+            src, h = mt.group(1), mt.group(2)
+            if mt.group(4) is not None:  # | read | write | sum |
+                rd, wr, total = int(mt.group(3)), int(mt.group(4)), int(mt.group(5))
+            else:
+                rd, wr, total = None, None, int(mt.group(3))
             try:
-                return traffic if kernel_source_hash(src) == h else None
+                if kernel_source_hash(src) != h:
+                    return None
             except OSError:
                 return None
+            return {"bytes": total, "read": rd, "write": wr}
     return None
 
 
@@ -265,29 +284,36 @@ def host_inputs(w, idx):
     return h
 
 
-def run_gpu(args):
-    import torch.distributed as dist
+def config_dict(name, w, args):
+    """The `config` object of the JSON line for workload `name` (the same on both arms)."""
+    return {"workload": DESCRIPTION[name], "m": w.m, "n": w.n, "nnz": w.nnz,
+            "N": int(w.meta["spec"].N) or None, "kd": int(w.meta["spec"].kd) or None,
+            "index": "int16" if max(w.m, w.n) <= 32768 else "int32", "sddmm_backend": args.sddmm_backend,
+            "spmm_path": args.spmm_path, "l2": "flushed before every step (256 MB write, outside step events)",
+            "parallelism": "replicas (independent problems per GPU)"}
 
-    import unstructured_sparse_linear_gb300 as sp
 
-    ws, rank, local = dist_env()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if ws > 1:
-        dist.init_process_group("nccl", device_id=dev)
+def workload_list(args):
+    return list(wl.CONFIG_ORDER) + EXTRA_WORKLOADS if args.workload == "all" else [args.workload]
 
-    w = wl.generate(args.workload)
+
+def headline_name(args):
+    return HEADLINE if args.workload == "all" else args.workload
+
+
+def measure(sp, lib, name, args, dev, ws, rank, local, flush):
+    """Time one workload's step (CUDA graph replays, L2 flushed before each) and its
+    operators one at a time; then the end-to-end leg, the next operators and, on rank 0 at
+    N = 1, the oracle on a bounded sample. Returns the workload's JSON record."""
+    w = wl.generate(name)
     acc = accounting(w)
     flops = step_flops(acc)
     idx = index_dtype(w)
     d = {k: v.to(dev) for k, v in host_inputs(w, idx).items()}
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     outs = {}
     ops = make_ops(sp, w, d, idx, args, outs)
-
     stream = torch.cuda.Stream(device=dev)
     side = [torch.cuda.Stream(device=dev) for _ in range(2)]
-    lib = sp._lib.load()
     with torch.cuda.stream(stream):
         for _ in range(max(args.warmup, 1)):
             run_step_forked(ops, stream, side)  # eager, on the streams the graph uses
@@ -301,11 +327,11 @@ def run_gpu(args):
         launches_per_step = lib.spops_kernel_launches() - launches0
         # one graph per operator, replayed in order, for the per-operator breakdown
         op_graphs = []
-        for name, f in ops:
+        for op_name, f in ops:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream, pool=pool):
                 f()
-            op_graphs.append((name, g))
+            op_graphs.append((op_name, g))
         for _ in range(args.warmup):
             step_graph.replay()
             for _, g in op_graphs:
@@ -315,7 +341,7 @@ def run_gpu(args):
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
         sampler = ClockSampler(local, args.clock_log_dir)
         if ws > 1:
-            dist.barrier()
+            torch.distributed.barrier()
         torch.cuda.synchronize(dev)
         sampler.start()
         time.sleep(0.2)
@@ -328,7 +354,7 @@ def run_gpu(args):
         torch.cuda.synchronize(dev)
         wall = time.perf_counter() - t0
         if ws > 1:
-            dist.barrier()
+            torch.distributed.barrier()
         clocks = sampler.stop()
 
         # per-operator breakdown: the same graphs one operator at a time, events between them
@@ -344,53 +370,93 @@ def run_gpu(args):
         torch.cuda.synchronize(dev)
 
     step_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
-    op_ms = {name: [evb[s][j].elapsed_time(evb[s][j + 1]) for s in range(nb)]
-             for j, (name, _) in enumerate(op_graphs)}
+    op_ms = {op_name: [evb[s][j].elapsed_time(evb[s][j + 1]) for s in range(nb)]
+             for j, (op_name, _) in enumerate(op_graphs)}
     total_ms = max_over_ranks(sum(step_ms), dev)
     ms_per_step = total_ms / args.steps
     value = ws * flops * args.steps / (total_ms * 1e-3) / 1e9
+    del step_graph, op_graphs
 
     e2e = run_e2e(sp, w, dev, idx, args, flops, ws)
-
     next_ops = time_next_ops(sp, w, d, idx, stream, pool, flush, nb) if not args.no_next_ops else None
 
     pk = peaks()
     per_op = {}
-    for name, times in op_ms.items():
+    for op_name, times in op_ms.items():
         t_avg = sum(times) / len(times)
-        a = acc[name]
-        per_op[name] = {"ms": round(t_avg, 5), "ms_min": round(min(times), 5),
-                        "GFLOP/s": round(a["flops"] / (t_avg * 1e-3) / 1e9, 2) if a["flops"] else None,
-                        "GB/s": round(a["bytes"] / (t_avg * 1e-3) / 1e9, 1),
-                        "hbm_frac": round(a["bytes"] / (t_avg * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}
+        a = acc[op_name]
+        per_op[op_name] = {"ms": round(t_avg, 5), "ms_median": round(statistics.median(times), 5),
+                           "ms_min": round(min(times), 5),
+                           "GFLOP/s": round(a["flops"] / (t_avg * 1e-3) / 1e9, 2) if a["flops"] else None,
+                           "GB/s": round(a["bytes"] / (t_avg * 1e-3) / 1e9, 1),
+                           "hbm_frac": round(a["bytes"] / (t_avg * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+                           "algorithmic_bytes": int(a["bytes"])}
     dominant = max((k for k in per_op if k not in ("sort_rows", "plan")), key=lambda k: per_op[k]["ms"])
     dom_t = per_op[dominant]["ms"] * 1e-3
     achieved = acc[dominant]["bytes"] / dom_t / 1e9
+    traffic = recorded_traffic(dominant, name)
     roofline = {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
-                "traffic": recorded_traffic(dominant, args.workload), "algorithmic_bytes": acc[dominant]["bytes"],
-                "peak_source": pk["source"],
-                "note": "achieved = algorithmic bytes of the op / its mean event time in the per-operator loop"}
+                "traffic": traffic["bytes"] if traffic else None,
+                "traffic_read": traffic["read"] if traffic else None,
+                "traffic_write": traffic["write"] if traffic else None,
+                "algorithmic_bytes": acc[dominant]["bytes"], "peak_source": pk["source"],
+                "note": "achieved = algorithmic bytes of the operator / its mean event time in the per-operator "
+                        "loop (L2 flushed before each step); traffic = ncu dram__bytes_read + dram__bytes_write "
+                        "summed over the operator's kernels, from one capture per kernel; writes of an output "
+                        "that stays in the write-back L2 during the capture are not in dram__bytes_write"}
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, acc, seconds=args.cpu_seconds)
+        cpu = cpu_baseline(w, acc, seconds=args.cpu_seconds,
+                           single_thread=name in SINGLE_THREAD_BASELINE and args.workload == "all")
+    rec = {"value": round(value, 2), "unit": "GFLOP/s", "ms_per_step": round(ms_per_step, 5), "steps": args.steps,
+           "dtype": w.dtype, "config": config_dict(name, w, args), "per_op": per_op, "roofline": roofline,
+           "cpu_baseline": cpu, "e2e": e2e, "next_ops": next_ops,
+           "gpu_launches": int(launches_per_step) * args.steps, "launches_per_step": int(launches_per_step),
+           "clocks": clocks, "breakdown_steps": nb,
+           "step_ms_sum_of_ops": round(sum(v["ms"] for v in per_op.values()), 5),
+           "wall_s_timed_region": round(wall, 4)}
+    del d, outs, ops
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return rec
 
+
+def run_gpu(args):
+    import torch.distributed as dist
+
+    import unstructured_sparse_linear_gb300 as sp
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    lib = sp._lib.load()
+
+    head = headline_name(args)
+    per_config = {}
+    for name in workload_list(args):
+        log(f"[bench] {name}")
+        per_config[name] = measure(sp, lib, name, args, dev, ws, rank, local, flush)
+    extra = time_fly_mlps(sp, dev, flush, args) if args.workload == "all" and not args.no_next_ops else None
+
+    h = per_config[head]
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GFLOP/s", "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded; workload recipes in DESIGN.md)",
-        "config": {"workload": DESCRIPTION[args.workload], "m": w.m, "n": w.n, "nnz": w.nnz,
-                   "N": int(w.B.shape[1]) if w.B is not None else None,
-                   "kd": int(w.A.shape[1]) if w.A is not None else None,
-                   "index": str(idx).replace("torch.", ""), "sddmm_backend": args.sddmm_backend,
-                   "spmm_path": args.spmm_path,
-                   "l2": "flushed before every step (256 MB write, outside step events)",
-                   "parallelism": f"replicas x{ws} (independent problems per GPU)"},
-        "per_op": per_op, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "next_ops": next_ops,
-        "gpu_launches": int(launches_per_step) * args.steps, "clocks": clocks,
-        "breakdown_steps": nb, "step_ms_sum_of_ops": round(sum(v["ms"] for v in per_op.values()), 5),
-        "wall_s_timed_region": round(wall, 4),
+        "metric": METRIC, "value": h["value"], "unit": "GFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": h["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": h["dtype"], "data": "synthetic (seeded; workload recipes in DESIGN.md)",
+        "config": h["config"], "per_op": h["per_op"], "roofline": h["roofline"], "cpu_baseline": h["cpu_baseline"],
+        "e2e": h["e2e"], "gpu_launches": h["gpu_launches"], "clocks": h["clocks"],
+        "headline": f"{head}: the step (sort_rows+plan+spmm+sddmm+csr_add where defined) on this workload; "
+                    "per_config holds every configuration measured the same way",
+        "per_config": {k: {kk: vv for kk, vv in v.items() if kk != "next_ops"} for k, v in per_config.items()},
+        "next_ops": {k: v["next_ops"] for k, v in per_config.items() if v.get("next_ops")},
+        "pixelfly_mlps": extra,
+        "breakdown_steps": h["breakdown_steps"], "step_ms_sum_of_ops": h["step_ms_sum_of_ops"],
+        "wall_s_timed_region": h["wall_s_timed_region"],
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -501,6 +567,95 @@ def time_next_ops(sp, w, d, idx, stream, pool, flush, reps):
     if "layer_fwd_bwd_sparse" in out:
         out["layer_speedup_vs_dense"] = round(out["layer_fwd_bwd_dense_cublas"]["ms"] /
                                               out["layer_fwd_bwd_sparse"]["ms"], 3)
+    return out
+
+
+def time_fly_mlps(sp, dev, flush, args, iters: int = 100):
+    """The two MLPs of the pixelfly issue's T4 comment ([16, 512, D] inputs, forward and
+    backward repeated 100 times): each layer a SparseLinear on its butterfly mask (forward
+    spmm; backward sddmm for dW, value refresh of the cached transpose and spmm for dX),
+    against the same layers with dense weights on cuBLAS (six GEMMs per iteration). Both run
+    as CUDA graphs replayed back to back (a training loop: no L2 flush between iterations).
+    No activation function sits between the layers (only the linear layers are timed)."""
+    out = {}
+    stream = torch.cuda.Stream(device=dev)
+    for mlp in wl.FLY_MLPS:
+        names = wl.fly_layer_names(mlp)
+        with torch.cuda.stream(stream):
+            layers, dense_w = [], []
+            for nm in names:
+                w = wl.generate(nm, operands=())
+                idx = index_dtype(w)
+                L = sp.SparseLinear(w.row_offsets.to(dev), w.col_idx.to(idx).to(dev), w.values.to(dev), w.n)
+                layers.append(L)
+                Wd = torch.zeros((w.m, w.n), dtype=w.values.dtype, device=dev)
+                rows_of = torch.repeat_interleave(torch.arange(w.m, device=dev), torch.diff(L.row_offsets.long()))
+                Wd[rows_of, L.col_idx.long()] = L.values.detach()
+                dense_w.append(Wd)
+            T = wl.FLY_MLPS[mlp]["tokens"]
+            g = torch.Generator(device="cpu").manual_seed(7)
+            X = torch.randn((layers[0].in_features, T), generator=g).to(torch.bfloat16).to(dev)
+            dY = torch.randn((layers[-1].out_features, T), generator=g).to(torch.bfloat16).to(dev)
+            vals = [L.values.detach() for L in layers]
+            vt = [torch.empty_like(v) for v in vals]
+
+            def sparse_iter():
+                acts = [X]
+                for L, v in zip(layers, vals):
+                    acts.append(sp.spmm(v, L.row_offsets, L.row_idx, L.col_idx, acts[-1], L.out_features,
+                                        plan=L.plan))
+                grad = dY
+                for li in range(len(layers) - 1, -1, -1):
+                    L = layers[li]
+                    sp.sddmm(L.row_offsets, L.row_idx, L.col_idx, grad, acts[li], plan=L.plan)
+                    sp.permute_values(vals[li], L.transpose, out=vt[li])
+                    grad = sp.spmm(vt[li], L.transpose.row_offsets, L.row_idx_t, L.transpose.col_idx, grad,
+                                   L.in_features, plan=L.plan_t)
+
+            def dense_iter():
+                acts = [X]
+                for Wd in dense_w:
+                    acts.append(torch.matmul(Wd, acts[-1]))
+                grad = dY
+                for li in range(len(dense_w) - 1, -1, -1):
+                    torch.matmul(grad, acts[li].t())
+                    grad = torch.matmul(dense_w[li].t(), grad)
+
+            res = {}
+            for kind, f in (("sparse", sparse_iter), ("dense_cublas", dense_iter)):
+                for _ in range(3):
+                    f()
+                torch.cuda.synchronize(dev)
+                gph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gph, stream=stream):
+                    f()
+                for _ in range(3):
+                    gph.replay()
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(iters):
+                    gph.replay()
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                ms = e0.elapsed_time(e1)
+                res[kind] = {"ms_per_iter": round(ms / iters, 5), f"s_for_{iters}_iters": round(ms * 1e-3, 5)}
+                del gph
+            nnz = sum(L.col_idx.numel() for L in layers)
+            dense_macs = sum(Wd.numel() for Wd in dense_w)
+            res["sparse"]["GFLOP/s"] = round(3 * 2 * nnz * T / (res["sparse"]["ms_per_iter"] * 1e-3) / 1e9, 1)
+            res["dense_cublas"]["GFLOP/s"] = round(3 * 2 * dense_macs * T /
+                                                   (res["dense_cublas"]["ms_per_iter"] * 1e-3) / 1e9, 1)
+            res["speedup_vs_dense"] = round(res["dense_cublas"]["ms_per_iter"] / res["sparse"]["ms_per_iter"], 3)
+            res["layers"] = [{"out": L.out_features, "in": L.in_features, "nnz": int(L.col_idx.numel()),
+                              "density": round(L.col_idx.numel() / (L.out_features * L.in_features), 4)}
+                             for L in layers]
+            res["block"] = wl.FLY_MLPS[mlp]["block"]
+            res["tokens"] = T
+            out[mlp] = res
+            del layers, dense_w, X, dY, vals, vt
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
     return out
 
 
@@ -642,8 +797,7 @@ class OracleStep:
             o.csr_add(self.ro, self.col, self.vals, d["W"], rows=r)
 
 
-def cpu_baseline(w, acc, seconds: float):
-    st = OracleStep(w, acc, target_gflop=2.0)
+def _time_oracle(st, seconds):
     st()
     n, t0 = 0, time.perf_counter()
     while True:
@@ -651,17 +805,35 @@ def cpu_baseline(w, acc, seconds: float):
         n += 1
         if time.perf_counter() - t0 >= seconds:
             break
-    dt = (time.perf_counter() - t0) / n
-    return {"value": round(st.flops / dt / 1e9, 3), "unit": "GFLOP/s", "cores": st.o.num_threads(), "kind": "oracle",
-            "sample": f"{st.sample}; {n} step(s) of sort_rows+spmm+sddmm+csr_add in fp64",
-            "ms_per_step": round(dt * 1e3, 2)}
+    return (time.perf_counter() - t0) / n, n
+
+
+def cpu_baseline(w, acc, seconds: float, single_thread: bool = False):
+    """The oracle as it stands on the host cores (all of them, and one when single_thread)
+    on a bounded sample of the workload (about 2 GFLOP per step)."""
+    st = OracleStep(w, acc, target_gflop=2.0)
+    dt, n = _time_oracle(st, seconds)
+    out = {"value": round(st.flops / dt / 1e9, 3), "unit": "GFLOP/s", "cores": st.o.num_threads(), "kind": "oracle",
+           "sample": f"{st.sample}; {n} step(s) of sort_rows+spmm+sddmm+csr_add in fp64",
+           "ms_per_step": round(dt * 1e3, 2)}
+    if single_thread:
+        threads = st.o.num_threads()
+        st.o.set_threads(1)
+        try:
+            dt1, n1 = _time_oracle(st, seconds)
+        finally:
+            st.o.set_threads(threads)
+        out["single_thread"] = {"value": round(st.flops / dt1 / 1e9, 3), "cores": 1, "steps": n1,
+                                "ms_per_step": round(dt1 * 1e3, 2)}
+    return out
 
 
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return
-    w = wl.generate(args.workload)
+    name = headline_name(args)
+    w = wl.generate(name)
     acc = accounting(w)
     st = OracleStep(w, acc, target_gflop=2.0)
     for _ in range(min(args.warmup, 1)):
@@ -675,7 +847,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": ws, "steps": steps,
             "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; workload recipes in DESIGN.md)",
-            "config": {"workload": DESCRIPTION[args.workload], "m": w.m, "n": w.n, "nnz": w.nnz},
+            "config": config_dict(name, w, args),
             "cpu_baseline": {"value": value, "unit": "GFLOP/s", "cores": st.o.num_threads(), "kind": "oracle",
                              "sample": f"{st.sample}, {steps} step(s)"},
             "e2e": {"value": value, "unit": "GFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -688,10 +860,11 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="rosa", choices=list(wl.SPECS))
+    ap.add_argument("--workload", default="all", choices=["all"] + list(wl.SPECS),
+                    help="all: every configuration, headline on the butterfly layer")
     ap.add_argument("--sddmm-backend", default="structure_aware", choices=["structure_aware", "general"])
     ap.add_argument("--spmm-path", default="auto", choices=["auto", "general"])
-    ap.add_argument("--cpu-seconds", type=float, default=8.0)
+    ap.add_argument("--cpu-seconds", type=float, default=3.0)
     ap.add_argument("--breakdown-steps", type=int, default=200)
     ap.add_argument("--ref-max-steps", type=int, default=20)
     ap.add_argument("--no-next-ops", action="store_true", help="skip timing csr_transpose / dB / masked Adam")

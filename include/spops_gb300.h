@@ -129,6 +129,9 @@ SPOPS_API int spops_sort_rows(const int32_t* row_offsets, int32_t m, int32_t nnz
 SPOPS_API int spops_sort_rows_static(const int32_t* row_offsets, int32_t m, int32_t nnz, void* row_idx_out,
                                      int itype, void* stream);
 SPOPS_API int32_t spops_sort_rows_static_max_rows(void);
+/* (The array's device address is looked up once per device and kept for the life of the
+ * process, so it does not survive cudaDeviceReset: do not use the library again in that
+ * process after a reset.) */
 
 /* bins_out[0..4) (device int32) = {0, #rows with nnz >= t_long, #rows with nnz >= 1, m}:
  * prefix offsets that split a sorted row_idx into long, short and empty rows. The counts
@@ -275,8 +278,22 @@ SPOPS_API int spops_check_csr(const int32_t* row_offsets, const void* col_idx, c
                     int32_t n, int32_t nnz, void* workspace, size_t ws_bytes, void* stream);
 
 /* Synchronize `stream`, then return in *code_out the first device error recorded on the
- * current device since the last call (SPOPS_DEV_*), and clear it. */
+ * current device since the last call (SPOPS_DEV_*), and clear it. The error word's device
+ * address is looked up once per device and kept for the life of the process: after
+ * cudaDeviceReset this library must not be used again in that process. */
 SPOPS_API int spops_get_device_error(void* stream, int32_t* code_out);
+
+/* Self-test of failure detection. Every wait of the library's TMA and tensor-core kernels
+ * on an asynchronous copy or an MMA gives up after a time limit (2 s), records
+ * SPOPS_DEV_MBAR_TIMEOUT in the device error word and lets its kernel return, so a copy
+ * that never completes cannot hang the GPU. This call queues one kernel whose single
+ * thread waits on a shared-memory barrier that nothing ever arrives on (no copy, TMA load
+ * or MMA is in flight) with the limit limit_ns, in [1e3, 1e9] nanoseconds; the wait gives
+ * up and records SPOPS_DEV_MBAR_TIMEOUT. waited_ns (device pointer to one uint64, 8-byte
+ * aligned, may be NULL) receives the nanoseconds the wait lasted (%globaltimer). Read and
+ * clear the code with spops_get_device_error; the context stays usable. The pages have no
+ * counterpart of this call. */
+SPOPS_API int spops_selftest_wait_timeout(int64_t limit_ns, uint64_t* waited_ns, void* stream);
 
 #ifdef __cplusplus
 }

@@ -53,6 +53,7 @@ def _load():
             P = ctypes.c_void_p
             i32 = ctypes.c_int32
             lib.oracle_num_threads.restype = ctypes.c_int
+            lib.oracle_set_threads.argtypes = [i32]
             lib.oracle_sort_rows.argtypes = [i32, P, P]
             lib.oracle_row_bins.argtypes = [i32, P, i32, P]
             lib.oracle_spmm.argtypes = [i32, i32, i32, P, P, P, P, P, P, i32]
@@ -84,6 +85,11 @@ def _ptr(a: np.ndarray):
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_threads(n: int) -> None:
+    """Threads of the oracle's parallel loops from now on (results do not depend on it)."""
+    _load().oracle_set_threads(int(n))
 
 
 def sort_rows(row_offsets) -> np.ndarray:

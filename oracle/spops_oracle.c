@@ -55,6 +55,16 @@ int oracle_num_threads(void) {
 #endif
 }
 
+/* Threads the parallel loops below use from now on (timing only; results do not depend on
+ * it: each output row is computed by one thread in a fixed order). */
+void oracle_set_threads(int32_t n) {
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* ------------------------------------------------------------------ row permutation */
 
 static int cmp_i64(const void* a, const void* b) {

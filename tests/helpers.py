@@ -58,6 +58,55 @@ def assert_close(got: torch.Tensor, want64: np.ndarray, fmt: str, what: str):
     return err
 
 
+# Element-wise bound on fp32 accumulation (any order, any split into partial sums, tensor
+# cores included): each of the `terms` additions of a result is off by at most one fp32 ulp
+# of a partial sum, and every partial sum is at most sum |a_t b_t| in magnitude, so
+#     |acc - exact| <= 2^-23 * terms * sum_t |a_t b_t|;
+# rounding acc to the output dtype then adds half an ulp of the dtype at |acc|.
+ACC_UNIT = 2.0 ** -23
+_FMT_BITS = {"f32": (23, -126), "f16": (10, -14), "bf16": (7, -126)}  # mantissa bits, min normal exponent
+
+
+def ulp(x: np.ndarray, fmt: str) -> np.ndarray:
+    """Spacing of the dtype's representable numbers at |x| (subnormal spacing below the
+    smallest normal)."""
+    p, emin = _FMT_BITS[fmt]
+    x = np.abs(np.asarray(x, dtype=np.float64))
+    _, e2 = np.frexp(x)                      # x = f * 2^e2, f in [0.5, 1)
+    e = np.maximum(e2 - 1, emin)
+    return np.ldexp(1.0, e - p)
+
+
+def assert_elementwise(got: torch.Tensor, want64: np.ndarray, absdot64: np.ndarray, terms, fmt: str, what: str):
+    """Every element within 2^-23 * terms * sum|a b| + 1/2 ulp_fmt of the oracle's fp64 value.
+    absdot64: the oracle run on |values| and |operands| (same shape as want64); terms: the
+    number of products summed per element (scalar or broadcastable to want64)."""
+    g = as_f64(got)
+    assert g.shape == want64.shape == absdot64.shape, (what, g.shape, want64.shape, absdot64.shape)
+    assert np.all(np.isfinite(g)), f"{what}: non-finite output"
+    acc_err = ACC_UNIT * np.asarray(terms, dtype=np.float64) * absdot64
+    bound = acc_err + 0.5 * ulp(np.abs(want64) + acc_err, fmt)
+    diff = np.abs(g - want64)
+    bad = diff > bound
+    if bad.any():
+        i = np.unravel_index(int(np.argmax(diff - bound)), diff.shape)
+        raise AssertionError(f"{what}: {int(bad.sum())} of {diff.size} elements outside the fp32-accumulation bound; "
+                             f"worst at {tuple(int(x) for x in i)}: got {g[i]!r} want {want64[i]!r} "
+                             f"bound {bound[i]:.3e}")
+
+
+def spmm_terms(row_offsets: np.ndarray, rows=None) -> np.ndarray:
+    """Products summed per SpMM output row (the row's entry count), as a column vector."""
+    lens = np.diff(np.asarray(row_offsets, dtype=np.int64))
+    if rows is not None:
+        lens = lens[np.asarray(rows, dtype=np.int64)]
+    return lens[:, None]
+
+
+def abs_of(t) -> np.ndarray:
+    return np.abs(as_f64(t) if isinstance(t, torch.Tensor) else np.asarray(t, dtype=np.float64))
+
+
 def assert_bits_equal(got: torch.Tensor, want64: np.ndarray, fmt: str, what: str):
     """Bit-for-bit equality with the oracle's fp64 result rounded to the dtype."""
     want = torch.from_numpy(oracle.round_to(want64, fmt)).to(got.dtype)

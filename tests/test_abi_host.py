@@ -89,6 +89,10 @@ def test_bad_arguments_rejected_on_host(lib):
     assert lib.spops_plan_build(FAKE, FAKE, FAKE, 0, 10, 10, 5, P(0x40000), 64, None) == 3
     assert lib.spops_row_bins(FAKE, 10, 0, FAKE, None) == 1
     assert lib.spops_get_device_error(None, None) == 1
+    # the wait self-test: limits outside [1 us, 1 s], misaligned output
+    assert lib.spops_selftest_wait_timeout(999, None, None) == 1
+    assert lib.spops_selftest_wait_timeout(1_000_000_001, None, None) == 1
+    assert lib.spops_selftest_wait_timeout(5_000_000, P(0x10004), None) == 1
 
 
 def test_plan_size_grows_with_the_mask(lib):

@@ -64,11 +64,16 @@ def test_recorded_traffic_follows_the_source_hash(tmp_path, monkeypatch):
     (tmp_path / "profiles" / "traffic.md").write_text(
         "| workload | op | sources | sha256[:16] | bytes |\n|---|---|---|---|---|\n"
         f"| rosa | spmm | k.cu | {h} | 12345 |\n")
-    assert bench.recorded_traffic("spmm", "rosa") == 12345
+    assert bench.recorded_traffic("spmm", "rosa") == {"bytes": 12345, "read": None, "write": None}
     assert bench.recorded_traffic("sddmm", "rosa") is None
     assert bench.recorded_traffic("spmm", "llama_mlp") is None
+    # rows with read and write columns
+    (tmp_path / "profiles" / "traffic.md").write_text(
+        "| workload | op | sources | sha256[:16] | read | write | bytes |\n|---|---|---|---|---|---|---|\n"
+        f"| butterfly | sddmm | k.cu | {h} | 100 | 20 | 120 |\n")
+    assert bench.recorded_traffic("sddmm", "butterfly") == {"bytes": 120, "read": 100, "write": 20}
     src.write_text("__global__ void k() { /* changed */ }\n")
-    assert bench.recorded_traffic("spmm", "rosa") is None
+    assert bench.recorded_traffic("sddmm", "butterfly") is None
 
 
 def test_committed_traffic_table_parses():
@@ -76,8 +81,30 @@ def test_committed_traffic_table_parses():
     rows = [ln for ln in open(os.path.join(ROOT, "profiles", "traffic.md")) if "/csrc/" in ln]
     assert rows
     for ln in rows:
-        wk, op, srcs, h, nbytes = [p.strip() for p in ln.strip().strip("|").split("|")]
+        cells = [p.strip() for p in ln.strip().strip("|").split("|")]
+        assert len(cells) in (5, 7), ln
+        wk, op, srcs, h = cells[:4]
         assert wk in wl.SPECS and op in ("sort_rows", "plan", "spmm", "sddmm", "csr_add")
-        assert len(h) == 16 and int(nbytes) > 0
+        assert len(h) == 16 and int(cells[-1]) > 0
+        if len(cells) == 7:
+            assert int(cells[4]) + int(cells[5]) == int(cells[6])
         for p in srcs.split("+"):
             assert os.path.exists(os.path.join(ROOT, p)), p
+
+
+def test_reference_arm_config_matches_the_gpu_arm():
+    """The reference arm's config object is the one the GPU arm prints for its headline
+    workload (both come from bench.config_dict), and the default run's headline is the
+    butterfly layer, the largest configuration."""
+    import argparse
+    args = argparse.Namespace(workload="all", sddmm_backend="structure_aware", spmm_path="auto")
+    assert bench.headline_name(args) == "butterfly"
+    assert bench.workload_list(args)[:5] == wl.CONFIG_ORDER
+    w = wl.generate("tiny")
+    cfg = bench.config_dict("tiny", w, args)
+    assert cfg["workload"] == bench.DESCRIPTION["tiny"] and cfg["N"] == 64 and cfg["kd"] == 64
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "tiny",
+                          "--steps", "1", "--warmup", "1"], capture_output=True, text=True, timeout=600, cwd=ROOT,
+                         env={**os.environ, "CUDA_VISIBLE_DEVICES": ""})
+    assert out.returncode == 0, out.stderr[-2000:]
+    assert json.loads(out.stdout.strip().splitlines()[-1])["config"] == cfg

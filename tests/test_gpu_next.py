@@ -6,7 +6,8 @@ import torch
 
 import oracle
 import workloads as wl
-from helpers import TOL, as_f64, assert_bits_equal, assert_close, index_dtype
+from helpers import (TOL, abs_of, as_f64, assert_bits_equal, assert_close, assert_elementwise, index_dtype,
+                     spmm_terms)
 
 pytestmark = pytest.mark.gpu
 
@@ -108,19 +109,20 @@ def test_spmm_grad_b_integer_exact_and_reused_transpose():
     assert_bits_equal(dB, want, "f32", "integer dB")
 
 
-def test_spmm_grad_b_full_size_rosa_sampled():
-    """The RoSA adapter at full size (4096 x 4096, 1 % clustered, fp16, 2048 tokens):
-    dB rows sampled against the oracle's transpose + SpMM."""
+def test_spmm_grad_b_full_size_rosa():
+    """The RoSA adapter at full size (4096 x 4096, 1 % clustered, fp16, 2048 tokens): every
+    element of dB against the oracle's transpose + SpMM, by the Frobenius tolerance and the
+    element-wise fp32-accumulation bound."""
     w = wl.generate("rosa", operands=())
     rng = np.random.default_rng(9)
     dC = torch.from_numpy(rng.standard_normal((w.m, 2048))).to(torch.float16)
     dB = sp.spmm_grad_b(w.values.to(DEV), w.row_offsets.to(DEV), w.col_idx.to(torch.int16).to(DEV), dC.to(DEV), w.n)
     torch.cuda.synchronize()
     ro_t, row_t, val_t, _ = oracle.csr_transpose(w.row_offsets.numpy(), w.col_idx.numpy(), w.values, w.n)
-    lens = np.diff(ro_t)
-    rows = np.unique(np.concatenate([np.argsort(-lens)[:24], rng.choice(w.n, 40, replace=False)]))
-    want = oracle.spmm(ro_t, row_t, val_t, dC, rows=rows)
-    assert_close(dB[torch.from_numpy(rows).to(DEV)], want, "f16", "full-size dB rows")
+    want = oracle.spmm(ro_t, row_t, val_t, dC)
+    absdot = oracle.spmm(ro_t, row_t, np.abs(val_t), abs_of(dC))
+    assert_close(dB, want, "f16", "full-size dB")
+    assert_elementwise(dB, want, absdot, spmm_terms(ro_t), "f16", "full-size dB")
 
 
 def test_transpose_full_size_zipf():
@@ -271,16 +273,20 @@ def test_spmm_narrow_integer_exact_unaligned_b_and_empty_rows():
     assert torch.equal(C.cpu(), expect)
 
 
-def test_spmm_narrow_full_size_sampled():
-    """The 8192 x 8192, 90 %-sparse, N = 8 workload: sampled rows against the oracle."""
+def test_spmm_narrow_full_size():
+    """The 8192 x 8192, 90 %-sparse, N = 8 workload and its SpMV column (N = 1): every
+    element against the oracle."""
     w = wl.generate("spmv")
     ro, col = w.row_offsets.to(DEV), w.col_idx.to(torch.int16).to(DEV)
     row_idx = sp.sort_rows(ro, nnz=w.nnz, index_dtype=torch.int16)
-    C = sp.spmm(w.values.to(DEV), ro, row_idx, col, w.B.to(DEV), w.m)
-    torch.cuda.synchronize()
-    rows = np.random.default_rng(15).choice(w.m, 200, replace=False)
-    want = oracle.spmm(w.row_offsets.numpy(), w.col_idx.numpy(), w.values, w.B, rows=rows)
-    assert_close(C[torch.from_numpy(rows).to(DEV)], want, "f16", "spmv full size")
+    ro_h, col_h = w.row_offsets.numpy(), w.col_idx.numpy()
+    for B in (w.B, w.B[:, :1].contiguous()):
+        C = sp.spmm(w.values.to(DEV), ro, row_idx, col, B.to(DEV), w.m)
+        torch.cuda.synchronize()
+        want = oracle.spmm(ro_h, col_h, w.values, B)
+        absdot = oracle.spmm(ro_h, col_h, abs_of(w.values), abs_of(B))
+        assert_close(C, want, "f16", f"narrow full size N={B.shape[1]}")
+        assert_elementwise(C, want, absdot, spmm_terms(ro_h), "f16", f"narrow full size N={B.shape[1]}")
 
 
 # ---------------------------------------------------------------- sparse linear layer (pixelfly)
@@ -309,3 +315,36 @@ def test_sparse_linear_forward_backward(dtype):
     dense[rows, col] = w.values.double()
     ref = (dense @ w.B.double()).numpy()
     assert_close(Yt.detach(), ref, dtype, "layer forward vs dense fp64")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", [n for mlp in wl.FLY_MLPS for n in wl.fly_layer_names(mlp)])
+def test_pixelfly_mlp_layer_full_size(name):
+    """The layers of the pixelfly issue's two MLPs at their own shapes (block 48: K chunks of
+    the tensor-core panels end inside a block; block 256), 8192 tokens: forward Y^T = W X^T,
+    dW = dY^T X on the mask and dX^T = W^T dY^T through SparseLinear's autograd function,
+    every element against the oracle by the Frobenius tolerance and the element-wise
+    fp32-accumulation bound."""
+    w = wl.generate(name, operands=("B", "A"))
+    layer = sp.SparseLinear(w.row_offsets.to(DEV), w.col_idx.to(torch.int16).to(DEV), w.values.to(DEV).clone(),
+                            in_features=w.n)
+    assert layer.plan.stats()["spmm_panels"] > 0  # the forward runs on the tensor cores
+    Xt = w.B.to(DEV).clone().requires_grad_(True)
+    Yt = layer(Xt)
+    Yt.backward(w.A.to(DEV))
+    torch.cuda.synchronize()
+    ro, col = w.row_offsets.numpy(), w.col_idx.numpy()
+    aval, aX, aG = abs_of(w.values), abs_of(w.B), abs_of(w.A)
+    want = oracle.spmm(ro, col, w.values, w.B)
+    assert_close(Yt.detach(), want, "bf16", f"{name} forward")
+    assert_elementwise(Yt.detach(), want, oracle.spmm(ro, col, aval, aX), spmm_terms(ro), "bf16", f"{name} forward")
+    del want
+    want = oracle.sddmm(ro, col, w.A, w.B)
+    assert_close(layer.values.grad, want, "bf16", f"{name} dW")
+    assert_elementwise(layer.values.grad, want, oracle.sddmm(ro, col, aG, aX), w.A.shape[1], "bf16", f"{name} dW")
+    del want
+    ro_t, row_t, val_t, _ = oracle.csr_transpose(ro, col, w.values, w.n)
+    want = oracle.spmm(ro_t, row_t, val_t, w.A)
+    assert_close(Xt.grad, want, "bf16", f"{name} dX")
+    assert_elementwise(Xt.grad, want, oracle.spmm(ro_t, row_t, np.abs(val_t), aG), spmm_terms(ro_t), "bf16",
+                       f"{name} dX")

@@ -1,6 +1,6 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same seeded
-inputs. Small cases compare every element; the full-size workloads compare sampled rows
-(and every element for csr_add, sort_rows and row_bins)."""
+inputs. Every case compares every element, the five full-size configurations included: by the
+stated relative Frobenius tolerance and by the element-wise bound of fp32 accumulation."""
 import dataclasses
 
 import numpy as np
@@ -9,7 +9,8 @@ import torch
 
 import oracle
 import workloads as wl
-from helpers import TOL, as_f64, assert_bits_equal, assert_close, index_dtype, sample_rows, to_gpu
+from helpers import (TOL, abs_of, as_f64, assert_bits_equal, assert_close, assert_elementwise, index_dtype,
+                     spmm_terms, to_gpu)
 
 pytestmark = pytest.mark.gpu
 
@@ -63,9 +64,15 @@ def test_small_all_elements(small_cases, name, backend):
     out = run_all_ops(w, g, backend)
     ro, col = w.row_offsets.numpy(), w.col_idx.numpy()
     if "spmm" in out:
-        assert_close(out["spmm"], oracle.spmm(ro, col, w.values, w.B), w.dtype, f"{name} spmm")
+        want = oracle.spmm(ro, col, w.values, w.B)
+        assert_close(out["spmm"], want, w.dtype, f"{name} spmm")
+        assert_elementwise(out["spmm"], want, oracle.spmm(ro, col, abs_of(w.values), abs_of(w.B)), spmm_terms(ro),
+                           w.dtype, f"{name} spmm")
     if "sddmm" in out:
-        assert_close(out["sddmm"], oracle.sddmm(ro, col, w.A, w.BT), w.dtype, f"{name} sddmm {backend}")
+        want = oracle.sddmm(ro, col, w.A, w.BT)
+        assert_close(out["sddmm"], want, w.dtype, f"{name} sddmm {backend}")
+        assert_elementwise(out["sddmm"], want, oracle.sddmm(ro, col, abs_of(w.A), abs_of(w.BT)), w.A.shape[1],
+                           w.dtype, f"{name} sddmm {backend}")
     if "csr_add" in out:
         assert_bits_equal(out["csr_add"], oracle.csr_add(ro, col, w.values, w.W), w.dtype, f"{name} csr_add")
 
@@ -285,26 +292,41 @@ def test_check_csr_accepts_valid_and_flags_invalid():
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", wl.CONFIG_ORDER)
-def test_full_size_sampled(name):
+def test_full_size_every_element(name):
+    """Each of the five configurations at full size, every output element: SpMM on the
+    tensor-core path and on the general path, SDDMM on both backends, each against the
+    oracle by the stated relative Frobenius tolerance and by the element-wise bound of fp32
+    accumulation (the oracle run on |values| and |operands| gives sum |a b| per element);
+    csr_add and sort_rows bit for bit."""
     w = wl.generate(name)
     g = to_gpu(w)
     ro, col = w.row_offsets.numpy(), w.col_idx.numpy()
-    dev_ro = g["ro"]
-    assert np.array_equal(sp.sort_rows(dev_ro, index_dtype=g["row_idx"].dtype).cpu().numpy().astype(np.int64),
+    assert np.array_equal(sp.sort_rows(g["ro"], index_dtype=g["row_idx"].dtype).cpu().numpy().astype(np.int64),
                           oracle.sort_rows(ro))
-    rows = sample_rows(ro, 48)
-    out = run_all_ops(w, g)
-    if "spmm" in out:
-        want = oracle.spmm(ro, col, w.values, w.B, rows=rows)
-        assert_close(out["spmm"][torch.from_numpy(rows).cuda()], want, w.dtype, f"{name} spmm rows")
-    if "sddmm" in out:
-        want = oracle.sddmm(ro, col, w.A, w.BT, rows=rows)
-        sel = np.concatenate([np.arange(ro[i], ro[i + 1]) for i in rows])
-        assert_close(out["sddmm"][torch.from_numpy(sel).cuda()], want, w.dtype, f"{name} sddmm rows")
-        gen = sp.sddmm(g["ro"], g["row_idx"], g["col"], g["A"], g["BT"], backend="general")
-        assert_close(gen[torch.from_numpy(sel).cuda()], want, w.dtype, f"{name} sddmm general rows")
-    if "csr_add" in out:
-        assert_bits_equal(out["csr_add"], oracle.csr_add(ro, col, w.values, w.W), w.dtype, f"{name} csr_add")
+    if w.B is not None:
+        want = oracle.spmm(ro, col, w.values, w.B)
+        absdot = oracle.spmm(ro, col, abs_of(w.values), abs_of(w.B))
+        terms = spmm_terms(ro)
+        for path in ("auto", "general"):
+            C = sp.spmm(g["val"], g["ro"], g["row_idx"], g["col"], g["B"], w.m, path=path)
+            torch.cuda.synchronize()
+            assert_close(C, want, w.dtype, f"{name} spmm {path}")
+            assert_elementwise(C, want, absdot, terms, w.dtype, f"{name} spmm {path}")
+            del C
+        del want, absdot
+    if w.A is not None:
+        want = oracle.sddmm(ro, col, w.A, w.BT)
+        absdot = oracle.sddmm(ro, col, abs_of(w.A), abs_of(w.BT))
+        for backend in ("structure_aware", "general"):
+            out = sp.sddmm(g["ro"], g["row_idx"], g["col"], g["A"], g["BT"], backend=backend)
+            torch.cuda.synchronize()
+            assert_close(out, want, w.dtype, f"{name} sddmm {backend}")
+            assert_elementwise(out, want, absdot, w.A.shape[1], w.dtype, f"{name} sddmm {backend}")
+        del want, absdot
+    if w.W is not None:
+        D = sp.csr_add(g["val"], g["ro"], g["row_idx"], g["col"], g["W"])
+        torch.cuda.synchronize()
+        assert_bits_equal(D, oracle.csr_add(ro, col, w.values, w.W), w.dtype, f"{name} csr_add")
 
 
 @pytest.mark.parametrize("case", ["butterfly", "clustered"])
@@ -314,7 +336,7 @@ def test_spmm_many_units_pipeline_exact(case):
     are runs of 64 consecutive columns, loaded as tiles) and a clustered mask (random U
     columns, gathered row by row); 17 or 9 column tiles, the last one 8 columns wide.
     Small-integer inputs make every sum exact, so the result must equal the general row
-    kernel bit for bit on every element, and the oracle on sampled rows."""
+    kernel and the oracle bit for bit on every element."""
     if case == "butterfly":
         s = wl.spec("butterfly", N=2056, kd=64)
     else:
@@ -329,9 +351,7 @@ def test_spmm_many_units_pipeline_exact(case):
     torch.cuda.synchronize()
     assert torch.equal(C.view(torch.int16), ref.view(torch.int16))
     ro, col = w.row_offsets.numpy(), w.col_idx.numpy()
-    rows = sample_rows(ro, 40)
-    want = oracle.spmm(ro, col, w.values, w.B, rows=rows)
-    assert_bits_equal(C[torch.from_numpy(rows).cuda()], want, w.dtype, f"{case} many-units spmm rows")
+    assert_bits_equal(C, oracle.spmm(ro, col, w.values, w.B), w.dtype, f"{case} many-units spmm")
 
 
 @pytest.mark.parametrize("case", ["butterfly", "clustered"])
@@ -340,7 +360,7 @@ def test_sddmm_many_tiles_pipeline_exact(case):
     tiles without a K split, eight warps per CTA: a butterfly mask (192 tiles) and a
     clustered mask with random rows and columns (52 tiles); kd = 136 leaves a partial last
     K chunk. Small-integer inputs make every dot product exact, so every entry must equal
-    the general kernel bit for bit, and the oracle on sampled rows."""
+    the general kernel and the oracle bit for bit."""
     if case == "butterfly":
         s = wl.spec("butterfly", N=64, kd=136)
     else:
@@ -354,10 +374,7 @@ def test_sddmm_many_tiles_pipeline_exact(case):
     torch.cuda.synchronize()
     assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
     ro, col = w.row_offsets.numpy(), w.col_idx.numpy()
-    rows = sample_rows(ro, 40)
-    want = oracle.sddmm(ro, col, w.A, w.BT, rows=rows)
-    sel = np.concatenate([np.arange(ro[i], ro[i + 1]) for i in rows])
-    assert_bits_equal(got[torch.from_numpy(sel).cuda()], want, w.dtype, f"{case} many-tiles sddmm rows")
+    assert_bits_equal(got, oracle.sddmm(ro, col, w.A, w.BT), w.dtype, f"{case} many-tiles sddmm")
 
 
 # ------------------------------------------------------------------ mask plan

@@ -2,8 +2,9 @@
 memory where they need it (a plugin whose host application owns all device memory, or a
 loop that must not call cudaMalloc because it can synchronize the device). Its scratch is
 a static device array inside the library. The test calls it through the C ABI, twice in a
-row on different masks, and checks each result against spops_sort_rows (which takes a
-workspace); index outputs must match bit for bit. This file is collected last."""
+row on different masks large enough to use that array, and checks each result against
+spops_sort_rows (which takes a workspace); index outputs must match bit for bit. This file
+is collected last."""
 import ctypes
 
 import numpy as np
@@ -33,20 +34,29 @@ def _static_sort(lib, ro: torch.Tensor, nnz: int, index_dtype) -> torch.Tensor:
 
 
 def test_static_scratch_sort_matches_workspace_sort_twice_in_a_row(lib):
+    """Both masks have more than 16384 rows, so both calls take the multi-CTA radix sort,
+    whose passes run through the static array (the single-CTA sort of smaller masks keeps
+    its keys in shared memory): an int16 RoSA-like clustered mask of 30000 rows, then an
+    int32 Zipf-banded mask of 20000 rows, queued back to back on one stream before either
+    result is read, so the second call reuses the array the first one left behind."""
     import unstructured_sparse_linear_gb300 as sp
     torch.cuda.set_device(0)
     cases = [
-        (wl.clustered_mask(1, 4096, 4096, 0.01), torch.int16),              # RoSA-adapter mask
-        (wl.zipf_band_mask(3, 20000, 20000, max_len=3000, band=2000), torch.int32),  # wide keys, many ties
+        (wl.clustered_mask(1, 30000, 30000, 0.0005), torch.int16),                    # int16 scatter
+        (wl.zipf_band_mask(3, 20000, 20000, max_len=3000, band=2000), torch.int32),   # wide keys, many ties
     ]
+    got, want = [], []
     for (ro_np, col_np), idx in cases:
         ro = torch.from_numpy(ro_np).cuda()
+        assert ro.numel() - 1 > 16384
         nnz = int(col_np.size)
-        got = _static_sort(lib, ro, nnz, idx)
-        want = sp.sort_rows(ro, nnz=nnz, index_dtype=idx)
-        torch.cuda.synchronize()
-        assert torch.equal(got, want)
-        assert np.array_equal(np.sort(got.cpu().numpy().astype(np.int64)), np.arange(ro.numel() - 1))
+        got.append(_static_sort(lib, ro, nnz, idx))
+    for (ro_np, col_np), idx in cases:
+        want.append(sp.sort_rows(torch.from_numpy(ro_np).cuda(), nnz=int(col_np.size), index_dtype=idx))
+    torch.cuda.synchronize()
+    for g, w_, ((ro_np, _), _) in zip(got, want, cases):
+        assert torch.equal(g, w_)
+        assert np.array_equal(np.sort(g.cpu().numpy().astype(np.int64)), np.arange(ro_np.size - 1))
 
 
 def test_static_scratch_rejects_more_rows_than_it_holds(lib):

@@ -37,6 +37,7 @@ SIGNATURES = {
     "spops_check_csr_workspace_size": (_SZ, [_I32]),
     "spops_check_csr": (_INT, [_P, _P, _P, _INT, _I32, _I32, _I32, _P, _SZ, _P]),
     "spops_get_device_error": (_INT, [_P, ctypes.POINTER(ctypes.c_int32)]),
+    "spops_selftest_wait_timeout": (_INT, [ctypes.c_int64, _P, _P]),
     "spops_csr_transpose_workspace_size": (_SZ, [_I32]),
     "spops_csr_transpose": (_INT, [_P, _P, _P, _INT, _INT, _I32, _I32, _I32, _P, _P, _P, _P, _P, _SZ, _P]),
     "spops_csr_permute_values": (_INT, [_P, _P, _INT, _I32, _P, _P]),

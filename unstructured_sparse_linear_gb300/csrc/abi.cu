@@ -4,6 +4,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "../../include/spops_gb300.h"
 #include "common.cuh"
@@ -21,7 +22,10 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 DeviceProps g_props[kMaxDevices];
+// Device address of g_device_error per device, looked up once with the device current and
+// kept for the life of the process (it does not survive cudaDeviceReset).
 int* g_err_addr[kMaxDevices];
+std::mutex g_err_mutex;
 thread_local char g_last_error[320];
 std::atomic<uint64_t> g_launches{0};
 
@@ -52,6 +56,7 @@ const DeviceProps& device_props() {
 int* device_error_word() {
     const int d = current_device();
     if (d < 0 || d >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_err_mutex);
     if (!g_err_addr[d]) {
         void* addr = nullptr;
         if (cudaGetSymbolAddress(&addr, g_device_error) != cudaSuccess) return nullptr;
@@ -445,6 +450,15 @@ int spops_check_csr(const int32_t* row_offsets, const void* col_idx, const void*
     return cuda_status(launch_check_csr(row_offsets, col_idx, row_idx, itype, m, n, nnz,
                                         static_cast<uint32_t*>(workspace), err, (cudaStream_t)stream),
                        "check_csr launch");
+}
+
+int spops_selftest_wait_timeout(int64_t limit_ns, uint64_t* waited_ns, void* stream) {
+    if (limit_ns < 1000 || limit_ns > 1000000000)
+        return fail(SPOPS_ERR_INVALID_ARG, "limit_ns must lie in [1e3, 1e9] (got %lld)", (long long)limit_ns);
+    if (waited_ns && !aligned(waited_ns, 8)) return fail(SPOPS_ERR_INVALID_ARG, "waited_ns is not 8-byte aligned");
+    return cuda_status(launch_wait_selftest((uint64_t)limit_ns, reinterpret_cast<unsigned long long*>(waited_ns),
+                                            (cudaStream_t)stream),
+                       "wait self-test launch");
 }
 
 int spops_get_device_error(void* stream, int32_t* code_out) {

@@ -142,11 +142,12 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
-// Wait until the mbarrier phase with the given parity completes. Gives up after
-// ~kTimeoutNs of wall time, records kDevErrMbarTimeout and returns false.
+// Wait until the mbarrier phase with the given parity completes. Gives up after about
+// limit_ns of wall time (kMbarTimeoutNs in mbar_wait), records kDevErrMbarTimeout and
+// returns false; the time is read every 256 polls.
 constexpr uint64_t kMbarTimeoutNs = 2000000000ull;  // 2 s
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, int* err, uint64_t limit_ns) {
     uint32_t done = 0;
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
@@ -161,12 +162,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* er
         if ((it & 255u) == 0) {
             uint64_t t = global_timer_ns();
             if (it == 0) t0 = t;
-            else if (t - t0 > kMbarTimeoutNs) {
+            else if (t - t0 > limit_ns) {
                 record_error(err, kDevErrMbarTimeout);
                 return false;
             }
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err) {
+    return mbar_wait_for(bar, parity, err, kMbarTimeoutNs);
 }
 
 // 1-D bulk async copies (TMA engine, no tensor map): global -> shared with mbarrier

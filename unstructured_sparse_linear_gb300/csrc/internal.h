@@ -127,4 +127,9 @@ cudaError_t launch_masked_adam_csr(int gdt, int it, float* param, float* exp_avg
                                    const int32_t* ro, const void* col, int32_t m, int32_t n, int32_t step, double lr,
                                    double beta1, double beta2, double eps, int maximize, cudaStream_t s);
 
+// selftest.cu: one thread waits on an mbarrier nothing arrives on, with a limit of limit_ns;
+// the wait gives up and records kDevErrMbarTimeout. waited_ns (device, may be null) receives
+// the time the wait took.
+cudaError_t launch_wait_selftest(uint64_t limit_ns, unsigned long long* waited_ns, cudaStream_t s);
+
 }  // namespace spops

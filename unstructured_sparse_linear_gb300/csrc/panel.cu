@@ -933,11 +933,12 @@ cudaError_t launch_spmm(int dt, int it, const void* vals, const int32_t* ro, con
     cudaStream_t side = side_fork(s);
     e = dt == kF16 ? run_spmm_panels<__half>(vals, ro, B, k, n, C, w, v, s)
                    : run_spmm_panels<__nv_bfloat16>(vals, ro, B, k, n, C, w, v, s);
-    if (e != cudaSuccess) return e;
-    e = launch_spmm_general(dt, it, vals, ro, row_idx, col, m, k, B, n, C, v.bins_spmm(), v.sp_dense,
-                            side ? side : s);
-    if (e != cudaSuccess) return e;
-    return side ? side_join(s) : cudaSuccess;
+    if (e == cudaSuccess)
+        e = launch_spmm_general(dt, it, vals, ro, row_idx, col, m, k, B, n, C, v.bins_spmm(), v.sp_dense,
+                                side ? side : s);
+    // join on every path, so that s never runs ahead of work queued on the side stream
+    const cudaError_t ej = side ? side_join(s) : cudaSuccess;
+    return e != cudaSuccess ? e : ej;
 }
 
 cudaError_t launch_sddmm(int dt, int it, const int32_t* ro, const void* row_idx, const void* col, int32_t m,
@@ -956,11 +957,11 @@ cudaError_t launch_sddmm(int dt, int it, const int32_t* ro, const void* row_idx,
     cudaStream_t side = side_fork(s);
     e = dt == kF16 ? run_sddmm_panels<__half>(A, BT, out, kd, v, s)
                    : run_sddmm_panels<__nv_bfloat16>(A, BT, out, kd, v, s);
-    if (e != cudaSuccess) return e;
-    e = launch_sddmm_general(dt, it, ro, row_idx, col, m, n, kd, A, BT, out, v.bins_sddmm(), v.dense,
-                             side ? side : s);
-    if (e != cudaSuccess) return e;
-    return side ? side_join(s) : cudaSuccess;
+    if (e == cudaSuccess)
+        e = launch_sddmm_general(dt, it, ro, row_idx, col, m, n, kd, A, BT, out, v.bins_sddmm(), v.dense,
+                                 side ? side : s);
+    const cudaError_t ej = side ? side_join(s) : cudaSuccess;
+    return e != cudaSuccess ? e : ej;
 }
 
 }  // namespace spops

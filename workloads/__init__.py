@@ -210,6 +210,30 @@ SPECS = {
 }
 CONFIG_ORDER = ["tiny", "rosa", "llama_mlp", "zipf", "butterfly"]
 
+# The two MLPs of the HazyResearch/fly issue "Pure torch implementaton of pixelfly" (the T4
+# timing comment): layers (in, out) = [(384, 1536), (1536, 384)] with block size 48 and
+# [(2048, 8192), (8192, 4096)] with block size 256, inputs [16, 512, in], i.e. 8192 tokens.
+# Each layer's weight W (out x in) keeps the butterfly block pattern of the workload above at
+# the issue's block size: block-row r holds block-columns c = r mod (in / block) and
+# c XOR 2^s for s = 0, 1, 2 (four blocks per block-row). As a workload: m = out, n = in,
+# B = X^T (in x tokens) for the forward product Y^T = W X^T, A = dY^T (out x tokens) and
+# BT (in x tokens) for the weight gradient on the mask; bf16, values N(0, 0.02),
+# activations and gradients N(0, 1).
+FLY_MLPS = {
+    "fly_small": {"layers": ((384, 1536), (1536, 384)), "block": 48, "tokens": 16 * 512},
+    "fly_large": {"layers": ((2048, 8192), (8192, 4096)), "block": 256, "tokens": 16 * 512},
+}
+for _mlp, (_base, _d) in zip(FLY_MLPS, ((6, FLY_MLPS["fly_small"]), (8, FLY_MLPS["fly_large"]))):
+    for _li, (_in, _out) in enumerate(_d["layers"]):
+        SPECS[f"{_mlp}_{_li + 1}"] = Spec(f"{_mlp}_{_li + 1}", _base + _li, "bf16", _out, _in, "butterfly", 0.0,
+                                          ("normal", 0.02), N=_d["tokens"], kd=_d["tokens"], w_sigma=None,
+                                          mask_kw=(("block", _d["block"]),))
+
+
+def fly_layer_names(mlp: str):
+    """Workload names of the MLP's layers, first layer first."""
+    return [f"{mlp}_{i + 1}" for i in range(len(FLY_MLPS[mlp]["layers"]))]
+
 
 def spec(name: str, **over) -> Spec:
     """A named spec, optionally with fields replaced (for scaled-down parity cases)."""
