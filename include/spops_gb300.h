@@ -31,6 +31,7 @@
  *   - The library allocates no device memory. Calls that need scratch take a caller
  *     `workspace` of at least the size the matching *_workspace_size function returns,
  *     16-byte aligned; it may be reused once the call's work on `stream` has finished.
+ *     (Its persistent resources are listed above spops_release_streams.)
  *   - Return value: an spops_status. Argument errors are detected on the host before any
  *     work is queued and leave every output untouched. SPOPS_ERR_CUDA reports a failed
  *     launch. spops_last_error() gives a one-line description of the last failure on the
@@ -100,6 +101,18 @@ SPOPS_API const char* spops_version(void);
  * threads). A call captured into a CUDA graph counts once, at capture. */
 SPOPS_API uint64_t spops_kernel_launches(void);
 
+/* Persistent resources. Besides two static device arrays (the 4-byte device error word and
+ * the scratch of spops_sort_rows_static), the only thing the library keeps between calls is,
+ * per calling host thread, up to 8 side streams with two events each: spops_spmm and
+ * spops_sddmm run their general row kernels on a side stream of the caller's stream beside
+ * the tensor-core panels (forked and joined with the events, so both are captured into CUDA
+ * graphs as a fork and a join). They are created on the first such call for a (device,
+ * caller stream) pair, never while that stream is being captured. spops_release_streams
+ * destroys the calling thread's side streams and events (work already queued on them
+ * completes); the next call creates them again. Call it when no capture that uses them is
+ * in progress, e.g. before a thread exits. Returns SPOPS_ERR_CUDA if a destroy call fails. */
+SPOPS_API int spops_release_streams(void);
+
 /* ---------------------------------------------------------------- row scheduler */
 
 /* Scratch bytes spops_sort_rows needs for m rows. */
@@ -154,7 +167,7 @@ SPOPS_API size_t spops_plan_size(int32_t m, int32_t n, int32_t nnz);
  *     that cluster in a few rows and columns): panels of 128 consecutive row_idx
  *     positions; a panel is filled when it has at least 16 non-empty rows and its entries
  *     fill at least a quarter of (non-empty rows) x |U|, U the union of its columns. Filled
- *     panels run SDDMM on the tensor cores when |U| <= 1024 and SpMM when |U| <= 2048
+ *     panels run SDDMM on the tensor cores when |U| <= 1024 and SpMM when |U| <= 4096
  *     (and their SpMM image fits the workspace's budget).
  * plan: device buffer of spops_plan_size bytes, 1024-byte aligned, owned by the caller and
  * left unchanged by the operators. Deterministic: the same mask gives the same plan. */
@@ -162,8 +175,8 @@ SPOPS_API int spops_plan_build(const int32_t* row_offsets, const void* row_idx, 
                                int32_t m, int32_t n, int32_t nnz, void* plan, size_t plan_size, void* stream);
 
 /* stats_out (device int32[16]) = {dense panels, SDDMM tiles, panels with a SpMM image,
- * entries in dense panels, SpMM image elements, panels, 0, 0, SpMM row bins [4], SDDMM
- * row bins [4]} of a built plan. */
+ * entries in dense panels, SpMM image elements, panels, SDDMM tile groups (up to 4
+ * consecutive tiles of a panel), 0, SpMM row bins [4], SDDMM row bins [4]} of a built plan. */
 SPOPS_API int spops_plan_stats(const void* plan, int32_t m, int32_t n, int32_t nnz, int32_t* stats_out, void* stream);
 
 /* ---------------------------------------------------------------- operators */

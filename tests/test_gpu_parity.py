@@ -140,6 +140,19 @@ def test_repeated_calls_are_bitwise_deterministic(small_cases):
         assert torch.equal(a[k].view(torch.int16), b[k].view(torch.int16)), k
 
 
+def test_release_streams_then_calls_recreate_them(small_cases):
+    """The side streams (the library's persistent host-side resources) can be released at
+    any point between calls; the next calls create them again and give identical results."""
+    w = small_cases["rosa_dense"]
+    g = to_gpu(w)
+    a = run_all_ops(w, g)
+    sp.release_streams()
+    sp.release_streams()  # nothing left to release: still fine
+    b = run_all_ops(w, g)
+    for k in a:
+        assert torch.equal(a[k].view(torch.int16), b[k].view(torch.int16)), k
+
+
 # ------------------------------------------------------------------ row scheduler
 
 
@@ -383,9 +396,10 @@ def test_sddmm_many_tiles_pipeline_exact(case):
 def expected_plan(ro, col, row_idx, n):
     """The panel rule restated on the host: 128 consecutive row_idx positions per panel;
     filled when it has at least 16 non-empty rows and entries * 4 >= rows * |U|; SDDMM tiles
-    when also |U| <= 1024, a SpMM image when |U| <= 2048 (images all fit the budget here)."""
+    when also |U| <= 1024 (in groups of up to four tiles), a SpMM image when |U| <= 4096
+    (images all fit the budget here)."""
     m = len(ro) - 1
-    dense = entries = tiles = spmm = 0
+    dense = entries = tiles = spmm = groups = 0
     P = (m + 127) // 128
     for p in range(P):
         rows = row_idx[p * 128:(p + 1) * 128]
@@ -398,11 +412,13 @@ def expected_plan(ro, col, row_idx, n):
             dense += 1
             entries += nnz_p
             tiles += (U + 127) // 128
-        if filled and U <= 2048:
+            groups += ((U + 127) // 128 + 3) // 4
+        if filled and U <= 4096:
             spmm += 1
     lens = np.diff(ro)
     bins = lambda t: [0, int((lens >= t).sum()), int((lens >= 1).sum()), m]  # noqa: E731
     return {"dense_panels": dense, "dense_entries": entries, "sddmm_tiles": tiles, "spmm_panels": spmm, "panels": P,
+            "sddmm_groups": groups,
             "bins_spmm": bins(sp.SPMM_LONG_ROW), "bins_sddmm": bins(sp.SDDMM_LONG_ROW)}
 
 
@@ -415,7 +431,7 @@ def test_plan_matches_rule(small_cases, name):
     want = expected_plan(ro, col, oracle.sort_rows(ro), w.n)
     for k, v in want.items():
         assert got[k] == v, (k, got[k], v)
-    if name == "rosa_wide":  # the SpMM-only panels: |U| between 1024 and 2048
+    if name == "rosa_wide":  # the SpMM-only panels: |U| between 1024 and 4096
         assert got["spmm_panels"] >= 1 and got["dense_panels"] == 0
     elif name != "llama_s":
         assert got["dense_panels"] >= 1  # these cases exercise the tensor-core path

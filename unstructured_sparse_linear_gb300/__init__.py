@@ -23,6 +23,7 @@ import torch
 from . import _lib
 
 __all__ = ["spmm", "sddmm", "csr_add", "sort_rows", "row_bins", "check_csr", "plan_build", "Plan", "SpopsError", "library_path",
+           "release_streams",
            "SPMM_LONG_ROW", "SDDMM_LONG_ROW"]
 
 SPMM_LONG_ROW = 256
@@ -92,6 +93,12 @@ def _ws(nbytes: int, device):
     return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
 
 
+def release_streams() -> None:
+    """Destroy the calling thread's side streams and events (the library's only persistent
+    host-side resources); later calls create them again."""
+    _check(_L().spops_release_streams(), "release_streams")
+
+
 def sort_rows(row_offsets: torch.Tensor, nnz: int | None = None, index_dtype=torch.int16) -> torch.Tensor:
     """row_idx: the rows ordered by nnz descending, ties by ascending row id."""
     _req(row_offsets, "row_offsets", torch.int32)
@@ -134,7 +141,8 @@ class Plan:
             _check(_L().spops_plan_stats(self.ptr(), self.m, self.n, self.nnz, _p(out), _stream()), "plan_stats")
         s = out.cpu().tolist()
         return {"dense_panels": s[0], "sddmm_tiles": s[1], "spmm_panels": s[2], "dense_entries": s[3],
-                "image_elems": s[4], "panels": s[5], "bins_spmm": s[8:12], "bins_sddmm": s[12:16]}
+                "image_elems": s[4], "panels": s[5], "sddmm_groups": s[6], "bins_spmm": s[8:12],
+                "bins_sddmm": s[12:16]}
 
 
 def plan_build(row_offsets, row_idx, col_idx, n: int) -> Plan:

@@ -21,6 +21,7 @@ SIGNATURES = {
     "spops_last_error": (ctypes.c_char_p, []),
     "spops_version": (ctypes.c_char_p, []),
     "spops_kernel_launches": (ctypes.c_uint64, []),
+    "spops_release_streams": (_INT, []),
     "spops_sort_rows_workspace_size": (_SZ, [_I32]),
     "spops_sort_rows": (_INT, [_P, _I32, _I32, _P, _INT, _P, _SZ, _P]),
     "spops_sort_rows_static": (_INT, [_P, _I32, _I32, _P, _INT, _P]),

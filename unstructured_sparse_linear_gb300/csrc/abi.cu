@@ -127,6 +127,23 @@ cudaStream_t side_fork(cudaStream_t s) {
     return sd->stream;
 }
 
+// Destroy the calling thread's side streams and their events (work already queued on them
+// still runs to completion; the CUDA runtime releases the stream afterwards).
+cudaError_t release_sides() {
+    cudaError_t first = cudaSuccess;
+    for (Side& sd : g_side) {
+        if (!sd.stream) continue;
+        cudaError_t e = cudaEventDestroy(sd.fork);
+        if (first == cudaSuccess) first = e;
+        e = cudaEventDestroy(sd.join);
+        if (first == cudaSuccess) first = e;
+        e = cudaStreamDestroy(sd.stream);
+        if (first == cudaSuccess) first = e;
+        sd = Side{};
+    }
+    return first;
+}
+
 cudaError_t side_join(cudaStream_t s) {
     Side* sd = find_side(current_device(), s);
     if (!sd) return cudaErrorInvalidResourceHandle;
@@ -451,6 +468,8 @@ int spops_check_csr(const int32_t* row_offsets, const void* col_idx, const void*
                                         static_cast<uint32_t*>(workspace), err, (cudaStream_t)stream),
                        "check_csr launch");
 }
+
+int spops_release_streams(void) { return cuda_status(release_sides(), "release side streams"); }
 
 int spops_selftest_wait_timeout(int64_t limit_ns, uint64_t* waited_ns, void* stream) {
     if (limit_ns < 1000 || limit_ns > 1000000000)

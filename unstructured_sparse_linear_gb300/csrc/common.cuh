@@ -124,6 +124,11 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
+// Invalidate an idle mbarrier (every phase consumed, nothing pending) before re-initializing it.
+__device__ __forceinline__ void mbar_inval(uint32_t bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -146,17 +151,21 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 // limit_ns of wall time (kMbarTimeoutNs in mbar_wait), records kDevErrMbarTimeout and
 // returns false; the time is read every 256 polls.
 constexpr uint64_t kMbarTimeoutNs = 2000000000ull;  // 2 s
+constexpr uint32_t kMbarPollNs = 64;                 // suspend-time hint of one poll
 
 __device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, int* err, uint64_t limit_ns) {
     uint32_t done = 0;
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
+        // a short suspend-time hint: the thread re-polls within ~kMbarPollNs instead of staying
+        // suspended for the (longer) system-dependent limit, so a pipeline stage hands over
+        // promptly
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
             "selp.u32 %0, 1, 0, p;\n\t}"
             : "=r"(done)
-            : "r"(bar), "r"(parity)
+            : "r"(bar), "r"(parity), "n"(kMbarPollNs)
             : "memory");
         if (done) return true;
         if ((it & 255u) == 0) {

@@ -34,6 +34,8 @@ void count_launches(int n);
 // be made.
 cudaStream_t side_fork(cudaStream_t s);
 cudaError_t side_join(cudaStream_t s);
+// Destroy the calling thread's side streams and events (spops_release_streams).
+cudaError_t release_sides();
 // Record the calling thread's spops_last_error() text (printf format) and return status.
 int set_last_error(int status, const char* fmt, ...);
 

@@ -299,14 +299,338 @@ sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
     if (warp == 0) tc::tmem_dealloc(tmem, kTileN);
 }
 
+// Grouped SDDMM for masks with many dense tiles: one item is a group of up to kGroupTiles
+// consecutive 128-column tiles of one panel, all accumulated at once in tensor memory
+// (kGroupTiles x 128 = 512 columns), so each 128 x 64 chunk of A rows is loaded once per
+// group instead of once per tile. A stage holds the A chunk and the group's BT chunks
+// (16 KB each); the ring takes as many stages (up to 4) as fit kGrpRing bytes.
+// The K loop is an mbarrier pipeline without CTA-wide barriers: when the panel's rows are
+// 128 consecutive rows of A (and a 64-row half of a tile's U list 64 consecutive rows of
+// BT), the chunk arrives by 2-D TMA boxes (128-byte swizzle, straight into the UMMA K-major
+// layout) issued by lane 0 of several warps (copies issued by one thread are served one
+// after another); otherwise every thread gathers its 16-byte pieces with cp.async. Each
+// thread arrives once per chunk on the stage's full barrier (after its gathers land), TMA
+// issuers adding the boxes' bytes; thread 0 waits for the full stage, issues the MMAs and
+// commits them to the stage's empty barrier, which the producers wait on before refilling
+// it. One CTA per SM. When the items fill less than the grid, K is split over the CTAs of a
+// thread-block cluster and the partial tiles are added in rank order through distributed
+// shared memory, one tile after the other, as in sddmm_panel_kernel.
+constexpr int kGrpThreads = 256;
+constexpr uint32_t kGrpChunk = kPM * kKC * 2;  // one 128 x 64 operand chunk: 16 KB
+constexpr uint32_t kGrpRing = 12 * kGrpChunk;  // 192 KB of stages
+constexpr int kGrpMaxStages = 4;
+constexpr int kGrpProducers = kGrpThreads - 32;  // warps 1.. gather when a chunk is not all TMA boxes
+constexpr uint32_t kGrpSmem = kGrpRing + 1024;
+static_assert(2 * (kPM / 2) * (kTileN + 4) * 4 + (kPM / 2) * (kTileN / 4 + 1) * 4 <= kGrpRing,
+              "grouped SDDMM receive slots (two ranks) fit in the ring");
+
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// 2-D TMA tile load of the box at (x = column, y = row) into shared memory, completing on bar.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kGrpThreads, 1)
+sddmm_group_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restrict__ out, int32_t kd, PlanView v,
+                   uint32_t idesc, int* err, const __grid_constant__ CUtensorMap tmap_a,
+                   const __grid_constant__ CUtensorMap tmap_bt, int use_tma) {
+    constexpr int NT = kGrpThreads;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[kGrpMaxStages], empty_bar[kGrpMaxStages], acc_bar;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ int32_t s_rows[kPM];
+    __shared__ int32_t s_u[kGroupTiles * kTileN];
+    __shared__ int32_t s_kb[kPM], s_cnt[kPM];
+    __shared__ uint4 s_mask[kPM];
+    __shared__ int s_box[1 + 2 * kGroupTiles];  // first row of each TMA box of the item, -1: gather
+    uint8_t* smem = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(smem_raw), 1024));
+    const uint32_t sbase = smem_u32(smem);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_trigger();
+
+    if (warp == 0) tc::tmem_alloc(smem_u32(&tmem_base_sh), kGroupTiles * kTileN);
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = tmem_base_sh;
+    const uint32_t idesc_n256 = idesc + ((uint32_t)((2 * kTileN - kTileN) >> 3) << 17);  // the N field
+    pdl_wait();  // the plan and the operands come from earlier kernels
+
+    const int nitems = v.counts()[kCntGroups];
+    const int csize = (int)cluster_size();
+    const bool split = csize > 1 && nitems * csize <= (int)gridDim.x;  // the same on every CTA
+    const int C = split ? csize : 1;
+    const int crank = split ? (int)cluster_rank() : 0;
+    const int cid = blockIdx.x / C, ncl = gridDim.x / C;
+    const int nkc = (kd + kKC - 1) / kKC;
+    const int per = (nkc + C - 1) / C;
+    const int S_ranks = (nkc + per - 1) / per;  // ranks that own at least one chunk
+    const int kc0 = crank * per;
+    const int nk = crank < S_ranks ? min(nkc, kc0 + per) - kc0 : 0;
+    const int rows_per = (kPM + C - 1) / C;
+    const int r0 = min(kPM, crank * rows_per), r1 = min(kPM, r0 + rows_per);
+
+    constexpr int kTS = kTileN + 4;      // receive slot row stride (floats)
+    constexpr int kMS = kTileN / 4 + 1;  // per-row word stride
+    float* recv = reinterpret_cast<float*>(smem);
+    uint32_t* meta = reinterpret_cast<uint32_t*>(recv + (size_t)C * rows_per * kTS);
+    bool failed = false;
+
+    for (int it = cid; it < nitems; it += ncl) {
+        const int item = v.gitems[it];
+        const int p = item >> 8, grp = item & 255;
+        const int nU = v.desc[p].y;
+        const int t0 = grp * kGroupTiles;
+        const int nt = min(kGroupTiles, (nU + kTileN - 1) / kTileN - t0);  // tiles in this group
+        const uint32_t stage_bytes = (uint32_t)(1 + nt) * kGrpChunk;
+        const int S = min(kGrpMaxStages, (int)(kGrpRing / stage_bytes));
+        if (tid < kPM) s_rows[tid] = v.prow[(size_t)p * kPM + tid];
+        for (int x = tid; x < nt * kTileN; x += NT) {
+            const int u = t0 * kTileN + x;
+            s_u[x] = u < nU ? v.ulist[(size_t)p * kUList + u] : -1;
+        }
+        __syncthreads();
+        // TMA boxes: A when the panel's 128 rows are consecutive rows; each 64-row half of a
+        // tile's BT rows when its 64 U columns are consecutive (U is sorted and distinct)
+        const bool a_run = __syncthreads_and(tid >= kPM || s_rows[tid] == s_rows[0] + tid) != 0;
+        if (tid <= 2 * nt) {
+            int first = -1;
+            if (tid == 0) first = a_run && s_rows[0] >= 0 ? s_rows[0] : -1;
+            else {
+                const int h = tid - 1;  // half h of the group's BT rows: positions 64 h .. 64 h + 63
+                const int lo = s_u[h * 64], hi = s_u[h * 64 + 63];
+                first = lo >= 0 && hi >= 0 && hi - lo == 63 ? lo : -1;
+            }
+            s_box[tid] = use_tma ? first : -1;
+        }
+        __syncthreads();
+
+        // The whole chunk by TMA (every box a run) or the whole chunk by gathers; the stage
+        // barriers are re-armed for the item's producer count (all of them are idle here).
+        bool tma_all = true;
+        for (int b = 0; b <= 2 * nt; ++b) tma_all = tma_all && s_box[b] >= 0;
+        if (tid == 0) {
+            for (int st = 0; st < kGrpMaxStages; ++st) {
+                mbar_inval(smem_u32(&full_bar[st]));
+                mbar_inval(smem_u32(&empty_bar[st]));
+                mbar_init(smem_u32(&full_bar[st]), tma_all ? 1 : kGrpProducers);
+                mbar_init(smem_u32(&empty_bar[st]), 1);  // the MMA commit
+            }
+            mbar_inval(smem_u32(&acc_bar));
+            mbar_init(smem_u32(&acc_bar), 1);
+            fence_mbar_init();
+        }
+        __syncthreads();
+
+        if (nk > 0 && !failed) {
+            if (warp == 0) {
+                // ---- MMA issuer (does nothing else, so the tensor pipe is fed without gaps):
+                // tile pairs as one N = 256 MMA (A read once per 256 columns), an odd last
+                // tile as N = 128
+                if (lane == 0) {
+                    uint32_t full_ph = 0;
+                    for (int j = 0; j < nk; ++j) {
+                        const int st = j % S;
+                        if (!mbar_wait(smem_u32(&full_bar[st]), (full_ph >> st) & 1u, err)) {
+                            failed = true;
+                            break;
+                        }
+                        full_ph ^= 1u << st;
+                        fence_proxy_async_smem();  // gathered data (generic proxy) before the tensor core reads it
+                        tc::fence_after_sync();
+                        const uint32_t sa = sbase + (uint32_t)st * stage_bytes;
+                        for (int i = 0; i < nt; i += 2) {
+                            const uint32_t id = i + 1 < nt ? idesc_n256 : idesc;
+#pragma unroll
+                            for (int kk = 0; kk < kKC / 16; ++kk) {
+                                const uint64_t ad = tc::smem_desc_sw128(sa + kk * 32, 16, 1024);
+                                const uint64_t bd =
+                                    tc::smem_desc_sw128(sa + (uint32_t)(1 + i) * kGrpChunk + kk * 32, 16, 1024);
+                                tc::mma_f16(tmem + (uint32_t)(i * kTileN), ad, bd, id, (j > 0 || kk > 0) ? 1u : 0u);
+                            }
+                        }
+                        tc::mma_commit(smem_u32(&empty_bar[st]));
+                    }
+                    // The producers waited for the empty completions of chunks 0 .. nk - S - 1;
+                    // wait here for the last ones (completion c of a stage's barrier is chunk
+                    // st + c S), so that no arrive is pending on any barrier when the next item
+                    // re-arms them. Then the accumulator barrier, which completes at once.
+                    if (!failed)
+                        for (int j = max(0, nk - S); j < nk; ++j)
+                            if (!mbar_wait(smem_u32(&empty_bar[j % S]), (uint32_t)(j / S) & 1u, err)) failed = true;
+                    tc::mma_commit(smem_u32(&acc_bar));
+                }
+                __syncwarp();
+            } else if (tma_all) {
+                // ---- one producer thread: whole chunks by TMA boxes, coordinates in registers
+                if (tid == 32) {
+                    int by[1 + 2 * kGroupTiles];
+#pragma unroll
+                    for (int b = 0; b <= 2 * kGroupTiles; ++b) by[b] = b <= 2 * nt ? s_box[b] : 0;
+                    uint32_t empty_ph = 0;
+                    for (int j = 0; j < nk; ++j) {
+                        const int st = j % S;
+                        if (j >= S) {  // the stage's previous chunk (j - S) has been consumed
+                            if (!mbar_wait(smem_u32(&empty_bar[st]), (empty_ph >> st) & 1u, err)) {
+                                failed = true;
+                                break;
+                            }
+                            empty_ph ^= 1u << st;
+                        }
+                        const uint32_t sa = sbase + (uint32_t)st * stage_bytes;
+                        const uint32_t fb = smem_u32(&full_bar[st]);
+                        const int k0 = (kc0 + j) * kKC;
+                        mbar_arrive_expect_tx(fb, stage_bytes);
+                        tma_load_2d(sa, &tmap_a, k0, by[0], fb);
+#pragma unroll
+                        for (int h = 0; h < 2 * kGroupTiles; ++h)
+                            if (h < 2 * nt)
+                                tma_load_2d(sa + (uint32_t)(1 + (h >> 1)) * kGrpChunk + (uint32_t)(h & 1) * (kGrpChunk / 2),
+                                            &tmap_bt, k0, by[1 + h], fb);
+                    }
+                }
+            } else {
+                // ---- producer warps 1..7: every 16-byte piece gathered with cp.async; each
+                // thread arrives on the stage's full barrier once its pieces have landed
+                const int pt = tid - 32;
+                uint32_t empty_ph = 0;
+                for (int j = 0; j < nk; ++j) {
+                    const int st = j % S;
+                    if (j >= S) {
+                        if (!mbar_wait(smem_u32(&empty_bar[st]), (empty_ph >> st) & 1u, err)) {
+                            failed = true;
+                            break;
+                        }
+                        empty_ph ^= 1u << st;
+                    }
+                    const uint32_t sa = sbase + (uint32_t)st * stage_bytes;
+                    const int k0 = (kc0 + j) * kKC;
+                    for (int c = pt; c < (1 + nt) * kPM * 8; c += kGrpProducers) {
+                        const int o = c / (kPM * 8), rc = c % (kPM * 8);
+                        const int row = rc >> 3, kch = rc & 7;
+                        const int kk = k0 + kch * 8;
+                        const int r = o == 0 ? s_rows[row] : s_u[(o - 1) * kTileN + row];
+                        const T* base = o == 0 ? A : BT;
+                        const bool ok = r >= 0 && kk < kd;
+                        tc::cp_async16(sa + (uint32_t)o * kGrpChunk + tc::sw128_off(row, kch),
+                                       ok ? (const void*)(base + (int64_t)r * kd + kk) : (const void*)base, ok ? 16 : 0);
+                    }
+                    cp_async_mbar_arrive(smem_u32(&full_bar[st]));
+                }
+            }
+            // the accumulator is final once the MMA issuer's last commit has arrived
+            if (!mbar_wait(smem_u32(&acc_bar), 0, err)) failed = true;
+        }
+        tc::cp_async_wait<0>();
+        failed = __syncthreads_or(failed);
+        tc::fence_after_sync();
+        for (int i = 0; i < nt; ++i) {
+            const int t = t0 + i;
+            // the epilogue's per-row data for tile t
+            if (tid < kPM) {
+                const size_t prow_at = (size_t)p * kPM + tid;
+                const int32_t* ts = v.ts + prow_at * (kTiles + 1);
+                const int32_t kb = ts[t], kn = ts[t + 1];
+                s_kb[tid] = kb;
+                s_cnt[tid] = s_rows[tid] >= 0 ? kn - kb : 0;
+                s_mask[tid] = *reinterpret_cast<const uint4*>(v.tmask + prow_at * (kUCap / 32) + t * (kTileN / 32));
+            }
+            // the ring (and the previous tile's receive slots) is free on every CTA of the
+            // cluster once all have passed this barrier
+            tc::fence_before_sync();
+            if (split) cluster_sync();
+            else __syncthreads();
+            tc::fence_after_sync();
+            if (nk > 0 && !failed) {
+                constexpr int kCols = kTileN * kPM / NT;  // TMEM columns per thread
+                const int row = tid & (kPM - 1), half = tid / kPM;
+                const int owner = row / rows_per;
+                const bool send = s_cnt[row] > 0;
+                const uint32_t dst =
+                    smem_u32(recv + ((size_t)crank * rows_per + (row - owner * rows_per)) * kTS + half * kCols);
+                const uint32_t lane_addr =
+                    tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)(i * kTileN) + half * kCols;
+                const uint32_t rdst = C == 1 ? dst : cluster_map(dst, owner);
+#pragma unroll
+                for (int c = 0; c < kCols / 32; ++c) {
+                    float x[32];
+                    tc::tmem_ld32(lane_addr + c * 32, x);
+                    if (send) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const float4 y = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+                            if (C == 1) st_shared_f4(rdst + (c * 32 + q * 4) * 4, y);
+                            else st_cluster_f4(rdst + (c * 32 + q * 4) * 4, y);
+                        }
+                    }
+                }
+            }
+            if (tid < kPM && tid >= r0 && tid < r1) {
+                const uint4 m = s_mask[tid];
+                const uint32_t w[4] = {m.x, m.y, m.z, m.w};
+                uint32_t run = 0;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint32_t b = (w[c] >> (4 * j)) & 0xFu;
+                        meta[(tid - r0) * kMS + c * 8 + j] = run | (b << 8);
+                        run += __popc(b);
+                    }
+            }
+            tc::fence_before_sync();
+            if (split) cluster_sync();  // every rank's rows have arrived
+            else __syncthreads();
+            if (!failed) {
+#pragma unroll 2
+                for (int r = r0 + warp; r < r1; r += NT / 32) {
+                    if (s_cnt[r] == 0) continue;  // uniform across the warp
+                    const float4* slot = reinterpret_cast<const float4*>(recv + (size_t)(r - r0) * kTS) + lane;
+                    const size_t slot_step = (size_t)rows_per * kTS / 4;
+                    float4 x = slot[0];
+                    for (int q = 1; q < S_ranks; ++q) {
+                        const float4 y = slot[q * slot_step];
+                        x.x += y.x;
+                        x.y += y.y;
+                        x.z += y.z;
+                        x.w += y.w;
+                    }
+                    const uint32_t mt = meta[(r - r0) * kMS + lane];
+                    const uint32_t bits = mt >> 8;
+                    T* o = out + (int64_t)s_kb[r] + (int)(mt & 0xFFu);
+                    const int k1 = bits & 1u, k2 = k1 + ((bits >> 1) & 1u), k3 = k2 + ((bits >> 2) & 1u);
+                    if (bits & 1u) o[0] = Elt<T>::from_f(x.x);
+                    if (bits & 2u) o[k1] = Elt<T>::from_f(x.y);
+                    if (bits & 4u) o[k2] = Elt<T>::from_f(x.z);
+                    if (bits & 8u) o[k3] = Elt<T>::from_f(x.w);
+                }
+            }
+            __syncthreads();  // s_kb / s_cnt / s_mask and the slots are rewritten for the next tile
+        }
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, kGroupTiles * kTileN);
+}
+
 // ------------------------------------------------------------------ SpMM dense panels
 
 // The 16 image rows of one row group: zeros, then the group's values at their U position,
 // written out as whole 128-byte-swizzled K-major rows (16-byte stores).
+constexpr uint32_t kDensifySmem = kGroupRows * kUList * 2;  // the group's rows, 16-bit values
+
 template <typename T>
 __global__ void __launch_bounds__(256) densify_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro,
                                                      T* __restrict__ img_base, PlanView v) {
-    __shared__ __align__(16) T stage[kGroupRows][kUList];
+    extern __shared__ __align__(16) uint8_t densify_smem[];
+    T(*stage)[kUList] = reinterpret_cast<T(*)[kUList]>(densify_smem);
     pdl_trigger();
     pdl_wait();
     const int p = blockIdx.x / kGroups, grp = blockIdx.x % kGroups;
@@ -361,7 +685,7 @@ spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restric
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t mma_bar[kStages];
     __shared__ uint32_t tmem_base_sh;
-    __shared__ int32_t s_u[kUList];
+    __shared__ uint16_t s_u[kUList];  // the panel's U list (columns < 65536); positions >= |U| unused
     uint8_t* smem = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(smem_raw), 1024));
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -391,7 +715,7 @@ spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restric
         const int nk = (nU + kKC - 1) / kKC;
         const T* img = img_base + v.img_slot[p];
         __syncthreads();
-        for (int x = tid; x < nk * kKC; x += NT) s_u[x] = x < nU ? v.ulist[(size_t)p * kUList + x] : -1;
+        for (int x = tid; x < nU; x += NT) s_u[x] = (uint16_t)v.ulist[(size_t)p * kUList + x];
         bulk_wait_read<0>();  // the previous unit's staged C row has been read out of shared memory
         __syncthreads();
 
@@ -409,9 +733,9 @@ spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restric
             for (int q = 0; q < kKC * kPieces / NT; ++q) {
                 const int c = tid + NT * q;
                 const int kk = c / kPieces, nch = c % kPieces;
-                const int u = s_u[j * kKC + kk];
                 const int ncol = n0 + nch * 8;
-                const bool ok = u >= 0 && ncol < N;
+                const bool ok = j * kKC + kk < nU && ncol < N;
+                const int u = ok ? (int)s_u[j * kKC + kk] : 0;
                 const uint32_t off = (uint32_t)(nch >> 3) * (kKC / 8 * 1024) + tc::sw128_off(kk, nch & 7);
                 tc::cp_async16(st + kSpStageA + off, ok ? (const void*)(B + (int64_t)u * N + ncol) : (const void*)B,
                                ok ? 16 : 0);
@@ -536,21 +860,10 @@ constexpr int kWsProdWarps = 4;
 constexpr int kWsProd = kWsProdWarps * 32;
 constexpr int kWsThreads = (kWsEpiWarps + kWsProdWarps + 1) * 32;
 constexpr uint32_t kWsCStage = kPM * kSpCRowBytes;  // staged C half rows (128 columns)
-constexpr uint32_t kWsUList = kUList * 4;           // one producer warp's copy of a U list
+constexpr uint32_t kWsUList = kUList * 2;           // one producer warp's copy of a U list (16-bit columns)
 constexpr uint32_t kWsSmem = kWsStages * kWsStageBytes + kWsCStage + kWsProdWarps * kWsUList + 1024;
 static_assert(kWsSmem <= 227 * 1024, "warp-specialized SpMM shared memory");
 
-__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-// 2-D TMA tile load of the box at (x = column, y = row) into shared memory, completing on bar.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-}
 
 template <typename T>
 __global__ void __launch_bounds__(kWsThreads, 1)
@@ -568,7 +881,8 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
     if (warp == kWsEpiWarps + kWsProdWarps) tc::tmem_alloc(smem_u32(&tmem_base_sh), 2 * kWsNT);
     if (tid == 0) {
         for (int i = 0; i < kWsStages; ++i) {
-            mbar_init(smem_u32(&full_bar[i]), kWsProd + 1);  // producer threads' cp.async + the bulk copy's arrive
+            // every producer thread once (cp.async or plain arrive) + one expect-tx arrive per producer warp
+            mbar_init(smem_u32(&full_bar[i]), kWsProd + kWsProdWarps);
             mbar_init(smem_u32(&empty_bar[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -642,7 +956,7 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
         // ---------------- producers
         const int pw = warp - kWsEpiWarps;
         const int pt = tid - kWsEpiWarps * 32;  // 0 .. kWsProd - 1
-        int32_t* s_u = reinterpret_cast<int32_t*>(smem + kWsStages * kWsStageBytes + kWsCStage + pw * kWsUList);
+        uint16_t* s_u = reinterpret_cast<uint16_t*>(smem + kWsStages * kWsStageBytes + kWsCStage + pw * kWsUList);
         constexpr int kPieces = kWsNT / 8;      // 16-byte pieces per B row of the tile
         constexpr int kRowsPer = kKC * kPieces / kWsProd;
         static_assert(kWsProd % kPieces == 0, "a producer thread keeps one piece column");
@@ -661,7 +975,7 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
                 img = img_base + v.img_slot[p];
                 const int32_t* ul = v.ulist + (size_t)p * kUList;
                 __syncwarp();  // the previous panel's copy has been read by the whole warp
-                for (int x = lane; x < nk * kKC; x += 32) s_u[x] = x < nU ? ul[x] : -1;
+                for (int x = lane; x < nU; x += 32) s_u[x] = (uint16_t)ul[x];
                 __syncwarp();
             }
             const int ncol = (int)(unit % ntn) * kWsNT + nch * 8;
@@ -675,28 +989,32 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
                 const uint32_t sa = sbase + st * kWsStageBytes;
                 const uint32_t fb = smem_u32(&full_bar[st]);
                 // U is sorted and distinct, so 64 positions spanning 63 columns are consecutive
-                const int u0 = s_u[j * kKC];
-                if (use_tma && j * kKC + kKC - 1 < nU && s_u[j * kKC + kKC - 1] - u0 == kKC - 1) {
-                    if (pt == 0) {
-                        mbar_arrive_expect_tx(fb, kWsStageBytes);
-                        bulk_g2s(sa, img + (size_t)j * kPM * kKC, kSpStageA, fb);
+                const int u0 = s_u[j * kKC];  // j * kKC < nU: every chunk holds at least one U position
+                // Lane 0 of each producer warp issues a quarter of the image chunk (and, on the
+                // tile path, one of the four B boxes): copies issued by one thread are served
+                // one after another, so four issuing warps move the stage several times faster.
+                const T* img_q = img + (size_t)j * kPM * kKC + (size_t)pw * (kPM * kKC / kWsProdWarps);
+                const uint32_t img_q_bytes = kSpStageA / kWsProdWarps;
+                static_assert(kWsNT / 64 == kWsProdWarps, "one B box per producer warp");
+                if (use_tma && j * kKC + kKC - 1 < nU && (int)s_u[j * kKC + kKC - 1] - u0 == kKC - 1) {
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(fb, img_q_bytes + (kKC / 8) * 1024);
+                        bulk_g2s(sa + pw * img_q_bytes, img_q, img_q_bytes, fb);
                         const int x0 = ncol - nch * 8;  // the tile's first column
-#pragma unroll
-                        for (int bx = 0; bx < kWsNT / 64; ++bx)
-                            tma_load_2d(sa + kSpStageA + bx * (kKC / 8) * 1024, &tmap_b, x0 + 64 * bx, u0, fb);
+                        tma_load_2d(sa + kSpStageA + pw * (kKC / 8) * 1024, &tmap_b, x0 + 64 * pw, u0, fb);
                     }
                     mbar_arrive(fb);  // every producer thread arrives once per chunk on either path
                     continue;
                 }
-                if (pt == 0) {
-                    mbar_arrive_expect_tx(fb, kSpStageA);
-                    bulk_g2s(sa, img + (size_t)j * kPM * kKC, kSpStageA, fb);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(fb, img_q_bytes);
+                    bulk_g2s(sa + pw * img_q_bytes, img_q, img_q_bytes, fb);
                 }
 #pragma unroll
                 for (int q = 0; q < kRowsPer; ++q) {
                     const int kk = pt / kPieces + (kWsProd / kPieces) * q;
-                    const int u = s_u[j * kKC + kk];
-                    const bool in = u >= 0 && ncol < N;
+                    const bool in = j * kKC + kk < nU && ncol < N;
+                    const int u = in ? (int)s_u[j * kKC + kk] : 0;
                     const uint32_t off = (uint32_t)(nch >> 3) * (kKC / 8 * 1024) + tc::sw128_off(kk, nch & 7);
                     tc::cp_async16(sa + kSpStageA + off, in ? (const void*)(B + (int64_t)u * N + ncol) : (const void*)B,
                                    in ? 16 : 0);
@@ -765,61 +1083,10 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
 
 // ------------------------------------------------------------------ host dispatch
 
-template <typename T>
-cudaError_t run_sddmm_panels(const void* A, const void* BT, void* out, int32_t kd, const PlanView& v, cudaStream_t s) {
-    // Many possible tiles (more than one per CTA): 8 warps per CTA keep more gathers in
-    // flight; otherwise 4 warps, which share the SMs better with concurrent operators.
-    const bool wide = (int64_t)v.P * kTiles >= (int64_t)device_props().sm_count * 2;
-    auto kern = wide ? sddmm_panel_kernel<T, 256> : sddmm_panel_kernel<T, 128>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSdSmem);
-    if (e != cudaSuccess) return e;
-    // Largest shared-memory carveout, so that two CTAs fit on an SM (also when placing clusters).
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return e;
-    const uint32_t idesc = tc::instr_desc_f16(std::is_same<T, __nv_bfloat16>::value ? 1u : 0u, 0, 0, kPM, kTileN);
-    const int64_t max_items = (int64_t)v.P * kTiles;
-    const int nkc = (kd + kKC - 1) / kKC;
-    int C = nkc < kMaxCluster ? nkc : kMaxCluster;
-
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cfg.blockDim = dim3(wide ? 256 : 128);
-    cfg.dynamicSmemBytes = kSdSmem;
-    cfg.stream = s;
-    int64_t nclusters = min64((int64_t)device_props().sm_count * 2, max_items);
-    if (C > 1) {
-        attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = (unsigned)C;
-        attr[1].val.clusterDim.y = 1;
-        attr[1].val.clusterDim.z = 1;
-        cfg.numAttrs = 2;
-        cfg.gridDim = dim3((unsigned)(C * ((device_props().sm_count * 2) / C)));
-        int active = 0;
-        e = cudaOccupancyMaxActiveClusters(&active, kern, &cfg);
-        if (e != cudaSuccess) return e;
-        if (active > 0) {
-            // Clusters beyond the co-resident count wait for a free slot; none waits on another.
-            nclusters = min64((int64_t)(device_props().sm_count * 2) / C, max_items);
-        } else {
-            C = 1;  // the cluster does not fit: one CTA per tile, no K split
-            cfg.numAttrs = 1;
-        }
-    }
-    cfg.gridDim = dim3((unsigned)(nclusters * C));
-    e = cudaLaunchKernelEx(&cfg, kern, static_cast<const T*>(A), static_cast<const T*>(BT), static_cast<T*>(out), kd, v,
-                           idesc, device_error_word());
-    count_launches(1);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
-}
-
-// Tensor map of a row-major K x N matrix of 16-bit elements for 64 x 64 boxes with the
-// 128-byte swizzle (false if the driver entry point is unavailable or rejects it).
-bool encode_rows_map(CUtensorMap* map, const void* base, int32_t K, int32_t N, bool bf16) {
+// Tensor map of a row-major rows x cols matrix of 16-bit elements for boxes of 64 columns x
+// box_rows rows with the 128-byte swizzle (false if the driver entry point is unavailable or
+// rejects it).
+bool encode_rows_map(CUtensorMap* map, const void* base, int32_t rows, int32_t cols, int32_t box_rows, bool bf16) {
     static const PFN_cuTensorMapEncodeTiled_v12000 encode = [] {
         void* f = nullptr;
         cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
@@ -831,10 +1098,11 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int32_t K, int32_t N, b
         }
         return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
     }();
-    if (!encode || K <= 0 || N <= 0 || (reinterpret_cast<uintptr_t>(base) & 15) || ((int64_t)N * 2) % 16) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)K};
-    const cuuint64_t strides[1] = {(cuuint64_t)N * 2};
-    const cuuint32_t box[2] = {64, 64};
+    if (!encode || rows <= 0 || cols <= 0 || (reinterpret_cast<uintptr_t>(base) & 15) || ((int64_t)cols * 2) % 16)
+        return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     const cuuint32_t elem[2] = {1, 1};
     return encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
                   const_cast<void*>(base), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -842,11 +1110,91 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int32_t K, int32_t N, b
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Cluster launch attributes for kern on `grid` CTAs in clusters of C (C = 1: none). Returns
+// the cluster size that can be placed (1 when clusters of C do not fit).
+template <typename K>
+int fit_cluster(K kern, cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int C) {
+    cfg->numAttrs = 1;
+    if (C <= 1) return 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)C;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg->numAttrs = 2;
+    int active = 0;
+    if (cudaOccupancyMaxActiveClusters(&active, kern, cfg) != cudaSuccess || active <= 0) {
+        cudaGetLastError();
+        cfg->numAttrs = 1;
+        return 1;
+    }
+    return C;
+}
+
+template <typename T>
+cudaError_t run_sddmm_panels(const void* A, const void* BT, void* out, int32_t kd, const PlanView& v, cudaStream_t s) {
+    const uint32_t idesc = tc::instr_desc_f16(std::is_same<T, __nv_bfloat16>::value ? 1u : 0u, 0, 0, kPM, kTileN);
+    const int sms = device_props().sm_count;
+    const int nkc = (kd + kKC - 1) / kKC;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.stream = s;
+    // Many possible tiles (at least two per SM): the grouped kernel, one CTA per SM, each
+    // gathering a panel's A rows once for up to four tiles; K split over pairs of CTAs when
+    // the groups do not fill the SMs.
+    if ((int64_t)v.P * kTiles >= (int64_t)sms * 2) {
+        auto kern = sddmm_group_kernel<T>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGrpSmem);
+        if (e != cudaSuccess) return e;
+        cfg.blockDim = dim3(kGrpThreads);
+        cfg.dynamicSmemBytes = kGrpSmem;
+        cfg.gridDim = dim3((unsigned)(sms / 2 * 2));
+        const int C = fit_cluster(kern, &cfg, attr, nkc >= 2 ? 2 : 1);
+        cfg.gridDim = dim3((unsigned)(sms / C * C));
+        CUtensorMap tmap_a, tmap_bt;
+        const bool bf16 = std::is_same<T, __nv_bfloat16>::value;
+        const int use_tma = encode_rows_map(&tmap_a, A, v.m, kd, kPM, bf16) &&
+                                    encode_rows_map(&tmap_bt, BT, v.n, kd, kKC, bf16)
+                                ? 1
+                                : 0;
+        e = cudaLaunchKernelEx(&cfg, kern, static_cast<const T*>(A), static_cast<const T*>(BT), static_cast<T*>(out),
+                               kd, v, idesc, device_error_word(), tmap_a, tmap_bt, use_tma);
+        count_launches(1);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
+    // Few tiles: one tile per item, 4 warps, two CTAs per SM, K split over clusters of up to 8.
+    auto kern = sddmm_panel_kernel<T, 128>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSdSmem);
+    if (e != cudaSuccess) return e;
+    // Largest shared-memory carveout, so that two CTAs fit on an SM (also when placing clusters).
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    const int64_t max_items = (int64_t)v.P * kTiles;
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = kSdSmem;
+    cfg.gridDim = dim3((unsigned)((sms * 2) / min(nkc, kMaxCluster) * min(nkc, kMaxCluster)));
+    const int C = fit_cluster(kern, &cfg, attr, nkc < kMaxCluster ? nkc : kMaxCluster);
+    // Clusters beyond the co-resident count wait for a free slot; none waits on another.
+    const int64_t nclusters = min64((int64_t)(sms * 2) / C, max_items);
+    cfg.gridDim = dim3((unsigned)(nclusters * C));
+    e = cudaLaunchKernelEx(&cfg, kern, static_cast<const T*>(A), static_cast<const T*>(BT), static_cast<T*>(out), kd, v,
+                           idesc, device_error_word());
+    count_launches(1);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t run_spmm_panels(const void* vals, const int32_t* ro, const void* B, int32_t K, int32_t N, void* C,
                             void* img, const PlanView& v, cudaStream_t s) {
-    cudaError_t e = launch_pdl(densify_kernel<T>, v.P * kGroups, 256, 0, s, static_cast<const T*>(vals), ro,
-                               static_cast<T*>(img), v);
+    cudaError_t e = cudaFuncSetAttribute(densify_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDensifySmem);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(densify_kernel<T>, v.P * kGroups, 256, kDensifySmem, s, static_cast<const T*>(vals), ro,
+                   static_cast<T*>(img), v);
     if (e != cudaSuccess) return e;
     const int ntn = (N + kSpNT - 1) / kSpNT;
     const uint32_t idesc_ws = tc::instr_desc_f16(std::is_same<T, __nv_bfloat16>::value ? 1u : 0u, 0, 1, kPM, kWsNT);
@@ -856,7 +1204,7 @@ cudaError_t run_spmm_panels(const void* vals, const int32_t* ro, const void* B, 
         e = cudaFuncSetAttribute(kws, cudaFuncAttributeMaxDynamicSharedMemorySize, kWsSmem);
         if (e != cudaSuccess) return e;
         CUtensorMap tmap;
-        const int use_tma = encode_rows_map(&tmap, B, K, N, std::is_same<T, __nv_bfloat16>::value) ? 1 : 0;
+        const int use_tma = encode_rows_map(&tmap, B, K, N, 64, std::is_same<T, __nv_bfloat16>::value) ? 1 : 0;
         e = launch_pdl(kws, device_props().sm_count, kWsThreads, kWsSmem, s, static_cast<const T*>(B),
                        static_cast<T*>(C), static_cast<const T*>(img), N, v, idesc_ws, device_error_word(), tmap,
                        use_tma);

@@ -15,7 +15,7 @@
 //      position, counts, and a column bitmap per CTA built with shared-memory atomics; after
 //      a cluster barrier, rank 0 ORs the 8 bitmaps through distributed shared memory,
 //      prefix-sums their popcounts, lists U and decides density (SDDMM tiles |U| <= 1024,
-//      SpMM image |U| <= 2048);
+//      SpMM image |U| <= 4096);
 //   2. row groups of dense panels (8 rows per CTA): each entry's position in U and, per row,
 //      the first entry of every 128-column tile of U and a bit mask of the U positions it
 //      holds; one extra CTA sums the panel counts into row bins, lists dense panels and
@@ -251,7 +251,7 @@ __device__ void lists_work(const PlanView& v, int64_t img_budget) {
         if (threadIdx.x < 8) v.counts()[threadIdx.x] = threadIdx.x == kCntPanels ? v.P : 0;
         return;
     }
-    int cd = 0, ct = 0, cs = 0, cn = 0;
+    int cd = 0, ct = 0, cs = 0, cn = 0, cg = 0;
     int64_t ci = 0;
     for (int base = 0; base < v.P; base += blockDim.x) {
         const int p = base + threadIdx.x;
@@ -259,12 +259,15 @@ __device__ void lists_work(const PlanView& v, int64_t img_budget) {
         const int dn = d.x & 1;          // SDDMM tiles
         const int dsp = (d.x >> 1) & 1;  // SpMM image candidate
         const int tiles = dn ? (d.y + kTileN - 1) / kTileN : 0;
+        const int groups = (tiles + kGroupTiles - 1) / kGroupTiles;
         const int img = dsp ? kPM * ((d.y + 63) / 64) * 64 : 0;
         int td, tt, ti, tn;
         const int ed = block_exclusive_scan(dn, sh, &td);
         const int et = block_exclusive_scan(tiles, sh, &tt);
         const int ei = block_exclusive_scan(img, sh, &ti);
         const int en = block_exclusive_scan(dn ? d.z : 0, sh, &tn);
+        int tgr;
+        const int egr = block_exclusive_scan(groups, sh, &tgr);
         (void)ed;
         (void)en;
         // image slots in panel order while they fit the budget
@@ -276,12 +279,14 @@ __device__ void lists_work(const PlanView& v, int64_t img_budget) {
             v.sp_dense[p] = fits ? 1 : 0;
             if (fits) v.dlist_sp[cs + ef] = p;
             for (int j = 0; j < tiles; ++j) v.items[ct + et + j] = (p << 8) | j;
+            for (int j = 0; j < groups; ++j) v.gitems[cg + egr + j] = (p << 8) | j;
         }
         cd += td;
         ct += tt;
         cs += tf;
         cn += tn;
         ci += ti;
+        cg += tgr;
     }
     if (threadIdx.x == 0) {
         int32_t* cnt = v.counts();
@@ -291,7 +296,7 @@ __device__ void lists_work(const PlanView& v, int64_t img_budget) {
         cnt[kCntDenseNnz] = cn;
         cnt[kCntImgElems] = (int32_t)min64(ci, img_budget);
         cnt[kCntPanels] = v.P;
-        cnt[6] = 0;
+        cnt[kCntGroups] = cg;
         cnt[7] = 0;
     }
 }
@@ -409,6 +414,7 @@ PlanLayout plan_layout(int32_t m, int32_t n, int32_t nnz) {
         L.dense = take(P);
         L.sp_dense = take(P);
         L.items = take(P * kTiles * 4);
+        L.gitems = take(P * (kTiles / kGroupTiles) * 4);
         L.dlist_sp = take(P * 4);
         L.img_slot = take(P * 4);
     }
@@ -440,6 +446,7 @@ PlanView plan_view(void* base, int32_t m, int32_t n, int32_t nnz) {
         v.dense = at<uint8_t>(b, L.dense);
         v.sp_dense = at<uint8_t>(b, L.sp_dense);
         v.items = at<int32_t>(b, L.items);
+        v.gitems = at<int32_t>(b, L.gitems);
         v.dlist_sp = at<int32_t>(b, L.dlist_sp);
         v.img_slot = at<int32_t>(b, L.img_slot);
     }

@@ -17,6 +17,8 @@
 //   dense      uint8[P]        panel runs on tensor cores (SDDMM)
 //   sp_dense   uint8[P]        panel has a SpMM image slot (tensor cores for SpMM)
 //   items      int32[P*kTiles] SDDMM work items (panel << 8 | tile)
+//   gitems     int32[P*kTiles/kGroupTiles]  SDDMM work items of the grouped kernel
+//                              (panel << 8 | group of kGroupTiles consecutive tiles)
 //   dlist_sp   int32[P]        panels with an image slot
 //   img_slot   int32[P]        image offset (elements) or -1
 #pragma once
@@ -31,9 +33,10 @@ namespace spops {
 
 constexpr int kPM = kPanelRows;   // rows per panel (UMMA M)
 constexpr int kUCap = 1024;       // most distinct columns of an SDDMM-dense panel (8 tiles of 128)
-constexpr int kUList = 2048;      // most distinct columns of a SpMM-dense panel (the image's K)
+constexpr int kUList = 4096;      // most distinct columns of a SpMM-dense panel (the image's K)
 constexpr int kTileN = 128;       // SDDMM tile width over U (UMMA N)
 constexpr int kTiles = kUCap / kTileN;
+constexpr int kGroupTiles = 4;    // tiles one CTA of the grouped SDDMM kernel keeps in tensor memory
 constexpr int kGroupRows = 8;     // rows per CTA of the U-position and image kernels, one per warp
 constexpr int kGroups = kPM / kGroupRows;
 constexpr int kPlanCluster = 8;   // CTAs per panel (one thread-block cluster) in the row step
@@ -48,6 +51,7 @@ enum PlanCount {
     kCntDenseNnz = 3,   // entries in dense panels
     kCntImgElems = 4,   // image elements assigned
     kCntPanels = 5,
+    kCntGroups = 6,     // SDDMM items of the grouped kernel
 };
 
 struct PlanView {
@@ -64,6 +68,7 @@ struct PlanView {
     uint8_t* dense;
     uint8_t* sp_dense;
     int32_t* items;
+    int32_t* gitems;
     int32_t* dlist_sp;
     int32_t* img_slot;
     int32_t m, n, nnz, P, W;
@@ -74,7 +79,7 @@ struct PlanView {
 };
 
 struct PlanLayout {
-    size_t hdr, pan_part, bm, wbase, desc, prow, ulist, upos, ts, tmask, dense, sp_dense, items, dlist_sp,
+    size_t hdr, pan_part, bm, wbase, desc, prow, ulist, upos, ts, tmask, dense, sp_dense, items, gitems, dlist_sp,
         img_slot;
     size_t total;
 };
