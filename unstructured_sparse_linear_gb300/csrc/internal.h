@@ -102,15 +102,19 @@ cudaError_t launch_check_csr(const int32_t* ro, const void* col, const void* row
 // spmm.cu
 cudaError_t launch_spmm_general(int dt, int it, const void* vals, const int32_t* ro, const void* row_idx,
                                 const void* col, int32_t m, int32_t k, const void* B, int32_t n, void* C,
-                                const int32_t* bins, const uint8_t* skip_panels, cudaStream_t s);
+                                const int32_t* bins, const uint8_t* skip_panels, const int32_t* order,
+                                cudaStream_t s);
 
 // sddmm.cu
 cudaError_t launch_sddmm_general(int dt, int it, const int32_t* ro, const void* row_idx, const void* col, int32_t m,
                                  int32_t n, int32_t kd, const void* A, const void* BT, void* out,
-                                 const int32_t* bins, const uint8_t* skip_panels, cudaStream_t s);
+                                 const int32_t* bins, const uint8_t* skip_panels, const int32_t* order,
+                                 cudaStream_t s);
 
-// Rows are grouped in panels of kPanelRows consecutive row_idx positions; the general
-// kernels skip positions whose panel flag in skip_panels is set (handled on tensor cores).
+// Rows are grouped in panels of kPanelRows consecutive positions of the plan's row order
+// (row_idx, or row_idx refined by column pattern); the general kernels walk the same order
+// (`order`, the plan's row at each position; row_idx when null) and skip positions whose
+// panel flag in skip_panels is set (handled on tensor cores).
 constexpr int kPanelRows = 128;
 
 // transpose.cu

@@ -304,15 +304,19 @@ sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
 // (kGroupTiles x 128 = 512 columns), so each 128 x 64 chunk of A rows is loaded once per
 // group instead of once per tile. A stage holds the A chunk and the group's BT chunks
 // (16 KB each); the ring takes as many stages (up to 4) as fit kGrpRing bytes.
-// The K loop is an mbarrier pipeline without CTA-wide barriers: when the panel's rows are
-// 128 consecutive rows of A (and a 64-row half of a tile's U list 64 consecutive rows of
-// BT), the chunk arrives by 2-D TMA boxes (128-byte swizzle, straight into the UMMA K-major
-// layout) issued by lane 0 of several warps (copies issued by one thread are served one
-// after another); otherwise every thread gathers its 16-byte pieces with cp.async. Each
-// thread arrives once per chunk on the stage's full barrier (after its gathers land), TMA
-// issuers adding the boxes' bytes; thread 0 waits for the full stage, issues the MMAs and
-// commits them to the stage's empty barrier, which the producers wait on before refilling
-// it. One CTA per SM. When the items fill less than the grid, K is split over the CTAs of a
+// Roles: warp 0 lane 0 issues the MMAs and does nothing else (tile pairs as one N = 256
+// MMA, so A is read from shared memory once per 256 columns; an odd last tile as N = 128).
+// While the tensor core runs, shared-memory loads of other warps wait behind its operand
+// reads, so the producers keep the chunk loop free of them. When each 64-row half of the
+// panel is 64 consecutive rows of A and each 64-row half of a tile's U list 64 consecutive
+// rows of BT, one thread (warp 1 lane 0) loads every chunk as 2-D TMA boxes (128-byte
+// swizzle, straight into the UMMA K-major layout) with one expect-tx arrive, from box
+// coordinates held in registers; otherwise warps 1 .. 7 gather every 16-byte piece with
+// cp.async and each thread arrives once its pieces have landed (the stage barriers are
+// re-armed per item for the producer count of its mode). The MMA issuer commits each stage
+// to its empty barrier, which the producers wait on before refilling it, and the item's
+// last MMAs to an accumulator barrier that every thread waits on before the epilogue. One
+// CTA per SM. When the items fill less than the grid, K is split over the CTAs of a
 // thread-block cluster and the partial tiles are added in rank order through distributed
 // shared memory, one tile after the other, as in sddmm_panel_kernel.
 constexpr int kGrpThreads = 256;
@@ -349,7 +353,7 @@ sddmm_group_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
     __shared__ int32_t s_u[kGroupTiles * kTileN];
     __shared__ int32_t s_kb[kPM], s_cnt[kPM];
     __shared__ uint4 s_mask[kPM];
-    __shared__ int s_box[1 + 2 * kGroupTiles];  // first row of each TMA box of the item, -1: gather
+    __shared__ int s_box[2 + 2 * kGroupTiles];  // first row of each 64-row TMA box of the item, -1: gather
     uint8_t* smem = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(smem_raw), 1024));
     const uint32_t sbase = smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -397,14 +401,18 @@ sddmm_group_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
             s_u[x] = u < nU ? v.ulist[(size_t)p * kUList + u] : -1;
         }
         __syncthreads();
-        // TMA boxes: A when the panel's 128 rows are consecutive rows; each 64-row half of a
-        // tile's BT rows when its 64 U columns are consecutive (U is sorted and distinct)
-        const bool a_run = __syncthreads_and(tid >= kPM || s_rows[tid] == s_rows[0] + tid) != 0;
-        if (tid <= 2 * nt) {
+        // 64-row TMA boxes: each half of the panel's A rows when its 64 rows are consecutive
+        // rows of A; each 64-row half of a tile's BT rows when its 64 U columns are consecutive
+        // (U is sorted and distinct)
+        const bool a_lo = __syncthreads_and(tid >= kPM / 2 || s_rows[tid] == s_rows[0] + tid) != 0;
+        const bool a_hi = __syncthreads_and(tid >= kPM / 2 || s_rows[kPM / 2 + tid] == s_rows[kPM / 2] + tid) != 0;
+        if (tid < 2 + 2 * nt) {
             int first = -1;
-            if (tid == 0) first = a_run && s_rows[0] >= 0 ? s_rows[0] : -1;
-            else {
-                const int h = tid - 1;  // half h of the group's BT rows: positions 64 h .. 64 h + 63
+            if (tid < 2) {
+                const int r = s_rows[tid * (kPM / 2)];
+                first = (tid == 0 ? a_lo : a_hi) && r >= 0 ? r : -1;
+            } else {
+                const int h = tid - 2;  // half h of the group's BT rows: positions 64 h .. 64 h + 63
                 const int lo = s_u[h * 64], hi = s_u[h * 64 + 63];
                 first = lo >= 0 && hi >= 0 && hi - lo == 63 ? lo : -1;
             }
@@ -415,7 +423,7 @@ sddmm_group_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
         // The whole chunk by TMA (every box a run) or the whole chunk by gathers; the stage
         // barriers are re-armed for the item's producer count (all of them are idle here).
         bool tma_all = true;
-        for (int b = 0; b <= 2 * nt; ++b) tma_all = tma_all && s_box[b] >= 0;
+        for (int b = 0; b < 2 + 2 * nt; ++b) tma_all = tma_all && s_box[b] >= 0;
         if (tid == 0) {
             for (int st = 0; st < kGrpMaxStages; ++st) {
                 mbar_inval(smem_u32(&full_bar[st]));
@@ -471,9 +479,9 @@ sddmm_group_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
             } else if (tma_all) {
                 // ---- one producer thread: whole chunks by TMA boxes, coordinates in registers
                 if (tid == 32) {
-                    int by[1 + 2 * kGroupTiles];
+                    int by[2 + 2 * kGroupTiles];
 #pragma unroll
-                    for (int b = 0; b <= 2 * kGroupTiles; ++b) by[b] = b <= 2 * nt ? s_box[b] : 0;
+                    for (int b = 0; b < 2 + 2 * kGroupTiles; ++b) by[b] = b < 2 + 2 * nt ? s_box[b] : 0;
                     uint32_t empty_ph = 0;
                     for (int j = 0; j < nk; ++j) {
                         const int st = j % S;
@@ -489,11 +497,12 @@ sddmm_group_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
                         const int k0 = (kc0 + j) * kKC;
                         mbar_arrive_expect_tx(fb, stage_bytes);
                         tma_load_2d(sa, &tmap_a, k0, by[0], fb);
+                        tma_load_2d(sa + kGrpChunk / 2, &tmap_a, k0, by[1], fb);
 #pragma unroll
                         for (int h = 0; h < 2 * kGroupTiles; ++h)
                             if (h < 2 * nt)
                                 tma_load_2d(sa + (uint32_t)(1 + (h >> 1)) * kGrpChunk + (uint32_t)(h & 1) * (kGrpChunk / 2),
-                                            &tmap_bt, k0, by[1 + h], fb);
+                                            &tmap_bt, k0, by[2 + h], fb);
                     }
                 }
             } else {
@@ -528,6 +537,7 @@ sddmm_group_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
             // the accumulator is final once the MMA issuer's last commit has arrived
             if (!mbar_wait(smem_u32(&acc_bar), 0, err)) failed = true;
         }
+        tc::cp_async_commit();  // (gathers are tracked by their mbarrier arrives; none is left in flight)
         tc::cp_async_wait<0>();
         failed = __syncthreads_or(failed);
         tc::fence_after_sync();
@@ -856,8 +866,10 @@ constexpr uint32_t kWsStageB = kKC * kWsNT * 2;                // 32 KB
 constexpr uint32_t kWsStageBytes = kSpStageA + kWsStageB;      // 48 KB
 constexpr int kWsStages = 3;
 constexpr int kWsEpiWarps = 4;
-constexpr int kWsProdWarps = 4;
-constexpr int kWsProd = kWsProdWarps * 32;
+// One producer warp per stage: chunk g goes to stage g mod 3 and warp g mod 3, so a warp only
+// ever waits for the consumption of its own previous chunk (one barrier phase back; a parity
+// wait cannot alias a phase two completions behind).
+constexpr int kWsProdWarps = kWsStages;
 constexpr int kWsThreads = (kWsEpiWarps + kWsProdWarps + 1) * 32;
 constexpr uint32_t kWsCStage = kPM * kSpCRowBytes;  // staged C half rows (128 columns)
 constexpr uint32_t kWsUList = kUList * 2;           // one producer warp's copy of a U list (16-bit columns)
@@ -881,8 +893,7 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
     if (warp == kWsEpiWarps + kWsProdWarps) tc::tmem_alloc(smem_u32(&tmem_base_sh), 2 * kWsNT);
     if (tid == 0) {
         for (int i = 0; i < kWsStages; ++i) {
-            // every producer thread once (cp.async or plain arrive) + one expect-tx arrive per producer warp
-            mbar_init(smem_u32(&full_bar[i]), kWsProd + kWsProdWarps);
+            mbar_init(smem_u32(&full_bar[i]), 1);  // the owning producer warp's single arrive
             mbar_init(smem_u32(&empty_bar[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -953,18 +964,21 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
         }
         bulk_wait<0>();
     } else if (warp < kWsEpiWarps + kWsProdWarps) {
-        // ---------------- producers
+        // ---------------- producers: chunk g belongs to producer warp g mod 3, which loads
+        // the whole stage: on the tile path (the chunk's 64 U rows are 64 consecutive rows
+        // of B) lane 0 issues the image chunk and four B boxes with one expect-tx arrive; on
+        // the gather path lane 0 issues the image chunk, the warp gathers B's 64 rows with
+        // cp.async, waits for its own copies and lane 0 arrives. One arrival per chunk, and
+        // the tile-path test is a per-panel bit mask in registers, so no shared-memory loads
+        // sit in the tile path's loop (they are slow while the tensor core reads operands).
         const int pw = warp - kWsEpiWarps;
-        const int pt = tid - kWsEpiWarps * 32;  // 0 .. kWsProd - 1
         uint16_t* s_u = reinterpret_cast<uint16_t*>(smem + kWsStages * kWsStageBytes + kWsCStage + pw * kWsUList);
-        constexpr int kPieces = kWsNT / 8;      // 16-byte pieces per B row of the tile
-        constexpr int kRowsPer = kKC * kPieces / kWsProd;
-        static_assert(kWsProd % kPieces == 0, "a producer thread keeps one piece column");
-        const int nch = pt % kPieces;           // this thread's piece of every row it copies
+        constexpr int kPieces = kWsNT / 8;  // 16-byte pieces per B row of the tile
         uint32_t g = 0;
         bool ok = true;
         int64_t cur = -1;
         int nU = 0, nk = 0;
+        uint64_t tile_mask = 0;  // bit j: chunk j of the panel loads B as tiles
         const T* img = img_base;
         for (int64_t unit = u_begin; unit < u_end && ok; ++unit) {
             if (unit / ntn != cur) {  // a new panel: its U list into this warp's shared copy
@@ -976,50 +990,62 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
                 const int32_t* ul = v.ulist + (size_t)p * kUList;
                 __syncwarp();  // the previous panel's copy has been read by the whole warp
                 for (int x = lane; x < nU; x += 32) s_u[x] = (uint16_t)ul[x];
+                // U is sorted and distinct, so 64 positions spanning 63 columns are consecutive
+                uint32_t lo = 0, hi = 0;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int j = lane + 32 * h;
+                    const bool run = use_tma && j * kKC + kKC - 1 < nU && ul[j * kKC + kKC - 1] - ul[j * kKC] == kKC - 1;
+                    const uint32_t bits = __ballot_sync(0xffffffffu, run);
+                    if (h == 0) lo = bits;
+                    else hi = bits;
+                }
+                static_assert(kUList / kKC <= 64, "one mask bit per chunk");
+                tile_mask = ((uint64_t)hi << 32) | lo;
                 __syncwarp();
             }
-            const int ncol = (int)(unit % ntn) * kWsNT + nch * 8;
+            const int n0 = (int)(unit % ntn) * kWsNT;  // the tile's first column
             for (int j = 0; j < nk; ++j, ++g) {
-                const uint32_t st = g % kWsStages;
-                // warp-uniform outcome: the warp synchronizes on its U list copy
+                if ((int)(g % kWsProdWarps) != pw) continue;
+                const uint32_t st = g % kWsStages;  // = pw
+                static_assert(kWsProdWarps == kWsStages, "stage g mod 3 is always loaded by warp g mod 3");
+                // warp-uniform outcome
                 if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty_bar[st]), ((g / kWsStages) + 1) & 1u, err))) {
                     ok = false;
                     break;
                 }
                 const uint32_t sa = sbase + st * kWsStageBytes;
                 const uint32_t fb = smem_u32(&full_bar[st]);
-                // U is sorted and distinct, so 64 positions spanning 63 columns are consecutive
-                const int u0 = s_u[j * kKC];  // j * kKC < nU: every chunk holds at least one U position
-                // Lane 0 of each producer warp issues a quarter of the image chunk (and, on the
-                // tile path, one of the four B boxes): copies issued by one thread are served
-                // one after another, so four issuing warps move the stage several times faster.
-                const T* img_q = img + (size_t)j * kPM * kKC + (size_t)pw * (kPM * kKC / kWsProdWarps);
-                const uint32_t img_q_bytes = kSpStageA / kWsProdWarps;
-                static_assert(kWsNT / 64 == kWsProdWarps, "one B box per producer warp");
-                if (use_tma && j * kKC + kKC - 1 < nU && (int)s_u[j * kKC + kKC - 1] - u0 == kKC - 1) {
+                const T* img_j = img + (size_t)j * kPM * kKC;
+                if ((tile_mask >> j) & 1u) {
                     if (lane == 0) {
-                        mbar_arrive_expect_tx(fb, img_q_bytes + (kKC / 8) * 1024);
-                        bulk_g2s(sa + pw * img_q_bytes, img_q, img_q_bytes, fb);
-                        const int x0 = ncol - nch * 8;  // the tile's first column
-                        tma_load_2d(sa + kSpStageA + pw * (kKC / 8) * 1024, &tmap_b, x0 + 64 * pw, u0, fb);
+                        const int u0 = s_u[j * kKC];
+                        mbar_arrive_expect_tx(fb, kWsStageBytes);
+                        bulk_g2s(sa, img_j, kSpStageA, fb);
+#pragma unroll
+                        for (int bx = 0; bx < kWsNT / 64; ++bx)
+                            tma_load_2d(sa + kSpStageA + bx * (kKC / 8) * 1024, &tmap_b, n0 + 64 * bx, u0, fb);
                     }
-                    mbar_arrive(fb);  // every producer thread arrives once per chunk on either path
                     continue;
                 }
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(fb, img_q_bytes);
-                    bulk_g2s(sa + pw * img_q_bytes, img_q, img_q_bytes, fb);
+                    asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(fb), "r"(kSpStageA) : "memory");
+                    bulk_g2s(sa, img_j, kSpStageA, fb);
                 }
-#pragma unroll
-                for (int q = 0; q < kRowsPer; ++q) {
-                    const int kk = pt / kPieces + (kWsProd / kPieces) * q;
+                // B[U rows j*64 .. +64, n0 .. n0 + 256): 64 x 32 pieces, 64 per lane
+                for (int c = lane; c < kKC * kPieces; c += 32) {
+                    const int kk = c / kPieces, nch = c % kPieces;
+                    const int ncol = n0 + nch * 8;
                     const bool in = j * kKC + kk < nU && ncol < N;
                     const int u = in ? (int)s_u[j * kKC + kk] : 0;
                     const uint32_t off = (uint32_t)(nch >> 3) * (kKC / 8 * 1024) + tc::sw128_off(kk, nch & 7);
                     tc::cp_async16(sa + kSpStageA + off, in ? (const void*)(B + (int64_t)u * N + ncol) : (const void*)B,
                                    in ? 16 : 0);
                 }
-                cp_async_mbar_arrive(fb);
+                tc::cp_async_commit();   // wait_group covers committed groups only
+                tc::cp_async_wait<0>();  // this lane's pieces have landed
+                __syncwarp();            // ... and every lane's, before lane 0 releases the stage
+                if (lane == 0) mbar_arrive(fb);
             }
         }
         tc::cp_async_wait<0>();
@@ -1156,7 +1182,7 @@ cudaError_t run_sddmm_panels(const void* A, const void* BT, void* out, int32_t k
         cfg.gridDim = dim3((unsigned)(sms / C * C));
         CUtensorMap tmap_a, tmap_bt;
         const bool bf16 = std::is_same<T, __nv_bfloat16>::value;
-        const int use_tma = encode_rows_map(&tmap_a, A, v.m, kd, kPM, bf16) &&
+        const int use_tma = encode_rows_map(&tmap_a, A, v.m, kd, kKC, bf16) &&
                                     encode_rows_map(&tmap_bt, BT, v.n, kd, kKC, bf16)
                                 ? 1
                                 : 0;
@@ -1273,8 +1299,9 @@ cudaError_t launch_spmm(int dt, int it, const void* vals, const int32_t* ro, con
     // Narrow B (n <= 16) is bound by streaming A, not by products: no tensor-core tiles.
     const bool panels = allow_panels && nnz > 0 && v.panels && dtype_ok(dt) && n % 8 == 0 && n > kNarrowMax &&
                         aligned16(B) && aligned16(C);
+    const int32_t* order = v.panels ? v.prow : nullptr;  // the plan's row order
     if (!panels)
-        return launch_spmm_general(dt, it, vals, ro, row_idx, col, m, k, B, n, C, v.bins_spmm(), nullptr, s);
+        return launch_spmm_general(dt, it, vals, ro, row_idx, col, m, k, B, n, C, v.bins_spmm(), nullptr, order, s);
     // The general rows (outside the panels that get an image) and the panels write disjoint
     // rows of C: the row kernel runs on the side stream while the panels run on s. The panels
     // are queued first, so that their CTAs are placed before the row kernel fills the SMs.
@@ -1282,7 +1309,7 @@ cudaError_t launch_spmm(int dt, int it, const void* vals, const int32_t* ro, con
     e = dt == kF16 ? run_spmm_panels<__half>(vals, ro, B, k, n, C, w, v, s)
                    : run_spmm_panels<__nv_bfloat16>(vals, ro, B, k, n, C, w, v, s);
     if (e == cudaSuccess)
-        e = launch_spmm_general(dt, it, vals, ro, row_idx, col, m, k, B, n, C, v.bins_spmm(), v.sp_dense,
+        e = launch_spmm_general(dt, it, vals, ro, row_idx, col, m, k, B, n, C, v.bins_spmm(), v.sp_dense, order,
                                 side ? side : s);
     // join on every path, so that s never runs ahead of work queued on the side stream
     const cudaError_t ej = side ? side_join(s) : cudaSuccess;
@@ -1298,15 +1325,16 @@ cudaError_t launch_sddmm(int dt, int it, const int32_t* ro, const void* row_idx,
     if (e != cudaSuccess) return e;
     const bool panels = structure_aware && nnz > 0 && v.panels && dtype_ok(dt) && kd > 0 && kd % 8 == 0 &&
                         aligned16(A) && aligned16(BT);
+    const int32_t* order = v.panels ? v.prow : nullptr;  // the plan's row order
     if (!panels)
-        return launch_sddmm_general(dt, it, ro, row_idx, col, m, n, kd, A, BT, out, v.bins_sddmm(), nullptr, s);
+        return launch_sddmm_general(dt, it, ro, row_idx, col, m, n, kd, A, BT, out, v.bins_sddmm(), nullptr, order, s);
     // The general rows and the dense panels write disjoint entries: side stream for the rows,
     // queued after the panels.
     cudaStream_t side = side_fork(s);
     e = dt == kF16 ? run_sddmm_panels<__half>(A, BT, out, kd, v, s)
                    : run_sddmm_panels<__nv_bfloat16>(A, BT, out, kd, v, s);
     if (e == cudaSuccess)
-        e = launch_sddmm_general(dt, it, ro, row_idx, col, m, n, kd, A, BT, out, v.bins_sddmm(), v.dense,
+        e = launch_sddmm_general(dt, it, ro, row_idx, col, m, n, kd, A, BT, out, v.bins_sddmm(), v.dense, order,
                                  side ? side : s);
     const cudaError_t ej = side ? side_join(s) : cudaSuccess;
     return e != cudaSuccess ? e : ej;

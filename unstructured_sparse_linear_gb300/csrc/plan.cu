@@ -97,6 +97,213 @@ __device__ __forceinline__ void or_bits_aggregated(uint32_t* bm, const int (&x)[
     }
 }
 
+// ---- 0. row order (masks of at most kOrderMaxRows rows): row_idx refined so that rows with
+// the same column set become neighbours. Rows of a block-structured mask that share their
+// blocks then fill the same panel, whose U is exactly their columns (the butterfly layer's
+// 64-row block-rows r, r + 32, ... share four blocks). One CTA sorts the positions of
+// row_idx stably by (nnz descending, signature) with an LSD radix sort and writes the order
+// to prow. The signature is a 16-bit hash of the row's first, middle and last column: rows
+// with the same column set always agree on it, and rows that agree on it with different
+// sets only share a panel (its U covers both), so no result depends on it. The sort is
+// skipped (prow = row_idx) when no aligned window of kOrdMinRun positions of row_idx holds
+// equal non-zero counts (then no panel half can be filled by rows of one pattern).
+constexpr int kOrdThreads = 1024;
+constexpr int kOrdWarps = kOrdThreads / 32;
+constexpr int kOrdPer = kOrderMaxRows / kOrdThreads;  // positions per thread
+constexpr int kOrdBins = 256;
+constexpr int kOrdMinRun = kPM / 2;
+constexpr size_t kOrdSmem = (size_t)kOrderMaxRows * 4      // keys, by row
+                            + (size_t)kOrderMaxRows * 4    // first entry, by position
+                            + (size_t)kOrderMaxRows * 2 * 2  // rows, two buffers
+                            + (size_t)kOrdWarps * kOrdBins * 4;
+
+__device__ __forceinline__ uint32_t mix_col(uint32_t c) {
+    uint32_t h = c * 0x9E3779B1u;
+    h ^= h >> 15;
+    h *= 0x85EBCA77u;
+    h ^= h >> 13;
+    return h;
+}
+
+// 16-bit signature of a row from its first, middle and last column (an empty row: 0)
+__device__ __forceinline__ uint32_t row_signature(uint32_t first, uint32_t mid, uint32_t last) {
+    const uint32_t h = mix_col(first) + mix_col(mid ^ 0x55555555u) + mix_col(last ^ 0xAAAAAAAAu);
+    return (h >> 16) ^ (h & 0xFFFFu);
+}
+
+template <typename I>
+__global__ void __launch_bounds__(kOrdThreads, 1)
+plan_order_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx, const I* __restrict__ col,
+                  PlanView v) {
+    extern __shared__ __align__(16) uint8_t osm[];
+    uint32_t* key = reinterpret_cast<uint32_t*>(osm);
+    int32_t* first = reinterpret_cast<int32_t*>(key + kOrderMaxRows);
+    uint16_t* va = reinterpret_cast<uint16_t*>(first + kOrderMaxRows);
+    uint16_t* vb = va + kOrderMaxRows;
+    uint32_t(*wcnt)[kOrdBins] = reinterpret_cast<uint32_t(*)[kOrdBins]>(vb + kOrderMaxRows);
+    __shared__ int red[3][kOrdWarps];
+    __shared__ int sh[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int m = v.m;
+    pdl_trigger();
+    pdl_wait();
+
+    // 1. each thread's positions p = tid + q * kOrdThreads: rows, then their offsets, each
+    // batch of loads issued together
+    int r[kOrdPer];
+    int32_t a[kOrdPer], b[kOrdPer];
+#pragma unroll
+    for (int q = 0; q < kOrdPer; ++q) {
+        const int p = tid + q * kOrdThreads;
+        r[q] = p < m ? idx_of(row_idx[p]) : -1;
+    }
+#pragma unroll
+    for (int q = 0; q < kOrdPer; ++q) {
+        a[q] = r[q] >= 0 ? ro[r[q]] : 0;
+        b[q] = r[q] >= 0 ? ro[r[q] + 1] : 0;
+    }
+    int mx = 0, mn = INT32_MAX, run_ok = 0;
+#pragma unroll
+    for (int q = 0; q < kOrdPer; ++q) {
+        if (r[q] < 0) continue;
+        va[tid + q * kOrdThreads] = (uint16_t)r[q];
+        first[tid + q * kOrdThreads] = a[q];
+        key[r[q]] = (uint32_t)(b[q] - a[q]);  // the count for now; the full key below
+        mx = max(mx, b[q] - a[q]);
+        mn = min(mn, b[q] - a[q]);
+    }
+    __syncthreads();
+    // 2. an aligned window of kOrdMinRun equal non-zero counts along row_idx
+    for (int p = tid * kOrdMinRun; p + kOrdMinRun <= m; p += kOrdThreads * kOrdMinRun) {
+        const uint32_t l0 = key[va[p]];
+        bool same = l0 > 0;
+        for (int q = 1; q < kOrdMinRun && same; ++q) same = key[va[p + q]] == l0;
+        run_ok |= same;
+    }
+    for (int o = 16; o; o >>= 1) {
+        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        run_ok |= __shfl_xor_sync(0xffffffffu, run_ok, o);
+    }
+    if (lane == 0) {
+        red[0][warp] = mx;
+        red[1][warp] = mn;
+        red[2][warp] = run_ok;
+    }
+    __syncthreads();
+    mx = 0;
+    mn = INT32_MAX;
+    run_ok = 0;
+    for (int w = 0; w < kOrdWarps; ++w) {
+        mx = max(mx, red[0][w]);
+        mn = min(mn, red[1][w]);
+        run_ok |= red[2][w];
+    }
+    if (run_ok) {
+        // 3. keys (nnz descending, then signature): the three column loads of half of this
+        // thread's positions together, then the other half
+        constexpr int kHalf = kOrdPer / 2;
+#pragma unroll
+        for (int hq = 0; hq < kOrdPer; hq += kHalf) {
+            int rr[kHalf], len[kHalf];
+            uint32_t c0[kHalf], c1[kHalf], c2[kHalf];
+#pragma unroll
+            for (int q = 0; q < kHalf; ++q) {
+                const int p = tid + (hq + q) * kOrdThreads;
+                rr[q] = p < m ? (int)va[p] : -1;
+                const int32_t a0 = p < m ? first[p] : 0;
+                len[q] = rr[q] >= 0 ? (int)key[rr[q]] : 0;
+                const bool ne = len[q] > 0;
+                c0[q] = ne ? (uint32_t)idx_of(col[a0]) : 0u;
+                c1[q] = ne ? (uint32_t)idx_of(col[a0 + len[q] / 2]) : 0u;
+                c2[q] = ne ? (uint32_t)idx_of(col[a0 + len[q] - 1]) : 0u;
+            }
+#pragma unroll
+            for (int q = 0; q < kHalf; ++q) {
+                if (rr[q] < 0) continue;
+                const uint32_t sg = len[q] > 0 ? row_signature(c0[q], c1[q], c2[q]) : 0u;
+                key[rr[q]] = ((uint32_t)min(mx - len[q], 0xFFFF) << 16) | sg;
+            }
+        }
+        __syncthreads();  // every key is final before any digit is read
+        int bits = 16;
+        while (bits < 32 && ((uint32_t)(mx - mn) >> (bits - 16)) != 0) ++bits;
+        // stable LSD radix sort of va by key, 8-bit digits; warp w owns positions [w L, (w + 1) L)
+        const int L = (m + kOrdWarps - 1) / kOrdWarps;
+        const int w0 = min(m, warp * L), w1 = min(m, w0 + L);
+        const uint32_t lt_mask = (1u << lane) - 1u;
+        uint16_t* src = va;
+        uint16_t* dst = vb;
+        for (int shift = 0; shift < bits; shift += 8) {
+            auto digit = [&](uint16_t rr) { return (int)((key[rr] >> shift) & (kOrdBins - 1)); };
+            for (int bn = lane; bn < kOrdBins; bn += 32) wcnt[warp][bn] = 0;
+            __syncwarp();
+            for (int c = w0; c < w1; c += 32) {
+                const int i = c + lane;
+                const bool valid = i < w1;
+                const int d = valid ? digit(src[i]) : kOrdBins + lane;
+                const uint32_t peers = __match_any_sync(0xffffffffu, d);
+                if (valid && lane == __ffs(peers) - 1) wcnt[warp][d] += __popc(peers);
+                __syncwarp();
+            }
+            __syncthreads();
+            // digit tid (< 256): exclusive prefix over warps, then a scan over the digits
+            int total = 0;
+            if (tid < kOrdBins) {
+                uint32_t acc = 0;
+                for (int w = 0; w < kOrdWarps; ++w) {
+                    const uint32_t cn = wcnt[w][tid];
+                    wcnt[w][tid] = acc;
+                    acc += cn;
+                }
+                total = (int)acc;
+            }
+            int x = total;
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (lane == 31) sh[warp] = x;
+            __syncthreads();
+            if (warp == 0) {
+                int ws = lane < kOrdBins / 32 ? sh[lane] : 0;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, ws, o);
+                    if (lane >= o) ws += y;
+                }
+                sh[lane] = ws;
+            }
+            __syncthreads();
+            if (tid < kOrdBins) {
+                const uint32_t before = (uint32_t)((warp ? sh[warp - 1] : 0) + x - total);
+                for (int w = 0; w < kOrdWarps; ++w) wcnt[w][tid] += before;
+            }
+            __syncthreads();
+            // stable scatter, each warp walking its positions in order
+            for (int c = w0; c < w1; c += 32) {
+                const int i = c + lane;
+                const bool valid = i < w1;
+                const uint16_t rr = valid ? src[i] : 0;
+                const int d = valid ? digit(rr) : kOrdBins + lane;
+                const uint32_t peers = __match_any_sync(0xffffffffu, d);
+                const uint32_t rk = __popc(peers & lt_mask);
+                if (valid) dst[wcnt[warp][d] + rk] = rr;
+                __syncwarp();
+                if (valid && lane == __ffs(peers) - 1) wcnt[warp][d] += __popc(peers);
+                __syncwarp();
+            }
+            __syncthreads();
+            uint16_t* t = src;
+            src = dst;
+            dst = t;
+        }
+        for (int p = tid; p < m; p += kOrdThreads) v.prow[p] = src[p];
+    } else {
+        for (int p = tid; p < m; p += kOrdThreads) v.prow[p] = va[p];
+    }
+    for (int p = m + tid; p < v.P * kPM; p += kOrdThreads) v.prow[p] = -1;
+}
+
 constexpr int kRowsPerWarp = kCtaRows / (kPlanThreads / 32);  // positions per warp in the row step
 constexpr int kLoadBatch = 8;                                  // index loads per lane in flight
 
@@ -106,7 +313,7 @@ __device__ void panel_work(const PlanView& v, int p, uint32_t* sm, int nnz_p, in
 template <typename I>
 __global__ void __launch_bounds__(kPlanThreads)
 plan_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx, const I* __restrict__ col,
-                 PlanView v) {
+                 PlanView v, int ordered) {
     extern __shared__ uint32_t bitmap[];  // W words (2 W in rank 0, whose panel step reuses them)
     __shared__ int red[4][kPlanThreads / 32];
     __shared__ int s_cnt[4], s_tot[4];
@@ -122,7 +329,8 @@ plan_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx, 
     int row[kRowsPerWarp];
     int32_t k0[kRowsPerWarp], len[kRowsPerWarp];
 #pragma unroll
-    for (int q = 0; q < kRowsPerWarp; ++q) row[q] = pos0 + q < v.m ? idx_of(row_idx[pos0 + q]) : -1;
+    for (int q = 0; q < kRowsPerWarp; ++q)
+        row[q] = ordered ? v.prow[pos0 + q] : (pos0 + q < v.m ? idx_of(row_idx[pos0 + q]) : -1);
 #pragma unroll
     for (int q = 0; q < kRowsPerWarp; ++q) {
         k0[q] = row[q] >= 0 ? ro[row[q]] : 0;
@@ -131,7 +339,7 @@ plan_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx, 
     int c_spmm = 0, c_sddmm = 0, c_ne = 0, c_ent = 0, total = 0;
 #pragma unroll
     for (int q = 0; q < kRowsPerWarp; ++q) {
-        if (v.panels && lane == q) v.prow[pos0 + q] = row[q];  // pos0 + q < P * 128 always
+        if (v.panels && !ordered && lane == q) v.prow[pos0 + q] = row[q];  // pos0 + q < P * 128 always
         c_spmm += len[q] >= kSpmmLongRow;
         c_sddmm += len[q] >= kSddmmLongRow;
         c_ne += len[q] >= 1;
@@ -461,6 +669,18 @@ size_t spmm_image_budget_elems(int32_t m, int32_t nnz) {
     return (size_t)8 * nnz + P * kPM * 64;
 }
 
+// Launch plan_order_kernel (one CTA) on s, stream-ordered (not as a programmatic dependent):
+// it reads row_idx, row_offsets and col_idx, which the caller's previous operations on s
+// (sort_rows, a transpose) have just written.
+template <typename I>
+cudaError_t launch_order(const int32_t* ro, const void* row_idx, const void* col, const PlanView& v, cudaStream_t s) {
+    auto kern = plan_order_kernel<I>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOrdSmem);
+    if (e != cudaSuccess) return e;
+    kern<<<1, kOrdThreads, kOrdSmem, s>>>(ro, static_cast<const I*>(row_idx), static_cast<const I*>(col), v);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_plan_build(int it, const int32_t* ro, const void* row_idx, const void* col, const PlanView& v,
                               int64_t img_budget, cudaStream_t s) {
     if (v.m <= 0) return cudaSuccess;
@@ -478,12 +698,22 @@ cudaError_t launch_plan_build(int it, const int32_t* ro, const void* row_idx, co
                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }
+    // the column-pattern row order (panels, at most kOrderMaxRows rows)
+    int ordered = 0;
+    int nlaunch = 2;
+    if (v.panels && v.m <= kOrderMaxRows) {
+        cudaError_t e = it == kIdx16 ? launch_order<uint16_t>(ro, row_idx, col, v, s)
+                                     : launch_order<int32_t>(ro, row_idx, col, v, s);
+        if (e != cudaSuccess) return e;
+        ordered = 1;
+        nlaunch = 3;
+    }
     const unsigned rows_grid = (unsigned)v.P * kPlanCluster;
     cudaError_t e = it == kIdx16
                         ? launch_pdl_cluster(plan_rows_kernel<uint16_t>, rows_grid, kPlanThreads, smem, kPlanCluster, s,
-                                             ro, (const uint16_t*)row_idx, (const uint16_t*)col, v)
+                                             ro, (const uint16_t*)row_idx, (const uint16_t*)col, v, ordered)
                         : launch_pdl_cluster(plan_rows_kernel<int32_t>, rows_grid, kPlanThreads, smem, kPlanCluster, s,
-                                             ro, (const int32_t*)row_idx, (const int32_t*)col, v);
+                                             ro, (const int32_t*)row_idx, (const int32_t*)col, v, ordered);
     if (e != cudaSuccess) return e;
     // U positions for every row group of every panel (only dense panels do work), plus the
     // lists CTA
@@ -493,7 +723,7 @@ cudaError_t launch_plan_build(int it, const int32_t* ro, const void* row_idx, co
                      : launch_pdl(plan_upos_kernel<int32_t>, upos_grid, kPlanThreads, smem, s, ro,
                                   (const int32_t*)col, v, img_budget);
     if (e != cudaSuccess) return e;
-    count_launches(2);
+    count_launches(nlaunch);
     return cudaGetLastError();
 }
 

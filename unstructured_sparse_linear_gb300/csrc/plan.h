@@ -43,6 +43,7 @@ constexpr int kPlanCluster = 8;   // CTAs per panel (one thread-block cluster) i
 constexpr int kCtaRows = kPM / kPlanCluster;
 constexpr int kMaxPanelCols = 65536;
 constexpr int kMinDenseRows = 16;
+constexpr int kOrderMaxRows = 16384;  // masks up to this many rows get the column-pattern row order
 
 enum PlanCount {
     kCntDense = 0,      // dense panels (SDDMM)

@@ -92,7 +92,8 @@ template <typename T, typename I, int V>
 __global__ void __launch_bounds__(kSddmmThreads, 3)
 sddmm_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx, const I* __restrict__ col,
                   const T* __restrict__ A, const T* __restrict__ BT, T* __restrict__ out, int32_t kd, int G,
-                  const int32_t* __restrict__ bins, const uint8_t* __restrict__ skip) {
+                  const int32_t* __restrict__ bins, const uint8_t* __restrict__ skip,
+                  const int32_t* __restrict__ order) {
     __shared__ uint8_t skip_cache[kSkipCache];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     pdl_trigger();
@@ -107,7 +108,7 @@ sddmm_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx,
     // ---- long rows: a CTA per row
     for (int32_t p = blockIdx.x; p < n_long; p += gridDim.x) {
         if (skipped(p)) continue;
-        const int row = idx_of(row_idx[p]);
+        const int row = order ? order[p] : idx_of(row_idx[p]);
         const int32_t k0 = ro[row], k1 = ro[row + 1];
         for (int32_t kb = k0 + warp * kNB; kb < k1; kb += kSddmmWarps * kNB)
             sddmm_batch<T, I, V>(row, kb, min(kNB, k1 - kb), col, A, BT, out, kd, 32, lane, 0xffffffffu);
@@ -121,7 +122,7 @@ sddmm_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx,
     const int64_t ngroups = (int64_t)gridDim.x * kSddmmWarps * gpw;
     for (int64_t p = n_long + gid; p < n_rows; p += ngroups) {
         if (skipped(p)) continue;
-        const int row = idx_of(row_idx[p]);
+        const int row = order ? order[p] : idx_of(row_idx[p]);
         const int32_t k0 = ro[row], k1 = ro[row + 1];
         for (int32_t kb = k0; kb < k1; kb += kNB)
             sddmm_batch<T, I, V>(row, kb, min(kNB, k1 - kb), col, A, BT, out, kd, G, gl, gmask);
@@ -130,7 +131,7 @@ sddmm_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx,
 
 template <typename T, typename I>
 cudaError_t run(const int32_t* ro, const void* row_idx, const void* col, int32_t kd, const void* A, const void* BT,
-                void* out, const int32_t* bins, const uint8_t* skip, cudaStream_t s) {
+                void* out, const int32_t* bins, const uint8_t* skip, const int32_t* order, cudaStream_t s) {
     constexpr int VV = Elt<T>::kVec;
     const bool vec = ((int64_t)kd * sizeof(T)) % 16 == 0 && (uintptr_t)A % 16 == 0 && (uintptr_t)BT % 16 == 0;
     auto kern = vec ? sddmm_rows_kernel<T, I, VV> : sddmm_rows_kernel<T, I, 1>;
@@ -141,8 +142,16 @@ cudaError_t run(const int32_t* ro, const void* row_idx, const void* col, int32_t
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kSddmmThreads, 0);
     if (e != cudaSuccess) return e;
     const int grid = device_props().sm_count * (occ > 0 ? occ : 1);
-    e = launch_pdl(kern, grid, kSddmmThreads, 0, s, ro, static_cast<const I*>(row_idx), static_cast<const I*>(col),
-                   static_cast<const T*>(A), static_cast<const T*>(BT), static_cast<T*>(out), kd, G, bins, skip);
+    // Beside tensor-core panels (skip flags set) the kernel runs on a side stream after an
+    // event wait: an ordinary launch there; on the caller's stream a programmatic dependent.
+    if (skip)
+        kern<<<grid, kSddmmThreads, 0, s>>>(ro, static_cast<const I*>(row_idx), static_cast<const I*>(col),
+                                            static_cast<const T*>(A), static_cast<const T*>(BT), static_cast<T*>(out),
+                                            kd, G, bins, skip, order);
+    else
+        e = launch_pdl(kern, grid, kSddmmThreads, 0, s, ro, static_cast<const I*>(row_idx), static_cast<const I*>(col),
+                       static_cast<const T*>(A), static_cast<const T*>(BT), static_cast<T*>(out), kd, G, bins, skip,
+                       order);
     if (e != cudaSuccess) return e;
     count_launches(1);
     return cudaGetLastError();
@@ -152,15 +161,17 @@ cudaError_t run(const int32_t* ro, const void* row_idx, const void* col, int32_t
 
 cudaError_t launch_sddmm_general(int dt, int it, const int32_t* ro, const void* row_idx, const void* col, int32_t m,
                                  int32_t n, int32_t kd, const void* A, const void* BT, void* out,
-                                 const int32_t* bins, const uint8_t* skip, cudaStream_t s) {
+                                 const int32_t* bins, const uint8_t* skip, const int32_t* order, cudaStream_t s) {
     (void)m;
     (void)n;
-    if (dt == kF32) return it == kIdx16 ? run<float, uint16_t>(ro, row_idx, col, kd, A, BT, out, bins, skip, s)
-                                        : run<float, int32_t>(ro, row_idx, col, kd, A, BT, out, bins, skip, s);
-    if (dt == kF16) return it == kIdx16 ? run<__half, uint16_t>(ro, row_idx, col, kd, A, BT, out, bins, skip, s)
-                                        : run<__half, int32_t>(ro, row_idx, col, kd, A, BT, out, bins, skip, s);
-    return it == kIdx16 ? run<__nv_bfloat16, uint16_t>(ro, row_idx, col, kd, A, BT, out, bins, skip, s)
-                        : run<__nv_bfloat16, int32_t>(ro, row_idx, col, kd, A, BT, out, bins, skip, s);
+    if (dt == kF32)
+        return it == kIdx16 ? run<float, uint16_t>(ro, row_idx, col, kd, A, BT, out, bins, skip, order, s)
+                            : run<float, int32_t>(ro, row_idx, col, kd, A, BT, out, bins, skip, order, s);
+    if (dt == kF16)
+        return it == kIdx16 ? run<__half, uint16_t>(ro, row_idx, col, kd, A, BT, out, bins, skip, order, s)
+                            : run<__half, int32_t>(ro, row_idx, col, kd, A, BT, out, bins, skip, order, s);
+    return it == kIdx16 ? run<__nv_bfloat16, uint16_t>(ro, row_idx, col, kd, A, BT, out, bins, skip, order, s)
+                        : run<__nv_bfloat16, int32_t>(ro, row_idx, col, kd, A, BT, out, bins, skip, order, s);
 }
 
 }  // namespace spops

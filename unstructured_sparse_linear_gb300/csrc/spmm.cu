@@ -86,7 +86,7 @@ template <typename T, typename I, int V>
 __global__ void __launch_bounds__(kSpmmThreads, 3)
 spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, const I* __restrict__ row_idx,
                  const I* __restrict__ col, const T* __restrict__ B, T* __restrict__ C, int32_t m, int32_t N, int G,
-                 const int32_t* __restrict__ bins, const uint8_t* __restrict__ skip) {
+                 const int32_t* __restrict__ bins, const uint8_t* __restrict__ skip, const int32_t* __restrict__ order) {
     __shared__ float red[kSpmmWarps][32 * V];
     __shared__ uint8_t skip_cache[kSkipCache];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -118,7 +118,7 @@ spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, con
                 const int64_t rel = item - i0;  // < 128 * nch
                 const int32_t p = (int32_t)(pan0 + (uint32_t)rel / (uint32_t)nch);
                 const int c = (int)((uint32_t)rel % (uint32_t)nch);
-                const int row = idx_of(row_idx[p]);
+                const int row = order ? order[p] : idx_of(row_idx[p]);
                 const int32_t k0 = ro[row], k1 = ro[row + 1];
                 const int col0 = c * chunk + lane * V;
                 float acc[V];
@@ -184,7 +184,7 @@ spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, con
                     cq[q] = (int)(item % nch);
                 }
                 live[q] = item < items && !skipped(p);  // uniform across the group
-                rowq[q] = live[q] ? idx_of(row_idx[p]) : 0;
+                rowq[q] = live[q] ? (order ? order[p] : idx_of(row_idx[p])) : 0;
             }
 #pragma unroll
             for (int q = 0; q < kBatch; ++q) {
@@ -336,7 +336,8 @@ int pow2_cover(int64_t units) {
 
 template <typename T, typename I>
 cudaError_t run(const void* vals, const int32_t* ro, const void* row_idx, const void* col, int32_t m,
-                const void* B, int32_t N, void* C, const int32_t* bins, const uint8_t* skip, cudaStream_t s) {
+                const void* B, int32_t N, void* C, const int32_t* bins, const uint8_t* skip, const int32_t* order,
+                cudaStream_t s) {
     if (N <= kNarrowN) return run_narrow<T, I>(vals, ro, row_idx, col, m, B, N, C, skip, s);
     constexpr int VV = Elt<T>::kVec;
     const bool vec = ((int64_t)N * sizeof(T)) % 16 == 0 && (uintptr_t)B % 16 == 0 && (uintptr_t)C % 16 == 0;
@@ -347,8 +348,16 @@ cudaError_t run(const void* vals, const int32_t* ro, const void* row_idx, const 
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kSpmmThreads, 0);
     if (e != cudaSuccess) return e;
     const int grid = device_props().sm_count * (occ > 0 ? occ : 1);
-    e = launch_pdl(kern, grid, kSpmmThreads, 0, s, static_cast<const T*>(vals), ro, static_cast<const I*>(row_idx),
-                   static_cast<const I*>(col), static_cast<const T*>(B), static_cast<T*>(C), m, N, G, bins, skip);
+    // Beside tensor-core panels (skip flags set) the kernel runs on a side stream after an
+    // event wait: an ordinary launch there; on the caller's stream a programmatic dependent.
+    if (skip)
+        kern<<<grid, kSpmmThreads, 0, s>>>(static_cast<const T*>(vals), ro, static_cast<const I*>(row_idx),
+                                           static_cast<const I*>(col), static_cast<const T*>(B), static_cast<T*>(C), m,
+                                           N, G, bins, skip, order);
+    else
+        e = launch_pdl(kern, grid, kSpmmThreads, 0, s, static_cast<const T*>(vals), ro, static_cast<const I*>(row_idx),
+                       static_cast<const I*>(col), static_cast<const T*>(B), static_cast<T*>(C), m, N, G, bins, skip,
+                       order);
     if (e != cudaSuccess) return e;
     count_launches(1);
     return cudaGetLastError();
@@ -358,14 +367,16 @@ cudaError_t run(const void* vals, const int32_t* ro, const void* row_idx, const 
 
 cudaError_t launch_spmm_general(int dt, int it, const void* vals, const int32_t* ro, const void* row_idx,
                                 const void* col, int32_t m, int32_t k, const void* B, int32_t n, void* C,
-                                const int32_t* bins, const uint8_t* skip, cudaStream_t s) {
+                                const int32_t* bins, const uint8_t* skip, const int32_t* order, cudaStream_t s) {
     (void)k;
-    if (dt == kF32) return it == kIdx16 ? run<float, uint16_t>(vals, ro, row_idx, col, m, B, n, C, bins, skip, s)
-                                        : run<float, int32_t>(vals, ro, row_idx, col, m, B, n, C, bins, skip, s);
-    if (dt == kF16) return it == kIdx16 ? run<__half, uint16_t>(vals, ro, row_idx, col, m, B, n, C, bins, skip, s)
-                                        : run<__half, int32_t>(vals, ro, row_idx, col, m, B, n, C, bins, skip, s);
-    return it == kIdx16 ? run<__nv_bfloat16, uint16_t>(vals, ro, row_idx, col, m, B, n, C, bins, skip, s)
-                        : run<__nv_bfloat16, int32_t>(vals, ro, row_idx, col, m, B, n, C, bins, skip, s);
+    if (dt == kF32)
+        return it == kIdx16 ? run<float, uint16_t>(vals, ro, row_idx, col, m, B, n, C, bins, skip, order, s)
+                            : run<float, int32_t>(vals, ro, row_idx, col, m, B, n, C, bins, skip, order, s);
+    if (dt == kF16)
+        return it == kIdx16 ? run<__half, uint16_t>(vals, ro, row_idx, col, m, B, n, C, bins, skip, order, s)
+                            : run<__half, int32_t>(vals, ro, row_idx, col, m, B, n, C, bins, skip, order, s);
+    return it == kIdx16 ? run<__nv_bfloat16, uint16_t>(vals, ro, row_idx, col, m, B, n, C, bins, skip, order, s)
+                        : run<__nv_bfloat16, int32_t>(vals, ro, row_idx, col, m, B, n, C, bins, skip, order, s);
 }
 
 }  // namespace spops
