@@ -275,6 +275,32 @@ def run_step_forked(ops, stream, side):
         stream.wait_event(j)
 
 
+def run_fixed_forked(ops, stream, side):
+    """The step with the mask fixed: row_idx and the plan of the last full step are reused, so
+    only the operators on values run, forked as in run_step_forked (csr_add and sddmm on the
+    side streams, spmm on `stream`)."""
+    by = dict(ops)
+    spare = list(side)
+    joins = []
+    for name in ("csr_add", "sddmm"):
+        if name in by and (name == "csr_add" or "spmm" in by):
+            e = torch.cuda.Event()
+            e.record(stream)
+            s = spare.pop(0)
+            s.wait_event(e)
+            with torch.cuda.stream(s):
+                by[name]()
+                j = torch.cuda.Event()
+                j.record(s)
+            joins.append(j)
+        elif name in by:
+            by[name]()
+    if "spmm" in by:
+        by["spmm"]()
+    for j in joins:
+        stream.wait_event(j)
+
+
 def host_inputs(w, idx):
     h = {"ro": w.row_offsets, "col": w.col_idx.to(idx), "val": w.values}
     for k in ("B", "A", "BT", "W"):
@@ -332,6 +358,11 @@ def measure(sp, lib, name, args, dev, ws, rank, local, flush):
             with torch.cuda.graph(g, stream=stream, pool=pool):
                 f()
             op_graphs.append((op_name, g))
+        # the mask-fixed step: the value operators on the row order and plan that the
+        # operator graphs above leave in their buffers
+        fixed_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(fixed_graph, stream=stream, pool=pool):
+            run_fixed_forked(ops, stream, side)
         for _ in range(args.warmup):
             step_graph.replay()
             for _, g in op_graphs:
@@ -368,6 +399,13 @@ def measure(sp, lib, name, args, dev, ws, rank, local, flush):
                 g.replay()
                 evb[s][j + 1].record(stream)
         torch.cuda.synchronize(dev)
+        evf = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(nb)]
+        for s in range(nb):
+            flush.zero_()
+            evf[s][0].record(stream)
+            fixed_graph.replay()
+            evf[s][1].record(stream)
+        torch.cuda.synchronize(dev)
 
     step_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
     op_ms = {op_name: [evb[s][j].elapsed_time(evb[s][j + 1]) for s in range(nb)]
@@ -375,7 +413,14 @@ def measure(sp, lib, name, args, dev, ws, rank, local, flush):
     total_ms = max_over_ranks(sum(step_ms), dev)
     ms_per_step = total_ms / args.steps
     value = ws * flops * args.steps / (total_ms * 1e-3) / 1e9
-    del step_graph, op_graphs
+    fixed_ms = [evf[s][0].elapsed_time(evf[s][1]) for s in range(nb)]
+    fixed_avg = sum(fixed_ms) / nb
+    mask_fixed = {"ms_per_step": round(fixed_avg, 5), "ms_median": round(statistics.median(fixed_ms), 5),
+                  "value": round(flops / (fixed_avg * 1e-3) / 1e9, 2), "unit": "GFLOP/s",
+                  "ops": [o for o, _ in ops if o not in ("sort_rows", "plan")],
+                  "note": "row_idx and the plan built once and reused (the mask does not change between steps); "
+                          "forked like the full step; L2 flushed before each step"}
+    del step_graph, op_graphs, fixed_graph
 
     e2e = run_e2e(sp, w, dev, idx, args, flops, ws)
     next_ops = time_next_ops(sp, w, d, idx, stream, pool, flush, nb) if not args.no_next_ops else None
@@ -412,7 +457,7 @@ def measure(sp, lib, name, args, dev, ws, rank, local, flush):
                            single_thread=name in SINGLE_THREAD_BASELINE and args.workload == "all")
     rec = {"value": round(value, 2), "unit": "GFLOP/s", "ms_per_step": round(ms_per_step, 5), "steps": args.steps,
            "dtype": w.dtype, "config": config_dict(name, w, args), "per_op": per_op, "roofline": roofline,
-           "cpu_baseline": cpu, "e2e": e2e, "next_ops": next_ops,
+           "cpu_baseline": cpu, "e2e": e2e, "next_ops": next_ops, "mask_fixed": mask_fixed,
            "gpu_launches": int(launches_per_step) * args.steps, "launches_per_step": int(launches_per_step),
            "clocks": clocks, "breakdown_steps": nb,
            "step_ms_sum_of_ops": round(sum(v["ms"] for v in per_op.values()), 5),
@@ -449,7 +494,7 @@ def run_gpu(args):
         "warmup": args.warmup, "ms_per_step": h["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": h["dtype"], "data": "synthetic (seeded; workload recipes in DESIGN.md)",
         "config": h["config"], "per_op": h["per_op"], "roofline": h["roofline"], "cpu_baseline": h["cpu_baseline"],
-        "e2e": h["e2e"], "gpu_launches": h["gpu_launches"], "clocks": h["clocks"],
+        "e2e": h["e2e"], "gpu_launches": h["gpu_launches"], "clocks": h["clocks"], "mask_fixed": h["mask_fixed"],
         "headline": f"{head}: the step (sort_rows+plan+spmm+sddmm+csr_add where defined) on this workload; "
                     "per_config holds every configuration measured the same way",
         "per_config": {k: {kk: vv for kk, vv in v.items() if kk != "next_ops"} for k, v in per_config.items()},

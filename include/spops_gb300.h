@@ -179,6 +179,17 @@ SPOPS_API int spops_plan_build(const int32_t* row_offsets, const void* row_idx, 
  * consecutive tiles of a panel), 0, SpMM row bins [4], SDDMM row bins [4]} of a built plan. */
 SPOPS_API int spops_plan_stats(const void* plan, int32_t m, int32_t n, int32_t nnz, int32_t* stats_out, void* stream);
 
+/* order_out (device int32[m]) = the row at each position of the plan's row order, the order
+ * in which the panels (128 consecutive positions each) and the operators' row kernels take
+ * the rows. It is row_idx, refined for masks of at most 16384 rows: when two runs of at least
+ * 32 positions of row_idx (stretches of non-empty rows with equal keys) share a key, the
+ * positions are sorted stably by key = (65535 - min(nnz, 65535)) << 16 | a 16-bit hash of the
+ * row's first, middle and last column, so that rows with one column pattern share panels.
+ * Returns SPOPS_ERR_UNSUPPORTED when the plan has no panels (n > 65536: the operators walk
+ * row_idx itself). */
+SPOPS_API int spops_plan_row_order(const void* plan, int32_t m, int32_t n, int32_t nnz, int32_t* order_out,
+                                   void* stream);
+
 /* ---------------------------------------------------------------- operators */
 
 /* Scratch bytes spops_spmm needs (enough to build its own plan and the dense-panel images). */

@@ -88,6 +88,10 @@ def test_bad_arguments_rejected_on_host(lib):
     assert lib.spops_sort_rows(FAKE, 10, 5, FAKE, 0, FAKE, 8, None) == 3
     assert lib.spops_plan_build(FAKE, FAKE, FAKE, 0, 10, 10, 5, P(0x40000), 64, None) == 3
     assert lib.spops_row_bins(FAKE, 10, 0, FAKE, None) == 1
+    # the plan's row order: misaligned plan or output; no panels beyond 65536 columns
+    assert lib.spops_plan_row_order(P(0x30010), 10, 10, 5, FAKE, None) == 1
+    assert lib.spops_plan_row_order(P(0x40000), 10, 10, 5, P(0x10002), None) == 1
+    assert lib.spops_plan_row_order(P(0x40000), 10, 70000, 5, FAKE, None) == 2
     assert lib.spops_get_device_error(None, None) == 1
     # the wait self-test: limits outside [1 us, 1 s], misaligned output
     assert lib.spops_selftest_wait_timeout(999, None, None) == 1

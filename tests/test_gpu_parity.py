@@ -31,6 +31,9 @@ SMALL = {
     # 200 x 1500 cluster half full: |U| = 1500 panels, SpMM on tensor cores, SDDMM general
     "rosa_wide": wl.spec("rosa", m=2000, n=3000, density=0.025, N=136, kd=72,
                          mask_kw=(("row_frac", 0.1), ("col_frac", 0.5))),
+    # the 384 -> 1536 pixelfly layer (48 x 48 blocks, not a multiple of the 64-wide K chunk),
+    # fewer tokens
+    "fly_s": wl.spec("fly_small_1", N=200, kd=136),
 }
 INT32_CASES = ("rosa_i32", "rosa_dense_i32")
 
@@ -254,6 +257,27 @@ def test_unaligned_pointers_take_the_plain_path():
                       "csr_add unaligned")
 
 
+@pytest.mark.parametrize("m,n,density,dtype,itype", [(64, 20000, 0.3, "f32", "int16"),
+                                                      (64, 20000, 1.0, "f32", "int32"),
+                                                      (3, 300000, 0.05, "bf16", "int32"),
+                                                      (40, 9000, 0.6, "f16", "int16")])
+def test_csr_add_wide_rows(m, n, density, dtype, itype):
+    """Rows wider than a 16 KB tile: each tile finds its first and last entry in the edge
+    rows by searching the sorted columns. Rows of every width from empty to full."""
+    rng = np.random.default_rng(m + n)
+    mask = rng.random((m, n)) < density
+    mask[1] = False
+    mask[2 % m, :] = True
+    mask[0, : n // 3] = False
+    ro, col, vals = _csr(m, n, *np.nonzero(mask), dtype, seed=4)
+    W = wl.normal(4, 2, (m, n), 1.0, dtype)
+    idt = torch.int16 if itype == "int16" else torch.int32
+    dro, dcol = torch.from_numpy(ro).cuda(), torch.from_numpy(col).to(idt).cuda()
+    ridx = torch.from_numpy(oracle.sort_rows(ro)).to(idt).cuda()
+    got = sp.csr_add(vals.cuda(), dro, ridx, dcol, W.cuda())
+    assert_bits_equal(got, oracle.csr_add(ro, col, vals, W), dtype, f"csr_add {m}x{n}")
+
+
 def test_csr_add_in_place():
     w = wl.generate(SMALL["llama_s"])
     g = to_gpu(w)
@@ -367,6 +391,48 @@ def test_spmm_many_units_pipeline_exact(case):
     assert_bits_equal(C, oracle.spmm(ro, col, w.values, w.B), w.dtype, f"{case} many-units spmm")
 
 
+def _mixed_panels(seed=5):
+    """A 16384 x 4096 mask whose panels alternate between the SpMM pipeline's kinds, in
+    row_idx order (rows by nnz): 400 of 1200 pool columns (|U| = 1200, gathered, streamed
+    image), 64-row block-rows of four 64-column blocks (|U| = 256, tiles, resident image),
+    180 of 600 (|U| = 600, gathered, streamed) and 150 of 200 (|U| = 200, gathered, resident)."""
+    rng = np.random.default_rng(seed)
+    n = 4096
+    rows, cols = [], []
+    for br in range(64):  # rows 0 .. 4095: block-rows
+        cs = np.concatenate([np.arange(b * 64, b * 64 + 64) for b in ((br % 16) * 4 + np.arange(4))])
+        rows.append(np.repeat(np.arange(br * 64, br * 64 + 64), cs.size))
+        cols.append(np.tile(cs, 64))
+    for base, per, pool_n in ((4096, 400, 1200), (8192, 180, 600), (12288, 150, 200)):
+        pool = rng.choice(n, pool_n, replace=False)
+        pick = np.argsort(rng.random((4096, pool_n)), axis=1)[:, :per]
+        rows.append(np.repeat(np.arange(base, base + 4096), per))
+        cols.append(pool[pick].ravel())
+    ro, col = wl.csr_from_coords(np.concatenate(rows), np.concatenate(cols), 16384)
+    vals = torch.from_numpy(rng.integers(-3, 4, size=col.size).astype(np.float32)).to(torch.bfloat16)
+    B = torch.from_numpy(rng.integers(-3, 4, size=(n, 2056)).astype(np.float32)).to(torch.bfloat16)
+    return ro, col, vals, B
+
+
+def test_spmm_mixed_panels_pipeline_exact():
+    """The warp-specialized SpMM pipeline across panel changes between resident images
+    (|U| <= 256, loaded once per run of units) and streamed ones, on tile and gather paths:
+    exact small-integer sums, so every element equals the general kernel and the oracle."""
+    ro, col, vals, B = _mixed_panels()
+    m = len(ro) - 1
+    dro = torch.from_numpy(ro).cuda()
+    dcol = torch.from_numpy(col).to(torch.int16).cuda()
+    ridx = torch.from_numpy(oracle.sort_rows(ro)).to(torch.int16).cuda()
+    plan = sp.plan_build(dro, ridx, dcol, B.shape[0])
+    st = plan.stats()
+    assert st["spmm_panels"] == st["panels"] == 128, st
+    C = sp.spmm(vals.cuda(), dro, ridx, dcol, B.cuda(), m, plan=plan)
+    ref = sp.spmm(vals.cuda(), dro, ridx, dcol, B.cuda(), m, path="general")
+    torch.cuda.synchronize()
+    assert torch.equal(C.view(torch.int16), ref.view(torch.int16))
+    assert_bits_equal(C, oracle.spmm(ro, col, vals, B), "bf16", "mixed panels spmm")
+
+
 @pytest.mark.parametrize("case", ["butterfly", "clustered"])
 def test_sddmm_many_tiles_pipeline_exact(case):
     """At least two SDDMM tiles per SM are possible, so the structure-aware SDDMM runs its
@@ -404,19 +470,15 @@ def _mix_col(c):
 
 def plan_order(ro, col, row_idx, n):
     """The plan's row order restated on the host: for masks of at most 16384 rows (with column
-    panels, n <= 65536), row_idx stably sorted by (nnz descending, 16-bit signature of the
-    row's first, middle and last column); left as row_idx when no aligned window of 64
-    positions holds equal non-zero counts."""
+    panels, n <= 65536), row_idx stably sorted by (nnz descending, counts of 65535 and more
+    tied, then a 16-bit signature of the row's first, middle and last column); left as
+    row_idx unless two runs of at least 32 positions (maximal stretches of non-empty rows
+    with one key, in row_idx order) have the same key."""
     m = len(ro) - 1
     order = np.asarray(row_idx, dtype=np.int64)
     if m > 16384 or n > 65536:
         return order
     lens = np.diff(ro).astype(np.int64)
-    lp = lens[order]
-    run = any(lp[p] > 0 and np.all(lp[p:p + 64] == lp[p]) for p in range(0, m - 63, 64))
-    if not run:
-        return order
-    sig = np.zeros(m, dtype=np.uint64)
     ne = lens > 0
     a = np.asarray(ro[:-1], dtype=np.int64)
     c0 = np.where(ne, col[np.minimum(a, len(col) - 1)], 0).astype(np.uint64)
@@ -424,8 +486,20 @@ def plan_order(ro, col, row_idx, n):
     c2 = np.where(ne, col[np.maximum(a + lens - 1, 0)], 0).astype(np.uint64)
     h = (_mix_col(c0) + _mix_col(c1 ^ np.uint64(0x55555555)) + _mix_col(c2 ^ np.uint64(0xAAAAAAAA))) & np.uint64(0xFFFFFFFF)
     sig = np.where(ne, (h >> np.uint64(16)) ^ (h & np.uint64(0xFFFF)), np.uint64(0))
-    key = np.minimum(lens.max() - lens, 0xFFFF).astype(np.uint64) << np.uint64(16) | sig
-    return order[np.argsort(key[order], kind="stable")]
+    key = (0xFFFF - np.minimum(lens, 0xFFFF)).astype(np.uint64) << np.uint64(16) | sig
+    kp, lp = key[order], lens[order]
+    long_keys = []
+    p = 0
+    while p < m:
+        e = p + 1
+        while e < m and kp[e] == kp[p]:
+            e += 1
+        if lp[p] > 0 and e - p >= 32:
+            long_keys.append(int(kp[p]))
+        p = e
+    if len(set(long_keys)) == len(long_keys):
+        return order
+    return order[np.argsort(kp, kind="stable")]
 
 
 def expected_plan(ro, col, row_idx, n):
@@ -457,19 +531,73 @@ def expected_plan(ro, col, row_idx, n):
             "bins_spmm": bins(sp.SPMM_LONG_ROW), "bins_sddmm": bins(sp.SDDMM_LONG_ROW)}
 
 
-@pytest.mark.parametrize("name", ["rosa_s", "llama_s", "butterfly_s", "rosa_dense", "rosa_dense_i32", "rosa_wide"])
+@pytest.mark.parametrize("name", ["rosa_s", "llama_s", "butterfly_s", "rosa_dense", "rosa_dense_i32", "rosa_wide",
+                                  "fly_s"])
 def test_plan_matches_rule(small_cases, name):
     w = small_cases[name]
     g = to_gpu(w, idx_dtype=torch.int32 if name in INT32_CASES else None)
     got = sp.plan_build(g["ro"], g["row_idx"], g["col"], w.n).stats()
     ro, col = w.row_offsets.numpy(), w.col_idx.numpy()
-    want = expected_plan(ro, col, plan_order(ro, col, oracle.sort_rows(ro), w.n), w.n)
+    row_idx = oracle.sort_rows(ro)
+    order = plan_order(ro, col, row_idx, w.n)
+    # block masks repeat their rows' patterns and get the order; these random masks keep row_idx
+    assert (not np.array_equal(order, row_idx)) == (name in ("butterfly_s", "fly_s")), name
+    want = expected_plan(ro, col, order, w.n)
     for k, v in want.items():
         assert got[k] == v, (k, got[k], v)
     if name == "rosa_wide":  # the SpMM-only panels: |U| between 1024 and 4096
         assert got["spmm_panels"] >= 1 and got["dense_panels"] == 0
     elif name != "llama_s":
         assert got["dense_panels"] >= 1  # these cases exercise the tensor-core path
+
+
+def _pattern_rows(m, n, runs, nnz=16, seed=0):
+    """A CSR mask of m rows with nnz entries each: rows in each (start, length) of `runs` hold
+    one shared column pattern, every other row its own random pattern."""
+    rng = np.random.default_rng(seed)
+    shared = np.sort(rng.choice(n, nnz, replace=False))
+    rows, cols = [], []
+    for i in range(m):
+        c = shared if any(s <= i < s + L for s, L in runs) else np.sort(rng.choice(n, nnz, replace=False))
+        rows += [i] * nnz
+        cols += list(c)
+    return _csr(m, n, rows, cols, "bf16", seed)
+
+
+ORDER_CASES = {
+    # two runs of 32 rows, each straddling a 64-position window boundary: ordered
+    "straddle": dict(m=512, n=1024, runs=[(48, 32), (300, 32)]),
+    # the second run one row short of a long run: row_idx kept
+    "short_run": dict(m=512, n=1024, runs=[(48, 32), (300, 31)]),
+    # one long run only (a clustered mask's full rows): row_idx kept
+    "one_run": dict(m=512, n=1024, runs=[(100, 200)]),
+    # more than 1024 runs (the positions' radix sort instead of the runs' bitonic sort)
+    "many_runs": dict(m=3000, n=1024, runs=[(48, 32), (2000, 40)]),
+}
+
+
+@pytest.mark.parametrize("name", list(ORDER_CASES) + ["butterfly_s", "fly_s", "rosa_s", "llama_s", "rosa_dense_i32",
+                                                      "butterfly", "fly_small_1", "fly_large_1", "rosa", "llama_mlp"])
+def test_plan_row_order_matches_rule(small_cases, name):
+    """The plan's row order, position by position, against the rule restated on the host."""
+    if name in ORDER_CASES:
+        c = ORDER_CASES[name]
+        ro, col, _ = _pattern_rows(c["m"], c["n"], c["runs"])
+        n, idt = c["n"], torch.int16
+    else:
+        w = small_cases[name] if name in small_cases else wl.generate(wl.spec(name, N=8, kd=8))
+        ro, col, n = w.row_offsets.numpy(), w.col_idx.numpy(), w.n
+        idt = torch.int32 if name in INT32_CASES else torch.int16
+    row_idx = oracle.sort_rows(ro)
+    dro = torch.from_numpy(np.asarray(ro, dtype=np.int32)).cuda()
+    dcol = torch.from_numpy(np.asarray(col)).to(idt).cuda()
+    ridx = torch.from_numpy(row_idx).to(idt).cuda()
+    got = sp.plan_build(dro, ridx, dcol, n).row_order().cpu().numpy()
+    want = plan_order(ro, col, row_idx, n)
+    assert np.array_equal(got, want), name
+    ordered = not np.array_equal(want, row_idx)
+    assert ordered == (name in ("straddle", "many_runs", "butterfly_s", "fly_s", "butterfly", "fly_small_1",
+                                "fly_large_1")), name
 
 
 @pytest.mark.parametrize("name", ["rosa_dense", "butterfly_s", "llama_s"])

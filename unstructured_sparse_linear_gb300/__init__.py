@@ -144,6 +144,17 @@ class Plan:
                 "image_elems": s[4], "panels": s[5], "sddmm_groups": s[6], "bins_spmm": s[8:12],
                 "bins_sddmm": s[12:16]}
 
+    def row_order(self) -> torch.Tensor:
+        """The row at each position of the plan's row order (int32 [m], on the plan's
+        device): row_idx, or row_idx sorted by (nnz, column pattern) when rows with one
+        pattern recur in separate runs. Masks wider than 65536 columns have no panels and
+        raise."""
+        out = torch.empty(self.m, dtype=torch.int32, device=self.buf.device)
+        with torch.cuda.device(self.buf.device):
+            _check(_L().spops_plan_row_order(self.ptr(), self.m, self.n, self.nnz, _p(out), _stream()),
+                   "plan_row_order")
+        return out
+
 
 def plan_build(row_offsets, row_idx, col_idx, n: int) -> Plan:
     """Build the mask plan of an m x n CSR structure (asynchronous on the current stream)."""

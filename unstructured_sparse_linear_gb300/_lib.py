@@ -31,6 +31,7 @@ SIGNATURES = {
     "spops_plan_size": (_SZ, [_I32, _I32, _I32]),
     "spops_plan_build": (_INT, [_P, _P, _P, _INT, _I32, _I32, _I32, _P, _SZ, _P]),
     "spops_plan_stats": (_INT, [_P, _I32, _I32, _I32, _P, _P]),
+    "spops_plan_row_order": (_INT, [_P, _I32, _I32, _I32, _P, _P]),
     "spops_spmm": (_INT, [_P, _P, _P, _P, _INT, _INT, _I32, _I32, _I32, _P, _I32, _P, _INT, _P, _P, _SZ, _P]),
     "spops_sddmm_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _INT, _INT, _INT]),
     "spops_sddmm": (_INT, [_P, _P, _P, _INT, _INT, _I32, _I32, _I32, _I32, _P, _P, _P, _INT, _P, _P, _SZ, _P]),

@@ -312,6 +312,17 @@ int spops_plan_stats(const void* plan, int32_t m, int32_t n, int32_t nnz, int32_
     return cuda_status(launch_plan_stats(v, stats_out, (cudaStream_t)stream), "plan_stats launch");
 }
 
+int spops_plan_row_order(const void* plan, int32_t m, int32_t n, int32_t nnz, int32_t* order_out, void* stream) {
+    if (m <= 0 || n < 0 || nnz < 0) return fail(SPOPS_ERR_INVALID_ARG, "bad sizes (m=%d n=%d nnz=%d)", m, n, nnz);
+    if (!plan || !aligned(plan, 1024)) return fail(SPOPS_ERR_INVALID_ARG, "plan is NULL or not 1024-byte aligned");
+    if (!order_out || !aligned(order_out, 4)) return fail(SPOPS_ERR_INVALID_ARG, "order_out is NULL or misaligned");
+    const PlanView v = plan_view(const_cast<void*>(plan), m, n, nnz);
+    if (!v.panels) return fail(SPOPS_ERR_UNSUPPORTED, "the plan of an m x %d mask has no panels (n > 65536)", n);
+    return cuda_status(cudaMemcpyAsync(order_out, v.prow, (size_t)m * sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                                       (cudaStream_t)stream),
+                       "plan_row_order copy");
+}
+
 size_t spops_spmm_workspace_size(int32_t m, int32_t k, int32_t n, int32_t nnz, int dtype, int itype) {
     (void)itype;
     return spmm_workspace_bytes(m, k, n, nnz, dtype);

@@ -116,6 +116,12 @@ __device__ __forceinline__ uint4 ld_v4(const void* p) {
 
 // ------------------------------------------------------------------ shared memory / mbarrier
 
+// Barrier `id` (1 .. 15; 0 is __syncthreads) over the first nthreads threads of the CTA
+// (a multiple of 32; every one of them must arrive).
+__device__ __forceinline__ void named_barrier(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

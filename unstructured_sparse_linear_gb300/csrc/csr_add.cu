@@ -11,6 +11,12 @@
 // of the row-major matrix, so the only alignment requirement is a 16-byte aligned B and
 // C; otherwise a plain-load variant of the same kernel runs.
 //
+// A tile covers the tail of row r0, whole rows and the head of row r1. Columns increase
+// inside a row, so when an edge row holds more than kSearchMin entries two warps find the
+// tile's first entry in r0 and its end in r1 by a 32-way search (each step one load per
+// lane and a ballot), and a row wider than a tile is scanned once in total, not once per
+// tile it spans.
+//
 // Each entry is added in fp32 and rounded once to T. For fp32 that is the IEEE sum. For
 // fp16/bf16 the fp32 sum of two such values is rounded twice (to fp32, then to T), which
 // gives the correctly rounded result because fp32 has at least 2p+2 significand bits
@@ -27,6 +33,28 @@ constexpr int kAddStages = 3;
 constexpr int kAddSmem = kAddTileBytes * kAddStages;
 constexpr int kRoCache = 512;  // row offsets of a tile kept in shared memory (tiles spanning fewer rows)
 constexpr int kPre = 4;        // entries per thread loaded before the tile arrives
+constexpr int kSearchMin = 2 * kAddThreads;  // edge rows with more entries are searched
+
+// First k in [lo, hi) with col[k] >= c (hi if none), columns increasing; all 32 lanes call it
+// with the same arguments and get the same result. Each step samples 32 evenly spaced
+// entries and keeps the gap in which the columns reach c.
+template <typename I>
+__device__ __forceinline__ int32_t warp_lower_bound(const I* __restrict__ col, int32_t lo, int32_t hi, int32_t c,
+                                                    int lane) {
+    while (hi - lo > 32) {
+        const int32_t step = (hi - lo + 31) / 32;
+        const int32_t x = lo + lane * step;
+        const bool below = x < hi && idx_of(col[x]) < c;
+        const int cnt = __popc(__ballot_sync(0xffffffffu, below));
+        if (cnt == 0) return lo;
+        const int32_t nlo = lo + (cnt - 1) * step + 1;
+        hi = min(hi, lo + cnt * step);
+        lo = nlo;
+    }
+    const int32_t x = lo + lane;
+    const bool below = x < hi && idx_of(col[x]) < c;
+    return lo + __popc(__ballot_sync(0xffffffffu, below));
+}
 
 template <typename T, typename I, bool kBulk>
 __global__ void __launch_bounds__(kAddThreads) csr_add_kernel(const T* __restrict__ vals,
@@ -36,6 +64,7 @@ __global__ void __launch_bounds__(kAddThreads) csr_add_kernel(const T* __restric
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ __align__(8) uint64_t full_bar[kAddStages];
     __shared__ int32_t ro_s[kRoCache];
+    __shared__ int32_t s_edge[2];
     constexpr int64_t E = kAddTileBytes / sizeof(T);
     const int tid = threadIdx.x;
     pdl_trigger();
@@ -80,8 +109,24 @@ __global__ void __launch_bounds__(kAddThreads) csr_add_kernel(const T* __restric
         if (cached)
             for (int x = tid; x < nro; x += kAddThreads) ro_s[x] = ro[r0 + x];
         __syncthreads();
-        const int32_t kb = cached ? ro_s[0] : ro[r0];
-        const int32_t ke = cached ? ro_s[nro - 1] : ro[r1 + 1];
+        int32_t kb = cached ? ro_s[0] : ro[r0];
+        int32_t ke = cached ? ro_s[nro - 1] : ro[r1 + 1];
+        {
+            // entries of r0 before the tile's first column and of r1 from its end column on
+            const int32_t r0_end = cached ? ro_s[1] : ro[r0 + 1];
+            const int32_t r1_beg = cached ? ro_s[nro - 2] : ro[r1];
+            const bool w0 = r0_end - kb > kSearchMin, w1 = ke - r1_beg > kSearchMin;
+            if (w0 || w1) {  // uniform over the CTA
+                const int warp = tid >> 5, lane = tid & 31;
+                if (warp == 0 && w0)
+                    s_edge[0] = warp_lower_bound(col, kb, r0_end, (int32_t)(f0 - (int64_t)r0 * n), lane);
+                if (warp == 1 && w1)
+                    s_edge[1] = warp_lower_bound(col, r1_beg, ke, (int32_t)(f1 - (int64_t)r1 * n), lane);
+                __syncthreads();
+                if (w0) kb = s_edge[0];
+                if (w1) ke = s_edge[1];  // s_edge is next written after two more barriers
+            }
+        }
         auto row_of = [&](int32_t k) {  // largest r in [r0, r1] with ro[r] <= k
             int32_t lo = 0, hi = nro - 2;
             while (lo < hi) {

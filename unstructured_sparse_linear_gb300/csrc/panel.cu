@@ -632,24 +632,29 @@ sddmm_group_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
 
 // ------------------------------------------------------------------ SpMM dense panels
 
-// The 16 image rows of one row group: zeros, then the group's values at their U position,
-// written out as whole 128-byte-swizzled K-major rows (16-byte stores).
-constexpr uint32_t kDensifySmem = kGroupRows * kUList * 2;  // the group's rows, 16-bit values
+// The 8 image rows of one row group: zeros, then the group's values at their U position,
+// written out as whole 128-byte-swizzled K-major rows (16-byte stores). The staging rows are
+// ucap = min(kUList, K rounded up to 64) values long (U is a set of the K columns), so that
+// narrow matrices leave room for more CTAs per SM.
+inline uint32_t densify_smem_bytes(int32_t K, size_t elt) {
+    const int32_t ucap = (int32_t)min64(kUList, ((int64_t)K + kKC - 1) / kKC * kKC);
+    return (uint32_t)(kGroupRows * (size_t)ucap * elt);
+}
 
 template <typename T>
 __global__ void __launch_bounds__(256) densify_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro,
-                                                     T* __restrict__ img_base, PlanView v) {
+                                                     T* __restrict__ img_base, PlanView v, int ucap) {
     extern __shared__ __align__(16) uint8_t densify_smem[];
-    T(*stage)[kUList] = reinterpret_cast<T(*)[kUList]>(densify_smem);
+    T* stage = reinterpret_cast<T*>(densify_smem);  // [kGroupRows][ucap]
     pdl_trigger();
     pdl_wait();
     const int p = blockIdx.x / kGroups, grp = blockIdx.x % kGroups;
     if (!v.sp_dense[p]) return;
     const int nU = v.desc[p].y;
-    const int upad = (nU + kKC - 1) / kKC * kKC;
+    const int upad = (nU + kKC - 1) / kKC * kKC;  // <= ucap
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    uint4* st4 = reinterpret_cast<uint4*>(&stage[0][0]);
-    const int row_vec = kUList * (int)sizeof(T) / 16;
+    uint4* st4 = reinterpret_cast<uint4*>(stage);
+    const int row_vec = ucap * (int)sizeof(T) / 16;
     for (int x = tid; x < kGroupRows * row_vec; x += 256) {
         if ((x % row_vec) * 16 < upad * (int)sizeof(T)) st4[x] = make_uint4(0, 0, 0, 0);
     }
@@ -672,7 +677,7 @@ __global__ void __launch_bounds__(256) densify_kernel(const T* __restrict__ vals
             }
 #pragma unroll
             for (int j = 0; j < kB; ++j)
-                if (u[j] >= 0) stage[lr][u[j]] = x[j];
+                if (u[j] >= 0) stage[lr * ucap + u[j]] = x[j];
         }
     }
     __syncthreads();
@@ -684,7 +689,7 @@ __global__ void __launch_bounds__(256) densify_kernel(const T* __restrict__ vals
         const int kc = c / 8, w = c % 8;               // 64-column chunk, 16-byte piece in it
         uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<char*>(img + (size_t)kc * kPM * kKC) +
                                               tc::sw128_off(r, w));
-        *dst = reinterpret_cast<const uint4*>(&stage[lr][0])[c];
+        *dst = reinterpret_cast<const uint4*>(stage + lr * ucap)[c];
     }
 }
 
@@ -843,16 +848,18 @@ spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restric
 //               accumulator (256 columns, in two halves), frees it, converts each half to
 //               the output dtype into its own shared row and sends it to C with one bulk
 //               async copy;
-//   warps 4-7   producers: per 64-wide K chunk, one bulk async copy of the image chunk
-//               (16 KB, contiguous, already swizzled) and the chunk's 64 rows of B (256
-//               columns): when they are 64 consecutive rows (block-structured masks), four
+//   warps 4-6   producers: per 64-wide K chunk, one bulk async copy of the image chunk
+//               (16 KB, contiguous, already swizzled; a panel of |U| <= 256 keeps its whole
+//               image in four slots, loaded with its first unit in the CTA only) and the
+//               chunk's 64 rows of B (256 columns): when they are 64 consecutive rows
+//               (block-structured masks), four
 //               TMA tile loads (64 x 64 boxes, 128-byte swizzle) straight into the MN-major
 //               operand layout;
 //               otherwise a gather (cp.async, 16 bytes each) whose completion is signalled
 //               on the stage's mbarrier (cp.async.mbarrier.arrive.noinc). Each producer warp
 //               keeps its own shared copy of the panel's U list (no barrier between the
 //               producer warps);
-//   warp 8      TMEM owner and MMA issuer (one thread): 4 MMAs (M = 128, N = 256, K = 16)
+//   warp 7      TMEM owner and MMA issuer (one thread): 4 MMAs (M = 128, N = 256, K = 16)
 //               per chunk, a commit that
 //               frees the stage, and a commit per unit that hands the accumulator to the
 //               epilogue.
@@ -863,8 +870,13 @@ spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restric
 // stops, and the others then give up on their next wait.
 constexpr int kWsNT = 256;                                     // columns of C per unit (UMMA N)
 constexpr uint32_t kWsStageB = kKC * kWsNT * 2;                // 32 KB
-constexpr uint32_t kWsStageBytes = kSpStageA + kWsStageB;      // 48 KB
 constexpr int kWsStages = 3;
+// Image chunk slots: a panel of at most kWsASlots chunks (|U| <= 256) loads its image once
+// per run of its units in a CTA and keeps it (slot j = chunk j); a larger panel streams its
+// chunks through slots 0 .. kWsStages - 1 beside the B stages.
+constexpr int kWsASlots = 4;
+constexpr uint32_t kWsAReg = kWsASlots * kSpStageA;            // 64 KB
+static_assert(kWsASlots >= kWsStages, "a streamed chunk uses the slot of its stage");
 constexpr int kWsEpiWarps = 4;
 // One producer warp per stage: chunk g goes to stage g mod 3 and warp g mod 3, so a warp only
 // ever waits for the consumption of its own previous chunk (one barrier phase back; a parity
@@ -873,7 +885,7 @@ constexpr int kWsProdWarps = kWsStages;
 constexpr int kWsThreads = (kWsEpiWarps + kWsProdWarps + 1) * 32;
 constexpr uint32_t kWsCStage = kPM * kSpCRowBytes;  // staged C half rows (128 columns)
 constexpr uint32_t kWsUList = kUList * 2;           // one producer warp's copy of a U list (16-bit columns)
-constexpr uint32_t kWsSmem = kWsStages * kWsStageBytes + kWsCStage + kWsProdWarps * kWsUList + 1024;
+constexpr uint32_t kWsSmem = kWsAReg + kWsStages * kWsStageB + kWsCStage + kWsProdWarps * kWsUList + 1024;
 static_assert(kWsSmem <= 227 * 1024, "warp-specialized SpMM shared memory");
 
 
@@ -885,8 +897,9 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
     __shared__ __align__(8) uint64_t full_bar[kWsStages], empty_bar[kWsStages], tfull_bar[2], tempty_bar[2], drain_bar;
     __shared__ uint32_t tmem_base_sh;
     uint8_t* smem = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(smem_raw), 1024));
-    const uint32_t sbase = smem_u32(smem);
-    const uint32_t cstage = sbase + kWsStages * kWsStageBytes;
+    const uint32_t sbase = smem_u32(smem);                 // image slots
+    const uint32_t bbase = sbase + kWsAReg;                 // B stages
+    const uint32_t cstage = bbase + kWsStages * kWsStageB;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pdl_trigger();
 
@@ -972,20 +985,35 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
         // the tile-path test is a per-panel bit mask in registers, so no shared-memory loads
         // sit in the tile path's loop (they are slow while the tensor core reads operands).
         const int pw = warp - kWsEpiWarps;
-        uint16_t* s_u = reinterpret_cast<uint16_t*>(smem + kWsStages * kWsStageBytes + kWsCStage + pw * kWsUList);
+        uint16_t* s_u = reinterpret_cast<uint16_t*>(smem + kWsAReg + kWsStages * kWsStageB + kWsCStage + pw * kWsUList);
         constexpr int kPieces = kWsNT / 8;  // 16-byte pieces per B row of the tile
-        uint32_t g = 0;
+        uint32_t g = 0, t = 0;
         bool ok = true;
         int64_t cur = -1;
         int nU = 0, nk = 0;
+        bool resident = false, load_a = true;
         uint64_t tile_mask = 0;  // bit j: chunk j of the panel loads B as tiles
         const T* img = img_base;
-        for (int64_t unit = u_begin; unit < u_end && ok; ++unit) {
+        for (int64_t unit = u_begin; unit < u_end && ok; ++unit, ++t) {
             if (unit / ntn != cur) {  // a new panel: its U list into this warp's shared copy
                 cur = unit / ntn;
                 const int p = v.dlist_sp[cur];
                 nU = v.desc[p].y;
                 nk = (nU + kKC - 1) / kKC;
+                const bool was_resident = resident;
+                resident = nk <= kWsASlots;
+                load_a = true;
+                // Image slots change meaning: the previous unit's MMAs, which may still read
+                // any slot, complete before this panel's chunks overwrite one. (The next
+                // completion of that barrier needs this unit's chunks, so the wait cannot
+                // alias a later phase.)
+                if (t > 0 && (resident || was_resident)) {
+                    const uint32_t tp = t - 1;
+                    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull_bar[tp & 1u]), (tp >> 1) & 1u, err))) {
+                        ok = false;
+                        break;
+                    }
+                }
                 img = img_base + v.img_slot[p];
                 const int32_t* ul = v.ulist + (size_t)p * kUList;
                 __syncwarp();  // the previous panel's copy has been read by the whole warp
@@ -1003,6 +1031,8 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
                 static_assert(kUList / kKC <= 64, "one mask bit per chunk");
                 tile_mask = ((uint64_t)hi << 32) | lo;
                 __syncwarp();
+            } else if (resident) {
+                load_a = false;  // the panel's image is already in its slots
             }
             const int n0 = (int)(unit % ntn) * kWsNT;  // the tile's first column
             for (int j = 0; j < nk; ++j, ++g) {
@@ -1014,21 +1044,23 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
                     ok = false;
                     break;
                 }
-                const uint32_t sa = sbase + st * kWsStageBytes;
+                const uint32_t sb = bbase + st * kWsStageB;
+                const uint32_t sa = sbase + (resident ? (uint32_t)j : st) * kSpStageA;
+                const uint32_t abytes = load_a ? kSpStageA : 0u;
                 const uint32_t fb = smem_u32(&full_bar[st]);
                 const T* img_j = img + (size_t)j * kPM * kKC;
                 if ((tile_mask >> j) & 1u) {
                     if (lane == 0) {
                         const int u0 = s_u[j * kKC];
-                        mbar_arrive_expect_tx(fb, kWsStageBytes);
-                        bulk_g2s(sa, img_j, kSpStageA, fb);
+                        mbar_arrive_expect_tx(fb, abytes + kWsStageB);
+                        if (load_a) bulk_g2s(sa, img_j, kSpStageA, fb);
 #pragma unroll
                         for (int bx = 0; bx < kWsNT / 64; ++bx)
-                            tma_load_2d(sa + kSpStageA + bx * (kKC / 8) * 1024, &tmap_b, n0 + 64 * bx, u0, fb);
+                            tma_load_2d(sb + bx * (kKC / 8) * 1024, &tmap_b, n0 + 64 * bx, u0, fb);
                     }
                     continue;
                 }
-                if (lane == 0) {
+                if (lane == 0 && load_a) {
                     asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(fb), "r"(kSpStageA) : "memory");
                     bulk_g2s(sa, img_j, kSpStageA, fb);
                 }
@@ -1039,7 +1071,7 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
                     const bool in = j * kKC + kk < nU && ncol < N;
                     const int u = in ? (int)s_u[j * kKC + kk] : 0;
                     const uint32_t off = (uint32_t)(nch >> 3) * (kKC / 8 * 1024) + tc::sw128_off(kk, nch & 7);
-                    tc::cp_async16(sa + kSpStageA + off, in ? (const void*)(B + (int64_t)u * N + ncol) : (const void*)B,
+                    tc::cp_async16(sb + off, in ? (const void*)(B + (int64_t)u * N + ncol) : (const void*)B,
                                    in ? 16 : 0);
                 }
                 tc::cp_async_commit();   // wait_group covers committed groups only
@@ -1053,20 +1085,21 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
         // ---------------- MMA issuer
         // Descriptors of each stage's first K step; K step kk adds 32 B (A) or 2 KB (B) to
         // the 16-byte-unit start address in the low bits (no carry: shared addresses < 256 KB).
-        uint64_t ad0[kWsStages], bd0[kWsStages];
+        uint64_t ad0[kWsASlots], bd0[kWsStages];
 #pragma unroll
-        for (int i = 0; i < kWsStages; ++i) {
-            ad0[i] = tc::smem_desc_sw128(sbase + i * kWsStageBytes, 16, 1024);
-            bd0[i] = tc::smem_desc_sw128(sbase + i * kWsStageBytes + kSpStageA, kKC / 8 * 1024, 1024);
-        }
+        for (int i = 0; i < kWsASlots; ++i) ad0[i] = tc::smem_desc_sw128(sbase + i * kSpStageA, 16, 1024);
+#pragma unroll
+        for (int i = 0; i < kWsStages; ++i) bd0[i] = tc::smem_desc_sw128(bbase + i * kWsStageB, kKC / 8 * 1024, 1024);
         uint32_t g = 0, t = 0, st = 0, ph = 0;  // chunk count, unit count, stage, stage parity
         bool ok = true;
         int64_t cur = -1;
         int nk = 0;
+        bool resident = false;
         for (int64_t unit = u_begin; unit < u_end && ok; ++unit, ++t) {
             if (unit / ntn != cur) {
                 cur = unit / ntn;
                 nk = (v.desc[v.dlist_sp[cur]].y + kKC - 1) / kKC;
+                resident = nk <= kWsASlots;
             }
             const uint32_t a = t & 1u;
             if (!mbar_wait(smem_u32(&tempty_bar[a]), ((t >> 1) + 1) & 1u, err)) break;
@@ -1079,13 +1112,14 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
                 }
                 fence_proxy_async_smem();  // cp.async data (generic proxy) before the tensor core reads it
                 tc::fence_after_sync();
+                const uint32_t slot = resident ? (uint32_t)j : st;  // j < kWsASlots when resident
                 uint64_t ad = ad0[0], bd = bd0[0];
 #pragma unroll
+                for (int i = 1; i < kWsASlots; ++i)
+                    if (slot == (uint32_t)i) ad = ad0[i];
+#pragma unroll
                 for (int i = 1; i < kWsStages; ++i)
-                    if (st == (uint32_t)i) {
-                        ad = ad0[i];
-                        bd = bd0[i];
-                    }
+                    if (st == (uint32_t)i) bd = bd0[i];
                 tc::mma_f16(acc, ad, bd, idesc, j > 0 ? 1u : 0u);
 #pragma unroll
                 for (int kk = 1; kk < kKC / 16; ++kk)
@@ -1217,10 +1251,11 @@ cudaError_t run_sddmm_panels(const void* A, const void* BT, void* out, int32_t k
 template <typename T>
 cudaError_t run_spmm_panels(const void* vals, const int32_t* ro, const void* B, int32_t K, int32_t N, void* C,
                             void* img, const PlanView& v, cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(densify_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDensifySmem);
+    const uint32_t dsmem = densify_smem_bytes(K, sizeof(T));
+    cudaError_t e = cudaFuncSetAttribute(densify_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsmem);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(densify_kernel<T>, v.P * kGroups, 256, kDensifySmem, s, static_cast<const T*>(vals), ro,
-                   static_cast<T*>(img), v);
+    e = launch_pdl(densify_kernel<T>, v.P * kGroups, 256, dsmem, s, static_cast<const T*>(vals), ro,
+                   static_cast<T*>(img), v, (int)(dsmem / (kGroupRows * sizeof(T))));
     if (e != cudaSuccess) return e;
     const int ntn = (N + kSpNT - 1) / kSpNT;
     const uint32_t idesc_ws = tc::instr_desc_f16(std::is_same<T, __nv_bfloat16>::value ? 1u : 0u, 0, 1, kPM, kWsNT);

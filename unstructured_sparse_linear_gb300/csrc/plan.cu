@@ -97,25 +97,57 @@ __device__ __forceinline__ void or_bits_aggregated(uint32_t* bm, const int (&x)[
     }
 }
 
+// Set bit x (x >= 0; -1: nothing) of the shared bitmap bm, called by all 32 lanes. When every
+// lane's bit falls in one word (a 32-column slice of one row of a block-structured mask) the
+// warp ORs them together and one lane does the atomic; otherwise every lane does its own
+// (sparse rows rarely collide, and the hardware handles a few lanes on one word well).
+__device__ __forceinline__ void or_bit_warp(uint32_t* bm, int x, int lane) {
+    const int w = x >= 0 ? x >> 5 : -1;
+    const uint32_t bit = x >= 0 ? 1u << (x & 31) : 0u;
+    const int w0 = __shfl_sync(0xffffffffu, w, 0);
+    if (__all_sync(0xffffffffu, w == w0 && w0 >= 0)) {
+        const uint32_t b = __reduce_or_sync(0xffffffffu, bit);
+        if (lane == 0) atomicOr(&bm[w0], b);
+    } else if (x >= 0) {
+        atomicOr(&bm[w], bit);
+    }
+}
+
 // ---- 0. row order (masks of at most kOrderMaxRows rows): row_idx refined so that rows with
 // the same column set become neighbours. Rows of a block-structured mask that share their
 // blocks then fill the same panel, whose U is exactly their columns (the butterfly layer's
-// 64-row block-rows r, r + 32, ... share four blocks). One CTA sorts the positions of
-// row_idx stably by (nnz descending, signature) with an LSD radix sort and writes the order
-// to prow. The signature is a 16-bit hash of the row's first, middle and last column: rows
-// with the same column set always agree on it, and rows that agree on it with different
-// sets only share a panel (its U covers both), so no result depends on it. The sort is
-// skipped (prow = row_idx) when no aligned window of kOrdMinRun positions of row_idx holds
-// equal non-zero counts (then no panel half can be filled by rows of one pattern).
+// 64-row block-rows r, r + 32, ... share four blocks). The positions of row_idx are sorted
+// stably by (nnz descending, signature); the signature is a 16-bit hash of the row's first,
+// middle and last column: rows with the same column set always agree on it, and rows that
+// agree on it with different sets only share a panel (its U covers both), so no result
+// depends on it. The sort runs only where it can merge panels: when two runs of row_idx
+// (maximal stretches of positions whose non-empty rows have one key) of at least
+// kOrdLongRun positions each have the same key, i.e. a column pattern recurs in separate
+// places (the butterfly's block-rows r and r + 32). A random mask has no such runs; a
+// clustered one keeps its repeated rows in one run already. Otherwise prow = row_idx and the
+// panels are as without an order. Two kernels:
+//   a. keys, one thread per position over the whole GPU (these are the gathers: the row's
+//      offsets and three of its columns): prow = row_idx (-1 past m), the key of each
+//      position, and per block of 32 positions the key of the long run that starts in it (or
+//      none), so that the second kernel tests for a repeated key before loading anything;
+//   b. one CTA: the repeated-key test; then coalesced loads of rows and keys into shared
+//      memory and the runs, stably sorted by key with a bitonic network over (key, run)
+//      pairs (at most 1024 runs), else a stable LSD radix sort of the positions with 8-bit
+//      digits, skipping digits that are the same in every key.
+constexpr int kKeyThreads = 256;
 constexpr int kOrdThreads = 1024;
 constexpr int kOrdWarps = kOrdThreads / 32;
-constexpr int kOrdPer = kOrderMaxRows / kOrdThreads;  // positions per thread
 constexpr int kOrdBins = 256;
-constexpr int kOrdMinRun = kPM / 2;
+constexpr int kOrdLongRun = 32;
+constexpr int kOrdHash = 2 * kOrderMaxRows / kOrdLongRun;  // slots for the keys of the long runs
+constexpr uint32_t kNoKey = 0xFFFFFFFFu;                    // no non-empty row has this key
 constexpr size_t kOrdSmem = (size_t)kOrderMaxRows * 4      // keys, by row
-                            + (size_t)kOrderMaxRows * 4    // first entry, by position
                             + (size_t)kOrderMaxRows * 2 * 2  // rows, two buffers
-                            + (size_t)kOrdWarps * kOrdBins * 4;
+                            + (size_t)kOrdWarps * kOrdBins * 4;  // digit counts, or the runs
+static_assert((size_t)kOrdWarps * kOrdBins * 4 >= kOrdThreads * 8 + (2 * kOrdThreads + 2) * 4,
+              "the run arrays fit in the digit counts");
+static_assert(kOrderMaxRows / 32 <= kOrdThreads, "one word of break flags per thread");
+static_assert(kOrderMaxRows % kOrdThreads == 0, "positions per thread");
 
 __device__ __forceinline__ uint32_t mix_col(uint32_t c) {
     uint32_t h = c * 0x9E3779B1u;
@@ -131,177 +163,291 @@ __device__ __forceinline__ uint32_t row_signature(uint32_t first, uint32_t mid, 
     return (h >> 16) ^ (h & 0xFFFFu);
 }
 
+// Sort key of a row with len entries: nnz descending (complemented, rows of 65535 entries or
+// more tie), then the signature.
+__device__ __forceinline__ uint32_t order_key(int32_t len, uint32_t sig) {
+    return ((uint32_t)(0xFFFF - min(len, 0xFFFF)) << 16) | sig;
+}
+
 template <typename I>
-__global__ void __launch_bounds__(kOrdThreads, 1)
-plan_order_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx, const I* __restrict__ col,
-                  PlanView v) {
+__global__ void __launch_bounds__(kKeyThreads)
+plan_keys_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx, const I* __restrict__ col,
+                 PlanView v) {
+    // keys of positions base - 1 .. base + kKeyThreads + kOrdLongRun - 1 (the run checks of
+    // this CTA's positions read up to kOrdLongRun - 1 positions past its end)
+    __shared__ uint32_t s_key[kKeyThreads + kOrdLongRun + 1];
+    __shared__ uint32_t s_brk[kKeyThreads / 32 + 1];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int base = blockIdx.x * kKeyThreads;
+    const int m = v.m;
+    pdl_trigger();
+    pdl_wait();
+    // this thread's position p0, and for threads 0 .. kOrdLongRun a halo position p1 (past the
+    // end, or base - 1); both keys are gathered together
+    const int p0 = base + tid;
+    const int p1 = tid < kOrdLongRun ? base + kKeyThreads + tid : (tid == kOrdLongRun ? base - 1 : -1);
+    const int r0 = p0 < m ? idx_of(row_idx[p0]) : -1;
+    const int r1 = p1 >= 0 && p1 < m ? idx_of(row_idx[p1]) : -1;
+    const int32_t a0 = r0 >= 0 ? ro[r0] : 0, a1 = r1 >= 0 ? ro[r1] : 0;
+    const int32_t l0 = r0 >= 0 ? ro[r0 + 1] - a0 : 0, l1 = r1 >= 0 ? ro[r1 + 1] - a1 : 0;
+    uint32_t c[6] = {0, 0, 0, 0, 0, 0};
+    if (l0 > 0) {
+        c[0] = (uint32_t)idx_of(col[a0]);
+        c[1] = (uint32_t)idx_of(col[a0 + l0 / 2]);
+        c[2] = (uint32_t)idx_of(col[a0 + l0 - 1]);
+    }
+    if (l1 > 0) {
+        c[3] = (uint32_t)idx_of(col[a1]);
+        c[4] = (uint32_t)idx_of(col[a1 + l1 / 2]);
+        c[5] = (uint32_t)idx_of(col[a1 + l1 - 1]);
+    }
+    const uint32_t k0 = r0 >= 0 ? order_key(l0, l0 > 0 ? row_signature(c[0], c[1], c[2]) : 0u) : kNoKey;
+    const uint32_t k1 = r1 >= 0 ? order_key(l1, l1 > 0 ? row_signature(c[3], c[4], c[5]) : 0u) : kNoKey;
+    if (p0 < v.P * kPM) v.prow[p0] = r0;
+    if (p0 < m) v.okey[p0] = k0;
+    s_key[1 + tid] = k0;
+    if (tid < kOrdLongRun) s_key[1 + kKeyThreads + tid] = k1;
+    if (tid == kOrdLongRun) s_key[0] = k1;
+    __syncthreads();
+    // breaks (a position whose key differs from the one before) at base + j, j < 256 + 32
+    {
+        const int j = tid;
+        const bool b = base + j < m && (base + j == 0 || s_key[1 + j] != s_key[j]);
+        const uint32_t word = __ballot_sync(0xffffffffu, b);
+        if (lane == 0) s_brk[warp] = word;
+        if (warp == 0) {
+            const int jh = kKeyThreads + lane;
+            const bool bh = base + jh < m && s_key[1 + jh] != s_key[jh];
+            const uint32_t wh = __ballot_sync(0xffffffffu, bh);
+            if (lane == 0) s_brk[kKeyThreads / 32] = wh;
+        }
+    }
+    __syncthreads();
+    // a long run of a non-empty key starts at p0: a break with no break in the next 31
+    // positions; two such starts are 32 apart, so a block of 32 positions holds one at most
+    static_assert(kOrdLongRun == 32, "one 32-bit window of break flags, one long run per 32 positions");
+    uint32_t win = s_brk[warp] >> lane;
+    if (lane) win |= s_brk[warp + 1] << (32 - lane);
+    const bool lng = win == 1u && p0 + kOrdLongRun <= m && (k0 >> 16) != 0xFFFFu;
+    const uint32_t lb = __ballot_sync(0xffffffffu, lng);
+    const int blk = blockIdx.x * (kKeyThreads / 32) + warp;
+    if (lane == 0 && blk < v.P * kPM / 32) {
+        v.olong[blk] = lb ? s_key[1 + warp * 32 + __ffs(lb) - 1] : kNoKey;
+        v.obrk[blk] = s_brk[warp];
+    }
+}
+
+__global__ void __launch_bounds__(kOrdThreads, 1) plan_sort_kernel(PlanView v) {
     extern __shared__ __align__(16) uint8_t osm[];
-    uint32_t* key = reinterpret_cast<uint32_t*>(osm);
-    int32_t* first = reinterpret_cast<int32_t*>(key + kOrderMaxRows);
-    uint16_t* va = reinterpret_cast<uint16_t*>(first + kOrderMaxRows);
+    uint32_t* key = reinterpret_cast<uint32_t*>(osm);  // by row
+    uint16_t* va = reinterpret_cast<uint16_t*>(key + kOrderMaxRows);
     uint16_t* vb = va + kOrderMaxRows;
     uint32_t(*wcnt)[kOrdBins] = reinterpret_cast<uint32_t(*)[kOrdBins]>(vb + kOrderMaxRows);
-    __shared__ int red[3][kOrdWarps];
+    __shared__ uint32_t s_var[kOrdWarps];
+    __shared__ uint32_t brk[kOrderMaxRows / 32];
+    __shared__ int wpre[kOrderMaxRows / 32];  // runs starting before each word of brk
+    __shared__ uint32_t s_hash[kOrdHash];
     __shared__ int sh[32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int m = v.m;
     pdl_trigger();
     pdl_wait();
-
-    // 1. each thread's positions p = tid + q * kOrdThreads: rows, then their offsets, each
-    // batch of loads issued together
-    int r[kOrdPer];
-    int32_t a[kOrdPer], b[kOrdPer];
+    // a repeated key among the long runs (at most one per 32 positions, so at most m / 32
+    // keys in 2 m / 32 hash slots)
+    for (int i = tid; i < kOrdHash; i += kOrdThreads) s_hash[i] = kNoKey;
+    __syncthreads();
+    int dup = 0;
+    for (int b = tid; b < (m + 31) / 32; b += kOrdThreads) {
+        const uint32_t k = v.olong[b];
+        if (k == kNoKey) continue;
+        uint32_t h = mix_col(k) & (kOrdHash - 1);
+        for (int t = 0; t < kOrdHash; ++t) {
+            const uint32_t old = atomicCAS(&s_hash[h], kNoKey, k);
+            if (old == kNoKey) break;
+            if (old == k) {
+                dup = 1;
+                break;
+            }
+            h = (h + 1) & (kOrdHash - 1);
+        }
+    }
+    if (!__syncthreads_or(dup)) return;  // prow already holds row_idx
+    // rows and keys (all of a thread's loads issued before any is used); the bits in which
+    // some key differs from the first
+    constexpr int kPer = kOrderMaxRows / kOrdThreads;
+    const uint32_t k0 = v.okey[0];
+    uint32_t var = 0;
+    int rq[kPer];
+    uint32_t kq[kPer];
 #pragma unroll
-    for (int q = 0; q < kOrdPer; ++q) {
+    for (int q = 0; q < kPer; ++q) {
         const int p = tid + q * kOrdThreads;
-        r[q] = p < m ? idx_of(row_idx[p]) : -1;
+        rq[q] = p < m ? v.prow[p] : -1;
+        kq[q] = p < m ? v.okey[p] : k0;
     }
 #pragma unroll
-    for (int q = 0; q < kOrdPer; ++q) {
-        a[q] = r[q] >= 0 ? ro[r[q]] : 0;
-        b[q] = r[q] >= 0 ? ro[r[q] + 1] : 0;
+    for (int q = 0; q < kPer; ++q) {
+        if (rq[q] < 0) continue;
+        key[rq[q]] = kq[q];
+        va[tid + q * kOrdThreads] = (uint16_t)rq[q];
+        var |= kq[q] ^ k0;
     }
-    int mx = 0, mn = INT32_MAX, run_ok = 0;
-#pragma unroll
-    for (int q = 0; q < kOrdPer; ++q) {
-        if (r[q] < 0) continue;
-        va[tid + q * kOrdThreads] = (uint16_t)r[q];
-        first[tid + q * kOrdThreads] = a[q];
-        key[r[q]] = (uint32_t)(b[q] - a[q]);  // the count for now; the full key below
-        mx = max(mx, b[q] - a[q]);
-        mn = min(mn, b[q] - a[q]);
-    }
+    // run breaks, from the keys kernel: bit p of brk is set when position p starts a
+    // stretch of one key (p = 0 or its key differs from position p - 1)
+    for (int w = tid; w < (m + 31) / 32; w += kOrdThreads) brk[w] = v.obrk[w];
+    for (int o = 16; o; o >>= 1) var |= __shfl_xor_sync(0xffffffffu, var, o);
+    if (lane == 0) s_var[warp] = var;
+    __syncthreads();  // keys, rows and breaks are in place
+    var = 0;
+    for (int w = 0; w < kOrdWarps; ++w) var |= s_var[w];
+    if (var == 0) return;  // one key: the order is row_idx
     __syncthreads();
-    // 2. an aligned window of kOrdMinRun equal non-zero counts along row_idx
-    for (int p = tid * kOrdMinRun; p + kOrdMinRun <= m; p += kOrdThreads * kOrdMinRun) {
-        const uint32_t l0 = key[va[p]];
-        bool same = l0 > 0;
-        for (int q = 1; q < kOrdMinRun && same; ++q) same = key[va[p + q]] == l0;
-        run_ok |= same;
+    // The stretches of one key (runs) in row_idx order: a stable sort of the positions by key
+    // keeps each run together and in place relative to the other runs of its key, so it is
+    // the runs, stably sorted by key, laid end to end. With at most kOrdThreads runs they are
+    // sorted as (key, run index) pairs by one bitonic network; more runs take the radix sort
+    // of the positions below.
+    const int nwords = (m + 31) / 32;
+    int total_runs;
+    {
+        const int c = tid < nwords ? __popc(brk[tid]) : 0;
+        const int before = block_exclusive_scan(c, sh, &total_runs);
+        if (tid < nwords) wpre[tid] = before;
     }
-    for (int o = 16; o; o >>= 1) {
-        mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-        run_ok |= __shfl_xor_sync(0xffffffffu, run_ok, o);
-    }
-    if (lane == 0) {
-        red[0][warp] = mx;
-        red[1][warp] = mn;
-        red[2][warp] = run_ok;
-    }
-    __syncthreads();
-    mx = 0;
-    mn = INT32_MAX;
-    run_ok = 0;
-    for (int w = 0; w < kOrdWarps; ++w) {
-        mx = max(mx, red[0][w]);
-        mn = min(mn, red[1][w]);
-        run_ok |= red[2][w];
-    }
-    if (run_ok) {
-        // 3. keys (nnz descending, then signature): the three column loads of half of this
-        // thread's positions together, then the other half
-        constexpr int kHalf = kOrdPer / 2;
-#pragma unroll
-        for (int hq = 0; hq < kOrdPer; hq += kHalf) {
-            int rr[kHalf], len[kHalf];
-            uint32_t c0[kHalf], c1[kHalf], c2[kHalf];
-#pragma unroll
-            for (int q = 0; q < kHalf; ++q) {
-                const int p = tid + (hq + q) * kOrdThreads;
-                rr[q] = p < m ? (int)va[p] : -1;
-                const int32_t a0 = p < m ? first[p] : 0;
-                len[q] = rr[q] >= 0 ? (int)key[rr[q]] : 0;
-                const bool ne = len[q] > 0;
-                c0[q] = ne ? (uint32_t)idx_of(col[a0]) : 0u;
-                c1[q] = ne ? (uint32_t)idx_of(col[a0 + len[q] / 2]) : 0u;
-                c2[q] = ne ? (uint32_t)idx_of(col[a0 + len[q] - 1]) : 0u;
-            }
-#pragma unroll
-            for (int q = 0; q < kHalf; ++q) {
-                if (rr[q] < 0) continue;
-                const uint32_t sg = len[q] > 0 ? row_signature(c0[q], c1[q], c2[q]) : 0u;
-                key[rr[q]] = ((uint32_t)min(mx - len[q], 0xFFFF) << 16) | sg;
+    if (total_runs <= kOrdThreads) {
+        const int R = total_runs;
+        unsigned long long* sk = reinterpret_cast<unsigned long long*>(&wcnt[0][0]);  // [kOrdThreads]
+        int32_t* rs = reinterpret_cast<int32_t*>(sk + kOrdThreads);                  // run starts
+        int32_t* os = rs + kOrdThreads + 1;                                           // run destinations
+        __syncthreads();  // wpre is complete
+        if (tid < nwords) {
+            uint32_t bits = brk[tid];
+            int i = wpre[tid];
+            while (bits) {
+                const int p = tid * 32 + __ffs(bits) - 1;
+                rs[i] = p;
+                sk[i] = ((unsigned long long)key[va[p]] << 32) | (unsigned)i;
+                ++i;
+                bits &= bits - 1;
             }
         }
-        __syncthreads();  // every key is final before any digit is read
-        int bits = 16;
-        while (bits < 32 && ((uint32_t)(mx - mn) >> (bits - 16)) != 0) ++bits;
-        // stable LSD radix sort of va by key, 8-bit digits; warp w owns positions [w L, (w + 1) L)
-        const int L = (m + kOrdWarps - 1) / kOrdWarps;
-        const int w0 = min(m, warp * L), w1 = min(m, w0 + L);
-        const uint32_t lt_mask = (1u << lane) - 1u;
-        uint16_t* src = va;
-        uint16_t* dst = vb;
-        for (int shift = 0; shift < bits; shift += 8) {
-            auto digit = [&](uint16_t rr) { return (int)((key[rr] >> shift) & (kOrdBins - 1)); };
-            for (int bn = lane; bn < kOrdBins; bn += 32) wcnt[warp][bn] = 0;
+        if (tid >= R) sk[tid] = ~0ull;
+        if (tid == 0) rs[R] = m;
+        __syncthreads();
+        // bitonic network over NP = the power of two >= max(R, 32) elements, one per thread
+        // of the first NP / 32 warps: partners less than 32 apart exchange by shuffles, the
+        // others through shared memory behind a named barrier of those warps
+        int NP = 32;
+        while (NP < R) NP <<= 1;
+        if (tid < NP) {
+            unsigned long long x = sk[tid];
+            for (int kk = 2; kk <= NP; kk <<= 1) {
+                for (int j = kk >> 1; j > 0; j >>= 1) {
+                    unsigned long long y;
+                    if (j >= 32) {
+                        named_barrier(1, NP);  // the previous round's reads are done
+                        sk[tid] = x;
+                        named_barrier(1, NP);
+                        y = sk[tid ^ j];
+                    } else {
+                        y = __shfl_xor_sync(0xffffffffu, x, j);
+                    }
+                    const bool up = (tid & kk) == 0, low = (tid & j) == 0;
+                    x = (up == low) ? (x < y ? x : y) : (x < y ? y : x);
+                }
+            }
+            named_barrier(1, NP);
+            sk[tid] = x;
+        }
+        __syncthreads();
+        // destinations: lengths summed in sorted order
+        const int ri = tid < R ? (int)(unsigned)sk[tid] : 0;
+        const int len = tid < R ? rs[ri + 1] - rs[ri] : 0;
+        int tot;
+        const int dst0 = block_exclusive_scan(len, sh, &tot);
+        if (tid < R) os[ri] = dst0;
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            const int p = tid + q * kOrdThreads;
+            if (p >= m) break;
+            const int w = p >> 5;
+            const int i = wpre[w] + __popc(brk[w] & (0xFFFFFFFFu >> (31 - (p & 31)))) - 1;  // run of p
+            v.prow[os[i] + (p - rs[i])] = va[p];
+        }
+        return;
+    }
+    // warp w owns positions [w L, (w + 1) L)
+    const int L = (m + kOrdWarps - 1) / kOrdWarps;
+    const int w0 = min(m, warp * L), w1 = min(m, w0 + L);
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    uint16_t* src = va;
+    uint16_t* dst = vb;
+    for (int shift = 0; shift < 32; shift += 8) {
+        if (((var >> shift) & (kOrdBins - 1)) == 0) continue;  // the same digit in every key
+        auto digit = [&](uint16_t rr) { return (int)((key[rr] >> shift) & (kOrdBins - 1)); };
+        for (int bn = lane; bn < kOrdBins; bn += 32) wcnt[warp][bn] = 0;
+        __syncwarp();
+        for (int c = w0; c < w1; c += 32) {
+            const int i = c + lane;
+            const bool valid = i < w1;
+            const int d = valid ? digit(src[i]) : kOrdBins + lane;
+            const uint32_t peers = __match_any_sync(0xffffffffu, d);
+            if (valid && lane == __ffs(peers) - 1) wcnt[warp][d] += __popc(peers);
             __syncwarp();
-            for (int c = w0; c < w1; c += 32) {
-                const int i = c + lane;
-                const bool valid = i < w1;
-                const int d = valid ? digit(src[i]) : kOrdBins + lane;
-                const uint32_t peers = __match_any_sync(0xffffffffu, d);
-                if (valid && lane == __ffs(peers) - 1) wcnt[warp][d] += __popc(peers);
-                __syncwarp();
-            }
-            __syncthreads();
-            // digit tid (< 256): exclusive prefix over warps, then a scan over the digits
-            int total = 0;
-            if (tid < kOrdBins) {
-                uint32_t acc = 0;
-                for (int w = 0; w < kOrdWarps; ++w) {
-                    const uint32_t cn = wcnt[w][tid];
-                    wcnt[w][tid] = acc;
-                    acc += cn;
-                }
-                total = (int)acc;
-            }
-            int x = total;
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, x, o);
-                if (lane >= o) x += y;
-            }
-            if (lane == 31) sh[warp] = x;
-            __syncthreads();
-            if (warp == 0) {
-                int ws = lane < kOrdBins / 32 ? sh[lane] : 0;
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y = __shfl_up_sync(0xffffffffu, ws, o);
-                    if (lane >= o) ws += y;
-                }
-                sh[lane] = ws;
-            }
-            __syncthreads();
-            if (tid < kOrdBins) {
-                const uint32_t before = (uint32_t)((warp ? sh[warp - 1] : 0) + x - total);
-                for (int w = 0; w < kOrdWarps; ++w) wcnt[w][tid] += before;
-            }
-            __syncthreads();
-            // stable scatter, each warp walking its positions in order
-            for (int c = w0; c < w1; c += 32) {
-                const int i = c + lane;
-                const bool valid = i < w1;
-                const uint16_t rr = valid ? src[i] : 0;
-                const int d = valid ? digit(rr) : kOrdBins + lane;
-                const uint32_t peers = __match_any_sync(0xffffffffu, d);
-                const uint32_t rk = __popc(peers & lt_mask);
-                if (valid) dst[wcnt[warp][d] + rk] = rr;
-                __syncwarp();
-                if (valid && lane == __ffs(peers) - 1) wcnt[warp][d] += __popc(peers);
-                __syncwarp();
-            }
-            __syncthreads();
-            uint16_t* t = src;
-            src = dst;
-            dst = t;
         }
-        for (int p = tid; p < m; p += kOrdThreads) v.prow[p] = src[p];
-    } else {
-        for (int p = tid; p < m; p += kOrdThreads) v.prow[p] = va[p];
+        __syncthreads();
+        // digit tid (< 256): exclusive prefix over warps, then a scan over the digits
+        int total = 0;
+        if (tid < kOrdBins) {
+            uint32_t acc = 0;
+            for (int w = 0; w < kOrdWarps; ++w) {
+                const uint32_t cn = wcnt[w][tid];
+                wcnt[w][tid] = acc;
+                acc += cn;
+            }
+            total = (int)acc;
+        }
+        int x = total;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) sh[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int ws = lane < kOrdBins / 32 ? sh[lane] : 0;
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, ws, o);
+                if (lane >= o) ws += y;
+            }
+            sh[lane] = ws;
+        }
+        __syncthreads();
+        if (tid < kOrdBins) {
+            const uint32_t before = (uint32_t)((warp ? sh[warp - 1] : 0) + x - total);
+            for (int w = 0; w < kOrdWarps; ++w) wcnt[w][tid] += before;
+        }
+        __syncthreads();
+        // stable scatter, each warp walking its positions in order
+        for (int c = w0; c < w1; c += 32) {
+            const int i = c + lane;
+            const bool valid = i < w1;
+            const uint16_t rr = valid ? src[i] : 0;
+            const int d = valid ? digit(rr) : kOrdBins + lane;
+            const uint32_t peers = __match_any_sync(0xffffffffu, d);
+            const uint32_t rk = __popc(peers & lt_mask);
+            if (valid) dst[wcnt[warp][d] + rk] = rr;
+            __syncwarp();
+            if (valid && lane == __ffs(peers) - 1) wcnt[warp][d] += __popc(peers);
+            __syncwarp();
+        }
+        __syncthreads();
+        uint16_t* t = src;
+        src = dst;
+        dst = t;
     }
-    for (int p = m + tid; p < v.P * kPM; p += kOrdThreads) v.prow[p] = -1;
+    for (int p = tid; p < m; p += kOrdThreads) v.prow[p] = src[p];
 }
 
 constexpr int kRowsPerWarp = kCtaRows / (kPlanThreads / 32);  // positions per warp in the row step
@@ -356,10 +502,8 @@ plan_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx, 
                 const int32_t k = t < len[0] ? k0[0] + t : k0[1] + (t - len[0]);
                 cc[j] = t < total ? idx_of(col[k]) : -1;
             }
-            // columns of a row are far apart in a sparse mask: plain atomics, few collide
 #pragma unroll
-            for (int j = 0; j < kLoadBatch; ++j)
-                if (cc[j] >= 0) atomicOr(&bitmap[cc[j] >> 5], 1u << (cc[j] & 31));
+            for (int j = 0; j < kLoadBatch; ++j) or_bit_warp(bitmap, cc[j], lane);
         }
     }
     if (lane == 0) {
@@ -625,6 +769,11 @@ PlanLayout plan_layout(int32_t m, int32_t n, int32_t nnz) {
         L.gitems = take(P * (kTiles / kGroupTiles) * 4);
         L.dlist_sp = take(P * 4);
         L.img_slot = take(P * 4);
+        if (m <= kOrderMaxRows) {
+            L.okey = take(P * kPM * 4);
+            L.olong = take(P * kPM / 32 * 4);
+            L.obrk = take(P * kPM / 32 * 4);
+        }
     }
     L.total = off;
     return L;
@@ -657,6 +806,11 @@ PlanView plan_view(void* base, int32_t m, int32_t n, int32_t nnz) {
         v.gitems = at<int32_t>(b, L.gitems);
         v.dlist_sp = at<int32_t>(b, L.dlist_sp);
         v.img_slot = at<int32_t>(b, L.img_slot);
+        if (m <= kOrderMaxRows) {
+            v.okey = at<uint32_t>(b, L.okey);
+            v.olong = at<uint32_t>(b, L.olong);
+            v.obrk = at<uint32_t>(b, L.obrk);
+        }
     }
     return v;
 }
@@ -669,16 +823,20 @@ size_t spmm_image_budget_elems(int32_t m, int32_t nnz) {
     return (size_t)8 * nnz + P * kPM * 64;
 }
 
-// Launch plan_order_kernel (one CTA) on s, stream-ordered (not as a programmatic dependent):
-// it reads row_idx, row_offsets and col_idx, which the caller's previous operations on s
-// (sort_rows, a transpose) have just written.
+// The order kernels. The keys kernel is launched stream-ordered (not as a programmatic
+// dependent): it reads row_idx, row_offsets and col_idx, which the caller's previous
+// operations on s (sort_rows, a transpose) have just written; the sort follows it as a
+// programmatic dependent.
 template <typename I>
 cudaError_t launch_order(const int32_t* ro, const void* row_idx, const void* col, const PlanView& v, cudaStream_t s) {
-    auto kern = plan_order_kernel<I>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOrdSmem);
+    const unsigned grid = (unsigned)(((int64_t)v.P * kPM + kKeyThreads - 1) / kKeyThreads);
+    plan_keys_kernel<I><<<grid, kKeyThreads, 0, s>>>(ro, static_cast<const I*>(row_idx), static_cast<const I*>(col),
+                                                      v);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    kern<<<1, kOrdThreads, kOrdSmem, s>>>(ro, static_cast<const I*>(row_idx), static_cast<const I*>(col), v);
-    return cudaGetLastError();
+    e = cudaFuncSetAttribute(plan_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOrdSmem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(plan_sort_kernel, 1, kOrdThreads, kOrdSmem, s, v);
 }
 
 cudaError_t launch_plan_build(int it, const int32_t* ro, const void* row_idx, const void* col, const PlanView& v,
@@ -706,7 +864,7 @@ cudaError_t launch_plan_build(int it, const int32_t* ro, const void* row_idx, co
                                      : launch_order<int32_t>(ro, row_idx, col, v, s);
         if (e != cudaSuccess) return e;
         ordered = 1;
-        nlaunch = 3;
+        nlaunch = 4;
     }
     const unsigned rows_grid = (unsigned)v.P * kPlanCluster;
     cudaError_t e = it == kIdx16

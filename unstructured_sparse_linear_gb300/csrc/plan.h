@@ -21,6 +21,10 @@
 //                              (panel << 8 | group of kGroupTiles consecutive tiles)
 //   dlist_sp   int32[P]        panels with an image slot
 //   img_slot   int32[P]        image offset (elements) or -1
+// when the rows are also ordered (m <= kOrderMaxRows):
+//   okey       uint32[P*128]   sort key of each position of row_idx
+//   olong      uint32[P*4]     per 32 positions: key of the run of >= 32 positions starting there, or ~0
+//   obrk       uint32[P*4]     bit p: position p of row_idx starts a stretch of one key
 #pragma once
 
 #include <cuda_runtime.h>
@@ -72,6 +76,9 @@ struct PlanView {
     int32_t* gitems;
     int32_t* dlist_sp;
     int32_t* img_slot;
+    uint32_t* okey;
+    uint32_t* olong;
+    uint32_t* obrk;
     int32_t m, n, nnz, P, W;
     bool panels;
     __host__ __device__ int32_t* bins_spmm() const { return hdr; }
@@ -81,7 +88,7 @@ struct PlanView {
 
 struct PlanLayout {
     size_t hdr, pan_part, bm, wbase, desc, prow, ulist, upos, ts, tmask, dense, sp_dense, items, gitems, dlist_sp,
-        img_slot;
+        img_slot, okey, olong, obrk;
     size_t total;
 };
 
