@@ -340,6 +340,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// 2-D TMA tile store of the box at (x = column, y = row) from shared memory, in the calling
+// thread's bulk group (callers only store boxes that lie inside the tensor).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kGrpThreads, 1)
 sddmm_group_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restrict__ out, int32_t kd, PlanView v,
@@ -892,9 +901,11 @@ static_assert(kWsSmem <= 227 * 1024, "warp-specialized SpMM shared memory");
 template <typename T>
 __global__ void __launch_bounds__(kWsThreads, 1)
 spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restrict__ img_base, int32_t N,
-                     PlanView v, uint32_t idesc, int* err, const __grid_constant__ CUtensorMap tmap_b, int use_tma) {
+                     PlanView v, uint32_t idesc, int* err, const __grid_constant__ CUtensorMap tmap_b, int use_tma,
+                     const __grid_constant__ CUtensorMap tmap_c, int use_tma_c) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kWsStages], empty_bar[kWsStages], tfull_bar[2], tempty_bar[2], drain_bar;
+    __shared__ int s_run[kWsEpiWarps];
     __shared__ uint32_t tmem_base_sh;
     uint8_t* smem = reinterpret_cast<uint8_t*>(align_up(reinterpret_cast<uintptr_t>(smem_raw), 1024));
     const uint32_t sbase = smem_u32(smem);                 // image slots
@@ -930,22 +941,86 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
 
     if (warp < kWsEpiWarps) {
         // ---------------- epilogue
+        // A unit leaves through the staging area in one of two ways. When the panel's rows are
+        // two runs of 64 consecutive rows of C and the unit lies inside C: per 64-column
+        // quarter, a 128-byte-swizzled 128 x 64 copy in one of two 16 KB buffers (alternating,
+        // so a quarter is written while the previous one is stored) and two 2-D TMA tile
+        // stores of 64 x 64 boxes issued by thread 0. Otherwise per 128-column half, one
+        // shared row per thread and one bulk copy per row. The epilogue warps meet at named
+        // barrier 1 before a buffer is rewritten and before the tile stores; every decision
+        // that leads to a barrier is taken by all of them (a barrier-reduced AND for the
+        // accumulator waits).
         const int r = tid;  // panel row = TMEM lane
+        constexpr int kEpi = kWsEpiWarps * 32;
+        constexpr uint32_t kQBuf = kPM * 128;  // one quarter: 128 rows x 64 columns
+        static_assert(2 * kQBuf <= kWsCStage, "two quarter buffers in the staging area");
         const uint32_t crow = cstage + (uint32_t)r * kSpCRowBytes;
-        uint32_t t = 0;
+        uint32_t t = 0, qq = 0;
         int64_t cur = -1;
-        int i = -1;
+        int i = -1, y0 = 0, y1 = 0;
+        bool tiles = false, prev_tile = false;
         for (int64_t unit = u_begin; unit < u_end; ++unit, ++t) {
             if (unit / ntn != cur) {
                 cur = unit / ntn;
-                i = v.prow[v.dlist_sp[cur] * kPM + r];
+                const int base = v.dlist_sp[cur] * kPM;
+                i = v.prow[base + r];
+                const int first = v.prow[base + (r & ~63)];
+                const bool run = __all_sync(0xffffffffu, use_tma_c && i >= 0 && first >= 0 && i == first + (r & 63));
+                if (lane == 0) s_run[warp] = run;
+                named_barrier(1, kEpi);
+                tiles = s_run[0] && s_run[1] && s_run[2] && s_run[3];
+                y0 = v.prow[base];
+                y1 = v.prow[base + 64];
             }
             const int n0 = (int)(unit % ntn) * kWsNT;
+            const bool tile_unit = tiles && n0 + kWsNT <= N;
             const uint32_t a = t & 1u;
-            // warp-uniform outcome: the TMEM loads below are warp-collective
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&tfull_bar[a]), (t >> 1) & 1u, err))) break;
+            // the same outcome in every epilogue thread: the TMEM loads below are warp-collective
+            // and the named barriers need all of them
+            if (!named_barrier_and(1, kEpi, mbar_wait(smem_u32(&tfull_bar[a]), (t >> 1) & 1u, err))) break;
             tc::fence_after_sync();
             const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16) + a * kWsNT;
+            if (tile_unit) {
+#pragma unroll
+                for (int c = 0; c < kWsNT / 64; ++c, ++qq) {
+                    uint4 packed[8];
+#pragma unroll
+                    for (int hc = 0; hc < 2; ++hc) {
+                        float x[32];
+                        tc::tmem_ld32(lane_addr + c * 64 + hc * 32, x);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) packed[hc * 4 + q] = Elt<T>::pack(x + q * 8);
+                    }
+                    if (c == kWsNT / 64 - 1) {  // the whole accumulator row has been read
+                        tc::fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[a]));
+                    }
+                    // buffer qq & 1 was last read by the store of two quarters ago (thread 0's
+                    // next-to-last group); after the row path every thread's copies must be read
+                    if (c > 0 || prev_tile) {
+                        if (tid == 0) bulk_wait_read<1>();
+                    } else {
+                        bulk_wait_read<0>();
+                    }
+                    named_barrier(1, kEpi);
+                    const uint32_t buf = cstage + (qq & 1u) * kQBuf;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf + tc::sw128_off(r, q)),
+                                     "r"(packed[q].x), "r"(packed[q].y), "r"(packed[q].z), "r"(packed[q].w)
+                                     : "memory");
+                    fence_proxy_async_smem();
+                    named_barrier(1, kEpi);
+                    if (tid == 0) {
+                        tma_store_2d(&tmap_c, n0 + c * 64, y0, buf);
+                        tma_store_2d(&tmap_c, n0 + c * 64, y1, buf + kQBuf / 2);
+                        bulk_commit();
+                    }
+                }
+                prev_tile = true;
+                continue;
+            }
 #pragma unroll
             for (int h = 0; h < kWsNT / kSpNT; ++h) {
                 uint4 packed[kSpNT / 8];
@@ -961,7 +1036,8 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[a]));
                 }
-                bulk_wait_read<0>();  // this thread's previous half row has left its shared row
+                bulk_wait_read<0>();     // this thread's stores have read the staging area
+                named_barrier(1, kEpi);  // ... and every epilogue thread's
 #pragma unroll
                 for (int q = 0; q < kSpNT / 8; ++q)
                     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(crow + q * 16), "r"(packed[q].x),
@@ -974,6 +1050,7 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
                     bulk_commit();
                 }
             }
+            prev_tile = false;
         }
         bulk_wait<0>();
     } else if (warp < kWsEpiWarps + kWsProdWarps) {
@@ -1264,11 +1341,13 @@ cudaError_t run_spmm_panels(const void* vals, const int32_t* ro, const void* B, 
         auto kws = spmm_panel_ws_kernel<T>;
         e = cudaFuncSetAttribute(kws, cudaFuncAttributeMaxDynamicSharedMemorySize, kWsSmem);
         if (e != cudaSuccess) return e;
-        CUtensorMap tmap;
-        const int use_tma = encode_rows_map(&tmap, B, K, N, 64, std::is_same<T, __nv_bfloat16>::value) ? 1 : 0;
+        CUtensorMap tmap, tmap_c;
+        const bool bf = std::is_same<T, __nv_bfloat16>::value;
+        const int use_tma = encode_rows_map(&tmap, B, K, N, 64, bf) ? 1 : 0;
+        const int use_tma_c = encode_rows_map(&tmap_c, C, v.m, N, 64, bf) ? 1 : 0;  // 64 x 64 boxes of C
         e = launch_pdl(kws, device_props().sm_count, kWsThreads, kWsSmem, s, static_cast<const T*>(B),
                        static_cast<T*>(C), static_cast<const T*>(img), N, v, idesc_ws, device_error_word(), tmap,
-                       use_tma);
+                       use_tma, tmap_c, use_tma_c);
         count_launches(2);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
