@@ -309,9 +309,10 @@ sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
 // While the tensor core runs, shared-memory loads of other warps wait behind its operand
 // reads, so the producers keep the chunk loop free of them. When each 64-row half of the
 // panel is 64 consecutive rows of A and each 64-row half of a tile's U list 64 consecutive
-// rows of BT, one thread (warp 1 lane 0) loads every chunk as 2-D TMA boxes (128-byte
-// swizzle, straight into the UMMA K-major layout) with one expect-tx arrive, from box
-// coordinates held in registers; otherwise warps 1 .. 7 gather every 16-byte piece with
+// rows of BT, one thread per stage (lane 0 of warps 1 .. S) loads that stage's chunks as 2-D
+// TMA boxes (128-byte swizzle, straight into the UMMA K-major layout) with one expect-tx
+// arrive each, from box coordinates held in registers (several TMA issuers keep more loads
+// in flight than one); otherwise warps 1 .. 7 gather every 16-byte piece with
 // cp.async and each thread arrives once its pieces have landed (the stage barriers are
 // re-armed per item for the producer count of its mode). The MMA issuer commits each stage
 // to its empty barrier, which the producers wait on before refilling it, and the item's
@@ -486,23 +487,26 @@ sddmm_group_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
                 }
                 __syncwarp();
             } else if (tma_all) {
-                // ---- one producer thread: whole chunks by TMA boxes, coordinates in registers
-                if (tid == 32) {
+                // ---- one producer thread per stage (lane 0 of warps 1 .. S): chunk j is loaded
+                // by the thread of stage j mod S, whole by TMA boxes with the coordinates in
+                // registers; several issuers keep more of the SM's loads in flight, and each
+                // waits only for the consumption of its own stage's previous chunk
+                if (lane == 0 && warp >= 1 && warp <= S) {
+                    const int st = warp - 1;
                     int by[2 + 2 * kGroupTiles];
 #pragma unroll
                     for (int b = 0; b < 2 + 2 * kGroupTiles; ++b) by[b] = b < 2 + 2 * nt ? s_box[b] : 0;
+                    const uint32_t sa = sbase + (uint32_t)st * stage_bytes;
+                    const uint32_t fb = smem_u32(&full_bar[st]);
                     uint32_t empty_ph = 0;
-                    for (int j = 0; j < nk; ++j) {
-                        const int st = j % S;
+                    for (int j = st; j < nk; j += S) {
                         if (j >= S) {  // the stage's previous chunk (j - S) has been consumed
-                            if (!mbar_wait(smem_u32(&empty_bar[st]), (empty_ph >> st) & 1u, err)) {
+                            if (!mbar_wait(smem_u32(&empty_bar[st]), empty_ph, err)) {
                                 failed = true;
                                 break;
                             }
-                            empty_ph ^= 1u << st;
+                            empty_ph ^= 1u;
                         }
-                        const uint32_t sa = sbase + (uint32_t)st * stage_bytes;
-                        const uint32_t fb = smem_u32(&full_bar[st]);
                         const int k0 = (kc0 + j) * kKC;
                         mbar_arrive_expect_tx(fb, stage_bytes);
                         tma_load_2d(sa, &tmap_a, k0, by[0], fb);
@@ -854,24 +858,23 @@ spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restric
 // contiguous range of units, so consecutive units mostly share their panel (its U list,
 // image and rows are looked up once per panel, not once per unit).
 //   warps 0-3   epilogue: thread r owns TMEM lane r (panel row r); it reads the finished
-//               accumulator (256 columns, in two halves), frees it, converts each half to
-//               the output dtype into its own shared row and sends it to C with one bulk
-//               async copy;
-//   warps 4-6   producers: per 64-wide K chunk, one bulk async copy of the image chunk
-//               (16 KB, contiguous, already swizzled; a panel of |U| <= 256 keeps its whole
-//               image in four slots, loaded with its first unit in the CTA only) and the
-//               chunk's 64 rows of B (256 columns): when they are 64 consecutive rows
-//               (block-structured masks), four
-//               TMA tile loads (64 x 64 boxes, 128-byte swizzle) straight into the MN-major
-//               operand layout;
+//               accumulator (256 columns, in four quarters), frees it and sends each quarter
+//               to C: as 2-D TMA tile stores when the panel's rows are two runs of 64
+//               consecutive rows of C, else one bulk async copy per row;
+//   warps 4-7   producers, one per stage of a 4-stage ring of B tiles (32 KB each): per
+//               64-wide K chunk the image chunk (16 KB, contiguous, already swizzled; a panel
+//               of |U| <= 256 keeps its whole image in four slots, loaded with its first
+//               unit in the CTA only) and the chunk's 64 rows of B (256 columns): when they
+//               are 64 consecutive rows (block-structured masks), four TMA tile loads (64 x 64
+//               boxes, 128-byte swizzle) straight into the MN-major operand layout;
 //               otherwise a gather (cp.async, 16 bytes each) whose completion is signalled
-//               on the stage's mbarrier (cp.async.mbarrier.arrive.noinc). Each producer warp
-//               keeps its own shared copy of the panel's U list (no barrier between the
-//               producer warps);
-//   warp 7      TMEM owner and MMA issuer (one thread): 4 MMAs (M = 128, N = 256, K = 16)
-//               per chunk, a commit that
-//               frees the stage, and a commit per unit that hands the accumulator to the
-//               epilogue.
+//               on the stage's mbarrier. The panel's U list is read from global memory;
+//   warp 8      TMEM owner and MMA issuer (one thread): 4 MMAs (M = 128, N = 256, K = 16)
+//               per chunk, a commit that frees the stage, and a commit per unit that hands
+//               the accumulator to the epilogue.
+// A B tile takes about a microsecond from issue to arrival and the MMAs of a chunk about a
+// quarter of that, so the ring holds four tiles (128 KB) in flight; the image slots, the
+// ring and the C staging buffers fill the 227 KB of shared memory.
 // Units are 256 columns wide, so every A chunk read by the tensor core serves 256 output
 // columns (shared-memory bandwidth, not the tensor pipe, bounds 128-column tiles). Two
 // accumulators of 256 columns (all of TMEM) alternate between units, so the MMAs of a unit
@@ -879,7 +882,7 @@ spmm_panel_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restric
 // stops, and the others then give up on their next wait.
 constexpr int kWsNT = 256;                                     // columns of C per unit (UMMA N)
 constexpr uint32_t kWsStageB = kKC * kWsNT * 2;                // 32 KB
-constexpr int kWsStages = 3;
+constexpr int kWsStages = 4;
 // Image chunk slots: a panel of at most kWsASlots chunks (|U| <= 256) loads its image once
 // per run of its units in a CTA and keeps it (slot j = chunk j); a larger panel streams its
 // chunks through slots 0 .. kWsStages - 1 beside the B stages.
@@ -887,14 +890,16 @@ constexpr int kWsASlots = 4;
 constexpr uint32_t kWsAReg = kWsASlots * kSpStageA;            // 64 KB
 static_assert(kWsASlots >= kWsStages, "a streamed chunk uses the slot of its stage");
 constexpr int kWsEpiWarps = 4;
-// One producer warp per stage: chunk g goes to stage g mod 3 and warp g mod 3, so a warp only
+// One producer warp per stage: chunk g goes to stage g mod 4 and warp g mod 4, so a warp only
 // ever waits for the consumption of its own previous chunk (one barrier phase back; a parity
 // wait cannot alias a phase two completions behind).
 constexpr int kWsProdWarps = kWsStages;
 constexpr int kWsThreads = (kWsEpiWarps + kWsProdWarps + 1) * 32;
-constexpr uint32_t kWsCStage = kPM * kSpCRowBytes;  // staged C half rows (128 columns)
-constexpr uint32_t kWsUList = kUList * 2;           // one producer warp's copy of a U list (16-bit columns)
-constexpr uint32_t kWsSmem = kWsAReg + kWsStages * kWsStageB + kWsCStage + kWsProdWarps * kWsUList + 1024;
+constexpr uint32_t kWsQBuf = kPM * 128;             // one 64-column quarter of a unit, 128 rows
+constexpr uint32_t kWsCStage = 2 * kWsQBuf;          // C staging: two quarter buffers
+constexpr uint32_t kWsCRow = 64 * 2 + 16;            // a quarter row on the per-row path, padded
+static_assert(kPM * kWsCRow <= kWsCStage, "per-row staging fits the quarter buffers");
+constexpr uint32_t kWsSmem = kWsAReg + kWsStages * kWsStageB + kWsCStage + 1024;
 static_assert(kWsSmem <= 227 * 1024, "warp-specialized SpMM shared memory");
 
 
@@ -941,20 +946,17 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
 
     if (warp < kWsEpiWarps) {
         // ---------------- epilogue
-        // A unit leaves through the staging area in one of two ways. When the panel's rows are
-        // two runs of 64 consecutive rows of C and the unit lies inside C: per 64-column
-        // quarter, a 128-byte-swizzled 128 x 64 copy in one of two 16 KB buffers (alternating,
-        // so a quarter is written while the previous one is stored) and two 2-D TMA tile
-        // stores of 64 x 64 boxes issued by thread 0. Otherwise per 128-column half, one
-        // shared row per thread and one bulk copy per row. The epilogue warps meet at named
-        // barrier 1 before a buffer is rewritten and before the tile stores; every decision
-        // that leads to a barrier is taken by all of them (a barrier-reduced AND for the
-        // accumulator waits).
+        // A unit leaves in 64-column quarters through the staging area, in one of two ways.
+        // When the panel's rows are two runs of 64 consecutive rows of C and the unit lies
+        // inside C: a 128-byte-swizzled 128 x 64 copy in one of two 16 KB buffers
+        // (alternating, so a quarter is written while the previous one is stored) and two
+        // 2-D TMA tile stores of 64 x 64 boxes issued by thread 0. Otherwise one shared row
+        // per thread and one bulk copy per row. The epilogue warps meet at named barrier 1
+        // before a buffer is rewritten and before the tile stores; every decision that leads
+        // to a barrier is taken by all of them (a barrier-reduced AND for the accumulator waits).
         const int r = tid;  // panel row = TMEM lane
         constexpr int kEpi = kWsEpiWarps * 32;
-        constexpr uint32_t kQBuf = kPM * 128;  // one quarter: 128 rows x 64 columns
-        static_assert(2 * kQBuf <= kWsCStage, "two quarter buffers in the staging area");
-        const uint32_t crow = cstage + (uint32_t)r * kSpCRowBytes;
+        const uint32_t crow = cstage + (uint32_t)r * kWsCRow;
         uint32_t t = 0, qq = 0;
         int64_t cur = -1;
         int i = -1, y0 = 0, y1 = 0;
@@ -980,22 +982,22 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
             if (!named_barrier_and(1, kEpi, mbar_wait(smem_u32(&tfull_bar[a]), (t >> 1) & 1u, err))) break;
             tc::fence_after_sync();
             const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16) + a * kWsNT;
-            if (tile_unit) {
 #pragma unroll
-                for (int c = 0; c < kWsNT / 64; ++c, ++qq) {
-                    uint4 packed[8];
+            for (int c = 0; c < kWsNT / 64; ++c) {
+                uint4 packed[8];
 #pragma unroll
-                    for (int hc = 0; hc < 2; ++hc) {
-                        float x[32];
-                        tc::tmem_ld32(lane_addr + c * 64 + hc * 32, x);
+                for (int hc = 0; hc < 2; ++hc) {
+                    float x[32];
+                    tc::tmem_ld32(lane_addr + c * 64 + hc * 32, x);
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) packed[hc * 4 + q] = Elt<T>::pack(x + q * 8);
-                    }
-                    if (c == kWsNT / 64 - 1) {  // the whole accumulator row has been read
-                        tc::fence_before_sync();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[a]));
-                    }
+                    for (int q = 0; q < 4; ++q) packed[hc * 4 + q] = Elt<T>::pack(x + q * 8);
+                }
+                if (c == kWsNT / 64 - 1) {  // the whole accumulator row has been read
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[a]));
+                }
+                if (tile_unit) {
                     // buffer qq & 1 was last read by the store of two quarters ago (thread 0's
                     // next-to-last group); after the row path every thread's copies must be read
                     if (c > 0 || prev_tile) {
@@ -1004,7 +1006,7 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
                         bulk_wait_read<0>();
                     }
                     named_barrier(1, kEpi);
-                    const uint32_t buf = cstage + (qq & 1u) * kQBuf;
+                    const uint32_t buf = cstage + (qq & 1u) * kWsQBuf;
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
                         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf + tc::sw128_off(r, q)),
@@ -1014,43 +1016,27 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
                     named_barrier(1, kEpi);
                     if (tid == 0) {
                         tma_store_2d(&tmap_c, n0 + c * 64, y0, buf);
-                        tma_store_2d(&tmap_c, n0 + c * 64, y1, buf + kQBuf / 2);
+                        tma_store_2d(&tmap_c, n0 + c * 64, y1, buf + kWsQBuf / 2);
+                        bulk_commit();
+                    }
+                    ++qq;
+                } else {
+                    bulk_wait_read<0>();     // this thread's copies have read the staging area
+                    named_barrier(1, kEpi);  // ... and every epilogue thread's
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(crow + q * 16),
+                                     "r"(packed[q].x), "r"(packed[q].y), "r"(packed[q].z), "r"(packed[q].w)
+                                     : "memory");
+                    fence_proxy_async_smem();
+                    const int nq = min(64, N - n0 - c * 64);  // columns of this quarter inside C
+                    if (i >= 0 && nq > 0) {
+                        bulk_s2g(C + (int64_t)i * N + n0 + c * 64, crow, (uint32_t)nq * (uint32_t)sizeof(T));
                         bulk_commit();
                     }
                 }
-                prev_tile = true;
-                continue;
             }
-#pragma unroll
-            for (int h = 0; h < kWsNT / kSpNT; ++h) {
-                uint4 packed[kSpNT / 8];
-#pragma unroll
-                for (int c = 0; c < kSpNT / 32; ++c) {
-                    float x[32];
-                    tc::tmem_ld32(lane_addr + h * kSpNT + c * 32, x);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) packed[c * 4 + q] = Elt<T>::pack(x + q * 8);
-                }
-                if (h == kWsNT / kSpNT - 1) {  // the whole accumulator row has been read
-                    tc::fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&tempty_bar[a]));
-                }
-                bulk_wait_read<0>();     // this thread's stores have read the staging area
-                named_barrier(1, kEpi);  // ... and every epilogue thread's
-#pragma unroll
-                for (int q = 0; q < kSpNT / 8; ++q)
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(crow + q * 16), "r"(packed[q].x),
-                                 "r"(packed[q].y), "r"(packed[q].z), "r"(packed[q].w)
-                                 : "memory");
-                fence_proxy_async_smem();
-                const int nh = min(kSpNT, N - n0 - h * kSpNT);  // columns of this half inside C
-                if (i >= 0 && nh > 0) {
-                    bulk_s2g(C + (int64_t)i * N + n0 + h * kSpNT, crow, (uint32_t)nh * (uint32_t)sizeof(T));
-                    bulk_commit();
-                }
-            }
-            prev_tile = false;
+            prev_tile = tile_unit;
         }
         bulk_wait<0>();
     } else if (warp < kWsEpiWarps + kWsProdWarps) {
@@ -1062,7 +1048,7 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
         // the tile-path test is a per-panel bit mask in registers, so no shared-memory loads
         // sit in the tile path's loop (they are slow while the tensor core reads operands).
         const int pw = warp - kWsEpiWarps;
-        uint16_t* s_u = reinterpret_cast<uint16_t*>(smem + kWsAReg + kWsStages * kWsStageB + kWsCStage + pw * kWsUList);
+        const int32_t* ul = v.ulist;  // the current panel's U list (global, read through L1)
         constexpr int kPieces = kWsNT / 8;  // 16-byte pieces per B row of the tile
         uint32_t g = 0, t = 0;
         bool ok = true;
@@ -1092,9 +1078,7 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
                     }
                 }
                 img = img_base + v.img_slot[p];
-                const int32_t* ul = v.ulist + (size_t)p * kUList;
-                __syncwarp();  // the previous panel's copy has been read by the whole warp
-                for (int x = lane; x < nU; x += 32) s_u[x] = (uint16_t)ul[x];
+                ul = v.ulist + (size_t)p * kUList;
                 // U is sorted and distinct, so 64 positions spanning 63 columns are consecutive
                 uint32_t lo = 0, hi = 0;
 #pragma unroll
@@ -1107,7 +1091,6 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
                 }
                 static_assert(kUList / kKC <= 64, "one mask bit per chunk");
                 tile_mask = ((uint64_t)hi << 32) | lo;
-                __syncwarp();
             } else if (resident) {
                 load_a = false;  // the panel's image is already in its slots
             }
@@ -1115,7 +1098,7 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
             for (int j = 0; j < nk; ++j, ++g) {
                 if ((int)(g % kWsProdWarps) != pw) continue;
                 const uint32_t st = g % kWsStages;  // = pw
-                static_assert(kWsProdWarps == kWsStages, "stage g mod 3 is always loaded by warp g mod 3");
+                static_assert(kWsProdWarps == kWsStages, "stage g mod 4 is always loaded by warp g mod 4");
                 // warp-uniform outcome
                 if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty_bar[st]), ((g / kWsStages) + 1) & 1u, err))) {
                     ok = false;
@@ -1128,7 +1111,7 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
                 const T* img_j = img + (size_t)j * kPM * kKC;
                 if ((tile_mask >> j) & 1u) {
                     if (lane == 0) {
-                        const int u0 = s_u[j * kKC];
+                        const int u0 = ul[j * kKC];
                         mbar_arrive_expect_tx(fb, abytes + kWsStageB);
                         if (load_a) bulk_g2s(sa, img_j, kSpStageA, fb);
 #pragma unroll
@@ -1146,7 +1129,7 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
                     const int kk = c / kPieces, nch = c % kPieces;
                     const int ncol = n0 + nch * 8;
                     const bool in = j * kKC + kk < nU && ncol < N;
-                    const int u = in ? (int)s_u[j * kKC + kk] : 0;
+                    const int u = in ? ul[j * kKC + kk] : 0;
                     const uint32_t off = (uint32_t)(nch >> 3) * (kKC / 8 * 1024) + tc::sw128_off(kk, nch & 7);
                     tc::cp_async16(sb + off, in ? (const void*)(B + (int64_t)u * N + ncol) : (const void*)B,
                                    in ? 16 : 0);
