@@ -241,10 +241,12 @@ def make_ops(sp, w, d, idx, args, outs):
     return ops
 
 
-def run_step_forked(ops, stream, side):
-    """The step on `stream` and the side streams, by data dependence: sort_rows first; csr_add
-    (which needs only row_idx) forks right after it, beside the plan; after the plan, sddmm
-    forks and spmm runs on `stream`; everything joins back into `stream`."""
+def run_step_forked(ops, stream, side, overlap=True):
+    """The step on `stream` and the side streams, by data dependence: sort_rows first; with
+    overlap, csr_add (which needs only row_idx) forks right after it, beside the plan, and after
+    the plan sddmm forks while spmm runs on `stream`; everything joins back into `stream`.
+    Without overlap (masks whose operators all run on the general row kernels, which gather or
+    stream at the memory system's bandwidth) the operators run one after the other."""
     by = dict(ops)
     spare = list(side)
     joins = []
@@ -261,29 +263,34 @@ def run_step_forked(ops, stream, side):
         joins.append(j)
 
     by["sort_rows"]()
-    if "csr_add" in by:
+    if "csr_add" in by and overlap:
         fork(by["csr_add"])
     by["plan"]()
-    if "sddmm" in by and "spmm" in by:
+    if "sddmm" in by and "spmm" in by and overlap:
         fork(by["sddmm"])
         by["spmm"]()
+    elif "sddmm" in by and "spmm" in by:
+        by["spmm"]()
+        by["sddmm"]()
     elif "sddmm" in by:
         by["sddmm"]()
     elif "spmm" in by:
         by["spmm"]()
+    if "csr_add" in by and not overlap:
+        by["csr_add"]()
     for j in joins:
         stream.wait_event(j)
 
 
-def run_fixed_forked(ops, stream, side):
+def run_fixed_forked(ops, stream, side, overlap=True):
     """The step with the mask fixed: row_idx and the plan of the last full step are reused, so
-    only the operators on values run, forked as in run_step_forked (csr_add and sddmm on the
-    side streams, spmm on `stream`)."""
+    only the operators on values run, forked as in run_step_forked (csr_add and, with overlap,
+    sddmm on the side streams, spmm on `stream`)."""
     by = dict(ops)
     spare = list(side)
     joins = []
     for name in ("csr_add", "sddmm"):
-        if name in by and (name == "csr_add" or "spmm" in by):
+        if name in by and overlap and (name == "csr_add" or "spmm" in by):
             e = torch.cuda.Event()
             e.record(stream)
             s = spare.pop(0)
@@ -293,10 +300,12 @@ def run_fixed_forked(ops, stream, side):
                 j = torch.cuda.Event()
                 j.record(s)
             joins.append(j)
-        elif name in by:
-            by[name]()
     if "spmm" in by:
         by["spmm"]()
+    if "sddmm" in by and not ("spmm" in by and overlap):
+        by["sddmm"]()
+    if "csr_add" in by and not overlap:
+        by["csr_add"]()
     for j in joins:
         stream.wait_event(j)
 
@@ -341,15 +350,22 @@ def measure(sp, lib, name, args, dev, ws, rank, local, flush):
     stream = torch.cuda.Stream(device=dev)
     side = [torch.cuda.Stream(device=dev) for _ in range(2)]
     with torch.cuda.stream(stream):
+        run_step_forked(ops, stream, side)
+        torch.cuda.synchronize(dev)
+        # the operators overlap when the mask has tensor-core panels; general row kernels
+        # gather from L2 at its bandwidth (and csr_add streams HBM), so beside each other they
+        # only slow each other down, and then they run one after the other
+        st = outs["plan"].stats()
+        overlap = st["dense_panels"] + st["spmm_panels"] > 0
         for _ in range(max(args.warmup, 1)):
-            run_step_forked(ops, stream, side)  # eager, on the streams the graph uses
+            run_step_forked(ops, stream, side, overlap)  # eager, on the streams the graph uses
             torch.cuda.synchronize(dev)
         pool = torch.cuda.graph_pool_handle()
         # the step on three streams by data dependence (fork / join inside one graph)
         step_graph = torch.cuda.CUDAGraph()
         launches0 = lib.spops_kernel_launches()
         with torch.cuda.graph(step_graph, stream=stream, pool=pool):
-            run_step_forked(ops, stream, side)
+            run_step_forked(ops, stream, side, overlap)
         launches_per_step = lib.spops_kernel_launches() - launches0
         # one graph per operator, replayed in order, for the per-operator breakdown
         op_graphs = []
@@ -362,7 +378,7 @@ def measure(sp, lib, name, args, dev, ws, rank, local, flush):
         # operator graphs above leave in their buffers
         fixed_graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(fixed_graph, stream=stream, pool=pool):
-            run_fixed_forked(ops, stream, side)
+            run_fixed_forked(ops, stream, side, overlap)
         for _ in range(args.warmup):
             step_graph.replay()
             for _, g in op_graphs:
@@ -458,6 +474,7 @@ def measure(sp, lib, name, args, dev, ws, rank, local, flush):
     rec = {"value": round(value, 2), "unit": "GFLOP/s", "ms_per_step": round(ms_per_step, 5), "steps": args.steps,
            "dtype": w.dtype, "config": config_dict(name, w, args), "per_op": per_op, "roofline": roofline,
            "cpu_baseline": cpu, "e2e": e2e, "next_ops": next_ops, "mask_fixed": mask_fixed,
+           "operators_overlap": overlap,
            "gpu_launches": int(launches_per_step) * args.steps, "launches_per_step": int(launches_per_step),
            "clocks": clocks, "breakdown_steps": nb,
            "step_ms_sum_of_ops": round(sum(v["ms"] for v in per_op.values()), 5),
