@@ -662,10 +662,13 @@ __global__ void __launch_bounds__(256) densify_kernel(const T* __restrict__ vals
     pdl_trigger();
     pdl_wait();
     const int p = blockIdx.x / kGroups, grp = blockIdx.x % kGroups;
-    if (!v.sp_dense[p]) return;
-    const int nU = v.desc[p].y;
-    const int upad = (nU + kKC - 1) / kKC * kKC;  // <= ucap
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // the panel's image slot and size, and the warp's row, are independent loads: issued together
+    const int slot = v.img_slot[p];
+    const int nU = v.desc[p].y;
+    const int i = v.prow[p * kPM + grp * kGroupRows + warp];
+    if (slot < 0) return;  // no image for this panel
+    const int upad = (nU + kKC - 1) / kKC * kKC;  // <= ucap
     uint4* st4 = reinterpret_cast<uint4*>(stage);
     const int row_vec = ucap * (int)sizeof(T) / 16;
     for (int x = tid; x < kGroupRows * row_vec; x += 256) {
@@ -675,7 +678,6 @@ __global__ void __launch_bounds__(256) densify_kernel(const T* __restrict__ vals
     static_assert(kGroupRows == 8, "one row per warp");
     {
         const int lr = warp;
-        const int i = v.prow[p * kPM + grp * kGroupRows + lr];
         const int32_t k0 = i >= 0 ? ro[i] : 0, k1 = i >= 0 ? ro[i + 1] : 0;
         // 8 (position, value) pairs per lane loaded before any is stored
         constexpr int kB = 8;
@@ -694,7 +696,7 @@ __global__ void __launch_bounds__(256) densify_kernel(const T* __restrict__ vals
         }
     }
     __syncthreads();
-    T* img = img_base + v.img_slot[p];
+    T* img = img_base + slot;
     const int chunks = upad / 8;  // 16-byte chunks per image row
     for (int x = tid; x < kGroupRows * chunks; x += 256) {
         const int lr = x / chunks, c = x % chunks;

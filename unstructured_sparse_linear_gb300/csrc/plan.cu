@@ -670,13 +670,15 @@ plan_upos_kernel(const int32_t* __restrict__ ro, const I* __restrict__ col, Plan
         return;
     }
     const int p = blockIdx.x / kGroups;
-    if (!(v.desc[p].x & 2)) return;  // U positions for SpMM-dense panels
-    const bool tiles = v.dense[p];    // tile starts and masks for SDDMM-dense ones (U <= kUCap)
-    uint32_t* bm = sm;
-    int* wb = reinterpret_cast<int*>(sm + v.W);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t pos = (int64_t)blockIdx.x * kGroupRows + warp;
+    // the panel's dense bits and the warp's row are independent loads: issued together
+    const int dbits = v.desc[p].x;
     const int row = v.prow[pos];
+    if (!(dbits & 2)) return;             // U positions for SpMM-dense panels
+    const bool tiles = (dbits & 1) != 0;  // tile starts and masks for SDDMM-dense ones (U <= kUCap)
+    uint32_t* bm = sm;
+    int* wb = reinterpret_cast<int*>(sm + v.W);
     const int32_t k0 = row >= 0 ? ro[row] : 0, k1 = row >= 0 ? ro[row + 1] : 0;
     for (int w = tid; w < v.W; w += kPlanThreads) {
         bm[w] = v.bm[(size_t)p * v.W + w];
