@@ -391,6 +391,36 @@ def test_spmm_many_units_pipeline_exact(case):
     assert_bits_equal(C, oracle.spmm(ro, col, w.values, w.B), w.dtype, f"{case} many-units spmm")
 
 
+def test_spmm_direct_values_gate_on_permuted_butterfly():
+    """Every row of the butterfly mask has the same length, and after the plan's row order its
+    panels are full, so the SpMM pipeline reads their A chunks straight from the CSR values,
+    but only when a panel's rows are two runs of 64 consecutive rows. Shuffling the rows in
+    blocks of 32 keeps runs long enough for the row order, so the panels stay full and dense,
+    but breaks the 64-row runs: the images are built as usual. Exact small-integer sums on
+    both masks, every element against the general kernel and the oracle."""
+    s = wl.spec("butterfly", N=2056, kd=64)
+    w = wl.generate(s, integer_valued=True)
+    ro, col = w.row_offsets.numpy(), w.col_idx.numpy()
+    rng = np.random.default_rng(11)
+    blocks = rng.permutation(w.m // 32)
+    perm = blocks[np.arange(w.m) // 32] * 32 + np.arange(w.m) % 32  # old row i becomes row perm[i]
+    rows = np.repeat(np.arange(w.m), np.diff(ro))
+    ro2, col2 = wl.csr_from_coords(perm[rows], col, w.m)
+    order = np.lexsort((col, perm[rows]))
+    vals2 = w.values[torch.from_numpy(order)]
+    for r_o, c_o, v_o, what in ((ro, col, w.values, "butterfly"), (ro2, col2, vals2, "permuted butterfly")):
+        dro = torch.from_numpy(np.asarray(r_o, dtype=np.int32)).cuda()
+        dcol = torch.from_numpy(np.asarray(c_o)).to(torch.int16).cuda()
+        ridx = torch.from_numpy(oracle.sort_rows(r_o)).to(torch.int16).cuda()
+        plan = sp.plan_build(dro, ridx, dcol, w.n)
+        assert plan.stats()["spmm_panels"] == 64, what
+        C = sp.spmm(v_o.cuda(), dro, ridx, dcol, w.B.cuda(), w.m, plan=plan)
+        ref = sp.spmm(v_o.cuda(), dro, ridx, dcol, w.B.cuda(), w.m, path="general")
+        torch.cuda.synchronize()
+        assert torch.equal(C.view(torch.int16), ref.view(torch.int16)), what
+        assert_bits_equal(C, oracle.spmm(r_o, c_o, v_o, w.B), w.dtype, what)
+
+
 def _mixed_panels(seed=5):
     """A 16384 x 4096 mask whose panels alternate between the SpMM pipeline's kinds, in
     row_idx order (rows by nnz): 400 of 1200 pool columns (|U| = 1200, gathered, streamed

@@ -25,6 +25,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <type_traits>
 
 #include "common.cuh"
@@ -656,7 +657,8 @@ inline uint32_t densify_smem_bytes(int32_t K, size_t elt) {
 
 template <typename T>
 __global__ void __launch_bounds__(256) densify_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro,
-                                                     T* __restrict__ img_base, PlanView v, int ucap) {
+                                                     T* __restrict__ img_base, PlanView v, int ucap,
+                                                     int skip_direct) {
     extern __shared__ __align__(16) uint8_t densify_smem[];
     T* stage = reinterpret_cast<T*>(densify_smem);  // [kGroupRows][ucap]
     pdl_trigger();
@@ -665,9 +667,11 @@ __global__ void __launch_bounds__(256) densify_kernel(const T* __restrict__ vals
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // the panel's image slot and size, and the warp's row, are independent loads: issued together
     const int slot = v.img_slot[p];
-    const int nU = v.desc[p].y;
+    const int2 d = *reinterpret_cast<const int2*>(&v.desc[p]);  // dense bits, |U|
+    const int nU = d.y;
     const int i = v.prow[p * kPM + grp * kGroupRows + warp];
-    if (slot < 0) return;  // no image for this panel
+    if (slot < 0) return;                        // no image for this panel
+    if (skip_direct && (d.x & 4)) return;        // the SpMM pipeline reads these values directly
     const int upad = (nU + kKC - 1) / kKC * kKC;  // <= ucap
     uint4* st4 = reinterpret_cast<uint4*>(stage);
     const int row_vec = ucap * (int)sizeof(T) / 16;
@@ -909,7 +913,8 @@ template <typename T>
 __global__ void __launch_bounds__(kWsThreads, 1)
 spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __restrict__ img_base, int32_t N,
                      PlanView v, uint32_t idesc, int* err, const __grid_constant__ CUtensorMap tmap_b, int use_tma,
-                     const __grid_constant__ CUtensorMap tmap_c, int use_tma_c) {
+                     const __grid_constant__ CUtensorMap tmap_c, int use_tma_c,
+                     const __grid_constant__ CUtensorMap tmap_v, int use_tma_v) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kWsStages], empty_bar[kWsStages], tfull_bar[2], tempty_bar[2], drain_bar;
     __shared__ int s_run[kWsEpiWarps];
@@ -1056,15 +1061,21 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
         bool ok = true;
         int64_t cur = -1;
         int nU = 0, nk = 0;
-        bool resident = false, load_a = true;
+        bool resident = false, load_a = true, direct = false;
+        int ay0 = 0, ay1 = 0;    // direct panels: the first rows of the two 64-row runs
         uint64_t tile_mask = 0;  // bit j: chunk j of the panel loads B as tiles
         const T* img = img_base;
         for (int64_t unit = u_begin; unit < u_end && ok; ++unit, ++t) {
             if (unit / ntn != cur) {  // a new panel: its U list into this warp's shared copy
                 cur = unit / ntn;
                 const int p = v.dlist_sp[cur];
-                nU = v.desc[p].y;
+                const int2 d = *reinterpret_cast<const int2*>(&v.desc[p]);  // dense bits, |U|
+                nU = d.y;
                 nk = (nU + kKC - 1) / kKC;
+                // A chunks straight from the CSR values (an m x L matrix) by two 64 x 64 boxes
+                direct = use_tma_v && (d.x & 4);
+                ay0 = direct ? v.prow[(int64_t)p * kPM] : 0;
+                ay1 = direct ? v.prow[(int64_t)p * kPM + 64] : 0;
                 const bool was_resident = resident;
                 resident = nk <= kWsASlots;
                 load_a = true;
@@ -1115,7 +1126,12 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
                     if (lane == 0) {
                         const int u0 = ul[j * kKC];
                         mbar_arrive_expect_tx(fb, abytes + kWsStageB);
-                        if (load_a) bulk_g2s(sa, img_j, kSpStageA, fb);
+                        if (load_a && direct) {
+                            tma_load_2d(sa, &tmap_v, j * kKC, ay0, fb);
+                            tma_load_2d(sa + kSpStageA / 2, &tmap_v, j * kKC, ay1, fb);
+                        } else if (load_a) {
+                            bulk_g2s(sa, img_j, kSpStageA, fb);
+                        }
 #pragma unroll
                         for (int bx = 0; bx < kWsNT / 64; ++bx)
                             tma_load_2d(sb + bx * (kKC / 8) * 1024, &tmap_b, n0 + 64 * bx, u0, fb);
@@ -1124,7 +1140,12 @@ spmm_panel_ws_kernel(const T* __restrict__ B, T* __restrict__ C, const T* __rest
                 }
                 if (lane == 0 && load_a) {
                     asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(fb), "r"(kSpStageA) : "memory");
-                    bulk_g2s(sa, img_j, kSpStageA, fb);
+                    if (direct) {
+                        tma_load_2d(sa, &tmap_v, j * kKC, ay0, fb);
+                        tma_load_2d(sa + kSpStageA / 2, &tmap_v, j * kKC, ay1, fb);
+                    } else {
+                        bulk_g2s(sa, img_j, kSpStageA, fb);
+                    }
                 }
                 // B[U rows j*64 .. +64, n0 .. n0 + 256): 64 x 32 pieces, 64 per lane
                 for (int c = lane; c < kKC * kPieces; c += 32) {
@@ -1313,26 +1334,37 @@ cudaError_t run_sddmm_panels(const void* A, const void* BT, void* out, int32_t k
 template <typename T>
 cudaError_t run_spmm_panels(const void* vals, const int32_t* ro, const void* B, int32_t K, int32_t N, void* C,
                             void* img, const PlanView& v, cudaStream_t s) {
+    const int ntn = (N + kSpNT - 1) / kSpNT;
+    const bool bf = std::is_same<T, __nv_bfloat16>::value;
+    // Many units per CTA: the warp-specialized pipeline, one CTA per SM. It reads the A chunks
+    // of panels whose values are already in image order (plan bit 4) straight from the CSR
+    // values, viewed as an m x L matrix when every row can have the same length L = nnz / m.
+    const bool ws = (int64_t)v.P * ntn >= (int64_t)device_props().sm_count * 6;
+    CUtensorMap tmap_v;
+    int use_tma_v = 0;
+    if (ws && v.m > 0 && v.nnz % v.m == 0) {
+        const int64_t L = (int64_t)v.nnz / v.m;
+        if (L >= kKC && L % 8 == 0 && L <= kUList && (uintptr_t)vals % 16 == 0)
+            use_tma_v = encode_rows_map(&tmap_v, vals, v.m, (int32_t)L, 64, bf) ? 1 : 0;
+    }
     const uint32_t dsmem = densify_smem_bytes(K, sizeof(T));
     cudaError_t e = cudaFuncSetAttribute(densify_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dsmem);
     if (e != cudaSuccess) return e;
     e = launch_pdl(densify_kernel<T>, v.P * kGroups, 256, dsmem, s, static_cast<const T*>(vals), ro,
-                   static_cast<T*>(img), v, (int)(dsmem / (kGroupRows * sizeof(T))));
+                   static_cast<T*>(img), v, (int)(dsmem / (kGroupRows * sizeof(T))), use_tma_v);
     if (e != cudaSuccess) return e;
-    const int ntn = (N + kSpNT - 1) / kSpNT;
-    const uint32_t idesc_ws = tc::instr_desc_f16(std::is_same<T, __nv_bfloat16>::value ? 1u : 0u, 0, 1, kPM, kWsNT);
-    // Many units per CTA: the warp-specialized pipeline, one CTA per SM.
-    if ((int64_t)v.P * ntn >= (int64_t)device_props().sm_count * 6) {
+    const uint32_t idesc_ws = tc::instr_desc_f16(bf ? 1u : 0u, 0, 1, kPM, kWsNT);
+    if (ws) {
         auto kws = spmm_panel_ws_kernel<T>;
         e = cudaFuncSetAttribute(kws, cudaFuncAttributeMaxDynamicSharedMemorySize, kWsSmem);
         if (e != cudaSuccess) return e;
         CUtensorMap tmap, tmap_c;
-        const bool bf = std::is_same<T, __nv_bfloat16>::value;
         const int use_tma = encode_rows_map(&tmap, B, K, N, 64, bf) ? 1 : 0;
         const int use_tma_c = encode_rows_map(&tmap_c, C, v.m, N, 64, bf) ? 1 : 0;  // 64 x 64 boxes of C
+        if (!use_tma_v) std::memset(&tmap_v, 0, sizeof(tmap_v));
         e = launch_pdl(kws, device_props().sm_count, kWsThreads, kWsSmem, s, static_cast<const T*>(B),
                        static_cast<T*>(C), static_cast<const T*>(img), N, v, idesc_ws, device_error_word(), tmap,
-                       use_tma, tmap_c, use_tma_c);
+                       use_tma, tmap_c, use_tma_c, tmap_v, use_tma_v);
         count_launches(2);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();

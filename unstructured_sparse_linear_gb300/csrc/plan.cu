@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(kOrdThreads, 1) plan_sort_kernel(PlanView v) {
 constexpr int kRowsPerWarp = kCtaRows / (kPlanThreads / 32);  // positions per warp in the row step
 constexpr int kLoadBatch = 8;                                  // index loads per lane in flight
 
-__device__ void panel_work(const PlanView& v, int p, uint32_t* sm, int nnz_p, int ne);
+__device__ void panel_work(const PlanView& v, const int32_t* __restrict__ ro, int p, uint32_t* sm, int nnz_p, int ne);
 
 // ---- 1. row step: cluster of kPlanCluster CTAs per panel
 template <typename I>
@@ -538,11 +538,12 @@ plan_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx, 
     }
     cluster_sync();  // the other CTAs keep their shared memory until rank 0 has read it
     if (rank != 0 || !v.panels) return;
-    panel_work(v, p, bitmap, s_tot[3], s_tot[2]);
+    panel_work(v, ro, p, bitmap, s_tot[3], s_tot[2]);
 }
 
 // ---- panel p (rank 0 of its cluster; sm holds the panel's OR-ed bitmap, W more words free)
-__device__ void panel_work(const PlanView& v, int p, uint32_t* sm, int nnz_p, int ne) {
+__device__ void panel_work(const PlanView& v, const int32_t* __restrict__ ro, int p, uint32_t* sm, int nnz_p,
+                           int ne) {
     uint32_t* bm = sm;  // bm[W], wbase[W]
     int* wb = reinterpret_cast<int*>(sm + v.W);
     __shared__ int sh[32];
@@ -561,8 +562,25 @@ __device__ void panel_work(const PlanView& v, int p, uint32_t* sm, int nnz_p, in
     const bool filled = nnz_p > 0 && ne >= kMinDenseRows && (int64_t)nnz_p * 4 >= (int64_t)ne * U;
     const bool dense = filled && U <= kUCap;     // SDDMM tiles
     const bool dense_sp = filled && U <= kUList; // SpMM image
+    // Values already in image order: every row of the mask has the same length L = nnz / m,
+    // this panel's 128 rows are two runs of 64 consecutive rows and each of them holds all of
+    // U (L == |U|). Then the panel's values are a 128 x |U| block of the m x L matrix the CSR
+    // values form, in column order, and the SpMM pipeline can load its A chunks from them
+    // directly instead of from a densified image.
+    bool direct = false;
+    if (dense_sp && v.m > 0 && v.nnz % v.m == 0 && (int64_t)v.nnz / v.m == U) {
+        const int64_t L = (int64_t)v.nnz / v.m;
+        bool ok = true;
+        if (tid < kPM) {
+            const int r = v.prow[(int64_t)p * kPM + tid];
+            const int first = v.prow[(int64_t)p * kPM + (tid & ~63)];
+            ok = r >= 0 && first >= 0 && r == first + (tid & 63) && (int64_t)ro[r] == (int64_t)r * L &&
+                 (int64_t)ro[r + 1] == (int64_t)(r + 1) * L;
+        }
+        direct = __syncthreads_and(ok) != 0;
+    }
     if (tid == 0) {
-        v.desc[p] = make_int4((dense ? 1 : 0) | (dense_sp ? 2 : 0), U, nnz_p, ne);
+        v.desc[p] = make_int4((dense ? 1 : 0) | (dense_sp ? 2 : 0) | (direct ? 4 : 0), U, nnz_p, ne);
         v.dense[p] = dense ? 1 : 0;
     }
     if (!dense_sp) return;

@@ -8,7 +8,9 @@
 // when panels are enabled (n <= 65536):
 //   bm, wbase  [P][W]          column bitmap of a panel; exclusive prefix of its popcounts
 //   desc       int4[P]         {dense bits, |U|, entries, non-empty rows}; dense bit 0: SDDMM
-//                              tiles (|U| <= kUCap), bit 1: SpMM image (|U| <= kUList)
+//                              tiles (|U| <= kUCap), bit 1: SpMM image (|U| <= kUList), bit 2:
+//                              the CSR values already hold the image (rows of one length
+//                              L = |U| in two runs of 64 consecutive rows)
 //   prow       int32[P*128]    row id at each panel position (-1 past m)
 //   ulist      int32[P][kUList] sorted columns of a dense panel
 //   upos       uint16[nnz]     column position of each entry in its panel's U
