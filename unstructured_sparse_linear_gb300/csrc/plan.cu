@@ -6,16 +6,19 @@
 // cluster in few rows and columns ("Sampled Dense-Dense Matrix Multiplication"). The plan
 // turns both into work lists:
 //   * row bins per operator (long rows get a CTA each, short rows a lane group);
-//   * panels = 128 consecutive row_idx positions. For each panel the union U of its
-//     columns; a panel is dense when |U| <= 1024, it has at least 16 non-empty rows and its
+//   * panels = 128 consecutive positions of the plan's row order (row_idx, reordered for
+//     masks of at most 16384 rows so that rows with one column pattern share panels when a
+//     pattern recurs in separate runs; kernels 0a and 0b below). For each panel the union U
+//     of its columns; a panel is dense when it has at least 16 non-empty rows and its
 //     entries fill at least a quarter of (non-empty rows) x |U|. Dense panels run on the
-//     tensor cores as 128 x |U| tiles.
-// Two kernels, no counters to reset between builds:
+//     tensor cores as 128 x |U| tiles (SDDMM when |U| <= 1024, SpMM when |U| <= 4096).
+// After the order, two kernels; no counters to reset between builds:
 //   1. a thread-block cluster of 8 CTAs per panel, 16 positions per CTA: row ids per
 //      position, counts, and a column bitmap per CTA built with shared-memory atomics; after
 //      a cluster barrier, rank 0 ORs the 8 bitmaps through distributed shared memory,
 //      prefix-sums their popcounts, lists U and decides density (SDDMM tiles |U| <= 1024,
-//      SpMM image |U| <= 4096);
+//      SpMM image |U| <= 4096) and whether the panel's CSR values are already in image
+//      order (rows of one length |U| in two runs of 64 consecutive rows);
 //   2. row groups of dense panels (8 rows per CTA): each entry's position in U and, per row,
 //      the first entry of every 128-column tile of U and a bit mask of the U positions it
 //      holds; one extra CTA sums the panel counts into row bins, lists dense panels and
