@@ -202,21 +202,25 @@ def recorded_traffic(op: str, workload: str):
         return None
     pat = re.compile(r"\|\s*" + re.escape(workload) + r"\s*\|\s*" + re.escape(op) +
                      r"\s*\|\s*([\w./+]+)\s*\|\s*([0-9a-f]+)\s*\|\s*([0-9]+)\s*\|"
-                     r"(?:\s*([0-9]+)\s*\|\s*([0-9]+)\s*\|)?")
+                     r"(?:\s*([0-9]+)\s*\|\s*([0-9]+)\s*\|)?(?:\s*([0-9]+)\s*\|)?")
     for line in open(p):
         mt = pat.match(line)
         if mt:
             src, h = mt.group(1), mt.group(2)
-            if mt.group(4) is not None:  # | read | write | sum |
+            if mt.group(4) is not None:  # | read | write | sum | (L2 write |)
                 rd, wr, total = int(mt.group(3)), int(mt.group(4)), int(mt.group(5))
             else:
                 rd, wr, total = None, None, int(mt.group(3))
+            l2w = int(mt.group(6)) if mt.group(6) is not None else None
             try:
                 if kernel_source_hash(src) != h:
                     return None
             except OSError:
                 return None
-            return {"bytes": total, "read": rd, "write": wr}
+            rec = {"bytes": total, "read": rd, "write": wr}
+            if l2w is not None:
+                rec["l2_write"] = l2w
+            return rec
     return None
 
 
@@ -352,11 +356,12 @@ def measure(sp, lib, name, args, dev, ws, rank, local, flush):
     with torch.cuda.stream(stream):
         run_step_forked(ops, stream, side)
         torch.cuda.synchronize(dev)
-        # the operators overlap when the mask has tensor-core panels; general row kernels
-        # gather from L2 at its bandwidth (and csr_add streams HBM), so beside each other they
-        # only slow each other down, and then they run one after the other
+        # the operators overlap unless they all run on the general row kernels with more than
+        # a GFLOP of gathers: those kernels gather from L2 at its bandwidth (and csr_add streams
+        # HBM), so beside each other they only slow each other down; small latency-bound
+        # steps and tensor-core panels gain from the overlap
         st = outs["plan"].stats()
-        overlap = st["dense_panels"] + st["spmm_panels"] > 0
+        overlap = st["dense_panels"] + st["spmm_panels"] > 0 or flops < 1e9
         for _ in range(max(args.warmup, 1)):
             run_step_forked(ops, stream, side, overlap)  # eager, on the streams the graph uses
             torch.cuda.synchronize(dev)
@@ -461,6 +466,7 @@ def measure(sp, lib, name, args, dev, ws, rank, local, flush):
                 "traffic": traffic["bytes"] if traffic else None,
                 "traffic_read": traffic["read"] if traffic else None,
                 "traffic_write": traffic["write"] if traffic else None,
+                "traffic_l2_write": traffic.get("l2_write") if traffic else None,
                 "algorithmic_bytes": acc[dominant]["bytes"], "peak_source": pk["source"],
                 "note": "achieved = algorithmic bytes of the operator / its mean event time in the per-operator "
                         "loop (L2 flushed before each step); traffic = ncu dram__bytes_read + dram__bytes_write "

@@ -72,6 +72,12 @@ def test_recorded_traffic_follows_the_source_hash(tmp_path, monkeypatch):
         "| workload | op | sources | sha256[:16] | read | write | bytes |\n|---|---|---|---|---|---|---|\n"
         f"| butterfly | sddmm | k.cu | {h} | 100 | 20 | 120 |\n")
     assert bench.recorded_traffic("sddmm", "butterfly") == {"bytes": 120, "read": 100, "write": 20}
+    # rows that also give the L2 write bytes
+    (tmp_path / "profiles" / "traffic.md").write_text(
+        "| workload | op | sources | sha256[:16] | read | write | bytes | L2 write bytes |\n"
+        "|---|---|---|---|---|---|---|---|\n"
+        f"| butterfly | sddmm | k.cu | {h} | 100 | 20 | 120 | 300 |\n")
+    assert bench.recorded_traffic("sddmm", "butterfly") == {"bytes": 120, "read": 100, "write": 20, "l2_write": 300}
     src.write_text("__global__ void k() { /* changed */ }\n")
     assert bench.recorded_traffic("sddmm", "butterfly") is None
 
@@ -82,12 +88,14 @@ def test_committed_traffic_table_parses():
     assert rows
     for ln in rows:
         cells = [p.strip() for p in ln.strip().strip("|").split("|")]
-        assert len(cells) in (5, 7), ln
+        assert len(cells) in (5, 7, 8), ln  # | read | write | bytes | (L2 write bytes |)
         wk, op, srcs, h = cells[:4]
         assert wk in wl.SPECS and op in ("sort_rows", "plan", "spmm", "sddmm", "csr_add")
-        assert len(h) == 16 and int(cells[-1]) > 0
-        if len(cells) == 7:
+        assert len(h) == 16 and int(cells[4 if len(cells) == 5 else 6]) > 0
+        if len(cells) >= 7:
             assert int(cells[4]) + int(cells[5]) == int(cells[6])
+        if len(cells) == 8:
+            assert int(cells[7]) >= 0
         for p in srcs.split("+"):
             assert os.path.exists(os.path.join(ROOT, p)), p
 
