@@ -471,7 +471,8 @@ def measure(sp, lib, name, args, dev, ws, rank, local, flush):
                 "note": "achieved = algorithmic bytes of the operator / its mean event time in the per-operator "
                         "loop (L2 flushed before each step); traffic = ncu dram__bytes_read + dram__bytes_write "
                         "summed over the operator's kernels, from one capture per kernel; writes of an output "
-                        "that stays in the write-back L2 during the capture are not in dram__bytes_write"}
+                        "that stays in the write-back L2 during the capture are not in dram__bytes_write, so "
+                        "traffic_l2_write gives the bytes the kernels wrote into L2 (lts__t_sectors_op_write x 32)"}
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
