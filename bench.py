@@ -12,8 +12,10 @@ LLaMA MLP weight, the Zipf matrix, the pixelfly butterfly layer, plus the narrow
 workload) and the headline fields (value, ms_per_step, roofline, cpu_baseline, e2e) are the
 butterfly layer's, the largest configuration; `per_config` holds each workload's record.
 Each step is one CUDA-graph replay of the library calls in which spmm, sddmm and csr_add
-(independent once row_idx and the plan exist) run on three streams; a second loop replays
-one graph per operator in order to give the per-operator times. L2 is flushed (a 256 MB
+(independent once row_idx and the plan exist) run on three streams, except on masks whose
+operators all run on the general row kernels with more than a GFLOP of gathers, where they
+run one after the other; a second loop replays one graph per operator in order to give the
+per-operator times. L2 is flushed (a 256 MB
 write) before every timed step, outside the step's events.
 
 --impl reference times the fp64 CPU oracle on the host cores on the headline workload, with
