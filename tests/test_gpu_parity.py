@@ -421,6 +421,32 @@ def test_spmm_direct_values_gate_on_permuted_butterfly():
         assert_bits_equal(C, oracle.spmm(r_o, c_o, v_o, w.B), w.dtype, what)
 
 
+def test_spmm_direct_values_with_a_partial_last_chunk():
+    """Rows of 200 entries (a multiple of 8, not of 64) in 64-row groups that share one run of
+    200 consecutive columns: the SpMM pipeline reads the A chunks straight from the values, the
+    last chunk's box reaching past the 200 columns (filled with zeros), and gathers the last
+    chunk's 8 B rows (the first three are 64-row tiles). Exact small-integer sums."""
+    m, n, L, N = 8192, 2048, 200, 2056
+    rng = np.random.default_rng(13)
+    g = np.arange(m) // 64
+    starts = (g % 8) * 240
+    rows = np.repeat(np.arange(m), L)
+    cols = (starts[:, None] + np.arange(L)[None, :]).ravel()
+    ro, col = wl.csr_from_coords(rows, cols, m)
+    vals = torch.from_numpy(rng.integers(-3, 4, size=col.size).astype(np.float32)).to(torch.bfloat16)
+    B = torch.from_numpy(rng.integers(-3, 4, size=(n, N)).astype(np.float32)).to(torch.bfloat16)
+    dro = torch.from_numpy(ro).cuda()
+    dcol = torch.from_numpy(col).to(torch.int16).cuda()
+    ridx = torch.from_numpy(oracle.sort_rows(ro)).to(torch.int16).cuda()
+    plan = sp.plan_build(dro, ridx, dcol, n)
+    assert plan.stats()["spmm_panels"] == 64
+    C = sp.spmm(vals.cuda(), dro, ridx, dcol, B.cuda(), m, plan=plan)
+    ref = sp.spmm(vals.cuda(), dro, ridx, dcol, B.cuda(), m, path="general")
+    torch.cuda.synchronize()
+    assert torch.equal(C.view(torch.int16), ref.view(torch.int16))
+    assert_bits_equal(C, oracle.spmm(ro, col, vals, B), "bf16", "direct values, partial chunk")
+
+
 def _mixed_panels(seed=5):
     """A 16384 x 4096 mask whose panels alternate between the SpMM pipeline's kinds, in
     row_idx order (rows by nnz): 400 of 1200 pool columns (|U| = 1200, gathered, streamed
