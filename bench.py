@@ -518,7 +518,7 @@ def run_gpu(args):
     line = {
         "metric": METRIC, "value": h["value"], "unit": "GFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": h["ms_per_step"], "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": h["dtype"], "data": "synthetic (seeded; workload recipes in DESIGN.md)",
+        "vs_baseline": None, "dtype": h["dtype"], "data": "synthetic (seeded generators in the workloads package)",
         "config": h["config"], "per_op": h["per_op"], "roofline": h["roofline"], "cpu_baseline": h["cpu_baseline"],
         "e2e": h["e2e"], "gpu_launches": h["gpu_launches"], "clocks": h["clocks"], "mask_fixed": h["mask_fixed"],
         "headline": f"{head}: the step (sort_rows+plan+spmm+sddmm+csr_add where defined) on this workload; "
@@ -917,7 +917,7 @@ def run_reference(args):
     value = round(st.flops / dt / 1e9, 3)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": ws, "steps": steps,
             "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; workload recipes in DESIGN.md)",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generators in the workloads package)",
             "config": config_dict(name, w, args),
             "cpu_baseline": {"value": value, "unit": "GFLOP/s", "cores": st.o.num_threads(), "kind": "oracle",
                              "sample": f"{st.sample}, {steps} step(s)"},
