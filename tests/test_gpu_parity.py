@@ -235,6 +235,35 @@ def test_ragged_and_unaligned_widths(dtype, N):
     assert_bits_equal(sp.csr_add(dv, dro, ridx, dcol, W.cuda()), oracle.csr_add(ro, col, vals, W), dtype, "csr_add")
 
 
+@pytest.mark.parametrize("m", [400, 800, 1500, 24000, 50000])
+def test_sddmm_row_teams_and_alternating_deal(m):
+    """The general SDDMM deals short rows in bands whose direction alternates, to teams of 8,
+    4 or 2 warp groups where rows are fewer than groups (these m give each size on a 152-SM
+    part, then one group per row), the members of a team splitting each row's entries; long
+    rows go a CTA each, also in alternating bands (over 500 of them at m = 50000: two bands).
+    Heavy-tailed lengths, empty rows, small-integer operands: every dot product is exact, so
+    the result must equal the oracle bit for bit, whatever team computed an entry."""
+    rng = np.random.default_rng(m)
+    n, kd = 2048, 256
+    lens = np.minimum(rng.zipf(1.6, size=m), 63)
+    lens[rng.random(m) < 0.1] = 0
+    longs = rng.choice(m, size=max(8, m // 90), replace=False)
+    lens[longs] = rng.integers(64, 700, size=longs.size)
+    rows = np.repeat(np.arange(m), lens)
+    start = rng.integers(0, n, size=m)
+    cols = (np.repeat(start, lens) + (np.arange(rows.size) - np.repeat(np.cumsum(lens) - lens, lens)) * 31) % n
+    ro, col = wl.csr_from_coords(rows, cols, m)
+    assert np.array_equal(np.diff(ro), lens)
+    A = wl.integers(m, 3, (m, kd), -2, 2, "f32")
+    BT = wl.integers(m, 4, (n, kd), -2, 2, "f32")
+    dro, dcol = torch.from_numpy(ro).cuda(), torch.from_numpy(col).cuda()
+    ridx = torch.from_numpy(oracle.sort_rows(ro)).to(torch.int32).cuda()
+    want = oracle.sddmm(ro, col, A, BT)
+    for be in ("general", "structure_aware"):
+        got = sp.sddmm(dro, ridx, dcol, A.cuda(), BT.cuda(), backend=be)
+        assert_bits_equal(got, want, "f32", f"sddmm {be} m={m}")
+
+
 def test_unaligned_pointers_take_the_plain_path():
     """Operands that start 2 bytes into an allocation (not 16-byte aligned)."""
     m, n, N = 64, 80, 40
