@@ -18,6 +18,9 @@
 // A batch holds NB entries: the group walks kd once, loading each A vector once and the NB
 // BT vectors beside it, keeps NB per-lane partial dot products and finishes them with an
 // xor-shuffle butterfly inside the group. Empty rows are skipped.
+// The gathers come from L2 and their latency, not L2 bandwidth, sets the pace; NB = 4 at 64
+// registers (4 CTAs, 32 warps per SM) keeps more bytes in flight per SM than NB = 8 at 80
+// registers (3 CTAs), and more CTAs at fewer registers spill.
 #include "common.cuh"
 #include "internal.h"
 
@@ -26,7 +29,7 @@ namespace {
 
 constexpr int kSddmmThreads = 256;
 constexpr int kSddmmWarps = kSddmmThreads / 32;
-constexpr int kNB = 8;  // entries per batch: 1 A load + up to 8 BT loads per lane per K step
+constexpr int kNB = 4;  // entries per batch: 1 A load + up to 4 BT loads per lane per K step
 
 // Raw operand words: one 16-byte vector (V elements), or one element for the scalar path.
 template <typename T, int V>
@@ -93,7 +96,7 @@ __device__ __forceinline__ void sddmm_batch(int row, int32_t kb, int cnt, const 
 }
 
 template <typename T, typename I, int V>
-__global__ void __launch_bounds__(kSddmmThreads, 3)
+__global__ void __launch_bounds__(kSddmmThreads, 4)
 sddmm_rows_kernel(const int32_t* __restrict__ ro, const I* __restrict__ row_idx, const I* __restrict__ col,
                   const T* __restrict__ A, const T* __restrict__ BT, T* __restrict__ out, int32_t kd, int G,
                   const int32_t* __restrict__ bins, const uint8_t* __restrict__ skip,
