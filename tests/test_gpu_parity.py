@@ -476,6 +476,40 @@ def test_spmm_direct_values_with_a_partial_last_chunk():
     assert_bits_equal(C, oracle.spmm(ro, col, vals, B), "bf16", "direct values, partial chunk")
 
 
+@pytest.mark.parametrize("L", [100, 200])
+def test_direct_panels_derive_their_positions(L):
+    """Rows of L entries in 64-row groups that share one run of L consecutive columns: every
+    panel is direct (each row holds all of U in order), so the plan skips their per-entry U
+    positions and tile tables and the kernels derive them from the row id and |U|. L = 100 is
+    not a multiple of 8, so SpMM densifies these panels (identity positions) instead of loading
+    the values by boxes; SDDMM's last tile is partial in both cases (100 and 72 columns).
+    Exact small-integer sums, bit for bit against the oracle and the general path."""
+    m, n, N, kd = 8192, 2048, 264, 136
+    rng = np.random.default_rng(L)
+    g = np.arange(m) // 64
+    starts = (g % 8) * 240
+    rows = np.repeat(np.arange(m), L)
+    cols = (starts[:, None] + np.arange(L)[None, :]).ravel()
+    ro, col = wl.csr_from_coords(rows, cols, m)
+    vals = wl.integers(L, 1, (col.size,), -3, 3, "bf16")
+    B = wl.integers(L, 2, (n, N), -3, 3, "bf16")
+    A = wl.integers(L, 3, (m, kd), -2, 2, "bf16")
+    BT = wl.integers(L, 4, (n, kd), -2, 2, "bf16")
+    dro = torch.from_numpy(ro).cuda()
+    dcol = torch.from_numpy(col).to(torch.int16).cuda()
+    ridx = torch.from_numpy(oracle.sort_rows(ro)).to(torch.int16).cuda()
+    plan = sp.plan_build(dro, ridx, dcol, n)
+    st = plan.stats()
+    assert st["spmm_panels"] == 64 and st["dense_panels"] == 64
+    C = sp.spmm(vals.cuda(), dro, ridx, dcol, B.cuda(), m, plan=plan)
+    assert_bits_equal(C, oracle.spmm(ro, col, vals, B), "bf16", f"spmm direct L={L}")
+    out = sp.sddmm(dro, ridx, dcol, A.cuda(), BT.cuda(), plan=plan)
+    ref = sp.sddmm(dro, ridx, dcol, A.cuda(), BT.cuda(), backend="general")
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert_bits_equal(out, oracle.sddmm(ro, col, A, BT), "bf16", f"sddmm direct L={L}")
+
+
 def _mixed_panels(seed=5):
     """A 16384 x 4096 mask whose panels alternate between the SpMM pipeline's kinds, in
     row_idx order (rows by nnz): 400 of 1200 pool columns (|U| = 1200, gathered, streamed

@@ -61,6 +61,22 @@ bool dtype_ok(int dt) { return dt == kF16 || dt == kBF16; }
 
 // ------------------------------------------------------------------ SDDMM dense panels
 
+// Epilogue data of tile t for one row of a panel whose rows each hold all of U in column
+// order (the direct panels: rows of one length |U| = nU, row i starting at entry i * nU): the
+// row's first entry of the tile, its entry count there and the mask of the U positions it
+// holds, without the plan's per-entry tables.
+__device__ __forceinline__ void direct_tile(int row, int nU, int t, int32_t& kb, int& cnt, uint4& mask) {
+    kb = row * nU + t * kTileN;  // row * nU <= nnz < 2^31
+    cnt = min(kTileN, nU - t * kTileN);
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int b = cnt - 32 * q;
+        w[q] = b >= 32 ? 0xffffffffu : (b > 0 ? (1u << b) - 1u : 0u);
+    }
+    mask = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // A cluster of C CTAs computes one tile (panel p, 128 columns t of U): CTA rank r multiplies
 // K chunks [r * per, (r + 1) * per) into its tensor memory. Rows are split among the ranks
 // (rank o finishes rows [o * 128 / C, ...)); after a cluster barrier (every ring is idle),
@@ -122,7 +138,9 @@ sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
     for (int it = cid; it < nitems; it += ncl) {
         const int item = v.items[it];
         const int p = item >> 8, t = item & 255;
-        const int nU = v.desc[p].y;
+        const int2 dsc = *reinterpret_cast<const int2*>(&v.desc[p]);  // dense bits, |U|
+        const int nU = dsc.y;
+        const bool direct = (dsc.x & 4) != 0;
         const int u0 = t * kTileN;
         const int ncols = min(kTileN, nU - u0);
         // One round of independent loads (all indexed by panel position, not by row): the
@@ -132,13 +150,21 @@ sddmm_panel_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
             const size_t prow_at = (size_t)p * kPM + tid;
             const int my_row = v.prow[prow_at];
             const int u = v.ulist[(size_t)p * kUList + u0 + tid];
-            const int32_t* ts = v.ts + prow_at * (kTiles + 1);
-            const int32_t kb = ts[t], kn = ts[t + 1];
-            const uint4 mk = *reinterpret_cast<const uint4*>(v.tmask + prow_at * (kUCap / 32) + t * (kTileN / 32));
+            int32_t kb;
+            int cnt;
+            uint4 mk;
+            if (direct) {
+                direct_tile(my_row, nU, t, kb, cnt, mk);
+            } else {
+                const int32_t* ts = v.ts + prow_at * (kTiles + 1);
+                kb = ts[t];
+                cnt = ts[t + 1] - kb;
+                mk = *reinterpret_cast<const uint4*>(v.tmask + prow_at * (kUCap / 32) + t * (kTileN / 32));
+            }
             s_rows[tid] = my_row;
             s_u[tid] = tid < ncols ? u : -1;
             s_kb[tid] = kb;
-            s_cnt[tid] = my_row >= 0 ? kn - kb : 0;
+            s_cnt[tid] = my_row >= 0 ? cnt : 0;
             s_mask[tid] = mk;
         }
         __syncthreads();
@@ -408,7 +434,9 @@ sddmm_group_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
     for (int it = cid; it < nitems; it += ncl) {
         const int item = v.gitems[it];
         const int p = item >> 8, grp = item & 255;
-        const int nU = v.desc[p].y;
+        const int2 dsc = *reinterpret_cast<const int2*>(&v.desc[p]);  // dense bits, |U|
+        const int nU = dsc.y;
+        const bool direct = (dsc.x & 4) != 0;
         const int t0 = grp * kGroupTiles;
         const int nt = min(kGroupTiles, (nU + kTileN - 1) / kTileN - t0);  // tiles in this group
         const uint32_t stage_bytes = (uint32_t)(1 + nt) * kGrpChunk;
@@ -577,11 +605,20 @@ sddmm_group_kernel(const T* __restrict__ A, const T* __restrict__ BT, T* __restr
             // the epilogue's per-row data for tile t
             if (tid < kPM) {
                 const size_t prow_at = (size_t)p * kPM + tid;
-                const int32_t* ts = v.ts + prow_at * (kTiles + 1);
-                const int32_t kb = ts[t], kn = ts[t + 1];
+                int32_t kb;
+                int cnt;
+                uint4 mk;
+                if (direct) {
+                    direct_tile(s_rows[tid], nU, t, kb, cnt, mk);
+                } else {
+                    const int32_t* ts = v.ts + prow_at * (kTiles + 1);
+                    kb = ts[t];
+                    cnt = ts[t + 1] - kb;
+                    mk = *reinterpret_cast<const uint4*>(v.tmask + prow_at * (kUCap / 32) + t * (kTileN / 32));
+                }
                 s_kb[tid] = kb;
-                s_cnt[tid] = s_rows[tid] >= 0 ? kn - kb : 0;
-                s_mask[tid] = *reinterpret_cast<const uint4*>(v.tmask + prow_at * (kUCap / 32) + t * (kTileN / 32));
+                s_cnt[tid] = s_rows[tid] >= 0 ? cnt : 0;
+                s_mask[tid] = mk;
             }
             // the ring (and the previous tile's receive slots) is free on every CTA of the
             // cluster once all have passed this barrier
@@ -688,7 +725,8 @@ __global__ void __launch_bounds__(256) densify_kernel(const T* __restrict__ vals
     const int nU = d.y;
     const int i = v.prow[p * kPM + grp * kGroupRows + warp];
     if (slot < 0) return;                        // no image for this panel
-    if (skip_direct && (d.x & 4)) return;        // the SpMM pipeline reads these values directly
+    const bool direct = (d.x & 4) != 0;  // row i holds all of U in order: entry k sits at k - ro[i]
+    if (skip_direct && direct) return;          // the SpMM pipeline reads these values directly
     const int upad = (nU + kKC - 1) / kKC * kKC;  // <= ucap
     uint4* st4 = reinterpret_cast<uint4*>(stage);
     const int row_vec = ucap * (int)sizeof(T) / 16;
@@ -708,7 +746,7 @@ __global__ void __launch_bounds__(256) densify_kernel(const T* __restrict__ vals
 #pragma unroll
             for (int j = 0; j < kB; ++j) {
                 const int32_t k = kb + j * 32 + lane;
-                u[j] = k < k1 ? (int)v.upos[k] : -1;
+                u[j] = k < k1 ? (direct ? (int)(k - k0) : (int)v.upos[k]) : -1;
                 x[j] = k < k1 ? vals[k] : T();
             }
 #pragma unroll

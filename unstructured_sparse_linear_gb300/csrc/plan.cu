@@ -21,8 +21,10 @@
 //      order (rows of one length |U| in two runs of 64 consecutive rows);
 //   2. row groups of dense panels (8 rows per CTA): each entry's position in U and, per row,
 //      the first entry of every 128-column tile of U and a bit mask of the U positions it
-//      holds; one extra CTA sums the panel counts into row bins, lists dense panels and
-//      SDDMM tiles, and assigns SpMM image slots within the image budget (in panel order).
+//      holds (not for panels whose rows each hold all of U in order: their consumers derive
+//      all three from the row id and |U|); one extra CTA sums the panel counts into row
+//      bins, lists dense panels and SDDMM tiles, and assigns SpMM image slots within the
+//      image budget (in panel order).
 // Index loads are batched (8 per lane) before their results are used, so a long row costs a
 // few dependent load latencies, not one per 32 entries. Every count is an integer sum in a
 // fixed order, so the plan is bit-identical on every build.
@@ -696,7 +698,9 @@ plan_upos_kernel(const int32_t* __restrict__ ro, const I* __restrict__ col, Plan
     // the panel's dense bits and the warp's row are independent loads: issued together
     const int dbits = v.desc[p].x;
     const int row = v.prow[pos];
-    if (!(dbits & 2)) return;             // U positions for SpMM-dense panels
+    // U positions for SpMM-dense panels, except the direct ones (bit 4: every row holds all
+    // of U in order), whose consumers derive them from the row id and |U|
+    if ((dbits & 6) != 2) return;
     const bool tiles = (dbits & 1) != 0;  // tile starts and masks for SDDMM-dense ones (U <= kUCap)
     uint32_t* bm = sm;
     int* wb = reinterpret_cast<int*>(sm + v.W);
