@@ -181,6 +181,21 @@ def test_sort_rows_many_ties_and_wide_keys():
     assert np.array_equal(got, oracle.sort_rows(ro))
 
 
+@pytest.mark.parametrize("m", [16384, 16385])
+def test_sort_rows_many_distinct_lengths(m):
+    """Row lengths spread over 0..5999 (up to 32 distinct radix digits in a warp): the one-CTA
+    sort at m = 16384 takes two passes (9 + 4 bits), the grid-wide sort at m = 16385 three of 8
+    bits; both must give the oracle's order (nnz descending, ties by ascending row id)."""
+    rng = np.random.default_rng(m)
+    lens = rng.integers(0, 6000, size=m)
+    ties = rng.random(m) < 0.2  # a fifth of the rows share three lengths: long runs of ties
+    lens[ties] = rng.integers(0, 3, size=int(ties.sum()))
+    ro = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    for itd in ([torch.int16, torch.int32] if m <= 32768 else [torch.int32]):
+        got = sp.sort_rows(torch.from_numpy(ro).cuda(), index_dtype=itd).cpu().numpy().astype(np.int64)
+        assert np.array_equal(got, oracle.sort_rows(ro))
+
+
 # ------------------------------------------------------------------ edge cases
 
 

@@ -42,26 +42,65 @@ radix_hist_kernel(const int32_t* __restrict__ ro, const uint32_t* __restrict__ k
     hist[threadIdx.x * gridDim.x + blockIdx.x] = cnt[threadIdx.x];
 }
 
-// Exclusive scan, in place, of `total` counters with one block.
+// Exclusive scan, in place, of `total` counters (a multiple of kRadix) with one block, in
+// tiles of kScanThreads x kScanPer: each thread loads its kScanPer consecutive counters with
+// independent 16-byte loads (one memory latency per tile, not one per counter), the block
+// scans the per-thread sums, and each thread writes its counters' running offsets.
+constexpr int kScanPer = 16;
+static_assert(kRadix % kScanPer == 0, "tiles hold whole vectors of counters");
+
 __global__ void __launch_bounds__(kScanThreads) radix_scan_kernel(uint32_t* __restrict__ hist, int32_t total) {
-    __shared__ uint32_t part[kScanThreads];
-    const int32_t per = (total + kScanThreads - 1) / kScanThreads;
-    const int32_t b = threadIdx.x * per, e = min(total, b + per);
-    uint32_t s = 0;
-    for (int32_t i = b; i < e; ++i) s += hist[i];
-    part[threadIdx.x] = s;
-    __syncthreads();
-    for (int off = 1; off < kScanThreads; off <<= 1) {  // Hillis-Steele inclusive scan
-        uint32_t v = threadIdx.x >= off ? part[threadIdx.x - off] : 0;
+    __shared__ uint32_t wsum[kScanThreads / 32];
+    __shared__ uint32_t carry_sh;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t carry = 0;  // sum of the tiles before this one
+    for (int32_t t0 = 0; t0 < total; t0 += kScanThreads * kScanPer) {
+        const int32_t i0 = t0 + tid * kScanPer;
+        uint4 v[kScanPer / 4];
+#pragma unroll
+        for (int q = 0; q < kScanPer / 4; ++q)
+            v[q] = i0 < total ? reinterpret_cast<const uint4*>(hist + i0)[q] : make_uint4(0u, 0u, 0u, 0u);
+        uint32_t s = 0;
+#pragma unroll
+        for (int q = 0; q < kScanPer / 4; ++q) s += v[q].x + v[q].y + v[q].z + v[q].w;
+        // block exclusive scan of s
+        uint32_t x = s;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) wsum[warp] = x;
         __syncthreads();
-        part[threadIdx.x] += v;
+        if (warp == 0) {
+            uint32_t w = lane < kScanThreads / 32 ? wsum[lane] : 0u;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += y;
+            }
+            wsum[lane] = w;  // inclusive sums of the warps
+            if (lane == kScanThreads / 32 - 1) carry_sh = w;
+        }
         __syncthreads();
-    }
-    uint32_t run = threadIdx.x ? part[threadIdx.x - 1] : 0;
-    for (int32_t i = b; i < e; ++i) {
-        const uint32_t c = hist[i];
-        hist[i] = run;
-        run += c;
+        uint32_t run = carry + (warp ? wsum[warp - 1] : 0u) + x - s;
+        if (i0 < total) {
+#pragma unroll
+            for (int q = 0; q < kScanPer / 4; ++q) {
+                uint4 o;
+                o.x = run;
+                run += v[q].x;
+                o.y = run;
+                run += v[q].y;
+                o.z = run;
+                run += v[q].z;
+                o.w = run;
+                run += v[q].w;
+                reinterpret_cast<uint4*>(hist + i0)[q] = o;
+            }
+        }
+        carry += carry_sh;
+        __syncthreads();  // wsum and carry_sh are rewritten by the next tile
     }
 }
 
