@@ -359,9 +359,9 @@ def measure(sp, lib, name, args, dev, ws, rank, local, flush):
         run_step_forked(ops, stream, side)
         torch.cuda.synchronize(dev)
         # the operators overlap unless they all run on the general row kernels with more than
-        # a GFLOP of gathers: those kernels gather from L2 at its bandwidth (and csr_add streams
-        # HBM), so beside each other they only slow each other down; small latency-bound
-        # steps and tensor-core panels gain from the overlap
+        # a GFLOP of gathers: those kernels fill every SM with gather warps (and csr_add
+        # streams HBM), so beside each other they only slow each other down; small
+        # latency-bound steps and tensor-core panels gain from the overlap
         st = outs["plan"].stats()
         overlap = st["dense_panels"] + st["spmm_panels"] > 0 or flops < 1e9
         for _ in range(max(args.warmup, 1)):
