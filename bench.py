@@ -12,9 +12,8 @@ LLaMA MLP weight, the Zipf matrix, the pixelfly butterfly layer, plus the narrow
 workload) and the headline fields (value, ms_per_step, roofline, cpu_baseline, e2e) are the
 butterfly layer's, the largest configuration; `per_config` holds each workload's record.
 Each step is one CUDA-graph replay of the library calls in which spmm, sddmm and csr_add
-(independent once row_idx and the plan exist) run on three streams, except on masks whose
-operators all run on the general row kernels with more than a GFLOP of gathers, where they
-run one after the other; a second loop replays one graph per operator in order to give the
+(independent once row_idx and the plan exist) run on three streams (csr_add beside the plan,
+sddmm beside spmm); a second loop replays one graph per operator in order to give the
 per-operator times. L2 is flushed (a 256 MB
 write) before every timed step, outside the step's events.
 
@@ -251,8 +250,7 @@ def run_step_forked(ops, stream, side, overlap=True):
     """The step on `stream` and the side streams, by data dependence: sort_rows first; with
     overlap, csr_add (which needs only row_idx) forks right after it, beside the plan, and after
     the plan sddmm forks while spmm runs on `stream`; everything joins back into `stream`.
-    Without overlap (masks whose operators all run on the general row kernels, which gather or
-    stream at the memory system's bandwidth) the operators run one after the other."""
+    Without overlap the operators run one after the other (kept for comparisons)."""
     by = dict(ops)
     spare = list(side)
     joins = []
@@ -358,12 +356,11 @@ def measure(sp, lib, name, args, dev, ws, rank, local, flush):
     with torch.cuda.stream(stream):
         run_step_forked(ops, stream, side)
         torch.cuda.synchronize(dev)
-        # the operators overlap unless they all run on the general row kernels with more than
-        # a GFLOP of gathers: those kernels fill every SM with gather warps (and csr_add
-        # streams HBM), so beside each other they only slow each other down; small
-        # latency-bound steps and tensor-core panels gain from the overlap
-        st = outs["plan"].stats()
-        overlap = st["dense_panels"] + st["spmm_panels"] > 0 or flops < 1e9
+        # the operators overlap on every workload: csr_add beside the plan takes the plan's
+        # latency chain off the step (llama 427 -> 419 us, RoSA 83 -> 65 us), and SDDMM beside
+        # SpMM shares the SMs between two tensor-core kernels or costs nothing measurable
+        # where both are general row kernels (llama mask-fixed 387 vs 388 us)
+        overlap = True
         for _ in range(max(args.warmup, 1)):
             run_step_forked(ops, stream, side, overlap)  # eager, on the streams the graph uses
             torch.cuda.synchronize(dev)
