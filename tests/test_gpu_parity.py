@@ -181,6 +181,20 @@ def test_sort_rows_many_ties_and_wide_keys():
     assert np.array_equal(got, oracle.sort_rows(ro))
 
 
+@pytest.mark.parametrize("m", [1, 2, 31, 100, 1024, 1025])
+def test_sort_rows_small_masks(m):
+    """Up to 1024 rows the sort ranks each row's (nnz descending, row id) key against all the
+    others; 1025 takes the one-CTA radix sort. Ties and empty rows included."""
+    rng = np.random.default_rng(m + 7)
+    lens = rng.integers(0, 40, size=m)
+    lens[rng.random(m) < 0.3] = 5  # runs of ties
+    lens[rng.random(m) < 0.1] = 0
+    ro = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    for itd in (torch.int16, torch.int32):
+        got = sp.sort_rows(torch.from_numpy(ro).cuda(), index_dtype=itd).cpu().numpy().astype(np.int64)
+        assert np.array_equal(got, oracle.sort_rows(ro))
+
+
 @pytest.mark.parametrize("m", [16384, 16385])
 def test_sort_rows_many_distinct_lengths(m):
     """Row lengths spread over 0..5999 (up to 32 distinct radix digits in a warp): the one-CTA

@@ -6,9 +6,10 @@
 // the direction; this library sorts by nnz descending and keeps ascending row ids among
 // rows with equal counts, so long rows come first and empty rows last.
 //
-// sort_rows is a stable least-significant-digit radix sort on the key (nnz - nnz_i),
-// 8 bits per pass: a per-block digit histogram, one exclusive scan over all blocks'
-// histograms, and a stable scatter that ranks equal digits inside a block with warp
+// sort_rows: up to 1024 rows, a rank sort in one CTA; up to 16384 rows, a one-CTA radix sort
+// in shared memory; beyond, a stable least-significant-digit radix sort on the key
+// (nnz - nnz_i), 8 bits per pass: a per-block digit histogram, one exclusive scan over all
+// blocks' histograms, and a stable scatter that ranks equal digits inside a block with warp
 // match masks. The first pass derives the key from row_offsets directly.
 #include "common.cuh"
 #include "internal.h"
@@ -153,6 +154,35 @@ radix_scatter_kernel(const int32_t* __restrict__ ro, const uint32_t* __restrict_
             vals_out[pos] = static_cast<OutI>(val);
         }
         __syncthreads();
+    }
+}
+
+// Up to kRankSortRows rows: one CTA, a thread per row, sorts by rank. The key
+// (0xFFFFFFFF - nnz_i) << 32 | i is distinct per row and orders rows by nnz descending, then by
+// ascending row id, so each row's position is the number of keys below its own: one barrier
+// and at most kRankSortRows broadcast shared-memory compares per thread, where the radix
+// passes below cost several block-wide phases each.
+constexpr int kRankSortRows = 1024;
+
+template <typename OutI>
+__global__ void __launch_bounds__(kRankSortRows) sort_rank_kernel(const int32_t* __restrict__ ro, int32_t m,
+                                                                   OutI* __restrict__ out) {
+    __shared__ unsigned long long key[kRankSortRows];
+    const int i = threadIdx.x;
+    pdl_trigger();
+    pdl_wait();
+    unsigned long long k = 0;
+    if (i < m) {
+        const uint32_t len = (uint32_t)(ro[i + 1] - ro[i]);
+        k = ((unsigned long long)(0xFFFFFFFFu - len) << 32) | (uint32_t)i;
+        key[i] = k;
+    }
+    __syncthreads();
+    if (i < m) {
+        int r = 0;
+#pragma unroll 8
+        for (int j = 0; j < m; ++j) r += key[j] < k ? 1 : 0;
+        out[r] = static_cast<OutI>(i);
     }
 }
 
@@ -384,6 +414,15 @@ size_t sort_rows_workspace_bytes(int32_t m) {
 cudaError_t launch_sort_rows(const int32_t* ro, int32_t m, int32_t nnz, void* row_idx_out, int it, void* ws,
                              cudaStream_t s) {
     if (m == 0) return cudaSuccess;
+    if (m <= kRankSortRows) {
+        cudaError_t e = it == kIdx16 ? launch_pdl(sort_rank_kernel<uint16_t>, 1, kRankSortRows, 0, s, ro, m,
+                                                  (uint16_t*)row_idx_out)
+                                     : launch_pdl(sort_rank_kernel<int32_t>, 1, kRankSortRows, 0, s, ro, m,
+                                                  (int32_t*)row_idx_out);
+        if (e != cudaSuccess) return e;
+        count_launches(1);
+        return cudaGetLastError();
+    }
     if (m <= kSmallSortRows) {
         cudaError_t e = it == kIdx16
                             ? cudaFuncSetAttribute(sort_small_kernel<uint16_t>,
