@@ -54,13 +54,27 @@ __device__ __forceinline__ void accumulate(float (&acc)[V], int cj, float vj, in
             c[u] = __shfl_sync(mask, cj, src0 + j + u);
             v[u] = __shfl_sync(mask, vj, src0 + j + u);
         }
-        float b[U][V];
+        if constexpr (V == 1) {
+            float b[U][V];
 #pragma unroll
-        for (int u = 0; u < U; ++u) load_b<T, V>(B + (int64_t)c[u] * N, col0, N, b[u]);
+            for (int u = 0; u < U; ++u) load_b<T, V>(B + (int64_t)c[u] * N, col0, N, b[u]);
 #pragma unroll
-        for (int u = 0; u < U; ++u)
+            for (int u = 0; u < U; ++u)
 #pragma unroll
-            for (int e = 0; e < V; ++e) acc[e] = fmaf(v[u], b[u][e], acc[e]);
+                for (int e = 0; e < V; ++e) acc[e] = fmaf(v[u], b[u][e], acc[e]);
+        } else {
+            uint4 r[U];  // raw 16-byte slices: 4 registers each, widened at their FMAs
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                r[u] = col0 < N ? ld_nc_v4(B + (int64_t)c[u] * N + col0) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                float b[V];
+                Elt<T>::unpack(r[u], b);
+#pragma unroll
+                for (int e = 0; e < V; ++e) acc[e] = fmaf(v[u], b[e], acc[e]);
+            }
+        }
     }
     for (; j < cnt; ++j) {
         const int c = __shfl_sync(mask, cj, src0 + j);
