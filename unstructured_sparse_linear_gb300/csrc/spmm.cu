@@ -97,7 +97,7 @@ __device__ __forceinline__ void store_c(T* __restrict__ Crow, int col0, int N, c
 }
 
 template <typename T, typename I, int V>
-__global__ void __launch_bounds__(kSpmmThreads, 3)
+__global__ void __launch_bounds__(kSpmmThreads, 4)
 spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, const I* __restrict__ row_idx,
                  const I* __restrict__ col, const T* __restrict__ B, T* __restrict__ C, int32_t m, int32_t N, int G,
                  const int32_t* __restrict__ bins, const uint8_t* __restrict__ skip, const int32_t* __restrict__ order) {
@@ -180,7 +180,7 @@ spmm_rows_kernel(const T* __restrict__ vals, const int32_t* __restrict__ ro, con
         // Items go in batches of kBatch: their row ids, then their row offsets, are loaded
         // together before any is processed, so short and empty rows do not wait on one
         // dependent load chain each.
-        constexpr int kBatch = 4;
+        constexpr int kBatch = 2;
         for (int64_t base = gid; base < items; base += kBatch * ngroups) {
             int rowq[kBatch], cq[kBatch];
             int32_t k0q[kBatch], k1q[kBatch];
